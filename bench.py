@@ -1,0 +1,508 @@
+#!/usr/bin/env python
+"""Benchmark of the 2Mamba second-order mixer on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tm2|reference]
+
+One step = one pass of the whole training hot path over one synthetic batch:
+forward + backward of the 2Mamba mixer at B=2, H=16, T=8192, d=dv=64, bf16 inputs,
+normalised ("2Mamba2Furious" Sec. 5; App. B shapes: 16 heads of dimension 64;
+sequence length 8192).  `value` is tokens/s over all ranks (weak scaling: each rank
+runs its own replica on its own batch; the path has no exchange step).  The same
+line carries the decode step (256 sequences x 16 heads, fp32 d^2 x dv state) in GB/s
+and 2Mamba-E fwd+bwd (B=2, H=16, T=4096) in tokens/s.
+
+Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events on the
+launching stream; a 256 MiB buffer is written between timed steps to flush the
+126 MB L2.  Per-kernel device times come from the library's own launch trace (CUDA
+events recorded around every kernel on its stream).  Rank 0 prints one JSON line.
+
+--impl reference times the CPU fp64 oracle (the only executable reference of this
+method; the paper's code is not available) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+import synth_inputs as si  # noqa: E402
+
+METRIC = "2Mamba fwd+bwd tokens/s at T=8192 on 1 B300; % bf16 tensor peak; decode GB/s"
+FLUSH_BYTES = 256 << 20
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]),
+                "sm_max_mhz": p.get("sm_max_mhz", 2032.0), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+                "sm_max_mhz": 2032.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------- counting
+def fwd_flops(d, dv, C, normalize=True):
+    """Algorithmic flops per token-head of the chunked forward (causal pairs only)."""
+    dv1 = dv + 1 if normalize else dv
+    return 4 * d * d * dv1 + (C + 1) * (d + dv) + 2 * d * d * dv1 / C
+
+
+def bwd_flops(d, dv, C, normalize=True):
+    dv1 = dv + 1 if normalize else dv
+    return 8 * d * d * dv1 + (C + 1) * (3 * d + 2 * dv) + 4 * d * d * dv1 / C
+
+
+def kernel_flops(name, d, dv, C, tokens):
+    """Algorithmic flops of one launch of a named kernel over `tokens` token-heads."""
+    dv1 = dv + 1
+    per = {
+        "state_scan_fwd": 2 * d * d * dv1 + 2 * d * d * dv1 / C,
+        "chunk_out": 2 * d * d * dv1 + (C + 1) * (d + dv),
+        "state_scan_bwd": 2 * d * d * dv1 + 2 * d * d * dv1 / C,
+        "bwd_chunk": 6 * d * d * dv1 + (C + 1) * (3 * d + 2 * dv),
+    }.get(name)
+    return None if per is None else per * tokens
+
+
+def decode_bytes_per_head(d, dv):
+    return 2 * d * d * dv * 4 + 2 * d * d * 4 + 3 * d * 4 + 4 + dv * 4 + 4
+
+
+# ----------------------------------------------------------------------------- tracing
+class Trace:
+    def __init__(self, lib):
+        self.lib = lib
+        lib.tm2_trace_enable.argtypes = [ctypes.c_int]
+        lib.tm2_trace_read.argtypes = [ctypes.c_int, ctypes.c_char_p, ctypes.c_int,
+                                       ctypes.POINTER(ctypes.c_float)]
+
+    def start(self):
+        self.lib.tm2_trace_enable(1)
+
+    def stop(self):
+        self.lib.tm2_trace_enable(0)
+        out = []
+        buf = ctypes.create_string_buffer(64)
+        ms = ctypes.c_float()
+        for i in range(self.lib.tm2_trace_count()):
+            if self.lib.tm2_trace_read(i, buf, 64, ctypes.byref(ms)) == 0:
+                out.append((buf.value.decode(), float(ms.value)))
+        return out
+
+
+def summarize(trace):
+    agg = {}
+    for name, ms in trace:
+        a = agg.setdefault(name, {"launches": 0, "ms": 0.0})
+        a["launches"] += 1
+        a["ms"] += ms
+    tot = sum(a["ms"] for a in agg.values()) or 1.0
+    for a in agg.values():
+        a["share"] = a["ms"] / tot
+        a["ms_per_launch"] = a["ms"] / a["launches"]
+    return agg
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        self.proc = None
+        self.path = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            self.gpu = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            self.gpu = str(device)
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu, "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 7:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    smax = max(smax, float(parts[1]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[3:7]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- helpers
+def source_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "ssm_sequence_mixer_chunked_b300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel, tokens_per_launch):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(kernel)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("source_sha") != source_sha():
+        return None
+    return rec["dram_bytes_per_token_head"] * tokens_per_launch
+
+
+def setup_dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, torch.device("cuda", torch.cuda.current_device())
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def oracle_fwd_bwd_sample(inp, heads):
+    import oracle
+    t0 = time.perf_counter()
+    for b, h in heads:
+        sel = (slice(b, b + 1), slice(h, h + 1))
+        q, k, v, a, dO = (inp[n][sel] for n in ("q", "k", "v", "a", "dO"))
+        oracle.fwd_quadratic(q, k, v, a, True)
+        oracle.bwd_quadratic(q, k, v, a, dO, True)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(inp, w):
+    import oracle
+    heads = [(0, 0), (1, 7)]
+    dt = oracle_fwd_bwd_sample(inp, heads)
+    frac = len(heads) / (w.B * w.H)
+    return {"value": frac * w.B * w.T / dt, "unit": "tokens/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": "fp64 quadratic-form forward+backward of %d of the %d (b,h) heads at full "
+                      "T=%d (%.1f s); tokens/s scaled by the head fraction" % (len(heads), w.B * w.H, w.T, dt)}
+
+
+# ----------------------------------------------------------------------------- arms
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import oracle
+    w = si.WORKLOADS[3]
+    inp = si.workload_inputs(3)
+    heads = [(0, 0)]
+    for _ in range(min(args.warmup, 1)):
+        oracle_fwd_bwd_sample(inp, heads)
+    times = [oracle_fwd_bwd_sample(inp, heads) for _ in range(args.steps)]
+    step_s = sum(times) / len(times)
+    frac = len(heads) / (w.B * w.H)
+    value = frac * w.B * w.T / step_s
+    sample = ("fp64 quadratic-form forward+backward of 1 of the %d (b,h) heads at full T=%d per step; "
+              "tokens/s scaled by the head fraction" % (w.B * w.H, w.T))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": step_s * 1e3 / frac, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(w, 64),
+            "cpu_baseline": {"kind": "oracle", "cores": oracle.num_threads(), "sample": sample,
+                             "value": value, "unit": "tokens/s"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w, C):
+    return {"workload": "2Mamba forward+backward, B=%d H=%d T=%d d=dv=%d, bf16 inputs, fp32 "
+                        "accumulate, normalised" % (w.B, w.H, w.T, w.d),
+            "B": w.B, "H": w.H, "T": w.T, "d": w.d, "dv": w.dv, "chunk": C,
+            "global_batch": w.B, "seq_len": w.T, "parallelism": "replicas (one per GPU)",
+            "l2": "flushed between timed steps (256 MiB write)"}
+
+
+def run_tm2(args, world, rank, device):
+    import ssm_sequence_mixer_chunked_b300 as tm2
+    lib = tm2.lib()
+    trace = Trace(lib)
+    pk = peaks()
+    w = si.WORKLOADS[3]
+    C = 64
+    inp_cpu = si.workload_inputs(3, seed=3 + 1000 * rank)
+    g = {k: v.to(device) for k, v in inp_cpu.items()}
+    B, H, T, d, dv = w.B, w.H, w.T, w.d, w.dv
+    o = torch.empty(g["v"].shape, dtype=torch.float32, device=device)
+    Z = torch.empty((B, H, T), dtype=torch.float32, device=device)
+    grads = tuple(torch.empty(g[n].shape, dtype=torch.float32, device=device) for n in ("q", "k", "v", "a"))
+    wsf = torch.empty(tm2.forward_workspace_bytes(B, H, T, d, dv, C), dtype=torch.uint8, device=device)
+    wsb = torch.empty(tm2.backward_workspace_bytes(B, H, T, d, dv, C), dtype=torch.uint8, device=device)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    def step(q, k, v, a, dO):
+        tm2.forward(q, k, v, a, chunk=C, out=o, Z=Z, workspace=wsf)
+        tm2.backward(q, k, v, a, o, Z, dO, chunk=C, workspace=wsb, grads=grads)
+
+    for _ in range(args.warmup):
+        step(g["q"], g["k"], g["v"], g["a"], g["dO"])
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(device)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    trace.start()
+    for i in range(args.steps):
+        flush.zero_()
+        evs[i][0].record()
+        step(g["q"], g["k"], g["v"], g["a"], g["dO"])
+        evs[i][1].record()
+    torch.cuda.synchronize()
+    recs = trace.stop()
+    barrier(world)
+    clk = clocks.stop()
+    step_ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
+    step_ms = max_over_ranks(step_ms, world)
+    tokens = B * T
+    value = world * tokens / (step_ms * 1e-3)
+    kern = summarize(recs)
+    launches = len(recs)
+
+    # roofline of the dominant kernel (largest share of step time)
+    dom = max(kern, key=lambda n: kern[n]["ms"])
+    per_launch_tokens = B * H * T
+    kf = kernel_flops(dom, d, dv, C, per_launch_tokens)
+    fp32_peak = 148 * 128 * 2 * pk["sm_max_mhz"] * 1e6 / 1e12   # FFMA, TFLOP/s
+    roof = None
+    if kf is not None:
+        ach = kf / (kern[dom]["ms_per_launch"] * 1e-3) / 1e12
+        roof = {"kernel": dom, "bound": "alu", "achieved": ach, "peak": fp32_peak, "unit": "TFLOP/s",
+                "frac": ach / fp32_peak, "traffic": ncu_traffic(dom, per_launch_tokens),
+                "peak_source": "derived: 148 SMs x 128 fp32 FMA/clk x 2 flop x %.0f MHz" % pk["sm_max_mhz"],
+                "algorithmic_flops_per_launch": kf}
+    counted = (fwd_flops(d, dv, C) + bwd_flops(d, dv, C)) * B * H * T
+    tensor_frac = counted / (step_ms * 1e-3) / (pk["bf16_tflops"] * 1e12)
+
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": config_of(w, C), "roofline": roof,
+            "step_bf16_tensor_peak_frac": tensor_frac,
+            "step_counted_flops": counted, "gpu_launches": launches,
+            "kernels": {n: {k: round(v, 4) if isinstance(v, float) else v for k, v in a.items()}
+                        for n, a in kern.items()},
+            "clocks": clk}
+
+    if not args.no_e2e:
+        line["e2e"] = run_e2e(args, tm2, inp_cpu, device, C, world)
+    if not args.no_decode:
+        line["decode"] = run_decode(args, tm2, device, trace, pk, world)
+    if not args.no_e:
+        line["e_variant"] = run_e_variant(args, tm2, device, trace, world)
+    if rank == 0 and world == 1 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(inp_cpu, w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, tm2, inp_cpu, device, C, world):
+    """Same metric through the public API with host buffers: pinned host -> device copies of
+    the step's inputs and device -> host copies of its results inside the timed region."""
+    host_in = {k: v.pin_memory() for k, v in inp_cpu.items()}
+    host_out = {n: torch.empty(inp_cpu[src].shape, dtype=torch.float32).pin_memory()
+                for n, src in (("o", "v"), ("dq", "q"), ("dk", "k"), ("dv", "v"), ("da", "a"))}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+    def step():
+        g = {k: v.to(device, non_blocking=True) for k, v in host_in.items()}
+        o, Z = tm2.forward(g["q"], g["k"], g["v"], g["a"], chunk=C)
+        dq, dk, dv, da = tm2.backward(g["q"], g["k"], g["v"], g["a"], o, Z, g["dO"], chunk=C)
+        for name, t in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv), ("da", da)):
+            host_out[name].copy_(t, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    n = max(1, min(args.steps, 5))
+    barrier(world)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(n):
+        step()
+    t1.record()
+    torch.cuda.synchronize()
+    ms = max_over_ranks(t0.elapsed_time(t1) / n, world)
+    B, T = inp_cpu["a"].shape[0], inp_cpu["a"].shape[2]
+    return {"value": world * B * T / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n}
+
+
+def run_decode(args, tm2, device, trace, pk, world):
+    w = si.WORKLOADS[4]
+    N, H, d, dv = w.B, w.H, w.d, w.dv
+    S, z = si.decode_initial_state(N, H, d, dv, S0_std=w.S0_std)
+    S, z = S.to(device), z.to(device)
+    toks = [{k: v.to(device) for k, v in si.decode_token(t, N, H, d, dv, qkv_std=w.qkv_std).items()}
+            for t in range(8)]
+    o = torch.empty((N, H, dv), dtype=torch.float32, device=device)
+    Zo = torch.empty((N, H), dtype=torch.float32, device=device)
+    for t in range(3):
+        x = toks[t % 8]
+        tm2.step(x["q"], x["k"], x["v"], x["a"], S, z, out=o, Z=Zo)
+    torch.cuda.synchronize()
+    n = max(args.steps, 10)
+    barrier(world)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    trace.start()
+    ev0.record()
+    for t in range(n):
+        x = toks[t % 8]
+        tm2.step(x["q"], x["k"], x["v"], x["a"], S, z, out=o, Z=Zo)
+    ev1.record()
+    torch.cuda.synchronize()
+    recs = trace.stop()
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / n, world)
+    kms = sum(m for _, m in recs) / max(len(recs), 1)
+    nbytes = decode_bytes_per_head(d, dv) * N * H
+    gbs = nbytes / (kms * 1e-3) / 1e9
+    return {"workload": "decode step, N=%d sequences x H=%d, d=dv=%d, fp32 state, %d steps" % (N, H, d, n),
+            "ms_per_step": ms, "kernel_ms_per_launch": kms, "bytes_per_step": nbytes,
+            "GBps": world * nbytes / (ms * 1e-3) / 1e9, "unit": "GB/s",
+            "roofline": {"kernel": "decode_step", "bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"],
+                         "unit": "GB/s", "frac": gbs / pk["hbm_gbs"],
+                         "traffic": ncu_traffic("decode_step", N * H)},
+            "tokens_per_s": world * N / (ms * 1e-3), "l2": "state (4.3 GB) larger than L2",
+            "gpu_launches": len(recs)}
+
+
+def run_e_variant(args, tm2, device, trace, world):
+    w = si.WORKLOADS[5]
+    inp = si.workload_inputs(5)
+    g = {k: v.to(device) for k, v in inp.items()}
+    B, H, T, d, dv = w.B, w.H, w.T, w.d, w.dv
+
+    def step():
+        o, lse = tm2.e_forward(g["q"], g["k"], g["v"], g["a"])
+        tm2.e_backward(g["q"], g["k"], g["v"], g["a"], o, lse, g["dO"])
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    n = max(1, min(args.steps, 5))
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    barrier(world)
+    trace.start()
+    for i in range(n):
+        flush.zero_()
+        evs[i][0].record()
+        step()
+        evs[i][1].record()
+    torch.cuda.synchronize()
+    recs = trace.stop()
+    ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in evs) / n, world)
+    flops = ((T + 1) * (d + dv) + (T + 1) * (3 * d + 2 * dv)) * B * H * T
+    return {"workload": "2Mamba-E forward+backward, B=%d H=%d T=%d d=dv=%d bf16" % (B, H, T, d),
+            "ms_per_step": ms, "tokens_per_s": world * B * T / (ms * 1e-3),
+            "counted_flops": flops, "bf16_tensor_peak_frac": flops / (ms * 1e-3) / (peaks()["bf16_tflops"] * 1e12),
+            "kernels": {n: round(a["ms"], 3) for n, a in summarize(recs).items()},
+            "gpu_launches": len(recs)}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="tm2", choices=["tm2", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        return run_reference(args, world, rank)
+    world, rank, device = setup_dist()
+    run_tm2(args, world, rank, device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

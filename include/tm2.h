@@ -1,0 +1,175 @@
+/*
+ * tm2.h -- C ABI of libtm2.so, the B300 (sm_103a) 2Mamba second-order sequence mixer.
+ *
+ * Method: "2Mamba2Furious: Linear in Complexity, Competitive in Accuracy"
+ * (Mongaras & Larson, arXiv 2602.17363).  Per batch b and head h, with tokens
+ * t = 0..T-1, q_t, k_t in R^d, v_t in R^dv and the A-mask input a_t in R:
+ *
+ *   l_t     = -softplus(a_t)                cumA_t = sum_{u <= t} l_u      (Sec. 3, Sec. 4)
+ *   w_ij    = exp(cumA_i - cumA_j) (q_i . k_j)^2              for j <= i   (Sec. 5)
+ *   N_i     = sum_{j <= i} w_ij v_j         Z_i = sum_{j <= i} w_ij
+ *   o_i     = N_i / Z_i   with TM2_NORMALIZE ("softmax normalisation", Sec. 5), else N_i
+ *
+ * Equivalent recurrent form with the second-order state of size (d^2, dv)
+ * (Sec. 2, "Softmax as a Recurrent Neural Network"; App. A):
+ *   S_t = exp(l_t) S_{t-1} + (k_t (x) k_t) v_t^T,   z_t = exp(l_t) z_{t-1} + k_t (x) k_t
+ *   N_t = (q_t (x) q_t)^T S_t,                      Z_t = (q_t (x) q_t)^T z_t
+ *
+ * 2Mamba-E (Sec. 6): o_i = sum_{j <= i} softmax_j(scale q_i . k_j + cumA_i - cumA_j) v_j.
+ *
+ * The boundary is the attention kernel of App. C: inputs are the post-projection,
+ * post-convolution q, k, v and a; outputs are the post-attention outputs.
+ *
+ * Conventions for every entry point:
+ *  - Pointers are DEVICE pointers unless stated otherwise, owned by the caller,
+ *    16-byte aligned (TM2_ERR_ALIGNMENT otherwise), and tensors are dense row-major:
+ *    q, k, dq, dk: (B,H,T,d); v, o, dO, dv: (B,H,T,dv); a, Z, lse, da: (B,H,T).
+ *  - dtype (tm2_dtype) is the element type of the inputs q, k, v and dO.  Every output
+ *    (o, Z, lse, dq, dk, dv, da), the A-mask input a and every state are fp32: the
+ *    arithmetic accumulates in fp32 and the results are returned unrounded.
+ *  - State layout: S is (B,H,d*d,dv) with row r = m*d + n (key feature indices m, n);
+ *    z is (B,H,d*d).  The same layout serves forward (initial/final state) and decode.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream).
+ *    Calls are asynchronous and never synchronise the host.
+ *  - Argument errors are reported before anything is launched.  A launch failure
+ *    returns TM2_ERR_CUDA.  Kernels whose waits are bounded record TM2_ERR_TIMEOUT in
+ *    a per-device status word that tm2_poll_status() returns after the stream drains.
+ *  - The library allocates no device memory: scratch comes from the caller's
+ *    workspace (`ws`, `ws_bytes` >= the matching *_workspace() size, 256-byte aligned).
+ *  - Supported: d = dv in {16, 32, 64}; any T >= 0 (a ragged last chunk is handled);
+ *    chunk in {0 (library choice), 64}.  Other values return TM2_ERR_UNSUPPORTED.
+ *    B*H <= 65535 for the sequence entry points.
+ */
+#ifndef TM2_H
+#define TM2_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TM2_OK = 0,
+    TM2_ERR_INVALID_ARG = -1,   /* null pointer, negative size, inconsistent arguments */
+    TM2_ERR_UNSUPPORTED = -2,   /* valid but not implemented (d, dv, chunk, dtype)      */
+    TM2_ERR_ALIGNMENT = -3,     /* a pointer is not 16-byte aligned (workspace: 256)     */
+    TM2_ERR_WORKSPACE = -4,     /* ws_bytes smaller than the *_workspace() size          */
+    TM2_ERR_CUDA = -5,          /* a CUDA launch or runtime call failed                  */
+    TM2_ERR_TIMEOUT = -6        /* a bounded device wait expired (see tm2_poll_status)   */
+} tm2_status;
+
+typedef enum { TM2_F32 = 0, TM2_BF16 = 1 } tm2_dtype;
+
+/* o = N / Z (the paper's "softmax normalisation", Sec. 5).  Without it o = N. */
+#define TM2_NORMALIZE 1u
+
+/* Library version (major*10000 + minor*100 + patch). */
+int tm2_version(void);
+
+/* Human-readable name of a tm2_status value.  Never NULL. */
+const char* tm2_status_string(int status);
+
+/* Bytes of device workspace tm2_forward needs for these arguments (0 if none).
+ * Returns 0 as well for arguments tm2_forward would reject. */
+size_t tm2_forward_workspace(int B, int H, int T, int d, int dv, int chunk, int dtype,
+                             unsigned flags);
+
+/*
+ * 2Mamba forward (Sec. 5), chunked: decay running sums, per-chunk second-order
+ * states, state passing across chunks, intra-chunk squared masked scores and the
+ * inter-chunk readout of the state entering each chunk.
+ *   q,k,v,a  inputs (see layout above).
+ *   S0, z0   optional initial state (state before token 0), fp32; NULL = zero.
+ *   o        output (B,H,T,dv) fp32.
+ *   Z        optional output (B,H,T) fp32, the normaliser Z_i (tm2_backward needs it).
+ *   S_final, z_final  optional outputs, the state after token T-1 (fp32).
+ * Returns TM2_OK or an error status.
+ */
+int tm2_forward(const void* q, const void* k, const void* v, const float* a,
+                const float* S0, const float* z0,
+                void* o, float* Z, float* S_final, float* z_final,
+                int B, int H, int T, int d, int dv, int chunk, int dtype, unsigned flags,
+                void* ws, size_t ws_bytes, void* stream);
+
+size_t tm2_backward_workspace(int B, int H, int T, int d, int dv, int chunk, int dtype,
+                              unsigned flags);
+
+/*
+ * 2Mamba backward (App. C, C.1): gradients of sum(dO * o) w.r.t. q, k, v and the raw
+ * A-mask input a, for a forward with no initial state.  o and Z are the forward's
+ * outputs for the same inputs and flags (Z may be NULL when TM2_NORMALIZE is off).
+ * o is the fp32 output of tm2_forward; dq, dk, dv, da are fp32.  The A-mask gradient is the row-axis sum minus the
+ * column-axis sum of w_ij * dL/dw_ij, accumulated from the end of the sequence and
+ * multiplied by d(-softplus(a))/da = -sigmoid(a).
+ */
+int tm2_backward(const void* q, const void* k, const void* v, const float* a,
+                 const void* o, const float* Z, const void* dO,
+                 void* dq, void* dk, void* dv, float* da,
+                 int B, int H, int T, int d, int dv_dim, int chunk, int dtype, unsigned flags,
+                 void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * One recurrent decode step (App. A) for N sequences x H heads, one token each:
+ *   S <- exp(l) S + (k (x) k) v^T,  z <- exp(l) z + k (x) k,  y = (q (x) q)^T S,  zeta = (q (x) q)^T z
+ * q, k: (N,H,d); v: (N,H,dv) in dtype; a: (N,H) fp32.
+ * S: (N,H,d*d,dv) fp32, updated in place.  z: (N,H,d*d) fp32 in place, or NULL
+ * (then no normaliser is tracked and TM2_NORMALIZE is rejected).
+ * o: (N,H,dv) fp32, = y / zeta with TM2_NORMALIZE, else y.  Z: (N,H) fp32 zeta, or NULL.
+ * No workspace.  The step is bound by HBM bandwidth: it streams S once in and once out.
+ */
+int tm2_step(const void* q, const void* k, const void* v, const float* a,
+             float* S, float* z, void* o, float* Z,
+             int N, int H, int d, int dv, int dtype, unsigned flags, void* stream);
+
+size_t tm2e_forward_workspace(int B, int H, int T, int d, int dv, int dtype);
+
+/*
+ * 2Mamba-E forward (Sec. 6): causal softmax attention with the additive A-mask
+ * cumA_i - cumA_j and logit scale `scale` (1/sqrt(d) in the paper's setting),
+ * evaluated blockwise with an online running maximum.
+ * o: (B,H,T,dv) fp32.  lse: (B,H,T) fp32 log-sum-exp of each row (needed by backward).
+ */
+int tm2e_forward(const void* q, const void* k, const void* v, const float* a,
+                 void* o, float* lse,
+                 int B, int H, int T, int d, int dv, float scale, int dtype,
+                 void* ws, size_t ws_bytes, void* stream);
+
+size_t tm2e_backward_workspace(int B, int H, int T, int d, int dv, int dtype);
+
+/*
+ * 2Mamba-E backward: gradients of sum(dO * o) w.r.t. q, k, v and a, given the
+ * forward's o (fp32) and lse.  dq, dk, dv, da are fp32.
+ */
+int tm2e_backward(const void* q, const void* k, const void* v, const float* a,
+                  const void* o, const float* lse, const void* dO,
+                  void* dq, void* dk, void* dv, float* da,
+                  int B, int H, int T, int d, int dv_dim, float scale, int dtype,
+                  void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Device status word of the current device: returns TM2_OK, or TM2_ERR_TIMEOUT if a
+ * kernel's bounded wait expired since the last poll, and clears it.  Synchronises
+ * with the device (call it after the stream of interest has drained).
+ */
+int tm2_poll_status(void);
+
+/*
+ * Launch tracing (for measurement; off by default).  While enabled, every kernel an
+ * entry point launches is bracketed by two CUDA events recorded on that launch's
+ * stream, so per-kernel device time can be read back without a profiler.  Not
+ * thread-safe: enable, call, read and disable from one host thread.
+ *   tm2_trace_enable(1) clears the record list and starts recording; (0) stops.
+ *   tm2_trace_count() is the number of recorded launches.
+ *   tm2_trace_read(i, name, len, &ms) waits for launch i to finish and returns its
+ *   kernel name (truncated to len-1 chars) and device time in milliseconds.
+ */
+int tm2_trace_enable(int on);
+int tm2_trace_count(void);
+int tm2_trace_read(int i, char* name, int name_len, float* ms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TM2_H */

@@ -1,0 +1,217 @@
+"""B300-native 2Mamba second-order sequence mixer -- thin Python binding over libtm2.so.
+
+The method ("2Mamba2Furious: Linear in Complexity, Competitive in Accuracy", Sec. 5):
+    o_i = sum_{j<=i} exp(cumA_i - cumA_j) (q_i . k_j)^2 v_j  [/ Z_i],
+    cumA_t = sum_{u<=t} -softplus(a_u),
+its recurrent decode step on the (d^2, dv) state (Sec. 2, App. A), the gradients
+(App. C) and the exponentiated-score variant 2Mamba-E (Sec. 6).
+
+Every step of the computation runs in the CUDA kernels of libtm2.so; this module only
+checks tensors, allocates outputs and workspace with PyTorch and passes raw pointers
+and sizes through the C ABI declared in include/tm2.h.  There is no CPU path: if the
+library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+__all__ = ["forward", "backward", "step", "e_forward", "e_backward", "library_path",
+           "forward_workspace_bytes", "backward_workspace_bytes", "TM2Error", "NORMALIZE"]
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(PKG, "libtm2.so")
+NORMALIZE = 1
+_DTYPES = {torch.float32: 0, torch.bfloat16: 1}
+_lib = None
+
+
+class TM2Error(RuntimeError):
+    pass
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise TM2Error("libtm2.so is not built (%s); run `python -m ssm_sequence_mixer_chunked_b300.build`"
+                       % _LIB_PATH)
+    lib = ctypes.CDLL(_LIB_PATH)
+    P, I, U, S, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint, ctypes.c_size_t, ctypes.c_float
+    lib.tm2_version.restype = I
+    lib.tm2_status_string.restype = ctypes.c_char_p
+    lib.tm2_status_string.argtypes = [I]
+    for name in ("tm2_forward_workspace", "tm2_backward_workspace"):
+        getattr(lib, name).restype = S
+        getattr(lib, name).argtypes = [I] * 7 + [U]
+    for name in ("tm2e_forward_workspace", "tm2e_backward_workspace"):
+        getattr(lib, name).restype = S
+        getattr(lib, name).argtypes = [I] * 6
+    lib.tm2_forward.restype = I
+    lib.tm2_forward.argtypes = [P] * 10 + [I] * 7 + [U, P, S, P]
+    lib.tm2_backward.restype = I
+    lib.tm2_backward.argtypes = [P] * 11 + [I] * 7 + [U, P, S, P]
+    lib.tm2_step.restype = I
+    lib.tm2_step.argtypes = [P] * 8 + [I] * 5 + [U, P]
+    lib.tm2e_forward.restype = I
+    lib.tm2e_forward.argtypes = [P] * 6 + [I] * 5 + [F, I, P, S, P]
+    lib.tm2e_backward.restype = I
+    lib.tm2e_backward.argtypes = [P] * 11 + [I] * 5 + [F, I, P, S, P]
+    lib.tm2_poll_status.restype = I
+    _lib = lib
+    return lib
+
+
+def lib():
+    """The loaded ctypes library (raw C ABI)."""
+    return _load()
+
+
+def status_string(st: int) -> str:
+    return _load().tm2_status_string(int(st)).decode()
+
+
+def _check(st: int):
+    if st != 0:
+        raise TM2Error(status_string(st))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _seq_checks(q, k, v, a):
+    for name, t in (("q", q), ("k", k), ("v", v), ("a", a)):
+        if not t.is_cuda:
+            raise TM2Error("%s must be a CUDA tensor" % name)
+        if not t.is_contiguous():
+            raise TM2Error("%s must be contiguous" % name)
+    if q.dtype not in _DTYPES or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TM2Error("q, k, v must share one dtype in {float32, bfloat16}")
+    if a.dtype != torch.float32:
+        raise TM2Error("a must be float32")
+    B, H, T, d = q.shape
+    dv = v.shape[-1]
+    if k.shape != q.shape or v.shape[:3] != (B, H, T) or a.shape != (B, H, T):
+        raise TM2Error("shape mismatch: q,k (B,H,T,d), v (B,H,T,dv), a (B,H,T)")
+    return B, H, T, d, dv, _DTYPES[q.dtype]
+
+
+def _workspace(nbytes, device, workspace):
+    if nbytes == 0:
+        return None
+    if workspace is not None and workspace.numel() * workspace.element_size() >= nbytes:
+        return workspace
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def forward_workspace_bytes(B, H, T, d, dv, chunk=0, dtype=torch.bfloat16, normalize=True):
+    return int(_load().tm2_forward_workspace(B, H, T, d, dv, chunk, _DTYPES[dtype],
+                                             NORMALIZE if normalize else 0))
+
+
+def backward_workspace_bytes(B, H, T, d, dv, chunk=0, dtype=torch.bfloat16, normalize=True):
+    return int(_load().tm2_backward_workspace(B, H, T, d, dv, chunk, _DTYPES[dtype],
+                                              NORMALIZE if normalize else 0))
+
+
+def forward(q, k, v, a, *, normalize=True, chunk=0, S0=None, z0=None, return_state=False,
+            out=None, Z=None, workspace=None, stream=None):
+    """2Mamba forward.  Returns (o, Z) or, with return_state, (o, Z, S_final, z_final)."""
+    B, H, T, d, dv, dt = _seq_checks(q, k, v, a)
+    L = _load()
+    flags = NORMALIZE if normalize else 0
+    o = torch.empty(v.shape, dtype=torch.float32, device=q.device) if out is None else out
+    Z = torch.empty((B, H, T), dtype=torch.float32, device=q.device) if Z is None else Z
+    Sf = zf = None
+    if return_state:
+        Sf = torch.empty((B, H, d * d, dv), dtype=torch.float32, device=q.device)
+        zf = torch.empty((B, H, d * d), dtype=torch.float32, device=q.device)
+    ws = _workspace(L.tm2_forward_workspace(B, H, T, d, dv, chunk, dt, flags), q.device, workspace)
+    nbytes = 0 if ws is None else ws.numel()
+    _check(L.tm2_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(S0), _ptr(z0), _ptr(o), _ptr(Z),
+                         _ptr(Sf), _ptr(zf), B, H, T, d, dv, chunk, dt, flags, _ptr(ws), nbytes,
+                         _stream(stream)))
+    return (o, Z, Sf, zf) if return_state else (o, Z)
+
+
+def backward(q, k, v, a, o, Z, dO, *, normalize=True, chunk=0, workspace=None, stream=None,
+             grads=None):
+    """2Mamba backward.  Returns (dq, dk, dv, da)."""
+    B, H, T, d, dv, dt = _seq_checks(q, k, v, a)
+    L = _load()
+    flags = NORMALIZE if normalize else 0
+    if grads is None:
+        grads = tuple(torch.empty(t.shape, dtype=torch.float32, device=q.device) for t in (q, k, v, a))
+    dq, dk, dvv, da = grads
+    ws = _workspace(L.tm2_backward_workspace(B, H, T, d, dv, chunk, dt, flags), q.device, workspace)
+    nbytes = 0 if ws is None else ws.numel()
+    _check(L.tm2_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(o), _ptr(Z), _ptr(dO), _ptr(dq),
+                          _ptr(dk), _ptr(dvv), _ptr(da), B, H, T, d, dv, chunk, dt, flags, _ptr(ws),
+                          nbytes, _stream(stream)))
+    return dq, dk, dvv, da
+
+
+def step(q, k, v, a, S, z, *, normalize=True, out=None, Z=None, stream=None):
+    """One decode step, updating S (N,H,d*d,dv) and z (N,H,d*d) in place.  Returns (o, zeta)."""
+    N, H, d = q.shape
+    dv = v.shape[-1]
+    L = _load()
+    for name, t in (("q", q), ("k", k), ("v", v), ("a", a), ("S", S)) + ((("z", z),) if z is not None else ()):
+        if not t.is_cuda or not t.is_contiguous():
+            raise TM2Error("%s must be a contiguous CUDA tensor" % name)
+    if q.dtype not in _DTYPES or S.dtype != torch.float32 or a.dtype != torch.float32:
+        raise TM2Error("q, k, v in {float32, bfloat16}; a, S, z float32")
+    o = torch.empty(v.shape, dtype=torch.float32, device=q.device) if out is None else out
+    Z = torch.empty((N, H), dtype=torch.float32, device=q.device) if Z is None else Z
+    _check(L.tm2_step(_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(S), _ptr(z), _ptr(o), _ptr(Z), N, H, d,
+                      dv, _DTYPES[q.dtype], NORMALIZE if normalize else 0, _stream(stream)))
+    return o, Z
+
+
+def e_forward(q, k, v, a, *, scale=None, workspace=None, stream=None, out=None, lse=None):
+    """2Mamba-E forward.  Returns (o, lse)."""
+    B, H, T, d, dv, dt = _seq_checks(q, k, v, a)
+    L = _load()
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty(v.shape, dtype=torch.float32, device=q.device) if out is None else out
+    lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device) if lse is None else lse
+    ws = _workspace(L.tm2e_forward_workspace(B, H, T, d, dv, dt), q.device, workspace)
+    nbytes = 0 if ws is None else ws.numel()
+    _check(L.tm2e_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(o), _ptr(lse), B, H, T, d, dv,
+                          scale, dt, _ptr(ws), nbytes, _stream(stream)))
+    return o, lse
+
+
+def e_backward(q, k, v, a, o, lse, dO, *, scale=None, workspace=None, stream=None, grads=None):
+    """2Mamba-E backward.  Returns (dq, dk, dv, da)."""
+    B, H, T, d, dv, dt = _seq_checks(q, k, v, a)
+    L = _load()
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if grads is None:
+        grads = tuple(torch.empty(t.shape, dtype=torch.float32, device=q.device) for t in (q, k, v, a))
+    dq, dk, dvv, da = grads
+    ws = _workspace(L.tm2e_backward_workspace(B, H, T, d, dv, dt), q.device, workspace)
+    nbytes = 0 if ws is None else ws.numel()
+    _check(L.tm2e_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(o), _ptr(lse), _ptr(dO),
+                           _ptr(dq), _ptr(dk), _ptr(dvv), _ptr(da), B, H, T, d, dv, scale, dt,
+                           _ptr(ws), nbytes, _stream(stream)))
+    return dq, dk, dvv, da
+
+
+def poll_status() -> int:
+    """Reads and clears the device status word (TM2_ERR_TIMEOUT after an expired wait)."""
+    return int(_load().tm2_poll_status())

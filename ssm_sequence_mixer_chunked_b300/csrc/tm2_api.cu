@@ -1,0 +1,360 @@
+// tm2_api.cu -- the C ABI of libtm2.so (declared and documented in include/tm2.h):
+// argument validation, workspace carving and the launch sequence of each entry point.
+// Every launch goes on the caller's stream; nothing here allocates device memory or
+// synchronises the host (except tm2_poll_status, which reads the status word).
+#include <stdint.h>
+#include <string.h>
+
+#include <vector>
+
+#include "tm2.h"
+#include "tm2_common.cuh"
+#include "tm2_launch.h"
+
+namespace tm2 {
+
+__device__ int g_status = 0;
+
+struct Carve {
+    size_t off = 0;
+    size_t take(size_t bytes) {
+        const size_t o = off;
+        off += (bytes + 255) & ~(size_t)255;
+        return o;
+    }
+};
+
+static bool aligned16(const void* p) { return p == nullptr || ((uintptr_t)p & 15u) == 0; }
+
+// Validates the shape arguments shared by the sequence entry points and fills p.
+static int make_problem(int B, int H, int T, int d, int dv, int chunk, int dtype, unsigned flags,
+                        Problem& p) {
+    if (B < 0 || H < 0 || T < 0 || d <= 0 || dv <= 0) return TM2_ERR_INVALID_ARG;
+    if (dtype != TM2_F32 && dtype != TM2_BF16) return TM2_ERR_UNSUPPORTED;
+    if (d != dv || (d != 16 && d != 32 && d != 64)) return TM2_ERR_UNSUPPORTED;
+    if (chunk != 0 && chunk != 64) return TM2_ERR_UNSUPPORTED;
+    if ((long)B * H > 65535) return TM2_ERR_UNSUPPORTED;
+    if (flags & ~TM2_NORMALIZE) return TM2_ERR_INVALID_ARG;
+    p.B = B; p.H = H; p.T = T; p.d = d; p.dv = dv;
+    p.C = 64;
+    p.NC = (T + p.C - 1) / p.C;
+    p.dtype = dtype;
+    p.normalize = (flags & TM2_NORMALIZE) != 0;
+    return TM2_OK;
+}
+
+static size_t state_floats(const Problem& p) { return (size_t)p.d * (p.dv + 1) * p.d; }
+
+struct FwdWs { size_t Aloc, g, states, total; };
+static FwdWs plan_fwd(const Problem& p) {
+    Carve c;
+    FwdWs w;
+    w.Aloc = c.take(sizeof(float) * p.BH() * p.Tp());
+    w.g = c.take(sizeof(float) * p.BH() * p.NC);
+    w.states = c.take(sizeof(float) * p.BH() * p.NC * state_floats(p));
+    w.total = c.off;
+    return w;
+}
+
+struct BwdWs { size_t Aloc, g, states, dstates, dY, rowterm, dcum, total; };
+static BwdWs plan_bwd(const Problem& p) {
+    Carve c;
+    BwdWs w;
+    w.Aloc = c.take(sizeof(float) * p.BH() * p.Tp());
+    w.g = c.take(sizeof(float) * p.BH() * p.NC);
+    w.states = c.take(sizeof(float) * p.BH() * p.NC * state_floats(p));
+    w.dstates = c.take(sizeof(float) * p.BH() * p.NC * state_floats(p));
+    w.dY = c.take(sizeof(float) * p.BH() * p.T * (p.dv + 1));
+    w.rowterm = c.take(sizeof(float) * p.BH() * p.T);
+    w.dcum = c.take(sizeof(float) * p.BH() * p.T);
+    w.total = c.off;
+    return w;
+}
+
+struct EWs { size_t Aloc, g, cum, Dvec, rowsum, colsum, total; };
+static EWs plan_e(const Problem& p, bool backward) {
+    Carve c;
+    EWs w{};
+    w.Aloc = c.take(sizeof(float) * p.BH() * p.Tp());
+    w.g = c.take(sizeof(float) * p.BH() * p.NC);
+    w.cum = c.take(sizeof(float) * p.BH() * p.T);
+    if (backward) {
+        w.Dvec = c.take(sizeof(float) * p.BH() * p.T);
+        w.rowsum = c.take(sizeof(float) * p.BH() * p.T);
+        w.colsum = c.take(sizeof(float) * p.BH() * p.T);
+    }
+    w.total = c.off;
+    return w;
+}
+
+static int check_ws(void* ws, size_t ws_bytes, size_t need) {
+    if (need == 0) return TM2_OK;
+    if (ws == nullptr) return TM2_ERR_WORKSPACE;
+    if (ws_bytes < need) return TM2_ERR_WORKSPACE;
+    if (((uintptr_t)ws & 255u) != 0) return TM2_ERR_ALIGNMENT;
+    return TM2_OK;
+}
+
+#define TM2_CK(call)                                                   \
+    do {                                                               \
+        cudaError_t e_ = (call);                                       \
+        if (e_ != cudaSuccess) return TM2_ERR_CUDA;                    \
+    } while (0)
+
+template <typename T>
+static T* at(void* ws, size_t off) { return reinterpret_cast<T*>((char*)ws + off); }
+
+// ---- launch tracing ----------------------------------------------------------------
+struct TraceRec {
+    const char* name;
+    cudaEvent_t beg, end;
+};
+static bool g_trace_on = false;
+static std::vector<TraceRec> g_trace;   // events are created once and reused
+static size_t g_trace_n = 0;
+
+struct TraceScope {
+    TraceRec* rec = nullptr;
+    cudaStream_t s;
+    TraceScope(const char* name, cudaStream_t st) : s(st) {
+        if (!g_trace_on) return;
+        if (g_trace_n == g_trace.size()) {
+            TraceRec r{name, nullptr, nullptr};
+            if (cudaEventCreate(&r.beg) != cudaSuccess || cudaEventCreate(&r.end) != cudaSuccess) return;
+            g_trace.push_back(r);
+        }
+        rec = &g_trace[g_trace_n++];
+        rec->name = name;
+        cudaEventRecord(rec->beg, s);
+    }
+    ~TraceScope() {
+        if (rec) cudaEventRecord(rec->end, s);
+    }
+};
+
+#define TM2_RUN(name, call)                  \
+    do {                                     \
+        TraceScope ts_(name, s);             \
+        TM2_CK(call);                        \
+    } while (0)
+
+}  // namespace tm2
+
+using namespace tm2;
+
+extern "C" {
+
+int tm2_version(void) { return 100; }
+
+const char* tm2_status_string(int status) {
+    switch (status) {
+        case TM2_OK: return "TM2_OK";
+        case TM2_ERR_INVALID_ARG: return "TM2_ERR_INVALID_ARG: null pointer, negative size or inconsistent arguments";
+        case TM2_ERR_UNSUPPORTED: return "TM2_ERR_UNSUPPORTED: shape, chunk or dtype not implemented";
+        case TM2_ERR_ALIGNMENT: return "TM2_ERR_ALIGNMENT: pointer not 16-byte aligned (workspace: 256)";
+        case TM2_ERR_WORKSPACE: return "TM2_ERR_WORKSPACE: workspace missing or smaller than required";
+        case TM2_ERR_CUDA: return "TM2_ERR_CUDA: a CUDA launch or runtime call failed";
+        case TM2_ERR_TIMEOUT: return "TM2_ERR_TIMEOUT: a bounded device wait expired";
+        default: return "TM2: unknown status";
+    }
+}
+
+size_t tm2_forward_workspace(int B, int H, int T, int d, int dv, int chunk, int dtype,
+                             unsigned flags) {
+    Problem p;
+    if (make_problem(B, H, T, d, dv, chunk, dtype, flags, p) != TM2_OK) return 0;
+    return plan_fwd(p).total;
+}
+
+int tm2_forward(const void* q, const void* k, const void* v, const float* a, const float* S0,
+                const float* z0, void* o, float* Z, float* S_final, float* z_final, int B, int H,
+                int T, int d, int dv, int chunk, int dtype, unsigned flags, void* ws,
+                size_t ws_bytes, void* stream) {
+    Problem p;
+    int st = make_problem(B, H, T, d, dv, chunk, dtype, flags, p);
+    if (st != TM2_OK) return st;
+    const bool work = p.BH() > 0 && T > 0;
+    if (work && (!q || !k || !v || !a || !o)) return TM2_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, a, S0, z0, o, Z, S_final, z_final};
+    for (const void* x : ptrs)
+        if (!aligned16(x)) return TM2_ERR_ALIGNMENT;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (!work) {
+        // no tokens: the final state is the initial state
+        const size_t sb = sizeof(float) * p.BH() * d * d * dv, zb = sizeof(float) * p.BH() * d * d;
+        if (S_final) TM2_CK(S0 ? cudaMemcpyAsync(S_final, S0, sb, cudaMemcpyDeviceToDevice, s)
+                               : cudaMemsetAsync(S_final, 0, sb, s));
+        if (z_final) TM2_CK(z0 ? cudaMemcpyAsync(z_final, z0, zb, cudaMemcpyDeviceToDevice, s)
+                               : cudaMemsetAsync(z_final, 0, zb, s));
+        return TM2_OK;
+    }
+    const FwdWs w = plan_fwd(p);
+    st = check_ws(ws, ws_bytes, w.total);
+    if (st != TM2_OK) return st;
+    float* Aloc = at<float>(ws, w.Aloc);
+    float* g = at<float>(ws, w.g);
+    float* states = at<float>(ws, w.states);
+    TM2_RUN("decay_chunk", launch_decay(p, a, Aloc, g, s));
+    TM2_RUN("state_scan_fwd", simt_state_scan_fwd(p, k, v, Aloc, g, S0, z0, states, S_final, z_final, s));
+    TM2_RUN("chunk_out", simt_chunk_out(p, q, k, v, Aloc, states, o, Z, s));
+    return TM2_OK;
+}
+
+size_t tm2_backward_workspace(int B, int H, int T, int d, int dv, int chunk, int dtype,
+                              unsigned flags) {
+    Problem p;
+    if (make_problem(B, H, T, d, dv, chunk, dtype, flags, p) != TM2_OK) return 0;
+    return plan_bwd(p).total;
+}
+
+int tm2_backward(const void* q, const void* k, const void* v, const float* a, const void* o,
+                 const float* Z, const void* dO, void* dq, void* dk, void* dv, float* da, int B,
+                 int H, int T, int d, int dv_dim, int chunk, int dtype, unsigned flags, void* ws,
+                 size_t ws_bytes, void* stream) {
+    Problem p;
+    int st = make_problem(B, H, T, d, dv_dim, chunk, dtype, flags, p);
+    if (st != TM2_OK) return st;
+    if (p.BH() == 0 || T == 0) return TM2_OK;
+    if (!q || !k || !v || !a || !o || !dO || !dq || !dk || !dv || !da) return TM2_ERR_INVALID_ARG;
+    if (p.normalize && !Z) return TM2_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, a, o, Z, dO, dq, dk, dv, da};
+    for (const void* x : ptrs)
+        if (!aligned16(x)) return TM2_ERR_ALIGNMENT;
+    const BwdWs w = plan_bwd(p);
+    st = check_ws(ws, ws_bytes, w.total);
+    if (st != TM2_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    float* Aloc = at<float>(ws, w.Aloc);
+    float* g = at<float>(ws, w.g);
+    float* states = at<float>(ws, w.states);
+    float* dstates = at<float>(ws, w.dstates);
+    float* dY = at<float>(ws, w.dY);
+    float* rowterm = at<float>(ws, w.rowterm);
+    float* dcum = at<float>(ws, w.dcum);
+    TM2_RUN("decay_chunk", launch_decay(p, a, Aloc, g, s));
+    TM2_RUN("state_scan_fwd", simt_state_scan_fwd(p, k, v, Aloc, g, nullptr, nullptr, states, nullptr, nullptr, s));
+    TM2_RUN("dy_prep", launch_dy_prep(p, o, Z, dO, dY, rowterm, s));
+    TM2_RUN("state_scan_bwd", simt_state_scan_bwd(p, q, dY, Aloc, g, dstates, s));
+    TM2_RUN("bwd_chunk", simt_bwd_chunk(p, q, k, v, Aloc, g, dY, rowterm, states, dstates, dq, dk, dv, dcum, s));
+    TM2_RUN("reverse_cumsum_da", launch_reverse_cumsum_da(p, a, dcum, nullptr, da, s));
+    return TM2_OK;
+}
+
+int tm2_step(const void* q, const void* k, const void* v, const float* a, float* S, float* z,
+             void* o, float* Z, int N, int H, int d, int dv, int dtype, unsigned flags,
+             void* stream) {
+    if (N < 0 || H < 0 || d <= 0 || dv <= 0) return TM2_ERR_INVALID_ARG;
+    if (dtype != TM2_F32 && dtype != TM2_BF16) return TM2_ERR_UNSUPPORTED;
+    if (d != dv || (d != 16 && d != 32 && d != 64)) return TM2_ERR_UNSUPPORTED;
+    if (flags & ~TM2_NORMALIZE) return TM2_ERR_INVALID_ARG;
+    const bool normalize = (flags & TM2_NORMALIZE) != 0;
+    if ((long)N * H == 0) return TM2_OK;
+    if ((long)N * H > 0x7fffffffL) return TM2_ERR_UNSUPPORTED;
+    if (!q || !k || !v || !a || !S || !o) return TM2_ERR_INVALID_ARG;
+    if (normalize && !z) return TM2_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, a, S, z, o, Z};
+    for (const void* x : ptrs)
+        if (!aligned16(x)) return TM2_ERR_ALIGNMENT;
+    cudaStream_t s = (cudaStream_t)stream;
+    TM2_RUN("decode_step", launch_decode_step(N, H, d, dv, dtype, normalize, q, k, v, a, S, z, o, Z, s));
+    return TM2_OK;
+}
+
+size_t tm2e_forward_workspace(int B, int H, int T, int d, int dv, int dtype) {
+    Problem p;
+    if (make_problem(B, H, T, d, dv, 0, dtype, 0, p) != TM2_OK) return 0;
+    return plan_e(p, false).total;
+}
+
+int tm2e_forward(const void* q, const void* k, const void* v, const float* a, void* o, float* lse,
+                 int B, int H, int T, int d, int dv, float scale, int dtype, void* ws,
+                 size_t ws_bytes, void* stream) {
+    Problem p;
+    int st = make_problem(B, H, T, d, dv, 0, dtype, 0, p);
+    if (st != TM2_OK) return st;
+    if (!(scale == scale) || scale == 0.f) return TM2_ERR_INVALID_ARG;
+    if (p.BH() == 0 || T == 0) return TM2_OK;
+    if (!q || !k || !v || !a || !o || !lse) return TM2_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, a, o, lse};
+    for (const void* x : ptrs)
+        if (!aligned16(x)) return TM2_ERR_ALIGNMENT;
+    const EWs w = plan_e(p, false);
+    st = check_ws(ws, ws_bytes, w.total);
+    if (st != TM2_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    float* Aloc = at<float>(ws, w.Aloc);
+    float* g = at<float>(ws, w.g);
+    float* cum = at<float>(ws, w.cum);
+    TM2_RUN("decay_chunk", launch_decay(p, a, Aloc, g, s));
+    TM2_RUN("global_cumsum", launch_global_cumsum(p, Aloc, g, cum, s));
+    TM2_RUN("e_fwd", simt_e_fwd(p, q, k, v, cum, scale, o, lse, s));
+    return TM2_OK;
+}
+
+size_t tm2e_backward_workspace(int B, int H, int T, int d, int dv, int dtype) {
+    Problem p;
+    if (make_problem(B, H, T, d, dv, 0, dtype, 0, p) != TM2_OK) return 0;
+    return plan_e(p, true).total;
+}
+
+int tm2e_backward(const void* q, const void* k, const void* v, const float* a, const void* o,
+                  const float* lse, const void* dO, void* dq, void* dk, void* dv, float* da, int B,
+                  int H, int T, int d, int dv_dim, float scale, int dtype, void* ws,
+                  size_t ws_bytes, void* stream) {
+    Problem p;
+    int st = make_problem(B, H, T, d, dv_dim, 0, dtype, 0, p);
+    if (st != TM2_OK) return st;
+    if (!(scale == scale) || scale == 0.f) return TM2_ERR_INVALID_ARG;
+    if (p.BH() == 0 || T == 0) return TM2_OK;
+    if (!q || !k || !v || !a || !o || !lse || !dO || !dq || !dk || !dv || !da)
+        return TM2_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, a, o, lse, dO, dq, dk, dv, da};
+    for (const void* x : ptrs)
+        if (!aligned16(x)) return TM2_ERR_ALIGNMENT;
+    const EWs w = plan_e(p, true);
+    st = check_ws(ws, ws_bytes, w.total);
+    if (st != TM2_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    float* Aloc = at<float>(ws, w.Aloc);
+    float* g = at<float>(ws, w.g);
+    float* cum = at<float>(ws, w.cum);
+    float* Dvec = at<float>(ws, w.Dvec);
+    float* rowsum = at<float>(ws, w.rowsum);
+    float* colsum = at<float>(ws, w.colsum);
+    TM2_RUN("decay_chunk", launch_decay(p, a, Aloc, g, s));
+    TM2_RUN("global_cumsum", launch_global_cumsum(p, Aloc, g, cum, s));
+    TM2_RUN("rowdot", launch_rowdot(p, o, dO, Dvec, s));
+    TM2_RUN("e_bwd", simt_e_bwd(p, q, k, v, cum, lse, Dvec, dO, scale, dq, dk, dv, rowsum, colsum, s));
+    TM2_RUN("reverse_cumsum_da", launch_reverse_cumsum_da(p, a, rowsum, colsum, da, s));
+    return TM2_OK;
+}
+
+int tm2_trace_enable(int on) {
+    g_trace_on = on != 0;
+    if (g_trace_on) g_trace_n = 0;
+    return TM2_OK;
+}
+
+int tm2_trace_count(void) { return (int)g_trace_n; }
+
+int tm2_trace_read(int i, char* name, int name_len, float* ms) {
+    if (i < 0 || (size_t)i >= g_trace_n || !ms) return TM2_ERR_INVALID_ARG;
+    const TraceRec& r = g_trace[i];
+    if (name && name_len > 0) {
+        strncpy(name, r.name, (size_t)name_len - 1);
+        name[name_len - 1] = 0;
+    }
+    if (cudaEventSynchronize(r.end) != cudaSuccess) return TM2_ERR_CUDA;
+    if (cudaEventElapsedTime(ms, r.beg, r.end) != cudaSuccess) return TM2_ERR_CUDA;
+    return TM2_OK;
+}
+
+int tm2_poll_status(void) {
+    int h = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&h, tm2::g_status, sizeof(int)) != cudaSuccess) return TM2_ERR_CUDA;
+    if (h != 0 && cudaMemcpyToSymbol(tm2::g_status, &zero, sizeof(int)) != cudaSuccess)
+        return TM2_ERR_CUDA;
+    return h;
+}
+
+}  // extern "C"

@@ -1,0 +1,416 @@
+// tm2_e_simt.cu -- 2Mamba-E ("2Mamba2Furious", Sec. 6) on CUDA cores (fp32 arithmetic):
+// causal softmax attention whose logits carry the softplus A-mask,
+//   x_ij = scale q_i . k_j + cumA_i - cumA_j   (j <= i),   o_i = sum_j softmax_j(x_i.) v_j,
+// forward with a blockwise online maximum (running max and rescaled sum), backward with
+// P_ij = exp(x_ij - lse_i), dx_ij = P_ij (dO_i . v_j - D_i), D_i = dO_i . o_i.
+// Blocks of 64 queries x 64 keys; thread (ti, tc) of 16 x 16 owns rows ti + 16 r and
+// columns tc + 16 s of each 64 x 64 tile.
+#include "tm2_common.cuh"
+#include "tm2_launch.h"
+
+namespace tm2 {
+
+constexpr int EB = 64;
+
+template <int D, int DV, typename Tin>
+__global__ void __launch_bounds__(256) e_fwd_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
+                                                    const Tin* __restrict__ v, const float* __restrict__ cum,
+                                                    float scale, float* __restrict__ o,
+                                                    float* __restrict__ lse, int T) {
+    constexpr int LDQ = D + 1, LDP = EB + 1, NCOL = DV / 16;
+    extern __shared__ float sm[];
+    float* sq = sm;               // [EB][LDQ]
+    float* sk = sq + EB * LDQ;    // [EB][LDQ]
+    float* sv = sk + EB * LDQ;    // [EB][DV]
+    float* sP = sv + EB * DV;     // [EB][LDP]
+    float* scq = sP + EB * LDP;   // [EB]
+    float* sck = scq + EB;        // [EB]
+    const int qb = blockIdx.x;
+    const long bh = blockIdx.y;
+    const int tid = threadIdx.x, ti = tid >> 4, tc = tid & 15;
+    for (int e = tid; e < EB * D; e += 256) {
+        const int i = e / D, f = e % D;
+        const long t = (long)qb * EB + i;
+        sq[i * LDQ + f] = t < T ? to_f(q[(bh * T + t) * D + f]) : 0.f;
+    }
+    for (int i = tid; i < EB; i += 256) {
+        const long t = (long)qb * EB + i;
+        scq[i] = t < T ? cum[bh * T + t] : 0.f;
+    }
+    float acc[4][NCOL], mrow[4], lrow[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        mrow[r] = -INFINITY;
+        lrow[r] = 0.f;
+#pragma unroll
+        for (int s = 0; s < NCOL; ++s) acc[r][s] = 0.f;
+    }
+    for (int kb = 0; kb <= qb; ++kb) {
+        __syncthreads();
+        for (int e = tid; e < EB * D; e += 256) {
+            const int j = e / D, f = e % D;
+            const long t = (long)kb * EB + j;
+            sk[j * LDQ + f] = t < T ? to_f(k[(bh * T + t) * D + f]) : 0.f;
+        }
+        for (int e = tid; e < EB * DV; e += 256) {
+            const int j = e / DV, f = e % DV;
+            const long t = (long)kb * EB + j;
+            sv[e] = t < T ? to_f(v[(bh * T + t) * DV + f]) : 0.f;
+        }
+        for (int j = tid; j < EB; j += 256) {
+            const long t = (long)kb * EB + j;
+            sck[j] = t < T ? cum[bh * T + t] : 0.f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int i = ti + 16 * r;
+            const long ig = (long)qb * EB + i;
+            float x[4];
+            float mx = -INFINITY;
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const int j = tc + 16 * s;
+                const long jg = (long)kb * EB + j;
+                float dot = 0.f;
+#pragma unroll 16
+                for (int n = 0; n < D; ++n) dot = fmaf(sq[i * LDQ + n], sk[j * LDQ + n], dot);
+                x[s] = (jg <= ig && jg < T) ? scale * dot + scq[i] - sck[j] : -INFINITY;
+                mx = fmaxf(mx, x[s]);
+            }
+#pragma unroll
+            for (int o2 = 8; o2 > 0; o2 >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
+            const float mnew = fmaxf(mrow[r], mx);
+            const float msafe = mnew == -INFINITY ? 0.f : mnew;
+            float rs = 0.f;
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const float p = __expf(x[s] - msafe);
+                sP[i * LDP + tc + 16 * s] = p;
+                rs += p;
+            }
+#pragma unroll
+            for (int o2 = 8; o2 > 0; o2 >>= 1) rs += __shfl_xor_sync(0xffffffffu, rs, o2);
+            const float alpha = __expf(mrow[r] - msafe);
+            lrow[r] = lrow[r] * alpha + rs;
+#pragma unroll
+            for (int s = 0; s < NCOL; ++s) acc[r][s] *= alpha;
+            mrow[r] = mnew;
+        }
+        __syncthreads();
+        for (int j = 0; j < EB; ++j) {
+            float vv[NCOL];
+#pragma unroll
+            for (int s = 0; s < NCOL; ++s) vv[s] = sv[j * DV + tc + 16 * s];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const float p = sP[(ti + 16 * r) * LDP + j];
+#pragma unroll
+                for (int s = 0; s < NCOL; ++s) acc[r][s] = fmaf(p, vv[s], acc[r][s]);
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const long t = (long)qb * EB + ti + 16 * r;
+        if (t >= T) continue;
+        const float inv = 1.f / lrow[r];
+#pragma unroll
+        for (int s = 0; s < NCOL; ++s) o[(bh * T + t) * DV + tc + 16 * s] = acc[r][s] * inv;
+        if (tc == 0) lse[bh * T + t] = mrow[r] + logf(lrow[r]);
+    }
+}
+
+// dk, dv and column sums of dx for one block of 64 keys, looping over query blocks.
+template <int D, int DV, typename Tin>
+__global__ void __launch_bounds__(256) e_bwd_dkdv_kernel(
+    const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
+    const float* __restrict__ cum, const float* __restrict__ lse, const float* __restrict__ Dvec,
+    const Tin* __restrict__ dO, float scale, float* __restrict__ dk, float* __restrict__ dvo,
+    float* __restrict__ colsum, int T, int NQB) {
+    constexpr int LDQ = D + 1, LDV = DV + 1, LDP = EB + 1, NCOL = DV / 16, NN = D / 16;
+    extern __shared__ float sm[];
+    float* sk = sm;                 // [EB][LDQ]
+    float* sv = sk + EB * LDQ;      // [EB][LDV]
+    float* sq = sv + EB * LDV;      // [EB][LDQ]
+    float* sdo = sq + EB * LDQ;     // [EB][LDV]
+    float* sP = sdo + EB * LDV;     // [EB][LDP]
+    float* sX = sP + EB * LDP;      // [EB][LDP]
+    float* sck = sX + EB * LDP;     // [EB]
+    float* scq = sck + EB;          // [EB]
+    float* slse = scq + EB;         // [EB]
+    float* sD = slse + EB;          // [EB]
+    const int kb = blockIdx.x;
+    const long bh = blockIdx.y;
+    const int tid = threadIdx.x, ti = tid >> 4, tc = tid & 15;
+    for (int e = tid; e < EB * D; e += 256) {
+        const int j = e / D, f = e % D;
+        const long t = (long)kb * EB + j;
+        sk[j * LDQ + f] = t < T ? to_f(k[(bh * T + t) * D + f]) : 0.f;
+    }
+    for (int e = tid; e < EB * DV; e += 256) {
+        const int j = e / DV, f = e % DV;
+        const long t = (long)kb * EB + j;
+        sv[j * LDV + f] = t < T ? to_f(v[(bh * T + t) * DV + f]) : 0.f;
+    }
+    for (int j = tid; j < EB; j += 256) {
+        const long t = (long)kb * EB + j;
+        sck[j] = t < T ? cum[bh * T + t] : 0.f;
+    }
+    float adk[4][NN], adv[4][NCOL], cs[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        cs[r] = 0.f;
+#pragma unroll
+        for (int s = 0; s < NN; ++s) adk[r][s] = 0.f;
+#pragma unroll
+        for (int s = 0; s < NCOL; ++s) adv[r][s] = 0.f;
+    }
+    for (int qb = kb; qb < NQB; ++qb) {
+        __syncthreads();
+        for (int e = tid; e < EB * D; e += 256) {
+            const int i = e / D, f = e % D;
+            const long t = (long)qb * EB + i;
+            sq[i * LDQ + f] = t < T ? to_f(q[(bh * T + t) * D + f]) : 0.f;
+        }
+        for (int e = tid; e < EB * DV; e += 256) {
+            const int i = e / DV, f = e % DV;
+            const long t = (long)qb * EB + i;
+            sdo[i * LDV + f] = t < T ? to_f(dO[(bh * T + t) * DV + f]) : 0.f;
+        }
+        for (int i = tid; i < EB; i += 256) {
+            const long t = (long)qb * EB + i;
+            scq[i] = t < T ? cum[bh * T + t] : 0.f;
+            slse[i] = t < T ? lse[bh * T + t] : 0.f;
+            sD[i] = t < T ? Dvec[bh * T + t] : 0.f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const int i = ti + 16 * r, j = tc + 16 * s;
+                const long ig = (long)qb * EB + i, jg = (long)kb * EB + j;
+                float P = 0.f, dX = 0.f;
+                if (jg <= ig && ig < T) {
+                    float dot = 0.f;
+#pragma unroll 16
+                    for (int n = 0; n < D; ++n) dot = fmaf(sq[i * LDQ + n], sk[j * LDQ + n], dot);
+                    float dP = 0.f;
+#pragma unroll 16
+                    for (int cc = 0; cc < DV; ++cc) dP = fmaf(sdo[i * LDV + cc], sv[j * LDV + cc], dP);
+                    P = __expf(scale * dot + scq[i] - sck[j] - slse[i]);
+                    dX = P * (dP - sD[i]);
+                }
+                sP[i * LDP + j] = P;
+                sX[i * LDP + j] = dX;
+            }
+        __syncthreads();
+        for (int i = 0; i < EB; ++i) {
+            float qn[NN], dn[NCOL];
+#pragma unroll
+            for (int s = 0; s < NN; ++s) qn[s] = sq[i * LDQ + tc + 16 * s];
+#pragma unroll
+            for (int s = 0; s < NCOL; ++s) dn[s] = sdo[i * LDV + tc + 16 * s];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int j = ti + 16 * r;
+                const float p = sP[i * LDP + j], dx = sX[i * LDP + j];
+                cs[r] += dx;
+#pragma unroll
+                for (int s = 0; s < NN; ++s) adk[r][s] = fmaf(dx, qn[s], adk[r][s]);
+#pragma unroll
+                for (int s = 0; s < NCOL; ++s) adv[r][s] = fmaf(p, dn[s], adv[r][s]);
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const long t = (long)kb * EB + ti + 16 * r;
+        if (t >= T) continue;
+#pragma unroll
+        for (int s = 0; s < NN; ++s) dk[(bh * T + t) * D + tc + 16 * s] = scale * adk[r][s];
+#pragma unroll
+        for (int s = 0; s < NCOL; ++s) dvo[(bh * T + t) * DV + tc + 16 * s] = adv[r][s];
+        if (tc == 0) colsum[bh * T + t] = cs[r];
+    }
+}
+
+// dq and row sums of dx for one block of 64 queries, looping over key blocks.
+template <int D, int DV, typename Tin>
+__global__ void __launch_bounds__(256) e_bwd_dq_kernel(
+    const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
+    const float* __restrict__ cum, const float* __restrict__ lse, const float* __restrict__ Dvec,
+    const Tin* __restrict__ dO, float scale, float* __restrict__ dq, float* __restrict__ rowsum, int T) {
+    constexpr int LDQ = D + 1, LDV = DV + 1, LDP = EB + 1, NN = D / 16;
+    extern __shared__ float sm[];
+    float* sq = sm;                 // [EB][LDQ]
+    float* sdo = sq + EB * LDQ;     // [EB][LDV]
+    float* sk = sdo + EB * LDV;     // [EB][LDQ]
+    float* sv = sk + EB * LDQ;      // [EB][LDV]
+    float* sX = sv + EB * LDV;      // [EB][LDP]
+    float* scq = sX + EB * LDP;     // [EB]
+    float* sck = scq + EB;          // [EB]
+    float* slse = sck + EB;         // [EB]
+    float* sD = slse + EB;          // [EB]
+    const int qb = blockIdx.x;
+    const long bh = blockIdx.y;
+    const int tid = threadIdx.x, ti = tid >> 4, tc = tid & 15;
+    for (int e = tid; e < EB * D; e += 256) {
+        const int i = e / D, f = e % D;
+        const long t = (long)qb * EB + i;
+        sq[i * LDQ + f] = t < T ? to_f(q[(bh * T + t) * D + f]) : 0.f;
+    }
+    for (int e = tid; e < EB * DV; e += 256) {
+        const int i = e / DV, f = e % DV;
+        const long t = (long)qb * EB + i;
+        sdo[i * LDV + f] = t < T ? to_f(dO[(bh * T + t) * DV + f]) : 0.f;
+    }
+    for (int i = tid; i < EB; i += 256) {
+        const long t = (long)qb * EB + i;
+        scq[i] = t < T ? cum[bh * T + t] : 0.f;
+        slse[i] = t < T ? lse[bh * T + t] : 0.f;
+        sD[i] = t < T ? Dvec[bh * T + t] : 0.f;
+    }
+    float adq[4][NN], rs[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        rs[r] = 0.f;
+#pragma unroll
+        for (int s = 0; s < NN; ++s) adq[r][s] = 0.f;
+    }
+    for (int kb = 0; kb <= qb; ++kb) {
+        __syncthreads();
+        for (int e = tid; e < EB * D; e += 256) {
+            const int j = e / D, f = e % D;
+            const long t = (long)kb * EB + j;
+            sk[j * LDQ + f] = t < T ? to_f(k[(bh * T + t) * D + f]) : 0.f;
+        }
+        for (int e = tid; e < EB * DV; e += 256) {
+            const int j = e / DV, f = e % DV;
+            const long t = (long)kb * EB + j;
+            sv[j * LDV + f] = t < T ? to_f(v[(bh * T + t) * DV + f]) : 0.f;
+        }
+        for (int j = tid; j < EB; j += 256) {
+            const long t = (long)kb * EB + j;
+            sck[j] = t < T ? cum[bh * T + t] : 0.f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const int i = ti + 16 * r, j = tc + 16 * s;
+                const long ig = (long)qb * EB + i, jg = (long)kb * EB + j;
+                float dX = 0.f;
+                if (jg <= ig && ig < T) {
+                    float dot = 0.f;
+#pragma unroll 16
+                    for (int n = 0; n < D; ++n) dot = fmaf(sq[i * LDQ + n], sk[j * LDQ + n], dot);
+                    float dP = 0.f;
+#pragma unroll 16
+                    for (int cc = 0; cc < DV; ++cc) dP = fmaf(sdo[i * LDV + cc], sv[j * LDV + cc], dP);
+                    const float P = __expf(scale * dot + scq[i] - sck[j] - slse[i]);
+                    dX = P * (dP - sD[i]);
+                }
+                sX[i * LDP + j] = dX;
+                rs[r] += dX;
+            }
+        __syncthreads();
+        for (int j = 0; j < EB; ++j) {
+            float kn[NN];
+#pragma unroll
+            for (int s = 0; s < NN; ++s) kn[s] = sk[j * LDQ + tc + 16 * s];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const float dx = sX[(ti + 16 * r) * LDP + j];
+#pragma unroll
+                for (int s = 0; s < NN; ++s) adq[r][s] = fmaf(dx, kn[s], adq[r][s]);
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        float x = rs[r];
+#pragma unroll
+        for (int o2 = 8; o2 > 0; o2 >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o2);
+        const long t = (long)qb * EB + ti + 16 * r;
+        if (t >= T) continue;
+#pragma unroll
+        for (int s = 0; s < NN; ++s) dq[(bh * T + t) * D + tc + 16 * s] = scale * adq[r][s];
+        if (tc == 0) rowsum[bh * T + t] = x;
+    }
+}
+
+template <int D, int DV, typename Tin>
+static cudaError_t run_e_fwd(const Problem& p, const void* q, const void* k, const void* v,
+                             const float* cum, float scale, void* o, float* lse, cudaStream_t s) {
+    const size_t smem = sizeof(float) * (size_t)(2 * EB * (D + 1) + EB * DV + EB * (EB + 1) + 2 * EB);
+    auto kern = e_fwd_kernel<D, DV, Tin>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((p.T + EB - 1) / EB, (unsigned)p.BH());
+    kern<<<grid, 256, smem, s>>>((const Tin*)q, (const Tin*)k, (const Tin*)v, cum, scale, (float*)o, lse, p.T);
+    return cudaGetLastError();
+}
+
+template <int D, int DV, typename Tin>
+static cudaError_t run_e_bwd(const Problem& p, const void* q, const void* k, const void* v,
+                             const float* cum, const float* lse, const float* Dvec, const void* dO,
+                             float scale, void* dq, void* dk, void* dv, float* rowsum, float* colsum,
+                             cudaStream_t s) {
+    const int NQB = (p.T + EB - 1) / EB;
+    dim3 grid(NQB, (unsigned)p.BH());
+    {
+        const size_t smem = sizeof(float) * (size_t)(2 * EB * (D + 1) + 2 * EB * (DV + 1) +
+                                                     2 * EB * (EB + 1) + 4 * EB);
+        auto kern = e_bwd_dkdv_kernel<D, DV, Tin>;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        kern<<<grid, 256, smem, s>>>((const Tin*)q, (const Tin*)k, (const Tin*)v, cum, lse, Dvec,
+                                     (const Tin*)dO, scale, (float*)dk, (float*)dv, colsum, p.T, NQB);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    {
+        const size_t smem = sizeof(float) * (size_t)(2 * EB * (D + 1) + 2 * EB * (DV + 1) +
+                                                     EB * (EB + 1) + 4 * EB);
+        auto kern = e_bwd_dq_kernel<D, DV, Tin>;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        kern<<<grid, 256, smem, s>>>((const Tin*)q, (const Tin*)k, (const Tin*)v, cum, lse, Dvec,
+                                     (const Tin*)dO, scale, (float*)dq, rowsum, p.T);
+    }
+    return cudaGetLastError();
+}
+
+#define TM2_E_DISPATCH(P, CALL)                                                                  \
+    do {                                                                                         \
+        if ((P).dtype == 1) {                                                                    \
+            typedef __nv_bfloat16 Tin;                                                           \
+            if ((P).d == 64) { constexpr int D = 64; return CALL; }                              \
+            if ((P).d == 32) { constexpr int D = 32; return CALL; }                              \
+            if ((P).d == 16) { constexpr int D = 16; return CALL; }                              \
+        } else {                                                                                 \
+            typedef float Tin;                                                                   \
+            if ((P).d == 64) { constexpr int D = 64; return CALL; }                              \
+            if ((P).d == 32) { constexpr int D = 32; return CALL; }                              \
+            if ((P).d == 16) { constexpr int D = 16; return CALL; }                              \
+        }                                                                                        \
+        return cudaErrorInvalidValue;                                                            \
+    } while (0)
+
+cudaError_t simt_e_fwd(const Problem& p, const void* q, const void* k, const void* v,
+                       const float* cum, float scale, void* o, float* lse, cudaStream_t s) {
+    TM2_E_DISPATCH(p, (run_e_fwd<D, D, Tin>(p, q, k, v, cum, scale, o, lse, s)));
+}
+
+cudaError_t simt_e_bwd(const Problem& p, const void* q, const void* k, const void* v,
+                       const float* cum, const float* lse, const float* Dvec, const void* dO,
+                       float scale, void* dq, void* dk, void* dv, float* rowsum, float* colsum,
+                       cudaStream_t s) {
+    TM2_E_DISPATCH(p, (run_e_bwd<D, D, Tin>(p, q, k, v, cum, lse, Dvec, dO, scale, dq, dk, dv,
+                                            rowsum, colsum, s)));
+}
+
+}  // namespace tm2

@@ -1,0 +1,65 @@
+// tm2_launch.h -- host-side launchers of the libtm2 kernels (internal to the library).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+namespace tm2 {
+
+// Scalar problem description shared by the launchers.
+struct Problem {
+    int B, H, T, d, dv, C;   // C: chunk length
+    int NC;                  // number of chunks = ceil(T / C)
+    int dtype;               // 0 fp32, 1 bf16
+    bool normalize;
+    long BH() const { return (long)B * H; }
+    long Tp() const { return (long)NC * C; }   // padded sequence stride of chunk-local buffers
+};
+
+// ---- K1: decay running sums ----------------------------------------------------------
+// Aloc[bh][t] (t < Tp): inclusive running sum of -softplus(a) inside each chunk
+// (padded positions repeat the last valid value); g[bh][c]: chunk total.
+cudaError_t launch_decay(const Problem& p, const float* a, float* Aloc, float* g, cudaStream_t s);
+// cum[bh][t] = global inclusive running sum (t < T), from Aloc and g.
+cudaError_t launch_global_cumsum(const Problem& p, const float* Aloc, const float* g, float* cum,
+                                 cudaStream_t s);
+// da[bh][u] = -sigmoid(a[bh][u]) * sum_{t >= u} (row[bh][t] - col[bh][t]); col may be NULL.
+cudaError_t launch_reverse_cumsum_da(const Problem& p, const float* a, const float* row,
+                                     const float* col, float* da, cudaStream_t s);
+
+// ---- SIMT (fp32 arithmetic) 2Mamba path ---------------------------------------------
+// states: [BH][NC][d][dv+1][d] fp32 -- the state entering each chunk, column dv = z.
+cudaError_t simt_state_scan_fwd(const Problem& p, const void* k, const void* v, const float* Aloc,
+                                const float* g, const float* S0, const float* z0, float* states,
+                                float* S_final, float* z_final, cudaStream_t s);
+cudaError_t simt_chunk_out(const Problem& p, const void* q, const void* k, const void* v,
+                           const float* Aloc, const float* states, void* o, float* Z,
+                           cudaStream_t s);
+// dY[bh][t][dv+1] = [dO/Z, -D/Z] (normalised) or [dO, 0]; rowterm[bh][t] = dY_t . Y_t.
+cudaError_t launch_dy_prep(const Problem& p, const void* o, const float* Z, const void* dO,
+                           float* dY, float* rowterm, cudaStream_t s);
+// dstates: [BH][NC][d][dv+1][d], gradient w.r.t. the state at the END of each chunk.
+cudaError_t simt_state_scan_bwd(const Problem& p, const void* q, const float* dY, const float* Aloc,
+                                const float* g, float* dstates, cudaStream_t s);
+cudaError_t simt_bwd_chunk(const Problem& p, const void* q, const void* k, const void* v,
+                           const float* Aloc, const float* g, const float* dY,
+                           const float* rowterm, const float* states, const float* dstates,
+                           void* dq, void* dk, void* dv, float* dcum, cudaStream_t s);
+
+// ---- decode --------------------------------------------------------------------------
+cudaError_t launch_decode_step(int N, int H, int d, int dv, int dtype, bool normalize,
+                               const void* q, const void* k, const void* v, const float* a,
+                               float* S, float* z, void* o, float* Z, cudaStream_t s);
+
+// ---- 2Mamba-E (SIMT) -----------------------------------------------------------------
+cudaError_t simt_e_fwd(const Problem& p, const void* q, const void* k, const void* v,
+                       const float* cum, float scale, void* o, float* lse, cudaStream_t s);
+// Dvec[bh][t] = dO_t . o_t
+cudaError_t launch_rowdot(const Problem& p, const void* o, const void* dO, float* Dvec,
+                          cudaStream_t s);
+cudaError_t simt_e_bwd(const Problem& p, const void* q, const void* k, const void* v,
+                       const float* cum, const float* lse, const float* Dvec, const void* dO,
+                       float scale, void* dq, void* dk, void* dv, float* rowsum, float* colsum,
+                       cudaStream_t s);
+
+}  // namespace tm2

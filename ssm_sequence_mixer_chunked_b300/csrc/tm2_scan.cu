@@ -1,0 +1,163 @@
+// tm2_scan.cu -- the fp32 A-mask kernels: chunked running sums of -softplus(a)
+// ("2Mamba2Furious", Sec. 3/4: the softplus A-mask; the decay running sum always
+// runs in fp32), the reverse running sum that turns dL/dcumA into dL/da (App. C.1),
+// and small per-token preparation kernels of the backward passes.
+#include "tm2_common.cuh"
+#include "tm2_launch.h"
+
+namespace tm2 {
+
+// Block-wide inclusive scan of one value per thread (blockDim.x <= 1024).
+TM2_DEV float block_inclusive_scan(float v, float* wsum /* >= 32 floats */) {
+    const int t = threadIdx.x, w = t >> 5, lane = t & 31, nw = (blockDim.x + 31) >> 5;
+    float s = warp_inclusive_scan(v);
+    if (lane == 31) wsum[w] = s;
+    __syncthreads();
+    if (w == 0) {
+        float x = lane < nw ? wsum[lane] : 0.f;
+        x = warp_inclusive_scan(x);
+        wsum[lane] = x;
+    }
+    __syncthreads();
+    if (w > 0) s += wsum[w - 1];
+    __syncthreads();
+    return s;
+}
+
+// grid (NC, BH), block C threads: one chunk per block.
+__global__ void decay_chunk_kernel(const float* __restrict__ a, float* __restrict__ Aloc,
+                                   float* __restrict__ g, int T, int C, int NC) {
+    __shared__ float wsum[32];
+    const int c = blockIdx.x, t = threadIdx.x;
+    const long bh = blockIdx.y;
+    const long tok = (long)c * C + t;
+    const float l = tok < T ? -softplus_f(a[bh * T + tok]) : 0.f;
+    const float s = block_inclusive_scan(l, wsum);
+    Aloc[bh * (long)NC * C + tok] = s;
+    const int last = min(C, T - c * C) - 1;
+    if (t == last) g[bh * NC + c] = s;
+}
+
+cudaError_t launch_decay(const Problem& p, const float* a, float* Aloc, float* g, cudaStream_t s) {
+    dim3 grid(p.NC, (unsigned)p.BH());
+    decay_chunk_kernel<<<grid, p.C, 0, s>>>(a, Aloc, g, p.T, p.C, p.NC);
+    return cudaGetLastError();
+}
+
+// grid BH, block 256.  Chunk offsets are summed in fp64 so that only the final
+// rounding to fp32 enters cum.
+__global__ void global_cumsum_kernel(const float* __restrict__ Aloc, const float* __restrict__ g,
+                                     float* __restrict__ cum, int T, int C, int NC) {
+    extern __shared__ double off[];   // NC doubles
+    const long bh = blockIdx.x;
+    if (threadIdx.x == 0) {
+        double acc = 0.0;
+        for (int c = 0; c < NC; ++c) {
+            off[c] = acc;
+            acc += (double)g[bh * NC + c];
+        }
+    }
+    __syncthreads();
+    for (int t = threadIdx.x; t < T; t += blockDim.x)
+        cum[bh * T + t] = (float)(off[t / C] + (double)Aloc[bh * (long)NC * C + t]);
+}
+
+cudaError_t launch_global_cumsum(const Problem& p, const float* Aloc, const float* g, float* cum,
+                                 cudaStream_t s) {
+    size_t smem = sizeof(double) * (size_t)p.NC;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(global_cumsum_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    global_cumsum_kernel<<<(unsigned)p.BH(), 256, smem, s>>>(Aloc, g, cum, p.T, p.C, p.NC);
+    return cudaGetLastError();
+}
+
+// grid BH, block 1024: walks the sequence from its end in tiles of 1024.
+__global__ void __launch_bounds__(1024) reverse_cumsum_da_kernel(
+    const float* __restrict__ a, const float* __restrict__ row, const float* __restrict__ col,
+    float* __restrict__ da, int T) {
+    __shared__ float wsum[32];
+    __shared__ float carry_s;
+    const long bh = blockIdx.x;
+    float carry = 0.f;
+    for (int base = T - 1; base >= 0; base -= blockDim.x) {
+        const int u = base - (int)threadIdx.x;   // thread 0 holds the latest token of the tile
+        float x = 0.f;
+        if (u >= 0) x = row[bh * T + u] - (col ? col[bh * T + u] : 0.f);
+        float s = block_inclusive_scan(x, wsum) + carry;
+        if (u >= 0) da[bh * T + u] = -sigmoid_f(a[bh * T + u]) * s;
+        if (threadIdx.x == blockDim.x - 1) carry_s = s;
+        __syncthreads();
+        carry = carry_s;
+        __syncthreads();
+    }
+}
+
+cudaError_t launch_reverse_cumsum_da(const Problem& p, const float* a, const float* row,
+                                     const float* col, float* da, cudaStream_t s) {
+    reverse_cumsum_da_kernel<<<(unsigned)p.BH(), 1024, 0, s>>>(a, row, col, da, p.T);
+    return cudaGetLastError();
+}
+
+// One warp per token: D = dO . o; dY = [dO/Z, -D/Z] (normalised) or [dO, 0];
+// rowterm = dY . Y, which is exactly 0 when normalised (Y = [N, Z] and o = N/Z)
+// and dO . o otherwise.
+template <typename Tin>
+__global__ void dy_prep_kernel(const float* __restrict__ o, const float* __restrict__ Z,
+                               const Tin* __restrict__ dO, float* __restrict__ dY,
+                               float* __restrict__ rowterm, long ntok, int dv, bool normalize) {
+    const long tok = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (tok >= ntok) return;
+    float D = 0.f;
+    for (int c = lane; c < dv; c += 32) D += to_f(dO[tok * dv + c]) * o[tok * dv + c];
+    D = warp_sum(D);
+    const float z = normalize ? Z[tok] : 1.f;
+    const float inv = (normalize && z != 0.f) ? 1.f / z : (normalize ? 0.f : 1.f);
+    for (int c = lane; c < dv; c += 32) dY[tok * (dv + 1) + c] = to_f(dO[tok * dv + c]) * inv;
+    if (lane == 0) {
+        dY[tok * (dv + 1) + dv] = normalize ? -D * inv : 0.f;
+        rowterm[tok] = normalize ? 0.f : D;
+    }
+}
+
+cudaError_t launch_dy_prep(const Problem& p, const void* o, const float* Z, const void* dO,
+                           float* dY, float* rowterm, cudaStream_t s) {
+    const long ntok = p.BH() * p.T;
+    const unsigned blocks = (unsigned)((ntok + 7) / 8);
+    if (p.dtype == 1)
+        dy_prep_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
+            (const float*)o, Z, (const __nv_bfloat16*)dO, dY, rowterm, ntok, p.dv, p.normalize);
+    else
+        dy_prep_kernel<float><<<blocks, 256, 0, s>>>((const float*)o, Z, (const float*)dO, dY,
+                                                     rowterm, ntok, p.dv, p.normalize);
+    return cudaGetLastError();
+}
+
+template <typename Tin>
+__global__ void rowdot_kernel(const float* __restrict__ o, const Tin* __restrict__ dO,
+                              float* __restrict__ out, long ntok, int dv) {
+    const long tok = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (tok >= ntok) return;
+    float D = 0.f;
+    for (int c = lane; c < dv; c += 32) D += to_f(dO[tok * dv + c]) * o[tok * dv + c];
+    D = warp_sum(D);
+    if (lane == 0) out[tok] = D;
+}
+
+cudaError_t launch_rowdot(const Problem& p, const void* o, const void* dO, float* Dvec,
+                          cudaStream_t s) {
+    const long ntok = p.BH() * p.T;
+    const unsigned blocks = (unsigned)((ntok + 7) / 8);
+    if (p.dtype == 1)
+        rowdot_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>((const float*)o,
+                                                           (const __nv_bfloat16*)dO, Dvec, ntok, p.dv);
+    else
+        rowdot_kernel<float><<<blocks, 256, 0, s>>>((const float*)o, (const float*)dO, Dvec, ntok, p.dv);
+    return cudaGetLastError();
+}
+
+}  // namespace tm2

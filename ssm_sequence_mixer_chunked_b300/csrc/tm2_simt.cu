@@ -1,0 +1,547 @@
+// tm2_simt.cu -- the fp32-arithmetic (CUDA-core FFMA) chunked 2Mamba path.
+//
+// "2Mamba2Furious", Sec. 5: w_ij = exp(cumA_i - cumA_j) (q_i . k_j)^2, N_i = sum_j w_ij v_j,
+// Z_i = sum_j w_ij; Sec. 2: the (d^2, dv) second-order state; App. C: gradients.
+//
+// Chunked evaluation with chunk length C = 64.  Inside chunk c, A_t is the running
+// sum of -softplus(a) restarted at the chunk start and g_c the chunk total, so
+// cumA_i - cumA_j = A_i - A_j for i, j in the chunk, and the state entering chunk c,
+//   S_{c-1}[(m,n), col] = sum_{j < cC} exp(cumA_{cC-1} - cumA_j) k_j[m] k_j[n] Vt_j[col],
+// (Vt_j = [v_j, 1]: column dv carries the normaliser z) satisfies
+//   S_c = exp(g_c) S_{c-1} + sum_{j in c} exp(g_c - A_j) (k_j (x) k_j) Vt_j^T,
+//   Y_i = [N_i, Z_i] = sum_{j in c, j <= i} exp(A_i - A_j) s_ij^2 Vt_j + exp(A_i) (q_i (x) q_i)^T S_{c-1}.
+// Every exponent is <= 0, so nothing overflows at any T.
+//
+// State storage (workspace): [BH][NC][m][col][n], col in [0, dv] -- for fixed (m, col)
+// the n index is contiguous.  This path is the fp32 mode (the 1e-4 tolerance rules out
+// TF32 tensor-core inputs) and the generic fallback for every d = dv in {16, 32, 64}.
+#include "tm2_common.cuh"
+#include "tm2_launch.h"
+
+namespace tm2 {
+
+constexpr int SIMT_C = 64;
+
+// ------------------------------------------------------------------------------------
+// Sequential chunk walk building the second-order state.  One thread owns 16
+// consecutive n of one (m, col) state row and keeps them in registers across chunks.
+//  forward (REV = false): key = k, val = [v, 1], weight w_j = exp(g_c - A_j);
+//      out[c] = state entering chunk c; S <- exp(g_c) S + sum_j w_j (k_j (x) k_j) val_j^T.
+//  reverse (REV = true):  key = q, val = dY, weight w_i = exp(A_i), chunks from the end;
+//      out[c] = dS_c, the gradient w.r.t. the state at the end of chunk c;
+//      dS_{c-1} = exp(g_c) dS_c + sum_{i in c} exp(A_i) (q_i (x) q_i) dY_i^T.
+// ------------------------------------------------------------------------------------
+template <int D, int DV, typename Tin, bool REV>
+__global__ void __launch_bounds__(256) state_scan_kernel(
+    const Tin* __restrict__ key, const Tin* __restrict__ vin, const float* __restrict__ dY,
+    const float* __restrict__ Aloc, const float* __restrict__ g, const float* __restrict__ S0,
+    const float* __restrict__ z0, float* __restrict__ states, float* __restrict__ S_final,
+    float* __restrict__ z_final, int T, int NC) {
+    constexpr int C = SIMT_C;
+    constexpr int NB = 16;
+    constexpr int NBLK = D / NB;
+    constexpr int DV1 = DV + 1;
+    constexpr int ELEMS = D * DV1 * NBLK;
+    __shared__ float skey[C][D];
+    __shared__ float sval[C][DV1];
+    __shared__ float sw[C];
+    const long bh = blockIdx.y;
+    const int idx = blockIdx.x * 256 + threadIdx.x;
+    const bool active = idx < ELEMS;
+    const int nb = idx % NBLK;
+    const int col = (idx / NBLK) % DV1;
+    const int m = min(idx / (NBLK * DV1), D - 1);
+    const int n0 = nb * NB;
+
+    float S[NB];
+#pragma unroll
+    for (int e = 0; e < NB; ++e) S[e] = 0.f;
+    if (!REV && active) {
+        if (col < DV) {
+            if (S0)
+#pragma unroll
+                for (int e = 0; e < NB; ++e) S[e] = S0[((bh * D + m) * D + n0 + e) * DV + col];
+        } else if (z0) {
+#pragma unroll
+            for (int e = 0; e < NB; ++e) S[e] = z0[(bh * D + m) * D + n0 + e];
+        }
+    }
+
+    for (int it = 0; it < NC; ++it) {
+        const int c = REV ? NC - 1 - it : it;
+        for (int e = threadIdx.x; e < C * D; e += 256) {
+            const int j = e / D, f = e % D;
+            const long t = (long)c * C + j;
+            skey[j][f] = t < T ? to_f(key[(bh * T + t) * D + f]) : 0.f;
+        }
+        for (int e = threadIdx.x; e < C * DV1; e += 256) {
+            const int j = e / DV1, f = e % DV1;
+            const long t = (long)c * C + j;
+            float x = 0.f;
+            if (t < T) {
+                if (REV) x = dY[(bh * T + t) * DV1 + f];
+                else x = f < DV ? to_f(vin[(bh * T + t) * DV + f]) : 1.f;
+            }
+            sval[j][f] = x;
+        }
+        const float gc = g[bh * NC + c];
+        for (int j = threadIdx.x; j < C; j += 256) {
+            const float A = Aloc[bh * (long)NC * C + (long)c * C + j];
+            sw[j] = REV ? __expf(A) : __expf(gc - A);
+        }
+        __syncthreads();
+        if (active) {
+            float4* dst = reinterpret_cast<float4*>(
+                states + ((((bh * NC + c) * D + m) * DV1 + col) * (long)D + n0));
+#pragma unroll
+            for (int e = 0; e < NB; e += 4) dst[e / 4] = make_float4(S[e], S[e + 1], S[e + 2], S[e + 3]);
+            float h[NB];
+#pragma unroll
+            for (int e = 0; e < NB; ++e) h[e] = 0.f;
+#pragma unroll 4
+            for (int j = 0; j < C; ++j) {
+                const float u = sw[j] * skey[j][m] * sval[j][col];
+#pragma unroll
+                for (int e = 0; e < NB; ++e) h[e] = fmaf(u, skey[j][n0 + e], h[e]);
+            }
+            const float dec = __expf(gc);
+#pragma unroll
+            for (int e = 0; e < NB; ++e) S[e] = fmaf(dec, S[e], h[e]);
+        }
+        __syncthreads();
+    }
+    if (!REV && active) {
+        if (col < DV) {
+            if (S_final)
+#pragma unroll
+                for (int e = 0; e < NB; ++e) S_final[((bh * D + m) * D + n0 + e) * DV + col] = S[e];
+        } else if (z_final) {
+#pragma unroll
+            for (int e = 0; e < NB; ++e) z_final[(bh * D + m) * D + n0 + e] = S[e];
+        }
+    }
+}
+
+template <int D, int DV, typename Tin, bool REV>
+static cudaError_t run_state_scan(const Problem& p, const void* key, const void* vin, const float* dY,
+                                  const float* Aloc, const float* g, const float* S0,
+                                  const float* z0, float* states, float* S_final, float* z_final,
+                                  cudaStream_t s) {
+    constexpr int ELEMS = D * (DV + 1) * (D / 16);
+    dim3 grid((ELEMS + 255) / 256, (unsigned)p.BH());
+    state_scan_kernel<D, DV, Tin, REV><<<grid, 256, 0, s>>>(
+        (const Tin*)key, (const Tin*)vin, dY, Aloc, g, S0, z0, states, S_final, z_final, p.T, p.NC);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------------------
+// Per-chunk output: intra-chunk squared masked scores, their product with [v, 1], and
+// the readout exp(A_i) (q_i (x) q_i)^T S_{c-1}; then o = N / Z (or N).
+// Thread (ti, tc) of 16 x 16 owns rows i = ti + 16 r (r < 4) and value columns
+// tc + 16 s (s < dv/16); column dv (Z) is carried by every thread, kept by tc == 0.
+// ------------------------------------------------------------------------------------
+template <int D, int DV, typename Tin>
+__global__ void __launch_bounds__(256) chunk_out_kernel(
+    const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
+    const float* __restrict__ Aloc, const float* __restrict__ states, float* __restrict__ o,
+    float* __restrict__ Z, int T, int NC, bool normalize) {
+    constexpr int C = SIMT_C, DV1 = DV + 1, NCOL = DV / 16, LDQ = D + 1, LDW = C + 1;
+    extern __shared__ float sm[];
+    float* sq = sm;                 // [C][D+1]
+    float* sk = sq + C * LDQ;       // [C][D+1]
+    float* sv = sk + C * LDQ;       // [C][DV+1]
+    float* sW = sv + C * DV1;       // [C][C+1]
+    float* sS = sW + C * LDW;       // [DV+1][D+1]
+    float* sA = sS + DV1 * LDQ;     // [C]
+    float* sZ = sA + C;             // [C]
+    const int c = blockIdx.x;
+    const long bh = blockIdx.y;
+    const int tid = threadIdx.x, ti = tid >> 4, tc = tid & 15;
+
+    for (int e = tid; e < C * D; e += 256) {
+        const int j = e / D, f = e % D;
+        const long t = (long)c * C + j;
+        sq[j * LDQ + f] = t < T ? to_f(q[(bh * T + t) * D + f]) : 0.f;
+        sk[j * LDQ + f] = t < T ? to_f(k[(bh * T + t) * D + f]) : 0.f;
+    }
+    for (int e = tid; e < C * DV1; e += 256) {
+        const int j = e / DV1, f = e % DV1;
+        const long t = (long)c * C + j;
+        sv[e] = t < T ? (f < DV ? to_f(v[(bh * T + t) * DV + f]) : 1.f) : 0.f;
+    }
+    for (int j = tid; j < C; j += 256) sA[j] = Aloc[bh * (long)NC * C + (long)c * C + j];
+    __syncthreads();
+
+    // intra-chunk weights W_ij = (q_i . k_j)^2 exp(A_i - A_j), j <= i
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int s2 = 0; s2 < 4; ++s2) {
+            const int i = ti + 16 * r, j = tc + 16 * s2;
+            float dot = 0.f;
+#pragma unroll 16
+            for (int n = 0; n < D; ++n) dot = fmaf(sq[i * LDQ + n], sk[j * LDQ + n], dot);
+            sW[i * LDW + j] = j <= i ? dot * dot * __expf(sA[i] - sA[j]) : 0.f;
+        }
+    __syncthreads();
+
+    float acc[4][NCOL + 1];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int s2 = 0; s2 <= NCOL; ++s2) acc[r][s2] = 0.f;
+    for (int j = 0; j < C; ++j) {
+        float vv[NCOL + 1];
+#pragma unroll
+        for (int s2 = 0; s2 < NCOL; ++s2) vv[s2] = sv[j * DV1 + tc + 16 * s2];
+        vv[NCOL] = sv[j * DV1 + DV];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const float w = sW[(ti + 16 * r) * LDW + j];
+#pragma unroll
+            for (int s2 = 0; s2 <= NCOL; ++s2) acc[r][s2] = fmaf(w, vv[s2], acc[r][s2]);
+        }
+    }
+
+    // inter-chunk readout of the state entering this chunk
+    float eA[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) eA[r] = __expf(sA[ti + 16 * r]);
+    const float* Sc = states + (bh * NC + c) * (long)D * DV1 * D;
+    for (int m = 0; m < D; ++m) {
+        __syncthreads();
+        const float4* src = reinterpret_cast<const float4*>(Sc + (long)m * DV1 * D);
+        for (int e = tid; e < DV1 * D / 4; e += 256) {
+            const float4 x = src[e];
+            const int cc = (4 * e) / D, n = (4 * e) % D;
+            float* d = sS + cc * LDQ + n;
+            d[0] = x.x; d[1] = x.y; d[2] = x.z; d[3] = x.w;
+        }
+        __syncthreads();
+        float U[4][NCOL + 1];
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int s2 = 0; s2 <= NCOL; ++s2) U[r][s2] = 0.f;
+#pragma unroll 4
+        for (int n = 0; n < D; ++n) {
+            float sv2[NCOL + 1];
+#pragma unroll
+            for (int s2 = 0; s2 < NCOL; ++s2) sv2[s2] = sS[(tc + 16 * s2) * LDQ + n];
+            sv2[NCOL] = sS[DV * LDQ + n];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const float qv = sq[(ti + 16 * r) * LDQ + n];
+#pragma unroll
+                for (int s2 = 0; s2 <= NCOL; ++s2) U[r][s2] = fmaf(qv, sv2[s2], U[r][s2]);
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const float coef = eA[r] * sq[(ti + 16 * r) * LDQ + m];
+#pragma unroll
+            for (int s2 = 0; s2 <= NCOL; ++s2) acc[r][s2] = fmaf(coef, U[r][s2], acc[r][s2]);
+        }
+    }
+
+    if (tc == 0)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) sZ[ti + 16 * r] = acc[r][NCOL];
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int i = ti + 16 * r;
+        const long t = (long)c * C + i;
+        if (t >= T) continue;
+        const float z = sZ[i];
+        const float inv = z != 0.f ? 1.f / z : 0.f;
+#pragma unroll
+        for (int s2 = 0; s2 < NCOL; ++s2) {
+            const float val = normalize ? acc[r][s2] * inv : acc[r][s2];
+            o[(bh * T + t) * DV + tc + 16 * s2] = val;
+        }
+        if (tc == 0 && Z) Z[bh * T + t] = z;
+    }
+}
+
+template <int D, int DV, typename Tin>
+static cudaError_t run_chunk_out(const Problem& p, const void* q, const void* k, const void* v,
+                                 const float* Aloc, const float* states, void* o, float* Z,
+                                 cudaStream_t s) {
+    constexpr int C = SIMT_C;
+    const size_t smem = sizeof(float) * (size_t)(2 * C * (D + 1) + C * (DV + 1) + C * (C + 1) +
+                                                 (DV + 1) * (D + 1) + 2 * C);
+    auto kern = chunk_out_kernel<D, DV, Tin>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(p.NC, (unsigned)p.BH());
+    kern<<<grid, 256, smem, s>>>((const Tin*)q, (const Tin*)k, (const Tin*)v, Aloc, states, (float*)o, Z,
+                                 p.T, p.NC, p.normalize);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------------------
+// Per-chunk backward.  With dY_i = dL/dY_i, dW_ij = dY_i . Vt_j, dS_ij = 2 s_ij E_ij dW_ij
+// (E_ij = exp(A_i - A_j), j <= i):
+//   dq_i = sum_j dS_ij k_j + 2 exp(A_i) sum_n q_i[n] sum_col S_{c-1}[(m,n),col] dY_i[col]
+//   dk_j = sum_i dS_ij q_i + 2 w_j sum_n k_j[n] sum_col dS_c[(m,n),col] Vt_j[col]
+//   dVt_j = sum_i W_ij dY_i + w_j (k_j (x) k_j)^T dS_c                (w_j = exp(g_c - A_j))
+//   dcumA_t = dY_t . Y_t - Vt_t . dVt_t   (row-axis sum minus column-axis sum)
+// The factor 2 uses the symmetry of both states in (m, n), which holds because the
+// backward assumes no initial state.
+// ------------------------------------------------------------------------------------
+template <int D, int DV, typename Tin>
+__global__ void __launch_bounds__(256) bwd_chunk_kernel(
+    const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
+    const float* __restrict__ Aloc, const float* __restrict__ g, const float* __restrict__ dY,
+    const float* __restrict__ rowterm, const float* __restrict__ states,
+    const float* __restrict__ dstates, float* __restrict__ dq, float* __restrict__ dk,
+    float* __restrict__ dvo, float* __restrict__ dcum, int T, int NC) {
+    constexpr int C = SIMT_C, DV1 = DV + 1, NCOL = DV / 16, NN = D / 16;
+    constexpr int LDQ = D + 1, LDV = DV1 + 1, LDW = C + 1;
+    extern __shared__ float sm[];
+    float* sq = sm;                   // [C][LDQ]
+    float* sk = sq + C * LDQ;         // [C][LDQ]
+    float* sv = sk + C * LDQ;         // [C][LDV]  Vt = [v, 1]
+    float* sdy = sv + C * LDV;        // [C][LDV]
+    float* sA = sdy + C * LDV;        // [C]
+    float* sw = sA + C;               // [C]  exp(g - A_j)
+    float* seA = sw + C;              // [C]  exp(A_i)
+    float* sW = seA + C;              // [C][LDW]
+    float* sdS = sW + C * LDW;        // [C][LDW]
+    float* sSp = sdS + C * LDW;       // [DV1][LDQ]
+    float* sdSt = sSp + DV1 * LDQ;    // [DV1][LDQ]
+    float* sdqi = sdSt + DV1 * LDQ;   // [C][LDQ]
+    float* sdki = sdqi + C * LDQ;     // [C][LDQ]
+    const int c = blockIdx.x;
+    const long bh = blockIdx.y;
+    const int tid = threadIdx.x, ti = tid >> 4, tc = tid & 15;
+
+    for (int e = tid; e < C * D; e += 256) {
+        const int j = e / D, f = e % D;
+        const long t = (long)c * C + j;
+        sq[j * LDQ + f] = t < T ? to_f(q[(bh * T + t) * D + f]) : 0.f;
+        sk[j * LDQ + f] = t < T ? to_f(k[(bh * T + t) * D + f]) : 0.f;
+    }
+    for (int e = tid; e < C * DV1; e += 256) {
+        const int j = e / DV1, f = e % DV1;
+        const long t = (long)c * C + j;
+        sv[j * LDV + f] = t < T ? (f < DV ? to_f(v[(bh * T + t) * DV + f]) : 1.f) : 0.f;
+        sdy[j * LDV + f] = t < T ? dY[(bh * T + t) * DV1 + f] : 0.f;
+    }
+    const float gc = g[bh * NC + c];
+    for (int j = tid; j < C; j += 256) {
+        const float A = Aloc[bh * (long)NC * C + (long)c * C + j];
+        sA[j] = A;
+        sw[j] = __expf(gc - A);
+        seA[j] = __expf(A);
+    }
+    __syncthreads();
+
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int s2 = 0; s2 < 4; ++s2) {
+            const int i = ti + 16 * r, j = tc + 16 * s2;
+            float dot = 0.f;
+#pragma unroll 16
+            for (int n = 0; n < D; ++n) dot = fmaf(sq[i * LDQ + n], sk[j * LDQ + n], dot);
+            float dw = 0.f;
+#pragma unroll 8
+            for (int cc = 0; cc < DV1; ++cc) dw = fmaf(sdy[i * LDV + cc], sv[j * LDV + cc], dw);
+            const float E = j <= i ? __expf(sA[i] - sA[j]) : 0.f;
+            sW[i * LDW + j] = dot * dot * E;
+            sdS[i * LDW + j] = 2.f * dot * E * dw;
+        }
+    __syncthreads();
+
+    float aq[4][NN], ak[4][NN], av[4][NCOL + 1];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+#pragma unroll
+        for (int s2 = 0; s2 < NN; ++s2) aq[r][s2] = ak[r][s2] = 0.f;
+#pragma unroll
+        for (int s2 = 0; s2 <= NCOL; ++s2) av[r][s2] = 0.f;
+    }
+    for (int j = 0; j < C; ++j) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const float ds = sdS[(ti + 16 * r) * LDW + j];
+#pragma unroll
+            for (int s2 = 0; s2 < NN; ++s2) aq[r][s2] = fmaf(ds, sk[j * LDQ + tc + 16 * s2], aq[r][s2]);
+        }
+    }
+    for (int i = 0; i < C; ++i) {
+        float qn[NN], yv[NCOL + 1];
+#pragma unroll
+        for (int s2 = 0; s2 < NN; ++s2) qn[s2] = sq[i * LDQ + tc + 16 * s2];
+#pragma unroll
+        for (int s2 = 0; s2 < NCOL; ++s2) yv[s2] = sdy[i * LDV + tc + 16 * s2];
+        yv[NCOL] = sdy[i * LDV + DV];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int j = ti + 16 * r;
+            const float ds = sdS[i * LDW + j], w = sW[i * LDW + j];
+#pragma unroll
+            for (int s2 = 0; s2 < NN; ++s2) ak[r][s2] = fmaf(ds, qn[s2], ak[r][s2]);
+#pragma unroll
+            for (int s2 = 0; s2 <= NCOL; ++s2) av[r][s2] = fmaf(w, yv[s2], av[r][s2]);
+        }
+    }
+
+    const float* Sp = states + (bh * NC + c) * (long)D * DV1 * D;
+    const float* dSt = dstates + (bh * NC + c) * (long)D * DV1 * D;
+    for (int m = 0; m < D; ++m) {
+        __syncthreads();
+        const float4* s1 = reinterpret_cast<const float4*>(Sp + (long)m * DV1 * D);
+        const float4* s2p = reinterpret_cast<const float4*>(dSt + (long)m * DV1 * D);
+        for (int e = tid; e < DV1 * D / 4; e += 256) {
+            const int cc = (4 * e) / D, n = (4 * e) % D;
+            const float4 x = s1[e], y = s2p[e];
+            float* d1 = sSp + cc * LDQ + n;
+            float* d2 = sdSt + cc * LDQ + n;
+            d1[0] = x.x; d1[1] = x.y; d1[2] = x.z; d1[3] = x.w;
+            d2[0] = y.x; d2[1] = y.y; d2[2] = y.z; d2[3] = y.w;
+        }
+        __syncthreads();
+        float U[4][NCOL + 1], V[4][NCOL + 1];
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int s2 = 0; s2 <= NCOL; ++s2) U[r][s2] = V[r][s2] = 0.f;
+#pragma unroll 2
+        for (int n = 0; n < D; ++n) {
+            float a1[NCOL + 1], a2[NCOL + 1];
+#pragma unroll
+            for (int s2 = 0; s2 < NCOL; ++s2) {
+                a1[s2] = sSp[(tc + 16 * s2) * LDQ + n];
+                a2[s2] = sdSt[(tc + 16 * s2) * LDQ + n];
+            }
+            a1[NCOL] = sSp[DV * LDQ + n];
+            a2[NCOL] = sdSt[DV * LDQ + n];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const float qv = sq[(ti + 16 * r) * LDQ + n], kv = sk[(ti + 16 * r) * LDQ + n];
+#pragma unroll
+                for (int s2 = 0; s2 <= NCOL; ++s2) {
+                    U[r][s2] = fmaf(qv, a1[s2], U[r][s2]);
+                    V[r][s2] = fmaf(kv, a2[s2], V[r][s2]);
+                }
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int i = ti + 16 * r;
+            float pq = 0.f, pk = 0.f;
+#pragma unroll
+            for (int s2 = 0; s2 < NCOL; ++s2) {
+                pq = fmaf(sdy[i * LDV + tc + 16 * s2], U[r][s2], pq);
+                pk = fmaf(sv[i * LDV + tc + 16 * s2], V[r][s2], pk);
+            }
+            if (tc == 0) {
+                pq = fmaf(sdy[i * LDV + DV], U[r][NCOL], pq);
+                pk = fmaf(sv[i * LDV + DV], V[r][NCOL], pk);
+            }
+#pragma unroll
+            for (int o2 = 8; o2 > 0; o2 >>= 1) {
+                pq += __shfl_xor_sync(0xffffffffu, pq, o2);
+                pk += __shfl_xor_sync(0xffffffffu, pk, o2);
+            }
+            if (tc == 0) {
+                sdqi[i * LDQ + m] = 2.f * seA[i] * pq;
+                sdki[i * LDQ + m] = 2.f * sw[i] * pk;
+            }
+            const float coef = sw[i] * sk[i * LDQ + m];
+#pragma unroll
+            for (int s2 = 0; s2 <= NCOL; ++s2) av[r][s2] = fmaf(coef, V[r][s2], av[r][s2]);
+        }
+    }
+    __syncthreads();
+
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int i = ti + 16 * r;
+        const long t = (long)c * C + i;
+        float vd = 0.f;
+#pragma unroll
+        for (int s2 = 0; s2 < NCOL; ++s2) vd = fmaf(sv[i * LDV + tc + 16 * s2], av[r][s2], vd);
+        if (tc == 0) vd = fmaf(sv[i * LDV + DV], av[r][NCOL], vd);
+#pragma unroll
+        for (int o2 = 8; o2 > 0; o2 >>= 1) vd += __shfl_xor_sync(0xffffffffu, vd, o2);
+        if (t >= T) continue;
+#pragma unroll
+        for (int s2 = 0; s2 < NN; ++s2) {
+            const int n = tc + 16 * s2;
+            dq[(bh * T + t) * D + n] = aq[r][s2] + sdqi[i * LDQ + n];
+            dk[(bh * T + t) * D + n] = ak[r][s2] + sdki[i * LDQ + n];
+        }
+#pragma unroll
+        for (int s2 = 0; s2 < NCOL; ++s2) dvo[(bh * T + t) * DV + tc + 16 * s2] = av[r][s2];
+        if (tc == 0) dcum[bh * T + t] = rowterm[bh * T + t] - vd;
+    }
+}
+
+template <int D, int DV, typename Tin>
+static cudaError_t run_bwd_chunk(const Problem& p, const void* q, const void* k, const void* v,
+                                 const float* Aloc, const float* g, const float* dY,
+                                 const float* rowterm, const float* states, const float* dstates,
+                                 void* dq, void* dk, void* dv, float* dcum, cudaStream_t s) {
+    constexpr int C = SIMT_C, DV1 = DV + 1;
+    const size_t smem = sizeof(float) * (size_t)(2 * C * (D + 1) + 2 * C * (DV1 + 1) + 3 * C +
+                                                 2 * C * (C + 1) + 2 * DV1 * (D + 1) + 2 * C * (D + 1));
+    auto kern = bwd_chunk_kernel<D, DV, Tin>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(p.NC, (unsigned)p.BH());
+    kern<<<grid, 256, smem, s>>>((const Tin*)q, (const Tin*)k, (const Tin*)v, Aloc, g, dY, rowterm,
+                                 states, dstates, (float*)dq, (float*)dk, (float*)dv, dcum, p.T, p.NC);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------------------
+// dispatch on (d = dv, dtype)
+// ------------------------------------------------------------------------------------
+#define TM2_DISPATCH(P, CALL)                                                                    \
+    do {                                                                                         \
+        if ((P).dtype == 1) {                                                                    \
+            typedef __nv_bfloat16 Tin;                                                           \
+            if ((P).d == 64) { constexpr int D = 64; return CALL; }                              \
+            if ((P).d == 32) { constexpr int D = 32; return CALL; }                              \
+            if ((P).d == 16) { constexpr int D = 16; return CALL; }                              \
+        } else {                                                                                 \
+            typedef float Tin;                                                                   \
+            if ((P).d == 64) { constexpr int D = 64; return CALL; }                              \
+            if ((P).d == 32) { constexpr int D = 32; return CALL; }                              \
+            if ((P).d == 16) { constexpr int D = 16; return CALL; }                              \
+        }                                                                                        \
+        return cudaErrorInvalidValue;                                                            \
+    } while (0)
+
+cudaError_t simt_state_scan_fwd(const Problem& p, const void* k, const void* v, const float* Aloc,
+                                const float* g, const float* S0, const float* z0, float* states,
+                                float* S_final, float* z_final, cudaStream_t s) {
+    TM2_DISPATCH(p, (run_state_scan<D, D, Tin, false>(p, k, v, nullptr, Aloc, g, S0, z0, states,
+                                                      S_final, z_final, s)));
+}
+
+cudaError_t simt_chunk_out(const Problem& p, const void* q, const void* k, const void* v,
+                           const float* Aloc, const float* states, void* o, float* Z,
+                           cudaStream_t s) {
+    TM2_DISPATCH(p, (run_chunk_out<D, D, Tin>(p, q, k, v, Aloc, states, o, Z, s)));
+}
+
+cudaError_t simt_state_scan_bwd(const Problem& p, const void* q, const float* dY, const float* Aloc,
+                                const float* g, float* dstates, cudaStream_t s) {
+    TM2_DISPATCH(p, (run_state_scan<D, D, Tin, true>(p, q, nullptr, dY, Aloc, g, nullptr, nullptr,
+                                                     dstates, nullptr, nullptr, s)));
+}
+
+cudaError_t simt_bwd_chunk(const Problem& p, const void* q, const void* k, const void* v,
+                           const float* Aloc, const float* g, const float* dY,
+                           const float* rowterm, const float* states, const float* dstates,
+                           void* dq, void* dk, void* dv, float* dcum, cudaStream_t s) {
+    TM2_DISPATCH(p, (run_bwd_chunk<D, D, Tin>(p, q, k, v, Aloc, g, dY, rowterm, states, dstates, dq,
+                                              dk, dv, dcum, s)));
+}
+
+}  // namespace tm2

@@ -1,0 +1,102 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol the header
+declares, and rejects bad arguments on the host before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import ssm_sequence_mixer_chunked_b300 as tm2
+from ssm_sequence_mixer_chunked_b300 import build as tm2_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tm2.h")
+
+OK, INVALID, UNSUPPORTED, ALIGNMENT, WORKSPACE = 0, -1, -2, -3, -4
+FAKE = 0x10000000  # a 256-byte aligned address that is never dereferenced (rejected first)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    tm2_build.build()
+    return tm2.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(tm2e?_[a-z_]+)\s*\(", src)))
+
+
+def test_header_symbols_exported(lib):
+    names = declared_functions()
+    assert {"tm2_forward", "tm2_backward", "tm2_step", "tm2e_forward", "tm2e_backward"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_version_and_status_strings(lib):
+    assert lib.tm2_version() >= 100
+    for st in (OK, INVALID, UNSUPPORTED, ALIGNMENT, WORKSPACE, -5, -6, 12345):
+        s = tm2.status_string(st)
+        assert s.startswith("TM2")
+
+
+def test_workspace_sizes(lib):
+    bf16 = 1
+    w = lib.tm2_forward_workspace(2, 16, 8192, 64, 64, 0, bf16, 1)
+    # states entering each of 128 chunks: 64 * 65 * 64 fp32 per (b, h, chunk)
+    assert w >= 2 * 16 * 128 * 64 * 65 * 64 * 4
+    assert lib.tm2_backward_workspace(2, 16, 8192, 64, 64, 0, bf16, 1) > w
+    assert lib.tm2_forward_workspace(2, 16, 8192, 48, 48, 0, bf16, 1) == 0      # unsupported -> 0
+    assert lib.tm2_forward_workspace(2, 16, 0, 64, 64, 0, bf16, 1) % 256 == 0
+    assert lib.tm2e_forward_workspace(2, 16, 4096, 64, 64, bf16) > 0
+
+
+def fwd(lib, q=FAKE, k=FAKE, v=FAKE, a=FAKE, o=FAKE, Z=FAKE, B=1, H=2, T=256, d=16, dv=16,
+        chunk=64, dtype=0, flags=1, ws=FAKE, ws_bytes=1 << 40):
+    P = lambda x: None if x is None else ctypes.c_void_p(x)
+    return lib.tm2_forward(P(q), P(k), P(v), P(a), None, None, P(o), P(Z), None, None, B, H, T, d,
+                           dv, chunk, dtype, flags, P(ws), ws_bytes, None)
+
+
+def test_forward_rejects_bad_arguments(lib):
+    assert fwd(lib, B=-1) == INVALID
+    assert fwd(lib, q=None) == INVALID
+    assert fwd(lib, flags=8) == INVALID
+    assert fwd(lib, d=48, dv=48) == UNSUPPORTED
+    assert fwd(lib, d=64, dv=32) == UNSUPPORTED
+    assert fwd(lib, chunk=48) == UNSUPPORTED
+    assert fwd(lib, dtype=7) == UNSUPPORTED
+    assert fwd(lib, k=FAKE + 4) == ALIGNMENT
+    assert fwd(lib, ws=None) == WORKSPACE
+    assert fwd(lib, ws_bytes=16) == WORKSPACE
+    assert fwd(lib, ws=FAKE + 16) == ALIGNMENT
+
+
+def test_step_and_e_reject_bad_arguments(lib):
+    P = ctypes.c_void_p
+    f = P(FAKE)
+    assert lib.tm2_step(f, f, f, f, f, None, f, None, 4, 2, 64, 64, 0, 1, None) == INVALID  # normalise needs z
+    assert lib.tm2_step(f, f, f, f, f, f, f, f, 4, 2, 40, 40, 0, 1, None) == UNSUPPORTED
+    assert lib.tm2_step(f, f, f, P(FAKE + 8), f, f, f, f, 4, 2, 64, 64, 0, 1, None) == ALIGNMENT
+    assert lib.tm2e_forward(f, f, f, f, f, f, 1, 1, 128, 64, 64, ctypes.c_float(0.0), 1, f, 1 << 30,
+                            None) == INVALID
+    assert lib.tm2e_forward(f, f, f, f, f, None, 1, 1, 128, 64, 64, ctypes.c_float(0.125), 1, f,
+                            1 << 30, None) == INVALID
+    assert lib.tm2e_backward(f, f, f, f, f, f, f, f, f, f, f, 1, 1, 128, 64, 64, ctypes.c_float(0.125),
+                             1, f, 8, None) == WORKSPACE
+
+
+def test_backward_needs_Z_when_normalised(lib):
+    P = ctypes.c_void_p
+    f = P(FAKE)
+    st = lib.tm2_backward(f, f, f, f, f, None, f, f, f, f, f, 1, 1, 128, 64, 64, 0, 1, 1, f, 1 << 40, None)
+    assert st == INVALID
+
+
+def test_binding_fails_loudly_without_cuda_tensors():
+    import torch
+    x = torch.zeros(1, 1, 4, 16)
+    with pytest.raises(tm2.TM2Error):
+        tm2.forward(x, x, x, torch.zeros(1, 1, 4))
