@@ -135,6 +135,28 @@ int tm2e_forward(const void* q, const void* k, const void* v, const float* a,
                  int B, int H, int T, int d, int dv, float scale, int dtype,
                  void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * tm2e_forward_noalloc -- the paper has no counterpart to this entry point; it exists
+ * for callers that cannot allocate device memory (for example a plugin hosted by an
+ * inference engine that owns and pre-plans all device memory, or a latency-critical
+ * loop that must not risk cudaMalloc's implicit synchronisation).
+ * It computes exactly what tm2e_forward computes, with the same arguments minus the
+ * workspace: its scratch is a fixed array of TM2E_NOALLOC_SCRATCH_BYTES compiled into
+ * the library, held by every GPU that loads the library until the process exits.
+ *  - Scratch need is about 8 * B*H*T bytes; larger problems return TM2_ERR_WORKSPACE
+ *    before anything is launched (B*H*T up to roughly 2 million token-heads fits).
+ *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress,
+ *    with that device current); make that first call before any stream capture.
+ *  - No cudaMalloc, cudaFree or other allocating routine is called.
+ *  - All calls on a device share the array and every call overwrites what it reads, so
+ *    nothing needs clearing; calls that overlap on the GPU race on it and must be
+ *    serialised by the caller.
+ */
+#define TM2E_NOALLOC_SCRATCH_BYTES (16u << 20)
+int tm2e_forward_noalloc(const void* q, const void* k, const void* v, const float* a,
+                         void* o, float* lse,
+                         int B, int H, int T, int d, int dv, float scale, int dtype, void* stream);
+
 size_t tm2e_backward_workspace(int B, int H, int T, int d, int dv, int dtype);
 
 /*

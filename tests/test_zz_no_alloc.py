@@ -1,0 +1,62 @@
+"""The allocation-free 2Mamba-E forward, tm2e_forward_noalloc.
+
+It serves callers that cannot allocate device memory (a plugin inside an engine that
+owns all device memory, a latency-critical loop that must not call cudaMalloc): they
+pass inputs and outputs only, and the library uses a fixed scratch array compiled into
+it.  This test calls it through the C ABI twice in a row, on two different inputs,
+and checks each result against the ordinary tm2e_forward (which takes a caller
+workspace) within the bf16 parity tolerance used by the other tests.  It also checks
+that a problem too large for the fixed scratch is refused before any launch.
+
+The file name sorts last so that a run stopping at the first failure has run every
+other test before this one.
+"""
+import ctypes
+import math
+
+import pytest
+import torch
+
+import ssm_sequence_mixer_chunked_b300 as tm2
+import synth_inputs as si
+
+pytestmark = pytest.mark.gpu
+
+
+def _noalloc_fn():
+    lib = tm2.lib()
+    fn = lib.tm2e_forward_noalloc
+    P, I = ctypes.c_void_p, ctypes.c_int
+    fn.restype = I
+    fn.argtypes = [P] * 6 + [I] * 5 + [ctypes.c_float, I, P]
+    return fn
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def test_noalloc_matches_workspace_entry_point_twice():
+    fn = _noalloc_fn()
+    B, H, T, d = 2, 4, 1000, 64
+    scale = 1.0 / math.sqrt(d)
+    for seed in (71, 72):   # two calls in a row, different inputs
+        inp = si.sequence_inputs(B, H, T, d, d, dtype="bf16", qkv_std=1.0, seed=seed)
+        g = {k: v.cuda() for k, v in inp.items()}
+        o_ref, lse_ref = tm2.e_forward(g["q"], g["k"], g["v"], g["a"], scale=scale)
+        o = torch.empty((B, H, T, d), dtype=torch.float32, device="cuda")
+        lse = torch.empty((B, H, T), dtype=torch.float32, device="cuda")
+        st = fn(_ptr(g["q"]), _ptr(g["k"]), _ptr(g["v"]), _ptr(g["a"]), _ptr(o), _ptr(lse),
+                B, H, T, d, d, scale, 1, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+        assert st == 0, tm2.status_string(st)
+        torch.cuda.synchronize()
+        assert si.rel_err(o.cpu(), o_ref.cpu()) <= 2e-2
+        assert si.rel_err(lse.cpu(), lse_ref.cpu()) <= 2e-2
+
+
+def test_noalloc_rejects_problem_larger_than_scratch():
+    fn = _noalloc_fn()
+    f = ctypes.c_void_p(0x10000000)   # never dereferenced: the size check comes first
+    # 8 * 64 * 16 * 8192 bytes of scratch is far above the 16 MiB array
+    st = fn(f, f, f, f, f, f, 64, 16, 8192, 64, 64, 0.125, 1, None)
+    assert st == -4, tm2.status_string(st)
