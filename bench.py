@@ -480,6 +480,35 @@ def run_e_variant(args, tm2, device, trace, world):
             "gpu_launches": len(recs)}
 
 
+def run_case(name):
+    """Small fixed cases for profiler captures (few launches, a few GB at most on the
+    device, working sets above the 126 MB L2).  Prints a one-line summary."""
+    import ssm_sequence_mixer_chunked_b300 as tm2
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    if name == "decode_small":          # 32 sequences x 16 heads: 545 MB of state
+        N, H, d = 32, 16, 64
+        S, z = si.decode_initial_state(N, H, d, d, S0_std=0.01)
+        S, z = S.to(dev), z.to(dev)
+        x = {k: v.to(dev) for k, v in si.decode_token(0, N, H, d, d, qkv_std=0.125).items()}
+        for _ in range(3):
+            tm2.step(x["q"], x["k"], x["v"], x["a"], S, z)
+    elif name == "fwdbwd_small":        # B=1, H=4, T=8192: chunk states well above L2
+        inp = si.sequence_inputs(1, 4, 8192, 64, 64, dtype="bf16", qkv_std=0.125, seed=3, with_dO=True)
+        g = {k: v.to(dev) for k, v in inp.items()}
+        o, Z = tm2.forward(g["q"], g["k"], g["v"], g["a"])
+        tm2.backward(g["q"], g["k"], g["v"], g["a"], o, Z, g["dO"])
+    elif name == "e_small":             # 2Mamba-E, B=1, H=4, T=4096
+        inp = si.sequence_inputs(1, 4, 4096, 64, 64, dtype="bf16", qkv_std=1.0, seed=5, with_dO=True)
+        g = {k: v.to(dev) for k, v in inp.items()}
+        o, lse = tm2.e_forward(g["q"], g["k"], g["v"], g["a"])
+        tm2.e_backward(g["q"], g["k"], g["v"], g["a"], o, lse, g["dO"])
+    else:
+        raise SystemExit("unknown case " + name)
+    torch.cuda.synchronize()
+    print("case %s ok" % name)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -490,7 +519,10 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--case", default=None, help="run one small profiling case and exit")
     args = ap.parse_args()
+    if args.case:
+        return run_case(args.case)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

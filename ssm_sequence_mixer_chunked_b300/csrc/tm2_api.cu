@@ -10,10 +10,9 @@
 #include "tm2.h"
 #include "tm2_common.cuh"
 #include "tm2_launch.h"
+#include "tm2_tc.h"
 
 namespace tm2 {
-
-__device__ int g_status = 0;
 
 struct Carve {
     size_t off = 0;
@@ -349,12 +348,6 @@ int tm2_trace_read(int i, char* name, int name_len, float* ms) {
     return TM2_OK;
 }
 
-int tm2_poll_status(void) {
-    int h = 0, zero = 0;
-    if (cudaMemcpyFromSymbol(&h, tm2::g_status, sizeof(int)) != cudaSuccess) return TM2_ERR_CUDA;
-    if (h != 0 && cudaMemcpyToSymbol(tm2::g_status, &zero, sizeof(int)) != cudaSuccess)
-        return TM2_ERR_CUDA;
-    return h;
-}
+int tm2_poll_status(void) { return tm2::read_tc_status(true); }
 
 }  // extern "C"

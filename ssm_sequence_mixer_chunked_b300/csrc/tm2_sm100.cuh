@@ -27,9 +27,6 @@
 
 namespace tm2 {
 
-// Status word of the current device (defined in tm2_tc.cu).
-extern __device__ int g_tc_status;
-
 TM2_DEV uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
 TM2_DEV uint64_t globaltimer_ns() {
@@ -61,14 +58,15 @@ TM2_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 // Waits for the phase with the given parity to complete; gives up after `limit_ns`
-// nanoseconds, records TM2_ERR_TIMEOUT (-6) and returns false.
-TM2_DEV bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = 2000000000ull) {
+// nanoseconds, records TM2_ERR_TIMEOUT (-6) in *status (the device status word whose
+// address the host passes to every tensor-core kernel) and returns false.
+TM2_DEV bool mbar_wait(uint32_t bar, uint32_t parity, int* status, uint64_t limit_ns = 2000000000ull) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (globaltimer_ns() - t0 > limit_ns) {
-            atomicExch(&g_tc_status, -6);
+            atomicExch(status, -6);
             return false;
         }
     }
@@ -129,18 +127,21 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// 32 lanes x 16 consecutive 32-bit columns -> 16 registers per thread.
+// 32 lanes x 16 consecutive 32-bit columns -> 16 registers per thread.  The load and
+// its wait sit in one asm statement so no use of the registers can be scheduled
+// before the data has arrived.
 TM2_DEV void tmem_ld16(uint32_t taddr, float* v) {
     uint32_t r[16];
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+        "tcgen05.wait::ld.sync.aligned;"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
+        : "r"(taddr)
+        : "memory");
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
-TM2_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // byte offset of (row, 16-byte chunk) inside a 128B-swizzled K-major tile
 TM2_DEV uint32_t swz128(uint32_t row, uint32_t chunk) { return row * 128u + ((chunk ^ (row & 7u)) << 4); }

@@ -1,0 +1,21 @@
+// tm2_tc.h -- host helpers of the tensor-core kernels (internal to the library).
+#pragma once
+
+#include <cuda.h>
+#include <stdint.h>
+
+namespace tm2 {
+
+// 2-D bf16 TMA descriptor over a row-major [rows][cols] matrix (row pitch in elements),
+// box of box_rows x 64 columns, 128-byte swizzle, zero fill outside the matrix.
+bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                       uint64_t pitch_elems, uint32_t box_rows);
+
+// Reads (and optionally clears) the device status word of the current device.
+int read_tc_status(bool clear);
+
+// Device address of the status word on the current device (looked up once per device);
+// nullptr on failure.
+int* tc_status_ptr();
+
+}  // namespace tm2
