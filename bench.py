@@ -179,28 +179,25 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- helpers
-def source_sha():
-    h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "ssm_sequence_mixer_chunked_b300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode())
-            h.update(fh.read())
-    return h.hexdigest()[:16]
+def file_sha(name):
+    path = os.path.join(ROOT, "ssm_sequence_mixer_chunked_b300", "csrc", name)
+    with open(path, "rb") as fh:
+        return hashlib.sha256(fh.read()).hexdigest()[:16]
 
 
-def ncu_traffic(kernel, tokens_per_launch):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it was taken
-    on the current kernel sources; else None."""
+def ncu_traffic(kernel, units_per_launch):
+    """DRAM bytes (read + write) per launch of `kernel`, scaled from the committed ncu
+    capture (profiles/ncu_traffic.json) by the units the launch processes -- or None when
+    there is no capture or the kernel's source file changed since it was taken."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f).get(kernel)
-    except (OSError, ValueError):
+        if not rec or rec.get("file_sha") != file_sha(rec["file"]):
+            return None
+    except (OSError, ValueError, KeyError):
         return None
-    if not rec or rec.get("source_sha") != source_sha():
-        return None
-    return rec["dram_bytes_per_token_head"] * tokens_per_launch
+    return rec["dram_bytes_per_unit"] * units_per_launch
 
 
 def setup_dist():
