@@ -178,14 +178,18 @@ int tm2_poll_status(void);
 
 /*
  * Self-test of the tensor-core building blocks (diagnostic; not part of the method).
- * D (128 x N, fp32) = A (128 x K, bf16, row-major) * B (N x K, bf16, row-major)^T through
- * TMA loads with 128-byte swizzle, tcgen05.mma (kind::f16) into tensor memory and
- * tcgen05.ld, i.e. the operand and accumulator conventions every tensor-core kernel of
- * the library relies on.  N in {16, 64, 80, 128, 256}; K a multiple of 64, <= 512.
- * mode 0: both operands loaded by TMA; mode 1: A written by the threads in the swizzled
- * layout; mode 2: one thread waits on a barrier that is never signalled, so the bounded
- * wait expires after wait_ns nanoseconds, TM2_ERR_TIMEOUT is recorded in the status word
- * (tm2_poll_status) and the kernel exits cleanly without touching D.
+ * D (128 x N, fp32) = A (128 x K, bf16, row-major) * B^T through tcgen05.mma (kind::f16)
+ * into tensor memory and tcgen05.ld, i.e. the operand and accumulator conventions every
+ * tensor-core kernel of the library relies on.  N in {16, 64, 80, 128, 256}; K a multiple
+ * of 64, <= 512 (<= 256 with an MN-major B).  Operand forms by mode:
+ *   0: A and B (N x K, row-major) loaded by TMA with 128-byte swizzle (K-major);
+ *   1: A written by the threads into shared memory in the swizzled layout, B as in 0;
+ *   2: one thread waits on a barrier that is never signalled, so the bounded wait expires
+ *      after wait_ns nanoseconds, TM2_ERR_TIMEOUT is recorded in the status word
+ *      (tm2_poll_status) and the kernel exits cleanly without touching D;
+ *   3: A written by the threads into tensor memory (tcgen05.st), B as in 0;
+ *   4: A as in 0, B given transposed (K x N, row-major) and consumed MN-major;
+ *   5: A in tensor memory as in 3, B MN-major as in 4.
  */
 int tm2_selftest_umma(const void* A, const void* B, float* D, int N, int K, int mode,
                       unsigned long long wait_ns, void* stream);

@@ -11,6 +11,12 @@ namespace tm2 {
 bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                        uint64_t pitch_elems, uint32_t box_rows);
 
+// 3-D bf16 TMA descriptor over a dense [heads][rows][cols] tensor (cols a multiple of 8),
+// box of 1 head x box_rows rows x 64 columns, 128-byte swizzle; rows past the end of a head
+// read as zero.
+bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t heads, uint64_t rows, uint64_t cols,
+                       uint32_t box_rows);
+
 // Reads (and optionally clears) the device status word of the current device.
 int read_tc_status(bool clear);
 

@@ -12,6 +12,9 @@ import ssm_sequence_mixer_chunked_b300 as tm2
 pytestmark = pytest.mark.gpu
 
 
+MN_MAJOR_B = (4, 5)   # modes whose B operand is given as B^T (K x N, row-major)
+
+
 def selftest(A, B, N, K, mode, wait_ns=0):
     lib = tm2.lib()
     fn = lib.tm2_selftest_umma
@@ -24,13 +27,17 @@ def selftest(A, B, N, K, mode, wait_ns=0):
     return st, D
 
 
-@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("mode", [0, 1, 3, 4, 5])
 @pytest.mark.parametrize("N,K", [(16, 64), (64, 64), (64, 256), (80, 128), (128, 192), (256, 128)])
 def test_umma_matches_matmul(mode, N, K):
+    """Modes: 0 A and B by TMA; 1 A written by the threads into shared memory; 3 A in
+    tensor memory; 4 B MN-major (B^T row-major in memory); 5 A in tensor memory and B
+    MN-major."""
     g = torch.Generator(device="cpu").manual_seed(N * 1000 + K + mode)
     A = torch.randn(128, K, generator=g).to(torch.bfloat16).cuda()
     B = torch.randn(N, K, generator=g).to(torch.bfloat16).cuda()
-    st, D = selftest(A, B, N, K, mode)
+    Bin = B.T.contiguous() if mode in MN_MAJOR_B else B
+    st, D = selftest(A, Bin, N, K, mode)
     assert st == 0, tm2.status_string(st)
     ref = A.double() @ B.double().T
     err = (D.double() - ref).abs().max().item() / ref.pow(2).mean().sqrt().item()
