@@ -26,16 +26,22 @@ struct Carve {
 static bool aligned16(const void* p) { return p == nullptr || ((uintptr_t)p & 15u) == 0; }
 
 // Validates the shape arguments shared by the sequence entry points and fills p.
+// chunk 64 selects the fp32-arithmetic CUDA-core path, chunk TC_CHUNK the bf16 tensor-core
+// path (bf16 inputs, d = dv = 64, and only where `tc_available`); chunk 0 picks the
+// tensor-core path whenever it applies.
 static int make_problem(int B, int H, int T, int d, int dv, int chunk, int dtype, unsigned flags,
-                        Problem& p) {
+                        Problem& p, bool tc_available = false) {
     if (B < 0 || H < 0 || T < 0 || d <= 0 || dv <= 0) return TM2_ERR_INVALID_ARG;
     if (dtype != TM2_F32 && dtype != TM2_BF16) return TM2_ERR_UNSUPPORTED;
     if (d != dv || (d != 16 && d != 32 && d != 64)) return TM2_ERR_UNSUPPORTED;
-    if (chunk != 0 && chunk != 64) return TM2_ERR_UNSUPPORTED;
+    if (chunk != 0 && chunk != 64 && chunk != TC_CHUNK) return TM2_ERR_UNSUPPORTED;
     if ((long)B * H > 65535) return TM2_ERR_UNSUPPORTED;
     if (flags & ~TM2_NORMALIZE) return TM2_ERR_INVALID_ARG;
+    const bool tc_ok = tc_available && dtype == TM2_BF16 && d == 64 && dv == 64;
+    if (chunk == TC_CHUNK && !tc_ok) return TM2_ERR_UNSUPPORTED;
     p.B = B; p.H = H; p.T = T; p.d = d; p.dv = dv;
-    p.C = 64;
+    p.tc = tc_ok && chunk != 64;
+    p.C = p.tc ? TC_CHUNK : 64;
     p.NC = (T + p.C - 1) / p.C;
     p.dtype = dtype;
     p.normalize = (flags & TM2_NORMALIZE) != 0;
@@ -44,23 +50,43 @@ static int make_problem(int B, int H, int T, int d, int dv, int chunk, int dtype
 
 static size_t state_floats(const Problem& p) { return (size_t)p.d * (p.dv + 1) * p.d; }
 
-struct FwdWs { size_t Aloc, g, states, total; };
+struct FwdWs { size_t Aloc, g, states, zx, total; };
 static FwdWs plan_fwd(const Problem& p) {
     Carve c;
-    FwdWs w;
+    FwdWs w{};
     w.Aloc = c.take(sizeof(float) * p.BH() * p.Tp());
     w.g = c.take(sizeof(float) * p.BH() * p.NC);
-    w.states = c.take(sizeof(float) * p.BH() * p.NC * state_floats(p));
+    if (p.tc) {   // fp16 value states [BH][NC][2][4096][64] + fp32 normaliser states [BH][NC][4096]
+        w.states = c.take(2 * 2 * (size_t)p.BH() * p.NC * 4096 * 64);
+        w.zx = c.take(sizeof(float) * (size_t)p.BH() * p.NC * 4096);
+    } else {
+        w.states = c.take(sizeof(float) * p.BH() * p.NC * state_floats(p));
+    }
     w.total = c.off;
     return w;
 }
 
-struct BwdWs { size_t Aloc, g, states, dstates, dY, rowterm, dcum, total; };
+struct BwdWs { size_t Aloc, g, states, dstates, dY, rowterm, dcum, zx, dzx, sscale, zeta, ucol, zmax, total; };
 static BwdWs plan_bwd(const Problem& p) {
     Carve c;
-    BwdWs w;
+    BwdWs w{};
     w.Aloc = c.take(sizeof(float) * p.BH() * p.Tp());
     w.g = c.take(sizeof(float) * p.BH() * p.NC);
+    if (p.tc) {
+        const size_t planes = 2 * 2 * (size_t)p.BH() * p.NC * 4096 * 64;   // two fp16 planes per slot
+        w.states = c.take(planes);
+        w.dstates = c.take(planes);
+        w.zx = c.take(sizeof(float) * (size_t)p.BH() * p.NC * 4096);
+        w.dzx = c.take(sizeof(float) * (size_t)p.BH() * p.NC * 4096);
+        w.sscale = c.take(sizeof(float) * (size_t)p.BH() * p.NC);
+        w.zmax = c.take(sizeof(float) * (size_t)p.BH() * p.NC);
+        w.zeta = c.take(sizeof(float) * p.BH() * p.T);
+        w.ucol = c.take(sizeof(float) * p.BH() * p.T);
+        w.rowterm = c.take(sizeof(float) * p.BH() * p.T);
+        w.dcum = c.take(sizeof(float) * p.BH() * p.T);
+        w.total = c.off;
+        return w;
+    }
     w.states = c.take(sizeof(float) * p.BH() * p.NC * state_floats(p));
     w.dstates = c.take(sizeof(float) * p.BH() * p.NC * state_floats(p));
     w.dY = c.take(sizeof(float) * p.BH() * p.T * (p.dv + 1));
@@ -161,7 +187,7 @@ const char* tm2_status_string(int status) {
 size_t tm2_forward_workspace(int B, int H, int T, int d, int dv, int chunk, int dtype,
                              unsigned flags) {
     Problem p;
-    if (make_problem(B, H, T, d, dv, chunk, dtype, flags, p) != TM2_OK) return 0;
+    if (make_problem(B, H, T, d, dv, chunk, dtype, flags, p, true) != TM2_OK) return 0;
     return plan_fwd(p).total;
 }
 
@@ -170,7 +196,7 @@ int tm2_forward(const void* q, const void* k, const void* v, const float* a, con
                 int T, int d, int dv, int chunk, int dtype, unsigned flags, void* ws,
                 size_t ws_bytes, void* stream) {
     Problem p;
-    int st = make_problem(B, H, T, d, dv, chunk, dtype, flags, p);
+    int st = make_problem(B, H, T, d, dv, chunk, dtype, flags, p, true);
     if (st != TM2_OK) return st;
     const bool work = p.BH() > 0 && T > 0;
     if (work && (!q || !k || !v || !a || !o)) return TM2_ERR_INVALID_ARG;
@@ -194,6 +220,15 @@ int tm2_forward(const void* q, const void* k, const void* v, const float* a, con
     float* g = at<float>(ws, w.g);
     float* states = at<float>(ws, w.states);
     TM2_RUN("decay_chunk", launch_decay(p, a, Aloc, g, s));
+    if (p.tc) {
+        float* zx = at<float>(ws, w.zx);
+        ScanIO io{};
+        io.rev = false; io.key = k; io.val = v; io.Aloc = Aloc; io.g = g; io.S0 = S0; io.z0 = z0;
+        io.Sx = states; io.zx = zx; io.S_final = S_final; io.z_final = z_final;
+        TM2_RUN("tc_state_scan_fwd", tc_state_scan(p, io, s));
+        TM2_RUN("tc_chunk_out", tc_chunk_out(p, q, k, v, Aloc, states, zx, (float*)o, Z, s));
+        return TM2_OK;
+    }
     TM2_RUN("state_scan_fwd", simt_state_scan_fwd(p, k, v, Aloc, g, S0, z0, states, S_final, z_final, s));
     TM2_RUN("chunk_out", simt_chunk_out(p, q, k, v, Aloc, states, o, Z, s));
     return TM2_OK;
@@ -202,7 +237,7 @@ int tm2_forward(const void* q, const void* k, const void* v, const float* a, con
 size_t tm2_backward_workspace(int B, int H, int T, int d, int dv, int chunk, int dtype,
                               unsigned flags) {
     Problem p;
-    if (make_problem(B, H, T, d, dv, chunk, dtype, flags, p) != TM2_OK) return 0;
+    if (make_problem(B, H, T, d, dv, chunk, dtype, flags, p, true) != TM2_OK) return 0;
     return plan_bwd(p).total;
 }
 
@@ -211,7 +246,7 @@ int tm2_backward(const void* q, const void* k, const void* v, const float* a, co
                  int H, int T, int d, int dv_dim, int chunk, int dtype, unsigned flags, void* ws,
                  size_t ws_bytes, void* stream) {
     Problem p;
-    int st = make_problem(B, H, T, d, dv_dim, chunk, dtype, flags, p);
+    int st = make_problem(B, H, T, d, dv_dim, chunk, dtype, flags, p, true);
     if (st != TM2_OK) return st;
     if (p.BH() == 0 || T == 0) return TM2_OK;
     if (!q || !k || !v || !a || !o || !dO || !dq || !dk || !dv || !da) return TM2_ERR_INVALID_ARG;
@@ -225,6 +260,32 @@ int tm2_backward(const void* q, const void* k, const void* v, const float* a, co
     cudaStream_t s = (cudaStream_t)stream;
     float* Aloc = at<float>(ws, w.Aloc);
     float* g = at<float>(ws, w.g);
+    if (p.tc) {
+        void* Sx = at<void>(ws, w.states);
+        void* dSx = at<void>(ws, w.dstates);
+        float* zx = at<float>(ws, w.zx);
+        float* dzx = at<float>(ws, w.dzx);
+        float* sscale = at<float>(ws, w.sscale);
+        float* zmax = at<float>(ws, w.zmax);
+        float* zeta = at<float>(ws, w.zeta);
+        float* ucol = at<float>(ws, w.ucol);
+        float* rowterm = at<float>(ws, w.rowterm);
+        float* dcum = at<float>(ws, w.dcum);
+        TM2_RUN("decay_chunk", launch_decay(p, a, Aloc, g, s));
+        ScanIO f{};
+        f.rev = false; f.key = k; f.val = v; f.Aloc = Aloc; f.g = g; f.Sx = Sx; f.zx = zx;
+        TM2_RUN("tc_state_scan_fwd", tc_state_scan(p, f, s));
+        TM2_RUN("tc_dy_prep", launch_tc_dy_prep(p, (const float*)o, Z, dO, Aloc, zeta, ucol, rowterm, zmax, s));
+        ScanIO r{};
+        r.rev = true; r.key = q; r.val = dO; r.Aloc = Aloc; r.g = g; r.zeta = zeta; r.ucol = ucol; r.zmax = zmax;
+        r.Sx = dSx; r.zx = dzx; r.sscale = sscale;
+        TM2_RUN("tc_state_scan_bwd", tc_state_scan(p, r, s));
+        TM2_RUN("tc_bwd_dq", tc_bwd_dq(p, q, k, v, dO, Aloc, zeta, ucol, Sx, zx, (float*)dq, s));
+        TM2_RUN("tc_bwd_dkdv", tc_bwd_dkdv(p, q, k, v, dO, Aloc, g, zeta, ucol, rowterm, dSx, dzx, sscale, (float*)dk,
+                                           (float*)dv, dcum, s));
+        TM2_RUN("reverse_cumsum_da", launch_reverse_cumsum_da(p, a, dcum, nullptr, da, s));
+        return TM2_OK;
+    }
     float* states = at<float>(ws, w.states);
     float* dstates = at<float>(ws, w.dstates);
     float* dY = at<float>(ws, w.dY);

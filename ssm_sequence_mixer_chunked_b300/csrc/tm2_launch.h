@@ -12,6 +12,7 @@ struct Problem {
     int NC;                  // number of chunks = ceil(T / C)
     int dtype;               // 0 fp32, 1 bf16
     bool normalize;
+    bool tc;                 // bf16 tensor-core path (d = dv = 64, C = TC_CHUNK)
     long BH() const { return (long)B * H; }
     long Tp() const { return (long)NC * C; }   // padded sequence stride of chunk-local buffers
 };
@@ -45,6 +46,52 @@ cudaError_t simt_bwd_chunk(const Problem& p, const void* q, const void* k, const
                            const float* Aloc, const float* g, const float* dY,
                            const float* rowterm, const float* states, const float* dstates,
                            void* dq, void* dk, void* dv, float* dcum, cudaStream_t s);
+
+// ---- bf16 tensor-core path (d = dv = 64, chunk TC_CHUNK) ------------------------------
+constexpr int TC_CHUNK = 256;
+// Chunk-state scan (tm2_tc_scan.cu).  Forward (rev = false): key = k, val = v, normaliser
+// column 1, weight exp(g_c - A_j); slot c = the state entering chunk c (slot 0 = S0/z0 or
+// zero); S_final/z_final (optional) = the state after the last token.  Reverse (rev = true):
+// key = q, val = dO, normaliser column ucol, weight exp(A_i) zeta_i; slot c = the gradient
+// w.r.t. the state at the end of chunk c, scaled per (slot, CTA) by 1/sscale.
+// Sx: [BH][NC][2][4096][64] fp16 (hi plane, residual plane); zx: [BH][NC][4096] fp32.
+struct ScanIO {
+    bool rev;
+    const void* key;
+    const void* val;
+    const float* Aloc;
+    const float* g;
+    const float* zeta;     // reverse only
+    const float* ucol;     // reverse only
+    const float* zmax;     // reverse only
+    const float* S0;       // forward only, optional
+    const float* z0;       // forward only, optional
+    void* Sx;
+    float* zx;
+    float* sscale;         // reverse only: [BH][NC] scale of each exported slot
+    float* S_final;        // forward only, optional
+    float* z_final;        // forward only, optional
+};
+cudaError_t tc_state_scan(const Problem& p, const ScanIO& io, cudaStream_t s);
+
+// Backward preparation: zeta = 1/Z (or 1), ucol = -dO.o (or 0), rowterm = 0 (or dO.o),
+// all (BH,T) fp32, and zmax (BH,NC) = per-chunk max of exp(A_i) zeta_i.
+cudaError_t launch_tc_dy_prep(const Problem& p, const float* o, const float* Z, const void* dO, const float* Aloc,
+                              float* zeta, float* ucol, float* rowterm, float* zmax, cudaStream_t s);
+
+// Gradient kernels (tm2_tc_bwd.cu).  dq: Sx/zx are the forward scan's states; dk, dv, dcum:
+// dSx/dzx/sscale the reverse scan's.  All outputs (BH,T,·) fp32.
+cudaError_t tc_bwd_dq(const Problem& p, const void* q, const void* k, const void* v, const void* dO, const float* Aloc,
+                      const float* zeta, const float* ucol, const void* Sx, const float* zx, float* dq, cudaStream_t s);
+cudaError_t tc_bwd_dkdv(const Problem& p, const void* q, const void* k, const void* v, const void* dO,
+                        const float* Aloc, const float* g, const float* zeta, const float* ucol, const float* rowterm,
+                        const void* dSx, const float* dzx, const float* sscale, float* dk, float* dv, float* dcum,
+                        cudaStream_t s);
+
+// Per-chunk output (intra-chunk squared masked scores and the readout of the state
+// entering the chunk, slot c of Sx/zx from tc_state_scan): o (BH,T,64) fp32, Z optional.
+cudaError_t tc_chunk_out(const Problem& p, const void* q, const void* k, const void* v, const float* Aloc,
+                         const void* Sx, const float* zx, float* o, float* Z, cudaStream_t s);
 
 // ---- decode --------------------------------------------------------------------------
 cudaError_t launch_decode_step(int N, int H, int d, int dv, int dtype, bool normalize,

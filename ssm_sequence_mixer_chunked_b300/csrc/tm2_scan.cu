@@ -136,6 +136,54 @@ cudaError_t launch_dy_prep(const Problem& p, const void* o, const float* Z, cons
     return cudaGetLastError();
 }
 
+// Tensor-core backward preparation.  One block of 256 threads per (chunk, b, h), one warp
+// per token at a time.  With D = dO . o:
+//   zeta = 1/Z (normalised) or 1, ucol = -D (normalised) or 0, rowterm = 0 (normalised)
+//   or D, so that dL/dY_i = zeta_i [dO_i, ucol_i];  zmax[c] = max over the chunk of
+//   exp(A_i) zeta_i (the scale of the reverse state scan's generated operand).
+__global__ void __launch_bounds__(256) tc_dy_prep_kernel(const float* __restrict__ o, const float* __restrict__ Z,
+                                                         const __nv_bfloat16* __restrict__ dO,
+                                                         const float* __restrict__ Aloc, float* __restrict__ zeta,
+                                                         float* __restrict__ ucol, float* __restrict__ rowterm,
+                                                         float* __restrict__ zmax, int T, int C, int NC,
+                                                         bool normalize) {
+    __shared__ float wmax[8];
+    const int c = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long bh = blockIdx.y;
+    float mx = 0.f;
+    for (int jj = warp; jj < C; jj += 8) {
+        const long t = (long)c * C + jj;
+        if (t >= T) break;
+        const long tok = bh * T + t;
+        float D = 0.f;
+        for (int cc = lane; cc < 64; cc += 32) D += __bfloat162float(dO[tok * 64 + cc]) * o[tok * 64 + cc];
+        D = warp_sum(D);
+        const float z = normalize ? Z[tok] : 1.f;
+        const float ze = normalize ? (z != 0.f ? 1.f / z : 0.f) : 1.f;
+        if (lane == 0) {
+            zeta[tok] = ze;
+            ucol[tok] = normalize ? -D : 0.f;
+            rowterm[tok] = normalize ? 0.f : D;
+        }
+        mx = fmaxf(mx, __expf(Aloc[bh * (long)NC * C + t]) * ze);
+    }
+    if (lane == 0) wmax[warp] = mx;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float m = 0.f;
+        for (int w = 0; w < 8; ++w) m = fmaxf(m, wmax[w]);
+        zmax[bh * NC + c] = m > 0.f ? m : 1.f;
+    }
+}
+
+cudaError_t launch_tc_dy_prep(const Problem& p, const float* o, const float* Z, const void* dO, const float* Aloc,
+                              float* zeta, float* ucol, float* rowterm, float* zmax, cudaStream_t s) {
+    dim3 grid(p.NC, (unsigned)p.BH());
+    tc_dy_prep_kernel<<<grid, 256, 0, s>>>(o, Z, (const __nv_bfloat16*)dO, Aloc, zeta, ucol, rowterm, zmax, p.T, p.C,
+                                          p.NC, p.normalize);
+    return cudaGetLastError();
+}
+
 template <typename Tin>
 __global__ void rowdot_kernel(const float* __restrict__ o, const Tin* __restrict__ dO,
                               float* __restrict__ out, long ntok, int dv) {

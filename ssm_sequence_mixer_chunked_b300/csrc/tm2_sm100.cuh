@@ -89,6 +89,12 @@ TM2_DEV void tma_load_3d(uint32_t dst, const void* tmap, uint32_t bar, int x, in
         "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z)
         : "memory");
 }
+TM2_DEV void tma_load_4d(uint32_t dst, const void* tmap, uint32_t bar, int x, int y, int z, int w) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+        "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w)
+        : "memory");
+}
 TM2_DEV void tma_load_3d_hint(uint32_t dst, const void* tmap, uint32_t bar, int x, int y, int z, uint64_t policy) {
     asm volatile(
         "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
@@ -153,6 +159,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn = 
     return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
+// Same with both operands fp16 (A/B format fields 0).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool a_mn = false, bool b_mn = false) {
+    return (1u << 4) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
 
 // 32 lanes x 16 consecutive 32-bit columns -> 16 registers per thread.  The load and
 // its wait sit in one asm statement so no use of the registers can be scheduled
@@ -205,6 +216,15 @@ TM2_DEV uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %2, %1;" : "=r"(r) : "f"(lo), "f"(hi));
     return r;
+}
+TM2_DEV uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %2, %1;" : "=r"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+// Two bf16 values (one 32-bit word) -> two fp16 values (exact inside the fp16 range).
+TM2_DEV uint32_t bf16x2_to_f16x2(uint32_t x) {
+    return pack_f16x2(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
 }
 TM2_DEV void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)

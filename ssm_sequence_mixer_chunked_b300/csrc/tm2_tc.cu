@@ -59,6 +59,20 @@ bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t heads, uint6
     return r == CUDA_SUCCESS;
 }
 
+bool make_tmap_state_slices(CUtensorMap* map, const void* base, uint64_t nplanes) {
+    auto enc = encoder();
+    if (!enc) return false;
+    // plane = [4096 rows r = m*64 + n][64 columns] of 16-bit values
+    cuuint64_t dims[4] = {64, 64, 64, nplanes};                     // col, n, m, plane
+    cuuint64_t strides[3] = {128, 64 * 128, 4096 * 128};            // bytes for n, m, plane
+    cuuint32_t box[4] = {64, 1, 64, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 static std::mutex g_status_mu;
 static int* g_status_addr[256];
 

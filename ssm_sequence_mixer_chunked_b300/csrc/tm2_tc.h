@@ -17,6 +17,11 @@ bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64
 bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t heads, uint64_t rows, uint64_t cols,
                        uint32_t box_rows);
 
+// 4-D descriptor over state planes [nplanes][4096 rows r = m*64 + n][64 columns] (16-bit):
+// one box is the 64 rows (m = 0..63, n fixed) x 64 columns of one plane, i.e. the slice
+// {S[(m, n), :]} for a fixed second key index n, landing as a [m][column] tile.
+bool make_tmap_state_slices(CUtensorMap* map, const void* base, uint64_t nplanes);
+
 // Reads (and optionally clears) the device status word of the current device.
 int read_tc_status(bool clear);
 

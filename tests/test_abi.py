@@ -45,8 +45,14 @@ def test_version_and_status_strings(lib):
 def test_workspace_sizes(lib):
     bf16 = 1
     w = lib.tm2_forward_workspace(2, 16, 8192, 64, 64, 0, bf16, 1)
-    # states entering each of 128 chunks: 64 * 65 * 64 fp32 per (b, h, chunk)
-    assert w >= 2 * 16 * 128 * 64 * 65 * 64 * 4
+    # tensor-core path (chunk 256): the state entering each of 32 chunks, 4096 x 64 bf16
+    # plus the 4096 fp32 normaliser entries, per (b, h, chunk)
+    assert w >= 2 * 16 * 32 * 4096 * (64 * 2 + 4)
+    w64 = lib.tm2_forward_workspace(2, 16, 8192, 64, 64, 64, bf16, 1)
+    # CUDA-core path (chunk 64): 128 chunk states of 64 * 65 * 64 fp32 per (b, h)
+    assert w64 >= 2 * 16 * 128 * 64 * 65 * 64 * 4
+    assert lib.tm2_forward_workspace(2, 16, 8192, 64, 64, 256, bf16, 1) == w
+    assert lib.tm2_forward_workspace(2, 16, 8192, 64, 64, 256, 0, 1) == 0     # fp32 has no chunk 256
     assert lib.tm2_backward_workspace(2, 16, 8192, 64, 64, 0, bf16, 1) > w
     assert lib.tm2_forward_workspace(2, 16, 8192, 48, 48, 0, bf16, 1) == 0      # unsupported -> 0
     assert lib.tm2_forward_workspace(2, 16, 0, 64, 64, 0, bf16, 1) % 256 == 0

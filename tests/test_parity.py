@@ -100,6 +100,40 @@ def test_fwd_initial_and_final_state():
     assert err(Sf.cpu(), Sf_r) <= 1e-4 and err(zf.cpu(), zf_r) <= 1e-4
 
 
+def test_fwd_bf16_d64_initial_and_final_state():
+    """bf16, d = dv = 64 (the tensor-core path): continue a sequence from the state a prefix
+    left behind (the oracle recurrence over 300 tokens gives S0, z0), over three chunks with
+    a ragged end; outputs and the final state against the oracle recurrence.  (A state that
+    no sequence can produce -- e.g. z0 with random signs -- lets Z cross zero, where o = N/Z
+    has no usable precision in any arithmetic.)"""
+    B, H, T, d = 1, 2, 600, 64
+    pre = si.sequence_inputs(B, H, 300, d, d, dtype="bf16", qkv_std=0.125, seed=16)
+    _, _, S0, z0 = oracle.fwd_recurrent(pre["q"], pre["k"], pre["v"], pre["a"], True)
+    S0 = torch.as_tensor(S0).float()
+    z0 = torch.as_tensor(z0).float()
+    inp = si.sequence_inputs(B, H, T, d, d, dtype="bf16", qkv_std=0.125, seed=17)
+    gi = cuda(inp)
+    o, Z, Sf, zf = tm2.forward(gi["q"], gi["k"], gi["v"], gi["a"], normalize=True, S0=S0.cuda(),
+                               z0=z0.cuda(), return_state=True)
+    torch.cuda.synchronize()
+    o_r, Z_r, Sf_r, zf_r = oracle.fwd_recurrent(inp["q"], inp["k"], inp["v"], inp["a"], True, S0=S0, z0=z0)
+    assert err(o.cpu(), o_r) <= 2e-2 and err(Z.cpu(), Z_r) <= 2e-2
+    assert err(Sf.cpu(), Sf_r) <= 2e-2 and err(zf.cpu(), zf_r) <= 2e-2
+
+
+@pytest.mark.parametrize("normalize", [True, False])
+def test_fwd_chunk_invariance_bf16_d64(normalize):
+    """chunk 64 (CUDA-core path) and chunk 256 (tensor-core path) give the same outputs,
+    both within the bf16 bar of the oracle."""
+    inp = si.sequence_inputs(2, 2, 1000, 64, 64, dtype="bf16", qkv_std=0.125, seed=19)
+    o64, Z64 = run_fwd(inp, normalize, chunk=64)
+    o256, Z256 = run_fwd(inp, normalize, chunk=256)
+    o_ref, Z_ref = oracle.fwd_quadratic(inp["q"], inp["k"], inp["v"], inp["a"], normalize)
+    assert err(o64.cpu(), o_ref) <= 2e-2 and err(o256.cpu(), o_ref) <= 2e-2
+    assert err(Z256.cpu(), Z_ref) <= 2e-2
+    assert err(o256.cpu(), o64.cpu()) <= 2e-2
+
+
 def test_fwd_empty_sequence():
     """T = 0 is a no-op; the final state is the initial state."""
     q = torch.zeros(1, 2, 0, 16, device="cuda")
@@ -162,6 +196,22 @@ def test_bwd_small_ragged(dtype, d, T, normalize):
     inp = si.sequence_inputs(2, 2, T, d, d, dtype=dtype, qkv_std=1 / math.sqrt(d), seed=200 + T + d,
                              with_dO=True)
     check_bwd(inp, dtype, normalize)
+
+
+@pytest.mark.parametrize("normalize", [True, False])
+def test_bwd_chunk_invariance_bf16_d64(normalize):
+    """Backward through chunk 64 (CUDA-core path) and chunk 256 (tensor-core path) over
+    four chunks with a ragged end: both within the bf16 bar of the oracle."""
+    inp = si.sequence_inputs(1, 3, 1000, 64, 64, dtype="bf16", qkv_std=0.125, seed=23, with_dO=True)
+    g = cuda(inp)
+    refs = oracle.bwd_quadratic(inp["q"], inp["k"], inp["v"], inp["a"], inp["dO"], normalize)
+    for chunk in (64, 256):
+        o, Z = tm2.forward(g["q"], g["k"], g["v"], g["a"], normalize=normalize, chunk=chunk)
+        grads = tm2.backward(g["q"], g["k"], g["v"], g["a"], o, Z, g["dO"], normalize=normalize, chunk=chunk)
+        torch.cuda.synchronize()
+        for name, x, ref in zip(("dq", "dk", "dv", "da"), grads, refs):
+            e = err(x.cpu(), ref)
+            assert e <= 2e-2, (chunk, name, e)
 
 
 def test_fwd_bwd_bf16_B2_H16_T8192_sampled_heads():
