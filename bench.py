@@ -69,15 +69,21 @@ def bwd_flops(d, dv, C, normalize=True):
 
 
 def kernel_flops(name, d, dv, C, tokens):
-    """Algorithmic flops of one launch of a named kernel over `tokens` token-heads."""
+    """Algorithmic flops of one launch of a named kernel over `tokens` token-heads: the
+    method's own work at chunk length C (causal pairs only, no recompute counted twice;
+    the tensor-core kernels' hi + lo split of operands is not counted)."""
     dv1 = dv + 1
+    state = 2 * d * d * dv1          # one d^2 x (dv+1) contraction per token
     per = {
-        "tc_state_scan_fwd": 2 * d * d * dv1 + 2 * d * d * dv1 / C,
-        "tc_chunk_out": 2 * d * d * dv1 + (C + 1) * (d + dv),
-        "state_scan_fwd": 2 * d * d * dv1 + 2 * d * d * dv1 / C,
-        "chunk_out": 2 * d * d * dv1 + (C + 1) * (d + dv),
-        "state_scan_bwd": 2 * d * d * dv1 + 2 * d * d * dv1 / C,
-        "bwd_chunk": 6 * d * d * dv1 + (C + 1) * (3 * d + 2 * dv),
+        "tc_state_scan_fwd": state + 2 * d * d * dv1 / C,
+        "tc_state_scan_bwd": state + 2 * d * d * dv1 / C,
+        "tc_chunk_out": state + (C + 1) * (d + dv),
+        "tc_bwd_dq": state + (C + 1) * (d + dv),
+        "tc_bwd_dkdv": 2 * state + (C + 1) * (2 * d + dv),
+        "state_scan_fwd": state + 2 * d * d * dv1 / C,
+        "chunk_out": state + (C + 1) * (d + dv),
+        "state_scan_bwd": state + 2 * d * d * dv1 / C,
+        "bwd_chunk": 3 * state + (C + 1) * (3 * d + 2 * dv),
     }.get(name)
     return None if per is None else per * tokens
 
@@ -215,13 +221,25 @@ def setup_dist():
     return world, rank, torch.device("cuda", torch.cuda.current_device())
 
 
-def max_over_ranks(x, world):
+def max_over_ranks(x, world, device="cuda"):
+    """Largest value of x over all ranks (the step time the whole job waits for)."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def rank_seed(base, rank):
+    """Seed of the synthetic batch of `rank`: every rank runs its own replica on its own
+    batch (the (b, h) problems are independent, so nothing is exchanged)."""
+    return base + 1000 * rank
+
+
+def whole_job_rate(units_per_rank, world, max_ms):
+    """Units per second of the whole job: all ranks' units over the slowest rank's time."""
+    return world * units_per_rank / (max_ms * 1e-3)
 
 
 def barrier(world):
@@ -295,7 +313,7 @@ def run_tm2(args, world, rank, device):
     pk = peaks()
     w = si.WORKLOADS[3]
     C = 0   # library choice: the tensor-core path wherever it applies
-    inp_cpu = si.workload_inputs(3, seed=3 + 1000 * rank)
+    inp_cpu = si.workload_inputs(3, seed=rank_seed(3, rank))
     g = {k: v.to(device) for k, v in inp_cpu.items()}
     B, H, T, d, dv = w.B, w.H, w.T, w.d, w.dv
     o = torch.empty(g["v"].shape, dtype=torch.float32, device=device)
@@ -332,31 +350,36 @@ def run_tm2(args, world, rank, device):
     step_ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
     step_ms = max_over_ranks(step_ms, world)
     tokens = B * T
-    value = world * tokens / (step_ms * 1e-3)
+    value = whole_job_rate(tokens, world, step_ms)
     kern = summarize(recs)
     launches = len(recs)
 
     # roofline of the dominant kernel (largest share of step time)
     dom = max(kern, key=lambda n: kern[n]["ms"])
     per_launch_tokens = B * H * T
-    kf = kernel_flops(dom, d, dv, 256 if dom.startswith("tc_") else 64, per_launch_tokens)
-    fp32_peak = 148 * 128 * 2 * pk["sm_max_mhz"] * 1e6 / 1e12   # FFMA, TFLOP/s
+    tc = dom.startswith("tc_")
+    kf = kernel_flops(dom, d, dv, 256 if tc else 64, per_launch_tokens)
     roof = None
     if kf is not None:
         ach = kf / (kern[dom]["ms_per_launch"] * 1e-3) / 1e12
-        roof = {"kernel": dom, "bound": "alu", "achieved": ach, "peak": fp32_peak, "unit": "TFLOP/s",
-                "frac": ach / fp32_peak, "traffic": ncu_traffic(dom, per_launch_tokens),
-                "peak_source": "derived: 148 SMs x 128 fp32 FMA/clk x 2 flop x %.0f MHz" % pk["sm_max_mhz"],
-                "algorithmic_flops_per_launch": kf}
-    CF, CB = 256, 64   # chunk lengths the library picks for bf16 d = 64: forward, backward
-    counted = (fwd_flops(d, dv, CF) + bwd_flops(d, dv, CB)) * B * H * T
-    tensor_frac = counted / (step_ms * 1e-3) / (pk["bf16_tflops"] * 1e12)
+        if tc:   # timed inside a long step: the sustained bf16 figure
+            peak, bound, src = pk["bf16_tflops_sustained"], "tensor", "MEASURED_PEAKS.json bf16_tflops_sustained (%s)" % pk["source"]
+        else:
+            peak = 148 * 128 * 2 * pk["sm_max_mhz"] * 1e6 / 1e12   # FFMA, TFLOP/s
+            bound, src = "alu", "derived: 148 SMs x 128 fp32 FMA/clk x 2 flop x %.0f MHz" % pk["sm_max_mhz"]
+        roof = {"kernel": dom, "bound": bound, "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                "frac": ach / peak, "traffic": ncu_traffic(dom, per_launch_tokens),
+                "peak_source": src, "algorithmic_flops_per_launch": kf}
+    CH = 256   # chunk length the library picks for bf16 inputs, d = dv = 64
+    counted = (fwd_flops(d, dv, CH) + bwd_flops(d, dv, CH)) * B * H * T
+    tensor_frac = counted / (step_ms * 1e-3) / (pk["bf16_tflops_sustained"] * 1e12)
 
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic", "config": config_of(w, {"forward": 256, "backward": 64}), "roofline": roof,
+            "data": "synthetic", "config": config_of(w, CH), "roofline": roof,
             "step_bf16_tensor_peak_frac": tensor_frac,
+            "step_tensor_peak": "bf16_tflops_sustained of MEASURED_PEAKS.json (%s)" % pk["source"],
             "step_counted_flops": counted, "gpu_launches": launches,
             "kernels": {n: {k: round(v, 4) if isinstance(v, float) else v for k, v in a.items()}
                         for n, a in kern.items()},

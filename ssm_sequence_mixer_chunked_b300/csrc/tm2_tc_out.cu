@@ -1,27 +1,28 @@
-// tm2_tc_out.cu -- the per-chunk output kernel of the bf16 tensor-core path (d = dv = 64).
+// tm2_tc_out.cu -- the per-chunk output kernel of the tensor-core path (bf16 inputs, d = dv = 64).
 //
 // "2Mamba2Furious", Sec. 5: w_ij = exp(cumA_i - cumA_j) (q_i . k_j)^2, o_i = N_i / Z_i with
 // N_i = sum_{j<=i} w_ij v_j and Z_i = sum_{j<=i} w_ij.  Split at the chunk boundary:
-//   [N_i, Z_i] = sum_{j in c, j<=i} P_ij [v_j, 1]  +  exp(A_i) sum_r (q_i (x) q_i)[r] [S_{c-1}, z_{c-1}][r, :]
+//   [N_i, Z_i] = sum_{j in c, j<=i} P_ij [v_j, 1]  +  exp(A_i) sum_{m,n} q_i[m] q_i[n] [S_{c-1}, z_{c-1}][(m,n), :]
 // with P_ij = (q_i . k_j)^2 exp(A_i - A_j) and S_{c-1}, z_{c-1} the state entering the chunk
-// (written by the chunk-state scan).
+// (written by the chunk-state scan as two fp16 planes, hi and residual, and fp32 z).
 //
 // One CTA per (chunk, b, h); the chunk's 256 tokens form two 128-row tiles.
 //  * Intra-chunk (causal 128 x 64 blocks: tile 0 x key blocks 0-1, tile 1 x key blocks 0-3):
-//    s = Q K^T by tcgen05.mma from TMA tiles (both K-major, bf16), the epilogue warps
-//    square it, apply the decay mask in fp32, keep the row sums (Z) in fp32 and write P
-//    into tensor memory as two bf16 terms P_hi + P_lo (one bf16 term alone would cost
-//    ~2^-9 relative per weight, enough to break the 2e-2 bar on unnormalised outputs);
-//    both are A operands of P V (V MN-major, straight from its TMA tile).
-//  * Inter-chunk readout: 64 slices of the 4096 state rows (one m each).  The A operand
-//    exp(A_i) q_i[m] q_i[n] (n = 0..63) is generated by the threads into tensor memory in
-//    fp16; the state arrives as two fp16 planes (hi and residual, written by the chunk-state
-//    scan), so each slice is two MMAs with B = [S | z] (64 rows x 80 columns, MN-major):
-//    S by TMA, z written by the threads into a second 64-column block; N = 80 puts Z_inter
-//    in accumulator column 64.
-//  * Epilogue: o = N / (Z_inter + Z_intra) (or N), fp32 out, Z saved for the backward.
-// Warps 0-7 compute (warp w: tile w / 4, tensor-memory lane quadrant w % 4), warp 8 issues
-// TMA, warp 9 the MMAs.  Every mbarrier wait is bounded (TM2_ERR_TIMEOUT on expiry).
+//    s = Q K^T by tcgen05.mma from TMA tiles (bf16, K-major), the compute warps square it,
+//    apply the decay mask in fp32, keep the row sums (Z) in fp32 and write P into tensor
+//    memory as two bf16 terms P_hi + P_lo (one bf16 term alone costs ~2^-9 relative per
+//    weight, enough to break the 2e-2 bar on unnormalised outputs); both are A operands
+//    of P V (V MN-major, straight from its TMA tile).
+//  * Inter-chunk readout: for each m, U_m = Q S_m with S_m[n][col] = S[(m,n), col] (the state
+//    slice by TMA, MN-major, hi and residual plane: two MMAs; Q converted exactly to fp16),
+//    and the compute warps accumulate N_x[col] += q_i[m] U_m[i][col] in fp32.  A 65th
+//    product U = Q zm^T with zm[m][n] = z[(m,n)] gives Z_x = sum_m q_i[m] U[i][m].  No
+//    operand is a rounded product; the readout of nearly orthogonal queries keeps its
+//    precision.
+//  * Epilogue: [N, Z] = intra + exp(A_i) [N_x, Z_x]; o = N / Z (or N), fp32; Z saved.
+// Warps 0-15 compute (warp w: tile (w >> 2) & 1, tensor-memory lane quadrant w & 3, column
+// half w >> 3), warp 16 issues TMA, warp 17 the MMAs.  Every mbarrier wait is bounded
+// (TM2_ERR_TIMEOUT on expiry).
 #include "tm2.h"
 #include "tm2_launch.h"
 #include "tm2_sm100.cuh"
@@ -31,28 +32,32 @@ namespace tm2 {
 namespace tcout {
 
 constexpr int C = TC_CHUNK;
-constexpr int NS = 3;                        // state-slice stage buffers
-constexpr int THREADS = 10 * 32;
-constexpr int WARP_TMA = 8, WARP_MMA = 9;
-constexpr int TILE_BYTES = C * 128;          // [256][64] bf16
-constexpr int SQ_OFF = 0, SK_OFF = TILE_BYTES, SV_OFF = 2 * TILE_BYTES;
-constexpr int SS_OFF = 3 * TILE_BYTES;       // NS x { S_hi 8 KB, z_hi 8 KB, S_lo 8 KB, z_lo 8 KB }
-constexpr int STAGE_BYTES = 32768;
-constexpr int SA_OFF = SS_OFF + NS * STAGE_BYTES;   // chunk-local A values, C floats
-constexpr int SMEM_BYTES = SA_OFF + C * 4 + 1024;
+constexpr int NS = 3;                        // state-slice stages (hi + residual plane)
+constexpr int NSL = 65;                      // 64 state slices + the normaliser product
+constexpr int THREADS = 18 * 32;
+constexpr int NCOMP = 512;                   // compute threads
+constexpr int WARP_TMA = 16, WARP_MMA = 17;
+constexpr int TILE_BYTES = C * 128;          // [256][64] 16-bit
+constexpr int SQ = 0, SQH = TILE_BYTES, SK = 2 * TILE_BYTES, SV = 3 * TILE_BYTES;
+constexpr int SZH = 4 * TILE_BYTES, SZL = SZH + 8192;             // zm hi / lo, [64][64] fp16
+constexpr int STG = SZL + 8192;                                    // NS x (hi 8 KB + lo 8 KB)
+constexpr int SAV = STG + NS * 16384;                              // A values, 256 floats
+constexpr int SRED = SAV + 1024;                                   // [2 halves][256 tokens][2]
+constexpr int SMEM_BYTES = SRED + 4096 + 1024;
 constexpr int NBLK = 6;                      // intra-chunk blocks: (tile, 64-key block)
 // tensor-memory columns
-constexpr uint32_t TM_Y = 0;                 // Y tile t at t * 80 (80 columns each)
-constexpr uint32_t TM_S = 160;               // Q K^T block, 64 columns
-constexpr uint32_t TM_PH = 224;              // P_hi (bf16), 32 columns
-constexpr uint32_t TM_PL = 256;              // P_lo (bf16), 32 columns
-constexpr uint32_t TM_A = 288;               // readout A buffers: 288 + buf*64 + tile*32
+constexpr uint32_t TM_Y = 0;                 // intra N, tile t at t * 64
+constexpr uint32_t TM_S = 128;               // Q K^T block, 64 columns
+constexpr uint32_t TM_PH = 192, TM_PL = 224; // P hi / lo (bf16), 32 columns each
+constexpr uint32_t TM_U = 256;               // U buffers: 256 + buf*128 + tile*64
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 64, false, false);
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, 64, false, true);
-constexpr uint32_t IDESC_RD = idesc_f16_f32(128, 80, false, true);
+constexpr uint32_t IDESC_RD = idesc_f16_f32(128, 64, false, true);
+constexpr uint32_t IDESC_RZ = idesc_f16_f32(128, 64, false, false);
 TM2_DEV int blk_tile(int b) { return b < 2 ? 0 : 1; }
 TM2_DEV int blk_key(int b) { return b < 2 ? b : b - 2; }
+TM2_DEV uint32_t swz_elem(int row, int col) { return row * 128 + ((((col >> 3) ^ (row & 7))) << 4) + (col & 7) * 2; }
 
 struct Args {
     const float* Aloc;   // [BH][Tp]
@@ -74,16 +79,17 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
                                                                   const __grid_constant__ Args a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    __shared__ __align__(8) uint64_t bar_qkv, bar_full[NS], bar_empty[NS], bar_afull[2], bar_aempty[2], bar_sfull[NBLK],
-        bar_sfree[NBLK], bar_pfull[NBLK], bar_pfree[NBLK], bar_yfull, bar_done;
+    __shared__ __align__(8) uint64_t bar_qkv, bar_full[NS], bar_empty[NS], bar_cvt, bar_sfull[NBLK], bar_sfree[NBLK],
+        bar_pfull[NBLK], bar_pfree[NBLK], bar_ufull[2], bar_uempty[2], bar_yfull, bar_red, bar_done;
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_s;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c = blockIdx.x;
     const long bh = blockIdx.y;
     const int NC = a.NC;
-    const uint32_t sbase = smem_u32(smem);
-    float* sAv = reinterpret_cast<float*>(smem + SA_OFF);
+    const uint32_t sb0 = smem_u32(smem);
+    float* sAv = reinterpret_cast<float*>(smem + SAV);
+    float* sRed = reinterpret_cast<float*>(smem + SRED);
 
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(&bar_qkv), 1);
@@ -91,28 +97,24 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
             mbar_init(smem_u32(&bar_full[i]), 1);
             mbar_init(smem_u32(&bar_empty[i]), 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(smem_u32(&bar_afull[i]), 256);
-            mbar_init(smem_u32(&bar_aempty[i]), 1);
-        }
+        mbar_init(smem_u32(&bar_cvt), NCOMP);
         for (int b = 0; b < NBLK; ++b) {   // one set per intra-chunk block, each used once
             mbar_init(smem_u32(&bar_sfull[b]), 1);
-            mbar_init(smem_u32(&bar_sfree[b]), 128);
-            mbar_init(smem_u32(&bar_pfull[b]), 128);
+            mbar_init(smem_u32(&bar_sfree[b]), 256);
+            mbar_init(smem_u32(&bar_pfull[b]), 256);
             mbar_init(smem_u32(&bar_pfree[b]), 1);
         }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&bar_ufull[i]), 1);
+            mbar_init(smem_u32(&bar_uempty[i]), NCOMP);
+        }
         mbar_init(smem_u32(&bar_yfull), 1);
+        mbar_init(smem_u32(&bar_red), NCOMP);
         mbar_init(smem_u32(&bar_done), 1);
         abort_s = 0;
         fence_mbar_init();
     }
-    // zero blocks of the [S | z] stages (the threads later write z into column 0)
-    for (int e = threadIdx.x; e < NS * 1024; e += THREADS) {
-        const int sb = e >> 10, pl = (e >> 9) & 1, off = (e & 511) * 16;
-        st_shared_v4(sbase + SS_OFF + sb * STAGE_BYTES + pl * 16384 + 8192 + off, 0, 0, 0, 0);
-    }
     for (int j = threadIdx.x; j < C; j += THREADS) sAv[j] = a.Aloc[bh * a.Tp + (long)c * C + j];
-    fence_proxy_async();
     if (warp == 0) {
         tmem_alloc(smem_u32(&tmem_base_s), TMEM_COLS);
         tmem_relinquish();
@@ -127,9 +129,9 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
             prefetch_tmap(&tmS);
             const uint32_t qb = smem_u32(&bar_qkv);
             mbar_arrive_expect_tx(qb, 3 * TILE_BYTES);
-            tma_load_3d(sbase + SQ_OFF, &tmQ, qb, 0, c * C, (int)bh);
-            tma_load_3d(sbase + SK_OFF, &tmK, qb, 0, c * C, (int)bh);
-            tma_load_3d(sbase + SV_OFF, &tmV, qb, 0, c * C, (int)bh);
+            tma_load_3d(sb0 + SQ, &tmQ, qb, 0, c * C, (int)bh);
+            tma_load_3d(sb0 + SK, &tmK, qb, 0, c * C, (int)bh);
+            tma_load_3d(sb0 + SV, &tmV, qb, 0, c * C, (int)bh);
             int issued = 0;
             for (int m = 0; m < 64 && !abort_s; ++m) {
                 const int sb = m % NS;
@@ -139,8 +141,9 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
                 }
                 const uint32_t fb = smem_u32(&bar_full[sb]);
                 mbar_arrive_expect_tx(fb, 16384);
-                tma_load_3d(sbase + SS_OFF + sb * STAGE_BYTES, &tmS, fb, 0, m * 64, (int)((bh * NC + c) * 2));
-                tma_load_3d(sbase + SS_OFF + sb * STAGE_BYTES + 16384, &tmS, fb, 0, m * 64, (int)((bh * NC + c) * 2 + 1));
+                const int plane = (int)((bh * NC + c) * 2);
+                tma_load_3d(sb0 + STG + sb * 16384, &tmS, fb, 0, m * 64, plane);
+                tma_load_3d(sb0 + STG + sb * 16384 + 8192, &tmS, fb, 0, m * 64, plane + 1);
                 issued = m + 1;
             }
             mbar_wait(qb, 0, a.status);
@@ -158,39 +161,46 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    umma_bf16(tmem + TM_S, sdesc_sw128(sbase + SQ_OFF + t * 16384 + kk * 32),
-                              sdesc_sw128(sbase + SK_OFF + jb * 8192 + kk * 32), IDESC_QK, kk > 0);
+                    umma_bf16(tmem + TM_S, sdesc_sw128(sb0 + SQ + t * 16384 + kk * 32),
+                              sdesc_sw128(sb0 + SK + jb * 8192 + kk * 32), IDESC_QK, kk > 0);
                 umma_commit(smem_u32(&bar_sfull[b]));
                 if (!(ok = mbar_wait(smem_u32(&bar_pfull[b]), 0, a.status))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t vd = sdesc_sw128_ex(sbase + SV_OFF + jb * 8192 + kk * 2048, 8192, 1024);
-                    umma_bf16_ts(tmem + TM_Y + t * 80, tmem + TM_PH + kk * 8, vd, IDESC_PV, (jb > 0 || kk > 0) ? 1u : 0u);
-                    umma_bf16_ts(tmem + TM_Y + t * 80, tmem + TM_PL + kk * 8, vd, IDESC_PV, 1u);
+                    const uint64_t vd = sdesc_sw128_ex(sb0 + SV + jb * 8192 + kk * 2048, 8192, 1024);
+                    umma_bf16_ts(tmem + TM_Y + t * 64, tmem + TM_PH + kk * 8, vd, IDESC_PV, (jb > 0 || kk > 0) ? 1u : 0u);
+                    umma_bf16_ts(tmem + TM_Y + t * 64, tmem + TM_PL + kk * 8, vd, IDESC_PV, 1u);
                 }
                 umma_commit(smem_u32(&bar_pfree[b]));
             }
-            // ---- inter-chunk readout over the 64 state slices
-            for (int m = 0; m < 64 && ok; ++m) {
-                const int sb = m % NS, ab = m & 1;
+            // ---- inter-chunk readout: U_m = Q S_m (m < 64), U_64 = Q zm^T
+            if (ok) ok = mbar_wait(smem_u32(&bar_cvt), 0, a.status);
+            tc_fence_after();
+            for (int m = 0; m < NSL && ok; ++m) {
+                const int sb = m % NS, ub = m & 1;
                 if (abort_s) { ok = false; break; }
-                if (!(ok = mbar_wait(smem_u32(&bar_full[sb]), (m / NS) & 1, a.status))) break;
-                if (!(ok = mbar_wait(smem_u32(&bar_afull[ab]), (m >> 1) & 1, a.status))) break;
+                if (m < 64 && !(ok = mbar_wait(smem_u32(&bar_full[sb]), (m / NS) & 1, a.status))) break;
+                if (m >= 2 && !(ok = mbar_wait(smem_u32(&bar_uempty[ub]), ((m >> 1) - 1) & 1, a.status))) break;
                 tc_fence_after();
-                const uint32_t sb_addr = sbase + SS_OFF + sb * STAGE_BYTES;
 #pragma unroll
-                for (int t = 0; t < 2; ++t)
+                for (int t = 0; t < 2; ++t) {
+                    const uint32_t d = tmem + TM_U + ub * 128 + t * 64;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        const uint32_t aa = tmem + TM_A + ab * 64 + t * 32 + kk * 8;
-                        umma_bf16_ts(tmem + TM_Y + t * 80, aa, sdesc_sw128_ex(sb_addr + kk * 2048, 8192, 1024),
-                                     IDESC_RD, 1u);
-                        umma_bf16_ts(tmem + TM_Y + t * 80, aa, sdesc_sw128_ex(sb_addr + 16384 + kk * 2048, 8192, 1024),
-                                     IDESC_RD, 1u);
+                        const uint64_t ad = sdesc_sw128(sb0 + SQH + t * 16384 + kk * 32);
+                        if (m < 64) {
+                            const uint32_t bs = sb0 + STG + sb * 16384 + kk * 2048;
+                            umma_bf16(d, ad, sdesc_sw128_ex(bs, 8192, 1024), IDESC_RD, kk > 0);
+                            umma_bf16(d, ad, sdesc_sw128_ex(bs + 8192, 8192, 1024), IDESC_RD, 1u);
+                        } else {
+                            umma_bf16(d, ad, sdesc_sw128(sb0 + SZH + kk * 32), IDESC_RZ, kk > 0);
+                            umma_bf16(d, ad, sdesc_sw128(sb0 + SZL + kk * 32), IDESC_RZ, 1u);
+                        }
                     }
-                umma_commit(smem_u32(&bar_empty[sb]));
-                umma_commit(smem_u32(&bar_aempty[ab]));
+                }
+                if (m < 64) umma_commit(smem_u32(&bar_empty[sb]));
+                umma_commit(smem_u32(&bar_ufull[ub]));
             }
             if (ok) umma_commit(smem_u32(&bar_yfull));
             else abort_s = 1;
@@ -199,29 +209,52 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
         }
     } else {
         // ---------------------------------------------------------------- compute warps
-        const int t = warp >> 2, quad = warp & 3;
+        const int quad = warp & 3, t = (warp >> 2) & 1, h = warp >> 3;
         const int l = quad * 32 + lane;              // row of tile t
         const int i = t * 128 + l;                   // token index inside the chunk
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         const float Ai = sAv[i];
         float zin = 0.f;
-        bool ok = true;
-        // columns 64..79 of this row's accumulator start at zero (the P V products only
-        // write columns 0..63; the readout accumulates all 80)
-        {
-            const uint32_t zr[16] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
-            tmem_st16(tmem + lane_base + TM_Y + t * 80 + 64, zr);
-            tmem_wait_st();
+        bool ok = mbar_wait(smem_u32(&bar_qkv), 0, a.status);
+        if (ok) {   // fp16 copy of the Q tile; the normaliser matrix of the state as hi + lo fp16
+            const int tt = threadIdx.x;
+            for (int pc = tt; pc < 2048; pc += NCOMP) {
+                uint32_t x[4];
+                asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                             : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3])
+                             : "r"(sb0 + SQ + pc * 16));
+                st_shared_v4(sb0 + SQH + pc * 16, bf16x2_to_f16x2(x[0]), bf16x2_to_f16x2(x[1]), bf16x2_to_f16x2(x[2]),
+                             bf16x2_to_f16x2(x[3]));
+            }
+            const float* zc = a.zx + (bh * NC + c) * 4096;
+            for (int pc = tt; pc < 512; pc += NCOMP) {
+                const int m = pc >> 3, k8 = pc & 7;
+                const float4 a0 = *reinterpret_cast<const float4*>(zc + m * 64 + k8 * 8);
+                const float4 a1 = *reinterpret_cast<const float4*>(zc + m * 64 + k8 * 8 + 4);
+                const float v[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                uint32_t hh[4], ll[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    hh[u] = pack_f16x2(v[2 * u], v[2 * u + 1]);
+                    const __half2 h2 = *reinterpret_cast<const __half2*>(&hh[u]);
+                    ll[u] = pack_f16x2(v[2 * u] - __low2float(h2), v[2 * u + 1] - __high2float(h2));
+                }
+                const uint32_t off = m * 128 + ((k8 ^ (m & 7)) << 4);
+                st_shared_v4(sb0 + SZH + off, hh[0], hh[1], hh[2], hh[3]);
+                st_shared_v4(sb0 + SZL + off, ll[0], ll[1], ll[2], ll[3]);
+            }
+            fence_proxy_async();
+            mbar_arrive(smem_u32(&bar_cvt));
         }
-        if (!mbar_wait(smem_u32(&bar_qkv), 0, a.status)) ok = false;
-        // ---- intra-chunk: tile 0 owns blocks 0-1, tile 1 owns blocks 2-5
+        // ---- intra-chunk: tile 0 owns blocks 0-1, tile 1 owns blocks 2-5; half h: 32 key columns
         for (int b = (t == 0 ? 0 : 2); b < (t == 0 ? 2 : NBLK) && ok; ++b) {
             const int jb = blk_key(b);
             if (!(ok = mbar_wait(smem_u32(&bar_sfull[b]), 0, a.status))) break;
             if (b > 0 && !(ok = mbar_wait(smem_u32(&bar_pfree[b - 1]), 0, a.status))) break;
             tc_fence_after();
-#pragma unroll 1
-            for (int cc = 0; cc < 4; ++cc) {
+#pragma unroll
+            for (int g2 = 0; g2 < 2; ++g2) {
+                const int cc = 2 * h + g2;
                 float s[16];
                 tmem_ld16(tmem + lane_base + TM_S + cc * 16, s);
                 uint32_t ph[8], pl[8];
@@ -248,64 +281,61 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
             mbar_arrive(smem_u32(&bar_sfree[b]));
             mbar_arrive(smem_u32(&bar_pfull[b]));
         }
-        // ---- inter-chunk readout: A = exp(A_i) q_i[m] q_i[n]
-        uint32_t qp[32];   // q_i as fp16 pairs (exact conversion of the bf16 input)
-        const uint8_t* qrow = smem + SQ_OFF + i * 128;
-        const float eA = __expf(Ai);
+        // ---- inter-chunk readout: nx[col] += q_i[m] U_m[i][col]; zx += q_i[m'] U_64[i][m']
+        float nx[32];
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-            const uint4 x = *reinterpret_cast<const uint4*>(qrow + ((ch ^ (i & 7)) << 4));
-            qp[ch * 4] = bf16x2_to_f16x2(x.x); qp[ch * 4 + 1] = bf16x2_to_f16x2(x.y);
-            qp[ch * 4 + 2] = bf16x2_to_f16x2(x.z); qp[ch * 4 + 3] = bf16x2_to_f16x2(x.w);
-        }
-        const long zbase = (bh * NC + c) * 4096;
+        for (int k = 0; k < 32; ++k) nx[k] = 0.f;
+        float zxp = 0.f;
+        const uint8_t* qrow = smem + SQ;
 #pragma unroll 1
-        for (int m = 0; m < 64 && ok; ++m) {
-            const int sb = m % NS, ab = m & 1;
-            if (abort_s) { ok = false; break; }
-            if (threadIdx.x < 64) {   // z block of this slice: z[m*64 + n] into column 0 of row n
-                if (!(ok = mbar_wait(smem_u32(&bar_full[sb]), (m / NS) & 1, a.status))) break;
-                const int n = threadIdx.x;
-                const float zv = a.zx[zbase + m * 64 + n];
-                const __half zh = __float2half_rn(zv);
-                uint8_t* zb = smem + SS_OFF + sb * STAGE_BYTES + 8192 + n * 128 + (n & 7) * 16;
-                *reinterpret_cast<__half*>(zb) = zh;
-                *reinterpret_cast<__half*>(zb + 16384) = __float2half_rn(zv - __half2float(zh));
-                fence_proxy_async();
-            }
-            if (m >= 2 && !(ok = mbar_wait(smem_u32(&bar_aempty[ab]), ((m >> 1) - 1) & 1, a.status))) break;
+        for (int m = 0; m < NSL && ok; ++m) {
+            const int ub = m & 1;
+            if (abort_s || !(ok = mbar_wait(smem_u32(&bar_ufull[ub]), (m >> 1) & 1, a.status))) break;
             tc_fence_after();
-            // scalar exp(A_i) q_i[m] in both halves
-            const float qm = __bfloat162float(
-                *reinterpret_cast<const __nv_bfloat16*>(qrow + (((m >> 3) ^ (i & 7)) << 4) + (m & 7) * 2));
-            const __half2 s2 = __float2half2_rn(qm * eA);
-            uint32_t r[32];
-#pragma unroll
-            for (int p = 0; p < 32; ++p) {
-                __half2 prod = __hmul2(s2, *reinterpret_cast<const __half2*>(&qp[p]));
-                r[p] = *reinterpret_cast<uint32_t*>(&prod);
-            }
-            const uint32_t ad = tmem + lane_base + TM_A + ab * 64 + t * 32;
-            tmem_st16(ad, r);
-            tmem_st16(ad + 16, r + 16);
-            tmem_wait_st();
+            float u[32];
+            const uint32_t ua = tmem + lane_base + TM_U + ub * 128 + t * 64 + h * 32;
+            tmem_ld16(ua, u);
+            tmem_ld16(ua + 16, u + 16);
             tc_fence_before();
-            mbar_arrive(smem_u32(&bar_afull[ab]));
+            mbar_arrive(smem_u32(&bar_uempty[ub]));
+            if (m < 64) {
+                const float qm = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(qrow + swz_elem(i, m)));
+#pragma unroll
+                for (int k = 0; k < 32; ++k) nx[k] = fmaf(qm, u[k], nx[k]);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 32; ++k)
+                    zxp = fmaf(__bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(qrow + swz_elem(i, h * 32 + k))),
+                               u[k], zxp);
+            }
         }
+        // ---- combine the two column halves' shares of Z, then the epilogue
+        if (ok) {
+            sRed[(h * 256 + i) * 2] = zin;
+            sRed[(h * 256 + i) * 2 + 1] = zxp;
+        }
+        mbar_arrive(smem_u32(&bar_red));
+        if (ok) ok = mbar_wait(smem_u32(&bar_red), 0, a.status);
         if (ok && !abort_s && (ok = mbar_wait(smem_u32(&bar_yfull), 0, a.status))) {
             tc_fence_after();
+            const float eA = __expf(Ai);
+            const float zi = sRed[i * 2] + sRed[(256 + i) * 2];
+            const float zo = sRed[i * 2 + 1] + sRed[(256 + i) * 2 + 1];
+            const float z = zi + eA * zo;
+            float y[32];
+            const uint32_t ya = tmem + lane_base + TM_Y + t * 64 + h * 32;
+            tmem_ld16(ya, y);
+            tmem_ld16(ya + 16, y + 16);
             const long tok = (long)c * C + i;
-            float y[64];
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) tmem_ld16(tmem + lane_base + TM_Y + t * 80 + cc * 16, y + cc * 16);
-            const float z = tmem_ld1(tmem + lane_base + TM_Y + t * 80 + 64) + zin;
             if (tok < a.T) {
                 const float inv = a.normalize ? (z != 0.f ? 1.f / z : 0.f) : 1.f;
-                float4* dst = reinterpret_cast<float4*>(a.o + (bh * a.T + tok) * 64);
+                float4* dst = reinterpret_cast<float4*>(a.o + (bh * a.T + tok) * 64 + h * 32);
 #pragma unroll
-                for (int u = 0; u < 16; ++u)
-                    dst[u] = make_float4(y[4 * u] * inv, y[4 * u + 1] * inv, y[4 * u + 2] * inv, y[4 * u + 3] * inv);
-                if (a.Z) a.Z[bh * a.T + tok] = z;
+                for (int q4 = 0; q4 < 8; ++q4)
+                    dst[q4] = make_float4((y[4 * q4] + eA * nx[4 * q4]) * inv, (y[4 * q4 + 1] + eA * nx[4 * q4 + 1]) * inv,
+                                          (y[4 * q4 + 2] + eA * nx[4 * q4 + 2]) * inv,
+                                          (y[4 * q4 + 3] + eA * nx[4 * q4 + 3]) * inv);
+                if (a.Z && h == 0) a.Z[bh * a.T + tok] = z;
             }
         }
         if (!ok) abort_s = 1;

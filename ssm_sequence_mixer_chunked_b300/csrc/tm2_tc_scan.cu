@@ -198,9 +198,29 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
         const int l = quad * 32 + lane;              // tensor-memory lane = tile row
         const int n = l & 63, moff = l >> 6;
         const int km = gt >> 6, kj = gt & 63;        // kw-table entry written by this thread
+        // per-token scalars of stage gs (read by the threads with km == 0), loaded one stage
+        // ahead so that no global-memory latency sits between a stage's TMA and its MMA
+        struct Scal { float A, ze, uc, gc, zm; };
+        auto load_scal = [&](int gs) {
+            Scal r{0.f, 0.f, 0.f, 0.f, 1.f};
+            if (km != 0 || gs >= nstages) return r;
+            const int c = chunk_of(gs / SPC);
+            const long tok = (long)c * C + (gs % SPC) * KS + kj;
+            r.A = a.Aloc[bh * a.Tp + tok];
+            r.gc = a.g[bh * NC + c];
+            if (rev) {
+                r.zm = a.zmax[bh * NC + c];
+                if (tok < a.T) {
+                    r.ze = a.zeta[bh * a.T + tok];
+                    r.uc = a.ucol[bh * a.T + tok];
+                }
+            }
+            return r;
+        };
+        Scal cur = load_scal(0);
         for (int gs = 0; gs < nstages; ++gs) {
             const int sb = gs % NS, ab = gs & 1;
-            const int c = chunk_of(gs / SPC), s = gs % SPC;
+            const Scal nxt = load_scal(gs + 1);
             if (abort_s || !mbar_wait(smem_u32(&bar_full[sb]), (gs / NS) & 1, a.status)) {
                 abort_s = 1;
                 break;
@@ -213,15 +233,12 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
                 kw[km * KS + j] = __float2half_rn(__bfloat162float(
                     *reinterpret_cast<const __nv_bfloat16*>(kt + j * 128 + (((m >> 3) ^ (j & 7)) << 4) + (m & 7) * 2)));
                 if (km == 0) {   // weight of this token, and its normaliser-column entry
-                    const long tok = (long)c * C + s * KS + j;
-                    const float A = a.Aloc[bh * a.Tp + tok];
                     float w, zc;
-                    if (rev) {
-                        const bool in = tok < a.T;
-                        w = in ? __expf(A) * a.zeta[bh * a.T + tok] / a.zmax[bh * NC + c] : 0.f;
-                        zc = in ? a.ucol[bh * a.T + tok] : 0.f;
+                    if (rev) {   // zeta = 0 past the end of the sequence
+                        w = __expf(cur.A) * cur.ze / cur.zm;
+                        zc = cur.uc;
                     } else {
-                        w = __expf(a.g[bh * NC + c] - A);
+                        w = __expf(cur.gc - cur.A);
                         zc = 1.f;
                     }
                     sw[j] = w;
@@ -294,6 +311,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(smem_u32(&bar_afull[ab]));
+            cur = nxt;
         }
     } else {
         // ---------------------------------------------------------------- epilogue: running state
@@ -341,13 +359,14 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
         bool ok = export_state(rev ? NC - 1 : 0);
         for (int it = 0; it < nchunks && ok; ++it) {
             const int c = chunk_of(it);
+            const float gcv = a.g[bh * NC + c];                 // loaded while the chunk's MMAs run
+            const float scl = rev ? a.zmax[bh * NC + c] : 1.f;
             if (abort_s || !(ok = mbar_wait(smem_u32(&bar_hfull), it & 1, a.status))) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const float dec = __expf(a.g[bh * NC + c]);
-            const float scl = rev ? a.zmax[bh * NC + c] : 1.f;
+            const float dec = __expf(gcv);
             if (rev) gam = it == 0 ? scl : fmaxf(gam, scl);
             const uint32_t hb = tmem + lane_base + TM_H + t * 80;
 #pragma unroll
