@@ -319,13 +319,13 @@ def run_tm2(args, world, rank, device):
     o = torch.empty(g["v"].shape, dtype=torch.float32, device=device)
     Z = torch.empty((B, H, T), dtype=torch.float32, device=device)
     grads = tuple(torch.empty(g[n].shape, dtype=torch.float32, device=device) for n in ("q", "k", "v", "a"))
-    wsf = torch.empty(tm2.forward_workspace_bytes(B, H, T, d, dv, C), dtype=torch.uint8, device=device)
-    wsb = torch.empty(tm2.backward_workspace_bytes(B, H, T, d, dv, C), dtype=torch.uint8, device=device)
+    # one workspace for both calls: the backward reads the chunk states the forward left in it
+    ws = torch.empty(tm2.workspace_bytes(B, H, T, d, dv, C), dtype=torch.uint8, device=device)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
 
     def step(q, k, v, a, dO):
-        tm2.forward(q, k, v, a, chunk=C, out=o, Z=Z, workspace=wsf)
-        tm2.backward(q, k, v, a, o, Z, dO, chunk=C, workspace=wsb, grads=grads)
+        tm2.forward(q, k, v, a, chunk=C, out=o, Z=Z, workspace=ws)
+        tm2.backward(q, k, v, a, o, Z, dO, chunk=C, workspace=ws, grads=grads, reuse_states=True)
 
     for _ in range(args.warmup):
         step(g["q"], g["k"], g["v"], g["a"], g["dO"])

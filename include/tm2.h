@@ -63,6 +63,12 @@ typedef enum { TM2_F32 = 0, TM2_BF16 = 1 } tm2_dtype;
 
 /* o = N / Z (the paper's "softmax normalisation", Sec. 5).  Without it o = N. */
 #define TM2_NORMALIZE 1u
+/* tm2_backward only: `ws` starts with the workspace of a tm2_forward call made with the same
+ * q, k, v, a, shapes, chunk, dtype and TM2_NORMALIZE setting and no initial state, and not
+ * modified since.  The backward then reads the decay sums and chunk states that forward
+ * left there instead of recomputing them.  (Allocate max(tm2_forward_workspace,
+ * tm2_backward_workspace) bytes and pass the same buffer to both calls.) */
+#define TM2_REUSE_STATES 2u
 
 /* Library version (major*10000 + minor*100 + patch). */
 int tm2_version(void);
@@ -99,7 +105,8 @@ size_t tm2_backward_workspace(int B, int H, int T, int d, int dv, int chunk, int
  * 2Mamba backward (App. C, C.1): gradients of sum(dO * o) w.r.t. q, k, v and the raw
  * A-mask input a, for a forward with no initial state.  o and Z are the forward's
  * outputs for the same inputs and flags (Z may be NULL when TM2_NORMALIZE is off).
- * o is the fp32 output of tm2_forward; dq, dk, dv, da are fp32.  The A-mask gradient is the row-axis sum minus the
+ * o is the fp32 output of tm2_forward; dq, dk, dv, da are fp32.  flags: TM2_NORMALIZE as in
+ * the forward, optionally TM2_REUSE_STATES.  The A-mask gradient is the row-axis sum minus the
  * column-axis sum of w_ij * dL/dw_ij, accumulated from the end of the sequence and
  * multiplied by d(-softplus(a))/da = -sigmoid(a).
  */
@@ -175,6 +182,10 @@ int tm2e_backward(const void* q, const void* k, const void* v, const float* a,
  * with the device (call it after the stream of interest has drained).
  */
 int tm2_poll_status(void);
+
+/* Text of the CUDA error behind the calling thread's last TM2_ERR_CUDA ("no CUDA error" if
+ * none).  Never NULL. */
+const char* tm2_last_cuda_error(void);
 
 /*
  * Self-test of the tensor-core building blocks (diagnostic; not part of the method).

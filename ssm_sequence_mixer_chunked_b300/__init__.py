@@ -20,11 +20,13 @@ import os
 import torch
 
 __all__ = ["forward", "backward", "step", "e_forward", "e_backward", "library_path",
-           "forward_workspace_bytes", "backward_workspace_bytes", "TM2Error", "NORMALIZE"]
+           "forward_workspace_bytes", "backward_workspace_bytes", "workspace_bytes", "TM2Error",
+           "NORMALIZE", "REUSE_STATES"]
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(PKG, "libtm2.so")
 NORMALIZE = 1
+REUSE_STATES = 2
 _DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 _lib = None
 
@@ -66,6 +68,7 @@ def _load():
     lib.tm2e_backward.restype = I
     lib.tm2e_backward.argtypes = [P] * 11 + [I] * 5 + [F, I, P, S, P]
     lib.tm2_poll_status.restype = I
+    lib.tm2_last_cuda_error.restype = ctypes.c_char_p
     _lib = lib
     return lib
 
@@ -81,7 +84,10 @@ def status_string(st: int) -> str:
 
 def _check(st: int):
     if st != 0:
-        raise TM2Error(status_string(st))
+        msg = status_string(st)
+        if st == -5:
+            msg += " (" + _load().tm2_last_cuda_error().decode() + ")"
+        raise TM2Error(msg)
 
 
 def _ptr(t):
@@ -128,6 +134,12 @@ def backward_workspace_bytes(B, H, T, d, dv, chunk=0, dtype=torch.bfloat16, norm
                                               NORMALIZE if normalize else 0))
 
 
+def workspace_bytes(B, H, T, d, dv, chunk=0, dtype=torch.bfloat16, normalize=True):
+    """Bytes of one workspace that serves a forward() and the backward() that reuses its states."""
+    return max(forward_workspace_bytes(B, H, T, d, dv, chunk, dtype, normalize),
+               backward_workspace_bytes(B, H, T, d, dv, chunk, dtype, normalize))
+
+
 def forward(q, k, v, a, *, normalize=True, chunk=0, S0=None, z0=None, return_state=False,
             out=None, Z=None, workspace=None, stream=None):
     """2Mamba forward.  Returns (o, Z) or, with return_state, (o, Z, S_final, z_final)."""
@@ -149,11 +161,16 @@ def forward(q, k, v, a, *, normalize=True, chunk=0, S0=None, z0=None, return_sta
 
 
 def backward(q, k, v, a, o, Z, dO, *, normalize=True, chunk=0, workspace=None, stream=None,
-             grads=None):
-    """2Mamba backward.  Returns (dq, dk, dv, da)."""
+             grads=None, reuse_states=False):
+    """2Mamba backward.  Returns (dq, dk, dv, da).  With reuse_states=True, `workspace` must
+    be the buffer the matching forward() call used (sized with workspace_bytes()); the chunk
+    states the forward left there are read instead of recomputed."""
     B, H, T, d, dv, dt = _seq_checks(q, k, v, a)
     L = _load()
-    flags = NORMALIZE if normalize else 0
+    flags = (NORMALIZE if normalize else 0) | (REUSE_STATES if reuse_states else 0)
+    if reuse_states and (workspace is None or workspace.numel() * workspace.element_size() <
+                         L.tm2_backward_workspace(B, H, T, d, dv, chunk, dt, flags)):
+        raise TM2Error("reuse_states needs the forward's workspace, sized with workspace_bytes()")
     if grads is None:
         grads = tuple(torch.empty(t.shape, dtype=torch.float32, device=q.device) for t in (q, k, v, a))
     dq, dk, dvv, da = grads

@@ -30,13 +30,13 @@ static bool aligned16(const void* p) { return p == nullptr || ((uintptr_t)p & 15
 // path (bf16 inputs, d = dv = 64, and only where `tc_available`); chunk 0 picks the
 // tensor-core path whenever it applies.
 static int make_problem(int B, int H, int T, int d, int dv, int chunk, int dtype, unsigned flags,
-                        Problem& p, bool tc_available = false) {
+                        Problem& p, bool tc_available = false, unsigned extra_flags = 0) {
     if (B < 0 || H < 0 || T < 0 || d <= 0 || dv <= 0) return TM2_ERR_INVALID_ARG;
     if (dtype != TM2_F32 && dtype != TM2_BF16) return TM2_ERR_UNSUPPORTED;
     if (d != dv || (d != 16 && d != 32 && d != 64)) return TM2_ERR_UNSUPPORTED;
     if (chunk != 0 && chunk != 64 && chunk != TC_CHUNK) return TM2_ERR_UNSUPPORTED;
     if ((long)B * H > 65535) return TM2_ERR_UNSUPPORTED;
-    if (flags & ~TM2_NORMALIZE) return TM2_ERR_INVALID_ARG;
+    if (flags & ~(TM2_NORMALIZE | extra_flags)) return TM2_ERR_INVALID_ARG;
     const bool tc_ok = tc_available && dtype == TM2_BF16 && d == 64 && dv == 64;
     if (chunk == TC_CHUNK && !tc_ok) return TM2_ERR_UNSUPPORTED;
     p.B = B; p.H = H; p.T = T; p.d = d; p.dv = dv;
@@ -72,11 +72,11 @@ static BwdWs plan_bwd(const Problem& p) {
     BwdWs w{};
     w.Aloc = c.take(sizeof(float) * p.BH() * p.Tp());
     w.g = c.take(sizeof(float) * p.BH() * p.NC);
-    if (p.tc) {
+    if (p.tc) {   // the prefix Aloc, g, states, zx is laid out exactly as plan_fwd's
         const size_t planes = 2 * 2 * (size_t)p.BH() * p.NC * 4096 * 64;   // two fp16 planes per slot
         w.states = c.take(planes);
-        w.dstates = c.take(planes);
         w.zx = c.take(sizeof(float) * (size_t)p.BH() * p.NC * 4096);
+        w.dstates = c.take(planes);
         w.dzx = c.take(sizeof(float) * (size_t)p.BH() * p.NC * 4096);
         w.sscale = c.take(sizeof(float) * (size_t)p.BH() * p.NC);
         w.zmax = c.take(sizeof(float) * (size_t)p.BH() * p.NC);
@@ -120,10 +120,15 @@ static int check_ws(void* ws, size_t ws_bytes, size_t need) {
     return TM2_OK;
 }
 
+static thread_local int g_last_cuda_error = 0;   // cudaError_t of the last TM2_ERR_CUDA
+
 #define TM2_CK(call)                                                   \
     do {                                                               \
         cudaError_t e_ = (call);                                       \
-        if (e_ != cudaSuccess) return TM2_ERR_CUDA;                    \
+        if (e_ != cudaSuccess) {                                       \
+            g_last_cuda_error = (int)e_;                               \
+            return TM2_ERR_CUDA;                                       \
+        }                                                              \
     } while (0)
 
 template <typename T>
@@ -237,7 +242,7 @@ int tm2_forward(const void* q, const void* k, const void* v, const float* a, con
 size_t tm2_backward_workspace(int B, int H, int T, int d, int dv, int chunk, int dtype,
                               unsigned flags) {
     Problem p;
-    if (make_problem(B, H, T, d, dv, chunk, dtype, flags, p, true) != TM2_OK) return 0;
+    if (make_problem(B, H, T, d, dv, chunk, dtype, flags, p, true, TM2_REUSE_STATES) != TM2_OK) return 0;
     return plan_bwd(p).total;
 }
 
@@ -246,8 +251,9 @@ int tm2_backward(const void* q, const void* k, const void* v, const float* a, co
                  int H, int T, int d, int dv_dim, int chunk, int dtype, unsigned flags, void* ws,
                  size_t ws_bytes, void* stream) {
     Problem p;
-    int st = make_problem(B, H, T, d, dv_dim, chunk, dtype, flags, p, true);
+    int st = make_problem(B, H, T, d, dv_dim, chunk, dtype, flags, p, true, TM2_REUSE_STATES);
     if (st != TM2_OK) return st;
+    const bool reuse = (flags & TM2_REUSE_STATES) != 0;
     if (p.BH() == 0 || T == 0) return TM2_OK;
     if (!q || !k || !v || !a || !o || !dO || !dq || !dk || !dv || !da) return TM2_ERR_INVALID_ARG;
     if (p.normalize && !Z) return TM2_ERR_INVALID_ARG;
@@ -271,10 +277,12 @@ int tm2_backward(const void* q, const void* k, const void* v, const float* a, co
         float* ucol = at<float>(ws, w.ucol);
         float* rowterm = at<float>(ws, w.rowterm);
         float* dcum = at<float>(ws, w.dcum);
-        TM2_RUN("decay_chunk", launch_decay(p, a, Aloc, g, s));
-        ScanIO f{};
-        f.rev = false; f.key = k; f.val = v; f.Aloc = Aloc; f.g = g; f.Sx = Sx; f.zx = zx;
-        TM2_RUN("tc_state_scan_fwd", tc_state_scan(p, f, s));
+        if (!reuse) {
+            TM2_RUN("decay_chunk", launch_decay(p, a, Aloc, g, s));
+            ScanIO f{};
+            f.rev = false; f.key = k; f.val = v; f.Aloc = Aloc; f.g = g; f.Sx = Sx; f.zx = zx;
+            TM2_RUN("tc_state_scan_fwd", tc_state_scan(p, f, s));
+        }
         TM2_RUN("tc_dy_prep", launch_tc_dy_prep(p, (const float*)o, Z, dO, Aloc, zeta, ucol, rowterm, zmax, s));
         ScanIO r{};
         r.rev = true; r.key = q; r.val = dO; r.Aloc = Aloc; r.g = g; r.zeta = zeta; r.ucol = ucol; r.zmax = zmax;
@@ -291,8 +299,10 @@ int tm2_backward(const void* q, const void* k, const void* v, const float* a, co
     float* dY = at<float>(ws, w.dY);
     float* rowterm = at<float>(ws, w.rowterm);
     float* dcum = at<float>(ws, w.dcum);
-    TM2_RUN("decay_chunk", launch_decay(p, a, Aloc, g, s));
-    TM2_RUN("state_scan_fwd", simt_state_scan_fwd(p, k, v, Aloc, g, nullptr, nullptr, states, nullptr, nullptr, s));
+    if (!reuse) {
+        TM2_RUN("decay_chunk", launch_decay(p, a, Aloc, g, s));
+        TM2_RUN("state_scan_fwd", simt_state_scan_fwd(p, k, v, Aloc, g, nullptr, nullptr, states, nullptr, nullptr, s));
+    }
     TM2_RUN("dy_prep", launch_dy_prep(p, o, Z, dO, dY, rowterm, s));
     TM2_RUN("state_scan_bwd", simt_state_scan_bwd(p, q, dY, Aloc, g, dstates, s));
     TM2_RUN("bwd_chunk", simt_bwd_chunk(p, q, k, v, Aloc, g, dY, rowterm, states, dstates, dq, dk, dv, dcum, s));
@@ -410,5 +420,9 @@ int tm2_trace_read(int i, char* name, int name_len, float* ms) {
 }
 
 int tm2_poll_status(void) { return tm2::read_tc_status(true); }
+
+const char* tm2_last_cuda_error(void) {
+    return g_last_cuda_error ? cudaGetErrorString((cudaError_t)g_last_cuda_error) : "no CUDA error";
+}
 
 }  // extern "C"

@@ -29,6 +29,11 @@ namespace tm2 {
 
 TM2_DEV uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
+// First 1024-byte boundary inside the dynamic shared-memory array.  The offset is applied
+// to the __shared__ pointer itself (no round trip through an integer), so the compiler keeps
+// the shared address space and emits shared-memory loads and stores, not generic ones.
+TM2_DEV uint8_t* smem_align1024(uint8_t* raw) { return raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u); }
+
 TM2_DEV uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -61,14 +66,26 @@ TM2_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// Same, but the thread may be suspended (not spinning, so it takes no issue slots from the
+// warps that are working) for up to `hint_ns` until the phase completes.
+TM2_DEV bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
 // Waits for the phase with the given parity to complete; gives up after `limit_ns`
 // nanoseconds, records TM2_ERR_TIMEOUT (-6) in *status (the device status word whose
-// address the host passes to every tensor-core kernel) and returns false.
+// address the host passes to every tensor-core kernel) and returns false.  Between polls
+// the waiting thread is suspended by the hardware rather than spinning.
 TM2_DEV bool mbar_wait(uint32_t bar, uint32_t parity, int* status, uint64_t limit_ns = 2000000000ull) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
         if (globaltimer_ns() - t0 > limit_ns) {
             atomicExch(status, -6);
             return false;

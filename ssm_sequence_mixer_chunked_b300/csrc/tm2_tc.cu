@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(128) umma_selftest_kernel(const __grid_constan
     constexpr uint32_t A_TMEM_COL = 256;
     constexpr int NA = (N + 63) / 64;   // 64-column blocks of an MN-major B
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t* smem = smem_align1024(smem_raw);
     const int KT = K / 64;
     const bool a_tma = mode == 0 || mode == 4;
     const bool a_tmem = mode == 3 || mode == 5;

@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_cons
                                                                const __grid_constant__ DqArgs a) {
     using namespace dqm;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t* smem = smem_align1024(smem_raw);
     __shared__ __align__(8) uint64_t bar_ld, bar_full[NS], bar_empty[NS], bar_cvt, bar_sfull[4], bar_sfree[4],
         bar_pfull[4], bar_pfree[4], bar_ufull[2], bar_uempty[2], bar_dqfull, bar_done;
     __shared__ uint32_t tmem_base_s;
@@ -369,7 +369,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
                                                                  const __grid_constant__ DkvArgs a) {
     using namespace kvm;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t* smem = smem_align1024(smem_raw);
     __shared__ __align__(8) uint64_t bar_ld, bar_full[NS], bar_empty[NS], bar_cvt, bar_sfull[4], bar_sfree[4],
         bar_pfull[4], bar_pfree[4], bar_ufull[2], bar_uempty[2], bar_kvfull, bar_red, bar_done;
     __shared__ uint32_t tmem_base_s;

@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
                                                                   const __grid_constant__ CUtensorMap tmS,
                                                                   const __grid_constant__ Args a) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t* smem = smem_align1024(smem_raw);
     __shared__ __align__(8) uint64_t bar_qkv, bar_full[NS], bar_empty[NS], bar_cvt, bar_sfull[NBLK], bar_sfree[NBLK],
         bar_pfull[NBLK], bar_pfree[NBLK], bar_ufull[2], bar_uempty[2], bar_yfull, bar_red, bar_done;
     __shared__ uint32_t tmem_base_s;

@@ -29,11 +29,14 @@
 // exports slot c divided by Gamma_c = max_{c' > c} zmax_{c'} (one value per slot, the same
 // in every CTA, recorded in `sscale`), so that the 1/Z factors cannot overflow fp16.
 //
-// Warp roles (576 threads): warps 0-7 build the A operand (warp w: tensor-memory lane
-// quadrant w % 4, half w / 4 of the 64 rows of a stage); warps 8-15 are the epilogue
-// (warp 8+e: tile e / 4, quadrant e % 4; one state row per thread); warp 16 issues the TMA
-// loads, warp 17 the MMAs.  Every mbarrier wait is bounded; on expiry the status word
-// records TM2_ERR_TIMEOUT and the CTA unwinds.
+// Warp roles (576 threads): warps 0-7 prepare each stage (a transposed fp16 copy of the key
+// tile, the key values of the CTA's four m, the weighted fp16 value tile and its normaliser
+// column) and then build the A operand from it (warp w: tensor-memory lane quadrant w % 4,
+// half w / 4 of the 64 rows of a stage); warps 8-15 fold the accumulator into the running
+// state once per chunk (warp 8+e: tile e / 4, quadrant e % 4; one state row per thread) and
+// export it; warp 16 issues the TMA loads, warp 17 the MMAs.
+// Every mbarrier wait is bounded; on expiry the status word records TM2_ERR_TIMEOUT and
+// the CTA unwinds.
 #include "tm2.h"
 #include "tm2_launch.h"
 #include "tm2_sm100.cuh"
@@ -55,8 +58,9 @@ constexpr int VAL_BYTES = 2 * KS * 128;      // value block + normaliser block (
 constexpr int SK_OFF = 0;
 constexpr int SV_OFF = SK_OFF + NS * KEY_BYTES;
 constexpr int SKW_OFF = SV_OFF + NS * VAL_BYTES;      // NS x [4][KS] fp16: key_j[4Q + m]
-constexpr int SW_OFF = SKW_OFF + NS * 4 * KS * 2;     // NS x [KS] fp32: w_j
-constexpr int SMEM_BYTES = SW_OFF + NS * KS * 4 + 1024;
+constexpr int KT_LD = 144;                            // bytes per row of the transposed key copy
+constexpr int SKT_OFF = SKW_OFF + NS * 4 * KS * 2;    // NS x [64 n][KS j] fp16, rows KT_LD apart
+constexpr int SMEM_BYTES = SKT_OFF + NS * 64 * KT_LD + 1024;
 constexpr uint32_t TM_H = 0;                 // accumulator: tile t at t * 80
 constexpr uint32_t TM_A = 160;               // A buffers: 160 + buf*128 + tile*64 + {0: hi, 32: lo}
 constexpr uint32_t TMEM_COLS = 512;
@@ -87,8 +91,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
                                                                    const __grid_constant__ CUtensorMap tmVal,
                                                                    const __grid_constant__ Args a) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    __shared__ __align__(8) uint64_t bar_full[NS], bar_empty[NS], bar_kw[NS], bar_afull[2], bar_aempty[2],
+    uint8_t* smem = smem_align1024(smem_raw);
+    __shared__ __align__(8) uint64_t bar_full[NS], bar_empty[NS], bar_prep[NS], bar_afull[2], bar_aempty[2],
         bar_hfull, bar_hempty, bar_done;
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_s;
@@ -105,7 +109,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
         for (int i = 0; i < NS; ++i) {
             mbar_init(smem_u32(&bar_full[i]), 1);
             mbar_init(smem_u32(&bar_empty[i]), 1);
-            mbar_init(smem_u32(&bar_kw[i]), NG_THREADS);
+            mbar_init(smem_u32(&bar_prep[i]), NG_THREADS);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&bar_afull[i]), NG_THREADS);
@@ -169,6 +173,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
                     const int gs = it * SPC + s, sb = gs % NS, ab = gs & 1;
                     if (abort_s) { ok = false; break; }
                     if (!(ok = mbar_wait(smem_u32(&bar_full[sb]), (gs / NS) & 1, a.status))) break;
+                    if (!(ok = mbar_wait(smem_u32(&bar_prep[sb]), (gs / NS) & 1, a.status))) break;
                     if (!(ok = mbar_wait(smem_u32(&bar_afull[ab]), (gs >> 1) & 1, a.status))) break;
                     tc_fence_after();
                     const uint32_t vb = sbase + SV_OFF + sb * VAL_BYTES;
@@ -192,82 +197,109 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
             mbar_wait(smem_u32(&bar_done), 0, a.status);
         }
     } else if (warp < 8) {
-        // ---------------------------------------------------------------- A-operand builders
+        // ---------------------------------------------------------------- stage preparation + A operand
         const int gt = threadIdx.x;                  // 0..255
         const int quad = warp & 3, h = warp >> 2;
         const int l = quad * 32 + lane;              // tensor-memory lane = tile row
         const int n = l & 63, moff = l >> 6;
-        const int km = gt >> 6, kj = gt & 63;        // kw-table entry written by this thread
-        // per-token scalars of stage gs (read by the threads with km == 0), loaded one stage
-        // ahead so that no global-memory latency sits between a stage's TMA and its MMA
-        struct Scal { float A, ze, uc, gc, zm; };
+        // preparation duties of this thread in every stage
+        const int et = gt;
+        const int j1 = et >> 3, j2 = j1 + 32;        // rows of its two 16-byte value pieces
+        const bool zw = (et & 7) == 0;               // writes the normaliser entries of j1, j2
+        const int km = et >> 6, kj = et & 63;        // key-table entry
+        const int tc_ = warp, tp = lane;                // transpose: column chunk, row pair
+        struct Scal { float A1, A2, z1, z2, u1, u2, gc, zm; };
         auto load_scal = [&](int gs) {
-            Scal r{0.f, 0.f, 0.f, 0.f, 1.f};
-            if (km != 0 || gs >= nstages) return r;
+            Scal v{0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 1.f};
+            if (gs >= nstages) return v;
             const int c = chunk_of(gs / SPC);
-            const long tok = (long)c * C + (gs % SPC) * KS + kj;
-            r.A = a.Aloc[bh * a.Tp + tok];
-            r.gc = a.g[bh * NC + c];
+            const long t1 = (long)c * C + (gs % SPC) * KS + j1, t2 = t1 + 32;
+            v.A1 = a.Aloc[bh * a.Tp + t1];
+            v.A2 = a.Aloc[bh * a.Tp + t2];
+            v.gc = a.g[bh * NC + c];
             if (rev) {
-                r.zm = a.zmax[bh * NC + c];
-                if (tok < a.T) {
-                    r.ze = a.zeta[bh * a.T + tok];
-                    r.uc = a.ucol[bh * a.T + tok];
+                v.zm = a.zmax[bh * NC + c];
+                if (t1 < a.T) { v.z1 = a.zeta[bh * a.T + t1]; v.u1 = a.ucol[bh * a.T + t1]; }
+                if (t2 < a.T) { v.z2 = a.zeta[bh * a.T + t2]; v.u2 = a.ucol[bh * a.T + t2]; }
+            }
+            return v;
+        };
+        // prepares stage gs in buffer gs % NS; returns false on an expired wait
+        auto prep = [&](int gs, const Scal& v) -> bool {
+            const int sb = gs % NS;
+            if (abort_s || !mbar_wait(smem_u32(&bar_full[sb]), (gs / NS) & 1, a.status)) return false;
+            const uint8_t* kt = smem + SK_OFF + sb * KEY_BYTES;
+            // weights of rows j1, j2 (<= 1) and their normaliser-column values
+            float w1, w2, c1 = 1.f, c2 = 1.f;
+            if (rev) {
+                w1 = __expf(v.A1) * v.z1 / v.zm;
+                w2 = __expf(v.A2) * v.z2 / v.zm;
+                c1 = v.u1;
+                c2 = v.u2;
+            } else {
+                w1 = __expf(v.gc - v.A1);
+                w2 = __expf(v.gc - v.A2);
+            }
+            const uint32_t vt = sbase + SV_OFF + sb * VAL_BYTES;
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {   // value pieces -> fp16(w_j val_j) in place
+                const uint32_t ad = vt + (et + u * 256) * 16;
+                const float w = u ? w2 : w1;
+                uint32_t x[4];
+                asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                             : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3])
+                             : "r"(ad));
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    x[i] = pack_f16x2(__uint_as_float(x[i] << 16) * w, __uint_as_float(x[i] & 0xFFFF0000u) * w);
+                st_shared_v4(ad, x[0], x[1], x[2], x[3]);
+            }
+            if (zw) {
+                uint8_t* zb = smem + SV_OFF + sb * VAL_BYTES + KEY_BYTES;
+                *reinterpret_cast<__half*>(zb + j1 * 128 + (j1 & 7) * 16) = __float2half_rn(w1 * c1);
+                *reinterpret_cast<__half*>(zb + j2 * 128 + (j2 & 7) * 16) = __float2half_rn(w2 * c2);
+            }
+            {   // key value of row kj at column 4Q + km, fp16
+                const int mm = 4 * Q + km;
+                reinterpret_cast<__half*>(smem + SKW_OFF + sb * 4 * KS * 2)[km * KS + kj] = __float2half_rn(__bfloat162float(
+                    *reinterpret_cast<const __nv_bfloat16*>(kt + kj * 128 + (((mm >> 3) ^ (kj & 7)) << 4) + (mm & 7) * 2)));
+            }
+            {   // transposed fp16 copy: rows 2tp, 2tp+1, columns 8tc_ .. 8tc_+7
+                const int ja = 2 * tp, jb2 = ja + 1;
+                uint32_t ra[4], rb[4];
+                asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                             : "=r"(ra[0]), "=r"(ra[1]), "=r"(ra[2]), "=r"(ra[3])
+                             : "r"(sbase + SK_OFF + sb * KEY_BYTES + ja * 128 + ((tc_ ^ (ja & 7)) << 4)));
+                asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                             : "=r"(rb[0]), "=r"(rb[1]), "=r"(rb[2]), "=r"(rb[3])
+                             : "r"(sbase + SK_OFF + sb * KEY_BYTES + jb2 * 128 + ((tc_ ^ (jb2 & 7)) << 4)));
+                const uint32_t dst = sbase + SKT_OFF + sb * 64 * KT_LD + (8 * tc_) * KT_LD + ja * 2;
+#pragma unroll
+                for (int q2 = 0; q2 < 4; ++q2) {
+                    // columns 8tc_ + 2q2 (low halves) and 8tc_ + 2q2 + 1 (high halves)
+                    const uint32_t lo = __byte_perm(ra[q2], rb[q2], 0x5410);
+                    const uint32_t hi = __byte_perm(ra[q2], rb[q2], 0x7632);
+                    asm volatile("st.shared.b32 [%0], %1;" ::"r"(dst + (2 * q2) * KT_LD), "r"(bf16x2_to_f16x2(lo)) : "memory");
+                    asm volatile("st.shared.b32 [%0], %1;" ::"r"(dst + (2 * q2 + 1) * KT_LD), "r"(bf16x2_to_f16x2(hi))
+                                 : "memory");
                 }
             }
-            return r;
+            fence_proxy_async();
+            mbar_arrive(smem_u32(&bar_prep[sb]));
+            return true;
         };
         Scal cur = load_scal(0);
         for (int gs = 0; gs < nstages; ++gs) {
             const int sb = gs % NS, ab = gs & 1;
             const Scal nxt = load_scal(gs + 1);
-            if (abort_s || !mbar_wait(smem_u32(&bar_full[sb]), (gs / NS) & 1, a.status)) {
+            if (!prep(gs, cur)) {
                 abort_s = 1;
                 break;
             }
-            const uint8_t* kt = smem + SK_OFF + sb * KEY_BYTES;
-            __half* kw = reinterpret_cast<__half*>(smem + SKW_OFF + sb * 4 * KS * 2);
-            float* sw = reinterpret_cast<float*>(smem + SW_OFF + sb * KS * 4);
-            {
-                const int j = kj, m = 4 * Q + km;
-                kw[km * KS + j] = __float2half_rn(__bfloat162float(
-                    *reinterpret_cast<const __nv_bfloat16*>(kt + j * 128 + (((m >> 3) ^ (j & 7)) << 4) + (m & 7) * 2)));
-                if (km == 0) {   // weight of this token, and its normaliser-column entry
-                    float w, zc;
-                    if (rev) {   // zeta = 0 past the end of the sequence
-                        w = __expf(cur.A) * cur.ze / cur.zm;
-                        zc = cur.uc;
-                    } else {
-                        w = __expf(cur.gc - cur.A);
-                        zc = 1.f;
-                    }
-                    sw[j] = w;
-                    *reinterpret_cast<__half*>(smem + SV_OFF + sb * VAL_BYTES + KEY_BYTES + j * 128 + (j & 7) * 16) =
-                        __float2half_rn(w * zc);
-                }
-            }
-            mbar_arrive(smem_u32(&bar_kw[sb]));
-            if (!mbar_wait(smem_u32(&bar_kw[sb]), (gs / NS) & 1, a.status)) {
+            cur = nxt;
+            if (abort_s || !mbar_wait(smem_u32(&bar_prep[sb]), (gs / NS) & 1, a.status)) {
                 abort_s = 1;
                 break;
-            }
-            {   // value tile -> fp16(w_j * val_j) in place (this thread's two 16-byte pieces)
-                const uint32_t vt = sbase + SV_OFF + sb * VAL_BYTES;
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int piece = gt + u * 256, j = piece >> 3;
-                    const uint32_t ad = vt + piece * 16;
-                    const float w = sw[j];
-                    uint32_t x[4];
-                    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                                 : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3])
-                                 : "r"(ad));
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        x[i] = pack_f16x2(__uint_as_float(x[i] << 16) * w, __uint_as_float(x[i] & 0xFFFF0000u) * w);
-                    st_shared_v4(ad, x[0], x[1], x[2], x[3]);
-                }
-                fence_proxy_async();
             }
             if (gs >= 2 && !mbar_wait(smem_u32(&bar_aempty[ab]), ((gs >> 1) - 1) & 1, a.status)) {
                 abort_s = 1;
@@ -276,15 +308,13 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
             tc_fence_after();
             // key_j[n] for this thread's 32 rows j of the stage, as fp16 pairs
             uint32_t kp[16];
+            const uint32_t kt = sbase + SKT_OFF + sb * 64 * KT_LD + n * KT_LD + h * 64;
 #pragma unroll
-            for (int p = 0; p < 16; ++p) {
-                const int j = h * 32 + 2 * p;
-                const uint16_t lo =
-                    *reinterpret_cast<const uint16_t*>(kt + j * 128 + (((n >> 3) ^ (j & 7)) << 4) + (n & 7) * 2);
-                const uint16_t hi = *reinterpret_cast<const uint16_t*>(kt + (j + 1) * 128 +
-                                                                       (((n >> 3) ^ ((j + 1) & 7)) << 4) + (n & 7) * 2);
-                kp[p] = bf16x2_to_f16x2((uint32_t)lo | ((uint32_t)hi << 16));
-            }
+            for (int v4 = 0; v4 < 4; ++v4)
+                asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                             : "=r"(kp[4 * v4]), "=r"(kp[4 * v4 + 1]), "=r"(kp[4 * v4 + 2]), "=r"(kp[4 * v4 + 3])
+                             : "r"(kt + v4 * 16));
+            const __half* kw = reinterpret_cast<const __half*>(smem + SKW_OFF + sb * 4 * KS * 2);
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
                 const uint4* kwp = reinterpret_cast<const uint4*>(kw + (2 * t + moff) * KS + h * 32);
@@ -311,10 +341,9 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(smem_u32(&bar_afull[ab]));
-            cur = nxt;
         }
     } else {
-        // ---------------------------------------------------------------- epilogue: running state
+        // ---------------------------------------------------------------- running state
         const int e = warp - 8, t = e >> 2, quad = e & 3;
         const int l = quad * 32 + lane;
         const int m = 4 * Q + 2 * t + (l >> 6), n = l & 63, r = m * 64 + n;
@@ -334,7 +363,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
         S[64] = (!rev && a.z0) ? a.z0[bh * 4096 + r] : 0.f;
         float gam = 1.f;   // reverse: running max of zmax over the chunks walked so far
         // exports the running state as two fp16 planes (divided by gam) plus fp32 z
-        auto export_state = [&](int slot) -> bool {
+        auto export_state = [&](int slot) {
             const float inv = 1.f / gam;
             if (a.sscale && Q == 0 && e == 0 && lane == 0) a.sscale[bh * NC + slot] = gam;
             __half* base = a.Sx + ((bh * NC + slot) * 2) * (4096L * 64) + (long)r * 64;
@@ -354,20 +383,12 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
                 dl[i] = make_uint4(pl[0], pl[1], pl[2], pl[3]);
             }
             a.zx[(bh * NC + slot) * 4096 + r] = S[64];
-            return true;
         };
-        bool ok = export_state(rev ? NC - 1 : 0);
-        for (int it = 0; it < nchunks && ok; ++it) {
-            const int c = chunk_of(it);
-            const float gcv = a.g[bh * NC + c];                 // loaded while the chunk's MMAs run
-            const float scl = rev ? a.zmax[bh * NC + c] : 1.f;
-            if (abort_s || !(ok = mbar_wait(smem_u32(&bar_hfull), it & 1, a.status))) {
-                ok = false;
-                break;
-            }
+        // folds the accumulator of chunk `it` into the running state
+        auto update = [&](int it, float gcv, float scl) -> bool {
+            if (abort_s || !mbar_wait(smem_u32(&bar_hfull), it & 1, a.status)) return false;
             tc_fence_after();
             const float dec = __expf(gcv);
-            if (rev) gam = it == 0 ? scl : fmaxf(gam, scl);
             const uint32_t hb = tmem + lane_base + TM_H + t * 80;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -379,8 +400,18 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
             S[64] = fmaf(dec, S[64], scl * tmem_ld1(hb + 64));
             tc_fence_before();
             mbar_arrive(smem_u32(&bar_hempty));
+            if (rev) gam = it == 0 ? scl : fmaxf(gam, scl);
+            return true;
+        };
+        export_state(rev ? NC - 1 : 0);
+        bool ok = true;
+        for (int it = 0; it < nchunks && ok; ++it) {
+            const int c = chunk_of(it);
+            const float gcv = a.g[bh * NC + c];                 // loaded while the chunk's MMAs run
+            const float scl = rev ? a.zmax[bh * NC + c] : 1.f;
+            if (!(ok = update(it, gcv, scl))) break;
             const int slot = rev ? c - 1 : c + 1;
-            if (slot >= 0 && slot < NC) ok = export_state(slot);
+            if (slot >= 0 && slot < NC) export_state(slot);
         }
         if (!ok) abort_s = 1;
         if (ok && !rev) {

@@ -59,6 +59,17 @@ def test_workspace_sizes(lib):
     assert lib.tm2e_forward_workspace(2, 16, 4096, 64, 64, bf16) > 0
 
 
+def test_reuse_states_flag(lib):
+    """TM2_REUSE_STATES (2) is a backward-only flag; the forward rejects it before launching,
+    and the backward workspace does not depend on it."""
+    bf16 = 1
+    assert lib.tm2_backward_workspace(2, 16, 8192, 64, 64, 0, bf16, 3) == \
+        lib.tm2_backward_workspace(2, 16, 8192, 64, 64, 0, bf16, 1) > 0
+    assert lib.tm2_forward_workspace(2, 16, 8192, 64, 64, 0, bf16, 3) == 0
+    assert fwd(lib, flags=3) == INVALID
+    assert lib.tm2_backward_workspace(2, 16, 8192, 64, 64, 0, bf16, 4) == 0   # unknown flag
+
+
 def fwd(lib, q=FAKE, k=FAKE, v=FAKE, a=FAKE, o=FAKE, Z=FAKE, B=1, H=2, T=256, d=16, dv=16,
         chunk=64, dtype=0, flags=1, ws=FAKE, ws_bytes=1 << 40):
     P = lambda x: None if x is None else ctypes.c_void_p(x)

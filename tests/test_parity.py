@@ -214,6 +214,22 @@ def test_bwd_chunk_invariance_bf16_d64(normalize):
             assert e <= 2e-2, (chunk, name, e)
 
 
+@pytest.mark.parametrize("chunk", [64, 256])
+def test_bwd_reuse_forward_states(chunk):
+    """TM2_REUSE_STATES: the backward reads the chunk states its forward left in the shared
+    workspace; the gradients are bitwise those of a backward that recomputes them."""
+    inp = si.sequence_inputs(2, 2, 700, 64, 64, dtype="bf16", qkv_std=0.125, seed=29, with_dO=True)
+    g = cuda(inp)
+    ws = torch.empty(tm2.workspace_bytes(2, 2, 700, 64, 64, chunk), dtype=torch.uint8, device="cuda")
+    o, Z = tm2.forward(g["q"], g["k"], g["v"], g["a"], chunk=chunk, workspace=ws)
+    reused = tm2.backward(g["q"], g["k"], g["v"], g["a"], o, Z, g["dO"], chunk=chunk, workspace=ws,
+                          reuse_states=True)
+    fresh = tm2.backward(g["q"], g["k"], g["v"], g["a"], o, Z, g["dO"], chunk=chunk)
+    torch.cuda.synchronize()
+    for x, y in zip(reused, fresh):
+        assert torch.equal(x, y)
+
+
 def test_fwd_bwd_bf16_B2_H16_T8192_sampled_heads():
     """fwd+bwd at B=2, H=16, T=8192, d=dv=64 bf16 on the whole batch; the oracle checks
     two full heads (all 8192 positions, all outputs and gradients)."""
