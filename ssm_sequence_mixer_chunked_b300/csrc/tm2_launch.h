@@ -57,12 +57,10 @@ constexpr int TC_CHUNK = 256;
 // Sx: [BH][NC][2][4096][64] fp16 (hi plane, residual plane); zx: [BH][NC][4096] fp32.
 struct ScanIO {
     bool rev;
-    const void* key;
-    const void* val;
-    const float* Aloc;
+    const void* Kt;        // operands from launch_tc_scan_operands
+    const void* WV;
+    const void* WZ;
     const float* g;
-    const float* zeta;     // reverse only
-    const float* ucol;     // reverse only
     const float* zmax;     // reverse only
     const float* S0;       // forward only, optional
     const float* z0;       // forward only, optional
@@ -73,6 +71,14 @@ struct ScanIO {
     float* z_final;        // forward only, optional
 };
 cudaError_t tc_state_scan(const Problem& p, const ScanIO& io, cudaStream_t s);
+
+// Operands of the chunk-state scan (tm2_scan.cu): Kt [BH][Tp/64][64][64] fp16 (each 64-token
+// block of the key, transposed), WV [BH][Tp][64] fp16 (w_t val_t), WZ [BH][Tp][64] fp16
+// (column 0: w_t zc_t).  Forward: key = k, val = v, w = exp(g_c - A_t), zc = 1.  Reverse:
+// key = q, val = dO, w = exp(A_t) zeta_t / zmax_c, zc = ucol_t.
+cudaError_t launch_tc_scan_operands(const Problem& p, bool rev, const void* key, const void* val, const float* Aloc,
+                                    const float* g, const float* zeta, const float* ucol, const float* zmax,
+                                    void* Kt, void* WV, void* WZ, cudaStream_t s);
 
 // Backward preparation: zeta = 1/Z (or 1), ucol = -dO.o (or 0), rowterm = 0 (or dO.o),
 // all (BH,T) fp32, and zmax (BH,NC) = per-chunk max of exp(A_i) zeta_i.

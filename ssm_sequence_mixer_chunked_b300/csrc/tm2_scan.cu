@@ -184,6 +184,96 @@ cudaError_t launch_tc_dy_prep(const Problem& p, const float* o, const float* Z, 
     return cudaGetLastError();
 }
 
+// Operands of the tensor-core chunk-state scan, one block of 256 threads per 64-token stage
+// of one (b, h):
+//   Kt[bh][stage][n][j] = fp16(key_j[n])                       (the stage's key block, transposed)
+//   WV[bh][t][col]      = fp16(w_t val_t[col])                 (the weighted value rows)
+//   WZ[bh][t][0]        = fp16(w_t zc_t), WZ[bh][t][1..63] = 0 (the normaliser column)
+// with the scan's weight w_t = exp(g_c - A_t), zc = 1 (forward walk) or
+// w_t = exp(A_t) zeta_t / zmax_c, zc = ucol_t (reverse walk); tokens past T give zeros.
+__global__ void __launch_bounds__(256) tc_scan_operands_kernel(
+    const __nv_bfloat16* __restrict__ key, const __nv_bfloat16* __restrict__ val, const float* __restrict__ Aloc,
+    const float* __restrict__ g, const float* __restrict__ zeta, const float* __restrict__ ucol,
+    const float* __restrict__ zmax, __half* __restrict__ Kt, __half* __restrict__ WV, __half* __restrict__ WZ,
+    int T, int C, int NC, int rev) {
+    __shared__ float sk[64][65];
+    __shared__ float sw[64], szc[64];
+    const int st = blockIdx.x, tid = threadIdx.x;
+    const long bh = blockIdx.y;
+    const int Tp = NC * C, c = (st * 64) / C;
+    const long t0 = (long)st * 64;
+    if (tid < 64) {
+        const long t = t0 + tid;
+        const float A = Aloc[bh * Tp + t];
+        float w = 0.f, zc = 0.f;
+        if (rev) {
+            if (t < T) {
+                w = __expf(A) * zeta[bh * T + t] / zmax[bh * NC + c];
+                zc = ucol[bh * T + t];
+            }
+        } else {
+            w = t < T ? __expf(g[bh * NC + c] - A) : 0.f;
+            zc = 1.f;
+        }
+        sw[tid] = w;
+        szc[tid] = zc;
+    }
+    for (int e = tid; e < 64 * 64; e += 256) {
+        const int j = e >> 6, n = e & 63;
+        const long t = t0 + j;
+        sk[j][n] = t < T ? __bfloat162float(key[(bh * T + t) * 64 + n]) : 0.f;
+    }
+    __syncthreads();
+    // transposed key block: thread writes 16 consecutive j of one row n
+    {
+        const int n = tid >> 2, j0 = (tid & 3) * 16;
+        uint32_t w[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const __half2 h2 = __floats2half2_rn(sk[j0 + 2 * u][n], sk[j0 + 2 * u + 1][n]);
+            w[u] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(Kt + ((bh * (Tp / 64) + st) * 64 + n) * 64 + j0);
+        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+    // weighted values and the normaliser column: thread writes 16 columns of one row
+    {
+        const int j = tid >> 2, c0 = (tid & 3) * 16;
+        const long t = t0 + j;
+        const float w = sw[j];
+        uint32_t x[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            float v0 = 0.f, v1 = 0.f;
+            if (t < T) {
+                v0 = __bfloat162float(val[(bh * T + t) * 64 + c0 + 2 * u]) * w;
+                v1 = __bfloat162float(val[(bh * T + t) * 64 + c0 + 2 * u + 1]) * w;
+            }
+            const __half2 h2 = __floats2half2_rn(v0, v1);
+            x[u] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+        uint4* dv = reinterpret_cast<uint4*>(WV + (bh * Tp + t) * 64 + c0);
+        dv[0] = make_uint4(x[0], x[1], x[2], x[3]);
+        dv[1] = make_uint4(x[4], x[5], x[6], x[7]);
+        const __half zh = __float2half_rn(c0 == 0 ? w * szc[j] : 0.f);
+        const uint32_t z0 = (uint32_t)(*reinterpret_cast<const uint16_t*>(&zh));
+        uint4* dz = reinterpret_cast<uint4*>(WZ + (bh * Tp + t) * 64 + c0);
+        dz[0] = make_uint4(z0, 0u, 0u, 0u);
+        dz[1] = make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
+cudaError_t launch_tc_scan_operands(const Problem& p, bool rev, const void* key, const void* val, const float* Aloc,
+                                    const float* g, const float* zeta, const float* ucol, const float* zmax,
+                                    void* Kt, void* WV, void* WZ, cudaStream_t s) {
+    dim3 grid((unsigned)(p.Tp() / 64), (unsigned)p.BH());
+    tc_scan_operands_kernel<<<grid, 256, 0, s>>>((const __nv_bfloat16*)key, (const __nv_bfloat16*)val, Aloc, g, zeta,
+                                                 ucol, zmax, (__half*)Kt, (__half*)WV, (__half*)WZ, p.T, p.C, p.NC,
+                                                 rev ? 1 : 0);
+    return cudaGetLastError();
+}
+
 template <typename Tin>
 __global__ void rowdot_kernel(const float* __restrict__ o, const Tin* __restrict__ dO,
                               float* __restrict__ out, long ntok, int dv) {

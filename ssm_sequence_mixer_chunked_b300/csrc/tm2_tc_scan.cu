@@ -29,12 +29,13 @@
 // exports slot c divided by Gamma_c = max_{c' > c} zmax_{c'} (one value per slot, the same
 // in every CTA, recorded in `sscale`), so that the 1/Z factors cannot overflow fp16.
 //
-// Warp roles (576 threads): warps 0-7 prepare each stage (a transposed fp16 copy of the key
-// tile, the key values of the CTA's four m, the weighted fp16 value tile and its normaliser
-// column) and then build the A operand from it (warp w: tensor-memory lane quadrant w % 4,
-// half w / 4 of the 64 rows of a stage); warps 8-15 fold the accumulator into the running
-// state once per chunk (warp 8+e: tile e / 4, quadrant e % 4; one state row per thread) and
-// export it; warp 16 issues the TMA loads, warp 17 the MMAs.
+// The operands come from a pre-pass (launch_tc_scan_operands): per 64-token stage the
+// transposed fp16 key block Kt[n][j], the weighted values fp16(w_j val_j) and the normaliser
+// column, all loaded by TMA.  Warp roles (576 threads): warps 0-7 build the A operand
+// straight from the Kt tile (warp w: tensor-memory lane quadrant w % 4, half w / 4 of the
+// 64 rows of a stage); warps 8-15 fold the accumulator into the running state once per chunk
+// (warp 8+e: tile e / 4, quadrant e % 4; one state row per thread) and export it; warp 16
+// issues the TMA loads, warp 17 the MMAs.
 // Every mbarrier wait is bounded; on expiry the status word records TM2_ERR_TIMEOUT and
 // the CTA unwinds.
 #include "tm2.h"
@@ -46,32 +47,24 @@ namespace tm2 {
 namespace tcscan {
 
 constexpr int C = TC_CHUNK;     // chunk length
-constexpr int KS = 64;          // key rows per stage
+constexpr int KS = 64;          // tokens per stage
 constexpr int SPC = C / KS;     // stages per chunk
 constexpr int NS = 4;           // stage buffers
 constexpr int NN = 80;          // MMA N
 constexpr int NG_THREADS = 256, NE_THREADS = 256;
 constexpr int WARP_TMA = 16, WARP_MMA = 17;
 constexpr int THREADS = 18 * 32;
-constexpr int KEY_BYTES = KS * 128;          // [KS][64] 16-bit, 128B-swizzled
-constexpr int VAL_BYTES = 2 * KS * 128;      // value block + normaliser block (MN-major)
-constexpr int SK_OFF = 0;
-constexpr int SV_OFF = SK_OFF + NS * KEY_BYTES;
-constexpr int SKW_OFF = SV_OFF + NS * VAL_BYTES;      // NS x [4][KS] fp16: key_j[4Q + m]
-constexpr int KT_LD = 144;                            // bytes per row of the transposed key copy
-constexpr int SKT_OFF = SKW_OFF + NS * 4 * KS * 2;    // NS x [64 n][KS j] fp16, rows KT_LD apart
-constexpr int SMEM_BYTES = SKT_OFF + NS * 64 * KT_LD + 1024;
-constexpr uint32_t TM_H = 0;                 // accumulator: tile t at t * 80
-constexpr uint32_t TM_A = 160;               // A buffers: 160 + buf*128 + tile*64 + {0: hi, 32: lo}
+constexpr int TILE = KS * 128;                // one [64][64] 16-bit tile, 128B-swizzled
+constexpr int STAGE = 3 * TILE;               // Kt, then the value block and the normaliser block
+constexpr int SMEM_BYTES = NS * STAGE + 1024;
+constexpr uint32_t TM_H = 0;                  // accumulator: tile t at t * 80
+constexpr uint32_t TM_A = 160;                // A buffers: 160 + buf*128 + tile*64 + {0: hi, 32: lo}
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t IDESC = idesc_f16_f32(128, NN, false, true);
 
 struct Args {
-    const float* Aloc;    // [BH][Tp] chunk-local running sums of -softplus(a)
     const float* g;       // [BH][NC] chunk totals
-    const float* zeta;    // reverse: [BH][T] 1/Z (or 1); forward: null
-    const float* ucol;    // reverse: [BH][T] -dO.o (or 0); forward: null (column of ones)
-    const float* zmax;    // reverse: [BH][NC] per-chunk max of exp(A_i) zeta_i; forward: null
+    const float* zmax;    // reverse: [BH][NC] weight scale of each chunk; forward: null
     const float* S0;      // forward: optional (BH, 4096, 64) fp32
     const float* z0;      // forward: optional (BH, 4096) fp32
     __half* Sx;           // [BH][NC][2][4096][64] fp16 planes (hi, lo), scaled by 1/sscale
@@ -87,13 +80,14 @@ struct Args {
 
 using namespace tcscan;
 
-__global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_constant__ CUtensorMap tmKey,
-                                                                   const __grid_constant__ CUtensorMap tmVal,
+__global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_constant__ CUtensorMap tmKt,
+                                                                   const __grid_constant__ CUtensorMap tmWV,
+                                                                   const __grid_constant__ CUtensorMap tmWZ,
                                                                    const __grid_constant__ Args a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_align1024(smem_raw);
-    __shared__ __align__(8) uint64_t bar_full[NS], bar_empty[NS], bar_prep[NS], bar_afull[2], bar_aempty[2],
-        bar_hfull, bar_hempty, bar_done;
+    __shared__ __align__(8) uint64_t bar_full[NS], bar_empty[NS], bar_afull[2], bar_aempty[2], bar_hfull,
+        bar_hempty, bar_done;
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_s;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -109,7 +103,6 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
         for (int i = 0; i < NS; ++i) {
             mbar_init(smem_u32(&bar_full[i]), 1);
             mbar_init(smem_u32(&bar_empty[i]), 1);
-            mbar_init(smem_u32(&bar_prep[i]), NG_THREADS);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&bar_afull[i]), NG_THREADS);
@@ -121,12 +114,6 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
         abort_s = 0;
         fence_mbar_init();
     }
-    // normaliser blocks of the value stages start at zero (the builders write column 0)
-    for (int e = threadIdx.x; e < NS * KS * 128 / 16; e += THREADS) {
-        const int sb = e / (KS * 8), off = (e % (KS * 8)) * 16;
-        st_shared_v4(sbase + SV_OFF + sb * VAL_BYTES + KEY_BYTES + off, 0, 0, 0, 0);
-    }
-    fence_proxy_async();
     if (warp == 0) {
         tmem_alloc(smem_u32(&tmem_base_s), TMEM_COLS);
         tmem_relinquish();
@@ -141,8 +128,9 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
     if (warp == WARP_TMA) {
         // ---------------------------------------------------------------- TMA producer
         if (lane == 0) {
-            prefetch_tmap(&tmKey);
-            prefetch_tmap(&tmVal);
+            prefetch_tmap(&tmKt);
+            prefetch_tmap(&tmWV);
+            prefetch_tmap(&tmWZ);
             int issued = 0;
             for (int gs = 0; gs < nstages && !abort_s; ++gs) {
                 const int sb = gs % NS;
@@ -151,11 +139,12 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
                     break;
                 }
                 const int c = chunk_of(gs / SPC), s = gs % SPC;
-                const int j0 = c * C + s * KS;
-                const uint32_t fb = smem_u32(&bar_full[sb]);
-                mbar_arrive_expect_tx(fb, KEY_BYTES + KS * 128);
-                tma_load_3d(sbase + SK_OFF + sb * KEY_BYTES, &tmKey, fb, 0, j0, (int)bh);
-                tma_load_3d(sbase + SV_OFF + sb * VAL_BYTES, &tmVal, fb, 0, j0, (int)bh);
+                const int stg = c * SPC + s;             // stage index within the sequence
+                const uint32_t fb = smem_u32(&bar_full[sb]), dst = sbase + sb * STAGE;
+                mbar_arrive_expect_tx(fb, STAGE);
+                tma_load_3d(dst, &tmKt, fb, 0, 0, (int)(bh * (a.Tp / KS) + stg));
+                tma_load_3d(dst + TILE, &tmWV, fb, 0, stg * KS, (int)bh);
+                tma_load_3d(dst + 2 * TILE, &tmWZ, fb, 0, stg * KS, (int)bh);
                 issued = gs + 1;
             }
             // wait for the last use of every stage buffer, so no copy is in flight at exit
@@ -173,15 +162,14 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
                     const int gs = it * SPC + s, sb = gs % NS, ab = gs & 1;
                     if (abort_s) { ok = false; break; }
                     if (!(ok = mbar_wait(smem_u32(&bar_full[sb]), (gs / NS) & 1, a.status))) break;
-                    if (!(ok = mbar_wait(smem_u32(&bar_prep[sb]), (gs / NS) & 1, a.status))) break;
                     if (!(ok = mbar_wait(smem_u32(&bar_afull[ab]), (gs >> 1) & 1, a.status))) break;
                     tc_fence_after();
-                    const uint32_t vb = sbase + SV_OFF + sb * VAL_BYTES;
+                    const uint32_t vb = sbase + sb * STAGE + TILE;
 #pragma unroll
                     for (int t = 0; t < 2; ++t)
 #pragma unroll
                         for (int kk = 0; kk < KS / 16; ++kk) {
-                            const uint64_t bd = sdesc_sw128_ex(vb + kk * 2048, KEY_BYTES, 1024);
+                            const uint64_t bd = sdesc_sw128_ex(vb + kk * 2048, TILE, 1024);
                             const uint32_t aa = tmem + TM_A + ab * 128 + t * 64 + kk * 8;
                             umma_bf16_ts(tmem + TM_H + t * 80, aa, bd, IDESC, (s > 0 || kk > 0) ? 1u : 0u);
                             umma_bf16_ts(tmem + TM_H + t * 80, aa + 32, bd, IDESC, 1u);
@@ -197,107 +185,13 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
             mbar_wait(smem_u32(&bar_done), 0, a.status);
         }
     } else if (warp < 8) {
-        // ---------------------------------------------------------------- stage preparation + A operand
-        const int gt = threadIdx.x;                  // 0..255
+        // ---------------------------------------------------------------- A-operand builders
         const int quad = warp & 3, h = warp >> 2;
         const int l = quad * 32 + lane;              // tensor-memory lane = tile row
         const int n = l & 63, moff = l >> 6;
-        // preparation duties of this thread in every stage
-        const int et = gt;
-        const int j1 = et >> 3, j2 = j1 + 32;        // rows of its two 16-byte value pieces
-        const bool zw = (et & 7) == 0;               // writes the normaliser entries of j1, j2
-        const int km = et >> 6, kj = et & 63;        // key-table entry
-        const int tc_ = warp, tp = lane;                // transpose: column chunk, row pair
-        struct Scal { float A1, A2, z1, z2, u1, u2, gc, zm; };
-        auto load_scal = [&](int gs) {
-            Scal v{0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 1.f};
-            if (gs >= nstages) return v;
-            const int c = chunk_of(gs / SPC);
-            const long t1 = (long)c * C + (gs % SPC) * KS + j1, t2 = t1 + 32;
-            v.A1 = a.Aloc[bh * a.Tp + t1];
-            v.A2 = a.Aloc[bh * a.Tp + t2];
-            v.gc = a.g[bh * NC + c];
-            if (rev) {
-                v.zm = a.zmax[bh * NC + c];
-                if (t1 < a.T) { v.z1 = a.zeta[bh * a.T + t1]; v.u1 = a.ucol[bh * a.T + t1]; }
-                if (t2 < a.T) { v.z2 = a.zeta[bh * a.T + t2]; v.u2 = a.ucol[bh * a.T + t2]; }
-            }
-            return v;
-        };
-        // prepares stage gs in buffer gs % NS; returns false on an expired wait
-        auto prep = [&](int gs, const Scal& v) -> bool {
-            const int sb = gs % NS;
-            if (abort_s || !mbar_wait(smem_u32(&bar_full[sb]), (gs / NS) & 1, a.status)) return false;
-            const uint8_t* kt = smem + SK_OFF + sb * KEY_BYTES;
-            // weights of rows j1, j2 (<= 1) and their normaliser-column values
-            float w1, w2, c1 = 1.f, c2 = 1.f;
-            if (rev) {
-                w1 = __expf(v.A1) * v.z1 / v.zm;
-                w2 = __expf(v.A2) * v.z2 / v.zm;
-                c1 = v.u1;
-                c2 = v.u2;
-            } else {
-                w1 = __expf(v.gc - v.A1);
-                w2 = __expf(v.gc - v.A2);
-            }
-            const uint32_t vt = sbase + SV_OFF + sb * VAL_BYTES;
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {   // value pieces -> fp16(w_j val_j) in place
-                const uint32_t ad = vt + (et + u * 256) * 16;
-                const float w = u ? w2 : w1;
-                uint32_t x[4];
-                asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                             : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3])
-                             : "r"(ad));
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    x[i] = pack_f16x2(__uint_as_float(x[i] << 16) * w, __uint_as_float(x[i] & 0xFFFF0000u) * w);
-                st_shared_v4(ad, x[0], x[1], x[2], x[3]);
-            }
-            if (zw) {
-                uint8_t* zb = smem + SV_OFF + sb * VAL_BYTES + KEY_BYTES;
-                *reinterpret_cast<__half*>(zb + j1 * 128 + (j1 & 7) * 16) = __float2half_rn(w1 * c1);
-                *reinterpret_cast<__half*>(zb + j2 * 128 + (j2 & 7) * 16) = __float2half_rn(w2 * c2);
-            }
-            {   // key value of row kj at column 4Q + km, fp16
-                const int mm = 4 * Q + km;
-                reinterpret_cast<__half*>(smem + SKW_OFF + sb * 4 * KS * 2)[km * KS + kj] = __float2half_rn(__bfloat162float(
-                    *reinterpret_cast<const __nv_bfloat16*>(kt + kj * 128 + (((mm >> 3) ^ (kj & 7)) << 4) + (mm & 7) * 2)));
-            }
-            {   // transposed fp16 copy: rows 2tp, 2tp+1, columns 8tc_ .. 8tc_+7
-                const int ja = 2 * tp, jb2 = ja + 1;
-                uint32_t ra[4], rb[4];
-                asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                             : "=r"(ra[0]), "=r"(ra[1]), "=r"(ra[2]), "=r"(ra[3])
-                             : "r"(sbase + SK_OFF + sb * KEY_BYTES + ja * 128 + ((tc_ ^ (ja & 7)) << 4)));
-                asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                             : "=r"(rb[0]), "=r"(rb[1]), "=r"(rb[2]), "=r"(rb[3])
-                             : "r"(sbase + SK_OFF + sb * KEY_BYTES + jb2 * 128 + ((tc_ ^ (jb2 & 7)) << 4)));
-                const uint32_t dst = sbase + SKT_OFF + sb * 64 * KT_LD + (8 * tc_) * KT_LD + ja * 2;
-#pragma unroll
-                for (int q2 = 0; q2 < 4; ++q2) {
-                    // columns 8tc_ + 2q2 (low halves) and 8tc_ + 2q2 + 1 (high halves)
-                    const uint32_t lo = __byte_perm(ra[q2], rb[q2], 0x5410);
-                    const uint32_t hi = __byte_perm(ra[q2], rb[q2], 0x7632);
-                    asm volatile("st.shared.b32 [%0], %1;" ::"r"(dst + (2 * q2) * KT_LD), "r"(bf16x2_to_f16x2(lo)) : "memory");
-                    asm volatile("st.shared.b32 [%0], %1;" ::"r"(dst + (2 * q2 + 1) * KT_LD), "r"(bf16x2_to_f16x2(hi))
-                                 : "memory");
-                }
-            }
-            fence_proxy_async();
-            mbar_arrive(smem_u32(&bar_prep[sb]));
-            return true;
-        };
-        Scal cur = load_scal(0);
         for (int gs = 0; gs < nstages; ++gs) {
             const int sb = gs % NS, ab = gs & 1;
-            const Scal nxt = load_scal(gs + 1);
-            if (!prep(gs, cur)) {
-                abort_s = 1;
-                break;
-            }
-            cur = nxt;
-            if (abort_s || !mbar_wait(smem_u32(&bar_prep[sb]), (gs / NS) & 1, a.status)) {
+            if (abort_s || !mbar_wait(smem_u32(&bar_full[sb]), (gs / NS) & 1, a.status)) {
                 abort_s = 1;
                 break;
             }
@@ -306,23 +200,24 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
                 break;
             }
             tc_fence_after();
+            const uint32_t kt = sbase + sb * STAGE;   // Kt tile: row n = key_j[n] over j, swizzled
             // key_j[n] for this thread's 32 rows j of the stage, as fp16 pairs
             uint32_t kp[16];
-            const uint32_t kt = sbase + SKT_OFF + sb * 64 * KT_LD + n * KT_LD + h * 64;
 #pragma unroll
             for (int v4 = 0; v4 < 4; ++v4)
                 asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
                              : "=r"(kp[4 * v4]), "=r"(kp[4 * v4 + 1]), "=r"(kp[4 * v4 + 2]), "=r"(kp[4 * v4 + 3])
-                             : "r"(kt + v4 * 16));
-            const __half* kw = reinterpret_cast<const __half*>(smem + SKW_OFF + sb * 4 * KS * 2);
+                             : "r"(kt + n * 128 + (((h * 4 + v4) ^ (n & 7)) << 4)));
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
-                const uint4* kwp = reinterpret_cast<const uint4*>(kw + (2 * t + moff) * KS + h * 32);
+                const int m = 4 * Q + 2 * t + moff;   // the same for the whole warp
                 uint32_t rh[16], rl[16];
 #pragma unroll
                 for (int v4 = 0; v4 < 4; ++v4) {
-                    const uint4 x = kwp[v4];
-                    const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+                    uint32_t xs[4];
+                    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                                 : "=r"(xs[0]), "=r"(xs[1]), "=r"(xs[2]), "=r"(xs[3])
+                                 : "r"(kt + m * 128 + (((h * 4 + v4) ^ (m & 7)) << 4)));
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const int p = v4 * 4 + i;
@@ -429,17 +324,19 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
 }
 
 cudaError_t tc_state_scan(const Problem& p, const ScanIO& io, cudaStream_t s) {
-    CUtensorMap tk, tv;
-    if (!make_tmap_bf16_3d(&tk, io.key, (uint64_t)p.BH(), (uint64_t)p.T, 64, KS)) return cudaErrorInvalidValue;
-    if (!make_tmap_bf16_3d(&tv, io.val, (uint64_t)p.BH(), (uint64_t)p.T, 64, KS)) return cudaErrorInvalidValue;
+    CUtensorMap tk, tv, tz;
+    const uint64_t BH = (uint64_t)p.BH(), Tp = (uint64_t)p.Tp();
+    if (!make_tmap_bf16_3d(&tk, io.Kt, BH * (Tp / KS), 64, 64, 64) || !make_tmap_bf16_3d(&tv, io.WV, BH, Tp, 64, KS) ||
+        !make_tmap_bf16_3d(&tz, io.WZ, BH, Tp, 64, KS))
+        return cudaErrorInvalidValue;
     int* status = tc_status_ptr();
     if (!status) return cudaErrorInvalidValue;
-    Args a{io.Aloc, io.g, io.zeta, io.ucol, io.zmax, io.S0, io.z0, (__half*)io.Sx, io.zx, io.sscale, io.S_final,
-           io.z_final, status, p.T, p.NC, (int)p.Tp(), io.rev ? 1 : 0};
+    Args a{io.g, io.zmax, io.S0, io.z0, (__half*)io.Sx, io.zx, io.sscale, io.S_final, io.z_final, status, p.T, p.NC,
+           (int)p.Tp(), io.rev ? 1 : 0};
     cudaError_t e = cudaFuncSetAttribute(tc_state_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     dim3 grid(16, (unsigned)p.BH());
-    tc_state_scan_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(tk, tv, a);
+    tc_state_scan_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(tk, tv, tz, a);
     return cudaGetLastError();
 }
 
