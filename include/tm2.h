@@ -37,7 +37,10 @@
  *  - The library allocates no device memory: scratch comes from the caller's
  *    workspace (`ws`, `ws_bytes` >= the matching *_workspace() size, 256-byte aligned).
  *  - Supported: d = dv in {16, 32, 64}; any T >= 0 (a ragged last chunk is handled);
- *    chunk in {0 (library choice), 64}.  Other values return TM2_ERR_UNSUPPORTED.
+ *    chunk in {0 (library choice), 64, 256}.  chunk 0 picks 256 (the tensor-core path)
+ *    for bf16 inputs with d = dv = 64 and 64 otherwise; 256 is accepted only where the
+ *    tensor-core path applies (bf16, d = dv = 64).  Other values return
+ *    TM2_ERR_UNSUPPORTED.
  *    B*H <= 65535 for the sequence entry points.
  */
 #ifndef TM2_H

@@ -50,7 +50,7 @@ static int make_problem(int B, int H, int T, int d, int dv, int chunk, int dtype
 
 static size_t state_floats(const Problem& p) { return (size_t)p.d * (p.dv + 1) * p.d; }
 
-struct FwdWs { size_t Aloc, g, states, zx, Kt, WV, WZ, total; };
+struct FwdWs { size_t Aloc, g, states, zx, ops, total; };
 static FwdWs plan_fwd(const Problem& p) {
     Carve c;
     FwdWs w{};
@@ -59,9 +59,7 @@ static FwdWs plan_fwd(const Problem& p) {
     if (p.tc) {   // fp16 value states [BH][NC][2][4096][64] + fp32 normaliser states [BH][NC][4096]
         w.states = c.take(2 * 2 * (size_t)p.BH() * p.NC * 4096 * 64);
         w.zx = c.take(sizeof(float) * (size_t)p.BH() * p.NC * 4096);
-        w.Kt = c.take(2 * (size_t)p.BH() * p.Tp() * 64);   // scan operands (scratch)
-        w.WV = c.take(2 * (size_t)p.BH() * p.Tp() * 64);
-        w.WZ = c.take(2 * (size_t)p.BH() * p.Tp() * 64);
+        w.ops = c.take(6 * (size_t)p.BH() * p.Tp() * 64);   // scan operand blocks (scratch)
     } else {
         w.states = c.take(sizeof(float) * p.BH() * p.NC * state_floats(p));
     }
@@ -69,7 +67,7 @@ static FwdWs plan_fwd(const Problem& p) {
     return w;
 }
 
-struct BwdWs { size_t Aloc, g, states, dstates, dY, rowterm, dcum, zx, dzx, sscale, zeta, ucol, zmax, Kt, WV, WZ, total; };
+struct BwdWs { size_t Aloc, g, states, dstates, dY, rowterm, dcum, zx, dzx, sscale, zeta, ucol, zmax, ops, total; };
 static BwdWs plan_bwd(const Problem& p) {
     Carve c;
     BwdWs w{};
@@ -87,9 +85,7 @@ static BwdWs plan_bwd(const Problem& p) {
         w.ucol = c.take(sizeof(float) * p.BH() * p.T);
         w.rowterm = c.take(sizeof(float) * p.BH() * p.T);
         w.dcum = c.take(sizeof(float) * p.BH() * p.T);
-        w.Kt = c.take(2 * (size_t)p.BH() * p.Tp() * 64);   // scan operands (scratch)
-        w.WV = c.take(2 * (size_t)p.BH() * p.Tp() * 64);
-        w.WZ = c.take(2 * (size_t)p.BH() * p.Tp() * 64);
+        w.ops = c.take(6 * (size_t)p.BH() * p.Tp() * 64);   // scan operand blocks (scratch)
         w.total = c.off;
         return w;
     }
@@ -233,13 +229,10 @@ int tm2_forward(const void* q, const void* k, const void* v, const float* a, con
     TM2_RUN("decay_chunk", launch_decay(p, a, Aloc, g, s));
     if (p.tc) {
         float* zx = at<float>(ws, w.zx);
-        void* Kt = at<void>(ws, w.Kt);
-        void* WV = at<void>(ws, w.WV);
-        void* WZ = at<void>(ws, w.WZ);
-        TM2_RUN("tc_scan_operands", launch_tc_scan_operands(p, false, k, v, Aloc, g, nullptr, nullptr, nullptr, Kt, WV,
-                                                            WZ, s));
+        void* ops = at<void>(ws, w.ops);
+        TM2_RUN("tc_scan_operands", launch_tc_scan_operands(p, false, k, v, Aloc, g, nullptr, nullptr, nullptr, ops, s));
         ScanIO io{};
-        io.rev = false; io.Kt = Kt; io.WV = WV; io.WZ = WZ; io.g = g; io.S0 = S0; io.z0 = z0;
+        io.rev = false; io.ops = ops; io.g = g; io.S0 = S0; io.z0 = z0;
         io.Sx = states; io.zx = zx; io.S_final = S_final; io.z_final = z_final;
         TM2_RUN("tc_state_scan_fwd", tc_state_scan(p, io, s));
         TM2_RUN("tc_chunk_out", tc_chunk_out(p, q, k, v, Aloc, states, zx, (float*)o, Z, s));
@@ -288,21 +281,19 @@ int tm2_backward(const void* q, const void* k, const void* v, const float* a, co
         float* ucol = at<float>(ws, w.ucol);
         float* rowterm = at<float>(ws, w.rowterm);
         float* dcum = at<float>(ws, w.dcum);
-        void* Kt = at<void>(ws, w.Kt);
-        void* WV = at<void>(ws, w.WV);
-        void* WZ = at<void>(ws, w.WZ);
+        void* ops = at<void>(ws, w.ops);
         if (!reuse) {
             TM2_RUN("decay_chunk", launch_decay(p, a, Aloc, g, s));
-            TM2_RUN("tc_scan_operands", launch_tc_scan_operands(p, false, k, v, Aloc, g, nullptr, nullptr, nullptr, Kt,
-                                                                WV, WZ, s));
+            TM2_RUN("tc_scan_operands", launch_tc_scan_operands(p, false, k, v, Aloc, g, nullptr, nullptr, nullptr, ops,
+                                                                s));
             ScanIO f{};
-            f.rev = false; f.Kt = Kt; f.WV = WV; f.WZ = WZ; f.g = g; f.Sx = Sx; f.zx = zx;
+            f.rev = false; f.ops = ops; f.g = g; f.Sx = Sx; f.zx = zx;
             TM2_RUN("tc_state_scan_fwd", tc_state_scan(p, f, s));
         }
         TM2_RUN("tc_dy_prep", launch_tc_dy_prep(p, (const float*)o, Z, dO, Aloc, zeta, ucol, rowterm, zmax, s));
-        TM2_RUN("tc_scan_operands", launch_tc_scan_operands(p, true, q, dO, Aloc, g, zeta, ucol, zmax, Kt, WV, WZ, s));
+        TM2_RUN("tc_scan_operands", launch_tc_scan_operands(p, true, q, dO, Aloc, g, zeta, ucol, zmax, ops, s));
         ScanIO r{};
-        r.rev = true; r.Kt = Kt; r.WV = WV; r.WZ = WZ; r.g = g; r.zmax = zmax;
+        r.rev = true; r.ops = ops; r.g = g; r.zmax = zmax;
         r.Sx = dSx; r.zx = dzx; r.sscale = sscale;
         TM2_RUN("tc_state_scan_bwd", tc_state_scan(p, r, s));
         TM2_RUN("tc_bwd_dq", tc_bwd_dq(p, q, k, v, dO, Aloc, zeta, ucol, Sx, zx, (float*)dq, s));

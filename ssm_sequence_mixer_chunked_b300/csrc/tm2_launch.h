@@ -57,9 +57,7 @@ constexpr int TC_CHUNK = 256;
 // Sx: [BH][NC][2][4096][64] fp16 (hi plane, residual plane); zx: [BH][NC][4096] fp32.
 struct ScanIO {
     bool rev;
-    const void* Kt;        // operands from launch_tc_scan_operands
-    const void* WV;
-    const void* WZ;
+    const void* ops;       // operand blocks from launch_tc_scan_operands
     const float* g;
     const float* zmax;     // reverse only
     const float* S0;       // forward only, optional
@@ -72,13 +70,16 @@ struct ScanIO {
 };
 cudaError_t tc_state_scan(const Problem& p, const ScanIO& io, cudaStream_t s);
 
-// Operands of the chunk-state scan (tm2_scan.cu): Kt [BH][Tp/64][64][64] fp16 (each 64-token
-// block of the key, transposed), WV [BH][Tp][64] fp16 (w_t val_t), WZ [BH][Tp][64] fp16
-// (column 0: w_t zc_t).  Forward: key = k, val = v, w = exp(g_c - A_t), zc = 1.  Reverse:
-// key = q, val = dO, w = exp(A_t) zeta_t / zmax_c, zc = ucol_t.
+// Operands of the chunk-state scan (tm2_scan.cu): ops [BH][Tp/64][192][64] fp16, one block
+// per 64-token stage (so that one TMA request brings whole stages): rows 0-63 the key block
+// transposed (row n = key_t[n] over the stage's tokens t), rows 64-127 w_t val_t (row = token),
+// rows 128-191 column 0 = w_t zc_t, the rest zero.  Forward: key = k, val = v,
+// w = exp(g_c - A_t), zc = 1.  Reverse: key = q, val = dO, w = exp(A_t) zeta_t / zmax_c,
+// zc = ucol_t.
+constexpr int TC_OPS_ROWS = 192;
 cudaError_t launch_tc_scan_operands(const Problem& p, bool rev, const void* key, const void* val, const float* Aloc,
                                     const float* g, const float* zeta, const float* ucol, const float* zmax,
-                                    void* Kt, void* WV, void* WZ, cudaStream_t s);
+                                    void* ops, cudaStream_t s);
 
 // Backward preparation: zeta = 1/Z (or 1), ucol = -dO.o (or 0), rowterm = 0 (or dO.o),
 // all (BH,T) fp32, and zmax (BH,NC) = per-chunk max of exp(A_i) zeta_i.

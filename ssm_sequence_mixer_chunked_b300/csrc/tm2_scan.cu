@@ -185,17 +185,16 @@ cudaError_t launch_tc_dy_prep(const Problem& p, const float* o, const float* Z, 
 }
 
 // Operands of the tensor-core chunk-state scan, one block of 256 threads per 64-token stage
-// of one (b, h):
-//   Kt[bh][stage][n][j] = fp16(key_j[n])                       (the stage's key block, transposed)
-//   WV[bh][t][col]      = fp16(w_t val_t[col])                 (the weighted value rows)
-//   WZ[bh][t][0]        = fp16(w_t zc_t), WZ[bh][t][1..63] = 0 (the normaliser column)
+// of one (b, h), written as one [192][64] fp16 block per stage (token j = stage*64 + row):
+//   rows   0-63 : [n][j]   = fp16(key_j[n])                      (the key block, transposed)
+//   rows  64-127: [j][col] = fp16(w_j val_j[col])                (the weighted value rows)
+//   rows 128-191: [j][0]   = fp16(w_j zc_j), [j][1..63] = 0      (the normaliser column)
 // with the scan's weight w_t = exp(g_c - A_t), zc = 1 (forward walk) or
 // w_t = exp(A_t) zeta_t / zmax_c, zc = ucol_t (reverse walk); tokens past T give zeros.
 __global__ void __launch_bounds__(256) tc_scan_operands_kernel(
     const __nv_bfloat16* __restrict__ key, const __nv_bfloat16* __restrict__ val, const float* __restrict__ Aloc,
     const float* __restrict__ g, const float* __restrict__ zeta, const float* __restrict__ ucol,
-    const float* __restrict__ zmax, __half* __restrict__ Kt, __half* __restrict__ WV, __half* __restrict__ WZ,
-    int T, int C, int NC, int rev) {
+    const float* __restrict__ zmax, __half* __restrict__ ops, int T, int C, int NC, int rev) {
     __shared__ float sk[64][65];
     __shared__ float sw[64], szc[64];
     const int st = blockIdx.x, tid = threadIdx.x;
@@ -224,6 +223,7 @@ __global__ void __launch_bounds__(256) tc_scan_operands_kernel(
         sk[j][n] = t < T ? __bfloat162float(key[(bh * T + t) * 64 + n]) : 0.f;
     }
     __syncthreads();
+    __half* blk = ops + (bh * (Tp / 64) + st) * (long)(TC_OPS_ROWS * 64);
     // transposed key block: thread writes 16 consecutive j of one row n
     {
         const int n = tid >> 2, j0 = (tid & 3) * 16;
@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(256) tc_scan_operands_kernel(
             const __half2 h2 = __floats2half2_rn(sk[j0 + 2 * u][n], sk[j0 + 2 * u + 1][n]);
             w[u] = *reinterpret_cast<const uint32_t*>(&h2);
         }
-        uint4* dst = reinterpret_cast<uint4*>(Kt + ((bh * (Tp / 64) + st) * 64 + n) * 64 + j0);
+        uint4* dst = reinterpret_cast<uint4*>(blk + n * 64 + j0);
         dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
         dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
     }
@@ -253,12 +253,12 @@ __global__ void __launch_bounds__(256) tc_scan_operands_kernel(
             const __half2 h2 = __floats2half2_rn(v0, v1);
             x[u] = *reinterpret_cast<const uint32_t*>(&h2);
         }
-        uint4* dv = reinterpret_cast<uint4*>(WV + (bh * Tp + t) * 64 + c0);
+        uint4* dv = reinterpret_cast<uint4*>(blk + (64 + j) * 64 + c0);
         dv[0] = make_uint4(x[0], x[1], x[2], x[3]);
         dv[1] = make_uint4(x[4], x[5], x[6], x[7]);
         const __half zh = __float2half_rn(c0 == 0 ? w * szc[j] : 0.f);
         const uint32_t z0 = (uint32_t)(*reinterpret_cast<const uint16_t*>(&zh));
-        uint4* dz = reinterpret_cast<uint4*>(WZ + (bh * Tp + t) * 64 + c0);
+        uint4* dz = reinterpret_cast<uint4*>(blk + (128 + j) * 64 + c0);
         dz[0] = make_uint4(z0, 0u, 0u, 0u);
         dz[1] = make_uint4(0u, 0u, 0u, 0u);
     }
@@ -266,11 +266,10 @@ __global__ void __launch_bounds__(256) tc_scan_operands_kernel(
 
 cudaError_t launch_tc_scan_operands(const Problem& p, bool rev, const void* key, const void* val, const float* Aloc,
                                     const float* g, const float* zeta, const float* ucol, const float* zmax,
-                                    void* Kt, void* WV, void* WZ, cudaStream_t s) {
+                                    void* ops, cudaStream_t s) {
     dim3 grid((unsigned)(p.Tp() / 64), (unsigned)p.BH());
     tc_scan_operands_kernel<<<grid, 256, 0, s>>>((const __nv_bfloat16*)key, (const __nv_bfloat16*)val, Aloc, g, zeta,
-                                                 ucol, zmax, (__half*)Kt, (__half*)WV, (__half*)WZ, p.T, p.C, p.NC,
-                                                 rev ? 1 : 0);
+                                                 ucol, zmax, (__half*)ops, p.T, p.C, p.NC, rev ? 1 : 0);
     return cudaGetLastError();
 }
 

@@ -93,6 +93,26 @@ TM2_DEV bool mbar_wait(uint32_t bar, uint32_t parity, int* status, uint64_t limi
     }
 }
 
+// Group wait: one warp of a role group (`leader`) waits on the mbarrier (bounded), the rest
+// of the group sleeps on hardware named barrier `bid` (nthr threads) instead of polling.
+// The leader publishes the outcome in flags[k & 1] before the named barrier, so every
+// thread of the group takes the same decision (no thread can be left behind at a later
+// named barrier).  k counts the calls of this group; it must advance identically in all
+// of its threads.  Ends with tcgen05.fence::after_thread_sync, so tensor-memory results the
+// barrier announced may be read right away.
+TM2_DEV bool group_wait(uint32_t bar, uint32_t parity, int* status, bool leader, uint32_t bid, uint32_t nthr,
+                        volatile int* flags, int& k, volatile int* abort_flag) {
+    if (leader) {
+        const bool ok = !*abort_flag && mbar_wait(bar, parity, status);
+        if ((threadIdx.x & 31) == 0) flags[k & 1] = ok ? 1 : 0;
+    }
+    named_bar_sync(bid, nthr);
+    const bool ok = flags[k & 1] != 0;
+    ++k;
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    return ok;
+}
+
 // ---- TMA -------------------------------------------------------------------------------
 TM2_DEV void tma_load_2d(uint32_t dst, const void* tmap, uint32_t bar, int x, int y) {
     asm volatile(
@@ -112,11 +132,27 @@ TM2_DEV void tma_load_4d(uint32_t dst, const void* tmap, uint32_t bar, int x, in
         "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w)
         : "memory");
 }
+TM2_DEV void tma_load_5d(uint32_t dst, const void* tmap, uint32_t bar, int x, int y, int z, int w, int v) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+        "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w), "r"(v)
+        : "memory");
+}
 TM2_DEV void tma_load_3d_hint(uint32_t dst, const void* tmap, uint32_t bar, int x, int y, int z, uint64_t policy) {
     asm volatile(
         "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
         "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z), "l"(policy)
         : "memory");
+}
+// Bring a tile into L2 ahead of its TMA load (no shared memory, no barrier).
+TM2_DEV void tma_prefetch_3d(const void* tmap, int x, int y, int z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(tmap), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+TM2_DEV void tma_prefetch_4d(const void* tmap, int x, int y, int z, int w) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(tmap), "r"(x), "r"(y),
+                 "r"(z), "r"(w)
+                 : "memory");
 }
 TM2_DEV void prefetch_tmap(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
@@ -199,6 +235,22 @@ TM2_DEV void tmem_ld16(uint32_t taddr, float* v) {
 }
 
 // 32 lanes x 8 consecutive 32-bit columns from 8 registers per thread (no wait).
+// 32 lanes x 32 consecutive columns -> 32 registers per thread (load and wait in one statement).
+TM2_DEV void tmem_ld32(uint32_t taddr, float* v) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
 TM2_DEV void tmem_st8(uint32_t taddr, const uint32_t* r) {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
                  "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])

@@ -29,70 +29,24 @@
 #include "tm2_launch.h"
 #include "tm2_sm100.cuh"
 #include "tm2_tc.h"
+#include "tm2_tc_tiles.cuh"
 
 namespace tm2 {
 namespace tcbwd {
+using namespace tctile;
 
 constexpr int C = TC_CHUNK;
 constexpr int THREADS = 10 * 32;
 constexpr int WARP_TMA = 8, WARP_MMA = 9;
-constexpr int NS = 3;                         // state-slice stages (hi + lo plane, 16 KB)
+constexpr int NP = 5;                         // stages of two state slices (hi + lo planes, 32 KB)
+constexpr int NP_EARLY = 2;                   // stages free from the start; the rest alias the
+                                              // intra-chunk tiles and open once those are done
+constexpr int PBYTES = 32768;
 constexpr int NSL = 65;                       // 64 state slices + the normaliser slice
 constexpr uint32_t IDESC_BF_K = idesc_bf16_f32(128, 64, false, false);
 constexpr uint32_t IDESC_BF_MN = idesc_bf16_f32(128, 64, false, true);
 constexpr uint32_t IDESC_H_K = idesc_f16_f32(128, 64, false, false);
 constexpr uint32_t IDESC_H_MN = idesc_f16_f32(128, 64, false, true);
-
-// 16-byte piece `piece` of a [rows][64] 16-bit swizzled tile: bf16 -> fp16 into another tile
-TM2_DEV void tile_bf16_to_f16(uint32_t src, uint32_t dst, int piece) {
-    uint32_t x[4];
-    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]) : "r"(src + piece * 16));
-    st_shared_v4(dst + piece * 16, bf16x2_to_f16x2(x[0]), bf16x2_to_f16x2(x[1]), bf16x2_to_f16x2(x[2]),
-                 bf16x2_to_f16x2(x[3]));
-}
-// element (row, col) of a [rows][64] 16-bit swizzled tile
-TM2_DEV uint32_t swz_elem(int row, int col) { return row * 128 + ((((col >> 3) ^ (row & 7))) << 4) + (col & 7) * 2; }
-// the 64 x 64 normaliser matrix zm[m][n] = scale * z[m*64 + n] as hi + lo fp16 K-major tiles
-TM2_DEV void build_z_tiles(uint8_t* hi, uint8_t* lo, const float* __restrict__ z, float scale, int t256) {
-    for (int pc = t256; pc < 512; pc += 256) {
-        const int m = pc >> 3, k8 = pc & 7;
-        const float4 a0 = *reinterpret_cast<const float4*>(z + m * 64 + k8 * 8);
-        const float4 a1 = *reinterpret_cast<const float4*>(z + m * 64 + k8 * 8 + 4);
-        const float v[8] = {a0.x * scale, a0.y * scale, a0.z * scale, a0.w * scale,
-                            a1.x * scale, a1.y * scale, a1.z * scale, a1.w * scale};
-        uint32_t h[4], l[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            h[u] = pack_f16x2(v[2 * u], v[2 * u + 1]);
-            const __half2 h2 = *reinterpret_cast<const __half2*>(&h[u]);
-            l[u] = pack_f16x2(v[2 * u] - __low2float(h2), v[2 * u + 1] - __high2float(h2));
-        }
-        const uint32_t off = m * 128 + ((k8 ^ (m & 7)) << 4);
-        st_shared_v4(smem_u32(hi) + off, h[0], h[1], h[2], h[3]);
-        st_shared_v4(smem_u32(lo) + off, l[0], l[1], l[2], l[3]);
-    }
-}
-
-struct DqArgs {
-    const float* Aloc;   // [BH][Tp]
-    const float* zeta;   // [BH][T]
-    const float* ucol;   // [BH][T]
-    const float* zx;     // [BH][NC][4096] forward normaliser states (slot c = entering chunk c)
-    float* dq;           // [BH][T][64]
-    int* status;
-    int T, NC, Tp;
-};
-
-// ---- shared-memory map of the dq kernel
-namespace dqm {
-constexpr int SQ = 0, SQH = 16384, SD = 32768, SDH = 49152;      // [128][64] tiles
-constexpr int SK = 65536, SV = 98304;                              // [256][64] tiles
-constexpr int SZH = 131072, SZL = 139264;                          // normaliser matrix hi / lo
-constexpr int STG = 147456;                                        // NS x (hi 8 KB + lo 8 KB)
-constexpr int SAV = STG + NS * 16384;                              // 256 floats
-constexpr int BYTES = SAV + 1024 + 1024;
-constexpr uint32_t TM_DQ = 0, TM_S = 64, TM_W = 128, TM_PH = 192, TM_PL = 224, TM_U = 256;   // U: 256 + 64*buf
-}  // namespace dqm
 
 struct DkvArgs {
     const float* Aloc;    // [BH][Tp]
@@ -110,11 +64,12 @@ struct DkvArgs {
 };
 
 namespace kvm {
-constexpr int SK = 0, SKH = 16384, SV = 32768, SVH = 49152;       // [128][64] tiles (keys of this tile)
-constexpr int SQ = 65536, SD = 98304;                              // [256][64] tiles (whole chunk)
-constexpr int SZH = 131072, SZL = 139264;
-constexpr int STG = 147456;
-constexpr int SAV = STG + NS * 16384;                              // A, zeta, ucol: 3 x 256 floats
+constexpr int STG = 0;                                             // NP x [plane][slice n, n+1][64][64]
+constexpr int SK = 65536, SV = 81920;                              // [128][64] bf16 tiles (stage 2)
+constexpr int SQ = 98304, SD = 131072;                             // [256][64] bf16 tiles (stages 3-4)
+constexpr int SKH = 163840, SVH = 180224;                          // [128][64] fp16 copies
+constexpr int SZH = 196608, SZL = 204800;
+constexpr int SAV = 212992;                                        // A, zeta, ucol: 3 x 256 floats
 constexpr int SRED = SAV + 3072;                                   // 2 x 128 partial sums
 constexpr int BYTES = SRED + 1024 + 1024;
 constexpr uint32_t TM_DK = 0, TM_DV = 64, TM_S = 128, TM_W = 192, TM_DH = 256, TM_DL = 288, TM_WH = 320, TM_WL = 352;
@@ -125,242 +80,6 @@ constexpr uint32_t TM_U0 = 128, TM_U1 = 384;                       // U at +0, U
 
 using namespace tcbwd;
 
-__global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ,
-                                                               const __grid_constant__ CUtensorMap tmD,
-                                                               const __grid_constant__ CUtensorMap tmK,
-                                                               const __grid_constant__ CUtensorMap tmV,
-                                                               const __grid_constant__ CUtensorMap tmS,
-                                                               const __grid_constant__ DqArgs a) {
-    using namespace dqm;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = smem_align1024(smem_raw);
-    __shared__ __align__(8) uint64_t bar_ld, bar_full[NS], bar_empty[NS], bar_cvt, bar_sfull[4], bar_sfree[4],
-        bar_pfull[4], bar_pfree[4], bar_ufull[2], bar_uempty[2], bar_dqfull, bar_done;
-    __shared__ uint32_t tmem_base_s;
-    __shared__ volatile int abort_s;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int it = blockIdx.x & 1, c = blockIdx.x >> 1;
-    const long bh = blockIdx.y;
-    const int NC = a.NC;
-    const int nblk = 2 * (it + 1);               // 64-key blocks at or before this tile
-    const uint32_t sb0 = smem_u32(smem);
-    float* sAv = reinterpret_cast<float*>(smem + SAV);
-
-    if (threadIdx.x == 0) {
-        mbar_init(smem_u32(&bar_ld), 1);
-        for (int i = 0; i < NS; ++i) {
-            mbar_init(smem_u32(&bar_full[i]), 1);
-            mbar_init(smem_u32(&bar_empty[i]), 1);
-        }
-        mbar_init(smem_u32(&bar_cvt), 256);
-        for (int b = 0; b < 4; ++b) {
-            mbar_init(smem_u32(&bar_sfull[b]), 1);
-            mbar_init(smem_u32(&bar_sfree[b]), 256);
-            mbar_init(smem_u32(&bar_pfull[b]), 256);
-            mbar_init(smem_u32(&bar_pfree[b]), 1);
-        }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(smem_u32(&bar_ufull[i]), 1);
-            mbar_init(smem_u32(&bar_uempty[i]), 256);
-        }
-        mbar_init(smem_u32(&bar_dqfull), 1);
-        mbar_init(smem_u32(&bar_done), 1);
-        abort_s = 0;
-        fence_mbar_init();
-    }
-    for (int j = threadIdx.x; j < C; j += THREADS) sAv[j] = a.Aloc[bh * a.Tp + (long)c * C + j];
-    if (warp == 0) {
-        tmem_alloc(smem_u32(&tmem_base_s), 512);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = tmem_base_s;
-
-    if (warp == WARP_TMA) {
-        if (lane == 0) {
-            prefetch_tmap(&tmS);
-            const uint32_t lb = smem_u32(&bar_ld);
-            mbar_arrive_expect_tx(lb, 2 * 16384 + 2 * 32768);
-            tma_load_3d(sb0 + SQ, &tmQ, lb, 0, c * C + it * 128, (int)bh);
-            tma_load_3d(sb0 + SD, &tmD, lb, 0, c * C + it * 128, (int)bh);
-            tma_load_3d(sb0 + SK, &tmK, lb, 0, c * C, (int)bh);
-            tma_load_3d(sb0 + SV, &tmV, lb, 0, c * C, (int)bh);
-            int issued = 0;
-            for (int n = 0; n < 64 && !abort_s; ++n) {
-                const int sb = n % NS;
-                if (n >= NS && !mbar_wait(smem_u32(&bar_empty[sb]), ((n / NS) - 1) & 1, a.status)) {
-                    abort_s = 1;
-                    break;
-                }
-                const uint32_t fb = smem_u32(&bar_full[sb]);
-                mbar_arrive_expect_tx(fb, 16384);
-                const int plane = (int)((bh * NC + c) * 2);
-                tma_load_4d(sb0 + STG + sb * 16384, &tmS, fb, 0, n, 0, plane);
-                tma_load_4d(sb0 + STG + sb * 16384 + 8192, &tmS, fb, 0, n, 0, plane + 1);
-                issued = n + 1;
-            }
-            mbar_wait(lb, 0, a.status);
-            for (int n = issued - 1; n >= 0 && n >= issued - NS; --n)
-                mbar_wait(smem_u32(&bar_full[n % NS]), (n / NS) & 1, a.status);
-        }
-    } else if (warp == WARP_MMA) {
-        if (lane == 0) {
-            bool ok = mbar_wait(smem_u32(&bar_ld), 0, a.status);
-            tc_fence_after();
-            // ---- intra-chunk: dq += (hi + lo of dSs) K over the 64-key blocks
-            for (int b = 0; b < nblk && ok; ++b) {
-                if (b > 0 && !(ok = mbar_wait(smem_u32(&bar_sfree[b - 1]), 0, a.status))) break;
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    umma_bf16(tmem + TM_S, sdesc_sw128(sb0 + SQ + kk * 32), sdesc_sw128(sb0 + SK + b * 8192 + kk * 32),
-                              IDESC_BF_K, kk > 0);
-                    umma_bf16(tmem + TM_W, sdesc_sw128(sb0 + SD + kk * 32), sdesc_sw128(sb0 + SV + b * 8192 + kk * 32),
-                              IDESC_BF_K, kk > 0);
-                }
-                umma_commit(smem_u32(&bar_sfull[b]));
-                if (!(ok = mbar_wait(smem_u32(&bar_pfull[b]), 0, a.status))) break;
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t kd = sdesc_sw128_ex(sb0 + SK + b * 8192 + kk * 2048, 8192, 1024);
-                    umma_bf16_ts(tmem + TM_DQ, tmem + TM_PH + kk * 8, kd, IDESC_BF_MN, (b > 0 || kk > 0) ? 1u : 0u);
-                    umma_bf16_ts(tmem + TM_DQ, tmem + TM_PL + kk * 8, kd, IDESC_BF_MN, 1u);
-                }
-                umma_commit(smem_u32(&bar_pfree[b]));
-            }
-            // ---- inter-chunk: U_n = dO S_n^T (n < 64), U_64 = Q zm^T
-            if (ok) ok = mbar_wait(smem_u32(&bar_cvt), 0, a.status);
-            tc_fence_after();
-            for (int n = 0; n < NSL && ok; ++n) {
-                const int sb = n % NS, ub = n & 1;
-                if (abort_s) { ok = false; break; }
-                if (n < 64 && !(ok = mbar_wait(smem_u32(&bar_full[sb]), (n / NS) & 1, a.status))) break;
-                if (n >= 2 && !(ok = mbar_wait(smem_u32(&bar_uempty[ub]), ((n >> 1) - 1) & 1, a.status))) break;
-                tc_fence_after();
-                const uint32_t aop = sb0 + (n < 64 ? SDH : SQH);
-                const uint32_t bhi = n < 64 ? sb0 + STG + sb * 16384 : sb0 + SZH;
-                const uint32_t blo = n < 64 ? bhi + 8192 : sb0 + SZL;
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    umma_bf16(tmem + TM_U + ub * 64, sdesc_sw128(aop + kk * 32), sdesc_sw128(bhi + kk * 32), IDESC_H_K,
-                              kk > 0);
-                    umma_bf16(tmem + TM_U + ub * 64, sdesc_sw128(aop + kk * 32), sdesc_sw128(blo + kk * 32), IDESC_H_K, 1u);
-                }
-                if (n < 64) umma_commit(smem_u32(&bar_empty[sb]));
-                umma_commit(smem_u32(&bar_ufull[ub]));
-            }
-            if (ok) umma_commit(smem_u32(&bar_dqfull));
-            else abort_s = 1;
-            umma_commit(smem_u32(&bar_done));
-            mbar_wait(smem_u32(&bar_done), 0, a.status);
-        }
-    } else {
-        // ---------------------------------------------------------------- compute warps
-        const int quad = warp & 3, h = warp >> 2;
-        const int l = quad * 32 + lane;                  // tile row
-        const int i = it * 128 + l;                      // chunk-local token
-        const long tok = (long)c * C + i;
-        const bool in = tok < a.T;
-        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-        const float Ai = sAv[i];
-        const float ze = in ? a.zeta[bh * a.T + tok] : 0.f;
-        const float uc = in ? a.ucol[bh * a.T + tok] : 0.f;
-        bool ok = mbar_wait(smem_u32(&bar_ld), 0, a.status);
-        if (ok) {   // fp16 copies of the Q and dO tiles, and the normaliser matrix of the state
-            const int t256 = threadIdx.x;
-            for (int pc = t256; pc < 1024; pc += 256) {
-                tile_bf16_to_f16(sb0 + SQ, sb0 + SQH, pc);
-                tile_bf16_to_f16(sb0 + SD, sb0 + SDH, pc);
-            }
-            build_z_tiles(smem + SZH, smem + SZL, a.zx + (bh * NC + c) * 4096, 1.f, t256);
-            fence_proxy_async();
-            mbar_arrive(smem_u32(&bar_cvt));
-        }
-        // ---- intra-chunk blocks
-        for (int b = 0; b < nblk && ok; ++b) {
-            if (!(ok = mbar_wait(smem_u32(&bar_sfull[b]), 0, a.status))) break;
-            if (b > 0 && !(ok = mbar_wait(smem_u32(&bar_pfree[b - 1]), 0, a.status))) break;
-            tc_fence_after();
-#pragma unroll
-            for (int g2 = 0; g2 < 2; ++g2) {
-                const int cc = 2 * h + g2;
-                float sv[16], wv[16];
-                tmem_ld16(tmem + lane_base + TM_S + cc * 16, sv);
-                tmem_ld16(tmem + lane_base + TM_W + cc * 16, wv);
-                uint32_t ph[8], pl[8];
-#pragma unroll
-                for (int k2 = 0; k2 < 8; ++k2) {
-                    float hi2[2], lo2[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int j = b * 64 + cc * 16 + 2 * k2 + u;
-                        const int kx = 2 * k2 + u;
-                        const float val = j <= i ? 2.f * sv[kx] * __expf(Ai - sAv[j]) * (wv[kx] + uc) : 0.f;
-                        hi2[u] = __bfloat162float(__float2bfloat16_rn(val));
-                        lo2[u] = val - hi2[u];
-                    }
-                    ph[k2] = pack_bf16x2(hi2[0], hi2[1]);
-                    pl[k2] = pack_bf16x2(lo2[0], lo2[1]);
-                }
-                tmem_st8(tmem + lane_base + TM_PH + cc * 8, ph);
-                tmem_st8(tmem + lane_base + TM_PL + cc * 8, pl);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(smem_u32(&bar_sfree[b]));
-            mbar_arrive(smem_u32(&bar_pfull[b]));
-        }
-        // ---- inter-chunk slices: dqx[m] += q_i[n] U_n[i][m]  (n = 64: ucol_i U_64[i][m])
-        float dqx[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k) dqx[k] = 0.f;
-        const uint8_t* qrow = smem + SQ;
-#pragma unroll 1
-        for (int n = 0; n < NSL && ok; ++n) {
-            const int ub = n & 1;
-            if (abort_s || !(ok = mbar_wait(smem_u32(&bar_ufull[ub]), (n >> 1) & 1, a.status))) break;
-            tc_fence_after();
-            float u0[16], u1[16];
-            tmem_ld16(tmem + lane_base + TM_U + ub * 64 + h * 32, u0);
-            tmem_ld16(tmem + lane_base + TM_U + ub * 64 + h * 32 + 16, u1);
-            tc_fence_before();
-            mbar_arrive(smem_u32(&bar_uempty[ub]));
-            const float coef = n < 64 ? __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(qrow + swz_elem(l, n))) : uc;
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                dqx[k] = fmaf(coef, u0[k], dqx[k]);
-                dqx[16 + k] = fmaf(coef, u1[k], dqx[16 + k]);
-            }
-        }
-        if (ok && !abort_s && (ok = mbar_wait(smem_u32(&bar_dqfull), 0, a.status))) {
-            tc_fence_after();
-            float d0[16], d1[16];
-            tmem_ld16(tmem + lane_base + TM_DQ + h * 32, d0);
-            tmem_ld16(tmem + lane_base + TM_DQ + h * 32 + 16, d1);
-            if (in) {
-                const float f = 2.f * __expf(Ai);
-                float4* dst = reinterpret_cast<float4*>(a.dq + (bh * a.T + tok) * 64 + h * 32);
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    dst[u] = make_float4(ze * (d0[4 * u] + f * dqx[4 * u]), ze * (d0[4 * u + 1] + f * dqx[4 * u + 1]),
-                                         ze * (d0[4 * u + 2] + f * dqx[4 * u + 2]), ze * (d0[4 * u + 3] + f * dqx[4 * u + 3]));
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    dst[4 + u] = make_float4(ze * (d1[4 * u] + f * dqx[16 + 4 * u]), ze * (d1[4 * u + 1] + f * dqx[16 + 4 * u + 1]),
-                                             ze * (d1[4 * u + 2] + f * dqx[16 + 4 * u + 2]),
-                                             ze * (d1[4 * u + 3] + f * dqx[16 + 4 * u + 3]));
-            }
-        }
-        if (!ok) abort_s = 1;
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 512);
-}
-
 __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmK,
                                                                  const __grid_constant__ CUtensorMap tmV,
                                                                  const __grid_constant__ CUtensorMap tmQ,
@@ -370,10 +89,11 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
     using namespace kvm;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_align1024(smem_raw);
-    __shared__ __align__(8) uint64_t bar_ld, bar_full[NS], bar_empty[NS], bar_cvt, bar_sfull[4], bar_sfree[4],
-        bar_pfull[4], bar_pfree[4], bar_ufull[2], bar_uempty[2], bar_kvfull, bar_red, bar_done;
+    __shared__ __align__(8) uint64_t bar_ld, bar_full[NP], bar_empty[NP], bar_cvt, bar_sfull[4], bar_sfree[4],
+        bar_pfull[4], bar_pfree[4], bar_ufull[2], bar_uempty[2], bar_kvfull, bar_red, bar_intra, bar_done;
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_s;
+    __shared__ volatile int gflags[2];         // group waits of the compute warps
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tj = blockIdx.x & 1, c = blockIdx.x >> 1;
     const long bh = blockIdx.y;
@@ -387,7 +107,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
 
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(&bar_ld), 1);
-        for (int i = 0; i < NS; ++i) {
+        for (int i = 0; i < NP; ++i) {
             mbar_init(smem_u32(&bar_full[i]), 1);
             mbar_init(smem_u32(&bar_empty[i]), 1);
         }
@@ -403,6 +123,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
             mbar_init(smem_u32(&bar_uempty[i]), 256);
         }
         mbar_init(smem_u32(&bar_kvfull), 1);
+        mbar_init(smem_u32(&bar_intra), 1);
         mbar_init(smem_u32(&bar_red), 256);
         mbar_init(smem_u32(&bar_done), 1);
         abort_s = 0;
@@ -433,22 +154,26 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
             tma_load_3d(sb0 + SQ, &tmQ, lb, 0, c * C, (int)bh);
             tma_load_3d(sb0 + SD, &tmD, lb, 0, c * C, (int)bh);
             int issued = 0;
-            for (int n = 0; n < 64 && !abort_s; ++n) {
-                const int sb = n % NS;
-                if (n >= NS && !mbar_wait(smem_u32(&bar_empty[sb]), ((n / NS) - 1) & 1, a.status)) {
+            const int chunk_id = (int)(bh * NC + c);
+            for (int pp = 0; pp < 32 && !abort_s; ++pp) {   // slices 2pp, 2pp+1, both planes
+                const int ps = pp % NP;
+                if (pp >= NP && !mbar_wait(smem_u32(&bar_empty[ps]), ((pp / NP) - 1) & 1, a.status)) {
                     abort_s = 1;
                     break;
                 }
-                const uint32_t fb = smem_u32(&bar_full[sb]);
-                mbar_arrive_expect_tx(fb, 16384);
-                const int plane = (int)((bh * NC + c) * 2);
-                tma_load_4d(sb0 + STG + sb * 16384, &tmS, fb, 0, n, 0, plane);
-                tma_load_4d(sb0 + STG + sb * 16384 + 8192, &tmS, fb, 0, n, 0, plane + 1);
-                issued = n + 1;
+                if (pp == NP_EARLY && (!mbar_wait(smem_u32(&bar_intra), 0, a.status) ||
+                                       !mbar_wait(smem_u32(&bar_cvt), 0, a.status))) {   // tiles dead, copies made
+                    abort_s = 1;
+                    break;
+                }
+                const uint32_t fb = smem_u32(&bar_full[ps]);
+                mbar_arrive_expect_tx(fb, PBYTES);
+                tma_load_5d(sb0 + STG + ps * PBYTES, &tmS, fb, 0, 0, 2 * pp, 0, chunk_id);
+                issued = pp + 1;
             }
             mbar_wait(lb, 0, a.status);
-            for (int n = issued - 1; n >= 0 && n >= issued - NS; --n)
-                mbar_wait(smem_u32(&bar_full[n % NS]), (n / NS) & 1, a.status);
+            for (int pp = issued - 1; pp >= 0 && pp >= issued - NP; --pp)
+                mbar_wait(smem_u32(&bar_full[pp % NP]), (pp / NP) & 1, a.status);
         }
     } else if (warp == WARP_MMA) {
         if (lane == 0) {
@@ -481,18 +206,20 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
                 }
                 umma_commit(smem_u32(&bar_pfree[b]));
             }
+            umma_commit(smem_u32(&bar_intra));   // arrives when every intra-chunk MMA has finished
             // ---- inter-chunk: U_n = K dS_n (N = column), U'_n = V dS_n^T (N = m); U'_64 = K dzm^T
             if (ok) ok = mbar_wait(smem_u32(&bar_cvt), 0, a.status);
             tc_fence_after();
             for (int n = 0; n < NSL && ok; ++n) {
-                const int sb = n % NS, ub = n & 1;
+                const int pp = n >> 1, ps = pp % NP, ub = n & 1;
                 const uint32_t tu = tmem + (ub ? TM_U1 : TM_U0);
                 if (abort_s) { ok = false; break; }
-                if (n < 64 && !(ok = mbar_wait(smem_u32(&bar_full[sb]), (n / NS) & 1, a.status))) break;
+                if (n < 64 && (n & 1) == 0 && !(ok = mbar_wait(smem_u32(&bar_full[ps]), (pp / NP) & 1, a.status)))
+                    break;
                 if (n >= 2 && !(ok = mbar_wait(smem_u32(&bar_uempty[ub]), ((n >> 1) - 1) & 1, a.status))) break;
                 tc_fence_after();
                 if (n < 64) {
-                    const uint32_t bhi = sb0 + STG + sb * 16384, blo = bhi + 8192;
+                    const uint32_t bhi = sb0 + STG + ps * PBYTES + (n & 1) * 8192, blo = bhi + 16384;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint64_t ak = sdesc_sw128(sb0 + SKH + kk * 32), av = sdesc_sw128(sb0 + SVH + kk * 32);
@@ -501,7 +228,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
                         umma_bf16(tu + 64, av, sdesc_sw128(bhi + kk * 32), IDESC_H_K, kk > 0);
                         umma_bf16(tu + 64, av, sdesc_sw128(blo + kk * 32), IDESC_H_K, 1u);
                     }
-                    umma_commit(smem_u32(&bar_empty[sb]));
+                    if (n & 1) umma_commit(smem_u32(&bar_empty[ps]));
                 } else {
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
@@ -527,6 +254,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         const float Aj = sAv[j];
         float dv64_in = 0.f;
+        int kg = 0;                                      // group-wait counter
         bool ok = mbar_wait(smem_u32(&bar_ld), 0, a.status);
         if (ok) {   // fp16 copies of the key and value tiles; the normaliser gradient matrix / scale
             const int t256 = threadIdx.x;
@@ -541,9 +269,10 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
         // ---- intra-chunk blocks (queries i >= j)
         for (int b = 0; b < nblk && ok; ++b) {
             const int ib = 2 * tj + b;
-            if (!(ok = mbar_wait(smem_u32(&bar_sfull[b]), 0, a.status))) break;
-            if (b > 0 && !(ok = mbar_wait(smem_u32(&bar_pfree[b - 1]), 0, a.status))) break;
-            tc_fence_after();
+            if (!(ok = group_wait(smem_u32(&bar_sfull[b]), 0, a.status, warp == 0, 1, 256, gflags, kg, &abort_s))) break;
+            if (b > 0 && !(ok = group_wait(smem_u32(&bar_pfree[b - 1]), 0, a.status, warp == 0, 1, 256, gflags, kg,
+                                           &abort_s)))
+                break;
 #pragma unroll
             for (int g2 = 0; g2 < 2; ++g2) {
                 const int cc = 2 * h + g2;
@@ -590,13 +319,14 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
 #pragma unroll
         for (int k = 0; k < 32; ++k) dkx[k] = dvx[k] = 0.f;
         float dv64x = 0.f;
-        const uint8_t* krow = smem + SK;
+        const uint8_t* krow = smem + SKH;            // fp16 copies (the bf16 tiles are reused for stages)
 #pragma unroll 1
         for (int n = 0; n < NSL && ok; ++n) {
             const int ub = n & 1;
             const uint32_t tu = tmem + lane_base + (ub ? TM_U1 : TM_U0);
-            if (abort_s || !(ok = mbar_wait(smem_u32(&bar_ufull[ub]), (n >> 1) & 1, a.status))) break;
-            tc_fence_after();
+            if (!(ok = group_wait(smem_u32(&bar_ufull[ub]), (n >> 1) & 1, a.status, warp == 0, 1, 256, gflags, kg,
+                                  &abort_s)))
+                break;
             float up[32], uv[32];
             tmem_ld16(tu + 64 + h * 32, up);
             tmem_ld16(tu + 64 + h * 32 + 16, up + 16);
@@ -607,7 +337,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
             tc_fence_before();
             mbar_arrive(smem_u32(&bar_uempty[ub]));
             if (n < 64) {
-                const float kn = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(krow + swz_elem(l, n)));
+                const float kn = __half2float(*reinterpret_cast<const __half*>(krow + swz_elem(l, n)));
 #pragma unroll
                 for (int k = 0; k < 32; ++k) {
                     dkx[k] = fmaf(kn, up[k], dkx[k]);
@@ -617,8 +347,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
 #pragma unroll
                 for (int k = 0; k < 32; ++k) {
                     dkx[k] += up[k];
-                    const float km = __bfloat162float(
-                        *reinterpret_cast<const __nv_bfloat16*>(krow + swz_elem(l, h * 32 + k)));
+                    const float km = __half2float(*reinterpret_cast<const __half*>(krow + swz_elem(l, h * 32 + k)));
                     dv64x = fmaf(km, up[k], dv64x);
                 }
             }
@@ -634,12 +363,12 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
             const float gsc = a.sscale[bh * NC + c];
             const float fk = 2.f * wj * gsc, fv = wj * gsc;
             float vdot = 0.f;
-            const uint8_t* vrow = smem + SV;
+            const uint8_t* vrow = smem + SVH;
 #pragma unroll
             for (int k = 0; k < 32; ++k) {
                 dk0[k] += fk * dkx[k];
                 dv0[k] += fv * dvx[k];
-                const float vv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(vrow + swz_elem(l, h * 32 + k)));
+                const float vv = __half2float(*reinterpret_cast<const __half*>(vrow + swz_elem(l, h * 32 + k)));
                 vdot = fmaf(vv, dv0[k], vdot);
             }
             const float part = vdot + dv64_in + fv * dv64x;   // this half's share of Vt_j . dVt_j
@@ -672,7 +401,7 @@ cudaError_t tc_bwd_dkdv(const Problem& p, const void* q, const void* k, const vo
     const uint64_t BH = (uint64_t)p.BH(), T = (uint64_t)p.T;
     if (!make_tmap_bf16_3d(&tk, k, BH, T, 64, 128) || !make_tmap_bf16_3d(&tv, v, BH, T, 64, 128) ||
         !make_tmap_bf16_3d(&tq, q, BH, T, 64, 256) || !make_tmap_bf16_3d(&td, dO, BH, T, 64, 256) ||
-        !make_tmap_state_slices(&ts, dSx, BH * (uint64_t)p.NC * 2))
+        !make_tmap_state_tpairs(&ts, dSx, BH * (uint64_t)p.NC))
         return cudaErrorInvalidValue;
     int* status = tc_status_ptr();
     if (!status) return cudaErrorInvalidValue;
@@ -681,24 +410,6 @@ cudaError_t tc_bwd_dkdv(const Problem& p, const void* q, const void* k, const vo
     if (e != cudaSuccess) return e;
     dim3 grid(2 * p.NC, (unsigned)p.BH());
     tc_bwd_dkdv_kernel<<<grid, THREADS, kvm::BYTES, s>>>(tk, tv, tq, td, ts, a);
-    return cudaGetLastError();
-}
-
-cudaError_t tc_bwd_dq(const Problem& p, const void* q, const void* k, const void* v, const void* dO, const float* Aloc,
-                      const float* zeta, const float* ucol, const void* Sx, const float* zx, float* dq, cudaStream_t s) {
-    CUtensorMap tq, td, tk, tv, ts;
-    const uint64_t BH = (uint64_t)p.BH(), T = (uint64_t)p.T;
-    if (!make_tmap_bf16_3d(&tq, q, BH, T, 64, 128) || !make_tmap_bf16_3d(&td, dO, BH, T, 64, 128) ||
-        !make_tmap_bf16_3d(&tk, k, BH, T, 64, 256) || !make_tmap_bf16_3d(&tv, v, BH, T, 64, 256) ||
-        !make_tmap_state_slices(&ts, Sx, BH * (uint64_t)p.NC * 2))
-        return cudaErrorInvalidValue;
-    int* status = tc_status_ptr();
-    if (!status) return cudaErrorInvalidValue;
-    DqArgs a{Aloc, zeta, ucol, zx, dq, status, p.T, p.NC, (int)p.Tp()};
-    cudaError_t e = cudaFuncSetAttribute(tc_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dqm::BYTES);
-    if (e != cudaSuccess) return e;
-    dim3 grid(2 * p.NC, (unsigned)p.BH());
-    tc_bwd_dq_kernel<<<grid, THREADS, dqm::BYTES, s>>>(tq, td, tk, tv, ts, a);
     return cudaGetLastError();
 }
 

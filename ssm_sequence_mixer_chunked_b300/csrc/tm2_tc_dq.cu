@@ -1,0 +1,365 @@
+// tm2_tc_dq.cu -- the query gradient of the tensor-core path (bf16 inputs, d = dv = 64).
+//
+// "2Mamba2Furious", App. C / C.1: inside chunk c (chunk-local running sums A), with
+//   s_ij = q_i . k_j,  E_ij = exp(A_i - A_j) [j <= i],  Vt_j = [v_j, 1],
+//   dL/dY_i = zeta_i u_i,  u_i = [dO_i, ucol_i]  (zeta = 1/Z, ucol = -dO.o when normalised),
+//   dSs_ij = 2 s_ij E_ij zeta_i (u_i . Vt_j)          (gradient w.r.t. s_ij),
+// and S_{c-1}, z_{c-1} the state entering the chunk (symmetric in (m, n)):
+//   dq_i[m] = sum_j dSs_ij k_j[m]
+//           + 2 exp(A_i) zeta_i sum_n q_i[n] ( sum_col dO_i[col] S[(m,n), col] + ucol_i z[(m,n)] ).
+//
+// One CTA per (128-token tile, chunk, b, h).  The inter-chunk sum runs first, over 16 groups
+// of four state slices: U_g[i][(n', m)] = sum_col dO_i[col] S[(m, 4g + n'), col] is one
+// tcgen05.mma of N = 256 per K step and plane (the state as two fp16 planes, hi and residual;
+// dO exact in fp16), and the compute warps fold U into fp32 registers,
+// dqx[m] += q_i[4g + n'] U_g[i][(n', m)].  A tensor-core instruction costs about the same
+// for any N up to 256, so four slices per instruction is what keeps this part short; the
+// slices arrive one plane of one group (32 KB) per TMA request.  A 17th product
+// U_z = Q zm^T (zm[m][n] = z[(m, n)]) carries the normaliser column.
+// The intra-chunk part follows in the same tensor memory: per 64-key block, s = Q K^T and
+// u.Vt = dO V^T (bf16 MMAs), dSs as bf16 hi + lo in tensor memory, dq += dSs K.
+// Warps 0-7 compute (warp w: tensor-memory lane quadrant w % 4, column half w / 4), warp 8
+// issues TMA, warp 9 the MMAs.  Every mbarrier wait is bounded (TM2_ERR_TIMEOUT on expiry).
+#include "tm2.h"
+#include "tm2_launch.h"
+#include "tm2_sm100.cuh"
+#include "tm2_tc.h"
+#include "tm2_tc_tiles.cuh"
+
+namespace tm2 {
+namespace tcdq {
+using namespace tctile;
+
+constexpr int C = TC_CHUNK;
+constexpr int THREADS = 10 * 32;
+constexpr int WARP_TMA = 8, WARP_MMA = 9;
+constexpr int NR = 5;                         // ring slots of 32 KB
+constexpr int RB = 32768;
+constexpr int NG = 16;                        // groups of four state slices
+constexpr int NREQ = 2 * NG + 3;              // hi/lo plane of each group, then Q|dO, K, V (intra part)
+constexpr int EARLY = NR - 1;                 // slot NR-1 first holds the Q and dO tiles for conversion
+// shared memory
+constexpr int RING = 0;
+constexpr int SQH = NR * RB;                  // fp16 copy of the Q tile [128][64]
+constexpr int SDH = SQH + 16384;              // fp16 copy of the dO tile
+constexpr int SZH = SDH + 16384, SZL = SZH + 8192;   // normaliser matrix hi / lo [64][64]
+constexpr int SAV = SZL + 8192;               // chunk-local A, 256 floats
+constexpr int BYTES = SAV + 1024 + 1024;
+// tensor memory: U buffers at 0 and 256; the intra part reuses [0, 256) after the inter part
+constexpr uint32_t TM_DQ = 0, TM_S = 64, TM_W = 128, TM_PH = 192, TM_PL = 224;
+constexpr uint32_t IDESC_U = idesc_f16_f32(128, 256, false, false);
+constexpr uint32_t IDESC_Z = idesc_f16_f32(128, 64, false, false);
+constexpr uint32_t IDESC_BF_K = idesc_bf16_f32(128, 64, false, false);
+constexpr uint32_t IDESC_BF_MN = idesc_bf16_f32(128, 64, false, true);
+
+struct Args {
+    const float* Aloc;   // [BH][Tp]
+    const float* zeta;   // [BH][T]
+    const float* ucol;   // [BH][T]
+    const float* zx;     // [BH][NC][4096] forward normaliser states (slot c = entering chunk c)
+    float* dq;           // [BH][T][64]
+    int* status;
+    int T, NC, Tp;
+};
+
+TM2_DEV int slot_of(int r) { return r % NR; }
+TM2_DEV uint32_t use_of(int r) { return (uint32_t)(r / NR); }
+
+}  // namespace tcdq
+
+using namespace tcdq;
+
+__global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ,
+                                                               const __grid_constant__ CUtensorMap tmD,
+                                                               const __grid_constant__ CUtensorMap tmK,
+                                                               const __grid_constant__ CUtensorMap tmV,
+                                                               const __grid_constant__ CUtensorMap tmS,
+                                                               const __grid_constant__ Args a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_align1024(smem_raw);
+    __shared__ __align__(8) uint64_t bar_ld, bar_full[NR], bar_empty[NR], bar_cvt, bar_sfull[4], bar_sfree[4],
+        bar_pfull[4], bar_pfree[4], bar_ufull[2], bar_uempty[2], bar_dqfull, bar_done;
+    __shared__ uint32_t tmem_base_s;
+    __shared__ volatile int abort_s;
+    __shared__ volatile int gflags[2];         // group waits of the compute warps
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int it = blockIdx.x & 1, c = blockIdx.x >> 1;
+    const long bh = blockIdx.y;
+    const int NC = a.NC;
+    const int nblk = 2 * (it + 1);               // 64-key blocks at or before this tile
+    const uint32_t sb0 = smem_u32(smem);
+    float* sAv = reinterpret_cast<float*>(smem + SAV);
+
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar_ld), 1);
+        for (int i = 0; i < NR; ++i) {
+            mbar_init(smem_u32(&bar_full[i]), 1);
+            mbar_init(smem_u32(&bar_empty[i]), 1);
+        }
+        mbar_init(smem_u32(&bar_cvt), 256);
+        for (int b = 0; b < 4; ++b) {
+            mbar_init(smem_u32(&bar_sfull[b]), 1);
+            mbar_init(smem_u32(&bar_sfree[b]), 256);
+            mbar_init(smem_u32(&bar_pfull[b]), 256);
+            mbar_init(smem_u32(&bar_pfree[b]), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&bar_ufull[i]), 1);
+            mbar_init(smem_u32(&bar_uempty[i]), 256);
+        }
+        mbar_init(smem_u32(&bar_dqfull), 1);
+        mbar_init(smem_u32(&bar_done), 1);
+        abort_s = 0;
+        fence_mbar_init();
+    }
+    for (int j = threadIdx.x; j < C; j += THREADS) sAv[j] = a.Aloc[bh * a.Tp + (long)c * C + j];
+    if (warp == 0) {
+        tmem_alloc(smem_u32(&tmem_base_s), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_s;
+    const uint32_t early = sb0 + RING + EARLY * RB;   // Q tile at +0, dO tile at +16384
+
+    if (warp == WARP_TMA) {
+        if (lane == 0) {
+            prefetch_tmap(&tmS);
+            const uint32_t lb = smem_u32(&bar_ld);
+            mbar_arrive_expect_tx(lb, 2 * 16384);
+            tma_load_3d(early, &tmQ, lb, 0, c * C + it * 128, (int)bh);
+            tma_load_3d(early + 16384, &tmD, lb, 0, c * C + it * 128, (int)bh);
+            const int chunk_id = (int)(bh * NC + c);
+            int issued = 0;
+            for (int r = 0; r < NREQ && !abort_s; ++r) {
+                const int sl = slot_of(r);
+                const uint32_t u = use_of(r);
+                if (u > 0 && !mbar_wait(smem_u32(&bar_empty[sl]), (u - 1) & 1, a.status)) {
+                    abort_s = 1;
+                    break;
+                }
+                if (r == EARLY && !mbar_wait(smem_u32(&bar_cvt), 0, a.status)) {   // copies made: slot free
+                    abort_s = 1;
+                    break;
+                }
+                const uint32_t fb = smem_u32(&bar_full[sl]), dst = sb0 + RING + sl * RB;
+                mbar_arrive_expect_tx(fb, RB);
+                if (r < 2 * NG) {
+                    tma_load_5d(dst, &tmS, fb, 0, 0, 4 * (r >> 1), r & 1, chunk_id);
+                } else if (r == 2 * NG) {
+                    tma_load_3d(dst, &tmQ, fb, 0, c * C + it * 128, (int)bh);
+                    tma_load_3d(dst + 16384, &tmD, fb, 0, c * C + it * 128, (int)bh);
+                } else {
+                    tma_load_3d(dst, r == 2 * NG + 1 ? &tmK : &tmV, fb, 0, c * C, (int)bh);
+                }
+                issued = r + 1;
+            }
+            // no copy may be in flight at exit
+            mbar_wait(lb, 0, a.status);
+            for (int r = issued - 1; r >= 0 && r >= issued - NR; --r)
+                mbar_wait(smem_u32(&bar_full[slot_of(r)]), use_of(r) & 1, a.status);
+        }
+    } else if (warp == WARP_MMA) {
+        if (lane == 0) {
+            bool ok = mbar_wait(smem_u32(&bar_cvt), 0, a.status);
+            tc_fence_after();
+            // ---- inter-chunk: U_g = dO [S_{4g}..S_{4g+3}]^T (hi + lo plane), then U_z = Q zm^T
+            for (int g = 0; g <= NG && ok; ++g) {
+                const int ub = g & 1;
+                const uint32_t k = (uint32_t)(g >> 1);
+                if (abort_s) { ok = false; break; }
+                if (g < NG) {
+                    const int r0 = 2 * g, r1 = 2 * g + 1;
+                    if (!(ok = mbar_wait(smem_u32(&bar_full[slot_of(r0)]), use_of(r0) & 1, a.status))) break;
+                    if (!(ok = mbar_wait(smem_u32(&bar_full[slot_of(r1)]), use_of(r1) & 1, a.status))) break;
+                }
+                if (k > 0 && !(ok = mbar_wait(smem_u32(&bar_uempty[ub]), (k - 1) & 1, a.status))) break;
+                tc_fence_after();
+                const uint32_t d = tmem + ub * 256;
+                if (g < NG) {
+                    const uint32_t bhi = sb0 + RING + slot_of(2 * g) * RB, blo = sb0 + RING + slot_of(2 * g + 1) * RB;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma_bf16(d, sdesc_sw128(sb0 + SDH + kk * 32), sdesc_sw128(bhi + kk * 32), IDESC_U, kk > 0);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma_bf16(d, sdesc_sw128(sb0 + SDH + kk * 32), sdesc_sw128(blo + kk * 32), IDESC_U, 1u);
+                    umma_commit(smem_u32(&bar_empty[slot_of(2 * g)]));
+                    umma_commit(smem_u32(&bar_empty[slot_of(2 * g + 1)]));
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        umma_bf16(d, sdesc_sw128(sb0 + SQH + kk * 32), sdesc_sw128(sb0 + SZH + kk * 32), IDESC_Z, kk > 0);
+                        umma_bf16(d, sdesc_sw128(sb0 + SQH + kk * 32), sdesc_sw128(sb0 + SZL + kk * 32), IDESC_Z, 1u);
+                    }
+                }
+                umma_commit(smem_u32(&bar_ufull[ub]));
+            }
+            // ---- intra-chunk: dq += (hi + lo of dSs) K over the 64-key blocks, in [0, 256)
+            const int rq = 2 * NG, rk = 2 * NG + 1, rv = 2 * NG + 2;
+            if (ok) ok = mbar_wait(smem_u32(&bar_uempty[0]), (uint32_t)(NG >> 1) & 1, a.status);   // U_z read
+            if (ok) ok = mbar_wait(smem_u32(&bar_full[slot_of(rq)]), use_of(rq) & 1, a.status);
+            if (ok) ok = mbar_wait(smem_u32(&bar_full[slot_of(rk)]), use_of(rk) & 1, a.status);
+            if (ok) ok = mbar_wait(smem_u32(&bar_full[slot_of(rv)]), use_of(rv) & 1, a.status);
+            tc_fence_after();
+            const uint32_t SQ = sb0 + RING + slot_of(rq) * RB, SD = SQ + 16384;
+            const uint32_t SK = sb0 + RING + slot_of(rk) * RB, SV = sb0 + RING + slot_of(rv) * RB;
+            for (int b = 0; b < nblk && ok; ++b) {
+                if (abort_s) { ok = false; break; }
+                if (b > 0 && !(ok = mbar_wait(smem_u32(&bar_sfree[b - 1]), 0, a.status))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    umma_bf16(tmem + TM_S, sdesc_sw128(SQ + kk * 32), sdesc_sw128(SK + b * 8192 + kk * 32), IDESC_BF_K,
+                              kk > 0);
+                    umma_bf16(tmem + TM_W, sdesc_sw128(SD + kk * 32), sdesc_sw128(SV + b * 8192 + kk * 32), IDESC_BF_K,
+                              kk > 0);
+                }
+                umma_commit(smem_u32(&bar_sfull[b]));
+                if (!(ok = mbar_wait(smem_u32(&bar_pfull[b]), 0, a.status))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint64_t kd = sdesc_sw128_ex(SK + b * 8192 + kk * 2048, 8192, 1024);
+                    umma_bf16_ts(tmem + TM_DQ, tmem + TM_PH + kk * 8, kd, IDESC_BF_MN, (b > 0 || kk > 0) ? 1u : 0u);
+                    umma_bf16_ts(tmem + TM_DQ, tmem + TM_PL + kk * 8, kd, IDESC_BF_MN, 1u);
+                }
+                umma_commit(smem_u32(&bar_pfree[b]));
+            }
+            if (ok) umma_commit(smem_u32(&bar_dqfull));
+            else abort_s = 1;
+            umma_commit(smem_u32(&bar_done));
+            mbar_wait(smem_u32(&bar_done), 0, a.status);
+        }
+    } else {
+        // ---------------------------------------------------------------- compute warps
+        const int quad = warp & 3, h = warp >> 2;
+        const int l = quad * 32 + lane;                  // tile row
+        const int i = it * 128 + l;                      // chunk-local token
+        const long tok = (long)c * C + i;
+        const bool in = tok < a.T;
+        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        const float Ai = sAv[i];
+        const float ze = in ? a.zeta[bh * a.T + tok] : 0.f;
+        const float uc = in ? a.ucol[bh * a.T + tok] : 0.f;
+        int kg = 0;                                      // group-wait counter
+        bool ok = mbar_wait(smem_u32(&bar_ld), 0, a.status);
+        if (ok) {   // fp16 copies of the Q and dO tiles, and the normaliser matrix of the state
+            const int t256 = threadIdx.x;
+            for (int pc = t256; pc < 1024; pc += 256) {
+                tile_bf16_to_f16(early, sb0 + SQH, pc);
+                tile_bf16_to_f16(early + 16384, sb0 + SDH, pc);
+            }
+            build_z_tiles(smem + SZH, smem + SZL, a.zx + (bh * NC + c) * 4096, 1.f, t256);
+            fence_proxy_async();
+        }
+        mbar_arrive(smem_u32(&bar_cvt));
+        // ---- inter-chunk: dqx[m] += q_i[n] U[i][(n, m)]  (U_z: ucol_i U_z[i][m])
+        float dqx[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) dqx[k] = 0.f;
+        const uint8_t* qrow = smem + SQH;
+#pragma unroll 1
+        for (int g = 0; g <= NG && ok; ++g) {
+            const int ub = g & 1;
+            if (!(ok = group_wait(smem_u32(&bar_ufull[ub]), (uint32_t)(g >> 1) & 1, a.status, warp == 0, 1, 256, gflags,
+                                  kg, &abort_s)))
+                break;
+            const uint32_t ua = tmem + lane_base + ub * 256 + h * 32;
+            if (g < NG) {
+#pragma unroll 1
+                for (int np = 0; np < 4; ++np) {
+                    float u[32];
+                    tmem_ld32(ua + np * 64, u);
+                    if (np == 3) {
+                        tc_fence_before();
+                        mbar_arrive(smem_u32(&bar_uempty[ub]));
+                    }
+                    const float qn = __half2float(*reinterpret_cast<const __half*>(qrow + swz_elem(l, 4 * g + np)));
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) dqx[k] = fmaf(qn, u[k], dqx[k]);
+                }
+            } else {
+                float u[32];
+                tmem_ld32(ua, u);
+                tc_fence_before();
+                mbar_arrive(smem_u32(&bar_uempty[ub]));
+#pragma unroll
+                for (int k = 0; k < 32; ++k) dqx[k] = fmaf(uc, u[k], dqx[k]);
+            }
+        }
+        // ---- intra-chunk blocks
+        for (int b = 0; b < nblk && ok; ++b) {
+            if (!(ok = group_wait(smem_u32(&bar_sfull[b]), 0, a.status, warp == 0, 1, 256, gflags, kg, &abort_s))) break;
+            if (b > 0 && !(ok = group_wait(smem_u32(&bar_pfree[b - 1]), 0, a.status, warp == 0, 1, 256, gflags, kg,
+                                           &abort_s)))
+                break;
+#pragma unroll
+            for (int g2 = 0; g2 < 2; ++g2) {
+                const int cc = 2 * h + g2;
+                float sv[16], wv[16];
+                tmem_ld16(tmem + lane_base + TM_S + cc * 16, sv);
+                tmem_ld16(tmem + lane_base + TM_W + cc * 16, wv);
+                uint32_t ph[8], pl[8];
+#pragma unroll
+                for (int k2 = 0; k2 < 8; ++k2) {
+                    float hi2[2], lo2[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int j = b * 64 + cc * 16 + 2 * k2 + u;
+                        const int kx = 2 * k2 + u;
+                        const float val = j <= i ? 2.f * sv[kx] * __expf(Ai - sAv[j]) * (wv[kx] + uc) : 0.f;
+                        hi2[u] = __bfloat162float(__float2bfloat16_rn(val));
+                        lo2[u] = val - hi2[u];
+                    }
+                    ph[k2] = pack_bf16x2(hi2[0], hi2[1]);
+                    pl[k2] = pack_bf16x2(lo2[0], lo2[1]);
+                }
+                tmem_st8(tmem + lane_base + TM_PH + cc * 8, ph);
+                tmem_st8(tmem + lane_base + TM_PL + cc * 8, pl);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bar_sfree[b]));
+            mbar_arrive(smem_u32(&bar_pfull[b]));
+        }
+        if (ok && !abort_s && (ok = mbar_wait(smem_u32(&bar_dqfull), 0, a.status))) {
+            tc_fence_after();
+            float d0[32];
+            tmem_ld32(tmem + lane_base + TM_DQ + h * 32, d0);
+            if (in) {
+                const float f = 2.f * __expf(Ai);
+                float4* dst = reinterpret_cast<float4*>(a.dq + (bh * a.T + tok) * 64 + h * 32);
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    dst[u] = make_float4(ze * (d0[4 * u] + f * dqx[4 * u]), ze * (d0[4 * u + 1] + f * dqx[4 * u + 1]),
+                                         ze * (d0[4 * u + 2] + f * dqx[4 * u + 2]), ze * (d0[4 * u + 3] + f * dqx[4 * u + 3]));
+            }
+        }
+        if (!ok) abort_s = 1;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+cudaError_t tc_bwd_dq(const Problem& p, const void* q, const void* k, const void* v, const void* dO, const float* Aloc,
+                      const float* zeta, const float* ucol, const void* Sx, const float* zx, float* dq, cudaStream_t s) {
+    CUtensorMap tq, td, tk, tv, ts;
+    const uint64_t BH = (uint64_t)p.BH(), T = (uint64_t)p.T;
+    if (!make_tmap_bf16_3d(&tq, q, BH, T, 64, 128) || !make_tmap_bf16_3d(&td, dO, BH, T, 64, 128) ||
+        !make_tmap_bf16_3d(&tk, k, BH, T, 64, 256) || !make_tmap_bf16_3d(&tv, v, BH, T, 64, 256) ||
+        !make_tmap_state_tquads(&ts, Sx, BH * (uint64_t)p.NC))
+        return cudaErrorInvalidValue;
+    int* status = tc_status_ptr();
+    if (!status) return cudaErrorInvalidValue;
+    Args a{Aloc, zeta, ucol, zx, dq, status, p.T, p.NC, (int)p.Tp()};
+    cudaError_t e = cudaFuncSetAttribute(tc_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, BYTES);
+    if (e != cudaSuccess) return e;
+    dim3 grid(2 * p.NC, (unsigned)p.BH());
+    tc_bwd_dq_kernel<<<grid, THREADS, BYTES, s>>>(tq, td, tk, tv, ts, a);
+    return cudaGetLastError();
+}
+
+}  // namespace tm2

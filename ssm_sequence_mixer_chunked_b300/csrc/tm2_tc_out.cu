@@ -32,16 +32,20 @@ namespace tm2 {
 namespace tcout {
 
 constexpr int C = TC_CHUNK;
-constexpr int NS = 3;                        // state-slice stages (hi + residual plane)
+constexpr int NP = 5;                        // stages of two state slices (hi + residual planes, 32 KB)
+constexpr int NP_EARLY = 2;                  // stages free from the start; the rest alias the
+                                             // intra-chunk tiles and open once those are done
+constexpr int PBYTES = 32768;
 constexpr int NSL = 65;                      // 64 state slices + the normaliser product
 constexpr int THREADS = 18 * 32;
 constexpr int NCOMP = 512;                   // compute threads
 constexpr int WARP_TMA = 16, WARP_MMA = 17;
 constexpr int TILE_BYTES = C * 128;          // [256][64] 16-bit
-constexpr int SQ = 0, SQH = TILE_BYTES, SK = 2 * TILE_BYTES, SV = 3 * TILE_BYTES;
-constexpr int SZH = 4 * TILE_BYTES, SZL = SZH + 8192;             // zm hi / lo, [64][64] fp16
-constexpr int STG = SZL + 8192;                                    // NS x (hi 8 KB + lo 8 KB)
-constexpr int SAV = STG + NS * 16384;                              // A values, 256 floats
+constexpr int STG = 0;                                             // NP x [plane][slice m, m+1][64][64]
+constexpr int SQ = 65536, SK = 98304, SV = 131072;                 // bf16 tiles (stages 2-4)
+constexpr int SQH = 163840;                                        // fp16 copy of Q
+constexpr int SZH = SQH + TILE_BYTES, SZL = SZH + 8192;            // zm hi / lo, [64][64] fp16
+constexpr int SAV = SZL + 8192;                                    // A values, 256 floats
 constexpr int SRED = SAV + 1024;                                   // [2 halves][256 tokens][2]
 constexpr int SMEM_BYTES = SRED + 4096 + 1024;
 constexpr int NBLK = 6;                      // intra-chunk blocks: (tile, 64-key block)
@@ -79,10 +83,11 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
                                                                   const __grid_constant__ Args a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_align1024(smem_raw);
-    __shared__ __align__(8) uint64_t bar_qkv, bar_full[NS], bar_empty[NS], bar_cvt, bar_sfull[NBLK], bar_sfree[NBLK],
-        bar_pfull[NBLK], bar_pfree[NBLK], bar_ufull[2], bar_uempty[2], bar_yfull, bar_red, bar_done;
+    __shared__ __align__(8) uint64_t bar_qkv, bar_full[NP], bar_empty[NP], bar_cvt, bar_sfull[NBLK], bar_sfree[NBLK],
+        bar_pfull[NBLK], bar_pfree[NBLK], bar_ufull[2], bar_uempty[2], bar_yfull, bar_red, bar_intra, bar_done;
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_s;
+    __shared__ volatile int gflags[3][2];      // group waits: all compute warps, tile 0, tile 1
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c = blockIdx.x;
     const long bh = blockIdx.y;
@@ -93,7 +98,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
 
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(&bar_qkv), 1);
-        for (int i = 0; i < NS; ++i) {
+        for (int i = 0; i < NP; ++i) {
             mbar_init(smem_u32(&bar_full[i]), 1);
             mbar_init(smem_u32(&bar_empty[i]), 1);
         }
@@ -109,6 +114,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
             mbar_init(smem_u32(&bar_uempty[i]), NCOMP);
         }
         mbar_init(smem_u32(&bar_yfull), 1);
+        mbar_init(smem_u32(&bar_intra), 1);
         mbar_init(smem_u32(&bar_red), NCOMP);
         mbar_init(smem_u32(&bar_done), 1);
         abort_s = 0;
@@ -133,22 +139,26 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
             tma_load_3d(sb0 + SK, &tmK, qb, 0, c * C, (int)bh);
             tma_load_3d(sb0 + SV, &tmV, qb, 0, c * C, (int)bh);
             int issued = 0;
-            for (int m = 0; m < 64 && !abort_s; ++m) {
-                const int sb = m % NS;
-                if (m >= NS && !mbar_wait(smem_u32(&bar_empty[sb]), ((m / NS) - 1) & 1, a.status)) {
+            const int chunk_id = (int)(bh * NC + c);
+            for (int pp = 0; pp < 32 && !abort_s; ++pp) {   // slices 2pp, 2pp+1, both planes
+                const int ps = pp % NP;
+                if (pp >= NP && !mbar_wait(smem_u32(&bar_empty[ps]), ((pp / NP) - 1) & 1, a.status)) {
                     abort_s = 1;
                     break;
                 }
-                const uint32_t fb = smem_u32(&bar_full[sb]);
-                mbar_arrive_expect_tx(fb, 16384);
-                const int plane = (int)((bh * NC + c) * 2);
-                tma_load_3d(sb0 + STG + sb * 16384, &tmS, fb, 0, m * 64, plane);
-                tma_load_3d(sb0 + STG + sb * 16384 + 8192, &tmS, fb, 0, m * 64, plane + 1);
-                issued = m + 1;
+                if (pp == NP_EARLY && (!mbar_wait(smem_u32(&bar_intra), 0, a.status) ||
+                                       !mbar_wait(smem_u32(&bar_cvt), 0, a.status))) {   // tiles dead, copies made
+                    abort_s = 1;
+                    break;
+                }
+                const uint32_t fb = smem_u32(&bar_full[ps]);
+                mbar_arrive_expect_tx(fb, PBYTES);
+                tma_load_4d(sb0 + STG + ps * PBYTES, &tmS, fb, 0, pp * 128, 0, chunk_id);
+                issued = pp + 1;
             }
             mbar_wait(qb, 0, a.status);
-            for (int m = issued - 1; m >= 0 && m >= issued - NS; --m)
-                mbar_wait(smem_u32(&bar_full[m % NS]), (m / NS) & 1, a.status);
+            for (int pp = issued - 1; pp >= 0 && pp >= issued - NP; --pp)
+                mbar_wait(smem_u32(&bar_full[pp % NP]), (pp / NP) & 1, a.status);
         }
     } else if (warp == WARP_MMA) {
         if (lane == 0) {
@@ -174,13 +184,15 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
                 }
                 umma_commit(smem_u32(&bar_pfree[b]));
             }
+            umma_commit(smem_u32(&bar_intra));   // arrives when every intra-chunk MMA has finished
             // ---- inter-chunk readout: U_m = Q S_m (m < 64), U_64 = Q zm^T
             if (ok) ok = mbar_wait(smem_u32(&bar_cvt), 0, a.status);
             tc_fence_after();
             for (int m = 0; m < NSL && ok; ++m) {
-                const int sb = m % NS, ub = m & 1;
+                const int pp = m >> 1, ps = pp % NP, ub = m & 1;
                 if (abort_s) { ok = false; break; }
-                if (m < 64 && !(ok = mbar_wait(smem_u32(&bar_full[sb]), (m / NS) & 1, a.status))) break;
+                if (m < 64 && (m & 1) == 0 && !(ok = mbar_wait(smem_u32(&bar_full[ps]), (pp / NP) & 1, a.status)))
+                    break;
                 if (m >= 2 && !(ok = mbar_wait(smem_u32(&bar_uempty[ub]), ((m >> 1) - 1) & 1, a.status))) break;
                 tc_fence_after();
 #pragma unroll
@@ -190,16 +202,16 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint64_t ad = sdesc_sw128(sb0 + SQH + t * 16384 + kk * 32);
                         if (m < 64) {
-                            const uint32_t bs = sb0 + STG + sb * 16384 + kk * 2048;
+                            const uint32_t bs = sb0 + STG + ps * PBYTES + (m & 1) * 8192 + kk * 2048;
                             umma_bf16(d, ad, sdesc_sw128_ex(bs, 8192, 1024), IDESC_RD, kk > 0);
-                            umma_bf16(d, ad, sdesc_sw128_ex(bs + 8192, 8192, 1024), IDESC_RD, 1u);
+                            umma_bf16(d, ad, sdesc_sw128_ex(bs + 16384, 8192, 1024), IDESC_RD, 1u);
                         } else {
                             umma_bf16(d, ad, sdesc_sw128(sb0 + SZH + kk * 32), IDESC_RZ, kk > 0);
                             umma_bf16(d, ad, sdesc_sw128(sb0 + SZL + kk * 32), IDESC_RZ, 1u);
                         }
                     }
                 }
-                if (m < 64) umma_commit(smem_u32(&bar_empty[sb]));
+                if (m < 64 && (m & 1)) umma_commit(smem_u32(&bar_empty[ps]));
                 umma_commit(smem_u32(&bar_ufull[ub]));
             }
             if (ok) umma_commit(smem_u32(&bar_yfull));
@@ -215,6 +227,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         const float Ai = sAv[i];
         float zin = 0.f;
+        int kall = 0, ktile = 0;                       // group-wait counters
         bool ok = mbar_wait(smem_u32(&bar_qkv), 0, a.status);
         if (ok) {   // fp16 copy of the Q tile; the normaliser matrix of the state as hi + lo fp16
             const int tt = threadIdx.x;
@@ -249,9 +262,12 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
         // ---- intra-chunk: tile 0 owns blocks 0-1, tile 1 owns blocks 2-5; half h: 32 key columns
         for (int b = (t == 0 ? 0 : 2); b < (t == 0 ? 2 : NBLK) && ok; ++b) {
             const int jb = blk_key(b);
-            if (!(ok = mbar_wait(smem_u32(&bar_sfull[b]), 0, a.status))) break;
-            if (b > 0 && !(ok = mbar_wait(smem_u32(&bar_pfree[b - 1]), 0, a.status))) break;
-            tc_fence_after();
+            if (!(ok = group_wait(smem_u32(&bar_sfull[b]), 0, a.status, warp == 4 * t, 2 + t, 256, gflags[1 + t],
+                                  ktile, &abort_s)))
+                break;
+            if (b > 0 && !(ok = group_wait(smem_u32(&bar_pfree[b - 1]), 0, a.status, warp == 4 * t, 2 + t, 256,
+                                           gflags[1 + t], ktile, &abort_s)))
+                break;
 #pragma unroll
             for (int g2 = 0; g2 < 2; ++g2) {
                 const int cc = 2 * h + g2;
@@ -286,12 +302,13 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
 #pragma unroll
         for (int k = 0; k < 32; ++k) nx[k] = 0.f;
         float zxp = 0.f;
-        const uint8_t* qrow = smem + SQ;
+        const uint8_t* qrow = smem + SQH;            // fp16 copy (the bf16 tile is reused for stages)
 #pragma unroll 1
         for (int m = 0; m < NSL && ok; ++m) {
             const int ub = m & 1;
-            if (abort_s || !(ok = mbar_wait(smem_u32(&bar_ufull[ub]), (m >> 1) & 1, a.status))) break;
-            tc_fence_after();
+            if (!(ok = group_wait(smem_u32(&bar_ufull[ub]), (m >> 1) & 1, a.status, warp == 0, 1, NCOMP, gflags[0], kall,
+                                  &abort_s)))
+                break;
             float u[32];
             const uint32_t ua = tmem + lane_base + TM_U + ub * 128 + t * 64 + h * 32;
             tmem_ld16(ua, u);
@@ -299,14 +316,13 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
             tc_fence_before();
             mbar_arrive(smem_u32(&bar_uempty[ub]));
             if (m < 64) {
-                const float qm = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(qrow + swz_elem(i, m)));
+                const float qm = __half2float(*reinterpret_cast<const __half*>(qrow + swz_elem(i, m)));
 #pragma unroll
                 for (int k = 0; k < 32; ++k) nx[k] = fmaf(qm, u[k], nx[k]);
             } else {
 #pragma unroll
                 for (int k = 0; k < 32; ++k)
-                    zxp = fmaf(__bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(qrow + swz_elem(i, h * 32 + k))),
-                               u[k], zxp);
+                    zxp = fmaf(__half2float(*reinterpret_cast<const __half*>(qrow + swz_elem(i, h * 32 + k))), u[k], zxp);
             }
         }
         // ---- combine the two column halves' shares of Z, then the epilogue
@@ -351,7 +367,7 @@ cudaError_t tc_chunk_out(const Problem& p, const void* q, const void* k, const v
     const uint64_t BH = (uint64_t)p.BH();
     if (!make_tmap_bf16_3d(&tq, q, BH, (uint64_t)p.T, 64, C) || !make_tmap_bf16_3d(&tk, k, BH, (uint64_t)p.T, 64, C) ||
         !make_tmap_bf16_3d(&tv, v, BH, (uint64_t)p.T, 64, C) ||
-        !make_tmap_bf16_3d(&ts, Sx, BH * (uint64_t)p.NC * 2, 4096, 64, 64))
+        !make_tmap_state_pairs(&ts, Sx, BH * (uint64_t)p.NC))
         return cudaErrorInvalidValue;
     int* status = tc_status_ptr();
     if (!status) return cudaErrorInvalidValue;

@@ -29,9 +29,11 @@
 // exports slot c divided by Gamma_c = max_{c' > c} zmax_{c'} (one value per slot, the same
 // in every CTA, recorded in `sscale`), so that the 1/Z factors cannot overflow fp16.
 //
-// The operands come from a pre-pass (launch_tc_scan_operands): per 64-token stage the
-// transposed fp16 key block Kt[n][j], the weighted values fp16(w_j val_j) and the normaliser
-// column, all loaded by TMA.  Warp roles (576 threads): warps 0-7 build the A operand
+// The operands come from a pre-pass (launch_tc_scan_operands): per 64-token stage one
+// [192][64] fp16 block holding the transposed key block Kt[n][j], the weighted values
+// fp16(w_j val_j) and the normaliser column.  One TMA request brings two consecutive stages
+// (48 KB): a TMA request costs a few hundred ns of issue time whatever its size, so large
+// requests are what keeps the stream ahead of the tensor cores.  Warp roles (576 threads): warps 0-7 build the A operand
 // straight from the Kt tile (warp w: tensor-memory lane quadrant w % 4, half w / 4 of the
 // 64 rows of a stage); warps 8-15 fold the accumulator into the running state once per chunk
 // (warp 8+e: tile e / 4, quadrant e % 4; one state row per thread) and export it; warp 16
@@ -49,14 +51,15 @@ namespace tcscan {
 constexpr int C = TC_CHUNK;     // chunk length
 constexpr int KS = 64;          // tokens per stage
 constexpr int SPC = C / KS;     // stages per chunk
-constexpr int NS = 4;           // stage buffers
+constexpr int NP = 4;           // stage-pair buffers (one TMA request brings two stages)
 constexpr int NN = 80;          // MMA N
 constexpr int NG_THREADS = 256, NE_THREADS = 256;
 constexpr int WARP_TMA = 16, WARP_MMA = 17;
 constexpr int THREADS = 18 * 32;
 constexpr int TILE = KS * 128;                // one [64][64] 16-bit tile, 128B-swizzled
 constexpr int STAGE = 3 * TILE;               // Kt, then the value block and the normaliser block
-constexpr int SMEM_BYTES = NS * STAGE + 1024;
+constexpr int PSLOT = 2 * STAGE;              // two consecutive stages
+constexpr int SMEM_BYTES = NP * PSLOT + 1024;
 constexpr uint32_t TM_H = 0;                  // accumulator: tile t at t * 80
 constexpr uint32_t TM_A = 160;                // A buffers: 160 + buf*128 + tile*64 + {0: hi, 32: lo}
 constexpr uint32_t TMEM_COLS = 512;
@@ -80,13 +83,11 @@ struct Args {
 
 using namespace tcscan;
 
-__global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_constant__ CUtensorMap tmKt,
-                                                                   const __grid_constant__ CUtensorMap tmWV,
-                                                                   const __grid_constant__ CUtensorMap tmWZ,
+__global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_constant__ CUtensorMap tmOps,
                                                                    const __grid_constant__ Args a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_align1024(smem_raw);
-    __shared__ __align__(8) uint64_t bar_full[NS], bar_empty[NS], bar_afull[2], bar_aempty[2], bar_hfull,
+    __shared__ __align__(8) uint64_t bar_full[NP], bar_empty[NP], bar_afull[2], bar_aempty[2], bar_hfull,
         bar_hempty, bar_done;
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_s;
@@ -100,7 +101,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
     const uint32_t sbase = smem_u32(smem);
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < NS; ++i) {
+        for (int i = 0; i < NP; ++i) {
             mbar_init(smem_u32(&bar_full[i]), 1);
             mbar_init(smem_u32(&bar_empty[i]), 1);
         }
@@ -128,28 +129,25 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
     if (warp == WARP_TMA) {
         // ---------------------------------------------------------------- TMA producer
         if (lane == 0) {
-            prefetch_tmap(&tmKt);
-            prefetch_tmap(&tmWV);
-            prefetch_tmap(&tmWZ);
+            prefetch_tmap(&tmOps);
+            const int npairs = nstages / 2;          // stage pairs never straddle a chunk
             int issued = 0;
-            for (int gs = 0; gs < nstages && !abort_s; ++gs) {
-                const int sb = gs % NS;
-                if (gs >= NS && !mbar_wait(smem_u32(&bar_empty[sb]), ((gs / NS) - 1) & 1, a.status)) {
+            for (int pg = 0; pg < npairs && !abort_s; ++pg) {
+                const int ps = pg % NP;
+                if (pg >= NP && !mbar_wait(smem_u32(&bar_empty[ps]), ((pg / NP) - 1) & 1, a.status)) {
                     abort_s = 1;
                     break;
                 }
-                const int c = chunk_of(gs / SPC), s = gs % SPC;
-                const int stg = c * SPC + s;             // stage index within the sequence
-                const uint32_t fb = smem_u32(&bar_full[sb]), dst = sbase + sb * STAGE;
-                mbar_arrive_expect_tx(fb, STAGE);
-                tma_load_3d(dst, &tmKt, fb, 0, 0, (int)(bh * (a.Tp / KS) + stg));
-                tma_load_3d(dst + TILE, &tmWV, fb, 0, stg * KS, (int)bh);
-                tma_load_3d(dst + 2 * TILE, &tmWZ, fb, 0, stg * KS, (int)bh);
-                issued = gs + 1;
+                const int c = chunk_of(pg / (SPC / 2));
+                const int stg = c * SPC + (pg % (SPC / 2)) * 2;   // first stage of the pair in the sequence
+                const uint32_t fb = smem_u32(&bar_full[ps]);
+                mbar_arrive_expect_tx(fb, PSLOT);
+                tma_load_3d(sbase + ps * PSLOT, &tmOps, fb, 0, 0, (int)(bh * (a.Tp / KS) + stg));
+                issued = pg + 1;
             }
-            // wait for the last use of every stage buffer, so no copy is in flight at exit
-            for (int gs = issued - 1; gs >= 0 && gs >= issued - NS; --gs)
-                mbar_wait(smem_u32(&bar_full[gs % NS]), (gs / NS) & 1, a.status);
+            // wait for the last use of every pair buffer, so no copy is in flight at exit
+            for (int pg = issued - 1; pg >= 0 && pg >= issued - NP; --pg)
+                mbar_wait(smem_u32(&bar_full[pg % NP]), (pg / NP) & 1, a.status);
         }
     } else if (warp == WARP_MMA) {
         // ---------------------------------------------------------------- MMA issuer
@@ -159,12 +157,12 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
                 if (it >= 1 && !(ok = mbar_wait(smem_u32(&bar_hempty), (it - 1) & 1, a.status))) break;
                 tc_fence_after();
                 for (int s = 0; s < SPC; ++s) {
-                    const int gs = it * SPC + s, sb = gs % NS, ab = gs & 1;
+                    const int gs = it * SPC + s, pg = gs >> 1, ps = pg % NP, ab = gs & 1;
                     if (abort_s) { ok = false; break; }
-                    if (!(ok = mbar_wait(smem_u32(&bar_full[sb]), (gs / NS) & 1, a.status))) break;
+                    if ((gs & 1) == 0 && !(ok = mbar_wait(smem_u32(&bar_full[ps]), (pg / NP) & 1, a.status))) break;
                     if (!(ok = mbar_wait(smem_u32(&bar_afull[ab]), (gs >> 1) & 1, a.status))) break;
                     tc_fence_after();
-                    const uint32_t vb = sbase + sb * STAGE + TILE;
+                    const uint32_t vb = sbase + ps * PSLOT + (gs & 1) * STAGE + TILE;
 #pragma unroll
                     for (int t = 0; t < 2; ++t)
 #pragma unroll
@@ -174,7 +172,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
                             umma_bf16_ts(tmem + TM_H + t * 80, aa, bd, IDESC, (s > 0 || kk > 0) ? 1u : 0u);
                             umma_bf16_ts(tmem + TM_H + t * 80, aa + 32, bd, IDESC, 1u);
                         }
-                    umma_commit(smem_u32(&bar_empty[sb]));
+                    if (gs & 1) umma_commit(smem_u32(&bar_empty[ps]));
                     umma_commit(smem_u32(&bar_aempty[ab]));
                 }
                 if (!ok) break;
@@ -190,8 +188,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
         const int l = quad * 32 + lane;              // tensor-memory lane = tile row
         const int n = l & 63, moff = l >> 6;
         for (int gs = 0; gs < nstages; ++gs) {
-            const int sb = gs % NS, ab = gs & 1;
-            if (abort_s || !mbar_wait(smem_u32(&bar_full[sb]), (gs / NS) & 1, a.status)) {
+            const int pg = gs >> 1, ps = pg % NP, ab = gs & 1;
+            if (abort_s || !mbar_wait(smem_u32(&bar_full[ps]), (pg / NP) & 1, a.status)) {
                 abort_s = 1;
                 break;
             }
@@ -200,7 +198,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
                 break;
             }
             tc_fence_after();
-            const uint32_t kt = sbase + sb * STAGE;   // Kt tile: row n = key_j[n] over j, swizzled
+            const uint32_t kt = sbase + ps * PSLOT + (gs & 1) * STAGE;   // Kt tile: row n = key_j[n] over j, swizzled
             // key_j[n] for this thread's 32 rows j of the stage, as fp16 pairs
             uint32_t kp[16];
 #pragma unroll
@@ -324,11 +322,12 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
 }
 
 cudaError_t tc_state_scan(const Problem& p, const ScanIO& io, cudaStream_t s) {
-    CUtensorMap tk, tv, tz;
+    CUtensorMap tops;
     const uint64_t BH = (uint64_t)p.BH(), Tp = (uint64_t)p.Tp();
-    if (!make_tmap_bf16_3d(&tk, io.Kt, BH * (Tp / KS), 64, 64, 64) || !make_tmap_bf16_3d(&tv, io.WV, BH, Tp, 64, KS) ||
-        !make_tmap_bf16_3d(&tz, io.WZ, BH, Tp, 64, KS))
-        return cudaErrorInvalidValue;
+    const uint64_t dims[3] = {64, (uint64_t)TC_OPS_ROWS, BH * (Tp / KS)};
+    const uint64_t strides[2] = {128, (uint64_t)TC_OPS_ROWS * 128};
+    const uint32_t box[3] = {64, (uint32_t)TC_OPS_ROWS, 2};
+    if (!make_tmap_f16_nd(&tops, io.ops, 3, dims, strides, box)) return cudaErrorInvalidValue;
     int* status = tc_status_ptr();
     if (!status) return cudaErrorInvalidValue;
     Args a{io.g, io.zmax, io.S0, io.z0, (__half*)io.Sx, io.zx, io.sscale, io.S_final, io.z_final, status, p.T, p.NC,
@@ -336,7 +335,7 @@ cudaError_t tc_state_scan(const Problem& p, const ScanIO& io, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(tc_state_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     dim3 grid(16, (unsigned)p.BH());
-    tc_state_scan_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(tk, tv, tz, a);
+    tc_state_scan_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(tops, a);
     return cudaGetLastError();
 }
 
