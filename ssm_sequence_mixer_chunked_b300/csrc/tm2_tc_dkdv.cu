@@ -1,0 +1,467 @@
+// tm2_tc_dkdv.cu -- the key / value / A-mask gradients of the tensor-core path (bf16 inputs,
+// d = dv = 64).
+//
+// "2Mamba2Furious", App. C / C.1: inside chunk c (chunk-local running sums A, chunk total g),
+//   s_ij = q_i . k_j,  E_ij = exp(A_i - A_j) [j <= i],  W_ij = s_ij^2 E_ij,  Vt_j = [v_j, 1],
+//   dL/dY_i = zeta_i u_i,  u_i = [dO_i, ucol_i]  (zeta = 1/Z, ucol = -dO.o when normalised),
+//   dSs_ij = 2 s_ij E_ij zeta_i (u_i . Vt_j)          (gradient w.r.t. s_ij),
+// and dS_c, dz_c the gradient w.r.t. the state at the end of the chunk (symmetric in (m, n)
+// because the backward has no initial state; stored scaled by 1/Gamma_c, Gamma_c = sscale):
+//   dk_j[m] = sum_i dSs_ij q_i[m] + 2 w_j Gamma_c sum_n k_j[n] ( sum_col v_j[col] dS[(m,n), col] + dz[(m,n)] )
+//   dv_j    = sum_i W_ij zeta_i dO_i + w_j Gamma_c sum_n k_j[n] sum_m k_j[m] dS[(m,n), :]
+//   dcumA_j = rowterm_j - Vt_j . dVt_j,      w_j = exp(g_c - A_j)
+// (the row-axis sum minus the column-axis sum of the A-mask gradient; rowterm = dY.Y is 0
+// when normalised; dVt_j[dv] = sum_i W_ij zeta_i ucol_i + w_j Gamma_c sum_{m,n} k_j[m] k_j[n] dz[(m,n)]).
+//
+// One CTA per (128-key tile, chunk, b, h).  The inter-chunk sums run first, over 16 groups of
+// four state slices n = 4g .. 4g+3, each one TMA box per plane ([n'][m][col], fp16 hi and
+// residual planes):
+//   U'_g[j][(n', m)]   = sum_col v_j[col] dS[(m, 4g+n'), col]   (N = 256, the box K-major)
+//   U_g[j][(n', col)]  = sum_m   k_j[m]   dS[(m, 4g+n'), col]   (N = 256, the box MN-major)
+// in the two halves of tensor memory, and the compute warps fold them into fp32 registers,
+// dkx[m] += k_j[4g+n'] U'_g, dvx[col] += k_j[4g+n'] U_g.  A tensor-core instruction costs about
+// the same for any N up to 256, so four slices per instruction keeps this part short.
+// A 17th product U'_z = K dzm^T (dzm[m][n] = dz[(m,n)]) adds the normaliser column.
+// The intra-chunk part follows in the same tensor memory: per 64-query block, s^T = K Q^T and
+// (u.Vt)^T = V dO^T (bf16), dSs^T and (W zeta)^T as bf16 hi + lo in tensor memory, then
+// dk += dSs^T Q and dv += (W zeta)^T dO.
+// Warps 0-7 compute (warp w: tensor-memory lane quadrant w % 4, column half w / 4), warp 8
+// issues TMA, warp 9 the MMAs.  Every mbarrier wait is bounded (TM2_ERR_TIMEOUT on expiry).
+#include "tm2.h"
+#include "tm2_launch.h"
+#include "tm2_sm100.cuh"
+#include "tm2_tc.h"
+#include "tm2_tc_tiles.cuh"
+
+namespace tm2 {
+namespace tckv {
+using namespace tctile;
+
+constexpr int C = TC_CHUNK;
+constexpr int THREADS = 10 * 32;
+constexpr int WARP_TMA = 8, WARP_MMA = 9;
+constexpr int NR = 5;                         // ring slots of 32 KB
+constexpr int RB = 32768;
+constexpr int NG = 16;                        // groups of four state slices
+constexpr int NREQ = 2 * NG + 3;              // hi/lo plane of each group, then K|V, Q, dO (intra part)
+constexpr int EARLY = NR - 1;                 // slot NR-1 first holds the K and V tiles for conversion
+// shared memory
+constexpr int RING = 0;
+constexpr int SKH = NR * RB, SVH = SKH + 16384;      // fp16 copies of the K and V tiles [128][64]
+constexpr int SZH = SVH + 16384, SZL = SZH + 8192;   // normaliser gradient matrix hi / lo
+constexpr int SAV = SZL + 8192;                      // A, zeta, ucol: 3 x 256 floats
+constexpr int SRED = SAV + 3072;                     // 128 partial sums
+constexpr int BYTES = SRED + 1024 + 1024;
+// tensor memory: U' in [0, 256), U in [256, 512); the intra part reuses both afterwards
+constexpr uint32_t TM_UP = 0, TM_U = 256;
+constexpr uint32_t TM_DK = 0, TM_DV = 64, TM_S = 128, TM_W = 192, TM_DH = 256, TM_DL = 288, TM_WH = 320, TM_WL = 352;
+constexpr uint32_t TM_PARK = 384;             // inter-chunk sums parked during the intra part: 384 + 64h
+constexpr uint32_t IDESC_UP = idesc_f16_f32(128, 256, false, false);
+constexpr uint32_t IDESC_U = idesc_f16_f32(128, 256, false, true);
+constexpr uint32_t IDESC_Z = idesc_f16_f32(128, 64, false, false);
+constexpr uint32_t IDESC_BF_K = idesc_bf16_f32(128, 64, false, false);
+constexpr uint32_t IDESC_BF_MN = idesc_bf16_f32(128, 64, false, true);
+
+struct Args {
+    const float* Aloc;    // [BH][Tp]
+    const float* g;       // [BH][NC]
+    const float* zeta;    // [BH][T]
+    const float* ucol;    // [BH][T]
+    const float* rowterm; // [BH][T]
+    const float* dzx;     // [BH][NC][4096] gradient normaliser states (unscaled)
+    const float* sscale;  // [BH][NC] scale of the gradient state planes
+    float* dk;            // [BH][T][64]
+    float* dv;            // [BH][T][64]
+    float* dcum;          // [BH][T]
+    int* status;
+    int T, NC, Tp;
+};
+
+TM2_DEV int slot_of(int r) { return r % NR; }
+TM2_DEV uint32_t use_of(int r) { return (uint32_t)(r / NR); }
+
+}  // namespace tckv
+
+using namespace tckv;
+
+__global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmK,
+                                                                 const __grid_constant__ CUtensorMap tmV,
+                                                                 const __grid_constant__ CUtensorMap tmQ,
+                                                                 const __grid_constant__ CUtensorMap tmD,
+                                                                 const __grid_constant__ CUtensorMap tmS,
+                                                                 const __grid_constant__ Args a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_align1024(smem_raw);
+    __shared__ __align__(8) uint64_t bar_ld, bar_full[NR], bar_empty[NR], bar_cvt, bar_sfull[4], bar_sfree[4],
+        bar_pfull[4], bar_pfree[4], bar_ufull[2], bar_uempty[2], bar_kvfull, bar_red, bar_done;
+    __shared__ uint32_t tmem_base_s;
+    __shared__ volatile int abort_s;
+    __shared__ volatile int gflags[2];         // group waits of the compute warps
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tj = blockIdx.x & 1, c = blockIdx.x >> 1;
+    const long bh = blockIdx.y;
+    const int NC = a.NC;
+    const int nblk = 4 - 2 * tj;                 // 64-query blocks at or after this key tile
+    const uint32_t sb0 = smem_u32(smem);
+    float* sAv = reinterpret_cast<float*>(smem + SAV);
+    float* sZe = sAv + 256;
+    float* sUc = sAv + 512;
+    float* sRed = reinterpret_cast<float*>(smem + SRED);
+
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar_ld), 1);
+        for (int i = 0; i < NR; ++i) {
+            mbar_init(smem_u32(&bar_full[i]), 1);
+            mbar_init(smem_u32(&bar_empty[i]), 1);
+        }
+        mbar_init(smem_u32(&bar_cvt), 256);
+        for (int b = 0; b < 4; ++b) {
+            mbar_init(smem_u32(&bar_sfull[b]), 1);
+            mbar_init(smem_u32(&bar_sfree[b]), 256);
+            mbar_init(smem_u32(&bar_pfull[b]), 256);
+            mbar_init(smem_u32(&bar_pfree[b]), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&bar_ufull[i]), 1);
+            mbar_init(smem_u32(&bar_uempty[i]), 256);
+        }
+        mbar_init(smem_u32(&bar_kvfull), 1);
+        mbar_init(smem_u32(&bar_red), 256);
+        mbar_init(smem_u32(&bar_done), 1);
+        abort_s = 0;
+        fence_mbar_init();
+    }
+    for (int j = threadIdx.x; j < C; j += THREADS) {
+        const long tok = (long)c * C + j;
+        sAv[j] = a.Aloc[bh * a.Tp + tok];
+        sZe[j] = tok < a.T ? a.zeta[bh * a.T + tok] : 0.f;
+        sUc[j] = tok < a.T ? a.ucol[bh * a.T + tok] : 0.f;
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(&tmem_base_s), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_s;
+    const uint32_t early = sb0 + RING + EARLY * RB;   // K tile at +0, V tile at +16384
+
+    if (warp == WARP_TMA) {
+        if (lane == 0) {
+            prefetch_tmap(&tmS);
+            const uint32_t lb = smem_u32(&bar_ld);
+            mbar_arrive_expect_tx(lb, 2 * 16384);
+            tma_load_3d(early, &tmK, lb, 0, c * C + tj * 128, (int)bh);
+            tma_load_3d(early + 16384, &tmV, lb, 0, c * C + tj * 128, (int)bh);
+            const int chunk_id = (int)(bh * NC + c);
+            int issued = 0;
+            for (int r = 0; r < NREQ && !abort_s; ++r) {
+                const int sl = slot_of(r);
+                const uint32_t u = use_of(r);
+                if (u > 0 && !mbar_wait(smem_u32(&bar_empty[sl]), (u - 1) & 1, a.status)) {
+                    abort_s = 1;
+                    break;
+                }
+                if (r == EARLY && !mbar_wait(smem_u32(&bar_cvt), 0, a.status)) {   // copies made: slot free
+                    abort_s = 1;
+                    break;
+                }
+                const uint32_t fb = smem_u32(&bar_full[sl]), dst = sb0 + RING + sl * RB;
+                mbar_arrive_expect_tx(fb, RB);
+                if (r < 2 * NG) {
+                    tma_load_5d(dst, &tmS, fb, 0, 0, 4 * (r >> 1), r & 1, chunk_id);
+                } else if (r == 2 * NG) {
+                    tma_load_3d(dst, &tmK, fb, 0, c * C + tj * 128, (int)bh);
+                    tma_load_3d(dst + 16384, &tmV, fb, 0, c * C + tj * 128, (int)bh);
+                } else {
+                    tma_load_3d(dst, r == 2 * NG + 1 ? &tmQ : &tmD, fb, 0, c * C, (int)bh);
+                }
+                issued = r + 1;
+            }
+            // no copy may be in flight at exit
+            mbar_wait(lb, 0, a.status);
+            for (int r = issued - 1; r >= 0 && r >= issued - NR; --r)
+                mbar_wait(smem_u32(&bar_full[slot_of(r)]), use_of(r) & 1, a.status);
+        }
+    } else if (warp == WARP_MMA) {
+        if (lane == 0) {
+            bool ok = mbar_wait(smem_u32(&bar_cvt), 0, a.status);
+            tc_fence_after();
+            // ---- inter-chunk: U'_g = V B_g^T (K-major view), U_g = K B_g (MN-major view), then U'_z
+            for (int g = 0; g <= NG && ok; ++g) {
+                if (abort_s) { ok = false; break; }
+                if (g < NG) {
+                    const int r0 = 2 * g, r1 = 2 * g + 1;
+                    if (!(ok = mbar_wait(smem_u32(&bar_full[slot_of(r0)]), use_of(r0) & 1, a.status))) break;
+                    if (!(ok = mbar_wait(smem_u32(&bar_full[slot_of(r1)]), use_of(r1) & 1, a.status))) break;
+                }
+                if (g > 0 && !(ok = mbar_wait(smem_u32(&bar_uempty[0]), (uint32_t)(g - 1) & 1, a.status))) break;
+                tc_fence_after();
+                if (g < NG) {
+                    const uint32_t bhi = sb0 + RING + slot_of(2 * g) * RB, blo = sb0 + RING + slot_of(2 * g + 1) * RB;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma_bf16(tmem + TM_UP, sdesc_sw128(sb0 + SVH + kk * 32), sdesc_sw128(bhi + kk * 32), IDESC_UP,
+                                  kk > 0);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma_bf16(tmem + TM_UP, sdesc_sw128(sb0 + SVH + kk * 32), sdesc_sw128(blo + kk * 32), IDESC_UP,
+                                  1u);
+                    umma_commit(smem_u32(&bar_ufull[0]));
+                    if (g > 0 && !(ok = mbar_wait(smem_u32(&bar_uempty[1]), (uint32_t)(g - 1) & 1, a.status))) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma_bf16(tmem + TM_U, sdesc_sw128(sb0 + SKH + kk * 32),
+                                  sdesc_sw128_ex(bhi + kk * 2048, 8192, 1024), IDESC_U, kk > 0);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma_bf16(tmem + TM_U, sdesc_sw128(sb0 + SKH + kk * 32),
+                                  sdesc_sw128_ex(blo + kk * 2048, 8192, 1024), IDESC_U, 1u);
+                    umma_commit(smem_u32(&bar_empty[slot_of(2 * g)]));
+                    umma_commit(smem_u32(&bar_empty[slot_of(2 * g + 1)]));
+                    umma_commit(smem_u32(&bar_ufull[1]));
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        umma_bf16(tmem + TM_UP, sdesc_sw128(sb0 + SKH + kk * 32), sdesc_sw128(sb0 + SZH + kk * 32),
+                                  IDESC_Z, kk > 0);
+                        umma_bf16(tmem + TM_UP, sdesc_sw128(sb0 + SKH + kk * 32), sdesc_sw128(sb0 + SZL + kk * 32),
+                                  IDESC_Z, 1u);
+                    }
+                    umma_commit(smem_u32(&bar_ufull[0]));
+                }
+            }
+            // ---- intra-chunk: dk += (dSs^T) Q, dv += (W zeta)^T dO over the 64-query blocks
+            const int rkv = 2 * NG, rq = 2 * NG + 1, rd = 2 * NG + 2;
+            if (ok) ok = mbar_wait(smem_u32(&bar_uempty[0]), (uint32_t)NG & 1, a.status);          // U'_z read
+            if (ok) ok = mbar_wait(smem_u32(&bar_uempty[1]), (uint32_t)(NG - 1) & 1, a.status);    // last U read
+            if (ok) ok = mbar_wait(smem_u32(&bar_full[slot_of(rkv)]), use_of(rkv) & 1, a.status);
+            if (ok) ok = mbar_wait(smem_u32(&bar_full[slot_of(rq)]), use_of(rq) & 1, a.status);
+            if (ok) ok = mbar_wait(smem_u32(&bar_full[slot_of(rd)]), use_of(rd) & 1, a.status);
+            tc_fence_after();
+            const uint32_t SK = sb0 + RING + slot_of(rkv) * RB, SV = SK + 16384;
+            const uint32_t SQ = sb0 + RING + slot_of(rq) * RB, SD = sb0 + RING + slot_of(rd) * RB;
+            for (int b = 0; b < nblk && ok; ++b) {
+                const int ib = 2 * tj + b;
+                if (abort_s) { ok = false; break; }
+                if (b > 0 && !(ok = mbar_wait(smem_u32(&bar_sfree[b - 1]), 0, a.status))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    umma_bf16(tmem + TM_S, sdesc_sw128(SK + kk * 32), sdesc_sw128(SQ + ib * 8192 + kk * 32), IDESC_BF_K,
+                              kk > 0);
+                    umma_bf16(tmem + TM_W, sdesc_sw128(SV + kk * 32), sdesc_sw128(SD + ib * 8192 + kk * 32), IDESC_BF_K,
+                              kk > 0);
+                }
+                umma_commit(smem_u32(&bar_sfull[b]));
+                if (!(ok = mbar_wait(smem_u32(&bar_pfull[b]), 0, a.status))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint64_t qd = sdesc_sw128_ex(SQ + ib * 8192 + kk * 2048, 8192, 1024);
+                    const uint64_t dd = sdesc_sw128_ex(SD + ib * 8192 + kk * 2048, 8192, 1024);
+                    const uint32_t acc0 = (b > 0 || kk > 0) ? 1u : 0u;
+                    umma_bf16_ts(tmem + TM_DK, tmem + TM_DH + kk * 8, qd, IDESC_BF_MN, acc0);
+                    umma_bf16_ts(tmem + TM_DK, tmem + TM_DL + kk * 8, qd, IDESC_BF_MN, 1u);
+                    umma_bf16_ts(tmem + TM_DV, tmem + TM_WH + kk * 8, dd, IDESC_BF_MN, acc0);
+                    umma_bf16_ts(tmem + TM_DV, tmem + TM_WL + kk * 8, dd, IDESC_BF_MN, 1u);
+                }
+                umma_commit(smem_u32(&bar_pfree[b]));
+            }
+            if (ok) umma_commit(smem_u32(&bar_kvfull));
+            else abort_s = 1;
+            umma_commit(smem_u32(&bar_done));
+            mbar_wait(smem_u32(&bar_done), 0, a.status);
+        }
+    } else {
+        // ---------------------------------------------------------------- compute warps
+        const int quad = warp & 3, h = warp >> 2;
+        const int l = quad * 32 + lane;                  // tile row (key)
+        const int j = tj * 128 + l;                      // chunk-local key index
+        const long tok = (long)c * C + j;
+        const bool in = tok < a.T;
+        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        const float Aj = sAv[j];
+        float dv64_in = 0.f;
+        int kg = 0;                                      // group-wait counter
+        bool ok = mbar_wait(smem_u32(&bar_ld), 0, a.status);
+        if (ok) {   // fp16 copies of the key and value tiles; the normaliser gradient matrix / scale
+            const int t256 = threadIdx.x;
+            for (int pc = t256; pc < 1024; pc += 256) {
+                tile_bf16_to_f16(early, sb0 + SKH, pc);
+                tile_bf16_to_f16(early + 16384, sb0 + SVH, pc);
+            }
+            build_z_tiles(smem + SZH, smem + SZL, a.dzx + (bh * NC + c) * 4096, 1.f / a.sscale[bh * NC + c], t256);
+            fence_proxy_async();
+        }
+        mbar_arrive(smem_u32(&bar_cvt));
+        // ---- inter-chunk groups
+        float dkx[32], dvx[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) dkx[k] = dvx[k] = 0.f;
+        float dv64x = 0.f;
+        const uint8_t* krow = smem + SKH;
+#pragma unroll 1
+        for (int g = 0; g <= NG && ok; ++g) {
+            if (!(ok = group_wait(smem_u32(&bar_ufull[0]), (uint32_t)g & 1, a.status, warp == 0, 1, 256, gflags, kg,
+                                  &abort_s)))
+                break;
+            if (g < NG) {
+#pragma unroll 1
+                for (int np = 0; np < 4; ++np) {
+                    float u[32];
+                    tmem_ld32(tmem + lane_base + TM_UP + np * 64 + h * 32, u);
+                    if (np == 3) {
+                        tc_fence_before();
+                        mbar_arrive(smem_u32(&bar_uempty[0]));
+                    }
+                    const float kn = __half2float(*reinterpret_cast<const __half*>(krow + swz_elem(l, 4 * g + np)));
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) dkx[k] = fmaf(kn, u[k], dkx[k]);
+                }
+                if (!(ok = group_wait(smem_u32(&bar_ufull[1]), (uint32_t)g & 1, a.status, warp == 0, 1, 256, gflags, kg,
+                                      &abort_s)))
+                    break;
+#pragma unroll 1
+                for (int np = 0; np < 4; ++np) {
+                    float u[32];
+                    tmem_ld32(tmem + lane_base + TM_U + np * 64 + h * 32, u);
+                    if (np == 3) {
+                        tc_fence_before();
+                        mbar_arrive(smem_u32(&bar_uempty[1]));
+                    }
+                    const float kn = __half2float(*reinterpret_cast<const __half*>(krow + swz_elem(l, 4 * g + np)));
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) dvx[k] = fmaf(kn, u[k], dvx[k]);
+                }
+            } else {
+                float u[32];
+                tmem_ld32(tmem + lane_base + TM_UP + h * 32, u);
+                tc_fence_before();
+                mbar_arrive(smem_u32(&bar_uempty[0]));
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    dkx[k] += u[k];
+                    const float km = __half2float(*reinterpret_cast<const __half*>(krow + swz_elem(l, h * 32 + k)));
+                    dv64x = fmaf(km, u[k], dv64x);
+                }
+            }
+        }
+        // park the inter-chunk sums in tensor memory (outside the intra part's columns), once
+        // every compute warp has read the last U (whose columns these are)
+        named_bar_sync(1, 256);
+        tmem_st32(tmem + lane_base + TM_PARK + h * 64, dkx);
+        tmem_st32(tmem + lane_base + TM_PARK + h * 64 + 32, dvx);
+        tmem_wait_st();
+        // ---- intra-chunk blocks (queries i >= j)
+        for (int b = 0; b < nblk && ok; ++b) {
+            const int ib = 2 * tj + b;
+            if (!(ok = group_wait(smem_u32(&bar_sfull[b]), 0, a.status, warp == 0, 1, 256, gflags, kg, &abort_s))) break;
+            if (b > 0 && !(ok = group_wait(smem_u32(&bar_pfree[b - 1]), 0, a.status, warp == 0, 1, 256, gflags, kg,
+                                           &abort_s)))
+                break;
+#pragma unroll
+            for (int g2 = 0; g2 < 2; ++g2) {
+                const int cc = 2 * h + g2;
+                float sv[16], wv[16];
+                tmem_ld16(tmem + lane_base + TM_S + cc * 16, sv);
+                tmem_ld16(tmem + lane_base + TM_W + cc * 16, wv);
+                uint32_t dh[8], dl[8], wh[8], wl[8];
+#pragma unroll
+                for (int k2 = 0; k2 < 8; ++k2) {
+                    float d2h[2], d2l[2], w2h[2], w2l[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int i = ib * 64 + cc * 16 + 2 * k2 + u;
+                        const int kx = 2 * k2 + u;
+                        float ds = 0.f, wz = 0.f;
+                        if (i >= j) {
+                            const float E = __expf(sAv[i] - Aj), ze = sZe[i], s = sv[kx];
+                            ds = 2.f * s * E * (wv[kx] + sUc[i]) * ze;
+                            wz = s * s * E * ze;
+                            dv64_in = fmaf(wz, sUc[i], dv64_in);
+                        }
+                        d2h[u] = __bfloat162float(__float2bfloat16_rn(ds));
+                        d2l[u] = ds - d2h[u];
+                        w2h[u] = __bfloat162float(__float2bfloat16_rn(wz));
+                        w2l[u] = wz - w2h[u];
+                    }
+                    dh[k2] = pack_bf16x2(d2h[0], d2h[1]);
+                    dl[k2] = pack_bf16x2(d2l[0], d2l[1]);
+                    wh[k2] = pack_bf16x2(w2h[0], w2h[1]);
+                    wl[k2] = pack_bf16x2(w2l[0], w2l[1]);
+                }
+                tmem_st8(tmem + lane_base + TM_DH + cc * 8, dh);
+                tmem_st8(tmem + lane_base + TM_DL + cc * 8, dl);
+                tmem_st8(tmem + lane_base + TM_WH + cc * 8, wh);
+                tmem_st8(tmem + lane_base + TM_WL + cc * 8, wl);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bar_sfree[b]));
+            mbar_arrive(smem_u32(&bar_pfull[b]));
+        }
+        if (ok && !abort_s && (ok = mbar_wait(smem_u32(&bar_kvfull), 0, a.status))) {
+            tc_fence_after();
+            float dk0[32], dv0[32];
+            tmem_ld32(tmem + lane_base + TM_DK + h * 32, dk0);
+            tmem_ld32(tmem + lane_base + TM_DV + h * 32, dv0);
+            tmem_ld32(tmem + lane_base + TM_PARK + h * 64, dkx);
+            tmem_ld32(tmem + lane_base + TM_PARK + h * 64 + 32, dvx);
+            const float wj = __expf(a.g[bh * NC + c] - Aj);
+            const float gsc = a.sscale[bh * NC + c];
+            const float fk = 2.f * wj * gsc, fv = wj * gsc;
+            float vdot = 0.f;
+            const uint8_t* vrow = smem + SVH;
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                dk0[k] += fk * dkx[k];
+                dv0[k] += fv * dvx[k];
+                const float vv = __half2float(*reinterpret_cast<const __half*>(vrow + swz_elem(l, h * 32 + k)));
+                vdot = fmaf(vv, dv0[k], vdot);
+            }
+            const float part = vdot + dv64_in + fv * dv64x;   // this half's share of Vt_j . dVt_j
+            if (h == 1) sRed[l] = part;
+            mbar_arrive(smem_u32(&bar_red));
+            ok = mbar_wait(smem_u32(&bar_red), 0, a.status);
+            if (in) {
+                float4* dkp = reinterpret_cast<float4*>(a.dk + (bh * a.T + tok) * 64 + h * 32);
+                float4* dvp = reinterpret_cast<float4*>(a.dv + (bh * a.T + tok) * 64 + h * 32);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    dkp[u] = make_float4(dk0[4 * u], dk0[4 * u + 1], dk0[4 * u + 2], dk0[4 * u + 3]);
+                    dvp[u] = make_float4(dv0[4 * u], dv0[4 * u + 1], dv0[4 * u + 2], dv0[4 * u + 3]);
+                }
+                if (h == 0 && ok) a.dcum[bh * a.T + tok] = a.rowterm[bh * a.T + tok] - (part + sRed[l]);
+            }
+        }
+        if (!ok) abort_s = 1;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+cudaError_t tc_bwd_dkdv(const Problem& p, const void* q, const void* k, const void* v, const void* dO,
+                        const float* Aloc, const float* g, const float* zeta, const float* ucol, const float* rowterm,
+                        const void* dSx, const float* dzx, const float* sscale, float* dk, float* dv, float* dcum,
+                        cudaStream_t s) {
+    CUtensorMap tk, tv, tq, td, ts;
+    const uint64_t BH = (uint64_t)p.BH(), T = (uint64_t)p.T;
+    if (!make_tmap_bf16_3d(&tk, k, BH, T, 64, 128) || !make_tmap_bf16_3d(&tv, v, BH, T, 64, 128) ||
+        !make_tmap_bf16_3d(&tq, q, BH, T, 64, 256) || !make_tmap_bf16_3d(&td, dO, BH, T, 64, 256) ||
+        !make_tmap_state_tquads(&ts, dSx, BH * (uint64_t)p.NC))
+        return cudaErrorInvalidValue;
+    int* status = tc_status_ptr();
+    if (!status) return cudaErrorInvalidValue;
+    Args a{Aloc, g, zeta, ucol, rowterm, dzx, sscale, dk, dv, dcum, status, p.T, p.NC, (int)p.Tp()};
+    cudaError_t e = cudaFuncSetAttribute(tc_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, BYTES);
+    if (e != cudaSuccess) return e;
+    dim3 grid(2 * p.NC, (unsigned)p.BH());
+    tc_bwd_dkdv_kernel<<<grid, THREADS, BYTES, s>>>(tk, tv, tq, td, ts, a);
+    return cudaGetLastError();
+}
+
+}  // namespace tm2

@@ -6,62 +6,54 @@
 // with P_ij = (q_i . k_j)^2 exp(A_i - A_j) and S_{c-1}, z_{c-1} the state entering the chunk
 // (written by the chunk-state scan as two fp16 planes, hi and residual, and fp32 z).
 //
-// One CTA per (chunk, b, h); the chunk's 256 tokens form two 128-row tiles.
-//  * Intra-chunk (causal 128 x 64 blocks: tile 0 x key blocks 0-1, tile 1 x key blocks 0-3):
-//    s = Q K^T by tcgen05.mma from TMA tiles (bf16, K-major), the compute warps square it,
-//    apply the decay mask in fp32, keep the row sums (Z) in fp32 and write P into tensor
-//    memory as two bf16 terms P_hi + P_lo (one bf16 term alone costs ~2^-9 relative per
-//    weight, enough to break the 2e-2 bar on unnormalised outputs); both are A operands
-//    of P V (V MN-major, straight from its TMA tile).
-//  * Inter-chunk readout: for each m, U_m = Q S_m with S_m[n][col] = S[(m,n), col] (the state
-//    slice by TMA, MN-major, hi and residual plane: two MMAs; Q converted exactly to fp16),
-//    and the compute warps accumulate N_x[col] += q_i[m] U_m[i][col] in fp32.  A 65th
-//    product U = Q zm^T with zm[m][n] = z[(m,n)] gives Z_x = sum_m q_i[m] U[i][m].  No
-//    operand is a rounded product; the readout of nearly orthogonal queries keeps its
-//    precision.
+// One CTA per (128-token tile, chunk, b, h).
+//  * Inter-chunk readout first, over 16 groups of four state slices: U_g[i][(m', col)] =
+//    sum_n q_i[n] S[(4g + m', n), col] is one tcgen05.mma of N = 256 per K step and plane
+//    (Q exact in fp16, the slices MN-major straight from their TMA box), and the compute warps
+//    fold it into fp32 registers, N_x[col] += q_i[4g + m'] U_g[i][(m', col)].  A tensor-core
+//    instruction costs about the same for any N up to 256, so four slices per instruction is
+//    what keeps the readout short.  A 17th product U_z = Q zm^T with zm[m][n] = z[(m,n)] gives
+//    Z_x = sum_m q_i[m] U_z[i][m].  No operand is a rounded product, so the readout of nearly
+//    orthogonal queries keeps its precision.
+//  * Intra-chunk (causal 128 x 64 key blocks) in the same tensor memory afterwards: s = Q K^T
+//    by tcgen05.mma from bf16 TMA tiles, the compute warps square it, apply the decay mask in
+//    fp32, keep the row sums (Z) in fp32 and write P as two bf16 terms P_hi + P_lo (one bf16
+//    term alone costs ~2^-9 relative per weight, enough to break the 2e-2 bar on
+//    unnormalised outputs); both are A operands of P V (V MN-major from its tile).
 //  * Epilogue: [N, Z] = intra + exp(A_i) [N_x, Z_x]; o = N / Z (or N), fp32; Z saved.
-// Warps 0-15 compute (warp w: tile (w >> 2) & 1, tensor-memory lane quadrant w & 3, column
-// half w >> 3), warp 16 issues TMA, warp 17 the MMAs.  Every mbarrier wait is bounded
-// (TM2_ERR_TIMEOUT on expiry).
+// Warps 0-7 compute (warp w: tensor-memory lane quadrant w % 4, column half w / 4), warp 8
+// issues TMA, warp 9 the MMAs.  Every mbarrier wait is bounded (TM2_ERR_TIMEOUT on expiry).
 #include "tm2.h"
 #include "tm2_launch.h"
 #include "tm2_sm100.cuh"
 #include "tm2_tc.h"
+#include "tm2_tc_tiles.cuh"
 
 namespace tm2 {
 namespace tcout {
+using namespace tctile;
 
 constexpr int C = TC_CHUNK;
-constexpr int NP = 5;                        // stages of two state slices (hi + residual planes, 32 KB)
-constexpr int NP_EARLY = 2;                  // stages free from the start; the rest alias the
-                                             // intra-chunk tiles and open once those are done
-constexpr int PBYTES = 32768;
-constexpr int NSL = 65;                      // 64 state slices + the normaliser product
-constexpr int THREADS = 18 * 32;
-constexpr int NCOMP = 512;                   // compute threads
-constexpr int WARP_TMA = 16, WARP_MMA = 17;
-constexpr int TILE_BYTES = C * 128;          // [256][64] 16-bit
-constexpr int STG = 0;                                             // NP x [plane][slice m, m+1][64][64]
-constexpr int SQ = 65536, SK = 98304, SV = 131072;                 // bf16 tiles (stages 2-4)
-constexpr int SQH = 163840;                                        // fp16 copy of Q
-constexpr int SZH = SQH + TILE_BYTES, SZL = SZH + 8192;            // zm hi / lo, [64][64] fp16
-constexpr int SAV = SZL + 8192;                                    // A values, 256 floats
-constexpr int SRED = SAV + 1024;                                   // [2 halves][256 tokens][2]
-constexpr int SMEM_BYTES = SRED + 4096 + 1024;
-constexpr int NBLK = 6;                      // intra-chunk blocks: (tile, 64-key block)
-// tensor-memory columns
-constexpr uint32_t TM_Y = 0;                 // intra N, tile t at t * 64
-constexpr uint32_t TM_S = 128;               // Q K^T block, 64 columns
-constexpr uint32_t TM_PH = 192, TM_PL = 224; // P hi / lo (bf16), 32 columns each
-constexpr uint32_t TM_U = 256;               // U buffers: 256 + buf*128 + tile*64
-constexpr uint32_t TMEM_COLS = 512;
+constexpr int THREADS = 10 * 32;
+constexpr int WARP_TMA = 8, WARP_MMA = 9;
+constexpr int NR = 5;                        // ring slots of 32 KB
+constexpr int RB = 32768;
+constexpr int NG = 16;                       // groups of four state slices
+constexpr int NREQ = 2 * NG + 3;             // hi/lo plane of each group, then Q, K, V (intra part)
+constexpr int EARLY = NR - 1;                // slot NR-1 first holds the Q tile for conversion
+// shared memory
+constexpr int RING = 0;
+constexpr int SQH = NR * RB;                 // fp16 copy of the Q tile [128][64]
+constexpr int SZH = SQH + 16384, SZL = SZH + 8192;   // zm hi / lo, [64][64] fp16
+constexpr int SAV = SZL + 8192;              // chunk-local A, 256 floats
+constexpr int SRED = SAV + 1024;             // [2 halves][128 rows][2]
+constexpr int SMEM_BYTES = SRED + 2048 + 1024;
+// tensor memory: U buffers at 0 and 256; the intra part reuses [0, 256) after the readout
+constexpr uint32_t TM_Y = 0, TM_S = 64, TM_PH = 128, TM_PL = 160;
+constexpr uint32_t IDESC_U = idesc_f16_f32(128, 256, false, true);
+constexpr uint32_t IDESC_Z = idesc_f16_f32(128, 64, false, false);
 constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 64, false, false);
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, 64, false, true);
-constexpr uint32_t IDESC_RD = idesc_f16_f32(128, 64, false, true);
-constexpr uint32_t IDESC_RZ = idesc_f16_f32(128, 64, false, false);
-TM2_DEV int blk_tile(int b) { return b < 2 ? 0 : 1; }
-TM2_DEV int blk_key(int b) { return b < 2 ? b : b - 2; }
-TM2_DEV uint32_t swz_elem(int row, int col) { return row * 128 + ((((col >> 3) ^ (row & 7))) << 4) + (col & 7) * 2; }
 
 struct Args {
     const float* Aloc;   // [BH][Tp]
@@ -71,6 +63,9 @@ struct Args {
     int* status;
     int T, NC, Tp, normalize;
 };
+
+TM2_DEV int slot_of(int r) { return r % NR; }
+TM2_DEV uint32_t use_of(int r) { return (uint32_t)(r / NR); }
 
 }  // namespace tcout
 
@@ -83,27 +78,28 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
                                                                   const __grid_constant__ Args a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_align1024(smem_raw);
-    __shared__ __align__(8) uint64_t bar_qkv, bar_full[NP], bar_empty[NP], bar_cvt, bar_sfull[NBLK], bar_sfree[NBLK],
-        bar_pfull[NBLK], bar_pfree[NBLK], bar_ufull[2], bar_uempty[2], bar_yfull, bar_red, bar_intra, bar_done;
+    __shared__ __align__(8) uint64_t bar_ld, bar_full[NR], bar_empty[NR], bar_cvt, bar_sfull[4], bar_sfree[4],
+        bar_pfull[4], bar_pfree[4], bar_ufull[2], bar_uempty[2], bar_yfull, bar_red, bar_done;
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_s;
-    __shared__ volatile int gflags[3][2];      // group waits: all compute warps, tile 0, tile 1
+    __shared__ volatile int gflags[2];         // group waits of the compute warps
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int c = blockIdx.x;
+    const int t = blockIdx.x & 1, c = blockIdx.x >> 1;
     const long bh = blockIdx.y;
     const int NC = a.NC;
+    const int nblk = 2 * (t + 1);                // 64-key blocks at or before this tile
     const uint32_t sb0 = smem_u32(smem);
     float* sAv = reinterpret_cast<float*>(smem + SAV);
     float* sRed = reinterpret_cast<float*>(smem + SRED);
 
     if (threadIdx.x == 0) {
-        mbar_init(smem_u32(&bar_qkv), 1);
-        for (int i = 0; i < NP; ++i) {
+        mbar_init(smem_u32(&bar_ld), 1);
+        for (int i = 0; i < NR; ++i) {
             mbar_init(smem_u32(&bar_full[i]), 1);
             mbar_init(smem_u32(&bar_empty[i]), 1);
         }
-        mbar_init(smem_u32(&bar_cvt), NCOMP);
-        for (int b = 0; b < NBLK; ++b) {   // one set per intra-chunk block, each used once
+        mbar_init(smem_u32(&bar_cvt), 256);
+        for (int b = 0; b < 4; ++b) {
             mbar_init(smem_u32(&bar_sfull[b]), 1);
             mbar_init(smem_u32(&bar_sfree[b]), 256);
             mbar_init(smem_u32(&bar_pfull[b]), 256);
@@ -111,108 +107,127 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&bar_ufull[i]), 1);
-            mbar_init(smem_u32(&bar_uempty[i]), NCOMP);
+            mbar_init(smem_u32(&bar_uempty[i]), 256);
         }
         mbar_init(smem_u32(&bar_yfull), 1);
-        mbar_init(smem_u32(&bar_intra), 1);
-        mbar_init(smem_u32(&bar_red), NCOMP);
+        mbar_init(smem_u32(&bar_red), 256);
         mbar_init(smem_u32(&bar_done), 1);
         abort_s = 0;
         fence_mbar_init();
     }
     for (int j = threadIdx.x; j < C; j += THREADS) sAv[j] = a.Aloc[bh * a.Tp + (long)c * C + j];
     if (warp == 0) {
-        tmem_alloc(smem_u32(&tmem_base_s), TMEM_COLS);
+        tmem_alloc(smem_u32(&tmem_base_s), 512);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base_s;
+    const uint32_t early = sb0 + RING + EARLY * RB;   // the Q tile, converted at the start
 
     if (warp == WARP_TMA) {
         if (lane == 0) {
             prefetch_tmap(&tmS);
-            const uint32_t qb = smem_u32(&bar_qkv);
-            mbar_arrive_expect_tx(qb, 3 * TILE_BYTES);
-            tma_load_3d(sb0 + SQ, &tmQ, qb, 0, c * C, (int)bh);
-            tma_load_3d(sb0 + SK, &tmK, qb, 0, c * C, (int)bh);
-            tma_load_3d(sb0 + SV, &tmV, qb, 0, c * C, (int)bh);
-            int issued = 0;
+            const uint32_t lb = smem_u32(&bar_ld);
+            mbar_arrive_expect_tx(lb, 16384);
+            tma_load_3d(early, &tmQ, lb, 0, c * C + t * 128, (int)bh);
             const int chunk_id = (int)(bh * NC + c);
-            for (int pp = 0; pp < 32 && !abort_s; ++pp) {   // slices 2pp, 2pp+1, both planes
-                const int ps = pp % NP;
-                if (pp >= NP && !mbar_wait(smem_u32(&bar_empty[ps]), ((pp / NP) - 1) & 1, a.status)) {
+            int issued = 0;
+            for (int r = 0; r < NREQ && !abort_s; ++r) {
+                const int sl = slot_of(r);
+                const uint32_t u = use_of(r);
+                if (u > 0 && !mbar_wait(smem_u32(&bar_empty[sl]), (u - 1) & 1, a.status)) {
                     abort_s = 1;
                     break;
                 }
-                if (pp == NP_EARLY && (!mbar_wait(smem_u32(&bar_intra), 0, a.status) ||
-                                       !mbar_wait(smem_u32(&bar_cvt), 0, a.status))) {   // tiles dead, copies made
+                if (r == EARLY && !mbar_wait(smem_u32(&bar_cvt), 0, a.status)) {   // copy made: slot free
                     abort_s = 1;
                     break;
                 }
-                const uint32_t fb = smem_u32(&bar_full[ps]);
-                mbar_arrive_expect_tx(fb, PBYTES);
-                tma_load_4d(sb0 + STG + ps * PBYTES, &tmS, fb, 0, pp * 128, 0, chunk_id);
-                issued = pp + 1;
+                const uint32_t fb = smem_u32(&bar_full[sl]), dst = sb0 + RING + sl * RB;
+                if (r < 2 * NG) {
+                    mbar_arrive_expect_tx(fb, RB);
+                    tma_load_4d(dst, &tmS, fb, 0, (r >> 1) * 256, r & 1, chunk_id);
+                } else if (r == 2 * NG) {
+                    mbar_arrive_expect_tx(fb, 16384);
+                    tma_load_3d(dst, &tmQ, fb, 0, c * C + t * 128, (int)bh);
+                } else {
+                    mbar_arrive_expect_tx(fb, RB);
+                    tma_load_3d(dst, r == 2 * NG + 1 ? &tmK : &tmV, fb, 0, c * C, (int)bh);
+                }
+                issued = r + 1;
             }
-            mbar_wait(qb, 0, a.status);
-            for (int pp = issued - 1; pp >= 0 && pp >= issued - NP; --pp)
-                mbar_wait(smem_u32(&bar_full[pp % NP]), (pp / NP) & 1, a.status);
+            // no copy may be in flight at exit
+            mbar_wait(lb, 0, a.status);
+            for (int r = issued - 1; r >= 0 && r >= issued - NR; --r)
+                mbar_wait(smem_u32(&bar_full[slot_of(r)]), use_of(r) & 1, a.status);
         }
     } else if (warp == WARP_MMA) {
         if (lane == 0) {
-            bool ok = mbar_wait(smem_u32(&bar_qkv), 0, a.status);
+            bool ok = mbar_wait(smem_u32(&bar_cvt), 0, a.status);
             tc_fence_after();
-            // ---- intra-chunk blocks (tile t, 64-key block jb)
-            for (int b = 0; b < NBLK && ok; ++b) {
-                const int t = blk_tile(b), jb = blk_key(b);
+            // ---- readout: U_g = Q [S_{4g} | .. | S_{4g+3}] (hi + lo plane), then U_z = Q zm^T
+            for (int g = 0; g <= NG && ok; ++g) {
+                const int ub = g & 1;
+                const uint32_t k = (uint32_t)(g >> 1);
+                if (abort_s) { ok = false; break; }
+                if (g < NG) {
+                    const int r0 = 2 * g, r1 = 2 * g + 1;
+                    if (!(ok = mbar_wait(smem_u32(&bar_full[slot_of(r0)]), use_of(r0) & 1, a.status))) break;
+                    if (!(ok = mbar_wait(smem_u32(&bar_full[slot_of(r1)]), use_of(r1) & 1, a.status))) break;
+                }
+                if (k > 0 && !(ok = mbar_wait(smem_u32(&bar_uempty[ub]), (k - 1) & 1, a.status))) break;
+                tc_fence_after();
+                const uint32_t d = tmem + ub * 256;
+                if (g < NG) {
+                    const uint32_t bhi = sb0 + RING + slot_of(2 * g) * RB, blo = sb0 + RING + slot_of(2 * g + 1) * RB;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma_bf16(d, sdesc_sw128(sb0 + SQH + kk * 32), sdesc_sw128_ex(bhi + kk * 2048, 8192, 1024),
+                                  IDESC_U, kk > 0);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma_bf16(d, sdesc_sw128(sb0 + SQH + kk * 32), sdesc_sw128_ex(blo + kk * 2048, 8192, 1024),
+                                  IDESC_U, 1u);
+                    umma_commit(smem_u32(&bar_empty[slot_of(2 * g)]));
+                    umma_commit(smem_u32(&bar_empty[slot_of(2 * g + 1)]));
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        umma_bf16(d, sdesc_sw128(sb0 + SQH + kk * 32), sdesc_sw128(sb0 + SZH + kk * 32), IDESC_Z, kk > 0);
+                        umma_bf16(d, sdesc_sw128(sb0 + SQH + kk * 32), sdesc_sw128(sb0 + SZL + kk * 32), IDESC_Z, 1u);
+                    }
+                }
+                umma_commit(smem_u32(&bar_ufull[ub]));
+            }
+            // ---- intra-chunk blocks (64 keys each), in [0, 256) once U_z has been read
+            const int rq = 2 * NG, rk = 2 * NG + 1, rv = 2 * NG + 2;
+            if (ok) ok = mbar_wait(smem_u32(&bar_uempty[0]), (uint32_t)(NG >> 1) & 1, a.status);
+            if (ok) ok = mbar_wait(smem_u32(&bar_full[slot_of(rq)]), use_of(rq) & 1, a.status);
+            if (ok) ok = mbar_wait(smem_u32(&bar_full[slot_of(rk)]), use_of(rk) & 1, a.status);
+            if (ok) ok = mbar_wait(smem_u32(&bar_full[slot_of(rv)]), use_of(rv) & 1, a.status);
+            tc_fence_after();
+            const uint32_t SQ = sb0 + RING + slot_of(rq) * RB;
+            const uint32_t SK = sb0 + RING + slot_of(rk) * RB, SV = sb0 + RING + slot_of(rv) * RB;
+            for (int b = 0; b < nblk && ok; ++b) {
+                if (abort_s) { ok = false; break; }
                 if (b > 0 && !(ok = mbar_wait(smem_u32(&bar_sfree[b - 1]), 0, a.status))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    umma_bf16(tmem + TM_S, sdesc_sw128(sb0 + SQ + t * 16384 + kk * 32),
-                              sdesc_sw128(sb0 + SK + jb * 8192 + kk * 32), IDESC_QK, kk > 0);
+                    umma_bf16(tmem + TM_S, sdesc_sw128(SQ + kk * 32), sdesc_sw128(SK + b * 8192 + kk * 32), IDESC_QK,
+                              kk > 0);
                 umma_commit(smem_u32(&bar_sfull[b]));
                 if (!(ok = mbar_wait(smem_u32(&bar_pfull[b]), 0, a.status))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t vd = sdesc_sw128_ex(sb0 + SV + jb * 8192 + kk * 2048, 8192, 1024);
-                    umma_bf16_ts(tmem + TM_Y + t * 64, tmem + TM_PH + kk * 8, vd, IDESC_PV, (jb > 0 || kk > 0) ? 1u : 0u);
-                    umma_bf16_ts(tmem + TM_Y + t * 64, tmem + TM_PL + kk * 8, vd, IDESC_PV, 1u);
+                    const uint64_t vd = sdesc_sw128_ex(SV + b * 8192 + kk * 2048, 8192, 1024);
+                    umma_bf16_ts(tmem + TM_Y, tmem + TM_PH + kk * 8, vd, IDESC_PV, (b > 0 || kk > 0) ? 1u : 0u);
+                    umma_bf16_ts(tmem + TM_Y, tmem + TM_PL + kk * 8, vd, IDESC_PV, 1u);
                 }
                 umma_commit(smem_u32(&bar_pfree[b]));
-            }
-            umma_commit(smem_u32(&bar_intra));   // arrives when every intra-chunk MMA has finished
-            // ---- inter-chunk readout: U_m = Q S_m (m < 64), U_64 = Q zm^T
-            if (ok) ok = mbar_wait(smem_u32(&bar_cvt), 0, a.status);
-            tc_fence_after();
-            for (int m = 0; m < NSL && ok; ++m) {
-                const int pp = m >> 1, ps = pp % NP, ub = m & 1;
-                if (abort_s) { ok = false; break; }
-                if (m < 64 && (m & 1) == 0 && !(ok = mbar_wait(smem_u32(&bar_full[ps]), (pp / NP) & 1, a.status)))
-                    break;
-                if (m >= 2 && !(ok = mbar_wait(smem_u32(&bar_uempty[ub]), ((m >> 1) - 1) & 1, a.status))) break;
-                tc_fence_after();
-#pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                    const uint32_t d = tmem + TM_U + ub * 128 + t * 64;
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t ad = sdesc_sw128(sb0 + SQH + t * 16384 + kk * 32);
-                        if (m < 64) {
-                            const uint32_t bs = sb0 + STG + ps * PBYTES + (m & 1) * 8192 + kk * 2048;
-                            umma_bf16(d, ad, sdesc_sw128_ex(bs, 8192, 1024), IDESC_RD, kk > 0);
-                            umma_bf16(d, ad, sdesc_sw128_ex(bs + 16384, 8192, 1024), IDESC_RD, 1u);
-                        } else {
-                            umma_bf16(d, ad, sdesc_sw128(sb0 + SZH + kk * 32), IDESC_RZ, kk > 0);
-                            umma_bf16(d, ad, sdesc_sw128(sb0 + SZL + kk * 32), IDESC_RZ, 1u);
-                        }
-                    }
-                }
-                if (m < 64 && (m & 1)) umma_commit(smem_u32(&bar_empty[ps]));
-                umma_commit(smem_u32(&bar_ufull[ub]));
             }
             if (ok) umma_commit(smem_u32(&bar_yfull));
             else abort_s = 1;
@@ -221,52 +236,61 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
         }
     } else {
         // ---------------------------------------------------------------- compute warps
-        const int quad = warp & 3, t = (warp >> 2) & 1, h = warp >> 3;
-        const int l = quad * 32 + lane;              // row of tile t
+        const int quad = warp & 3, h = warp >> 2;
+        const int l = quad * 32 + lane;              // tile row
         const int i = t * 128 + l;                   // token index inside the chunk
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         const float Ai = sAv[i];
-        float zin = 0.f;
-        int kall = 0, ktile = 0;                       // group-wait counters
-        bool ok = mbar_wait(smem_u32(&bar_qkv), 0, a.status);
+        int kg = 0;                                  // group-wait counter
+        bool ok = mbar_wait(smem_u32(&bar_ld), 0, a.status);
         if (ok) {   // fp16 copy of the Q tile; the normaliser matrix of the state as hi + lo fp16
-            const int tt = threadIdx.x;
-            for (int pc = tt; pc < 2048; pc += NCOMP) {
-                uint32_t x[4];
-                asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                             : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3])
-                             : "r"(sb0 + SQ + pc * 16));
-                st_shared_v4(sb0 + SQH + pc * 16, bf16x2_to_f16x2(x[0]), bf16x2_to_f16x2(x[1]), bf16x2_to_f16x2(x[2]),
-                             bf16x2_to_f16x2(x[3]));
-            }
-            const float* zc = a.zx + (bh * NC + c) * 4096;
-            for (int pc = tt; pc < 512; pc += NCOMP) {
-                const int m = pc >> 3, k8 = pc & 7;
-                const float4 a0 = *reinterpret_cast<const float4*>(zc + m * 64 + k8 * 8);
-                const float4 a1 = *reinterpret_cast<const float4*>(zc + m * 64 + k8 * 8 + 4);
-                const float v[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-                uint32_t hh[4], ll[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    hh[u] = pack_f16x2(v[2 * u], v[2 * u + 1]);
-                    const __half2 h2 = *reinterpret_cast<const __half2*>(&hh[u]);
-                    ll[u] = pack_f16x2(v[2 * u] - __low2float(h2), v[2 * u + 1] - __high2float(h2));
-                }
-                const uint32_t off = m * 128 + ((k8 ^ (m & 7)) << 4);
-                st_shared_v4(sb0 + SZH + off, hh[0], hh[1], hh[2], hh[3]);
-                st_shared_v4(sb0 + SZL + off, ll[0], ll[1], ll[2], ll[3]);
-            }
+            const int t256 = threadIdx.x;
+            for (int pc = t256; pc < 1024; pc += 256) tile_bf16_to_f16(early, sb0 + SQH, pc);
+            build_z_tiles(smem + SZH, smem + SZL, a.zx + (bh * NC + c) * 4096, 1.f, t256);
             fence_proxy_async();
-            mbar_arrive(smem_u32(&bar_cvt));
         }
-        // ---- intra-chunk: tile 0 owns blocks 0-1, tile 1 owns blocks 2-5; half h: 32 key columns
-        for (int b = (t == 0 ? 0 : 2); b < (t == 0 ? 2 : NBLK) && ok; ++b) {
-            const int jb = blk_key(b);
-            if (!(ok = group_wait(smem_u32(&bar_sfull[b]), 0, a.status, warp == 4 * t, 2 + t, 256, gflags[1 + t],
-                                  ktile, &abort_s)))
+        mbar_arrive(smem_u32(&bar_cvt));
+        // ---- readout: nx[col] += q_i[m] U[i][(m, col)]; zxp += q_i[m'] U_z[i][m']
+        float nx[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) nx[k] = 0.f;
+        float zxp = 0.f, zin = 0.f;
+        const uint8_t* qrow = smem + SQH;
+#pragma unroll 1
+        for (int g = 0; g <= NG && ok; ++g) {
+            const int ub = g & 1;
+            if (!(ok = group_wait(smem_u32(&bar_ufull[ub]), (uint32_t)(g >> 1) & 1, a.status, warp == 0, 1, 256, gflags,
+                                  kg, &abort_s)))
                 break;
-            if (b > 0 && !(ok = group_wait(smem_u32(&bar_pfree[b - 1]), 0, a.status, warp == 4 * t, 2 + t, 256,
-                                           gflags[1 + t], ktile, &abort_s)))
+            const uint32_t ua = tmem + lane_base + ub * 256 + h * 32;
+            if (g < NG) {
+#pragma unroll 1
+                for (int mp = 0; mp < 4; ++mp) {
+                    float u[32];
+                    tmem_ld32(ua + mp * 64, u);
+                    if (mp == 3) {
+                        tc_fence_before();
+                        mbar_arrive(smem_u32(&bar_uempty[ub]));
+                    }
+                    const float qm = __half2float(*reinterpret_cast<const __half*>(qrow + swz_elem(l, 4 * g + mp)));
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) nx[k] = fmaf(qm, u[k], nx[k]);
+                }
+            } else {
+                float u[32];
+                tmem_ld32(ua, u);
+                tc_fence_before();
+                mbar_arrive(smem_u32(&bar_uempty[ub]));
+#pragma unroll
+                for (int k = 0; k < 32; ++k)
+                    zxp = fmaf(__half2float(*reinterpret_cast<const __half*>(qrow + swz_elem(l, h * 32 + k))), u[k], zxp);
+            }
+        }
+        // ---- intra-chunk blocks; half h covers 32 of the 64 keys of a block
+        for (int b = 0; b < nblk && ok; ++b) {
+            if (!(ok = group_wait(smem_u32(&bar_sfull[b]), 0, a.status, warp == 0, 1, 256, gflags, kg, &abort_s))) break;
+            if (b > 0 && !(ok = group_wait(smem_u32(&bar_pfree[b - 1]), 0, a.status, warp == 0, 1, 256, gflags, kg,
+                                           &abort_s)))
                 break;
 #pragma unroll
             for (int g2 = 0; g2 < 2; ++g2) {
@@ -279,7 +303,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
                     float hi2[2], lo2[2];
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
-                        const int j = jb * 64 + cc * 16 + 2 * k2 + u;
+                        const int j = b * 64 + cc * 16 + 2 * k2 + u;
                         const float sv = s[2 * k2 + u];
                         const float pv = j <= i ? sv * sv * __expf(Ai - sAv[j]) : 0.f;
                         zin += pv;
@@ -297,51 +321,21 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
             mbar_arrive(smem_u32(&bar_sfree[b]));
             mbar_arrive(smem_u32(&bar_pfull[b]));
         }
-        // ---- inter-chunk readout: nx[col] += q_i[m] U_m[i][col]; zx += q_i[m'] U_64[i][m']
-        float nx[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k) nx[k] = 0.f;
-        float zxp = 0.f;
-        const uint8_t* qrow = smem + SQH;            // fp16 copy (the bf16 tile is reused for stages)
-#pragma unroll 1
-        for (int m = 0; m < NSL && ok; ++m) {
-            const int ub = m & 1;
-            if (!(ok = group_wait(smem_u32(&bar_ufull[ub]), (m >> 1) & 1, a.status, warp == 0, 1, NCOMP, gflags[0], kall,
-                                  &abort_s)))
-                break;
-            float u[32];
-            const uint32_t ua = tmem + lane_base + TM_U + ub * 128 + t * 64 + h * 32;
-            tmem_ld16(ua, u);
-            tmem_ld16(ua + 16, u + 16);
-            tc_fence_before();
-            mbar_arrive(smem_u32(&bar_uempty[ub]));
-            if (m < 64) {
-                const float qm = __half2float(*reinterpret_cast<const __half*>(qrow + swz_elem(i, m)));
-#pragma unroll
-                for (int k = 0; k < 32; ++k) nx[k] = fmaf(qm, u[k], nx[k]);
-            } else {
-#pragma unroll
-                for (int k = 0; k < 32; ++k)
-                    zxp = fmaf(__half2float(*reinterpret_cast<const __half*>(qrow + swz_elem(i, h * 32 + k))), u[k], zxp);
-            }
-        }
         // ---- combine the two column halves' shares of Z, then the epilogue
         if (ok) {
-            sRed[(h * 256 + i) * 2] = zin;
-            sRed[(h * 256 + i) * 2 + 1] = zxp;
+            sRed[(h * 128 + l) * 2] = zin;
+            sRed[(h * 128 + l) * 2 + 1] = zxp;
         }
         mbar_arrive(smem_u32(&bar_red));
         if (ok) ok = mbar_wait(smem_u32(&bar_red), 0, a.status);
         if (ok && !abort_s && (ok = mbar_wait(smem_u32(&bar_yfull), 0, a.status))) {
             tc_fence_after();
             const float eA = __expf(Ai);
-            const float zi = sRed[i * 2] + sRed[(256 + i) * 2];
-            const float zo = sRed[i * 2 + 1] + sRed[(256 + i) * 2 + 1];
+            const float zi = sRed[l * 2] + sRed[(128 + l) * 2];
+            const float zo = sRed[l * 2 + 1] + sRed[(128 + l) * 2 + 1];
             const float z = zi + eA * zo;
             float y[32];
-            const uint32_t ya = tmem + lane_base + TM_Y + t * 64 + h * 32;
-            tmem_ld16(ya, y);
-            tmem_ld16(ya + 16, y + 16);
+            tmem_ld32(tmem + lane_base + TM_Y + h * 32, y);
             const long tok = (long)c * C + i;
             if (tok < a.T) {
                 const float inv = a.normalize ? (z != 0.f ? 1.f / z : 0.f) : 1.f;
@@ -358,23 +352,22 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
+    if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
 cudaError_t tc_chunk_out(const Problem& p, const void* q, const void* k, const void* v, const float* Aloc,
                          const void* Sx, const float* zx, float* o, float* Z, cudaStream_t s) {
     CUtensorMap tq, tk, tv, ts;
     const uint64_t BH = (uint64_t)p.BH();
-    if (!make_tmap_bf16_3d(&tq, q, BH, (uint64_t)p.T, 64, C) || !make_tmap_bf16_3d(&tk, k, BH, (uint64_t)p.T, 64, C) ||
-        !make_tmap_bf16_3d(&tv, v, BH, (uint64_t)p.T, 64, C) ||
-        !make_tmap_state_pairs(&ts, Sx, BH * (uint64_t)p.NC))
+    if (!make_tmap_bf16_3d(&tq, q, BH, (uint64_t)p.T, 64, 128) || !make_tmap_bf16_3d(&tk, k, BH, (uint64_t)p.T, 64, C) ||
+        !make_tmap_bf16_3d(&tv, v, BH, (uint64_t)p.T, 64, C) || !make_tmap_state_quads(&ts, Sx, BH * (uint64_t)p.NC))
         return cudaErrorInvalidValue;
     int* status = tc_status_ptr();
     if (!status) return cudaErrorInvalidValue;
     Args a{Aloc, zx, o, Z, status, p.T, p.NC, (int)p.Tp(), p.normalize ? 1 : 0};
     cudaError_t e = cudaFuncSetAttribute(tc_chunk_out_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    dim3 grid(p.NC, (unsigned)p.BH());
+    dim3 grid(2 * p.NC, (unsigned)p.BH());
     tc_chunk_out_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(tq, tk, tv, ts, a);
     return cudaGetLastError();
 }
