@@ -70,13 +70,13 @@ struct ScanIO {
 };
 cudaError_t tc_state_scan(const Problem& p, const ScanIO& io, cudaStream_t s);
 
-// Operands of the chunk-state scan (tm2_scan.cu): ops [BH][Tp/64][192][64] fp16, one block
-// per 64-token stage (so that one TMA request brings whole stages): rows 0-63 the key block
-// transposed (row n = key_t[n] over the stage's tokens t), rows 64-127 w_t val_t (row = token),
-// rows 128-191 column 0 = w_t zc_t, the rest zero.  Forward: key = k, val = v,
+// Operands of the chunk-state scan (tm2_scan.cu): ops [BH][Tp/64][136][64] fp16, one block
+// per 64-token stage (one TMA request each): rows 0-63 the key block transposed (row n =
+// key_t[n] over the stage's tokens t), rows 64-127 the weighted values transposed (row col =
+// w_t val_t[col]), row 128 = w_t zc_t, rows 129-135 zero.  Forward: key = k, val = v,
 // w = exp(g_c - A_t), zc = 1.  Reverse: key = q, val = dO, w = exp(A_t) zeta_t / zmax_c,
 // zc = ucol_t.
-constexpr int TC_OPS_ROWS = 192;
+constexpr int TC_OPS_ROWS = 136;
 cudaError_t launch_tc_scan_operands(const Problem& p, bool rev, const void* key, const void* val, const float* Aloc,
                                     const float* g, const float* zeta, const float* ucol, const float* zmax,
                                     void* ops, cudaStream_t s);

@@ -185,10 +185,11 @@ cudaError_t launch_tc_dy_prep(const Problem& p, const float* o, const float* Z, 
 }
 
 // Operands of the tensor-core chunk-state scan, one block of 256 threads per 64-token stage
-// of one (b, h), written as one [192][64] fp16 block per stage (token j = stage*64 + row):
-//   rows   0-63 : [n][j]   = fp16(key_j[n])                      (the key block, transposed)
-//   rows  64-127: [j][col] = fp16(w_j val_j[col])                (the weighted value rows)
-//   rows 128-191: [j][0]   = fp16(w_j zc_j), [j][1..63] = 0      (the normaliser column)
+// of one (b, h), written as one [136][64] fp16 block per stage (token j = stage*64 + column):
+//   rows   0-63 : [n][j]   = fp16(key_j[n])         (the key block, transposed)
+//   rows  64-127: [col][j] = fp16(w_j val_j[col])   (the weighted values, transposed)
+//   row   128   : [j]      = fp16(w_j zc_j)         (the normaliser column)
+//   rows 129-135: 0
 // with the scan's weight w_t = exp(g_c - A_t), zc = 1 (forward walk) or
 // w_t = exp(A_t) zeta_t / zmax_c, zc = ucol_t (reverse walk); tokens past T give zeros.
 __global__ void __launch_bounds__(256) tc_scan_operands_kernel(
@@ -196,6 +197,7 @@ __global__ void __launch_bounds__(256) tc_scan_operands_kernel(
     const float* __restrict__ g, const float* __restrict__ zeta, const float* __restrict__ ucol,
     const float* __restrict__ zmax, __half* __restrict__ ops, int T, int C, int NC, int rev) {
     __shared__ float sk[64][65];
+    __shared__ float sv[64][65];
     __shared__ float sw[64], szc[64];
     const int st = blockIdx.x, tid = threadIdx.x;
     const long bh = blockIdx.y;
@@ -217,50 +219,38 @@ __global__ void __launch_bounds__(256) tc_scan_operands_kernel(
         sw[tid] = w;
         szc[tid] = zc;
     }
+    __syncthreads();
     for (int e = tid; e < 64 * 64; e += 256) {
         const int j = e >> 6, n = e & 63;
         const long t = t0 + j;
-        sk[j][n] = t < T ? __bfloat162float(key[(bh * T + t) * 64 + n]) : 0.f;
+        const bool in = t < T;
+        sk[j][n] = in ? __bfloat162float(key[(bh * T + t) * 64 + n]) : 0.f;
+        sv[j][n] = in ? __bfloat162float(val[(bh * T + t) * 64 + n]) * sw[j] : 0.f;
     }
     __syncthreads();
     __half* blk = ops + (bh * (Tp / 64) + st) * (long)(TC_OPS_ROWS * 64);
-    // transposed key block: thread writes 16 consecutive j of one row n
+    // transposed key and weighted-value blocks: thread writes 16 consecutive j of one row
     {
         const int n = tid >> 2, j0 = (tid & 3) * 16;
-        uint32_t w[8];
+        uint32_t wk[8], wv[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-            const __half2 h2 = __floats2half2_rn(sk[j0 + 2 * u][n], sk[j0 + 2 * u + 1][n]);
-            w[u] = *reinterpret_cast<const uint32_t*>(&h2);
+            const __half2 hk = __floats2half2_rn(sk[j0 + 2 * u][n], sk[j0 + 2 * u + 1][n]);
+            const __half2 hv = __floats2half2_rn(sv[j0 + 2 * u][n], sv[j0 + 2 * u + 1][n]);
+            wk[u] = *reinterpret_cast<const uint32_t*>(&hk);
+            wv[u] = *reinterpret_cast<const uint32_t*>(&hv);
         }
-        uint4* dst = reinterpret_cast<uint4*>(blk + n * 64 + j0);
-        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        uint4* dk = reinterpret_cast<uint4*>(blk + n * 64 + j0);
+        dk[0] = make_uint4(wk[0], wk[1], wk[2], wk[3]);
+        dk[1] = make_uint4(wk[4], wk[5], wk[6], wk[7]);
+        uint4* dv = reinterpret_cast<uint4*>(blk + (64 + n) * 64 + j0);
+        dv[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+        dv[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
     }
-    // weighted values and the normaliser column: thread writes 16 columns of one row
-    {
-        const int j = tid >> 2, c0 = (tid & 3) * 16;
-        const long t = t0 + j;
-        const float w = sw[j];
-        uint32_t x[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            float v0 = 0.f, v1 = 0.f;
-            if (t < T) {
-                v0 = __bfloat162float(val[(bh * T + t) * 64 + c0 + 2 * u]) * w;
-                v1 = __bfloat162float(val[(bh * T + t) * 64 + c0 + 2 * u + 1]) * w;
-            }
-            const __half2 h2 = __floats2half2_rn(v0, v1);
-            x[u] = *reinterpret_cast<const uint32_t*>(&h2);
-        }
-        uint4* dv = reinterpret_cast<uint4*>(blk + (64 + j) * 64 + c0);
-        dv[0] = make_uint4(x[0], x[1], x[2], x[3]);
-        dv[1] = make_uint4(x[4], x[5], x[6], x[7]);
-        const __half zh = __float2half_rn(c0 == 0 ? w * szc[j] : 0.f);
-        const uint32_t z0 = (uint32_t)(*reinterpret_cast<const uint16_t*>(&zh));
-        uint4* dz = reinterpret_cast<uint4*>(blk + (128 + j) * 64 + c0);
-        dz[0] = make_uint4(z0, 0u, 0u, 0u);
-        dz[1] = make_uint4(0u, 0u, 0u, 0u);
+    // the normaliser row and the zero rows after it
+    for (int e = tid; e < 8 * 64; e += 256) {
+        const int r = e >> 6, j = e & 63;
+        blk[(128 + r) * 64 + j] = __float2half_rn(r == 0 ? sw[j] * szc[j] : 0.f);
     }
 }
 

@@ -10,34 +10,37 @@
 // with zeta_i = 1/Z_i and ucol_i = -dO_i . o_i (normalised) or zeta = 1, ucol = 0.
 //
 // One CTA owns the 256 state rows r = m*64 + n with m in {4Q .. 4Q+3} of one (b, h) and
-// walks every chunk in order.  Per chunk, the local contribution of each 128-row tile is a
-// dense contraction  H[(m,n), col] = sum_j key_j[m] key_j[n] (w_j val_j[col])  (M = 128 rows,
-// N = 80 = 64 value columns + the normaliser column + 15 zero columns, K = chunk length),
-// issued as tcgen05.mma with A (the key (x) key rows) in tensor memory and B (the weighted
-// value tile, MN-major) in shared memory.
+// walks every chunk in order.  The chunk's contribution is computed transposed,
+//     H^T[col][(m,n)] = sum_j (w_j val_j[col]) key_j[m] key_j[n],
+// as tcgen05.mma with M = 128 (the 64 value columns, the normaliser column and zero rows),
+// N = 256 (the CTA's state rows) and K = tokens: a tensor-core instruction costs about the
+// same for any N up to 256, so putting the 256 state rows on N takes 8 instructions per
+// 64-token stage where 128 state rows on M and the 80 columns on N took 16.
 //
 // Precision.  Tokens whose query is nearly orthogonal to the state read it out with heavy
 // cancellation, so the state must carry more than one 16-bit rounding (a single fp16
 // rounding of k[m] k[n] or of the exported state puts such tokens near the 2e-2 parity
-// bar).  The A operand is therefore the exact product as two fp16 terms, hi = fp16(k[m] k[n])
-// and lo = fma(k[m], k[n], -hi) (exact: bf16 inputs give 16-bit products), run as two MMAs;
-// the decay weight goes into B (a rounding of the value side only perturbs each token's
-// contribution, which the readout then sees through non-negative weights).  The running
-// state is fp32 in the epilogue warps' registers and is exported as two fp16 planes
+// bar).  The key (x) key operand is therefore the exact product as two fp16 terms,
+// hi = fp16(k[m] k[n]) and lo = fma(k[m], k[n], -hi) (exact: bf16 inputs give 16-bit
+// products), run as two MMAs; the decay weight goes into the value side (a rounding there
+// only perturbs each token's contribution, which the readout then sees through non-negative
+// weights).  The running state is fp32 in tensor memory and is exported as two fp16 planes
 // (hi and the fp16 residual), the normaliser column as fp32.  The reverse walk scales its
 // weights by 1/zmax_c (zmax_c = max over chunk c of exp(A_i) zeta_i, so they are <= 1) and
 // exports slot c divided by Gamma_c = max_{c' > c} zmax_{c'} (one value per slot, the same
 // in every CTA, recorded in `sscale`), so that the 1/Z factors cannot overflow fp16.
 //
-// The operands come from a pre-pass (launch_tc_scan_operands): per 64-token stage one
-// [192][64] fp16 block holding the transposed key block Kt[n][j], the weighted values
-// fp16(w_j val_j) and the normaliser column.  One TMA request brings two consecutive stages
-// (48 KB): a TMA request costs a few hundred ns of issue time whatever its size, so large
-// requests are what keeps the stream ahead of the tensor cores.  Warp roles (576 threads): warps 0-7 build the A operand
-// straight from the Kt tile (warp w: tensor-memory lane quadrant w % 4, half w / 4 of the
-// 64 rows of a stage); warps 8-15 fold the accumulator into the running state once per chunk
-// (warp 8+e: tile e / 4, quadrant e % 4; one state row per thread) and export it; warp 16
-// issues the TMA loads, warp 17 the MMAs.
+// Data flow.  A pre-pass (launch_tc_scan_operands) writes one [136][64] fp16 block per
+// 64-token stage: the transposed key block and the transposed weighted values with the
+// normaliser row (and 7 zero rows); one TMA request brings a stage into a ring slot.  Warps
+// 0-7 build the key (x) key operand of a stage in shared memory (thread = one key index n and
+// 16 tokens, the four state rows of that n, hi and lo planes, 128-byte swizzled K-major),
+// double-buffered; warp 15 issues the MMAs into tensor-memory buffer
+// (chunk & 1); warps 8, 9, 12, 13 (value columns, lane quadrants 0 and 1) and 10, 14 (the
+// normaliser column, lane 64) fold the chunk into the running state,
+//     S_c = exp(g_c) S_{c-1} + scale H^T_c,
+// written back over H^T_c in tensor memory (so the buffer of chunk c-1 frees as soon as it
+// has been read), and export it; warp 11 issues the TMA loads.
 // Every mbarrier wait is bounded; on expiry the status word records TM2_ERR_TIMEOUT and
 // the CTA unwinds.
 #include "tm2.h"
@@ -51,19 +54,16 @@ namespace tcscan {
 constexpr int C = TC_CHUNK;     // chunk length
 constexpr int KS = 64;          // tokens per stage
 constexpr int SPC = C / KS;     // stages per chunk
-constexpr int NP = 4;           // stage-pair buffers (one TMA request brings two stages)
-constexpr int NN = 80;          // MMA N
-constexpr int NG_THREADS = 256, NE_THREADS = 256;
-constexpr int WARP_TMA = 16, WARP_MMA = 17;
-constexpr int THREADS = 18 * 32;
-constexpr int TILE = KS * 128;                // one [64][64] 16-bit tile, 128B-swizzled
-constexpr int STAGE = 3 * TILE;               // Kt, then the value block and the normaliser block
-constexpr int PSLOT = 2 * STAGE;              // two consecutive stages
-constexpr int SMEM_BYTES = NP * PSLOT + 1024;
-constexpr uint32_t TM_H = 0;                  // accumulator: tile t at t * 80
-constexpr uint32_t TM_A = 160;                // A buffers: 160 + buf*128 + tile*64 + {0: hi, 32: lo}
-constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t IDESC = idesc_f16_f32(128, NN, false, true);
+constexpr int NSLOT = 5;        // ring slots, one stage each
+constexpr int SLOT = TC_OPS_ROWS * 128;   // [Kt 64 rows | value^T 64 rows | normaliser row | 7 zero rows]
+constexpr int BBUF = 65536;     // key (x) key operand of a stage: hi [256][64] then lo [256][64]
+constexpr int SB = NSLOT * SLOT;
+constexpr int SMEM_BYTES = SB + 2 * BBUF + 1024;
+constexpr int THREADS = 16 * 32;
+constexpr int NBUILD = 256;     // builder threads (warps 0-7)
+constexpr int NEPI = 192;       // epilogue threads (warps 8, 9, 10, 12, 13, 14)
+constexpr int WARP_TMA = 11, WARP_MMA = 15;
+constexpr uint32_t IDESC = idesc_f16_f32(128, 256, false, false);
 
 struct Args {
     const float* g;       // [BH][NC] chunk totals
@@ -87,8 +87,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
                                                                    const __grid_constant__ Args a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_align1024(smem_raw);
-    __shared__ __align__(8) uint64_t bar_full[NP], bar_empty[NP], bar_afull[2], bar_aempty[2], bar_hfull,
-        bar_hempty, bar_done;
+    __shared__ __align__(8) uint64_t bar_full[NSLOT], bar_empty[NSLOT], bar_bfull[2], bar_bempty[2], bar_hfull[2],
+        bar_dfree[2], bar_done;
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_s;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -101,22 +101,22 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
     const uint32_t sbase = smem_u32(smem);
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < NP; ++i) {
+        for (int i = 0; i < NSLOT; ++i) {
             mbar_init(smem_u32(&bar_full[i]), 1);
-            mbar_init(smem_u32(&bar_empty[i]), 1);
+            mbar_init(smem_u32(&bar_empty[i]), NBUILD + 1);   // builders read Kt, the MMAs read the values
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(smem_u32(&bar_afull[i]), NG_THREADS);
-            mbar_init(smem_u32(&bar_aempty[i]), 1);
+            mbar_init(smem_u32(&bar_bfull[i]), NBUILD);
+            mbar_init(smem_u32(&bar_bempty[i]), 1);
+            mbar_init(smem_u32(&bar_hfull[i]), 1);
+            mbar_init(smem_u32(&bar_dfree[i]), NEPI);
         }
-        mbar_init(smem_u32(&bar_hfull), 1);
-        mbar_init(smem_u32(&bar_hempty), NE_THREADS);
         mbar_init(smem_u32(&bar_done), 1);
         abort_s = 0;
         fence_mbar_init();
     }
     if (warp == 0) {
-        tmem_alloc(smem_u32(&tmem_base_s), TMEM_COLS);
+        tmem_alloc(smem_u32(&tmem_base_s), 512);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -130,195 +130,228 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
         // ---------------------------------------------------------------- TMA producer
         if (lane == 0) {
             prefetch_tmap(&tmOps);
-            const int npairs = nstages / 2;          // stage pairs never straddle a chunk
             int issued = 0;
-            for (int pg = 0; pg < npairs && !abort_s; ++pg) {
-                const int ps = pg % NP;
-                if (pg >= NP && !mbar_wait(smem_u32(&bar_empty[ps]), ((pg / NP) - 1) & 1, a.status)) {
+            for (int gs = 0; gs < nstages && !abort_s; ++gs) {
+                const int sl = gs % NSLOT;
+                const uint32_t u = (uint32_t)(gs / NSLOT);
+                if (u > 0 && !mbar_wait(smem_u32(&bar_empty[sl]), (u - 1) & 1, a.status)) {
                     abort_s = 1;
                     break;
                 }
-                const int c = chunk_of(pg / (SPC / 2));
-                const int stg = c * SPC + (pg % (SPC / 2)) * 2;   // first stage of the pair in the sequence
-                const uint32_t fb = smem_u32(&bar_full[ps]);
-                mbar_arrive_expect_tx(fb, PSLOT);
-                tma_load_3d(sbase + ps * PSLOT, &tmOps, fb, 0, 0, (int)(bh * (a.Tp / KS) + stg));
-                issued = pg + 1;
+                const int stg = chunk_of(gs / SPC) * SPC + gs % SPC;   // stage index within the sequence
+                const uint32_t fb = smem_u32(&bar_full[sl]);
+                mbar_arrive_expect_tx(fb, SLOT);
+                tma_load_3d(sbase + sl * SLOT, &tmOps, fb, 0, 0, (int)(bh * (a.Tp / KS) + stg));
+                issued = gs + 1;
             }
-            // wait for the last use of every pair buffer, so no copy is in flight at exit
-            for (int pg = issued - 1; pg >= 0 && pg >= issued - NP; --pg)
-                mbar_wait(smem_u32(&bar_full[pg % NP]), (pg / NP) & 1, a.status);
+            // no copy may be in flight at exit
+            for (int gs = issued - 1; gs >= 0 && gs >= issued - NSLOT; --gs)
+                mbar_wait(smem_u32(&bar_full[gs % NSLOT]), (uint32_t)(gs / NSLOT) & 1, a.status);
         }
     } else if (warp == WARP_MMA) {
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
             bool ok = true;
             for (int it = 0; it < nchunks && ok; ++it) {
-                if (it >= 1 && !(ok = mbar_wait(smem_u32(&bar_hempty), (it - 1) & 1, a.status))) break;
-                tc_fence_after();
+                const int b = it & 1;
+                if (it >= 1 && !(ok = mbar_wait(smem_u32(&bar_dfree[b]), (uint32_t)((it - 1) >> 1) & 1, a.status)))
+                    break;
                 for (int s = 0; s < SPC; ++s) {
-                    const int gs = it * SPC + s, pg = gs >> 1, ps = pg % NP, ab = gs & 1;
+                    const int gs = it * SPC + s, sl = gs % NSLOT, sb = gs & 1;
                     if (abort_s) { ok = false; break; }
-                    if ((gs & 1) == 0 && !(ok = mbar_wait(smem_u32(&bar_full[ps]), (pg / NP) & 1, a.status))) break;
-                    if (!(ok = mbar_wait(smem_u32(&bar_afull[ab]), (gs >> 1) & 1, a.status))) break;
+                    if (!(ok = mbar_wait(smem_u32(&bar_full[sl]), (uint32_t)(gs / NSLOT) & 1, a.status))) break;
+                    if (!(ok = mbar_wait(smem_u32(&bar_bfull[sb]), (uint32_t)(gs >> 1) & 1, a.status))) break;
                     tc_fence_after();
-                    const uint32_t vb = sbase + ps * PSLOT + (gs & 1) * STAGE + TILE;
+                    // value^T rows (M), K-major.  M rows 72-127 read whatever follows the slot: they
+                    // only reach accumulator lanes 72-127, which nothing reads.
+                    const uint32_t av = sbase + sl * SLOT + 8192;
+                    const uint32_t bhi = sbase + SB + sb * BBUF, blo = bhi + 32768;
+                    const uint32_t d = tmem + (uint32_t)b * 256;
 #pragma unroll
-                    for (int t = 0; t < 2; ++t)
+                    for (int kk = 0; kk < KS / 16; ++kk)
+                        umma_bf16(d, sdesc_sw128(av + kk * 32), sdesc_sw128(bhi + kk * 32), IDESC, (s > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-                        for (int kk = 0; kk < KS / 16; ++kk) {
-                            const uint64_t bd = sdesc_sw128_ex(vb + kk * 2048, TILE, 1024);
-                            const uint32_t aa = tmem + TM_A + ab * 128 + t * 64 + kk * 8;
-                            umma_bf16_ts(tmem + TM_H + t * 80, aa, bd, IDESC, (s > 0 || kk > 0) ? 1u : 0u);
-                            umma_bf16_ts(tmem + TM_H + t * 80, aa + 32, bd, IDESC, 1u);
-                        }
-                    if (gs & 1) umma_commit(smem_u32(&bar_empty[ps]));
-                    umma_commit(smem_u32(&bar_aempty[ab]));
+                    for (int kk = 0; kk < KS / 16; ++kk)
+                        umma_bf16(d, sdesc_sw128(av + kk * 32), sdesc_sw128(blo + kk * 32), IDESC, 1u);
+                    umma_commit(smem_u32(&bar_empty[sl]));
+                    umma_commit(smem_u32(&bar_bempty[sb]));
                 }
                 if (!ok) break;
-                umma_commit(smem_u32(&bar_hfull));
+                umma_commit(smem_u32(&bar_hfull[b]));
             }
             if (!ok) abort_s = 1;
             umma_commit(smem_u32(&bar_done));
             mbar_wait(smem_u32(&bar_done), 0, a.status);
         }
     } else if (warp < 8) {
-        // ---------------------------------------------------------------- A-operand builders
-        const int quad = warp & 3, h = warp >> 2;
-        const int l = quad * 32 + lane;              // tensor-memory lane = tile row
-        const int n = l & 63, moff = l >> 6;
+        // ---------------------------------------------------------------- key (x) key builders
+        // thread: key index n = t & 63, tokens 16 * (t >> 6) .. +15, the four state rows
+        // (m' = 0..3, m = 4Q + m') of that n: the Kt row of n is read once, the rows of m are
+        // warp-uniform (broadcast).
+        const int n = threadIdx.x & 63, kq = threadIdx.x >> 6;
         for (int gs = 0; gs < nstages; ++gs) {
-            const int pg = gs >> 1, ps = pg % NP, ab = gs & 1;
-            if (abort_s || !mbar_wait(smem_u32(&bar_full[ps]), (pg / NP) & 1, a.status)) {
+            const int sl = gs % NSLOT, sb = gs & 1;
+            if (abort_s || !mbar_wait(smem_u32(&bar_full[sl]), (uint32_t)(gs / NSLOT) & 1, a.status)) {
                 abort_s = 1;
                 break;
             }
-            if (gs >= 2 && !mbar_wait(smem_u32(&bar_aempty[ab]), ((gs >> 1) - 1) & 1, a.status)) {
+            if (gs >= 2 && !mbar_wait(smem_u32(&bar_bempty[sb]), (uint32_t)((gs >> 1) - 1) & 1, a.status)) {
                 abort_s = 1;
                 break;
             }
-            tc_fence_after();
-            const uint32_t kt = sbase + ps * PSLOT + (gs & 1) * STAGE;   // Kt tile: row n = key_j[n] over j, swizzled
-            // key_j[n] for this thread's 32 rows j of the stage, as fp16 pairs
-            uint32_t kp[16];
+            const uint32_t kt = sbase + sl * SLOT;   // Kt: row x = key_j[x] over the stage's 64 tokens j
+            uint32_t xn[8];
 #pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4)
+            for (int c2 = 0; c2 < 2; ++c2)
                 asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                             : "=r"(kp[4 * v4]), "=r"(kp[4 * v4 + 1]), "=r"(kp[4 * v4 + 2]), "=r"(kp[4 * v4 + 3])
-                             : "r"(kt + n * 128 + (((h * 4 + v4) ^ (n & 7)) << 4)));
+                             : "=r"(xn[4 * c2]), "=r"(xn[4 * c2 + 1]), "=r"(xn[4 * c2 + 2]), "=r"(xn[4 * c2 + 3])
+                             : "r"(kt + n * 128 + (((2 * kq + c2) ^ (n & 7)) << 4)));
 #pragma unroll
-            for (int t = 0; t < 2; ++t) {
-                const int m = 4 * Q + 2 * t + moff;   // the same for the whole warp
-                uint32_t rh[16], rl[16];
+            for (int mp = 0; mp < 4; ++mp) {
+                const int m = 4 * Q + mp, r = mp * 64 + n;
+                const uint32_t dhi = sbase + SB + sb * BBUF + r * 128, dlo = dhi + 32768;
 #pragma unroll
-                for (int v4 = 0; v4 < 4; ++v4) {
-                    uint32_t xs[4];
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    const int k8 = 2 * kq + c2;
+                    uint32_t xm[4], rh[4], rl[4];
                     asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                                 : "=r"(xs[0]), "=r"(xs[1]), "=r"(xs[2]), "=r"(xs[3])
-                                 : "r"(kt + m * 128 + (((h * 4 + v4) ^ (m & 7)) << 4)));
+                                 : "=r"(xm[0]), "=r"(xm[1]), "=r"(xm[2]), "=r"(xm[3])
+                                 : "r"(kt + m * 128 + ((k8 ^ (m & 7)) << 4)));
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        const int p = v4 * 4 + i;
-                        const __half2 km2 = *reinterpret_cast<const __half2*>(&xs[i]);
-                        const __half2 kn2 = *reinterpret_cast<const __half2*>(&kp[p]);
+                        const __half2 km2 = *reinterpret_cast<const __half2*>(&xm[i]);
+                        const __half2 kn2 = *reinterpret_cast<const __half2*>(&xn[4 * c2 + i]);
                         const __half2 hi2 = __hmul2(km2, kn2);
                         const __half2 lo2 = __hfma2(km2, kn2, __hneg2(hi2));
-                        rh[p] = *reinterpret_cast<const uint32_t*>(&hi2);
-                        rl[p] = *reinterpret_cast<const uint32_t*>(&lo2);
+                        rh[i] = *reinterpret_cast<const uint32_t*>(&hi2);
+                        rl[i] = *reinterpret_cast<const uint32_t*>(&lo2);
                     }
+                    const uint32_t off = (uint32_t)((k8 ^ (r & 7)) << 4);
+                    st_shared_v4(dhi + off, rh[0], rh[1], rh[2], rh[3]);
+                    st_shared_v4(dlo + off, rl[0], rl[1], rl[2], rl[3]);
                 }
-                const uint32_t ad = tmem + ((uint32_t)(quad * 32) << 16) + TM_A + ab * 128 + t * 64 + h * 16;
-                tmem_st16(ad, rh);
-                tmem_st16(ad + 32, rl);
+            }
+            fence_proxy_async();
+            mbar_arrive(smem_u32(&bar_bfull[sb]));
+            mbar_arrive(smem_u32(&bar_empty[sl]));
+        }
+    } else {
+        // ---------------------------------------------------------------- running state (epilogue)
+        // warps 8, 12: value columns 0-31; 9, 13: columns 32-63; 10, 14: the normaliser column
+        // (tensor-memory lane 64 = lane 0 of the warp); e = which 128 of the 256 state rows.
+        const int q = warp & 3, e = warp >= 12 ? 1 : 0;
+        const bool zwarp = q == 2;
+        const int col = 32 * q + lane;               // value column (q < 2)
+        const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+        const long row0 = (long)Q * 256 + 128 * e;   // first state row of this warp's 128
+        float gam = 1.f;   // reverse: running max of zmax over the chunks walked so far
+        // the 32 values of rows row0 + 32k + i (i = 0..31) held by lane `src` move to lane i
+        auto gather_lane = [&](const float* v, int src) {
+            float out = 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float t = __shfl_sync(0xffffffffu, v[i], src);
+                if (lane == i) out = t;
+            }
+            return out;
+        };
+        // exports 32 rows (row0 + 32k ..) of the state held as v[i] (divided by gam)
+        auto export_rows = [&](int slot, int k, const float* v) {
+            const float inv = 1.f / gam;
+            const long rbase = row0 + 32 * k;
+            if (zwarp) {
+                const float zv = gather_lane(v, 0);
+                a.zx[(bh * NC + slot) * 4096 + rbase + lane] = zv;
+                return;
+            }
+            __half* hi = a.Sx + ((bh * NC + slot) * 2) * (4096L * 64) + rbase * 64 + col;
+            __half* lo = hi + 4096L * 64;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float x = v[i] * inv;
+                const __half h = __float2half_rn(x);
+                hi[i * 64] = h;
+                lo[i * 64] = __float2half_rn(x - __half2float(h));
+            }
+        };
+        // the initial state (forward: S0 / z0 or zero; reverse: zero), rows row0 + 32k + i
+        auto initial_rows = [&](int k, float* v) {
+            const long rbase = row0 + 32 * k;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0.f;
+            if (rev) return;
+            if (zwarp) {
+                if (a.z0) {
+                    const float zl = a.z0[bh * 4096 + rbase + lane];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = __shfl_sync(0xffffffffu, zl, i);
+                }
+            } else if (a.S0) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = a.S0[(bh * 4096 + rbase + i) * 64 + col];
+            }
+        };
+        {
+            const int slot0 = rev ? NC - 1 : 0;
+            if (a.sscale && Q == 0 && warp == 8 && lane == 0) a.sscale[bh * NC + slot0] = 1.f;
+            for (int k = 0; k < 4; ++k) {
+                float v[32];
+                initial_rows(k, v);
+                export_rows(slot0, k, v);
+            }
+        }
+        bool ok = true;
+        for (int it = 0; it < nchunks && ok; ++it) {
+            const int c = chunk_of(it), b = it & 1;
+            const float dec = __expf(a.g[bh * NC + c]);
+            const float scl = rev ? a.zmax[bh * NC + c] : 1.f;
+            if (abort_s || !(ok = mbar_wait(smem_u32(&bar_hfull[b]), (uint32_t)(it >> 1) & 1, a.status))) break;
+            tc_fence_after();
+            // pass 1: S_c = dec S_{c-1} + scl H^T_c over the buffer of chunk c
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t cur = tmem + lane_base + (uint32_t)b * 256 + 128 * e + 32 * k;
+                float h[32], p[32];
+                tmem_ld32(cur, h);
+                if (it > 0) tmem_ld32(tmem + lane_base + (uint32_t)(1 - b) * 256 + 128 * e + 32 * k, p);
+                else initial_rows(k, p);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) h[i] = fmaf(dec, p[i], scl * h[i]);
+                tmem_st32(cur, h);
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(smem_u32(&bar_afull[ab]));
-        }
-    } else {
-        // ---------------------------------------------------------------- running state
-        const int e = warp - 8, t = e >> 2, quad = e & 3;
-        const int l = quad * 32 + lane;
-        const int m = 4 * Q + 2 * t + (l >> 6), n = l & 63, r = m * 64 + n;
-        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-        float S[65];
-        if (!rev && a.S0) {
-            const float4* src = reinterpret_cast<const float4*>(a.S0 + (bh * 4096 + r) * 64);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const float4 x = src[i];
-                S[4 * i] = x.x; S[4 * i + 1] = x.y; S[4 * i + 2] = x.z; S[4 * i + 3] = x.w;
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 64; ++i) S[i] = 0.f;
-        }
-        S[64] = (!rev && a.z0) ? a.z0[bh * 4096 + r] : 0.f;
-        float gam = 1.f;   // reverse: running max of zmax over the chunks walked so far
-        // exports the running state as two fp16 planes (divided by gam) plus fp32 z
-        auto export_state = [&](int slot) {
-            const float inv = 1.f / gam;
-            if (a.sscale && Q == 0 && e == 0 && lane == 0) a.sscale[bh * NC + slot] = gam;
-            __half* base = a.Sx + ((bh * NC + slot) * 2) * (4096L * 64) + (long)r * 64;
-            uint4* dh = reinterpret_cast<uint4*>(base);
-            uint4* dl = reinterpret_cast<uint4*>(base + 4096L * 64);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                uint32_t ph[4], pl[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float x0 = S[8 * i + 2 * u] * inv, x1 = S[8 * i + 2 * u + 1] * inv;
-                    ph[u] = pack_f16x2(x0, x1);
-                    const __half2 h2 = *reinterpret_cast<const __half2*>(&ph[u]);
-                    pl[u] = pack_f16x2(x0 - __low2float(h2), x1 - __high2float(h2));
-                }
-                dh[i] = make_uint4(ph[0], ph[1], ph[2], ph[3]);
-                dl[i] = make_uint4(pl[0], pl[1], pl[2], pl[3]);
-            }
-            a.zx[(bh * NC + slot) * 4096 + r] = S[64];
-        };
-        // folds the accumulator of chunk `it` into the running state
-        auto update = [&](int it, float gcv, float scl) -> bool {
-            if (abort_s || !mbar_wait(smem_u32(&bar_hfull), it & 1, a.status)) return false;
-            tc_fence_after();
-            const float dec = __expf(gcv);
-            const uint32_t hb = tmem + lane_base + TM_H + t * 80;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                float hv[16];
-                tmem_ld16(hb + 16 * i, hv);
-#pragma unroll
-                for (int k = 0; k < 16; ++k) S[16 * i + k] = fmaf(dec, S[16 * i + k], scl * hv[k]);
-            }
-            S[64] = fmaf(dec, S[64], scl * tmem_ld1(hb + 64));
-            tc_fence_before();
-            mbar_arrive(smem_u32(&bar_hempty));
+            mbar_arrive(smem_u32(&bar_dfree[(it + 1) & 1]));   // the previous buffer has been read
             if (rev) gam = it == 0 ? scl : fmaxf(gam, scl);
-            return true;
-        };
-        export_state(rev ? NC - 1 : 0);
-        bool ok = true;
-        for (int it = 0; it < nchunks && ok; ++it) {
-            const int c = chunk_of(it);
-            const float gcv = a.g[bh * NC + c];                 // loaded while the chunk's MMAs run
-            const float scl = rev ? a.zmax[bh * NC + c] : 1.f;
-            if (!(ok = update(it, gcv, scl))) break;
+            // pass 2: export the state of slot c + 1 (forward) / c - 1 (reverse)
             const int slot = rev ? c - 1 : c + 1;
-            if (slot >= 0 && slot < NC) export_state(slot);
+            if (slot >= 0 && slot < NC) {
+                if (a.sscale && Q == 0 && warp == 8 && lane == 0) a.sscale[bh * NC + slot] = gam;
+                for (int k = 0; k < 4; ++k) {
+                    float v[32];
+                    tmem_ld32(tmem + lane_base + (uint32_t)b * 256 + 128 * e + 32 * k, v);
+                    export_rows(slot, k, v);
+                }
+            }
+            if (!rev && it == nchunks - 1 && (a.S_final || a.z_final)) {
+                for (int k = 0; k < 4; ++k) {
+                    float v[32];
+                    tmem_ld32(tmem + lane_base + (uint32_t)b * 256 + 128 * e + 32 * k, v);
+                    const long rbase = row0 + 32 * k;
+                    if (zwarp) {
+                        const float zv = gather_lane(v, 0);
+                        if (a.z_final) a.z_final[bh * 4096 + rbase + lane] = zv;
+                    } else if (a.S_final) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) a.S_final[(bh * 4096 + rbase + i) * 64 + col] = v[i];
+                    }
+                }
+            }
         }
         if (!ok) abort_s = 1;
-        if (ok && !rev) {
-            if (a.S_final) {
-                float4* dst = reinterpret_cast<float4*>(a.S_final + (bh * 4096 + r) * 64);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) dst[i] = make_float4(S[4 * i], S[4 * i + 1], S[4 * i + 2], S[4 * i + 3]);
-            }
-            if (a.z_final) a.z_final[bh * 4096 + r] = S[64];
-        }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
+    if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
 cudaError_t tc_state_scan(const Problem& p, const ScanIO& io, cudaStream_t s) {
@@ -326,7 +359,7 @@ cudaError_t tc_state_scan(const Problem& p, const ScanIO& io, cudaStream_t s) {
     const uint64_t BH = (uint64_t)p.BH(), Tp = (uint64_t)p.Tp();
     const uint64_t dims[3] = {64, (uint64_t)TC_OPS_ROWS, BH * (Tp / KS)};
     const uint64_t strides[2] = {128, (uint64_t)TC_OPS_ROWS * 128};
-    const uint32_t box[3] = {64, (uint32_t)TC_OPS_ROWS, 2};
+    const uint32_t box[3] = {64, (uint32_t)TC_OPS_ROWS, 1};
     if (!make_tmap_f16_nd(&tops, io.ops, 3, dims, strides, box)) return cudaErrorInvalidValue;
     int* status = tc_status_ptr();
     if (!status) return cudaErrorInvalidValue;
