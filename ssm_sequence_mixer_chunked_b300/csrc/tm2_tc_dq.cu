@@ -45,8 +45,10 @@ constexpr int SDH = SQH + 16384;              // fp16 copy of the dO tile
 constexpr int SZH = SDH + 16384, SZL = SZH + 8192;   // normaliser matrix hi / lo [64][64]
 constexpr int SAV = SZL + 8192;               // chunk-local A, 256 floats
 constexpr int BYTES = SAV + 1024 + 1024;
-// tensor memory: U buffers at 0 and 256; the intra part reuses [0, 256) after the inter part
-constexpr uint32_t TM_DQ = 0, TM_S = 64, TM_W = 128, TM_PH = 192, TM_PL = 224;
+// tensor memory: U buffers at 0 and 256; the intra part reuses it after the inter part: dq
+// accumulator, two (s, u.Vt) buffers and two (P hi, P lo) buffers, so that block b+1's scores
+// are computed while block b's products run
+constexpr uint32_t TM_DQ = 0, TM_SW = 64, TM_P = 320;   // SW buffer x: 64 + 128x (s, +64 u.Vt); P: 320 + 64x
 constexpr uint32_t IDESC_U = idesc_f16_f32(128, 256, false, false);
 constexpr uint32_t IDESC_Z = idesc_f16_f32(128, 64, false, false);
 constexpr uint32_t IDESC_BF_K = idesc_bf16_f32(128, 64, false, false);
@@ -196,34 +198,42 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_cons
                 }
                 umma_commit(smem_u32(&bar_ufull[ub]));
             }
-            // ---- intra-chunk: dq += (hi + lo of dSs) K over the 64-key blocks, in [0, 256)
+            // ---- intra-chunk: dq += (hi + lo of dSs) K over the 64-key blocks
             const int rq = 2 * NG, rk = 2 * NG + 1, rv = 2 * NG + 2;
-            if (ok) ok = mbar_wait(smem_u32(&bar_uempty[0]), (uint32_t)(NG >> 1) & 1, a.status);   // U_z read
+            if (ok) ok = mbar_wait(smem_u32(&bar_uempty[0]), (uint32_t)(NG >> 1) & 1, a.status);          // U_z read
+            if (ok) ok = mbar_wait(smem_u32(&bar_uempty[1]), (uint32_t)((NG - 1) >> 1) & 1, a.status);    // last U read
             if (ok) ok = mbar_wait(smem_u32(&bar_full[slot_of(rq)]), use_of(rq) & 1, a.status);
             if (ok) ok = mbar_wait(smem_u32(&bar_full[slot_of(rk)]), use_of(rk) & 1, a.status);
             if (ok) ok = mbar_wait(smem_u32(&bar_full[slot_of(rv)]), use_of(rv) & 1, a.status);
             tc_fence_after();
             const uint32_t SQ = sb0 + RING + slot_of(rq) * RB, SD = SQ + 16384;
             const uint32_t SK = sb0 + RING + slot_of(rk) * RB, SV = sb0 + RING + slot_of(rv) * RB;
-            for (int b = 0; b < nblk && ok; ++b) {
-                if (abort_s) { ok = false; break; }
-                if (b > 0 && !(ok = mbar_wait(smem_u32(&bar_sfree[b - 1]), 0, a.status))) break;
-                tc_fence_after();
+            auto issue_sw = [&](int b) {   // s = Q K_b^T and u.Vt = dO V_b^T into buffer b & 1
+                const uint32_t sw = tmem + TM_SW + (uint32_t)(b & 1) * 128;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
-                    umma_bf16(tmem + TM_S, sdesc_sw128(SQ + kk * 32), sdesc_sw128(SK + b * 8192 + kk * 32), IDESC_BF_K,
-                              kk > 0);
-                    umma_bf16(tmem + TM_W, sdesc_sw128(SD + kk * 32), sdesc_sw128(SV + b * 8192 + kk * 32), IDESC_BF_K,
+                    umma_bf16(sw, sdesc_sw128(SQ + kk * 32), sdesc_sw128(SK + b * 8192 + kk * 32), IDESC_BF_K, kk > 0);
+                    umma_bf16(sw + 64, sdesc_sw128(SD + kk * 32), sdesc_sw128(SV + b * 8192 + kk * 32), IDESC_BF_K,
                               kk > 0);
                 }
                 umma_commit(smem_u32(&bar_sfull[b]));
+            };
+            if (ok && nblk > 0) issue_sw(0);
+            for (int b = 0; b < nblk && ok; ++b) {
+                if (abort_s) { ok = false; break; }
+                if (b + 1 < nblk) {
+                    if (b >= 1 && !(ok = mbar_wait(smem_u32(&bar_sfree[b - 1]), 0, a.status))) break;
+                    tc_fence_after();
+                    issue_sw(b + 1);
+                }
                 if (!(ok = mbar_wait(smem_u32(&bar_pfull[b]), 0, a.status))) break;
                 tc_fence_after();
+                const uint32_t pb = tmem + TM_P + (uint32_t)(b & 1) * 64;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                     const uint64_t kd = sdesc_sw128_ex(SK + b * 8192 + kk * 2048, 8192, 1024);
-                    umma_bf16_ts(tmem + TM_DQ, tmem + TM_PH + kk * 8, kd, IDESC_BF_MN, (b > 0 || kk > 0) ? 1u : 0u);
-                    umma_bf16_ts(tmem + TM_DQ, tmem + TM_PL + kk * 8, kd, IDESC_BF_MN, 1u);
+                    umma_bf16_ts(tmem + TM_DQ, pb + kk * 8, kd, IDESC_BF_MN, (b > 0 || kk > 0) ? 1u : 0u);
+                    umma_bf16_ts(tmem + TM_DQ, pb + 32 + kk * 8, kd, IDESC_BF_MN, 1u);
                 }
                 umma_commit(smem_u32(&bar_pfree[b]));
             }
@@ -292,15 +302,17 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_cons
         // ---- intra-chunk blocks
         for (int b = 0; b < nblk && ok; ++b) {
             if (!(ok = group_wait(smem_u32(&bar_sfull[b]), 0, a.status, warp == 0, 1, 256, gflags, kg, &abort_s))) break;
-            if (b > 0 && !(ok = group_wait(smem_u32(&bar_pfree[b - 1]), 0, a.status, warp == 0, 1, 256, gflags, kg,
-                                           &abort_s)))
+            if (b >= 2 && !(ok = group_wait(smem_u32(&bar_pfree[b - 2]), 0, a.status, warp == 0, 1, 256, gflags, kg,
+                                            &abort_s)))
                 break;
+            const uint32_t swb = tmem + lane_base + TM_SW + (uint32_t)(b & 1) * 128;
+            const uint32_t pbb = tmem + lane_base + TM_P + (uint32_t)(b & 1) * 64;
 #pragma unroll
             for (int g2 = 0; g2 < 2; ++g2) {
                 const int cc = 2 * h + g2;
                 float sv[16], wv[16];
-                tmem_ld16(tmem + lane_base + TM_S + cc * 16, sv);
-                tmem_ld16(tmem + lane_base + TM_W + cc * 16, wv);
+                tmem_ld16(swb + cc * 16, sv);
+                tmem_ld16(swb + 64 + cc * 16, wv);
                 uint32_t ph[8], pl[8];
 #pragma unroll
                 for (int k2 = 0; k2 < 8; ++k2) {
@@ -316,8 +328,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_cons
                     ph[k2] = pack_bf16x2(hi2[0], hi2[1]);
                     pl[k2] = pack_bf16x2(lo2[0], lo2[1]);
                 }
-                tmem_st8(tmem + lane_base + TM_PH + cc * 8, ph);
-                tmem_st8(tmem + lane_base + TM_PL + cc * 8, pl);
+                tmem_st8(pbb + cc * 8, ph);
+                tmem_st8(pbb + 32 + cc * 8, pl);
             }
             tmem_wait_st();
             tc_fence_before();

@@ -48,8 +48,10 @@ constexpr int SZH = SQH + 16384, SZL = SZH + 8192;   // zm hi / lo, [64][64] fp1
 constexpr int SAV = SZL + 8192;              // chunk-local A, 256 floats
 constexpr int SRED = SAV + 1024;             // [2 halves][128 rows][2]
 constexpr int SMEM_BYTES = SRED + 2048 + 1024;
-// tensor memory: U buffers at 0 and 256; the intra part reuses [0, 256) after the readout
-constexpr uint32_t TM_Y = 0, TM_S = 64, TM_PH = 128, TM_PL = 160;
+// tensor memory: U buffers at 0 and 256; the intra part reuses it after the readout: the
+// intra accumulator, two score buffers and two (P hi, P lo) buffers, so that block b+1's
+// scores are computed while block b's products run
+constexpr uint32_t TM_Y = 0, TM_S = 64, TM_P = 192;   // score buffer x: 64 + 64x; P buffer x: 192 + 64x
 constexpr uint32_t IDESC_U = idesc_f16_f32(128, 256, false, true);
 constexpr uint32_t IDESC_Z = idesc_f16_f32(128, 64, false, false);
 constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 64, false, false);
@@ -201,31 +203,39 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
                 }
                 umma_commit(smem_u32(&bar_ufull[ub]));
             }
-            // ---- intra-chunk blocks (64 keys each), in [0, 256) once U_z has been read
+            // ---- intra-chunk blocks (64 keys each), once the last U and U_z have been read
             const int rq = 2 * NG, rk = 2 * NG + 1, rv = 2 * NG + 2;
             if (ok) ok = mbar_wait(smem_u32(&bar_uempty[0]), (uint32_t)(NG >> 1) & 1, a.status);
+            if (ok) ok = mbar_wait(smem_u32(&bar_uempty[1]), (uint32_t)((NG - 1) >> 1) & 1, a.status);
             if (ok) ok = mbar_wait(smem_u32(&bar_full[slot_of(rq)]), use_of(rq) & 1, a.status);
             if (ok) ok = mbar_wait(smem_u32(&bar_full[slot_of(rk)]), use_of(rk) & 1, a.status);
             if (ok) ok = mbar_wait(smem_u32(&bar_full[slot_of(rv)]), use_of(rv) & 1, a.status);
             tc_fence_after();
             const uint32_t SQ = sb0 + RING + slot_of(rq) * RB;
             const uint32_t SK = sb0 + RING + slot_of(rk) * RB, SV = sb0 + RING + slot_of(rv) * RB;
-            for (int b = 0; b < nblk && ok; ++b) {
-                if (abort_s) { ok = false; break; }
-                if (b > 0 && !(ok = mbar_wait(smem_u32(&bar_sfree[b - 1]), 0, a.status))) break;
-                tc_fence_after();
+            auto issue_s = [&](int b) {   // s = Q K_b^T into score buffer b & 1
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    umma_bf16(tmem + TM_S, sdesc_sw128(SQ + kk * 32), sdesc_sw128(SK + b * 8192 + kk * 32), IDESC_QK,
-                              kk > 0);
+                    umma_bf16(tmem + TM_S + (uint32_t)(b & 1) * 64, sdesc_sw128(SQ + kk * 32),
+                              sdesc_sw128(SK + b * 8192 + kk * 32), IDESC_QK, kk > 0);
                 umma_commit(smem_u32(&bar_sfull[b]));
+            };
+            if (ok && nblk > 0) issue_s(0);
+            for (int b = 0; b < nblk && ok; ++b) {
+                if (abort_s) { ok = false; break; }
+                if (b + 1 < nblk) {
+                    if (b >= 1 && !(ok = mbar_wait(smem_u32(&bar_sfree[b - 1]), 0, a.status))) break;
+                    tc_fence_after();
+                    issue_s(b + 1);
+                }
                 if (!(ok = mbar_wait(smem_u32(&bar_pfull[b]), 0, a.status))) break;
                 tc_fence_after();
+                const uint32_t pb = tmem + TM_P + (uint32_t)(b & 1) * 64;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                     const uint64_t vd = sdesc_sw128_ex(SV + b * 8192 + kk * 2048, 8192, 1024);
-                    umma_bf16_ts(tmem + TM_Y, tmem + TM_PH + kk * 8, vd, IDESC_PV, (b > 0 || kk > 0) ? 1u : 0u);
-                    umma_bf16_ts(tmem + TM_Y, tmem + TM_PL + kk * 8, vd, IDESC_PV, 1u);
+                    umma_bf16_ts(tmem + TM_Y, pb + kk * 8, vd, IDESC_PV, (b > 0 || kk > 0) ? 1u : 0u);
+                    umma_bf16_ts(tmem + TM_Y, pb + 32 + kk * 8, vd, IDESC_PV, 1u);
                 }
                 umma_commit(smem_u32(&bar_pfree[b]));
             }
@@ -289,14 +299,16 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
         // ---- intra-chunk blocks; half h covers 32 of the 64 keys of a block
         for (int b = 0; b < nblk && ok; ++b) {
             if (!(ok = group_wait(smem_u32(&bar_sfull[b]), 0, a.status, warp == 0, 1, 256, gflags, kg, &abort_s))) break;
-            if (b > 0 && !(ok = group_wait(smem_u32(&bar_pfree[b - 1]), 0, a.status, warp == 0, 1, 256, gflags, kg,
-                                           &abort_s)))
+            if (b >= 2 && !(ok = group_wait(smem_u32(&bar_pfree[b - 2]), 0, a.status, warp == 0, 1, 256, gflags, kg,
+                                            &abort_s)))
                 break;
+            const uint32_t sbb = tmem + lane_base + TM_S + (uint32_t)(b & 1) * 64;
+            const uint32_t pbb = tmem + lane_base + TM_P + (uint32_t)(b & 1) * 64;
 #pragma unroll
             for (int g2 = 0; g2 < 2; ++g2) {
                 const int cc = 2 * h + g2;
                 float s[16];
-                tmem_ld16(tmem + lane_base + TM_S + cc * 16, s);
+                tmem_ld16(sbb + cc * 16, s);
                 uint32_t ph[8], pl[8];
 #pragma unroll
                 for (int k2 = 0; k2 < 8; ++k2) {
@@ -313,8 +325,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
                     ph[k2] = pack_bf16x2(hi2[0], hi2[1]);
                     pl[k2] = pack_bf16x2(lo2[0], lo2[1]);
                 }
-                tmem_st8(tmem + lane_base + TM_PH + cc * 8, ph);
-                tmem_st8(tmem + lane_base + TM_PL + cc * 8, pl);
+                tmem_st8(pbb + cc * 8, ph);
+                tmem_st8(pbb + 32 + cc * 8, pl);
             }
             tmem_wait_st();
             tc_fence_before();
