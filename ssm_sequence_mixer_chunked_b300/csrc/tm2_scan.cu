@@ -149,24 +149,40 @@ __global__ void __launch_bounds__(256) tc_dy_prep_kernel(const float* __restrict
                                                          bool normalize) {
     __shared__ float wmax[8];
     const int c = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int sub = lane >> 3, l8 = lane & 7;   // four tokens per warp pass, eight lanes per token
     const long bh = blockIdx.y;
     float mx = 0.f;
-    for (int jj = warp; jj < C; jj += 8) {
-        const long t = (long)c * C + jj;
-        if (t >= T) break;
-        const long tok = bh * T + t;
+    for (int j0 = warp * 4; j0 < C; j0 += 32) {
+        const long t = (long)c * C + j0 + sub;
+        const bool in = t < T;
+        const long tok = bh * T + (in ? t : 0);
         float D = 0.f;
-        for (int cc = lane; cc < 64; cc += 32) D += __bfloat162float(dO[tok * 64 + cc]) * o[tok * 64 + cc];
-        D = warp_sum(D);
-        const float z = normalize ? Z[tok] : 1.f;
-        const float ze = normalize ? (z != 0.f ? 1.f / z : 0.f) : 1.f;
-        if (lane == 0) {
-            zeta[tok] = ze;
-            ucol[tok] = normalize ? -D : 0.f;
-            rowterm[tok] = normalize ? 0.f : D;
+        if (in) {   // elements 8*l8 .. 8*l8+7 of the row: one 16-byte dO load, two 16-byte o loads
+            const uint4 d8 = *reinterpret_cast<const uint4*>(dO + tok * 64 + 8 * l8);
+            const float4 o0 = *reinterpret_cast<const float4*>(o + tok * 64 + 8 * l8);
+            const float4 o1 = *reinterpret_cast<const float4*>(o + tok * 64 + 8 * l8 + 4);
+            const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&d8);
+            const float2 f0 = __bfloat1622float2(b2[0]), f1 = __bfloat1622float2(b2[1]);
+            const float2 f2 = __bfloat1622float2(b2[2]), f3 = __bfloat1622float2(b2[3]);
+            D = f0.x * o0.x + f0.y * o0.y + f1.x * o0.z + f1.y * o0.w + f2.x * o1.x + f2.y * o1.y + f3.x * o1.z +
+                f3.y * o1.w;
         }
-        mx = fmaxf(mx, __expf(Aloc[bh * (long)NC * C + t]) * ze);
+        D += __shfl_xor_sync(0xffffffffu, D, 1);
+        D += __shfl_xor_sync(0xffffffffu, D, 2);
+        D += __shfl_xor_sync(0xffffffffu, D, 4);
+        if (in) {
+            const float z = normalize ? Z[tok] : 1.f;
+            const float ze = normalize ? (z != 0.f ? 1.f / z : 0.f) : 1.f;
+            if (l8 == 0) {
+                zeta[tok] = ze;
+                ucol[tok] = normalize ? -D : 0.f;
+                rowterm[tok] = normalize ? 0.f : D;
+            }
+            mx = fmaxf(mx, __expf(Aloc[bh * (long)NC * C + t]) * ze);
+        }
     }
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
     if (lane == 0) wmax[warp] = mx;
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -220,12 +236,30 @@ __global__ void __launch_bounds__(256) tc_scan_operands_kernel(
         szc[tid] = zc;
     }
     __syncthreads();
-    for (int e = tid; e < 64 * 64; e += 256) {
-        const int j = e >> 6, n = e & 63;
+    for (int e = tid; e < 64 * 8; e += 256) {   // 16-byte loads: token j, elements 8*q8 .. 8*q8+7
+        const int j = e >> 3, q8 = e & 7;
         const long t = t0 + j;
-        const bool in = t < T;
-        sk[j][n] = in ? __bfloat162float(key[(bh * T + t) * 64 + n]) : 0.f;
-        sv[j][n] = in ? __bfloat162float(val[(bh * T + t) * 64 + n]) * sw[j] : 0.f;
+        float kf[8], vf[8];
+        if (t < T) {
+            const uint4 k8 = *reinterpret_cast<const uint4*>(key + (bh * T + t) * 64 + 8 * q8);
+            const uint4 v8 = *reinterpret_cast<const uint4*>(val + (bh * T + t) * 64 + 8 * q8);
+            const __nv_bfloat162* kb = reinterpret_cast<const __nv_bfloat162*>(&k8);
+            const __nv_bfloat162* vb = reinterpret_cast<const __nv_bfloat162*>(&v8);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float2 kk = __bfloat1622float2(kb[u]), vv = __bfloat1622float2(vb[u]);
+                kf[2 * u] = kk.x; kf[2 * u + 1] = kk.y;
+                vf[2 * u] = vv.x * sw[j]; vf[2 * u + 1] = vv.y * sw[j];
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) kf[u] = vf[u] = 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            sk[j][8 * q8 + u] = kf[u];
+            sv[j][8 * q8 + u] = vf[u];
+        }
     }
     __syncthreads();
     __half* blk = ops + (bh * (Tp / 64) + st) * (long)(TC_OPS_ROWS * 64);
