@@ -286,6 +286,12 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
         const float Aj = sAv[j];
         float dv64_in = 0.f;
         int kg = 0;                                      // group-wait counter
+        // global reads issued before the first wait, so their latency hides under the tile loads
+        const float gsc = a.sscale[bh * NC + c];
+        const float gcv = a.g[bh * NC + c];
+        const float rowt = in ? a.rowterm[bh * a.T + tok] : 0.f;
+        float4 zr[4];
+        z_tiles_load(a.dzx + (bh * NC + c) * 4096, threadIdx.x, zr);
         bool ok = mbar_wait(smem_u32(&bar_ld), 0, a.status);
         if (ok) {   // fp16 copies of the key and value tiles; the normaliser gradient matrix / scale
             const int t256 = threadIdx.x;
@@ -293,7 +299,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
                 tile_bf16_to_f16(early, sb0 + SKH, pc);
                 tile_bf16_to_f16(early + 16384, sb0 + SVH, pc);
             }
-            build_z_tiles(smem + SZH, smem + SZL, a.dzx + (bh * NC + c) * 4096, 1.f / a.sscale[bh * NC + c], t256);
+            z_tiles_store(smem + SZH, smem + SZL, zr, 1.f / gsc, t256);
             fence_proxy_async();
         }
         mbar_arrive(smem_u32(&bar_cvt));
@@ -410,8 +416,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
             tmem_ld32(tmem + lane_base + TM_DV + h * 32, dv0);
             tmem_ld32(tmem + lane_base + TM_PARK + h * 64, dkx);
             tmem_ld32(tmem + lane_base + TM_PARK + h * 64 + 32, dvx);
-            const float wj = __expf(a.g[bh * NC + c] - Aj);
-            const float gsc = a.sscale[bh * NC + c];
+            const float wj = __expf(gcv - Aj);
             const float fk = 2.f * wj * gsc, fv = wj * gsc;
             float vdot = 0.f;
             const uint8_t* vrow = smem + SVH;
@@ -434,7 +439,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
                     dkp[u] = make_float4(dk0[4 * u], dk0[4 * u + 1], dk0[4 * u + 2], dk0[4 * u + 3]);
                     dvp[u] = make_float4(dv0[4 * u], dv0[4 * u + 1], dv0[4 * u + 2], dv0[4 * u + 3]);
                 }
-                if (h == 0 && ok) a.dcum[bh * a.T + tok] = a.rowterm[bh * a.T + tok] - (part + sRed[l]);
+                if (h == 0 && ok) a.dcum[bh * a.T + tok] = rowt - (part + sRed[l]);
             }
         }
         if (!ok) abort_s = 1;

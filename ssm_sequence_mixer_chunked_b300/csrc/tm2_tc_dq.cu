@@ -254,6 +254,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_cons
         const float ze = in ? a.zeta[bh * a.T + tok] : 0.f;
         const float uc = in ? a.ucol[bh * a.T + tok] : 0.f;
         int kg = 0;                                      // group-wait counter
+        float4 zr[4];
+        z_tiles_load(a.zx + (bh * NC + c) * 4096, threadIdx.x, zr);   // in flight during the tile wait
         bool ok = mbar_wait(smem_u32(&bar_ld), 0, a.status);
         if (ok) {   // fp16 copies of the Q and dO tiles, and the normaliser matrix of the state
             const int t256 = threadIdx.x;
@@ -261,7 +263,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_cons
                 tile_bf16_to_f16(early, sb0 + SQH, pc);
                 tile_bf16_to_f16(early + 16384, sb0 + SDH, pc);
             }
-            build_z_tiles(smem + SZH, smem + SZL, a.zx + (bh * NC + c) * 4096, 1.f, t256);
+            z_tiles_store(smem + SZH, smem + SZL, zr, 1.f, t256);
             fence_proxy_async();
         }
         mbar_arrive(smem_u32(&bar_cvt));

@@ -252,11 +252,13 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         const float Ai = sAv[i];
         int kg = 0;                                  // group-wait counter
+        float4 zr[4];
+        z_tiles_load(a.zx + (bh * NC + c) * 4096, threadIdx.x, zr);   // in flight during the tile wait
         bool ok = mbar_wait(smem_u32(&bar_ld), 0, a.status);
         if (ok) {   // fp16 copy of the Q tile; the normaliser matrix of the state as hi + lo fp16
             const int t256 = threadIdx.x;
             for (int pc = t256; pc < 1024; pc += 256) tile_bf16_to_f16(early, sb0 + SQH, pc);
-            build_z_tiles(smem + SZH, smem + SZL, a.zx + (bh * NC + c) * 4096, 1.f, t256);
+            z_tiles_store(smem + SZH, smem + SZL, zr, 1.f, t256);
             fence_proxy_async();
         }
         mbar_arrive(smem_u32(&bar_cvt));
