@@ -36,7 +36,7 @@ using namespace tctile;
 constexpr int C = TC_CHUNK;
 constexpr int THREADS = 10 * 32;
 constexpr int WARP_TMA = 8, WARP_MMA = 9;
-constexpr int NR = 5;                        // ring slots of 32 KB
+constexpr int NR = 6;                        // ring slots of 32 KB
 constexpr int RB = 32768;
 constexpr int NG = 16;                       // groups of four state slices
 constexpr int NREQ = 2 * NG + 3;             // hi/lo plane of each group, then Q, K, V (intra part)
@@ -46,8 +46,8 @@ constexpr int RING = 0;
 constexpr int SQH = NR * RB;                 // fp16 copy of the Q tile [128][64]
 constexpr int SZH = SQH + 16384, SZL = SZH + 8192;   // zm hi / lo, [64][64] fp16
 constexpr int SAV = SZL + 8192;              // chunk-local A, 256 floats
-constexpr int SRED = SAV + 1024;             // [2 halves][128 rows][2]
-constexpr int SMEM_BYTES = SRED + 2048 + 1024;
+constexpr int SRED = RING;                   // [2 halves][128 rows][2], in ring slot 0 (idle by then)
+constexpr int SMEM_BYTES = SAV + 1024 + 1024;
 // tensor memory: U buffers at 0 and 256; the intra part reuses it after the readout: the
 // intra accumulator, two score buffers and two (P hi, P lo) buffers, so that block b+1's
 // scores are computed while block b's products run
