@@ -33,7 +33,7 @@ using namespace tctile;
 constexpr int C = TC_CHUNK;
 constexpr int THREADS = 10 * 32;
 constexpr int WARP_TMA = 8, WARP_MMA = 9;
-constexpr int NR = 5;                         // ring slots of 32 KB
+constexpr int NR = 6;                         // ring slots of 32 KB
 constexpr int RB = 32768;
 constexpr int NG = 16;                        // groups of four state slices
 constexpr int NREQ = 2 * NG + 3;              // hi/lo plane of each group, then Q|dO, K, V (intra part)
@@ -42,8 +42,11 @@ constexpr int EARLY = NR - 1;                 // slot NR-1 first holds the Q and
 constexpr int RING = 0;
 constexpr int SQH = NR * RB;                  // fp16 copy of the Q tile [128][64]
 constexpr int SDH = SQH + 16384;              // fp16 copy of the dO tile
-constexpr int SZH = SDH + 16384, SZL = SZH + 8192;   // normaliser matrix hi / lo [64][64]
-constexpr int SAV = SZL + 8192;               // chunk-local A, 256 floats
+// the normaliser matrix (hi, lo [64][64]) goes into the ring slot of group NG-2's lo plane,
+// which no later request uses, once that group's products are done
+constexpr int ZREQ = 2 * NG - 3;
+static_assert(ZREQ + NR >= 2 * NG + 3, "no later request may reuse the normaliser slot");
+constexpr int SAV = SDH + 16384;              // chunk-local A, 256 floats
 constexpr int BYTES = SAV + 1024 + 1024;
 // tensor memory: U buffers at 0 and 256; the intra part reuses it after the inter part: dq
 // accumulator, two (s, u.Vt) buffers and two (P hi, P lo) buffers, so that block b+1's scores
@@ -80,7 +83,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_cons
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_align1024(smem_raw);
     __shared__ __align__(8) uint64_t bar_ld, bar_full[NR], bar_empty[NR], bar_cvt, bar_sfull[4], bar_sfree[4],
-        bar_pfull[4], bar_pfree[4], bar_ufull[2], bar_uempty[2], bar_dqfull, bar_done;
+        bar_pfull[4], bar_pfree[4], bar_ufull[2], bar_uempty[2], bar_dqfull, bar_zrdy, bar_done;
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_s;
     __shared__ volatile int gflags[2];         // group waits of the compute warps
@@ -110,6 +113,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_cons
             mbar_init(smem_u32(&bar_uempty[i]), 256);
         }
         mbar_init(smem_u32(&bar_dqfull), 1);
+        mbar_init(smem_u32(&bar_zrdy), 256);
         mbar_init(smem_u32(&bar_done), 1);
         abort_s = 0;
         fence_mbar_init();
@@ -190,10 +194,13 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_cons
                     umma_commit(smem_u32(&bar_empty[slot_of(2 * g)]));
                     umma_commit(smem_u32(&bar_empty[slot_of(2 * g + 1)]));
                 } else {
+                    if (!(ok = mbar_wait(smem_u32(&bar_zrdy), 0, a.status))) break;   // normaliser tiles built
+                    tc_fence_after();
+                    const uint32_t zh = sb0 + RING + slot_of(ZREQ) * RB, zl = zh + 8192;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        umma_bf16(d, sdesc_sw128(sb0 + SQH + kk * 32), sdesc_sw128(sb0 + SZH + kk * 32), IDESC_Z, kk > 0);
-                        umma_bf16(d, sdesc_sw128(sb0 + SQH + kk * 32), sdesc_sw128(sb0 + SZL + kk * 32), IDESC_Z, 1u);
+                        umma_bf16(d, sdesc_sw128(sb0 + SQH + kk * 32), sdesc_sw128(zh + kk * 32), IDESC_Z, kk > 0);
+                        umma_bf16(d, sdesc_sw128(sb0 + SQH + kk * 32), sdesc_sw128(zl + kk * 32), IDESC_Z, 1u);
                     }
                 }
                 umma_commit(smem_u32(&bar_ufull[ub]));
@@ -257,13 +264,12 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_cons
         float4 zr[4];
         z_tiles_load(a.zx + (bh * NC + c) * 4096, threadIdx.x, zr);   // in flight during the tile wait
         bool ok = mbar_wait(smem_u32(&bar_ld), 0, a.status);
-        if (ok) {   // fp16 copies of the Q and dO tiles, and the normaliser matrix of the state
+        if (ok) {   // fp16 copies of the Q and dO tiles
             const int t256 = threadIdx.x;
             for (int pc = t256; pc < 1024; pc += 256) {
                 tile_bf16_to_f16(early, sb0 + SQH, pc);
                 tile_bf16_to_f16(early + 16384, sb0 + SDH, pc);
             }
-            z_tiles_store(smem + SZH, smem + SZL, zr, 1.f, t256);
             fence_proxy_async();
         }
         mbar_arrive(smem_u32(&bar_cvt));
@@ -278,6 +284,12 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_cons
             if (!(ok = group_wait(smem_u32(&bar_ufull[ub]), (uint32_t)(g >> 1) & 1, a.status, warp == 0, 1, 256, gflags,
                                   kg, &abort_s)))
                 break;
+            if (g == NG - 2) {   // group NG-2's products are done: its lo slot takes the normaliser matrix
+                const uint32_t zh = RING + slot_of(ZREQ) * RB;
+                z_tiles_store(smem + zh, smem + zh + 8192, zr, 1.f, threadIdx.x);
+                fence_proxy_async();
+                mbar_arrive(smem_u32(&bar_zrdy));
+            }
             const uint32_t ua = tmem + lane_base + ub * 256 + h * 32;
             if (g < NG) {
 #pragma unroll 1
