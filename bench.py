@@ -88,6 +88,22 @@ def kernel_flops(name, d, dv, C, tokens):
     return None if per is None else per * tokens
 
 
+def kernel_bytes(name, d, dv, C, tokens, in_bytes=2):
+    """Algorithmic HBM bytes of one launch over `tokens` token-heads: the token rows the kernel
+    must read or write, plus the chunk states it must write or read (two fp16 planes of
+    d^2 x dv and the fp32 normaliser column per chunk, amortised over the C tokens of a
+    chunk).  Scratch the implementation adds (operand blocks) is not counted."""
+    state = (2 * 2 * d * d * dv + 4 * d * d) / C
+    per = {
+        "tc_state_scan_fwd": state + in_bytes * (d + dv),
+        "tc_state_scan_bwd": state + in_bytes * (d + dv) + 4 * 2,
+        "tc_chunk_out": state + in_bytes * (2 * d + dv) + 4 * (dv + 1),
+        "tc_bwd_dq": state + in_bytes * (2 * d + 2 * dv) + 4 * (d + 2),
+        "tc_bwd_dkdv": state + in_bytes * (2 * d + 2 * dv) + 4 * (d + dv + 4),
+    }.get(name)
+    return None if per is None else per * tokens
+
+
 def decode_bytes_per_head(d, dv):
     return 2 * d * d * dv * 4 + 2 * d * d * 4 + 3 * d * 4 + 4 + dv * 4 + 4
 
@@ -291,11 +307,14 @@ def run_reference(args, world, rank):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": step_s * 1e3 / frac, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": config_of(w, 64),
+            "config": config_of(w, TC_CHUNK),
             "cpu_baseline": {"kind": "oracle", "cores": oracle.num_threads(), "sample": sample,
                              "value": value, "unit": "tokens/s"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+TC_CHUNK = 256   # the chunk length the library picks for bf16 inputs with d = dv = 64
 
 
 def config_of(w, C):
@@ -359,18 +378,35 @@ def run_tm2(args, world, rank, device):
     per_launch_tokens = B * H * T
     tc = dom.startswith("tc_")
     kf = kernel_flops(dom, d, dv, 256 if tc else 64, per_launch_tokens)
+    kb = kernel_bytes(dom, d, dv, 256, per_launch_tokens) if tc else None
     roof = None
     if kf is not None:
-        ach = kf / (kern[dom]["ms_per_launch"] * 1e-3) / 1e12
-        if tc:   # timed inside a long step: the sustained bf16 figure
-            peak, bound, src = pk["bf16_tflops_sustained"], "tensor", "MEASURED_PEAKS.json bf16_tflops_sustained (%s)" % pk["source"]
+        sec = kern[dom]["ms_per_launch"] * 1e-3
+        if tc:   # timed inside a long step: the sustained bf16 figure; the bound is whichever of
+            # the algorithmic flops and bytes takes longer at its measured peak
+            t_flop = kf / (pk["bf16_tflops_sustained"] * 1e12)
+            t_byte = kb / (pk["hbm_gbs"] * 1e9)
+            if t_byte > t_flop:
+                roof = {"kernel": dom, "bound": "hbm", "achieved": kb / sec / 1e9, "peak": pk["hbm_gbs"],
+                        "unit": "GB/s", "frac": kb / sec / 1e9 / pk["hbm_gbs"],
+                        "peak_source": "MEASURED_PEAKS.json hbm_gbs (%s)" % pk["source"]}
+            else:
+                roof = {"kernel": dom, "bound": "tensor", "achieved": kf / sec / 1e12,
+                        "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                        "frac": kf / sec / 1e12 / pk["bf16_tflops_sustained"],
+                        "peak_source": "MEASURED_PEAKS.json bf16_tflops_sustained (%s)" % pk["source"]}
+            roof["algorithmic_flops_per_launch"] = kf
+            roof["algorithmic_bytes_per_launch"] = kb
+            roof["tensor_frac"] = kf / sec / 1e12 / pk["bf16_tflops_sustained"]
+            roof["hbm_frac"] = kb / sec / 1e9 / pk["hbm_gbs"]
         else:
             peak = 148 * 128 * 2 * pk["sm_max_mhz"] * 1e6 / 1e12   # FFMA, TFLOP/s
-            bound, src = "alu", "derived: 148 SMs x 128 fp32 FMA/clk x 2 flop x %.0f MHz" % pk["sm_max_mhz"]
-        roof = {"kernel": dom, "bound": bound, "achieved": ach, "peak": peak, "unit": "TFLOP/s",
-                "frac": ach / peak, "traffic": ncu_traffic(dom, per_launch_tokens),
-                "peak_source": src, "algorithmic_flops_per_launch": kf}
-    CH = 256   # chunk length the library picks for bf16 inputs, d = dv = 64
+            roof = {"kernel": dom, "bound": "alu", "achieved": kf / sec / 1e12, "peak": peak, "unit": "TFLOP/s",
+                    "frac": kf / sec / 1e12 / peak,
+                    "peak_source": "derived: 148 SMs x 128 fp32 FMA/clk x 2 flop x %.0f MHz" % pk["sm_max_mhz"],
+                    "algorithmic_flops_per_launch": kf}
+        roof["traffic"] = ncu_traffic(dom, per_launch_tokens)
+    CH = TC_CHUNK
     counted = (fwd_flops(d, dv, CH) + bwd_flops(d, dv, CH)) * B * H * T
     tensor_frac = counted / (step_ms * 1e-3) / (pk["bf16_tflops_sustained"] * 1e12)
 
