@@ -86,7 +86,7 @@ cudaError_t launch_tc_scan_operands(const Problem& p, bool rev, const void* key,
 cudaError_t launch_tc_dy_prep(const Problem& p, const float* o, const float* Z, const void* dO, const float* Aloc,
                               float* zeta, float* ucol, float* rowterm, float* zmax, cudaStream_t s);
 
-// Gradient kernels (tm2_tc_bwd.cu).  dq: Sx/zx are the forward scan's states; dk, dv, dcum:
+// Gradient kernels (tm2_tc_dq.cu, tm2_tc_dkdv.cu).  dq: Sx/zx are the forward scan's states; dk, dv, dcum:
 // dSx/dzx/sscale the reverse scan's.  All outputs (BH,T,·) fp32.
 cudaError_t tc_bwd_dq(const Problem& p, const void* q, const void* k, const void* v, const void* dO, const float* Aloc,
                       const float* zeta, const float* ucol, const void* Sx, const float* zx, float* dq, cudaStream_t s);

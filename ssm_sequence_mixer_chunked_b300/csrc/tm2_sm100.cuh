@@ -138,22 +138,6 @@ TM2_DEV void tma_load_5d(uint32_t dst, const void* tmap, uint32_t bar, int x, in
         "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w), "r"(v)
         : "memory");
 }
-TM2_DEV void tma_load_3d_hint(uint32_t dst, const void* tmap, uint32_t bar, int x, int y, int z, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
-        "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z), "l"(policy)
-        : "memory");
-}
-// Bring a tile into L2 ahead of its TMA load (no shared memory, no barrier).
-TM2_DEV void tma_prefetch_3d(const void* tmap, int x, int y, int z) {
-    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(tmap), "r"(x), "r"(y), "r"(z)
-                 : "memory");
-}
-TM2_DEV void tma_prefetch_4d(const void* tmap, int x, int y, int z, int w) {
-    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(tmap), "r"(x), "r"(y),
-                 "r"(z), "r"(w)
-                 : "memory");
-}
 TM2_DEV void prefetch_tmap(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
@@ -255,14 +239,6 @@ TM2_DEV void tmem_st8(uint32_t taddr, const uint32_t* r) {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
                  "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
                  : "memory");
-}
-TM2_DEV void tmem_st16(uint32_t taddr, const uint32_t* r) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
-            taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
-        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-        : "memory");
 }
 // 32 registers per thread -> 32 lanes x 32 consecutive columns (no wait).
 TM2_DEV void tmem_st32(uint32_t taddr, const float* v) {

@@ -59,40 +59,6 @@ bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t heads, uint6
     return r == CUDA_SUCCESS;
 }
 
-bool make_tmap_state_slices(CUtensorMap* map, const void* base, uint64_t nplanes) {
-    auto enc = encoder();
-    if (!enc) return false;
-    // plane = [4096 rows r = m*64 + n][64 columns] of 16-bit values
-    cuuint64_t dims[4] = {64, 64, 64, nplanes};                     // col, n, m, plane
-    cuuint64_t strides[3] = {128, 64 * 128, 4096 * 128};            // bytes for n, m, plane
-    cuuint32_t box[4] = {64, 1, 64, 1};
-    cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
-// Generic tiled map over 16-bit data with up to 5 dimensions (strides in bytes for dims 1..),
-// 128-byte swizzle; the innermost box extent must be 64 elements.
-// Chunk states [nchunks][2 planes][4096 rows (m*64 + n)][64] fp16; one box = rows
-// 128p .. 128p+127 (slices m = 2p, 2p+1) of both planes, landing as [plane][128][64].
-bool make_tmap_state_pairs(CUtensorMap* map, const void* base, uint64_t nchunks) {
-    const uint64_t dims[4] = {64, 4096, 2, nchunks};
-    const uint64_t strides[3] = {128, 4096 * 128, 2 * 4096 * 128};
-    const uint32_t box[4] = {64, 128, 2, 1};
-    return make_tmap_f16_nd(map, base, 4, dims, strides, box);
-}
-
-// The same states read by the transposed slices {S[(m, n), :] : m} of two consecutive n:
-// dims (col, m, n, plane, chunk), box (64, 64, 2, 2, 1), landing as [plane][n'][m][64].
-bool make_tmap_state_tpairs(CUtensorMap* map, const void* base, uint64_t nchunks) {
-    const uint64_t dims[5] = {64, 64, 64, 2, nchunks};
-    const uint64_t strides[4] = {64 * 128, 128, 4096 * 128, 2 * 4096 * 128};
-    const uint32_t box[5] = {64, 64, 2, 2, 1};
-    return make_tmap_f16_nd(map, base, 5, dims, strides, box);
-}
-
 // Four contiguous slices m = 4g .. 4g+3 of one plane: box rows 256g .. 256g+255,
 // landing as [m'][n][col] (32 KB).  Coordinates (0, 256g, plane, chunk).
 bool make_tmap_state_quads(CUtensorMap* map, const void* base, uint64_t nchunks) {

@@ -17,23 +17,12 @@ bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64
 bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t heads, uint64_t rows, uint64_t cols,
                        uint32_t box_rows);
 
-// 4-D descriptor over state planes [nplanes][4096 rows r = m*64 + n][64 columns] (16-bit):
-// one box is the 64 rows (m = 0..63, n fixed) x 64 columns of one plane, i.e. the slice
-// {S[(m, n), :]} for a fixed second key index n, landing as a [m][column] tile.
-bool make_tmap_state_slices(CUtensorMap* map, const void* base, uint64_t nplanes);
-
 // Tiled map over 16-bit data, `rank` <= 5 dimensions: dims[i] extents (dims[0] contiguous),
 // strides[i - 1] the byte stride of dimension i (any order, multiples of 16), box[i] the box;
 // 128-byte swizzle, box[0] = 64.  The box lands in shared memory dimension 0 fastest.
 bool make_tmap_f16_nd(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
                       const uint32_t* box);
 
-// Chunk-state maps over [nchunks][2][4096][64] fp16 (row m*64 + n): make_tmap_state_pairs
-// boxes the contiguous slices m = 2p, 2p+1 of both planes (32 KB, smem [plane][m'][n][col]);
-// make_tmap_state_tpairs boxes the transposed slices n = 2p, 2p+1 of both planes (32 KB,
-// smem [plane][n'][m][col]).  Coordinates: (0, 128p, 0, chunk) and (0, 0, 2p, 0, chunk).
-bool make_tmap_state_pairs(CUtensorMap* map, const void* base, uint64_t nchunks);
-bool make_tmap_state_tpairs(CUtensorMap* map, const void* base, uint64_t nchunks);
 // One plane of four slices per box (32 KB): make_tmap_state_quads boxes the contiguous slices
 // m = 4g .. 4g+3 (smem [m'][n][col], coordinates (0, 256g, plane, chunk));
 // make_tmap_state_tquads the transposed slices n = 4g .. 4g+3 (smem [n'][m][col],

@@ -45,26 +45,6 @@ TM2_DEV void z_tiles_store(uint8_t* hi, uint8_t* lo, const float4 (&r)[4], float
         st_shared_v4(smem_u32(lo) + off, l[0], l[1], l[2], l[3]);
     }
 }
-// the 64 x 64 normaliser matrix zm[m][n] = scale * z[m*64 + n] as hi + lo fp16 K-major tiles
-TM2_DEV void build_z_tiles(uint8_t* hi, uint8_t* lo, const float* __restrict__ z, float scale, int t256) {
-    for (int pc = t256; pc < 512; pc += 256) {
-        const int m = pc >> 3, k8 = pc & 7;
-        const float4 a0 = *reinterpret_cast<const float4*>(z + m * 64 + k8 * 8);
-        const float4 a1 = *reinterpret_cast<const float4*>(z + m * 64 + k8 * 8 + 4);
-        const float v[8] = {a0.x * scale, a0.y * scale, a0.z * scale, a0.w * scale,
-                            a1.x * scale, a1.y * scale, a1.z * scale, a1.w * scale};
-        uint32_t h[4], l[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            h[u] = pack_f16x2(v[2 * u], v[2 * u + 1]);
-            const __half2 h2 = *reinterpret_cast<const __half2*>(&h[u]);
-            l[u] = pack_f16x2(v[2 * u] - __low2float(h2), v[2 * u + 1] - __high2float(h2));
-        }
-        const uint32_t off = m * 128 + ((k8 ^ (m & 7)) << 4);
-        st_shared_v4(smem_u32(hi) + off, h[0], h[1], h[2], h[3]);
-        st_shared_v4(smem_u32(lo) + off, l[0], l[1], l[2], l[3]);
-    }
-}
 
 }  // namespace tctile
 }  // namespace tm2
