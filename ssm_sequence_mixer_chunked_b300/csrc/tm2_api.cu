@@ -365,7 +365,10 @@ int tm2e_forward(const void* q, const void* k, const void* v, const float* a, vo
     float* cum = at<float>(ws, w.cum);
     TM2_RUN("decay_chunk", launch_decay(p, a, Aloc, g, s));
     TM2_RUN("global_cumsum", launch_global_cumsum(p, Aloc, g, cum, s));
-    TM2_RUN("e_fwd", simt_e_fwd(p, q, k, v, cum, scale, o, lse, s));
+    if (p.dtype == TM2_BF16 && p.d == 64 && p.dv == 64)
+        TM2_RUN("tc_e_fwd", tc_e_fwd(p, q, k, v, cum, scale, (float*)o, lse, s));
+    else
+        TM2_RUN("e_fwd", simt_e_fwd(p, q, k, v, cum, scale, o, lse, s));
     return TM2_OK;
 }
 

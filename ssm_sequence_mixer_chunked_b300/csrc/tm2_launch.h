@@ -106,6 +106,10 @@ cudaError_t launch_decode_step(int N, int H, int d, int dv, int dtype, bool norm
                                float* S, float* z, void* o, float* Z, cudaStream_t s);
 
 // ---- 2Mamba-E (SIMT) -----------------------------------------------------------------
+// 2Mamba-E forward on the tensor cores (tm2_tc_e.cu): bf16, d = dv = 64; cum = global running
+// sum of -softplus(a) (BH, T); o (BH, T, 64) and lse (BH, T) fp32.
+cudaError_t tc_e_fwd(const Problem& p, const void* q, const void* k, const void* v, const float* cum, float scale,
+                     float* o, float* lse, cudaStream_t s);
 cudaError_t simt_e_fwd(const Problem& p, const void* q, const void* k, const void* v,
                        const float* cum, float scale, void* o, float* lse, cudaStream_t s);
 // Dvec[bh][t] = dO_t . o_t

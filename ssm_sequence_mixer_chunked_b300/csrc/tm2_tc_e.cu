@@ -1,0 +1,296 @@
+// tm2_tc_e.cu -- the 2Mamba-E forward on the tensor cores (bf16 inputs, d = dv = 64).
+//
+// "2Mamba2Furious", Sec. 6: causal softmax attention whose logits carry the softplus A-mask,
+//   x_ij = scale q_i . k_j + cumA_i - cumA_j   (j <= i),   o_i = sum_j softmax_j(x_i.) v_j,
+// with lse_i = log sum_j exp(x_ij) saved for the backward.
+//
+// One CTA per (128-query tile, b, h), walking the 128-key blocks at or before the tile from the
+// newest (the diagonal block) to the oldest: the decay bias makes the newest keys' logits the
+// largest, so the running maximum is (nearly) settled by the first block.  Per
+// block: s = Q K^T by tcgen05.mma (M = N = 128, K = 64, bf16 tiles from TMA) into one of two
+// tensor-memory score buffers; the compute warps (row = tensor-memory lane, half h = 64 of
+// the block's keys) add the decay bias, mask, take the row maximum across both halves and
+// write P = exp(x - m) as bf16 into one of two tensor-memory P buffers; O += P V (P from
+// tensor memory, V MN-major from its tile).  The maximum is lazy: O and the row sums are
+// rescaled only when a block's maximum exceeds the one in use by more than 8 (so P <= e^8,
+// well inside bf16), which makes rescales rare.  The next block's QK^T overlaps this block's
+// softmax, and its softmax overlaps this block's PV.  The row sums add the bf16-rounded P
+// that the MMA uses, so o = O / l is exactly normalised for those weights.
+// Warps 0-7 compute (warp w: lane quadrant w % 4, key half w / 4), warp 8 issues TMA, warp 9
+// the MMAs.  Every mbarrier wait is bounded (TM2_ERR_TIMEOUT on expiry).
+#include "tm2.h"
+#include "tm2_launch.h"
+#include "tm2_sm100.cuh"
+#include "tm2_tc.h"
+
+namespace tm2 {
+namespace tce {
+
+constexpr int BQ = 128, BK = 128;
+constexpr int THREADS = 10 * 32;
+constexpr int WARP_TMA = 8, WARP_MMA = 9;
+constexpr int NS = 4;                        // key/value stages
+constexpr int TILE = BK * 128;               // [128][64] bf16
+constexpr int STAGE = 2 * TILE;              // K then V
+constexpr int SQ = 0;
+constexpr int SSTG = TILE;                   // NS stages after the Q tile
+constexpr int SMAX = SSTG + NS * STAGE;      // [2 buffers][2 halves][128] row maxima
+constexpr int SSUM = SMAX + 2 * 2 * BQ * 4;  // [2 halves][128] row sums
+constexpr int SFLAG = SSUM + 2 * BQ * 4;     // [2 buffers][8 warps] rescale requests
+constexpr int SMEM_BYTES = SFLAG + 64 + 1024;
+constexpr uint32_t TM_S = 0;                 // score buffer x at 128 x
+constexpr uint32_t TM_P = 256;               // P buffer x at 256 + 64 x (bf16 pairs)
+constexpr uint32_t TM_O = 384;
+constexpr float LAZY = 8.f;                  // rescale only when the maximum grows by more than this
+constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, false, false);
+constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, 64, false, true);
+
+struct Args {
+    const float* cum;    // [BH][T] inclusive running sum of -softplus(a)
+    float* o;            // [BH][T][64]
+    float* lse;          // [BH][T]
+    int* status;
+    int T, NQ;
+    float scale;
+};
+
+}  // namespace tce
+
+using namespace tce;
+
+__global__ void __launch_bounds__(THREADS, 1) tc_e_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
+                                                              const __grid_constant__ CUtensorMap tmK,
+                                                              const __grid_constant__ CUtensorMap tmV,
+                                                              const __grid_constant__ Args a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_align1024(smem_raw);
+    __shared__ __align__(8) uint64_t bar_q, bar_full[NS], bar_empty[NS], bar_sfull[2], bar_sfree[2], bar_pfull[2],
+        bar_pfree[2], bar_ofull, bar_done;
+    __shared__ uint32_t tmem_base_s;
+    __shared__ volatile int abort_s;
+    __shared__ volatile int gflags[2];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int qt = a.NQ - 1 - (int)blockIdx.x;   // longest tiles first
+    const long bh = blockIdx.y;
+    const int nkb = qt + 1;                      // key blocks at or before the tile
+    const uint32_t sb0 = smem_u32(smem);
+    float* sMax = reinterpret_cast<float*>(smem + SMAX);
+    float* sSum = reinterpret_cast<float*>(smem + SSUM);
+    volatile int* sFlag = reinterpret_cast<volatile int*>(smem + SFLAG);
+
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar_q), 1);
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(smem_u32(&bar_full[i]), 1);
+            mbar_init(smem_u32(&bar_empty[i]), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&bar_sfull[i]), 1);
+            mbar_init(smem_u32(&bar_sfree[i]), 256);
+            mbar_init(smem_u32(&bar_pfull[i]), 256);
+            mbar_init(smem_u32(&bar_pfree[i]), 1);
+        }
+        mbar_init(smem_u32(&bar_ofull), 1);
+        mbar_init(smem_u32(&bar_done), 1);
+        abort_s = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(&tmem_base_s), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_s;
+
+    if (warp == WARP_TMA) {
+        if (lane == 0) {
+            const uint32_t qb = smem_u32(&bar_q);
+            mbar_arrive_expect_tx(qb, TILE);
+            tma_load_3d(sb0 + SQ, &tmQ, qb, 0, qt * BQ, (int)bh);
+            int issued = 0;
+            for (int b = 0; b < nkb && !abort_s; ++b) {
+                const int st = b % NS;
+                if (b >= NS && !mbar_wait(smem_u32(&bar_empty[st]), (uint32_t)((b / NS) - 1) & 1, a.status)) {
+                    abort_s = 1;
+                    break;
+                }
+                const uint32_t fb = smem_u32(&bar_full[st]), dst = sb0 + SSTG + st * STAGE;
+                mbar_arrive_expect_tx(fb, STAGE);
+                tma_load_3d(dst, &tmK, fb, 0, (qt - b) * BK, (int)bh);          // newest block first
+                tma_load_3d(dst + TILE, &tmV, fb, 0, (qt - b) * BK, (int)bh);
+                issued = b + 1;
+            }
+            mbar_wait(qb, 0, a.status);
+            for (int b = issued - 1; b >= 0 && b >= issued - NS; --b)
+                mbar_wait(smem_u32(&bar_full[b % NS]), (uint32_t)(b / NS) & 1, a.status);
+        }
+    } else if (warp == WARP_MMA) {
+        if (lane == 0) {
+            bool ok = mbar_wait(smem_u32(&bar_q), 0, a.status);
+            tc_fence_after();
+            // s(b) = Q K_b^T, then O += P(b-1) V(b-1): block b's scores overlap block b-1's softmax
+            for (int b = 0; b <= nkb && ok; ++b) {
+                if (abort_s) { ok = false; break; }
+                if (b < nkb) {
+                    const int st = b % NS, x = b & 1;
+                    if (!(ok = mbar_wait(smem_u32(&bar_full[st]), (uint32_t)(b / NS) & 1, a.status))) break;
+                    if (b >= 2 && !(ok = mbar_wait(smem_u32(&bar_sfree[x]), (uint32_t)((b >> 1) - 1) & 1, a.status)))
+                        break;
+                    tc_fence_after();
+                    const uint32_t kb = sb0 + SSTG + st * STAGE;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma_bf16(tmem + TM_S + x * 128, sdesc_sw128(sb0 + SQ + kk * 32), sdesc_sw128(kb + kk * 32),
+                                  IDESC_S, kk > 0);
+                    umma_commit(smem_u32(&bar_sfull[x]));
+                }
+                if (b >= 1) {
+                    const int c = b - 1, st = c % NS, x = c & 1;
+                    if (!(ok = mbar_wait(smem_u32(&bar_pfull[x]), (uint32_t)(c >> 1) & 1, a.status))) break;
+                    tc_fence_after();
+                    const uint32_t vb = sb0 + SSTG + st * STAGE + TILE;
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        umma_bf16_ts(tmem + TM_O, tmem + TM_P + x * 64 + kk * 8,
+                                     sdesc_sw128_ex(vb + kk * 2048, 8192, 1024), IDESC_PV, (c > 0 || kk > 0) ? 1u : 0u);
+                    umma_commit(smem_u32(&bar_pfree[x]));
+                    umma_commit(smem_u32(&bar_empty[st]));
+                }
+            }
+            if (ok) umma_commit(smem_u32(&bar_ofull));
+            else abort_s = 1;
+            umma_commit(smem_u32(&bar_done));
+            mbar_wait(smem_u32(&bar_done), 0, a.status);
+        }
+    } else {
+        // ---------------------------------------------------------------- compute warps
+        const int quad = warp & 3, h = warp >> 2;
+        const int l = quad * 32 + lane;                  // tile row
+        const long i = (long)qt * BQ + l;                // query
+        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        const float* cumh = a.cum + bh * a.T;
+        const float ci = i < a.T ? cumh[i] : 0.f;
+        float m_used = -INFINITY, lsum = 0.f;
+        int kg = 0;
+        bool ok = true;
+        for (int b = 0; b < nkb && ok; ++b) {
+            const int x = b & 1;
+            if (!(ok = group_wait(smem_u32(&bar_sfull[x]), (uint32_t)(b >> 1) & 1, a.status, warp == 0, 1, 256, gflags,
+                                  kg, &abort_s)))
+                break;
+            float s[64];
+            tmem_ld32(tmem + lane_base + TM_S + x * 128 + h * 64, s);
+            tmem_ld32(tmem + lane_base + TM_S + x * 128 + h * 64 + 32, s + 32);
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bar_sfree[x]));        // the score buffer may take block b+2
+            const long j0 = (long)(qt - b) * BK + h * 64;   // keys of this block (newest first)
+            float bmax = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+                const long j = j0 + c;
+                const float cj = j < a.T ? __ldg(cumh + j) : 0.f;   // the same address in every lane
+                s[c] = (j <= i && j < a.T) ? fmaf(a.scale, s[c], ci - cj) : -INFINITY;
+                bmax = fmaxf(bmax, s[c]);
+            }
+            // row maximum over both key halves (the partner thread holds the other 64 keys), and
+            // whether any row needs a rescale (one decision for the whole CTA, so that every wait
+            // and every warp-wide tensor-memory access below is taken by all compute threads)
+            sMax[(x * 2 + h) * BQ + l] = bmax;
+            const float bm_own = bmax;
+            bool need = false;
+            {
+                // the partner's maximum is read after the barrier; the request flag is this warp's
+                const int req = __any_sync(0xffffffffu, bm_own > m_used + LAZY) ? 1 : 0;
+                if (lane == 0) sFlag[x * 8 + warp] = req;
+            }
+            named_bar_sync(2, 256);
+            bmax = fmaxf(bmax, sMax[(x * 2 + (1 - h)) * BQ + l]);
+            need = bmax > m_used + LAZY;   // the same in both halves of a row
+            int any = 0;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) any |= sFlag[x * 8 + w];
+            if (any) {
+                const float fac = !need ? 1.f : (m_used == -INFINITY ? 0.f : __expf(m_used - bmax));
+                if (b > 0) {             // O holds blocks < b once the previous product is done
+                    if (!(ok = group_wait(smem_u32(&bar_pfree[(b - 1) & 1]), (uint32_t)((b - 1) >> 1) & 1, a.status,
+                                          warp == 0, 1, 256, gflags, kg, &abort_s)))
+                        break;
+                    float ov[32];
+                    tmem_ld32(tmem + lane_base + TM_O + h * 32, ov);
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) ov[c] *= fac;
+                    tmem_st32(tmem + lane_base + TM_O + h * 32, ov);
+                    tmem_wait_st();
+                }
+                if (need) {
+                    lsum *= fac;
+                    m_used = bmax;
+                }
+            }
+            // P = exp(x - m) in bf16 into P buffer x (free once block b-2's product is done)
+            if (b >= 2 && !(ok = group_wait(smem_u32(&bar_pfree[x]), (uint32_t)((b >> 1) - 1) & 1, a.status, warp == 0,
+                                            1, 256, gflags, kg, &abort_s)))
+                break;
+            uint32_t pk[32];
+#pragma unroll
+            for (int c2 = 0; c2 < 32; ++c2) {
+                float p0 = m_used == -INFINITY ? 0.f : __expf(s[2 * c2] - m_used);
+                float p1 = m_used == -INFINITY ? 0.f : __expf(s[2 * c2 + 1] - m_used);
+                const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+                const float2 r2 = __bfloat1622float2(b2);
+                lsum += r2.x + r2.y;
+                pk[c2] = *reinterpret_cast<const uint32_t*>(&b2);
+            }
+            tmem_st8(tmem + lane_base + TM_P + x * 64 + h * 32, pk);
+            tmem_st8(tmem + lane_base + TM_P + x * 64 + h * 32 + 8, pk + 8);
+            tmem_st8(tmem + lane_base + TM_P + x * 64 + h * 32 + 16, pk + 16);
+            tmem_st8(tmem + lane_base + TM_P + x * 64 + h * 32 + 24, pk + 24);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bar_pfull[x]));
+        }
+        // ---- o = O / l, lse = m + log l (the two halves' sums combined)
+        if (ok) sSum[h * BQ + l] = lsum;
+        named_bar_sync(2, 256);
+        if (ok && !abort_s && (ok = mbar_wait(smem_u32(&bar_ofull), 0, a.status))) {
+            tc_fence_after();
+            const float lt = lsum + sSum[(1 - h) * BQ + l];
+            float ov[32];
+            tmem_ld32(tmem + lane_base + TM_O + h * 32, ov);
+            if (i < a.T) {
+                const float inv = lt > 0.f ? 1.f / lt : 0.f;
+                float4* dst = reinterpret_cast<float4*>(a.o + (bh * a.T + i) * 64 + h * 32);
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    dst[u] = make_float4(ov[4 * u] * inv, ov[4 * u + 1] * inv, ov[4 * u + 2] * inv, ov[4 * u + 3] * inv);
+                if (h == 0) a.lse[bh * a.T + i] = m_used + __logf(lt);
+            }
+        }
+        if (!ok) abort_s = 1;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+cudaError_t tc_e_fwd(const Problem& p, const void* q, const void* k, const void* v, const float* cum, float scale,
+                     float* o, float* lse, cudaStream_t s) {
+    CUtensorMap tq, tk, tv;
+    const uint64_t BH = (uint64_t)p.BH(), T = (uint64_t)p.T;
+    if (!make_tmap_bf16_3d(&tq, q, BH, T, 64, BQ) || !make_tmap_bf16_3d(&tk, k, BH, T, 64, BK) ||
+        !make_tmap_bf16_3d(&tv, v, BH, T, 64, BK))
+        return cudaErrorInvalidValue;
+    int* status = tc_status_ptr();
+    if (!status) return cudaErrorInvalidValue;
+    const int NQ = (p.T + BQ - 1) / BQ;
+    Args a{cum, o, lse, status, p.T, NQ, scale};
+    cudaError_t e = cudaFuncSetAttribute(tc_e_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)NQ, (unsigned)p.BH());
+    tc_e_fwd_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(tq, tk, tv, a);
+    return cudaGetLastError();
+}
+
+}  // namespace tm2
