@@ -154,7 +154,7 @@ int tm2e_forward(const void* q, const void* k, const void* v, const float* a,
  * workspace: its scratch is a fixed array of TM2E_NOALLOC_SCRATCH_BYTES compiled into
  * the library, held by every GPU that loads the library until the process exits.
  *  - Scratch need is about 8 * B*H*T bytes; larger problems return TM2_ERR_WORKSPACE
- *    before anything is launched (B*H*T up to roughly 2 million token-heads fits).
+ *    before anything is launched (B*H*T up to roughly 1.3 million token-heads fits).
  *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress,
  *    with that device current); make that first call before any stream capture.
  *  - No cudaMalloc, cudaFree or other allocating routine is called.

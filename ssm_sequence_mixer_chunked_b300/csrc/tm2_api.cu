@@ -98,13 +98,14 @@ static BwdWs plan_bwd(const Problem& p) {
     return w;
 }
 
-struct EWs { size_t Aloc, g, cum, Dvec, rowsum, colsum, total; };
+struct EWs { size_t Aloc, g, cum, cum_lo, Dvec, rowsum, colsum, total; };
 static EWs plan_e(const Problem& p, bool backward) {
     Carve c;
     EWs w{};
     w.Aloc = c.take(sizeof(float) * p.BH() * p.Tp());
     w.g = c.take(sizeof(float) * p.BH() * p.NC);
     w.cum = c.take(sizeof(float) * p.BH() * p.T);
+    w.cum_lo = c.take(sizeof(float) * p.BH() * p.T);
     if (backward) {
         w.Dvec = c.take(sizeof(float) * p.BH() * p.T);
         w.rowsum = c.take(sizeof(float) * p.BH() * p.T);
@@ -363,12 +364,13 @@ int tm2e_forward(const void* q, const void* k, const void* v, const float* a, vo
     float* Aloc = at<float>(ws, w.Aloc);
     float* g = at<float>(ws, w.g);
     float* cum = at<float>(ws, w.cum);
+    float* cum_lo = at<float>(ws, w.cum_lo);
     TM2_RUN("decay_chunk", launch_decay(p, a, Aloc, g, s));
-    TM2_RUN("global_cumsum", launch_global_cumsum(p, Aloc, g, cum, s));
+    TM2_RUN("global_cumsum", launch_global_cumsum(p, Aloc, g, cum, cum_lo, s));
     if (p.dtype == TM2_BF16 && p.d == 64 && p.dv == 64)
-        TM2_RUN("tc_e_fwd", tc_e_fwd(p, q, k, v, cum, scale, (float*)o, lse, s));
+        TM2_RUN("tc_e_fwd", tc_e_fwd(p, q, k, v, cum, cum_lo, scale, (float*)o, lse, s));
     else
-        TM2_RUN("e_fwd", simt_e_fwd(p, q, k, v, cum, scale, o, lse, s));
+        TM2_RUN("e_fwd", simt_e_fwd(p, q, k, v, cum, cum_lo, scale, o, lse, s));
     return TM2_OK;
 }
 
@@ -399,13 +401,14 @@ int tm2e_backward(const void* q, const void* k, const void* v, const float* a, c
     float* Aloc = at<float>(ws, w.Aloc);
     float* g = at<float>(ws, w.g);
     float* cum = at<float>(ws, w.cum);
+    float* cum_lo = at<float>(ws, w.cum_lo);
     float* Dvec = at<float>(ws, w.Dvec);
     float* rowsum = at<float>(ws, w.rowsum);
     float* colsum = at<float>(ws, w.colsum);
     TM2_RUN("decay_chunk", launch_decay(p, a, Aloc, g, s));
-    TM2_RUN("global_cumsum", launch_global_cumsum(p, Aloc, g, cum, s));
+    TM2_RUN("global_cumsum", launch_global_cumsum(p, Aloc, g, cum, cum_lo, s));
     TM2_RUN("rowdot", launch_rowdot(p, o, dO, Dvec, s));
-    TM2_RUN("e_bwd", simt_e_bwd(p, q, k, v, cum, lse, Dvec, dO, scale, dq, dk, dv, rowsum, colsum, s));
+    TM2_RUN("e_bwd", simt_e_bwd(p, q, k, v, cum, cum_lo, lse, Dvec, dO, scale, dq, dk, dv, rowsum, colsum, s));
     TM2_RUN("reverse_cumsum_da", launch_reverse_cumsum_da(p, a, rowsum, colsum, da, s));
     return TM2_OK;
 }

@@ -15,7 +15,7 @@ constexpr int EB = 64;
 template <int D, int DV, typename Tin>
 __global__ void __launch_bounds__(256) e_fwd_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
                                                     const Tin* __restrict__ v, const float* __restrict__ cum,
-                                                    float scale, float* __restrict__ o,
+                                                    const float* __restrict__ cum_lo, float scale, float* __restrict__ o,
                                                     float* __restrict__ lse, int T) {
     constexpr int LDQ = D + 1, LDP = EB + 1, NCOL = DV / 16;
     extern __shared__ float sm[];
@@ -25,6 +25,8 @@ __global__ void __launch_bounds__(256) e_fwd_kernel(const Tin* __restrict__ q, c
     float* sP = sv + EB * DV;     // [EB][LDP]
     float* scq = sP + EB * LDP;   // [EB]
     float* sck = scq + EB;        // [EB]
+    float* scql = sck + EB;       // [EB] residuals of the running sums
+    float* sckl = scql + EB;      // [EB]
     const int qb = blockIdx.x;
     const long bh = blockIdx.y;
     const int tid = threadIdx.x, ti = tid >> 4, tc = tid & 15;
@@ -36,6 +38,7 @@ __global__ void __launch_bounds__(256) e_fwd_kernel(const Tin* __restrict__ q, c
     for (int i = tid; i < EB; i += 256) {
         const long t = (long)qb * EB + i;
         scq[i] = t < T ? cum[bh * T + t] : 0.f;
+        scql[i] = t < T ? cum_lo[bh * T + t] : 0.f;
     }
     float acc[4][NCOL], mrow[4], lrow[4];
 #pragma unroll
@@ -60,6 +63,7 @@ __global__ void __launch_bounds__(256) e_fwd_kernel(const Tin* __restrict__ q, c
         for (int j = tid; j < EB; j += 256) {
             const long t = (long)kb * EB + j;
             sck[j] = t < T ? cum[bh * T + t] : 0.f;
+            sckl[j] = t < T ? cum_lo[bh * T + t] : 0.f;
         }
         __syncthreads();
 #pragma unroll
@@ -75,7 +79,7 @@ __global__ void __launch_bounds__(256) e_fwd_kernel(const Tin* __restrict__ q, c
                 float dot = 0.f;
 #pragma unroll 16
                 for (int n = 0; n < D; ++n) dot = fmaf(sq[i * LDQ + n], sk[j * LDQ + n], dot);
-                x[s] = (jg <= ig && jg < T) ? scale * dot + scq[i] - sck[j] : -INFINITY;
+                x[s] = (jg <= ig && jg < T) ? scale * dot + (scq[i] - sck[j]) + (scql[i] - sckl[j]) : -INFINITY;
                 mx = fmaxf(mx, x[s]);
             }
 #pragma unroll
@@ -125,8 +129,8 @@ __global__ void __launch_bounds__(256) e_fwd_kernel(const Tin* __restrict__ q, c
 template <int D, int DV, typename Tin>
 __global__ void __launch_bounds__(256) e_bwd_dkdv_kernel(
     const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
-    const float* __restrict__ cum, const float* __restrict__ lse, const float* __restrict__ Dvec,
-    const Tin* __restrict__ dO, float scale, float* __restrict__ dk, float* __restrict__ dvo,
+    const float* __restrict__ cum, const float* __restrict__ cum_lo, const float* __restrict__ lse,
+    const float* __restrict__ Dvec, const Tin* __restrict__ dO, float scale, float* __restrict__ dk, float* __restrict__ dvo,
     float* __restrict__ colsum, int T, int NQB) {
     constexpr int LDQ = D + 1, LDV = DV + 1, LDP = EB + 1, NCOL = DV / 16, NN = D / 16;
     extern __shared__ float sm[];
@@ -140,6 +144,8 @@ __global__ void __launch_bounds__(256) e_bwd_dkdv_kernel(
     float* scq = sck + EB;          // [EB]
     float* slse = scq + EB;         // [EB]
     float* sD = slse + EB;          // [EB]
+    float* sckl = sD + EB;          // [EB] residuals of the running sums
+    float* scql = sckl + EB;        // [EB]
     const int kb = blockIdx.x;
     const long bh = blockIdx.y;
     const int tid = threadIdx.x, ti = tid >> 4, tc = tid & 15;
@@ -156,6 +162,7 @@ __global__ void __launch_bounds__(256) e_bwd_dkdv_kernel(
     for (int j = tid; j < EB; j += 256) {
         const long t = (long)kb * EB + j;
         sck[j] = t < T ? cum[bh * T + t] : 0.f;
+        sckl[j] = t < T ? cum_lo[bh * T + t] : 0.f;
     }
     float adk[4][NN], adv[4][NCOL], cs[4];
 #pragma unroll
@@ -181,6 +188,7 @@ __global__ void __launch_bounds__(256) e_bwd_dkdv_kernel(
         for (int i = tid; i < EB; i += 256) {
             const long t = (long)qb * EB + i;
             scq[i] = t < T ? cum[bh * T + t] : 0.f;
+            scql[i] = t < T ? cum_lo[bh * T + t] : 0.f;
             slse[i] = t < T ? lse[bh * T + t] : 0.f;
             sD[i] = t < T ? Dvec[bh * T + t] : 0.f;
         }
@@ -199,7 +207,7 @@ __global__ void __launch_bounds__(256) e_bwd_dkdv_kernel(
                     float dP = 0.f;
 #pragma unroll 16
                     for (int cc = 0; cc < DV; ++cc) dP = fmaf(sdo[i * LDV + cc], sv[j * LDV + cc], dP);
-                    P = __expf(scale * dot + scq[i] - sck[j] - slse[i]);
+                    P = __expf(scale * dot + (scq[i] - sck[j]) + (scql[i] - sckl[j]) - slse[i]);
                     dX = P * (dP - sD[i]);
                 }
                 sP[i * LDP + j] = P;
@@ -240,8 +248,8 @@ __global__ void __launch_bounds__(256) e_bwd_dkdv_kernel(
 template <int D, int DV, typename Tin>
 __global__ void __launch_bounds__(256) e_bwd_dq_kernel(
     const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
-    const float* __restrict__ cum, const float* __restrict__ lse, const float* __restrict__ Dvec,
-    const Tin* __restrict__ dO, float scale, float* __restrict__ dq, float* __restrict__ rowsum, int T) {
+    const float* __restrict__ cum, const float* __restrict__ cum_lo, const float* __restrict__ lse,
+    const float* __restrict__ Dvec, const Tin* __restrict__ dO, float scale, float* __restrict__ dq, float* __restrict__ rowsum, int T) {
     constexpr int LDQ = D + 1, LDV = DV + 1, LDP = EB + 1, NN = D / 16;
     extern __shared__ float sm[];
     float* sq = sm;                 // [EB][LDQ]
@@ -253,6 +261,8 @@ __global__ void __launch_bounds__(256) e_bwd_dq_kernel(
     float* sck = scq + EB;          // [EB]
     float* slse = sck + EB;         // [EB]
     float* sD = slse + EB;          // [EB]
+    float* scql = sD + EB;          // [EB] residuals of the running sums
+    float* sckl = scql + EB;        // [EB]
     const int qb = blockIdx.x;
     const long bh = blockIdx.y;
     const int tid = threadIdx.x, ti = tid >> 4, tc = tid & 15;
@@ -269,6 +279,7 @@ __global__ void __launch_bounds__(256) e_bwd_dq_kernel(
     for (int i = tid; i < EB; i += 256) {
         const long t = (long)qb * EB + i;
         scq[i] = t < T ? cum[bh * T + t] : 0.f;
+        scql[i] = t < T ? cum_lo[bh * T + t] : 0.f;
         slse[i] = t < T ? lse[bh * T + t] : 0.f;
         sD[i] = t < T ? Dvec[bh * T + t] : 0.f;
     }
@@ -294,6 +305,7 @@ __global__ void __launch_bounds__(256) e_bwd_dq_kernel(
         for (int j = tid; j < EB; j += 256) {
             const long t = (long)kb * EB + j;
             sck[j] = t < T ? cum[bh * T + t] : 0.f;
+            sckl[j] = t < T ? cum_lo[bh * T + t] : 0.f;
         }
         __syncthreads();
 #pragma unroll
@@ -310,7 +322,7 @@ __global__ void __launch_bounds__(256) e_bwd_dq_kernel(
                     float dP = 0.f;
 #pragma unroll 16
                     for (int cc = 0; cc < DV; ++cc) dP = fmaf(sdo[i * LDV + cc], sv[j * LDV + cc], dP);
-                    const float P = __expf(scale * dot + scq[i] - sck[j] - slse[i]);
+                    const float P = __expf(scale * dot + (scq[i] - sck[j]) + (scql[i] - sckl[j]) - slse[i]);
                     dX = P * (dP - sD[i]);
                 }
                 sX[i * LDP + j] = dX;
@@ -344,41 +356,43 @@ __global__ void __launch_bounds__(256) e_bwd_dq_kernel(
 
 template <int D, int DV, typename Tin>
 static cudaError_t run_e_fwd(const Problem& p, const void* q, const void* k, const void* v,
-                             const float* cum, float scale, void* o, float* lse, cudaStream_t s) {
-    const size_t smem = sizeof(float) * (size_t)(2 * EB * (D + 1) + EB * DV + EB * (EB + 1) + 2 * EB);
+                             const float* cum, const float* cum_lo, float scale, void* o, float* lse,
+                             cudaStream_t s) {
+    const size_t smem = sizeof(float) * (size_t)(2 * EB * (D + 1) + EB * DV + EB * (EB + 1) + 4 * EB);
     auto kern = e_fwd_kernel<D, DV, Tin>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((p.T + EB - 1) / EB, (unsigned)p.BH());
-    kern<<<grid, 256, smem, s>>>((const Tin*)q, (const Tin*)k, (const Tin*)v, cum, scale, (float*)o, lse, p.T);
+    kern<<<grid, 256, smem, s>>>((const Tin*)q, (const Tin*)k, (const Tin*)v, cum, cum_lo, scale, (float*)o, lse,
+                                 p.T);
     return cudaGetLastError();
 }
 
 template <int D, int DV, typename Tin>
 static cudaError_t run_e_bwd(const Problem& p, const void* q, const void* k, const void* v,
-                             const float* cum, const float* lse, const float* Dvec, const void* dO,
-                             float scale, void* dq, void* dk, void* dv, float* rowsum, float* colsum,
-                             cudaStream_t s) {
+                             const float* cum, const float* cum_lo, const float* lse, const float* Dvec,
+                             const void* dO, float scale, void* dq, void* dk, void* dv, float* rowsum,
+                             float* colsum, cudaStream_t s) {
     const int NQB = (p.T + EB - 1) / EB;
     dim3 grid(NQB, (unsigned)p.BH());
     {
         const size_t smem = sizeof(float) * (size_t)(2 * EB * (D + 1) + 2 * EB * (DV + 1) +
-                                                     2 * EB * (EB + 1) + 4 * EB);
+                                                     2 * EB * (EB + 1) + 6 * EB);
         auto kern = e_bwd_dkdv_kernel<D, DV, Tin>;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        kern<<<grid, 256, smem, s>>>((const Tin*)q, (const Tin*)k, (const Tin*)v, cum, lse, Dvec,
+        kern<<<grid, 256, smem, s>>>((const Tin*)q, (const Tin*)k, (const Tin*)v, cum, cum_lo, lse, Dvec,
                                      (const Tin*)dO, scale, (float*)dk, (float*)dv, colsum, p.T, NQB);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     {
         const size_t smem = sizeof(float) * (size_t)(2 * EB * (D + 1) + 2 * EB * (DV + 1) +
-                                                     EB * (EB + 1) + 4 * EB);
+                                                     EB * (EB + 1) + 6 * EB);
         auto kern = e_bwd_dq_kernel<D, DV, Tin>;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        kern<<<grid, 256, smem, s>>>((const Tin*)q, (const Tin*)k, (const Tin*)v, cum, lse, Dvec,
+        kern<<<grid, 256, smem, s>>>((const Tin*)q, (const Tin*)k, (const Tin*)v, cum, cum_lo, lse, Dvec,
                                      (const Tin*)dO, scale, (float*)dq, rowsum, p.T);
     }
     return cudaGetLastError();
@@ -401,15 +415,15 @@ static cudaError_t run_e_bwd(const Problem& p, const void* q, const void* k, con
     } while (0)
 
 cudaError_t simt_e_fwd(const Problem& p, const void* q, const void* k, const void* v,
-                       const float* cum, float scale, void* o, float* lse, cudaStream_t s) {
-    TM2_E_DISPATCH(p, (run_e_fwd<D, D, Tin>(p, q, k, v, cum, scale, o, lse, s)));
+                       const float* cum, const float* cum_lo, float scale, void* o, float* lse, cudaStream_t s) {
+    TM2_E_DISPATCH(p, (run_e_fwd<D, D, Tin>(p, q, k, v, cum, cum_lo, scale, o, lse, s)));
 }
 
 cudaError_t simt_e_bwd(const Problem& p, const void* q, const void* k, const void* v,
-                       const float* cum, const float* lse, const float* Dvec, const void* dO,
-                       float scale, void* dq, void* dk, void* dv, float* rowsum, float* colsum,
-                       cudaStream_t s) {
-    TM2_E_DISPATCH(p, (run_e_bwd<D, D, Tin>(p, q, k, v, cum, lse, Dvec, dO, scale, dq, dk, dv,
+                       const float* cum, const float* cum_lo, const float* lse, const float* Dvec,
+                       const void* dO, float scale, void* dq, void* dk, void* dv, float* rowsum,
+                       float* colsum, cudaStream_t s) {
+    TM2_E_DISPATCH(p, (run_e_bwd<D, D, Tin>(p, q, k, v, cum, cum_lo, lse, Dvec, dO, scale, dq, dk, dv,
                                             rowsum, colsum, s)));
 }
 

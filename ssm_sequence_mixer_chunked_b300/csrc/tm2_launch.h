@@ -21,8 +21,10 @@ struct Problem {
 // Aloc[bh][t] (t < Tp): inclusive running sum of -softplus(a) inside each chunk
 // (padded positions repeat the last valid value); g[bh][c]: chunk total.
 cudaError_t launch_decay(const Problem& p, const float* a, float* Aloc, float* g, cudaStream_t s);
-// cum[bh][t] = global inclusive running sum (t < T), from Aloc and g.
-cudaError_t launch_global_cumsum(const Problem& p, const float* Aloc, const float* g, float* cum,
+// cum[bh][t] = global inclusive running sum (t < T), from Aloc and g, rounded to fp32; cum_lo
+// (optional) its rounding residual, so that cum_i - cum_j = (hi_i - hi_j) + (lo_i - lo_j) keeps
+// fp32 precision however large the sums grow.
+cudaError_t launch_global_cumsum(const Problem& p, const float* Aloc, const float* g, float* cum, float* cum_lo,
                                  cudaStream_t s);
 // da[bh][u] = -sigmoid(a[bh][u]) * sum_{t >= u} (row[bh][t] - col[bh][t]); col may be NULL.
 cudaError_t launch_reverse_cumsum_da(const Problem& p, const float* a, const float* row,
@@ -108,15 +110,15 @@ cudaError_t launch_decode_step(int N, int H, int d, int dv, int dtype, bool norm
 // ---- 2Mamba-E (SIMT) -----------------------------------------------------------------
 // 2Mamba-E forward on the tensor cores (tm2_tc_e.cu): bf16, d = dv = 64; cum = global running
 // sum of -softplus(a) (BH, T); o (BH, T, 64) and lse (BH, T) fp32.
-cudaError_t tc_e_fwd(const Problem& p, const void* q, const void* k, const void* v, const float* cum, float scale,
-                     float* o, float* lse, cudaStream_t s);
+cudaError_t tc_e_fwd(const Problem& p, const void* q, const void* k, const void* v, const float* cum,
+                     const float* cum_lo, float scale, float* o, float* lse, cudaStream_t s);
 cudaError_t simt_e_fwd(const Problem& p, const void* q, const void* k, const void* v,
-                       const float* cum, float scale, void* o, float* lse, cudaStream_t s);
+                       const float* cum, const float* cum_lo, float scale, void* o, float* lse, cudaStream_t s);
 // Dvec[bh][t] = dO_t . o_t
 cudaError_t launch_rowdot(const Problem& p, const void* o, const void* dO, float* Dvec,
                           cudaStream_t s);
 cudaError_t simt_e_bwd(const Problem& p, const void* q, const void* k, const void* v,
-                       const float* cum, const float* lse, const float* Dvec, const void* dO,
+                       const float* cum, const float* cum_lo, const float* lse, const float* Dvec, const void* dO,
                        float scale, void* dq, void* dk, void* dv, float* rowsum, float* colsum,
                        cudaStream_t s);
 

@@ -60,10 +60,11 @@ extern "C" int tm2e_forward_noalloc(const void* q, const void* k, const void* v,
     p.NC = (T + p.C - 1) / p.C;
     p.dtype = dtype;
     p.normalize = false;
-    // scratch: chunk-local running sums, chunk totals, global running sums
+    // scratch: chunk-local running sums, chunk totals, global running sums and their residuals
     const size_t off_g = round256(sizeof(float) * (size_t)p.BH() * p.Tp());
     const size_t off_cum = off_g + round256(sizeof(float) * (size_t)p.BH() * p.NC);
-    const size_t need = off_cum + round256(sizeof(float) * (size_t)p.BH() * T);
+    const size_t off_lo = off_cum + round256(sizeof(float) * (size_t)p.BH() * T);
+    const size_t need = off_lo + round256(sizeof(float) * (size_t)p.BH() * T);
     if (need > (size_t)TM2E_NOALLOC_SCRATCH_BYTES) return TM2_ERR_WORKSPACE;
 
     int dev = -1;
@@ -81,9 +82,10 @@ extern "C" int tm2e_forward_noalloc(const void* q, const void* k, const void* v,
     float* Aloc = reinterpret_cast<float*>((char*)base);
     float* g = reinterpret_cast<float*>((char*)base + off_g);
     float* cum = reinterpret_cast<float*>((char*)base + off_cum);
+    float* cum_lo = reinterpret_cast<float*>((char*)base + off_lo);
     cudaStream_t s = (cudaStream_t)stream;
     if (launch_decay(p, a, Aloc, g, s) != cudaSuccess) return TM2_ERR_CUDA;
-    if (launch_global_cumsum(p, Aloc, g, cum, s) != cudaSuccess) return TM2_ERR_CUDA;
-    if (simt_e_fwd(p, q, k, v, cum, scale, o, lse, s) != cudaSuccess) return TM2_ERR_CUDA;
+    if (launch_global_cumsum(p, Aloc, g, cum, cum_lo, s) != cudaSuccess) return TM2_ERR_CUDA;
+    if (simt_e_fwd(p, q, k, v, cum, cum_lo, scale, o, lse, s) != cudaSuccess) return TM2_ERR_CUDA;
     return TM2_OK;
 }

@@ -47,7 +47,7 @@ cudaError_t launch_decay(const Problem& p, const float* a, float* Aloc, float* g
 // grid BH, block 256.  Chunk offsets are summed in fp64 so that only the final
 // rounding to fp32 enters cum.
 __global__ void global_cumsum_kernel(const float* __restrict__ Aloc, const float* __restrict__ g,
-                                     float* __restrict__ cum, int T, int C, int NC) {
+                                     float* __restrict__ cum, float* __restrict__ cum_lo, int T, int C, int NC) {
     extern __shared__ double off[];   // NC doubles
     const long bh = blockIdx.x;
     if (threadIdx.x == 0) {
@@ -58,11 +58,15 @@ __global__ void global_cumsum_kernel(const float* __restrict__ Aloc, const float
         }
     }
     __syncthreads();
-    for (int t = threadIdx.x; t < T; t += blockDim.x)
-        cum[bh * T + t] = (float)(off[t / C] + (double)Aloc[bh * (long)NC * C + t]);
+    for (int t = threadIdx.x; t < T; t += blockDim.x) {
+        const double x = off[t / C] + (double)Aloc[bh * (long)NC * C + t];
+        const float hi = (float)x;
+        cum[bh * T + t] = hi;
+        if (cum_lo) cum_lo[bh * T + t] = (float)(x - (double)hi);
+    }
 }
 
-cudaError_t launch_global_cumsum(const Problem& p, const float* Aloc, const float* g, float* cum,
+cudaError_t launch_global_cumsum(const Problem& p, const float* Aloc, const float* g, float* cum, float* cum_lo,
                                  cudaStream_t s) {
     size_t smem = sizeof(double) * (size_t)p.NC;
     if (smem > 48 * 1024) {
@@ -70,7 +74,7 @@ cudaError_t launch_global_cumsum(const Problem& p, const float* Aloc, const floa
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    global_cumsum_kernel<<<(unsigned)p.BH(), 256, smem, s>>>(Aloc, g, cum, p.T, p.C, p.NC);
+    global_cumsum_kernel<<<(unsigned)p.BH(), 256, smem, s>>>(Aloc, g, cum, cum_lo, p.T, p.C, p.NC);
     return cudaGetLastError();
 }
 

@@ -46,7 +46,8 @@ constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, false, false);
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, 64, false, true);
 
 struct Args {
-    const float* cum;    // [BH][T] inclusive running sum of -softplus(a)
+    const float* cum;    // [BH][T] inclusive running sum of -softplus(a), fp32
+    const float* cum_lo; // [BH][T] its rounding residual
     float* o;            // [BH][T][64]
     float* lse;          // [BH][T]
     int* status;
@@ -171,7 +172,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_e_fwd_kernel(const __grid_const
         const long i = (long)qt * BQ + l;                // query
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         const float* cumh = a.cum + bh * a.T;
-        const float ci = i < a.T ? cumh[i] : 0.f;
+        const float* cuml = a.cum_lo + bh * a.T;
+        const float ci = i < a.T ? cumh[i] : 0.f, cil = i < a.T ? cuml[i] : 0.f;
         float m_used = -INFINITY, lsum = 0.f;
         int kg = 0;
         bool ok = true;
@@ -191,7 +193,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_e_fwd_kernel(const __grid_const
             for (int c = 0; c < 64; ++c) {
                 const long j = j0 + c;
                 const float cj = j < a.T ? __ldg(cumh + j) : 0.f;   // the same address in every lane
-                s[c] = (j <= i && j < a.T) ? fmaf(a.scale, s[c], ci - cj) : -INFINITY;
+                const float cjl = j < a.T ? __ldg(cuml + j) : 0.f;
+                s[c] = (j <= i && j < a.T) ? fmaf(a.scale, s[c], (ci - cj) + (cil - cjl)) : -INFINITY;
                 bmax = fmaxf(bmax, s[c]);
             }
             // row maximum over both key halves (the partner thread holds the other 64 keys), and
@@ -275,8 +278,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_e_fwd_kernel(const __grid_const
     if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
-cudaError_t tc_e_fwd(const Problem& p, const void* q, const void* k, const void* v, const float* cum, float scale,
-                     float* o, float* lse, cudaStream_t s) {
+cudaError_t tc_e_fwd(const Problem& p, const void* q, const void* k, const void* v, const float* cum,
+                     const float* cum_lo, float scale, float* o, float* lse, cudaStream_t s) {
     CUtensorMap tq, tk, tv;
     const uint64_t BH = (uint64_t)p.BH(), T = (uint64_t)p.T;
     if (!make_tmap_bf16_3d(&tq, q, BH, T, 64, BQ) || !make_tmap_bf16_3d(&tk, k, BH, T, 64, BK) ||
@@ -285,7 +288,7 @@ cudaError_t tc_e_fwd(const Problem& p, const void* q, const void* k, const void*
     int* status = tc_status_ptr();
     if (!status) return cudaErrorInvalidValue;
     const int NQ = (p.T + BQ - 1) / BQ;
-    Args a{cum, o, lse, status, p.T, NQ, scale};
+    Args a{cum, cum_lo, o, lse, status, p.T, NQ, scale};
     cudaError_t e = cudaFuncSetAttribute(tc_e_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)NQ, (unsigned)p.BH());

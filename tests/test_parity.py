@@ -353,8 +353,8 @@ def run_e(inp):
     return o, lse, dq, dk, dv, da
 
 
-@pytest.mark.parametrize("dtype,T", [("f32", 1), ("f32", 64), ("f32", 190), ("bf16", 1), ("bf16", 64),
-                                     ("bf16", 190), ("bf16", 1000)])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("T", [1, 64, 190, 1000])
 def test_e_small_ragged(dtype, T):
     d = 64
     inp = si.sequence_inputs(2, 2, T, d, d, dtype=dtype, qkv_std=1.0, seed=300 + T, with_dO=True)
