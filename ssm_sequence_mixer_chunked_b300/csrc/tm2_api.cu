@@ -408,7 +408,11 @@ int tm2e_backward(const void* q, const void* k, const void* v, const float* a, c
     TM2_RUN("decay_chunk", launch_decay(p, a, Aloc, g, s));
     TM2_RUN("global_cumsum", launch_global_cumsum(p, Aloc, g, cum, cum_lo, s));
     TM2_RUN("rowdot", launch_rowdot(p, o, dO, Dvec, s));
-    TM2_RUN("e_bwd", simt_e_bwd(p, q, k, v, cum, cum_lo, lse, Dvec, dO, scale, dq, dk, dv, rowsum, colsum, s));
+    if (p.dtype == TM2_BF16 && p.d == 64 && p.dv == 64)
+        TM2_RUN("tc_e_bwd", tc_e_bwd(p, q, k, v, cum, cum_lo, lse, Dvec, dO, scale, (float*)dq, (float*)dk,
+                                     (float*)dv, rowsum, colsum, s));
+    else
+        TM2_RUN("e_bwd", simt_e_bwd(p, q, k, v, cum, cum_lo, lse, Dvec, dO, scale, dq, dk, dv, rowsum, colsum, s));
     TM2_RUN("reverse_cumsum_da", launch_reverse_cumsum_da(p, a, rowsum, colsum, da, s));
     return TM2_OK;
 }

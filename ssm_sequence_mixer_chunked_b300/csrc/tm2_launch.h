@@ -107,7 +107,7 @@ cudaError_t launch_decode_step(int N, int H, int d, int dv, int dtype, bool norm
                                const void* q, const void* k, const void* v, const float* a,
                                float* S, float* z, void* o, float* Z, cudaStream_t s);
 
-// ---- 2Mamba-E (SIMT) -----------------------------------------------------------------
+// ---- 2Mamba-E ----------------------------------------------------------------------
 // 2Mamba-E forward on the tensor cores (tm2_tc_e.cu): bf16, d = dv = 64; cum = global running
 // sum of -softplus(a) (BH, T); o (BH, T, 64) and lse (BH, T) fp32.
 cudaError_t tc_e_fwd(const Problem& p, const void* q, const void* k, const void* v, const float* cum,
@@ -117,6 +117,11 @@ cudaError_t simt_e_fwd(const Problem& p, const void* q, const void* k, const voi
 // Dvec[bh][t] = dO_t . o_t
 cudaError_t launch_rowdot(const Problem& p, const void* o, const void* dO, float* Dvec,
                           cudaStream_t s);
+// 2Mamba-E backward on the tensor cores (tm2_tc_e_bwd.cu): bf16, d = dv = 64; dq, dk, dv fp32;
+// rowsum[t] = sum_j dx_tj and colsum[t] = sum_i dx_it (the A-mask gradient's two halves).
+cudaError_t tc_e_bwd(const Problem& p, const void* q, const void* k, const void* v, const float* cum,
+                     const float* cum_lo, const float* lse, const float* Dvec, const void* dO, float scale, float* dq,
+                     float* dk, float* dv, float* rowsum, float* colsum, cudaStream_t s);
 cudaError_t simt_e_bwd(const Problem& p, const void* q, const void* k, const void* v,
                        const float* cum, const float* cum_lo, const float* lse, const float* Dvec, const void* dO,
                        float scale, void* dq, void* dk, void* dv, float* rowsum, float* colsum,

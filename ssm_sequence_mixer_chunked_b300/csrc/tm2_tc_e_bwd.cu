@@ -1,0 +1,328 @@
+// tm2_tc_e_bwd.cu -- the 2Mamba-E backward on the tensor cores (bf16 inputs, d = dv = 64).
+//
+// "2Mamba2Furious", Sec. 6 (softmax attention with the softplus A-mask as logit bias):
+//   x_ij = scale q_i . k_j + cumA_i - cumA_j (j <= i),   P_ij = exp(x_ij - lse_i),
+//   dP_ij = dO_i . v_j,   dx_ij = P_ij (dP_ij - D_i),   D_i = dO_i . o_i,
+//   dq_i = scale sum_j dx_ij k_j,   dk_j = scale sum_i dx_ij q_i,   dv_j = sum_i P_ij dO_i,
+// and the A-mask gradient from the row sums sum_j dx_ij and column sums sum_i dx_ij
+// (dcumA_t = rowsum_t - colsum_t, accumulated from the end of the sequence elsewhere).
+//
+// Two kernels, one CTA per 128-token tile:
+//  * keys (tc_e_bwd_dkdv): per 128-query block at or after the key tile, s^T = K Q^T and
+//    dP^T = V dO^T (tcgen05.mma, M = N = 128) in tensor memory; the compute warps form P^T
+//    (bf16) and dx^T as bf16 hi + lo (its sums over queries cancel, so one bf16 rounding would
+//    cost the 2e-2 bar), written back over the scores; then dv += P^T dO and
+//    dk += (dx_hi + dx_lo)^T Q with Q, dO MN-major straight from their tiles.
+//  * queries (tc_e_bwd_dq): per 128-key block at or before the query tile, s = Q K^T and
+//    dP = dO V^T, dx hi + lo, dq += dx K.
+// The per-token scalars of the walked blocks (lse, D, and the running sums as fp32 value +
+// residual) are staged in shared memory each block.  Warps 0-7 compute (warp w: lane
+// quadrant w % 4, half w / 4 of the walked block's 128 tokens), warp 8 issues TMA, warp 9
+// the MMAs.  Every mbarrier wait is bounded (TM2_ERR_TIMEOUT on expiry).
+#include "tm2.h"
+#include "tm2_launch.h"
+#include "tm2_sm100.cuh"
+#include "tm2_tc.h"
+
+namespace tm2 {
+namespace tceb {
+
+constexpr int BT = 128;                      // tokens per tile / block
+constexpr int THREADS = 10 * 32;
+constexpr int WARP_TMA = 8, WARP_MMA = 9;
+constexpr int NS = 4;                        // stages of the walked blocks (two tiles each)
+constexpr int TILE = BT * 128;               // [128][64] bf16
+constexpr int STAGE = 2 * TILE;
+constexpr int SFIX = 0;                      // this CTA's two tiles (K, V or Q, dO)
+constexpr int SSTG = 2 * TILE;
+constexpr int SSC = SSTG + NS * STAGE;       // [2 buffers][4 arrays][128] per-token scalars
+constexpr int SRED = SSC + 2 * 4 * BT * 4;   // [2 halves][128]
+constexpr int SMEM_BYTES = SRED + 2 * BT * 4 + 1024;
+// tensor memory: scores at 0, dP at 128, accumulators at 256 (dk or dq) and 320 (dv); the
+// softmax step writes its operands where no other warp reads: dk/dv kernel P at 384, dx hi at
+// 448, dx lo over the writing warp's own dP columns (128 + 64 h .. +32); dq kernel dx hi at 384,
+// dx lo at 448.  Column c of an operand holds the walked tokens 2c, 2c+1 of that half.
+constexpr uint32_t TM_S = 0, TM_DP = 128, TM_ACC = 256, TM_ACC2 = 320, TM_O1 = 384, TM_O2 = 448;
+constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, false, false);
+constexpr uint32_t IDESC_MN = idesc_bf16_f32(128, 64, false, true);
+
+struct Args {
+    const float* cum;      // [BH][T] running sums of -softplus(a), fp32
+    const float* cum_lo;   // [BH][T] their rounding residuals
+    const float* lse;      // [BH][T]
+    const float* Dv;       // [BH][T] dO . o
+    float* g1;             // dk kernel: dk [BH][T][64]; dq kernel: dq
+    float* g2;             // dk kernel: dv [BH][T][64]; dq kernel: unused
+    float* sums;           // dk kernel: column sums [BH][T]; dq kernel: row sums
+    int* status;
+    int T, NT;
+    float scale;
+};
+
+}  // namespace tceb
+
+using namespace tceb;
+
+// kd = true: the key-tile kernel (dk, dv, column sums); false: the query-tile kernel (dq, row sums)
+template <bool kd>
+__global__ void __launch_bounds__(THREADS, 1) tc_e_bwd_kernel(const __grid_constant__ CUtensorMap tmA,
+                                                              const __grid_constant__ CUtensorMap tmB,
+                                                              const __grid_constant__ CUtensorMap tmC,
+                                                              const __grid_constant__ CUtensorMap tmD,
+                                                              const __grid_constant__ Args a) {
+    // kd: A = K, B = V (this CTA's tiles), C = Q, D = dO (walked)
+    // dq: A = Q, B = dO (this CTA's tiles), C = K, D = V (walked)
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_align1024(smem_raw);
+    __shared__ __align__(8) uint64_t bar_fix, bar_full[NS], bar_empty[NS], bar_sfull, bar_pfull, bar_tfree, bar_accfull,
+        bar_done;
+    __shared__ uint32_t tmem_base_s;
+    __shared__ volatile int abort_s;
+    __shared__ volatile int gflags[2];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tile = kd ? (int)blockIdx.x : a.NT - 1 - (int)blockIdx.x;   // heaviest tiles first
+    const long bh = blockIdx.y;
+    const int nblk = kd ? a.NT - tile : tile + 1;   // walked blocks: queries at or after / keys at or before
+    const int blk0 = kd ? tile : 0;
+    const uint32_t sb0 = smem_u32(smem);
+    float* sSc = reinterpret_cast<float*>(smem + SSC);
+    float* sRed = reinterpret_cast<float*>(smem + SRED);
+
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar_fix), 1);
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(smem_u32(&bar_full[i]), 1);
+            mbar_init(smem_u32(&bar_empty[i]), 1);
+        }
+        mbar_init(smem_u32(&bar_sfull), 1);
+        mbar_init(smem_u32(&bar_pfull), 256);
+        mbar_init(smem_u32(&bar_tfree), 1);
+        mbar_init(smem_u32(&bar_accfull), 1);
+        mbar_init(smem_u32(&bar_done), 1);
+        abort_s = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(&tmem_base_s), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_s;
+
+    if (warp == WARP_TMA) {
+        if (lane == 0) {
+            const uint32_t fb0 = smem_u32(&bar_fix);
+            mbar_arrive_expect_tx(fb0, 2 * TILE);
+            tma_load_3d(sb0 + SFIX, &tmA, fb0, 0, tile * BT, (int)bh);
+            tma_load_3d(sb0 + SFIX + TILE, &tmB, fb0, 0, tile * BT, (int)bh);
+            int issued = 0;
+            for (int c = 0; c < nblk && !abort_s; ++c) {
+                const int st = c % NS;
+                if (c >= NS && !mbar_wait(smem_u32(&bar_empty[st]), (uint32_t)((c / NS) - 1) & 1, a.status)) {
+                    abort_s = 1;
+                    break;
+                }
+                const uint32_t fb = smem_u32(&bar_full[st]), dst = sb0 + SSTG + st * STAGE;
+                mbar_arrive_expect_tx(fb, STAGE);
+                tma_load_3d(dst, &tmC, fb, 0, (blk0 + c) * BT, (int)bh);
+                tma_load_3d(dst + TILE, &tmD, fb, 0, (blk0 + c) * BT, (int)bh);
+                issued = c + 1;
+            }
+            mbar_wait(fb0, 0, a.status);
+            for (int c = issued - 1; c >= 0 && c >= issued - NS; --c)
+                mbar_wait(smem_u32(&bar_full[c % NS]), (uint32_t)(c / NS) & 1, a.status);
+        }
+    } else if (warp == WARP_MMA) {
+        if (lane == 0) {
+            bool ok = mbar_wait(smem_u32(&bar_fix), 0, a.status);
+            tc_fence_after();
+            for (int c = 0; c < nblk && ok; ++c) {
+                const int st = c % NS;
+                if (abort_s) { ok = false; break; }
+                if (!(ok = mbar_wait(smem_u32(&bar_full[st]), (uint32_t)(c / NS) & 1, a.status))) break;
+                if (c > 0 && !(ok = mbar_wait(smem_u32(&bar_tfree), (uint32_t)(c - 1) & 1, a.status))) break;
+                tc_fence_after();
+                const uint32_t sc = sb0 + SSTG + st * STAGE, sd = sc + TILE;
+                // scores and dP: (fixed tile) x (walked tile)^T, M = N = 128, K = 64
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    umma_bf16(tmem + TM_S, sdesc_sw128(sb0 + SFIX + kk * 32), sdesc_sw128(sc + kk * 32), IDESC_S, kk > 0);
+                    umma_bf16(tmem + TM_DP, sdesc_sw128(sb0 + SFIX + TILE + kk * 32), sdesc_sw128(sd + kk * 32), IDESC_S,
+                              kk > 0);
+                }
+                umma_commit(smem_u32(&bar_sfull));
+                if (!(ok = mbar_wait(smem_u32(&bar_pfull), (uint32_t)c & 1, a.status))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < BT / 16; ++kk) {
+                    const uint32_t acc0 = (c > 0 || kk > 0) ? 1u : 0u;
+                    if (kd) {   // dv += P^T dO, dk += (dx hi + lo)^T Q
+                        const uint64_t qd = sdesc_sw128_ex(sc + kk * 2048, 8192, 1024);
+                        const uint64_t dd = sdesc_sw128_ex(sd + kk * 2048, 8192, 1024);
+                        const uint32_t lo_col = TM_DP + (kk >> 2) * 64 + (kk & 3) * 8;   // half kk / 4's dP columns
+                        umma_bf16_ts(tmem + TM_ACC2, tmem + TM_O1 + kk * 8, dd, IDESC_MN, acc0);
+                        umma_bf16_ts(tmem + TM_ACC, tmem + TM_O2 + kk * 8, qd, IDESC_MN, acc0);
+                        umma_bf16_ts(tmem + TM_ACC, tmem + lo_col, qd, IDESC_MN, 1u);
+                    } else {    // dq += (dx hi + lo) K
+                        const uint64_t kdsc = sdesc_sw128_ex(sc + kk * 2048, 8192, 1024);
+                        umma_bf16_ts(tmem + TM_ACC, tmem + TM_O1 + kk * 8, kdsc, IDESC_MN, acc0);
+                        umma_bf16_ts(tmem + TM_ACC, tmem + TM_O2 + kk * 8, kdsc, IDESC_MN, 1u);
+                    }
+                }
+                umma_commit(smem_u32(&bar_tfree));
+                umma_commit(smem_u32(&bar_empty[st]));
+            }
+            if (ok) umma_commit(smem_u32(&bar_accfull));
+            else abort_s = 1;
+            umma_commit(smem_u32(&bar_done));
+            mbar_wait(smem_u32(&bar_done), 0, a.status);
+        }
+    } else {
+        // ---------------------------------------------------------------- compute warps
+        const int quad = warp & 3, h = warp >> 2;
+        const int l = quad * 32 + lane;                  // row of this CTA's tile
+        const long r = (long)tile * BT + l;              // this thread's token (key for kd, query for dq)
+        const bool rin = r < a.T;
+        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        const long base = bh * a.T;
+        // scalars of this thread's own token
+        const float cr = rin ? a.cum[base + r] : 0.f, crl = rin ? a.cum_lo[base + r] : 0.f;
+        const float lse_r = (!kd && rin) ? a.lse[base + r] : 0.f, D_r = (!kd && rin) ? a.Dv[base + r] : 0.f;
+        float sum = 0.f;
+        int kg = 0;
+        bool ok = true;
+        for (int c = 0; c < nblk && ok; ++c) {
+            const int x = c & 1;
+            const long t0 = (long)(blk0 + c) * BT;
+            // the walked block's per-token scalars into buffer x (2 or 4 arrays of 128)
+            float* sc = sSc + x * 4 * BT;
+            for (int e = threadIdx.x; e < (kd ? 4 : 2) * BT; e += 256) {
+                const int arr = e >> 7, tt = e & 127;
+                const long t = t0 + tt;
+                float val = 0.f;
+                if (t < a.T) {
+                    if (kd) val = arr == 0 ? a.lse[base + t] : arr == 1 ? a.Dv[base + t] : arr == 2 ? a.cum[base + t] : a.cum_lo[base + t];
+                    else val = arr == 0 ? a.cum[base + t] : a.cum_lo[base + t];
+                }
+                sc[arr * BT + tt] = val;
+            }
+            // (the group wait's barrier also publishes the staged scalars to every thread)
+            if (!(ok = group_wait(smem_u32(&bar_sfull), (uint32_t)c & 1, a.status, warp == 0, 1, 256, gflags, kg,
+                                  &abort_s)))
+                break;
+            // 16 walked tokens at a time: read scores and dP, write P / dx hi / dx lo (the outputs
+            // go to columns only this warp reads, so no barrier is needed between reads and writes)
+#pragma unroll 1
+            for (int q4 = 0; q4 < 4; ++q4) {
+                float s[16], dp[16];
+                tmem_ld16(tmem + lane_base + TM_S + h * 64 + q4 * 16, s);
+                tmem_ld16(tmem + lane_base + TM_DP + h * 64 + q4 * 16, dp);
+                uint32_t pp[8], dh[8], dl[8];
+#pragma unroll
+                for (int c2 = 0; c2 < 8; ++c2) {
+                    float pv[2], dxh[2], dxl[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int cc = 2 * c2 + u, tt = h * 64 + q4 * 16 + cc;
+                        const long t = t0 + tt;          // the walked token
+                        float P = 0.f, dx = 0.f;
+                        if (kd) {   // row r = key j, t = query i
+                            if (t >= r && t < a.T) {
+                                const float bias = (sc[2 * BT + tt] - cr) + (sc[3 * BT + tt] - crl);
+                                P = __expf(fmaf(a.scale, s[cc], bias) - sc[tt]);
+                                dx = P * (dp[cc] - sc[BT + tt]);
+                            }
+                        } else {    // row r = query i, t = key j
+                            if (t <= r && rin) {
+                                const float bias = (cr - sc[tt]) + (crl - sc[BT + tt]);
+                                P = __expf(fmaf(a.scale, s[cc], bias) - lse_r);
+                                dx = P * (dp[cc] - D_r);
+                            }
+                        }
+                        sum += dx;
+                        pv[u] = P;
+                        dxh[u] = __bfloat162float(__float2bfloat16_rn(dx));
+                        dxl[u] = dx - dxh[u];
+                    }
+                    pp[c2] = pack_bf16x2(pv[0], pv[1]);
+                    dh[c2] = pack_bf16x2(dxh[0], dxh[1]);
+                    dl[c2] = pack_bf16x2(dxl[0], dxl[1]);
+                }
+                const uint32_t ocol = h * 32 + q4 * 8;   // operand column of these 16 tokens
+                if (kd) {
+                    tmem_st8(tmem + lane_base + TM_O1 + ocol, pp);
+                    tmem_st8(tmem + lane_base + TM_O2 + ocol, dh);
+                    tmem_st8(tmem + lane_base + TM_DP + h * 64 + q4 * 8, dl);   // own dP columns, already read
+                } else {
+                    tmem_st8(tmem + lane_base + TM_O1 + ocol, dh);
+                    tmem_st8(tmem + lane_base + TM_O2 + ocol, dl);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bar_pfull));
+        }
+        // ---- gradients of this tile's tokens; the two halves' sums combined
+        if (ok) sRed[h * BT + l] = sum;
+        named_bar_sync(2, 256);
+        if (ok && !abort_s && (ok = mbar_wait(smem_u32(&bar_accfull), 0, a.status))) {
+            tc_fence_after();
+            const float tot = sum + sRed[(1 - h) * BT + l];
+            float g[32];
+            tmem_ld32(tmem + lane_base + TM_ACC + h * 32, g);
+            if (rin) {
+                float4* d1 = reinterpret_cast<float4*>(a.g1 + (base + r) * 64 + h * 32);
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    d1[u] = make_float4(a.scale * g[4 * u], a.scale * g[4 * u + 1], a.scale * g[4 * u + 2],
+                                        a.scale * g[4 * u + 3]);
+                if (h == 0) a.sums[base + r] = tot;
+            }
+            if (kd) {
+                tmem_ld32(tmem + lane_base + TM_ACC2 + h * 32, g);
+                if (rin) {
+                    float4* d2 = reinterpret_cast<float4*>(a.g2 + (base + r) * 64 + h * 32);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) d2[u] = make_float4(g[4 * u], g[4 * u + 1], g[4 * u + 2], g[4 * u + 3]);
+                }
+            }
+        }
+        if (!ok) abort_s = 1;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+cudaError_t tc_e_bwd(const Problem& p, const void* q, const void* k, const void* v, const float* cum,
+                     const float* cum_lo, const float* lse, const float* Dvec, const void* dO, float scale, float* dq,
+                     float* dk, float* dv, float* rowsum, float* colsum, cudaStream_t s) {
+    CUtensorMap tq, tk, tv, td;
+    const uint64_t BH = (uint64_t)p.BH(), T = (uint64_t)p.T;
+    if (!make_tmap_bf16_3d(&tq, q, BH, T, 64, BT) || !make_tmap_bf16_3d(&tk, k, BH, T, 64, BT) ||
+        !make_tmap_bf16_3d(&tv, v, BH, T, 64, BT) || !make_tmap_bf16_3d(&td, dO, BH, T, 64, BT))
+        return cudaErrorInvalidValue;
+    int* status = tc_status_ptr();
+    if (!status) return cudaErrorInvalidValue;
+    const int NT = (p.T + BT - 1) / BT;
+    dim3 grid((unsigned)NT, (unsigned)p.BH());
+    {
+        Args a{cum, cum_lo, lse, Dvec, dk, dv, colsum, status, p.T, NT, scale};
+        cudaError_t e = cudaFuncSetAttribute(tc_e_bwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        tc_e_bwd_kernel<true><<<grid, THREADS, SMEM_BYTES, s>>>(tk, tv, tq, td, a);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    {
+        Args a{cum, cum_lo, lse, Dvec, dq, nullptr, rowsum, status, p.T, NT, scale};
+        cudaError_t e = cudaFuncSetAttribute(tc_e_bwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        tc_e_bwd_kernel<false><<<grid, THREADS, SMEM_BYTES, s>>>(tq, td, tk, tv, a);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace tm2
