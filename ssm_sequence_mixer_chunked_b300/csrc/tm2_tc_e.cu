@@ -16,6 +16,9 @@
 // well inside bf16), which makes rescales rare.  The next block's QK^T overlaps this block's
 // softmax, and its softmax overlaps this block's PV.  The row sums add the bf16-rounded P
 // that the MMA uses, so o = O / l is exactly normalised for those weights.
+// Logits are kept in log2 units (x log2 e); the decay terms are taken relative to the running
+// sum at the tile's first query, so the fp32 differences stay small, and each block's key
+// terms are staged once in shared memory.  Only the diagonal block is masked.
 // Warps 0-7 compute (warp w: lane quadrant w % 4, key half w / 4), warp 8 issues TMA, warp 9
 // the MMAs.  Every mbarrier wait is bounded (TM2_ERR_TIMEOUT on expiry).
 #include "tm2.h"
@@ -37,11 +40,13 @@ constexpr int SSTG = TILE;                   // NS stages after the Q tile
 constexpr int SMAX = SSTG + NS * STAGE;      // [2 buffers][2 halves][128] row maxima
 constexpr int SSUM = SMAX + 2 * 2 * BQ * 4;  // [2 halves][128] row sums
 constexpr int SFLAG = SSUM + 2 * BQ * 4;     // [2 buffers][8 warps] rescale requests
-constexpr int SMEM_BYTES = SFLAG + 64 + 1024;
+constexpr int SKW = SFLAG + 64;              // [2 buffers][128] decay terms of the block's keys
+constexpr int SMEM_BYTES = SKW + 2 * BK * 4 + 1024;
 constexpr uint32_t TM_S = 0;                 // score buffer x at 128 x
 constexpr uint32_t TM_P = 256;               // P buffer x at 256 + 64 x (bf16 pairs)
 constexpr uint32_t TM_O = 384;
-constexpr float LAZY = 8.f;                  // rescale only when the maximum grows by more than this
+constexpr float LOG2E = 1.4426950408889634f, LN2 = 0.6931471805599453f;
+constexpr float LAZY = 8.f * LOG2E;          // rescale only when the maximum grows by more than e^8
 constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, false, false);
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, 64, false, true);
 
@@ -51,7 +56,7 @@ struct Args {
     float* o;            // [BH][T][64]
     float* lse;          // [BH][T]
     int* status;
-    int T, NQ;
+    int T, NQ, BH;
     float scale;
 };
 
@@ -71,8 +76,11 @@ __global__ void __launch_bounds__(THREADS, 1) tc_e_fwd_kernel(const __grid_const
     __shared__ volatile int abort_s;
     __shared__ volatile int gflags[2];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int qt = a.NQ - 1 - (int)blockIdx.x;   // longest tiles first
-    const long bh = blockIdx.y;
+    // longest tiles of every head first: linear block index -> (rank of the tile's length, head)
+    const long lin = (long)blockIdx.y * gridDim.x + blockIdx.x;
+    const int rank = (int)(lin / a.BH);
+    const long bh = lin - (long)rank * a.BH;
+    const int qt = a.NQ - 1 - rank;
     const int nkb = qt + 1;                      // key blocks at or before the tile
     const uint32_t sb0 = smem_u32(smem);
     float* sMax = reinterpret_cast<float*>(smem + SMAX);
@@ -173,12 +181,21 @@ __global__ void __launch_bounds__(THREADS, 1) tc_e_fwd_kernel(const __grid_const
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         const float* cumh = a.cum + bh * a.T;
         const float* cuml = a.cum_lo + bh * a.T;
-        const float ci = i < a.T ? cumh[i] : 0.f, cil = i < a.T ? cuml[i] : 0.f;
+        // decay terms relative to the running sum at the tile's first query, in log2 units
+        const float ref = cumh[(long)qt * BQ], reflo = cuml[(long)qt * BQ];
+        const float crr = i < a.T ? ((cumh[i] - ref) + (cuml[i] - reflo)) * LOG2E : 0.f;
+        const float sl2 = a.scale * LOG2E;
+        float* sKW = reinterpret_cast<float*>(smem + SKW);
         float m_used = -INFINITY, lsum = 0.f;
         int kg = 0;
         bool ok = true;
         for (int b = 0; b < nkb && ok; ++b) {
             const int x = b & 1;
+            // this block's key terms into buffer x (published by the group wait's barrier)
+            if (threadIdx.x < BK) {
+                const long j = (long)(qt - b) * BK + threadIdx.x;
+                sKW[x * BK + threadIdx.x] = j < a.T ? ((cumh[j] - ref) + (cuml[j] - reflo)) * LOG2E : 0.f;
+            }
             if (!(ok = group_wait(smem_u32(&bar_sfull[x]), (uint32_t)(b >> 1) & 1, a.status, warp == 0, 1, 256, gflags,
                                   kg, &abort_s)))
                 break;
@@ -187,15 +204,32 @@ __global__ void __launch_bounds__(THREADS, 1) tc_e_fwd_kernel(const __grid_const
             tmem_ld32(tmem + lane_base + TM_S + x * 128 + h * 64 + 32, s + 32);
             tc_fence_before();
             mbar_arrive(smem_u32(&bar_sfree[x]));        // the score buffer may take block b+2
-            const long j0 = (long)(qt - b) * BK + h * 64;   // keys of this block (newest first)
+            const float4* kw4 = reinterpret_cast<const float4*>(sKW + x * BK + h * 64);
             float bmax = -INFINITY;
+            if (b == 0) {   // the diagonal block: key h 64 + c is visible to row l when h 64 + c <= l
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                const long j = j0 + c;
-                const float cj = j < a.T ? __ldg(cumh + j) : 0.f;   // the same address in every lane
-                const float cjl = j < a.T ? __ldg(cuml + j) : 0.f;
-                s[c] = (j <= i && j < a.T) ? fmaf(a.scale, s[c], (ci - cj) + (cil - cjl)) : -INFINITY;
-                bmax = fmaxf(bmax, s[c]);
+                for (int u = 0; u < 16; ++u) {
+                    const float4 w = kw4[u];
+                    const float wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int c = 4 * u + e;
+                        s[c] = h * 64 + c <= l ? fmaf(sl2, s[c], crr - wv[e]) : -INFINITY;
+                        bmax = fmaxf(bmax, s[c]);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    const float4 w = kw4[u];
+                    const float wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int c = 4 * u + e;
+                        s[c] = fmaf(sl2, s[c], crr - wv[e]);
+                        bmax = fmaxf(bmax, s[c]);
+                    }
+                }
             }
             // row maximum over both key halves (the partner thread holds the other 64 keys), and
             // whether any row needs a rescale (one decision for the whole CTA, so that every wait
@@ -215,7 +249,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_e_fwd_kernel(const __grid_const
 #pragma unroll
             for (int w = 0; w < 8; ++w) any |= sFlag[x * 8 + w];
             if (any) {
-                const float fac = !need ? 1.f : (m_used == -INFINITY ? 0.f : __expf(m_used - bmax));
+                const float fac = !need ? 1.f : (m_used == -INFINITY ? 0.f : exp2f(m_used - bmax));
                 if (b > 0) {             // O holds blocks < b once the previous product is done
                     if (!(ok = group_wait(smem_u32(&bar_pfree[(b - 1) & 1]), (uint32_t)((b - 1) >> 1) & 1, a.status,
                                           warp == 0, 1, 256, gflags, kg, &abort_s)))
@@ -239,8 +273,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_e_fwd_kernel(const __grid_const
             uint32_t pk[32];
 #pragma unroll
             for (int c2 = 0; c2 < 32; ++c2) {
-                float p0 = m_used == -INFINITY ? 0.f : __expf(s[2 * c2] - m_used);
-                float p1 = m_used == -INFINITY ? 0.f : __expf(s[2 * c2 + 1] - m_used);
+                float p0 = m_used == -INFINITY ? 0.f : exp2f(s[2 * c2] - m_used);
+                float p1 = m_used == -INFINITY ? 0.f : exp2f(s[2 * c2 + 1] - m_used);
                 const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
                 const float2 r2 = __bfloat1622float2(b2);
                 lsum += r2.x + r2.y;
@@ -268,7 +302,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_e_fwd_kernel(const __grid_const
 #pragma unroll
                 for (int u = 0; u < 8; ++u)
                     dst[u] = make_float4(ov[4 * u] * inv, ov[4 * u + 1] * inv, ov[4 * u + 2] * inv, ov[4 * u + 3] * inv);
-                if (h == 0) a.lse[bh * a.T + i] = m_used + __logf(lt);
+                if (h == 0) a.lse[bh * a.T + i] = m_used * LN2 + __logf(lt);
             }
         }
         if (!ok) abort_s = 1;
@@ -288,7 +322,7 @@ cudaError_t tc_e_fwd(const Problem& p, const void* q, const void* k, const void*
     int* status = tc_status_ptr();
     if (!status) return cudaErrorInvalidValue;
     const int NQ = (p.T + BQ - 1) / BQ;
-    Args a{cum, cum_lo, o, lse, status, p.T, NQ, scale};
+    Args a{cum, cum_lo, o, lse, status, p.T, NQ, (int)p.BH(), scale};
     cudaError_t e = cudaFuncSetAttribute(tc_e_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)NQ, (unsigned)p.BH());

@@ -55,13 +55,44 @@ struct Args {
     float* g2;             // dk kernel: dv [BH][T][64]; dq kernel: unused
     float* sums;           // dk kernel: column sums [BH][T]; dq kernel: row sums
     int* status;
-    int T, NT;
+    int T, NT, BH;
     float scale;
 };
 
 }  // namespace tceb
 
 using namespace tceb;
+
+// The softmax-gradient step for 16 walked tokens of one row (tokens tt0 .. tt0 + 15 of the
+// block): scores s, dP dp, the staged per-token terms W (log2 units) and, for the key-tile
+// kernel, Dq (dO . o of each walked query).  P = 2^(scale log2e s + bias) and
+// dx = P (dP - D) with bias = W - crr (key tiles: W holds the query's running sum minus its
+// lse) or crr - W (query tiles: crr holds the query's, W the key's).  Masked blocks zero the
+// entries outside lo <= tt < hi.  Writes P, dx hi, dx lo as packed bf16 pairs.
+template <bool kd, bool masked>
+__device__ __forceinline__ void softmax_grad16(const float* s, const float* dp, const float* W, const float* Dq,
+                                               float crr, float Dr, float sl2, int tt0, int lo, int hi, float& sum,
+                                               uint32_t* pp, uint32_t* dh, uint32_t* dl) {
+#pragma unroll
+    for (int c2 = 0; c2 < 8; ++c2) {
+        float pv[2], dx[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int cc = 2 * c2 + u;
+            const float bias = kd ? W[cc] - crr : crr - W[cc];
+            float P = exp2f(fmaf(sl2, s[cc], bias));
+            if (masked && !(tt0 + cc >= lo && tt0 + cc < hi)) P = 0.f;
+            const float g = P * (dp[cc] - (kd ? Dq[cc] : Dr));
+            sum += g;
+            pv[u] = P;
+            dx[u] = g;
+        }
+        pp[c2] = pack_bf16x2(pv[0], pv[1]);
+        const uint32_t h2 = pack_bf16x2(dx[0], dx[1]);
+        dh[c2] = h2;
+        dl[c2] = pack_bf16x2(dx[0] - __uint_as_float(h2 << 16), dx[1] - __uint_as_float(h2 & 0xffff0000u));
+    }
+}
 
 // kd = true: the key-tile kernel (dk, dv, column sums); false: the query-tile kernel (dq, row sums)
 template <bool kd>
@@ -80,8 +111,11 @@ __global__ void __launch_bounds__(THREADS, 1) tc_e_bwd_kernel(const __grid_const
     __shared__ volatile int abort_s;
     __shared__ volatile int gflags[2];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tile = kd ? (int)blockIdx.x : a.NT - 1 - (int)blockIdx.x;   // heaviest tiles first
-    const long bh = blockIdx.y;
+    // heaviest tiles of every head first: linear block index -> (rank of the tile's length, head)
+    const long lin = (long)blockIdx.y * gridDim.x + blockIdx.x;
+    const int rank = (int)(lin / a.BH);
+    const long bh = lin - (long)rank * a.BH;
+    const int tile = kd ? rank : a.NT - 1 - rank;
     const int nblk = kd ? a.NT - tile : tile + 1;   // walked blocks: queries at or after / keys at or before
     const int blk0 = kd ? tile : 0;
     const uint32_t sb0 = smem_u32(smem);
@@ -187,28 +221,45 @@ __global__ void __launch_bounds__(THREADS, 1) tc_e_bwd_kernel(const __grid_const
         const bool rin = r < a.T;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         const long base = bh * a.T;
-        // scalars of this thread's own token
-        const float cr = rin ? a.cum[base + r] : 0.f, crl = rin ? a.cum_lo[base + r] : 0.f;
-        const float lse_r = (!kd && rin) ? a.lse[base + r] : 0.f, D_r = (!kd && rin) ? a.Dv[base + r] : 0.f;
+        // Decay biases in log2 units, offset by the running sum at this tile's first token so
+        // the fp32 differences stay small: crr is this thread's own term (key tiles: its key's
+        // offset sum; query tiles: its query's offset sum minus lse), the staged W the walked
+        // tokens' (key tiles: offset sum minus lse of each query; query tiles: offset sum of
+        // each key).
+        constexpr float LOG2E = 1.4426950408889634f;
+        const long t_ref = base + (long)tile * BT;
+        const float ref = a.cum[t_ref], reflo = a.cum_lo[t_ref];
+        float crr = 0.f, Dr = 0.f;
+        if (rin) {
+            const float off = (a.cum[base + r] - ref) + (a.cum_lo[base + r] - reflo);
+            crr = kd ? off * LOG2E : (off - a.lse[base + r]) * LOG2E;
+            if (!kd) Dr = a.Dv[base + r];
+        }
+        const float sl2 = a.scale * LOG2E;
         float sum = 0.f;
         int kg = 0;
         bool ok = true;
         for (int c = 0; c < nblk && ok; ++c) {
             const int x = c & 1;
             const long t0 = (long)(blk0 + c) * BT;
-            // the walked block's per-token scalars into buffer x (2 or 4 arrays of 128)
+            // the walked block's per-token terms into buffer x: W at [0, 128), D at [128, 256)
             float* sc = sSc + x * 4 * BT;
-            for (int e = threadIdx.x; e < (kd ? 4 : 2) * BT; e += 256) {
+            for (int e = threadIdx.x; e < (kd ? 2 : 1) * BT; e += 256) {
                 const int arr = e >> 7, tt = e & 127;
                 const long t = t0 + tt;
                 float val = 0.f;
                 if (t < a.T) {
-                    if (kd) val = arr == 0 ? a.lse[base + t] : arr == 1 ? a.Dv[base + t] : arr == 2 ? a.cum[base + t] : a.cum_lo[base + t];
-                    else val = arr == 0 ? a.cum[base + t] : a.cum_lo[base + t];
+                    const float off = (a.cum[base + t] - ref) + (a.cum_lo[base + t] - reflo);
+                    if (arr == 1) val = a.Dv[base + t];
+                    else val = kd ? (off - a.lse[base + t]) * LOG2E : off * LOG2E;
                 }
                 sc[arr * BT + tt] = val;
             }
-            // (the group wait's barrier also publishes the staged scalars to every thread)
+            // masks only on the diagonal block and on a block that runs past the sequence end
+            const bool masked = kd ? (c == 0 || t0 + BT > a.T) : (c == nblk - 1);
+            const int lo = kd ? (int)(r - t0) : 0;
+            const int hi = kd ? (int)min((long)BT, (long)a.T - t0) : (int)(r - t0) + 1;
+            // (the group wait's barrier also publishes the staged terms to every thread)
             if (!(ok = group_wait(smem_u32(&bar_sfull), (uint32_t)c & 1, a.status, warp == 0, 1, 256, gflags, kg,
                                   &abort_s)))
                 break;
@@ -216,40 +267,24 @@ __global__ void __launch_bounds__(THREADS, 1) tc_e_bwd_kernel(const __grid_const
             // go to columns only this warp reads, so no barrier is needed between reads and writes)
 #pragma unroll 1
             for (int q4 = 0; q4 < 4; ++q4) {
-                float s[16], dp[16];
-                tmem_ld16(tmem + lane_base + TM_S + h * 64 + q4 * 16, s);
-                tmem_ld16(tmem + lane_base + TM_DP + h * 64 + q4 * 16, dp);
-                uint32_t pp[8], dh[8], dl[8];
+                const int tt0 = h * 64 + q4 * 16;
+                float s[16], dp[16], W[16], Dq[16];
+                tmem_ld16(tmem + lane_base + TM_S + tt0, s);
+                tmem_ld16(tmem + lane_base + TM_DP + tt0, dp);
 #pragma unroll
-                for (int c2 = 0; c2 < 8; ++c2) {
-                    float pv[2], dxh[2], dxl[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int cc = 2 * c2 + u, tt = h * 64 + q4 * 16 + cc;
-                        const long t = t0 + tt;          // the walked token
-                        float P = 0.f, dx = 0.f;
-                        if (kd) {   // row r = key j, t = query i
-                            if (t >= r && t < a.T) {
-                                const float bias = (sc[2 * BT + tt] - cr) + (sc[3 * BT + tt] - crl);
-                                P = __expf(fmaf(a.scale, s[cc], bias) - sc[tt]);
-                                dx = P * (dp[cc] - sc[BT + tt]);
-                            }
-                        } else {    // row r = query i, t = key j
-                            if (t <= r && rin) {
-                                const float bias = (cr - sc[tt]) + (crl - sc[BT + tt]);
-                                P = __expf(fmaf(a.scale, s[cc], bias) - lse_r);
-                                dx = P * (dp[cc] - D_r);
-                            }
-                        }
-                        sum += dx;
-                        pv[u] = P;
-                        dxh[u] = __bfloat162float(__float2bfloat16_rn(dx));
-                        dxl[u] = dx - dxh[u];
+                for (int u = 0; u < 4; ++u) {
+                    const float4 w4 = reinterpret_cast<const float4*>(sc + tt0)[u];
+                    W[4 * u] = w4.x, W[4 * u + 1] = w4.y, W[4 * u + 2] = w4.z, W[4 * u + 3] = w4.w;
+                    if (kd) {
+                        const float4 d4 = reinterpret_cast<const float4*>(sc + BT + tt0)[u];
+                        Dq[4 * u] = d4.x, Dq[4 * u + 1] = d4.y, Dq[4 * u + 2] = d4.z, Dq[4 * u + 3] = d4.w;
                     }
-                    pp[c2] = pack_bf16x2(pv[0], pv[1]);
-                    dh[c2] = pack_bf16x2(dxh[0], dxh[1]);
-                    dl[c2] = pack_bf16x2(dxl[0], dxl[1]);
                 }
+                uint32_t pp[8], dh[8], dl[8];
+                if (masked)
+                    softmax_grad16<kd, true>(s, dp, W, Dq, crr, Dr, sl2, tt0, lo, hi, sum, pp, dh, dl);
+                else
+                    softmax_grad16<kd, false>(s, dp, W, Dq, crr, Dr, sl2, tt0, lo, hi, sum, pp, dh, dl);
                 const uint32_t ocol = h * 32 + q4 * 8;   // operand column of these 16 tokens
                 if (kd) {
                     tmem_st8(tmem + lane_base + TM_O1 + ocol, pp);
@@ -309,7 +344,7 @@ cudaError_t tc_e_bwd(const Problem& p, const void* q, const void* k, const void*
     const int NT = (p.T + BT - 1) / BT;
     dim3 grid((unsigned)NT, (unsigned)p.BH());
     {
-        Args a{cum, cum_lo, lse, Dvec, dk, dv, colsum, status, p.T, NT, scale};
+        Args a{cum, cum_lo, lse, Dvec, dk, dv, colsum, status, p.T, NT, (int)p.BH(), scale};
         cudaError_t e = cudaFuncSetAttribute(tc_e_bwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess) return e;
         tc_e_bwd_kernel<true><<<grid, THREADS, SMEM_BYTES, s>>>(tk, tv, tq, td, a);
@@ -317,7 +352,7 @@ cudaError_t tc_e_bwd(const Problem& p, const void* q, const void* k, const void*
         if (e != cudaSuccess) return e;
     }
     {
-        Args a{cum, cum_lo, lse, Dvec, dq, nullptr, rowsum, status, p.T, NT, scale};
+        Args a{cum, cum_lo, lse, Dvec, dq, nullptr, rowsum, status, p.T, NT, (int)p.BH(), scale};
         cudaError_t e = cudaFuncSetAttribute(tc_e_bwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess) return e;
         tc_e_bwd_kernel<false><<<grid, THREADS, SMEM_BYTES, s>>>(tq, td, tk, tv, a);
