@@ -9,13 +9,16 @@
 //     dS_{c-1} = exp(g_c) dS_c + sum_{i in c} exp(A_i) zeta_i (q_i (x) q_i) [dO_i, ucol_i]^T,
 // with zeta_i = 1/Z_i and ucol_i = -dO_i . o_i (normalised) or zeta = 1, ucol = 0.
 //
-// One CTA owns the 256 state rows r = m*64 + n with m in {4Q .. 4Q+3} of one (b, h) and
-// walks every chunk in order.  The chunk's contribution is computed transposed,
+// One CTA owns NR (128 or 256) state rows r = m*64 + n with m in {MP Q .. MP Q + MP - 1}
+// (MP = NR / 64) of one (b, h) and walks every chunk in order.  The chunk's contribution is
+// computed transposed,
 //     H^T[col][(m,n)] = sum_j (w_j val_j[col]) key_j[m] key_j[n],
 // as tcgen05.mma with M = 128 (the 64 value columns, the normaliser column and zero rows),
-// N = 256 (the CTA's state rows) and K = tokens: a tensor-core instruction costs about the
-// same for any N up to 256, so putting the 256 state rows on N takes 8 instructions per
-// 64-token stage where 128 state rows on M and the 80 columns on N took 16.
+// N = NR (the CTA's state rows) and K = tokens: 8 instructions per 64-token stage.  NR = 128
+// would give 32 CTAs per head (1024 at B = 2, H = 16: 6.9 waves on 148 SMs where NR = 256
+// gives 3.5, i.e. 4 with a half-empty last one) and halve each stage's operand building, but
+// a stage still costs its 8 instructions (0.85 us at N = 128 against 1.2 us at N = 256), so
+// the walk took 0.76 ms against 0.62 ms at B = 2, H = 16, T = 8192: NR = 256 is used.
 //
 // Precision.  Tokens whose query is nearly orthogonal to the state read it out with heavy
 // cancellation, so the state must carry more than one 16-bit rounding (a single fp16
@@ -56,14 +59,15 @@ constexpr int KS = 64;          // tokens per stage
 constexpr int SPC = C / KS;     // stages per chunk
 constexpr int NSLOT = 5;        // ring slots, one stage each
 constexpr int SLOT = TC_OPS_ROWS * 128;   // [Kt 64 rows | value^T 64 rows | normaliser row | 7 zero rows]
-constexpr int BBUF = 65536;     // key (x) key operand of a stage: hi [256][64] then lo [256][64]
+constexpr int NR_ROWS = 256;    // state rows per CTA (128 or 256; 256 measured faster)
+// key (x) key operand of a stage: hi [NR][64] then lo [NR][64]
+__host__ __device__ constexpr int bbuf(int NR) { return NR * 256; }
 constexpr int SB = NSLOT * SLOT;
-constexpr int SMEM_BYTES = SB + 2 * BBUF + 1024;
+__host__ __device__ constexpr int smem_bytes(int NR) { return SB + 2 * bbuf(NR) + 1024; }
 constexpr int THREADS = 16 * 32;
 constexpr int NBUILD = 256;     // builder threads (warps 0-7)
 constexpr int NEPI = 192;       // epilogue threads (warps 8, 9, 10, 12, 13, 14)
 constexpr int WARP_TMA = 11, WARP_MMA = 15;
-constexpr uint32_t IDESC = idesc_f16_f32(128, 256, false, false);
 
 struct Args {
     const float* g;       // [BH][NC] chunk totals
@@ -83,8 +87,13 @@ struct Args {
 
 using namespace tcscan;
 
+template <int NR>
 __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_constant__ CUtensorMap tmOps,
                                                                    const __grid_constant__ Args a) {
+    constexpr int MP = NR / 64;                  // key indices m per CTA
+    constexpr int BBUF = bbuf(NR);
+    constexpr uint32_t IDESC = idesc_f16_f32(128, NR, false, false);
+    constexpr uint32_t TCOLS = 2 * NR;           // two accumulator buffers of NR columns
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_align1024(smem_raw);
     __shared__ __align__(8) uint64_t bar_full[NSLOT], bar_empty[NSLOT], bar_bfull[2], bar_bempty[2], bar_hfull[2],
@@ -116,7 +125,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
         fence_mbar_init();
     }
     if (warp == 0) {
-        tmem_alloc(smem_u32(&tmem_base_s), 512);
+        tmem_alloc(smem_u32(&tmem_base_s), TCOLS);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -165,8 +174,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
                     // value^T rows (M), K-major.  M rows 72-127 read whatever follows the slot: they
                     // only reach accumulator lanes 72-127, which nothing reads.
                     const uint32_t av = sbase + sl * SLOT + 8192;
-                    const uint32_t bhi = sbase + SB + sb * BBUF, blo = bhi + 32768;
-                    const uint32_t d = tmem + (uint32_t)b * 256;
+                    const uint32_t bhi = sbase + SB + sb * BBUF, blo = bhi + NR * 128;
+                    const uint32_t d = tmem + (uint32_t)b * NR;
 #pragma unroll
                     for (int kk = 0; kk < KS / 16; ++kk)
                         umma_bf16(d, sdesc_sw128(av + kk * 32), sdesc_sw128(bhi + kk * 32), IDESC, (s > 0 || kk > 0) ? 1u : 0u);
@@ -185,9 +194,9 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
         }
     } else if (warp < 8) {
         // ---------------------------------------------------------------- key (x) key builders
-        // thread: key index n = t & 63, tokens 16 * (t >> 6) .. +15, the four state rows
-        // (m' = 0..3, m = 4Q + m') of that n: the Kt row of n is read once, the rows of m are
-        // warp-uniform (broadcast).
+        // thread: key index n = t & 63, tokens 16 * (t >> 6) .. +15, the MP state rows
+        // (m' = 0..MP-1, m = MP Q + m') of that n: the Kt row of n is read once, the rows of m
+        // are warp-uniform (broadcast).
         const int n = threadIdx.x & 63, kq = threadIdx.x >> 6;
         for (int gs = 0; gs < nstages; ++gs) {
             const int sl = gs % NSLOT, sb = gs & 1;
@@ -207,9 +216,9 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
                              : "=r"(xn[4 * c2]), "=r"(xn[4 * c2 + 1]), "=r"(xn[4 * c2 + 2]), "=r"(xn[4 * c2 + 3])
                              : "r"(kt + n * 128 + (((2 * kq + c2) ^ (n & 7)) << 4)));
 #pragma unroll
-            for (int mp = 0; mp < 4; ++mp) {
-                const int m = 4 * Q + mp, r = mp * 64 + n;
-                const uint32_t dhi = sbase + SB + sb * BBUF + r * 128, dlo = dhi + 32768;
+            for (int mp = 0; mp < MP; ++mp) {
+                const int m = MP * Q + mp, r = mp * 64 + n;
+                const uint32_t dhi = sbase + SB + sb * BBUF + r * 128, dlo = dhi + NR * 128;
 #pragma unroll
                 for (int c2 = 0; c2 < 2; ++c2) {
                     const int k8 = 2 * kq + c2;
@@ -238,12 +247,14 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
     } else {
         // ---------------------------------------------------------------- running state (epilogue)
         // warps 8, 12: value columns 0-31; 9, 13: columns 32-63; 10, 14: the normaliser column
-        // (tensor-memory lane 64 = lane 0 of the warp); e = which 128 of the 256 state rows.
+        // (tensor-memory lane 64 = lane 0 of the warp); e = which half of the NR state rows,
+        // NK groups of 32 rows each.
         const int q = warp & 3, e = warp >= 12 ? 1 : 0;
         const bool zwarp = q == 2;
         const int col = 32 * q + lane;               // value column (q < 2)
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-        const long row0 = (long)Q * 256 + 128 * e;   // first state row of this warp's 128
+        constexpr int NK = NR / 64;
+        const long row0 = (long)Q * NR + (NR / 2) * e;   // first state row of this warp's NR / 2
         float gam = 1.f;   // reverse: running max of zmax over the chunks walked so far
         // the 32 values of rows row0 + 32k + i (i = 0..31) held by lane `src` move to lane i
         auto gather_lane = [&](const float* v, int src) {
@@ -294,7 +305,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
         {
             const int slot0 = rev ? NC - 1 : 0;
             if (a.sscale && Q == 0 && warp == 8 && lane == 0) a.sscale[bh * NC + slot0] = 1.f;
-            for (int k = 0; k < 4; ++k) {
+            for (int k = 0; k < NK; ++k) {
                 float v[32];
                 initial_rows(k, v);
                 export_rows(slot0, k, v);
@@ -308,11 +319,11 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
             if (abort_s || !(ok = mbar_wait(smem_u32(&bar_hfull[b]), (uint32_t)(it >> 1) & 1, a.status))) break;
             tc_fence_after();
             // pass 1: S_c = dec S_{c-1} + scl H^T_c over the buffer of chunk c
-            for (int k = 0; k < 4; ++k) {
-                const uint32_t cur = tmem + lane_base + (uint32_t)b * 256 + 128 * e + 32 * k;
+            for (int k = 0; k < NK; ++k) {
+                const uint32_t cur = tmem + lane_base + (uint32_t)b * NR + (NR / 2) * e + 32 * k;
                 float h[32], p[32];
                 tmem_ld32(cur, h);
-                if (it > 0) tmem_ld32(tmem + lane_base + (uint32_t)(1 - b) * 256 + 128 * e + 32 * k, p);
+                if (it > 0) tmem_ld32(tmem + lane_base + (uint32_t)(1 - b) * NR + (NR / 2) * e + 32 * k, p);
                 else initial_rows(k, p);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) h[i] = fmaf(dec, p[i], scl * h[i]);
@@ -326,16 +337,16 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
             const int slot = rev ? c - 1 : c + 1;
             if (slot >= 0 && slot < NC) {
                 if (a.sscale && Q == 0 && warp == 8 && lane == 0) a.sscale[bh * NC + slot] = gam;
-                for (int k = 0; k < 4; ++k) {
+                for (int k = 0; k < NK; ++k) {
                     float v[32];
-                    tmem_ld32(tmem + lane_base + (uint32_t)b * 256 + 128 * e + 32 * k, v);
+                    tmem_ld32(tmem + lane_base + (uint32_t)b * NR + (NR / 2) * e + 32 * k, v);
                     export_rows(slot, k, v);
                 }
             }
             if (!rev && it == nchunks - 1 && (a.S_final || a.z_final)) {
-                for (int k = 0; k < 4; ++k) {
+                for (int k = 0; k < NK; ++k) {
                     float v[32];
-                    tmem_ld32(tmem + lane_base + (uint32_t)b * 256 + 128 * e + 32 * k, v);
+                    tmem_ld32(tmem + lane_base + (uint32_t)b * NR + (NR / 2) * e + 32 * k, v);
                     const long rbase = row0 + 32 * k;
                     if (zwarp) {
                         const float zv = gather_lane(v, 0);
@@ -351,7 +362,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 512);
+    if (warp == 0) tmem_dealloc(tmem, TCOLS);
 }
 
 cudaError_t tc_state_scan(const Problem& p, const ScanIO& io, cudaStream_t s) {
@@ -365,10 +376,11 @@ cudaError_t tc_state_scan(const Problem& p, const ScanIO& io, cudaStream_t s) {
     if (!status) return cudaErrorInvalidValue;
     Args a{io.g, io.zmax, io.S0, io.z0, (__half*)io.Sx, io.zx, io.sscale, io.S_final, io.z_final, status, p.T, p.NC,
            (int)p.Tp(), io.rev ? 1 : 0};
-    cudaError_t e = cudaFuncSetAttribute(tc_state_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    constexpr int NR = NR_ROWS, SMEM = smem_bytes(NR);
+    cudaError_t e = cudaFuncSetAttribute(tc_state_scan_kernel<NR>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
-    dim3 grid(16, (unsigned)p.BH());
-    tc_state_scan_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(tops, a);
+    dim3 grid(4096 / NR, (unsigned)p.BH());
+    tc_state_scan_kernel<NR><<<grid, THREADS, SMEM, s>>>(tops, a);
     return cudaGetLastError();
 }
 
