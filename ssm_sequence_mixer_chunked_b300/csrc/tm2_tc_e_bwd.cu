@@ -7,18 +7,23 @@
 // and the A-mask gradient from the row sums sum_j dx_ij and column sums sum_i dx_ij
 // (dcumA_t = rowsum_t - colsum_t, accumulated from the end of the sequence elsewhere).
 //
-// Two kernels, one CTA per 128-token tile:
-//  * keys (tc_e_bwd_dkdv): per 128-query block at or after the key tile, s^T = K Q^T and
-//    dP^T = V dO^T (tcgen05.mma, M = N = 128) in tensor memory; the compute warps form P^T
-//    (bf16) and dx^T as bf16 hi + lo (its sums over queries cancel, so one bf16 rounding would
-//    cost the 2e-2 bar), written back over the scores; then dv += P^T dO and
-//    dk += (dx_hi + dx_lo)^T Q with Q, dO MN-major straight from their tiles.
-//  * queries (tc_e_bwd_dq): per 128-key block at or before the query tile, s = Q K^T and
+// Two kernels, one CTA per 128-token tile, walking the other side in 64-token sub-blocks
+// (the 128-token tiles arrive by TMA in a 4-stage ring, two sub-blocks per stage):
+//  * keys (kd = true): per 64-query sub-block at or after the key tile, s^T = K Q^T and
+//    dP^T = V dO^T (tcgen05.mma, M = 128, N = 64) into one of three tensor-memory buffers; the
+//    compute warps form P^T (bf16) and dx^T as bf16 hi + lo (its sums over queries cancel, so
+//    one bf16 rounding would cost the 2e-2 bar), written back over the scores and dP they
+//    have read; then dv += P^T dO and dk += (dx_hi + dx_lo)^T Q with Q, dO MN-major straight
+//    from their tiles.
+//  * queries (kd = false): per 64-key sub-block at or before the query tile, s = Q K^T and
 //    dP = dO V^T, dx hi + lo, dq += dx K.
-// The per-token scalars of the walked blocks (lse, D, and the running sums as fp32 value +
-// residual) are staged in shared memory each block.  Warps 0-7 compute (warp w: lane
-// quadrant w % 4, half w / 4 of the walked block's 128 tokens), warp 8 issues TMA, warp 9
-// the MMAs.  Every mbarrier wait is bounded (TM2_ERR_TIMEOUT on expiry).
+// With three sub-block buffers the MMA thread issues the scores of sub-block s while the
+// compute warps work on s - 1 and the gradient products of s - 2 drain, so the softmax step
+// overlaps the tensor core (a whole 128-token block needs 256 columns for scores + dP and
+// cannot be double-buffered beside the operands and accumulators).
+// The per-token terms of the walked sub-blocks are staged in shared memory.  Warps 0-7
+// compute (warp w: lane quadrant w % 4, half w / 4 of the sub-block's 64 tokens), warp 8
+// issues TMA, warp 9 the MMAs.  Every mbarrier wait is bounded (TM2_ERR_TIMEOUT on expiry).
 #include "tm2.h"
 #include "tm2_launch.h"
 #include "tm2_sm100.cuh"
@@ -28,6 +33,8 @@ namespace tm2 {
 namespace tceb {
 
 constexpr int BT = 128;                      // tokens per tile / block
+constexpr int SUB = 64;                      // walked tokens per sub-block
+constexpr int NB = 3;                        // tensor-memory sub-block buffers
 constexpr int THREADS = 10 * 32;
 constexpr int WARP_TMA = 8, WARP_MMA = 9;
 constexpr int NS = 4;                        // stages of the walked blocks (two tiles each)
@@ -38,12 +45,14 @@ constexpr int SSTG = 2 * TILE;
 constexpr int SSC = SSTG + NS * STAGE;       // [2 buffers][4 arrays][128] per-token scalars
 constexpr int SRED = SSC + 2 * 4 * BT * 4;   // [2 halves][128]
 constexpr int SMEM_BYTES = SRED + 2 * BT * 4 + 1024;
-// tensor memory: scores at 0, dP at 128, accumulators at 256 (dk or dq) and 320 (dv); the
-// softmax step writes its operands where no other warp reads: dk/dv kernel P at 384, dx hi at
-// 448, dx lo over the writing warp's own dP columns (128 + 64 h .. +32); dq kernel dx hi at 384,
-// dx lo at 448.  Column c of an operand holds the walked tokens 2c, 2c+1 of that half.
-constexpr uint32_t TM_S = 0, TM_DP = 128, TM_ACC = 256, TM_ACC2 = 320, TM_O1 = 384, TM_O2 = 448;
-constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, false, false);
+// tensor memory: sub-block buffer u at 128 u holds the scores (columns 0-63) and dP (64-127);
+// accumulators at 384 (dk or dq) and 448 (dv).  The warp of half h owns score columns
+// 32 h .. +31 and dP columns 64 + 32 h .. +31 of its lanes and writes, per 16 tokens
+// (round q of 2), P to score columns 32 h + 16 q .. +7, dx hi to the next 8 and dx lo to dP
+// columns 64 + 32 h + 8 q .. +7, all already read.  Column c of an operand holds tokens
+// 2c, 2c+1 of its 16.
+constexpr uint32_t TM_ACC = 384, TM_ACC2 = 448;
+constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 64, false, false);
 constexpr uint32_t IDESC_MN = idesc_bf16_f32(128, 64, false, true);
 
 struct Args {
@@ -105,8 +114,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_e_bwd_kernel(const __grid_const
     // dq: A = Q, B = dO (this CTA's tiles), C = K, D = V (walked)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_align1024(smem_raw);
-    __shared__ __align__(8) uint64_t bar_fix, bar_full[NS], bar_empty[NS], bar_sfull, bar_pfull, bar_tfree, bar_accfull,
-        bar_done;
+    __shared__ __align__(8) uint64_t bar_fix, bar_full[NS], bar_empty[NS], bar_sfull[NB], bar_pfull[NB], bar_bfree[NB],
+        bar_accfull, bar_done;
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_s;
     __shared__ volatile int gflags[2];
@@ -128,9 +137,11 @@ __global__ void __launch_bounds__(THREADS, 1) tc_e_bwd_kernel(const __grid_const
             mbar_init(smem_u32(&bar_full[i]), 1);
             mbar_init(smem_u32(&bar_empty[i]), 1);
         }
-        mbar_init(smem_u32(&bar_sfull), 1);
-        mbar_init(smem_u32(&bar_pfull), 256);
-        mbar_init(smem_u32(&bar_tfree), 1);
+        for (int i = 0; i < NB; ++i) {
+            mbar_init(smem_u32(&bar_sfull[i]), 1);
+            mbar_init(smem_u32(&bar_pfull[i]), 256);
+            mbar_init(smem_u32(&bar_bfree[i]), 1);
+        }
         mbar_init(smem_u32(&bar_accfull), 1);
         mbar_init(smem_u32(&bar_done), 1);
         abort_s = 0;
@@ -172,41 +183,54 @@ __global__ void __launch_bounds__(THREADS, 1) tc_e_bwd_kernel(const __grid_const
         if (lane == 0) {
             bool ok = mbar_wait(smem_u32(&bar_fix), 0, a.status);
             tc_fence_after();
-            for (int c = 0; c < nblk && ok; ++c) {
-                const int st = c % NS;
+            const int nsb = 2 * nblk;
+            // scores of sub-block s, then the gradient products of sub-block s - 1
+            for (int s = 0; s <= nsb && ok; ++s) {
                 if (abort_s) { ok = false; break; }
-                if (!(ok = mbar_wait(smem_u32(&bar_full[st]), (uint32_t)(c / NS) & 1, a.status))) break;
-                if (c > 0 && !(ok = mbar_wait(smem_u32(&bar_tfree), (uint32_t)(c - 1) & 1, a.status))) break;
-                tc_fence_after();
-                const uint32_t sc = sb0 + SSTG + st * STAGE, sd = sc + TILE;
-                // scores and dP: (fixed tile) x (walked tile)^T, M = N = 128, K = 64
+                if (s < nsb) {
+                    const int c = s >> 1, st = c % NS, u = s % NB;
+                    if ((s & 1) == 0 && !(ok = mbar_wait(smem_u32(&bar_full[st]), (uint32_t)(c / NS) & 1, a.status)))
+                        break;
+                    if (s >= NB && !(ok = mbar_wait(smem_u32(&bar_bfree[u]), (uint32_t)((s / NB) - 1) & 1, a.status)))
+                        break;
+                    tc_fence_after();
+                    const uint32_t sc = sb0 + SSTG + st * STAGE + (s & 1) * (SUB * 128), sd = sc + TILE;
+                    const uint32_t d = tmem + 128u * (uint32_t)u;
+                    // scores and dP: (fixed tile) x (walked sub-block)^T, M = 128, N = 64, K = 64
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    umma_bf16(tmem + TM_S, sdesc_sw128(sb0 + SFIX + kk * 32), sdesc_sw128(sc + kk * 32), IDESC_S, kk > 0);
-                    umma_bf16(tmem + TM_DP, sdesc_sw128(sb0 + SFIX + TILE + kk * 32), sdesc_sw128(sd + kk * 32), IDESC_S,
-                              kk > 0);
-                }
-                umma_commit(smem_u32(&bar_sfull));
-                if (!(ok = mbar_wait(smem_u32(&bar_pfull), (uint32_t)c & 1, a.status))) break;
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < BT / 16; ++kk) {
-                    const uint32_t acc0 = (c > 0 || kk > 0) ? 1u : 0u;
-                    if (kd) {   // dv += P^T dO, dk += (dx hi + lo)^T Q
-                        const uint64_t qd = sdesc_sw128_ex(sc + kk * 2048, 8192, 1024);
-                        const uint64_t dd = sdesc_sw128_ex(sd + kk * 2048, 8192, 1024);
-                        const uint32_t lo_col = TM_DP + (kk >> 2) * 64 + (kk & 3) * 8;   // half kk / 4's dP columns
-                        umma_bf16_ts(tmem + TM_ACC2, tmem + TM_O1 + kk * 8, dd, IDESC_MN, acc0);
-                        umma_bf16_ts(tmem + TM_ACC, tmem + TM_O2 + kk * 8, qd, IDESC_MN, acc0);
-                        umma_bf16_ts(tmem + TM_ACC, tmem + lo_col, qd, IDESC_MN, 1u);
-                    } else {    // dq += (dx hi + lo) K
-                        const uint64_t kdsc = sdesc_sw128_ex(sc + kk * 2048, 8192, 1024);
-                        umma_bf16_ts(tmem + TM_ACC, tmem + TM_O1 + kk * 8, kdsc, IDESC_MN, acc0);
-                        umma_bf16_ts(tmem + TM_ACC, tmem + TM_O2 + kk * 8, kdsc, IDESC_MN, 1u);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        umma_bf16(d, sdesc_sw128(sb0 + SFIX + kk * 32), sdesc_sw128(sc + kk * 32), IDESC_S, kk > 0);
+                        umma_bf16(d + 64, sdesc_sw128(sb0 + SFIX + TILE + kk * 32), sdesc_sw128(sd + kk * 32), IDESC_S,
+                                  kk > 0);
                     }
+                    umma_commit(smem_u32(&bar_sfull[u]));
                 }
-                umma_commit(smem_u32(&bar_tfree));
-                umma_commit(smem_u32(&bar_empty[st]));
+                if (s >= 1) {
+                    const int pz = s - 1, c = pz >> 1, st = c % NS, u = pz % NB;
+                    if (!(ok = mbar_wait(smem_u32(&bar_pfull[u]), (uint32_t)(pz / NB) & 1, a.status))) break;
+                    tc_fence_after();
+                    const uint32_t sc = sb0 + SSTG + st * STAGE + (pz & 1) * (SUB * 128), sd = sc + TILE;
+                    const uint32_t base = tmem + 128u * (uint32_t)u;
+#pragma unroll
+                    for (int kk = 0; kk < SUB / 16; ++kk) {   // 16 tokens: half kk / 2, round kk % 2
+                        const uint32_t acc0 = (pz > 0 || kk > 0) ? 1u : 0u;
+                        const uint32_t opP = base + (kk >> 1) * 32 + (kk & 1) * 16, opH = opP + 8;
+                        const uint32_t opL = base + 64 + (kk >> 1) * 32 + (kk & 1) * 8;
+                        if (kd) {   // dv += P^T dO, dk += (dx hi + lo)^T Q
+                            const uint64_t qd = sdesc_sw128_ex(sc + kk * 2048, 8192, 1024);
+                            const uint64_t dd = sdesc_sw128_ex(sd + kk * 2048, 8192, 1024);
+                            umma_bf16_ts(tmem + TM_ACC2, opP, dd, IDESC_MN, acc0);
+                            umma_bf16_ts(tmem + TM_ACC, opH, qd, IDESC_MN, acc0);
+                            umma_bf16_ts(tmem + TM_ACC, opL, qd, IDESC_MN, 1u);
+                        } else {    // dq += (dx hi + lo) K
+                            const uint64_t kdsc = sdesc_sw128_ex(sc + kk * 2048, 8192, 1024);
+                            umma_bf16_ts(tmem + TM_ACC, opH, kdsc, IDESC_MN, acc0);
+                            umma_bf16_ts(tmem + TM_ACC, opL, kdsc, IDESC_MN, 1u);
+                        }
+                    }
+                    umma_commit(smem_u32(&bar_bfree[u]));
+                    if (pz & 1) umma_commit(smem_u32(&bar_empty[st]));   // both sub-blocks of the stage done
+                }
             }
             if (ok) umma_commit(smem_u32(&bar_accfull));
             else abort_s = 1;
@@ -239,45 +263,54 @@ __global__ void __launch_bounds__(THREADS, 1) tc_e_bwd_kernel(const __grid_const
         float sum = 0.f;
         int kg = 0;
         bool ok = true;
-        for (int c = 0; c < nblk && ok; ++c) {
-            const int x = c & 1;
-            const long t0 = (long)(blk0 + c) * BT;
-            // the walked block's per-token terms into buffer x: W at [0, 128), D at [128, 256)
-            float* sc = sSc + x * 4 * BT;
-            for (int e = threadIdx.x; e < (kd ? 2 : 1) * BT; e += 256) {
-                const int arr = e >> 7, tt = e & 127;
-                const long t = t0 + tt;
-                float val = 0.f;
-                if (t < a.T) {
-                    const float off = (a.cum[base + t] - ref) + (a.cum_lo[base + t] - reflo);
-                    if (arr == 1) val = a.Dv[base + t];
-                    else val = kd ? (off - a.lse[base + t]) * LOG2E : off * LOG2E;
-                }
-                sc[arr * BT + tt] = val;
+        const int nsb = 2 * nblk;
+        // per-token term of walked sub-block j held by this thread (threads below 64 or 128):
+        // arrays W at [0, 64) and D at [64, 128) of a staging buffer
+        const bool stager = threadIdx.x < (kd ? 2 : 1) * SUB;
+        const int arr = threadIdx.x >> 6, tt_st = threadIdx.x & 63;
+        auto term = [&](int j) {
+            const long t = (long)blk0 * BT + (long)j * SUB + tt_st;
+            float val = 0.f;
+            if (t < a.T) {
+                const float off = (a.cum[base + t] - ref) + (a.cum_lo[base + t] - reflo);
+                if (arr == 1) val = a.Dv[base + t];
+                else val = kd ? (off - a.lse[base + t]) * LOG2E : off * LOG2E;
             }
-            // masks only on the diagonal block and on a block that runs past the sequence end
-            const bool masked = kd ? (c == 0 || t0 + BT > a.T) : (c == nblk - 1);
+            return val;
+        };
+        float nxt = stager ? term(0) : 0.f;
+        for (int sbk = 0; sbk < nsb && ok; ++sbk) {
+            const int x = sbk & 1, u = sbk % NB;
+            const long t0 = (long)blk0 * BT + (long)sbk * SUB;
+            // the walked sub-block's terms into buffer x; the next one's loads fly meanwhile
+            float* sc = sSc + x * 2 * SUB;
+            if (stager) {
+                sc[arr * SUB + tt_st] = nxt;
+                if (sbk + 1 < nsb) nxt = term(sbk + 1);
+            }
+            // masks only on the diagonal block's sub-blocks and on a sub-block that runs past
+            // the sequence end
+            const bool masked = kd ? (sbk < 2 || t0 + SUB > a.T) : (sbk >= nsb - 2);
             const int lo = kd ? (int)(r - t0) : 0;
-            const int hi = kd ? (int)min((long)BT, (long)a.T - t0) : (int)(r - t0) + 1;
+            const int hi = kd ? (int)min((long)SUB, (long)a.T - t0) : (int)(r - t0) + 1;
             // (the group wait's barrier also publishes the staged terms to every thread)
-            if (!(ok = group_wait(smem_u32(&bar_sfull), (uint32_t)c & 1, a.status, warp == 0, 1, 256, gflags, kg,
-                                  &abort_s)))
+            if (!(ok = group_wait(smem_u32(&bar_sfull[u]), (uint32_t)(sbk / NB) & 1, a.status, warp == 0, 1, 256,
+                                  gflags, kg, &abort_s)))
                 break;
-            // 16 walked tokens at a time: read scores and dP, write P / dx hi / dx lo (the outputs
-            // go to columns only this warp reads, so no barrier is needed between reads and writes)
+            const uint32_t bufc = tmem + lane_base + 128u * (uint32_t)u;
 #pragma unroll 1
-            for (int q4 = 0; q4 < 4; ++q4) {
-                const int tt0 = h * 64 + q4 * 16;
+            for (int q4 = 0; q4 < 2; ++q4) {
+                const int tt0 = h * 32 + q4 * 16;
                 float s[16], dp[16], W[16], Dq[16];
-                tmem_ld16(tmem + lane_base + TM_S + tt0, s);
-                tmem_ld16(tmem + lane_base + TM_DP + tt0, dp);
+                tmem_ld16(bufc + tt0, s);
+                tmem_ld16(bufc + 64 + tt0, dp);
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float4 w4 = reinterpret_cast<const float4*>(sc + tt0)[u];
-                    W[4 * u] = w4.x, W[4 * u + 1] = w4.y, W[4 * u + 2] = w4.z, W[4 * u + 3] = w4.w;
+                for (int v4 = 0; v4 < 4; ++v4) {
+                    const float4 w4 = reinterpret_cast<const float4*>(sc + tt0)[v4];
+                    W[4 * v4] = w4.x, W[4 * v4 + 1] = w4.y, W[4 * v4 + 2] = w4.z, W[4 * v4 + 3] = w4.w;
                     if (kd) {
-                        const float4 d4 = reinterpret_cast<const float4*>(sc + BT + tt0)[u];
-                        Dq[4 * u] = d4.x, Dq[4 * u + 1] = d4.y, Dq[4 * u + 2] = d4.z, Dq[4 * u + 3] = d4.w;
+                        const float4 d4 = reinterpret_cast<const float4*>(sc + SUB + tt0)[v4];
+                        Dq[4 * v4] = d4.x, Dq[4 * v4 + 1] = d4.y, Dq[4 * v4 + 2] = d4.z, Dq[4 * v4 + 3] = d4.w;
                     }
                 }
                 uint32_t pp[8], dh[8], dl[8];
@@ -285,19 +318,14 @@ __global__ void __launch_bounds__(THREADS, 1) tc_e_bwd_kernel(const __grid_const
                     softmax_grad16<kd, true>(s, dp, W, Dq, crr, Dr, sl2, tt0, lo, hi, sum, pp, dh, dl);
                 else
                     softmax_grad16<kd, false>(s, dp, W, Dq, crr, Dr, sl2, tt0, lo, hi, sum, pp, dh, dl);
-                const uint32_t ocol = h * 32 + q4 * 8;   // operand column of these 16 tokens
-                if (kd) {
-                    tmem_st8(tmem + lane_base + TM_O1 + ocol, pp);
-                    tmem_st8(tmem + lane_base + TM_O2 + ocol, dh);
-                    tmem_st8(tmem + lane_base + TM_DP + h * 64 + q4 * 8, dl);   // own dP columns, already read
-                } else {
-                    tmem_st8(tmem + lane_base + TM_O1 + ocol, dh);
-                    tmem_st8(tmem + lane_base + TM_O2 + ocol, dl);
-                }
+                const uint32_t oc = bufc + h * 32 + q4 * 16;   // this round's P, then dx hi
+                if (kd) tmem_st8(oc, pp);
+                tmem_st8(oc + 8, dh);
+                tmem_st8(bufc + 64 + h * 32 + q4 * 8, dl);
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(smem_u32(&bar_pfull));
+            mbar_arrive(smem_u32(&bar_pfull[u]));
         }
         // ---- gradients of this tile's tokens; the two halves' sums combined
         if (ok) sRed[h * BT + l] = sum;
