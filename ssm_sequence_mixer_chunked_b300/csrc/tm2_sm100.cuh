@@ -253,18 +253,6 @@ TM2_DEV void tmem_st32(uint32_t taddr, const float* v) {
 }
 TM2_DEV void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// 32 lanes x 1 column -> 1 register per thread (load and wait in one statement).
-TM2_DEV float tmem_ld1(uint32_t taddr) {
-    uint32_t r;
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];\n"
-        "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(r)
-        : "r"(taddr)
-        : "memory");
-    return __uint_as_float(r);
-}
-
 // byte offset of (row, 16-byte chunk) inside a 128B-swizzled K-major tile
 TM2_DEV uint32_t swz128(uint32_t row, uint32_t chunk) { return row * 128u + ((chunk ^ (row & 7u)) << 4); }
 
