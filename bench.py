@@ -108,6 +108,39 @@ def decode_bytes_per_head(d, dv):
     return 2 * d * d * dv * 4 + 2 * d * d * 4 + 3 * d * 4 + 4 + dv * 4 + 4
 
 
+def roofline(kernel, kf, kb, ms_per_launch, pk, tc):
+    """Roofline entry of one kernel from its algorithmic flops kf and bytes kb per launch and its
+    live launch time.  Tensor-core kernels (timed inside a long step) are measured against the
+    sustained bf16 figure or the HBM copy bandwidth, whichever bound takes longer for the
+    kernel's algorithmic work; CUDA-core kernels against the fp32 FMA rate derived from the SM
+    count and clock.  None when the kernel's work is not counted."""
+    if kf is None:
+        return None
+    sec = ms_per_launch * 1e-3
+    if tc:
+        t_flop = kf / (pk["bf16_tflops_sustained"] * 1e12)
+        t_byte = kb / (pk["hbm_gbs"] * 1e9)
+        if t_byte > t_flop:
+            roof = {"kernel": kernel, "bound": "hbm", "achieved": kb / sec / 1e9, "peak": pk["hbm_gbs"],
+                    "unit": "GB/s", "frac": kb / sec / 1e9 / pk["hbm_gbs"],
+                    "peak_source": "MEASURED_PEAKS.json hbm_gbs (%s)" % pk["source"]}
+        else:
+            roof = {"kernel": kernel, "bound": "tensor", "achieved": kf / sec / 1e12,
+                    "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                    "frac": kf / sec / 1e12 / pk["bf16_tflops_sustained"],
+                    "peak_source": "MEASURED_PEAKS.json bf16_tflops_sustained (%s)" % pk["source"]}
+        roof["algorithmic_flops_per_launch"] = kf
+        roof["algorithmic_bytes_per_launch"] = kb
+        roof["tensor_frac"] = kf / sec / 1e12 / pk["bf16_tflops_sustained"]
+        roof["hbm_frac"] = kb / sec / 1e9 / pk["hbm_gbs"]
+        return roof
+    peak = 148 * 128 * 2 * pk["sm_max_mhz"] * 1e6 / 1e12   # FFMA, TFLOP/s
+    return {"kernel": kernel, "bound": "alu", "achieved": kf / sec / 1e12, "peak": peak, "unit": "TFLOP/s",
+            "frac": kf / sec / 1e12 / peak,
+            "peak_source": "derived: 148 SMs x 128 fp32 FMA/clk x 2 flop x %.0f MHz" % pk["sm_max_mhz"],
+            "algorithmic_flops_per_launch": kf}
+
+
 # ----------------------------------------------------------------------------- tracing
 class Trace:
     def __init__(self, lib):
@@ -180,26 +213,34 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.fh.close()
-        sm, smax, reasons = [], 0.0, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 7:
-                    continue
-                try:
-                    sm.append(float(parts[0]))
-                    smax = max(smax, float(parts[1]))
-                except ValueError:
-                    continue
-                for n, v in zip(names, parts[3:7]):
-                    if v.lower() == "active":
-                        reasons.add(n)
+            out = parse_clocks(f)
         os.unlink(self.path)
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return out
+
+
+def parse_clocks(lines):
+    """Summary of `nvidia-smi --query-gpu=<ClockSampler.FIELDS> --format=csv,noheader,nounits`
+    samples: median SM clock, the highest max-clock reading, and every throttle reason seen
+    Active in any sample (None when no sample parsed)."""
+    sm, smax, reasons = [], 0.0, set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in lines:
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 7:
+            continue
+        try:
+            sm.append(float(parts[0]))
+            smax = max(smax, float(parts[1]))
+        except ValueError:
+            continue
+        for n, v in zip(names, parts[3:7]):
+            if v.lower() == "active":
+                reasons.add(n)
+    if not sm:
+        return None
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+            "samples": len(sm)}
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -379,32 +420,8 @@ def run_tm2(args, world, rank, device):
     tc = dom.startswith("tc_")
     kf = kernel_flops(dom, d, dv, 256 if tc else 64, per_launch_tokens)
     kb = kernel_bytes(dom, d, dv, 256, per_launch_tokens) if tc else None
-    roof = None
-    if kf is not None:
-        sec = kern[dom]["ms_per_launch"] * 1e-3
-        if tc:   # timed inside a long step: the sustained bf16 figure; the bound is whichever of
-            # the algorithmic flops and bytes takes longer at its measured peak
-            t_flop = kf / (pk["bf16_tflops_sustained"] * 1e12)
-            t_byte = kb / (pk["hbm_gbs"] * 1e9)
-            if t_byte > t_flop:
-                roof = {"kernel": dom, "bound": "hbm", "achieved": kb / sec / 1e9, "peak": pk["hbm_gbs"],
-                        "unit": "GB/s", "frac": kb / sec / 1e9 / pk["hbm_gbs"],
-                        "peak_source": "MEASURED_PEAKS.json hbm_gbs (%s)" % pk["source"]}
-            else:
-                roof = {"kernel": dom, "bound": "tensor", "achieved": kf / sec / 1e12,
-                        "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                        "frac": kf / sec / 1e12 / pk["bf16_tflops_sustained"],
-                        "peak_source": "MEASURED_PEAKS.json bf16_tflops_sustained (%s)" % pk["source"]}
-            roof["algorithmic_flops_per_launch"] = kf
-            roof["algorithmic_bytes_per_launch"] = kb
-            roof["tensor_frac"] = kf / sec / 1e12 / pk["bf16_tflops_sustained"]
-            roof["hbm_frac"] = kb / sec / 1e9 / pk["hbm_gbs"]
-        else:
-            peak = 148 * 128 * 2 * pk["sm_max_mhz"] * 1e6 / 1e12   # FFMA, TFLOP/s
-            roof = {"kernel": dom, "bound": "alu", "achieved": kf / sec / 1e12, "peak": peak, "unit": "TFLOP/s",
-                    "frac": kf / sec / 1e12 / peak,
-                    "peak_source": "derived: 148 SMs x 128 fp32 FMA/clk x 2 flop x %.0f MHz" % pk["sm_max_mhz"],
-                    "algorithmic_flops_per_launch": kf}
+    roof = roofline(dom, kf, kb, kern[dom]["ms_per_launch"], pk, tc)
+    if roof is not None:
         roof["traffic"] = ncu_traffic(dom, per_launch_tokens)
     CH = TC_CHUNK
     counted = (fwd_flops(d, dv, CH) + bwd_flops(d, dv, CH)) * B * H * T
