@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_align1024(smem_raw);
     __shared__ __align__(8) uint64_t bar_ld, bar_full[NR], bar_empty[NR], bar_cvt, bar_sfull[4], bar_sfree[4],
-        bar_pfull[4], bar_pfree[4], bar_ufull[2], bar_uempty[2], bar_kvfull, bar_red, bar_done;
+        bar_pfull[4], bar_ufull[2], bar_uempty[2], bar_kvfull, bar_red, bar_done;
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_s;
     __shared__ volatile int gflags[2];         // group waits of the compute warps
@@ -119,7 +119,6 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
             mbar_init(smem_u32(&bar_sfull[b]), 1);
             mbar_init(smem_u32(&bar_sfree[b]), 256);
             mbar_init(smem_u32(&bar_pfull[b]), 256);
-            mbar_init(smem_u32(&bar_pfree[b]), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&bar_ufull[i]), 1);
@@ -268,7 +267,6 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
                     umma_bf16_ts(tmem + TM_DV, tmem + TM_WH + kk * 8, dd, IDESC_BF_MN, acc0);
                     umma_bf16_ts(tmem + TM_DV, tmem + TM_WL + kk * 8, dd, IDESC_BF_MN, 1u);
                 }
-                umma_commit(smem_u32(&bar_pfree[b]));
             }
             if (ok) umma_commit(smem_u32(&bar_kvfull));
             else abort_s = 1;
@@ -365,9 +363,9 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
         for (int b = 0; b < nblk && ok; ++b) {
             const int ib = 2 * tj + b;
             if (!(ok = group_wait(smem_u32(&bar_sfull[b]), 0, a.status, warp == 0, 1, 256, gflags, kg, &abort_s))) break;
-            if (b > 0 && !(ok = group_wait(smem_u32(&bar_pfree[b - 1]), 0, a.status, warp == 0, 1, 256, gflags, kg,
-                                           &abort_s)))
-                break;
+            // (the P buffer's last reader, the product of block b-1, was issued before this block's
+            // scores; the commit that announced them completes only after every earlier MMA of the
+            // issuing thread, so the buffer is free)
 #pragma unroll
             for (int g2 = 0; g2 < 2; ++g2) {
                 const int cc = 2 * h + g2;

@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_cons
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_align1024(smem_raw);
     __shared__ __align__(8) uint64_t bar_ld, bar_full[NR], bar_empty[NR], bar_cvt, bar_sfull[4], bar_sfree[4],
-        bar_pfull[4], bar_pfree[4], bar_ufull[2], bar_uempty[2], bar_dqfull, bar_zrdy, bar_done;
+        bar_pfull[4], bar_ufull[2], bar_uempty[2], bar_dqfull, bar_zrdy, bar_done;
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_s;
     __shared__ volatile int gflags[2];         // group waits of the compute warps
@@ -106,7 +106,6 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_cons
             mbar_init(smem_u32(&bar_sfull[b]), 1);
             mbar_init(smem_u32(&bar_sfree[b]), 256);
             mbar_init(smem_u32(&bar_pfull[b]), 256);
-            mbar_init(smem_u32(&bar_pfree[b]), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&bar_ufull[i]), 1);
@@ -242,7 +241,6 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_cons
                     umma_bf16_ts(tmem + TM_DQ, pb + kk * 8, kd, IDESC_BF_MN, (b > 0 || kk > 0) ? 1u : 0u);
                     umma_bf16_ts(tmem + TM_DQ, pb + 32 + kk * 8, kd, IDESC_BF_MN, 1u);
                 }
-                umma_commit(smem_u32(&bar_pfree[b]));
             }
             if (ok) umma_commit(smem_u32(&bar_dqfull));
             else abort_s = 1;
@@ -316,9 +314,9 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_cons
         // ---- intra-chunk blocks
         for (int b = 0; b < nblk && ok; ++b) {
             if (!(ok = group_wait(smem_u32(&bar_sfull[b]), 0, a.status, warp == 0, 1, 256, gflags, kg, &abort_s))) break;
-            if (b >= 2 && !(ok = group_wait(smem_u32(&bar_pfree[b - 2]), 0, a.status, warp == 0, 1, 256, gflags, kg,
-                                            &abort_s)))
-                break;
+            // (the P buffer's last reader, the product of block b-2, was issued before this block's
+            // scores; the commit that announced them completes only after every earlier MMA of the
+            // issuing thread, so the buffer is free)
             const uint32_t swb = tmem + lane_base + TM_SW + (uint32_t)(b & 1) * 128;
             const uint32_t pbb = tmem + lane_base + TM_P + (uint32_t)(b & 1) * 64;
 #pragma unroll

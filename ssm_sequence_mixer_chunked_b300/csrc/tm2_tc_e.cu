@@ -266,10 +266,9 @@ __global__ void __launch_bounds__(THREADS, 1) tc_e_fwd_kernel(const __grid_const
                     m_used = bmax;
                 }
             }
-            // P = exp(x - m) in bf16 into P buffer x (free once block b-2's product is done)
-            if (b >= 2 && !(ok = group_wait(smem_u32(&bar_pfree[x]), (uint32_t)((b >> 1) - 1) & 1, a.status, warp == 0,
-                                            1, 256, gflags, kg, &abort_s)))
-                break;
+            // P = exp(x - m) in bf16 into P buffer x.  Its last reader, the product of block b-2, was
+            // issued before the scores of block b, and the commit that announced those scores
+            // completes only when every earlier MMA of the issuing thread has, so it is free.
             uint32_t pk[32];
 #pragma unroll
             for (int c2 = 0; c2 < 32; ++c2) {

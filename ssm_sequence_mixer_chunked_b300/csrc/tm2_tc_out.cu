@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_align1024(smem_raw);
     __shared__ __align__(8) uint64_t bar_ld, bar_full[NR], bar_empty[NR], bar_cvt, bar_sfull[4], bar_sfree[4],
-        bar_pfull[4], bar_pfree[4], bar_ufull[2], bar_uempty[2], bar_yfull, bar_red, bar_done;
+        bar_pfull[4], bar_ufull[2], bar_uempty[2], bar_yfull, bar_red, bar_done;
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_s;
     __shared__ volatile int gflags[2];         // group waits of the compute warps
@@ -105,7 +105,6 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
             mbar_init(smem_u32(&bar_sfull[b]), 1);
             mbar_init(smem_u32(&bar_sfree[b]), 256);
             mbar_init(smem_u32(&bar_pfull[b]), 256);
-            mbar_init(smem_u32(&bar_pfree[b]), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&bar_ufull[i]), 1);
@@ -237,7 +236,6 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
                     umma_bf16_ts(tmem + TM_Y, pb + kk * 8, vd, IDESC_PV, (b > 0 || kk > 0) ? 1u : 0u);
                     umma_bf16_ts(tmem + TM_Y, pb + 32 + kk * 8, vd, IDESC_PV, 1u);
                 }
-                umma_commit(smem_u32(&bar_pfree[b]));
             }
             if (ok) umma_commit(smem_u32(&bar_yfull));
             else abort_s = 1;
@@ -301,9 +299,9 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
         // ---- intra-chunk blocks; half h covers 32 of the 64 keys of a block
         for (int b = 0; b < nblk && ok; ++b) {
             if (!(ok = group_wait(smem_u32(&bar_sfull[b]), 0, a.status, warp == 0, 1, 256, gflags, kg, &abort_s))) break;
-            if (b >= 2 && !(ok = group_wait(smem_u32(&bar_pfree[b - 2]), 0, a.status, warp == 0, 1, 256, gflags, kg,
-                                            &abort_s)))
-                break;
+            // (the P buffer's last reader, the product of block b-2, was issued before this block's
+            // scores; the commit that announced them completes only after every earlier MMA of the
+            // issuing thread, so the buffer is free)
             const uint32_t sbb = tmem + lane_base + TM_S + (uint32_t)(b & 1) * 64;
             const uint32_t pbb = tmem + lane_base + TM_P + (uint32_t)(b & 1) * 64;
 #pragma unroll
