@@ -1,7 +1,7 @@
 """Host-side logic of bench.py, run without a GPU: the algorithmic work per token-head that
 the roofline divides by, the choice of the bound, the summary of the clock samples that
-decides whether a run is rejected, and the rule that drops a DRAM-traffic capture once the
-kernel's source has changed.
+decides whether a run is rejected, the rule that drops a DRAM-traffic capture once the
+kernel's source has changed, and the JSON line of the reference (oracle) arm.
 """
 import json
 import os
@@ -111,3 +111,24 @@ def test_committed_traffic_records_name_existing_sources():
     for name, rec in recs.items():
         assert os.path.exists(os.path.join(bench.ROOT, "ssm_sequence_mixer_chunked_b300", "csrc", rec["file"])), name
         assert rec["dram_bytes_per_unit"] > 0 and rec["unit"]
+
+
+def test_reference_arm_prints_one_contract_line():
+    """`bench.py --impl reference` times the fp64 oracle on the CPU (one head of the bench
+    workload per step) and prints the same JSON line as the CUDA arm, marked as reference."""
+    import subprocess
+    import sys
+    out = subprocess.run([sys.executable, os.path.join(bench.ROOT, "bench.py"), "--impl", "reference",
+                          "--steps", "1", "--warmup", "0"], capture_output=True, text=True, timeout=600,
+                         cwd=bench.ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC
+    assert line["unit"] == "tokens/s" and line["higher_is_better"] is True and line["value"] > 0
+    assert line["warmup"] >= 3 and line["steps"] == 1 and line["n_gpus"] == 1
+    assert line["config"]["B"] == 2 and line["config"]["T"] == 8192 and line["config"]["d"] == 64
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
