@@ -50,7 +50,7 @@ def _load():
         _lib.orc_fwd_quadratic.argtypes = [i] * 5 + [p] * 6 + [i, p, p]
         _lib.orc_fwd_recurrent.argtypes = [i] * 5 + [p] * 6 + [i, p, p, p, p]
         _lib.orc_step.argtypes = [i] * 4 + [p] * 6 + [i, p, p]
-        _lib.orc_bwd_quadratic.argtypes = [i] * 5 + [p] * 5 + [i, p, p, p, p]
+        _lib.orc_bwd_quadratic.argtypes = [i] * 5 + [p] * 5 + [i, p, p, p, p, p, p]
         _lib.orc_e_fwd.argtypes = [i] * 5 + [p] * 4 + [d, p, p]
         _lib.orc_e_bwd.argtypes = [i] * 5 + [p] * 5 + [d, p, p, p, p]
         _lib.orc_running_log_decay.argtypes = [p, ctypes.c_long, ctypes.c_long, p]
@@ -125,17 +125,26 @@ def step(q, k, v, a, S, z, normalize=True):
     return o, zeta
 
 
-def bwd_quadratic(q, k, v, a, dO, normalize=True):
-    """Gradients of the quadratic form (no initial state). Returns (dq, dk, dv, da)."""
-    q, k, v, a, dO = map(_f64, (q, k, v, a, dO))
+def bwd_quadratic(q, k, v, a, dO, normalize=True, o=None, Z=None):
+    """Gradients of the quadratic form (no initial state). Returns (dq, dk, dv, da).
+
+    With o and Z given (normalised only), the backward uses them in place of the forward
+    values it would recompute: the kernel boundary's backward takes o and Z as inputs, and
+    this evaluates it as a function of those inputs (e.g. at a forward output that was
+    rounded to fp32)."""
+    q, k, v, a, dO, o, Z = map(_f64, (q, k, v, a, dO, o, Z))
     B, H, T, d = q.shape
     dv = v.shape[-1]
+    if (o is None) != (Z is None):
+        raise ValueError("give both o and Z, or neither")
+    if o is not None and (o.shape != (B, H, T, dv) or Z.shape != (B, H, T)):
+        raise ValueError("o must be (B,H,T,dv) and Z (B,H,T)")
     dq = np.zeros_like(q)
     dk = np.zeros_like(k)
     dvv = np.zeros_like(v)
     da = np.zeros_like(a)
     _load().orc_bwd_quadratic(B, H, T, d, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(dO),
-                              int(normalize), _ptr(dq), _ptr(dk), _ptr(dvv), _ptr(da))
+                              int(normalize), _ptr(o), _ptr(Z), _ptr(dq), _ptr(dk), _ptr(dvv), _ptr(da))
     return dq, dk, dvv, da
 
 

@@ -221,7 +221,7 @@ void orc_step(int N, int H, int d, int dv,
  */
 void orc_bwd_quadratic(int B, int H, int T, int d, int dv,
                        const double* q, const double* k, const double* v, const double* a,
-                       const double* dO, int normalize,
+                       const double* dO, int normalize, const double* o_in, const double* Z_in,
                        double* dq, double* dk, double* dvv, double* da) {
     long BH = (long)B * H;
     for (long bh = 0; bh < BH; ++bh) {
@@ -238,8 +238,15 @@ void orc_bwd_quadratic(int B, int H, int T, int d, int dv,
         double* rowsum = (double*)malloc(sizeof(double) * (size_t)(T + 1));
         double* colsum = (double*)malloc(sizeof(double) * (size_t)(T + 1));
         running_log_decay(ab, T, cum);
-        /* forward values of this head */
-        orc_fwd_quadratic(1, 1, T, d, dv, qb, kb, vb, ab, NULL, NULL, normalize, o, Zs);
+        /* forward values of this head: recomputed, or (o_in, Z_in non-NULL) the ones the caller
+           gives -- the backward of the kernel boundary takes o and Z as inputs (App. C), and with
+           given values it is that function of them */
+        if (o_in && Z_in) {
+            memcpy(o, o_in + bh * T * dv, sizeof(double) * (size_t)(T * dv));
+            memcpy(Zs, Z_in + bh * T, sizeof(double) * (size_t)T);
+        } else {
+            orc_fwd_quadratic(1, 1, T, d, dv, qb, kb, vb, ab, NULL, NULL, normalize, o, Zs);
+        }
         for (long i = 0; i < T; ++i) {
             if (normalize) {
                 double zi = Zs[i];

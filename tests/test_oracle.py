@@ -277,6 +277,39 @@ def test_gradients_vs_torch_autograd(normalize):
         assert relmax(g, ref.numpy()) < 1e-10
 
 
+def test_backward_at_given_forward_values_vs_torch_autograd():
+    """The normalised backward as a function of the forward values it is given (the kernel
+    boundary's backward takes o and Z as inputs, App. C): with o^g, Z^g held fixed, its
+    gradients are those of F = sum_i (dO_i . N_i - (dO_i . o^g_i) Z_i) / Z^g_i, N_i and Z_i the
+    weighted sums of the quadratic form, which torch fp64 autograd differentiates directly.
+    Pinned at perturbed o^g, Z^g (where it differs from the plain backward) and at the exact
+    ones (where it must equal it)."""
+    q, k, v, a = small_case(B=1, H=2, T=40, d=5, dv=4, seed=51)
+    rng = np.random.default_rng(52)
+    dO = rng.standard_normal(v.shape)
+    o, Z = oracle.fwd_quadratic(q, k, v, a, True)
+    exact = oracle.bwd_quadratic(q, k, v, a, dO, True)
+    same = oracle.bwd_quadratic(q, k, v, a, dO, True, o=o, Z=Z)
+    for x, y in zip(same, exact):
+        assert np.array_equal(x, y)
+    og = o + 1e-2 * rng.standard_normal(o.shape)
+    Zg = Z * (1 + 1e-2 * rng.standard_normal(Z.shape))
+    got = oracle.bwd_quadratic(q, k, v, a, dO, True, o=og, Z=Zg)
+    tq, tk, tv, ta = (torch.tensor(x, requires_grad=True) for x in (q, k, v, a))
+    cum = torch.cumsum(-torch.nn.functional.softplus(ta), -1)
+    T = q.shape[2]
+    causal = torch.tril(torch.ones(T, T, dtype=torch.bool))
+    diff = torch.where(causal, cum[..., :, None] - cum[..., None, :], torch.tensor(-math.inf, dtype=torch.float64))
+    W = torch.exp(diff) * (tq @ tk.transpose(-1, -2)) ** 2
+    N, Zs = W @ tv, W.sum(-1)
+    tdO, tog, tZg = torch.tensor(dO), torch.tensor(og), torch.tensor(Zg)
+    F = (((tdO * N).sum(-1) - (tdO * tog).sum(-1) * Zs) / tZg).sum()
+    F.backward()
+    for g, ref in zip(got, (tq.grad, tk.grad, tv.grad, ta.grad)):
+        assert relmax(g, ref.numpy()) < 1e-10
+    assert relmax(got[0], exact[0]) > 1e-4   # the given values do enter
+
+
 @pytest.mark.parametrize("variant", ["norm", "raw", "e"])
 def test_first_token_decay_gradient_is_zero(variant):
     """Shifting a_0 shifts every cumA_t equally, and only differences of cumA enter
