@@ -50,7 +50,7 @@ static int make_problem(int B, int H, int T, int d, int dv, int chunk, int dtype
 
 static size_t state_floats(const Problem& p) { return (size_t)p.d * (p.dv + 1) * p.d; }
 
-struct FwdWs { size_t Aloc, g, states, zx, ops, total; };
+struct FwdWs { size_t Aloc, g, states, zx, amax, ops, total; };
 static FwdWs plan_fwd(const Problem& p) {
     Carve c;
     FwdWs w{};
@@ -59,6 +59,7 @@ static FwdWs plan_fwd(const Problem& p) {
     if (p.tc) {   // fp16 value states [BH][NC][2][4096][64] + fp32 normaliser states [BH][NC][4096]
         w.states = c.take(2 * 2 * (size_t)p.BH() * p.NC * 4096 * 64);
         w.zx = c.take(sizeof(float) * (size_t)p.BH() * p.NC * 4096);
+        w.amax = c.take(sizeof(unsigned) * 4 * (size_t)p.BH());   // operand maxima of the scan
         w.ops = c.take(6 * (size_t)p.BH() * p.Tp() * 64);   // scan operand blocks (scratch)
     } else {
         w.states = c.take(sizeof(float) * p.BH() * p.NC * state_floats(p));
@@ -67,16 +68,19 @@ static FwdWs plan_fwd(const Problem& p) {
     return w;
 }
 
-struct BwdWs { size_t Aloc, g, states, dstates, dY, rowterm, dcum, zx, dzx, sscale, zeta, ucol, zmax, ops, total; };
+struct BwdWs {
+    size_t Aloc, g, states, dstates, dY, rowterm, dcum, zx, dzx, sscale, zeta, ucol, zmax, amax_f, amax_r, ops, total;
+};
 static BwdWs plan_bwd(const Problem& p) {
     Carve c;
     BwdWs w{};
     w.Aloc = c.take(sizeof(float) * p.BH() * p.Tp());
     w.g = c.take(sizeof(float) * p.BH() * p.NC);
-    if (p.tc) {   // the prefix Aloc, g, states, zx is laid out exactly as plan_fwd's
+    if (p.tc) {   // the prefix Aloc, g, states, zx, amax_f is laid out exactly as plan_fwd's
         const size_t planes = 2 * 2 * (size_t)p.BH() * p.NC * 4096 * 64;   // two fp16 planes per slot
         w.states = c.take(planes);
         w.zx = c.take(sizeof(float) * (size_t)p.BH() * p.NC * 4096);
+        w.amax_f = c.take(sizeof(unsigned) * 4 * (size_t)p.BH());
         w.dstates = c.take(planes);
         w.dzx = c.take(sizeof(float) * (size_t)p.BH() * p.NC * 4096);
         w.sscale = c.take(sizeof(float) * (size_t)p.BH() * p.NC);
@@ -85,6 +89,7 @@ static BwdWs plan_bwd(const Problem& p) {
         w.ucol = c.take(sizeof(float) * p.BH() * p.T);
         w.rowterm = c.take(sizeof(float) * p.BH() * p.T);
         w.dcum = c.take(sizeof(float) * p.BH() * p.T);
+        w.amax_r = c.take(sizeof(unsigned) * 4 * (size_t)p.BH());
         w.ops = c.take(6 * (size_t)p.BH() * p.Tp() * 64);   // scan operand blocks (scratch)
         w.total = c.off;
         return w;
@@ -171,6 +176,40 @@ struct TraceScope {
         TM2_CK(call);                        \
     } while (0)
 
+// ---- the 2Mamba-E forward, shared by tm2e_forward and tm2e_forward_noalloc ----------------
+int e_forward_check(const void* q, const void* k, const void* v, const float* a, const void* o, const float* lse,
+                    int B, int H, int T, int d, int dv, float scale, int dtype, Problem& p) {
+    int st = make_problem(B, H, T, d, dv, 0, dtype, 0, p);
+    if (st != TM2_OK) return st;
+    if (!(scale == scale) || scale == 0.f) return TM2_ERR_INVALID_ARG;
+    if (p.BH() == 0 || T == 0) return TM2_OK;
+    if (!q || !k || !v || !a || !o || !lse) return TM2_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, a, o, lse};
+    for (const void* x : ptrs)
+        if (!aligned16(x)) return TM2_ERR_ALIGNMENT;
+    return TM2_OK;
+}
+
+size_t e_forward_scratch_bytes(const Problem& p) { return plan_e(p, false).total; }
+
+int e_forward_run(const Problem& p, const void* q, const void* k, const void* v, const float* a, void* o, float* lse,
+                  float scale, void* ws, cudaStream_t s) {
+    const EWs w = plan_e(p, false);
+    float* Aloc = at<float>(ws, w.Aloc);
+    float* g = at<float>(ws, w.g);
+    float* cum = at<float>(ws, w.cum);
+    float* cum_lo = at<float>(ws, w.cum_lo);
+    TM2_RUN("decay_chunk", launch_decay(p, a, Aloc, g, s));
+    TM2_RUN("global_cumsum", launch_global_cumsum(p, Aloc, g, cum, cum_lo, s));
+    if (p.dtype == TM2_BF16 && p.d == 64 && p.dv == 64)
+        TM2_RUN("tc_e_fwd", tc_e_fwd(p, q, k, v, cum, cum_lo, scale, (float*)o, lse, s));
+    else
+        TM2_RUN("e_fwd", simt_e_fwd(p, q, k, v, cum, cum_lo, scale, o, lse, s));
+    return TM2_OK;
+}
+
+void record_cuda_error(cudaError_t e) { g_last_cuda_error = (int)e; }
+
 }  // namespace tm2
 
 using namespace tm2;
@@ -230,13 +269,16 @@ int tm2_forward(const void* q, const void* k, const void* v, const float* a, con
     TM2_RUN("decay_chunk", launch_decay(p, a, Aloc, g, s));
     if (p.tc) {
         float* zx = at<float>(ws, w.zx);
+        unsigned* amax = at<unsigned>(ws, w.amax);
         void* ops = at<void>(ws, w.ops);
-        TM2_RUN("tc_scan_operands", launch_tc_scan_operands(p, false, k, v, Aloc, g, nullptr, nullptr, nullptr, ops, s));
+        TM2_RUN("head_absmax", launch_head_absmax(p, k, v, amax, true, s));
+        TM2_RUN("tc_scan_operands",
+                launch_tc_scan_operands(p, false, k, v, Aloc, g, nullptr, nullptr, nullptr, amax, ops, s));
         ScanIO io{};
-        io.rev = false; io.ops = ops; io.g = g; io.S0 = S0; io.z0 = z0;
+        io.rev = false; io.ops = ops; io.g = g; io.S0 = S0; io.z0 = z0; io.amax = amax;
         io.Sx = states; io.zx = zx; io.S_final = S_final; io.z_final = z_final;
         TM2_RUN("tc_state_scan_fwd", tc_state_scan(p, io, s));
-        TM2_RUN("tc_chunk_out", tc_chunk_out(p, q, k, v, Aloc, states, zx, (float*)o, Z, s));
+        TM2_RUN("tc_chunk_out", tc_chunk_out(p, q, k, v, Aloc, states, zx, amax, (float*)o, Z, s));
         return TM2_OK;
     }
     TM2_RUN("state_scan_fwd", simt_state_scan_fwd(p, k, v, Aloc, g, S0, z0, states, S_final, z_final, s));
@@ -282,24 +324,28 @@ int tm2_backward(const void* q, const void* k, const void* v, const float* a, co
         float* ucol = at<float>(ws, w.ucol);
         float* rowterm = at<float>(ws, w.rowterm);
         float* dcum = at<float>(ws, w.dcum);
+        unsigned* amax_f = at<unsigned>(ws, w.amax_f);
+        unsigned* amax_r = at<unsigned>(ws, w.amax_r);
         void* ops = at<void>(ws, w.ops);
         if (!reuse) {
             TM2_RUN("decay_chunk", launch_decay(p, a, Aloc, g, s));
-            TM2_RUN("tc_scan_operands", launch_tc_scan_operands(p, false, k, v, Aloc, g, nullptr, nullptr, nullptr, ops,
-                                                                s));
+            TM2_RUN("head_absmax", launch_head_absmax(p, k, v, amax_f, true, s));
+            TM2_RUN("tc_scan_operands",
+                    launch_tc_scan_operands(p, false, k, v, Aloc, g, nullptr, nullptr, nullptr, amax_f, ops, s));
             ScanIO f{};
-            f.rev = false; f.ops = ops; f.g = g; f.Sx = Sx; f.zx = zx;
+            f.rev = false; f.ops = ops; f.g = g; f.Sx = Sx; f.zx = zx; f.amax = amax_f;
             TM2_RUN("tc_state_scan_fwd", tc_state_scan(p, f, s));
         }
-        TM2_RUN("tc_dy_prep", launch_tc_dy_prep(p, (const float*)o, Z, dO, Aloc, zeta, ucol, rowterm, zmax, s));
-        TM2_RUN("tc_scan_operands", launch_tc_scan_operands(p, true, q, dO, Aloc, g, zeta, ucol, zmax, ops, s));
+        TM2_RUN("tc_dy_prep", launch_tc_dy_prep(p, (const float*)o, Z, dO, Aloc, zeta, ucol, rowterm, zmax, amax_r, s));
+        TM2_RUN("head_absmax", launch_head_absmax(p, q, dO, amax_r, false, s));
+        TM2_RUN("tc_scan_operands", launch_tc_scan_operands(p, true, q, dO, Aloc, g, zeta, ucol, zmax, amax_r, ops, s));
         ScanIO r{};
-        r.rev = true; r.ops = ops; r.g = g; r.zmax = zmax;
+        r.rev = true; r.ops = ops; r.g = g; r.zmax = zmax; r.amax = amax_r;
         r.Sx = dSx; r.zx = dzx; r.sscale = sscale;
         TM2_RUN("tc_state_scan_bwd", tc_state_scan(p, r, s));
-        TM2_RUN("tc_bwd_dq", tc_bwd_dq(p, q, k, v, dO, Aloc, zeta, ucol, Sx, zx, (float*)dq, s));
-        TM2_RUN("tc_bwd_dkdv", tc_bwd_dkdv(p, q, k, v, dO, Aloc, g, zeta, ucol, rowterm, dSx, dzx, sscale, (float*)dk,
-                                           (float*)dv, dcum, s));
+        TM2_RUN("tc_bwd_dq", tc_bwd_dq(p, q, k, v, dO, Aloc, zeta, ucol, Sx, zx, amax_f, (float*)dq, s));
+        TM2_RUN("tc_bwd_dkdv", tc_bwd_dkdv(p, q, k, v, dO, Aloc, g, zeta, ucol, rowterm, dSx, dzx, sscale, amax_r,
+                                           (float*)dk, (float*)dv, dcum, s));
         TM2_RUN("reverse_cumsum_da", launch_reverse_cumsum_da(p, a, dcum, nullptr, da, s));
         return TM2_OK;
     }
@@ -349,29 +395,11 @@ int tm2e_forward(const void* q, const void* k, const void* v, const float* a, vo
                  int B, int H, int T, int d, int dv, float scale, int dtype, void* ws,
                  size_t ws_bytes, void* stream) {
     Problem p;
-    int st = make_problem(B, H, T, d, dv, 0, dtype, 0, p);
+    int st = tm2::e_forward_check(q, k, v, a, o, lse, B, H, T, d, dv, scale, dtype, p);
+    if (st != TM2_OK || p.BH() == 0 || T == 0) return st;
+    st = check_ws(ws, ws_bytes, plan_e(p, false).total);
     if (st != TM2_OK) return st;
-    if (!(scale == scale) || scale == 0.f) return TM2_ERR_INVALID_ARG;
-    if (p.BH() == 0 || T == 0) return TM2_OK;
-    if (!q || !k || !v || !a || !o || !lse) return TM2_ERR_INVALID_ARG;
-    const void* ptrs[] = {q, k, v, a, o, lse};
-    for (const void* x : ptrs)
-        if (!aligned16(x)) return TM2_ERR_ALIGNMENT;
-    const EWs w = plan_e(p, false);
-    st = check_ws(ws, ws_bytes, w.total);
-    if (st != TM2_OK) return st;
-    cudaStream_t s = (cudaStream_t)stream;
-    float* Aloc = at<float>(ws, w.Aloc);
-    float* g = at<float>(ws, w.g);
-    float* cum = at<float>(ws, w.cum);
-    float* cum_lo = at<float>(ws, w.cum_lo);
-    TM2_RUN("decay_chunk", launch_decay(p, a, Aloc, g, s));
-    TM2_RUN("global_cumsum", launch_global_cumsum(p, Aloc, g, cum, cum_lo, s));
-    if (p.dtype == TM2_BF16 && p.d == 64 && p.dv == 64)
-        TM2_RUN("tc_e_fwd", tc_e_fwd(p, q, k, v, cum, cum_lo, scale, (float*)o, lse, s));
-    else
-        TM2_RUN("e_fwd", simt_e_fwd(p, q, k, v, cum, cum_lo, scale, o, lse, s));
-    return TM2_OK;
+    return tm2::e_forward_run(p, q, k, v, a, o, lse, scale, ws, (cudaStream_t)stream);
 }
 
 size_t tm2e_backward_workspace(int B, int H, int T, int d, int dv, int dtype) {

@@ -22,6 +22,20 @@ template <> TM2_DEV __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __floa
 TM2_DEV float softplus_f(float x) { return fmaxf(x, 0.f) + log1pf(__expf(-fabsf(x))); }
 TM2_DEV float sigmoid_f(float x) { return 1.f / (1.f + __expf(-x)); }
 
+// ---- power-of-two operand scales ---------------------------------------------------------
+// The factor 2^-e that brings a non-negative maximum m = f 2^e (f in [0.5, 1)) into [0.5, 1),
+// from m's fp32 bit pattern; 1 when m is 0, subnormal-free zero, infinite or NaN.  e is
+// clamped to [-40, 40], so products of a few such factors stay inside fp32.  Multiplying by
+// it is exact, so a value scaled on the way into a 16-bit operand and unscaled afterwards is
+// unchanged unless the unscaled value would have left the 16-bit range.
+TM2_DEV float pow2_scale(uint32_t maxbits) {
+    const float m = __uint_as_float(maxbits);
+    if (!(m > 0.f) || !(m < INFINITY)) return 1.f;
+    int e = (int)((maxbits >> 23) & 0xffu) - 126;
+    e = max(-40, min(40, e));
+    return __uint_as_float((uint32_t)(127 - e) << 23);
+}
+
 // ---- warp reductions -----------------------------------------------------------------
 TM2_DEV float warp_sum(float v) {
 #pragma unroll

@@ -69,6 +69,7 @@ struct ScanIO {
     float* sscale;         // reverse only: [BH][NC] scale of each exported slot
     float* S_final;        // forward only, optional
     float* z_final;        // forward only, optional
+    const unsigned* amax;  // [BH][4] operand maxima of this walk (see launch_tc_scan_operands)
 };
 cudaError_t tc_state_scan(const Problem& p, const ScanIO& io, cudaStream_t s);
 
@@ -78,29 +79,41 @@ cudaError_t tc_state_scan(const Problem& p, const ScanIO& io, cudaStream_t s);
 // w_t val_t[col]), row 128 = w_t zc_t, rows 129-135 zero.  Forward: key = k, val = v,
 // w = exp(g_c - A_t), zc = 1.  Reverse: key = q, val = dO, w = exp(A_t) zeta_t / zmax_c,
 // zc = ucol_t.
+// The key and value operands (and the reverse walk's normaliser row) are multiplied by the
+// powers of two pow2_scale(amax[bh][0]), pow2_scale(amax[bh][1]) (and pow2_scale(amax[bh][2])),
+// so the walk's states come out multiplied by ks^2 vs (value columns) and ks^2 zs (normaliser).
 constexpr int TC_OPS_ROWS = 136;
 cudaError_t launch_tc_scan_operands(const Problem& p, bool rev, const void* key, const void* val, const float* Aloc,
                                     const float* g, const float* zeta, const float* ucol, const float* zmax,
-                                    void* ops, cudaStream_t s);
+                                    const unsigned* amax, void* ops, cudaStream_t s);
+
+// amax[bh][0], amax[bh][1] (fp32 bits) = the largest |x|, |y| of head bh of two bf16 tensors
+// (BH,T,64); zero_first clears amax[BH][4] first (otherwise the maxima combine with it).
+cudaError_t launch_head_absmax(const Problem& p, const void* x, const void* y, unsigned* amax, bool zero_first,
+                               cudaStream_t s);
 
 // Backward preparation: zeta = 1/Z (or 1), ucol = -dO.o (or 0), rowterm = 0 (or dO.o),
-// all (BH,T) fp32, and zmax (BH,NC) = per-chunk max of exp(A_i) zeta_i.
+// all (BH,T) fp32, and zmax (BH,NC) = per-chunk max of exp(A_i) zeta_i.  Clears amax[BH][4]
+// and sets amax[bh][2] to the largest |ucol| of the head (fp32 bits).
 cudaError_t launch_tc_dy_prep(const Problem& p, const float* o, const float* Z, const void* dO, const float* Aloc,
-                              float* zeta, float* ucol, float* rowterm, float* zmax, cudaStream_t s);
+                              float* zeta, float* ucol, float* rowterm, float* zmax, unsigned* amax, cudaStream_t s);
 
-// Gradient kernels (tm2_tc_dq.cu, tm2_tc_dkdv.cu).  dq: Sx/zx are the forward scan's states; dk, dv, dcum:
-// dSx/dzx/sscale the reverse scan's.  All outputs (BH,T,·) fp32.
+// Gradient kernels (tm2_tc_dq.cu, tm2_tc_dkdv.cu).  dq: Sx/zx are the forward scan's states
+// (amax_f its operand maxima); dk, dv, dcum: dSx/dzx/sscale the reverse scan's (amax_r).  All
+// outputs (BH,T,·) fp32.
 cudaError_t tc_bwd_dq(const Problem& p, const void* q, const void* k, const void* v, const void* dO, const float* Aloc,
-                      const float* zeta, const float* ucol, const void* Sx, const float* zx, float* dq, cudaStream_t s);
+                      const float* zeta, const float* ucol, const void* Sx, const float* zx, const unsigned* amax_f,
+                      float* dq, cudaStream_t s);
 cudaError_t tc_bwd_dkdv(const Problem& p, const void* q, const void* k, const void* v, const void* dO,
                         const float* Aloc, const float* g, const float* zeta, const float* ucol, const float* rowterm,
-                        const void* dSx, const float* dzx, const float* sscale, float* dk, float* dv, float* dcum,
-                        cudaStream_t s);
+                        const void* dSx, const float* dzx, const float* sscale, const unsigned* amax_r, float* dk,
+                        float* dv, float* dcum, cudaStream_t s);
 
 // Per-chunk output (intra-chunk squared masked scores and the readout of the state
-// entering the chunk, slot c of Sx/zx from tc_state_scan): o (BH,T,64) fp32, Z optional.
+// entering the chunk, slot c of Sx/zx from tc_state_scan, whose operand maxima are amax):
+// o (BH,T,64) fp32, Z optional.
 cudaError_t tc_chunk_out(const Problem& p, const void* q, const void* k, const void* v, const float* Aloc,
-                         const void* Sx, const float* zx, float* o, float* Z, cudaStream_t s);
+                         const void* Sx, const float* zx, const unsigned* amax, float* o, float* Z, cudaStream_t s);
 
 // ---- decode --------------------------------------------------------------------------
 cudaError_t launch_decode_step(int N, int H, int d, int dv, int dtype, bool normalize,
@@ -108,6 +121,18 @@ cudaError_t launch_decode_step(int N, int H, int d, int dv, int dtype, bool norm
                                float* S, float* z, void* o, float* Z, cudaStream_t s);
 
 // ---- 2Mamba-E ----------------------------------------------------------------------
+// The forward entry points' shared steps (tm2_api.cu): argument checks (fills p; TM2_OK with
+// p.BH() == 0 or T == 0 means nothing to do), the scratch size, and the launch sequence over a
+// scratch area of that size (the tensor-core kernel for bf16 with d = dv = 64, the CUDA-core
+// kernel otherwise), which traces its launches and records a failing launch's CUDA error for
+// tm2_last_cuda_error().
+int e_forward_check(const void* q, const void* k, const void* v, const float* a, const void* o, const float* lse,
+                    int B, int H, int T, int d, int dv, float scale, int dtype, Problem& p);
+size_t e_forward_scratch_bytes(const Problem& p);
+int e_forward_run(const Problem& p, const void* q, const void* k, const void* v, const float* a, void* o, float* lse,
+                  float scale, void* ws, cudaStream_t s);
+// Records e as the calling thread's last CUDA error (read back by tm2_last_cuda_error()).
+void record_cuda_error(cudaError_t e);
 // 2Mamba-E forward on the tensor cores (tm2_tc_e.cu): bf16, d = dv = 64; cum = global running
 // sum of -softplus(a) (BH, T); o (BH, T, 64) and lse (BH, T) fp32.
 cudaError_t tc_e_fwd(const Problem& p, const void* q, const void* k, const void* v, const float* cum,

@@ -24,6 +24,32 @@ TM2_DEV float block_inclusive_scan(float v, float* wsum /* >= 32 floats */) {
     return s;
 }
 
+// The same in fp64 (the long reverse sums of the A-mask gradient).
+TM2_DEV double block_inclusive_scan_d(double v, double* wsum /* >= 32 doubles */) {
+    const int t = threadIdx.x, w = t >> 5, lane = t & 31, nw = (blockDim.x + 31) >> 5;
+    double s = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const double u = __shfl_up_sync(0xffffffffu, s, o);
+        if (lane >= o) s += u;
+    }
+    if (lane == 31) wsum[w] = s;
+    __syncthreads();
+    if (w == 0) {
+        double x = lane < nw ? wsum[lane] : 0.0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const double u = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += u;
+        }
+        wsum[lane] = x;
+    }
+    __syncthreads();
+    if (w > 0) s += wsum[w - 1];
+    __syncthreads();
+    return s;
+}
+
 // grid (NC, BH), block C threads: one chunk per block.
 __global__ void decay_chunk_kernel(const float* __restrict__ a, float* __restrict__ Aloc,
                                    float* __restrict__ g, int T, int C, int NC) {
@@ -44,20 +70,25 @@ cudaError_t launch_decay(const Problem& p, const float* a, float* Aloc, float* g
     return cudaGetLastError();
 }
 
-// grid BH, block 256.  Chunk offsets are summed in fp64 so that only the final
-// rounding to fp32 enters cum.
-__global__ void global_cumsum_kernel(const float* __restrict__ Aloc, const float* __restrict__ g,
-                                     float* __restrict__ cum, float* __restrict__ cum_lo, int T, int C, int NC) {
+// grid BH, block 256.  Chunk offsets are summed in fp64 (a block-wide scan over the chunk
+// totals, 256 chunks per pass) so that only the final rounding to fp32 enters cum.
+__global__ void __launch_bounds__(256) global_cumsum_kernel(const float* __restrict__ Aloc, const float* __restrict__ g,
+                                                            float* __restrict__ cum, float* __restrict__ cum_lo, int T,
+                                                            int C, int NC) {
     extern __shared__ double off[];   // NC doubles
+    __shared__ double wsum[32];
     const long bh = blockIdx.x;
-    if (threadIdx.x == 0) {
-        double acc = 0.0;
-        for (int c = 0; c < NC; ++c) {
-            off[c] = acc;
-            acc += (double)g[bh * NC + c];
-        }
+    double carry = 0.0;
+    for (int c0 = 0; c0 < NC; c0 += blockDim.x) {
+        const int c = c0 + (int)threadIdx.x;
+        const double gc = c < NC ? (double)g[bh * NC + c] : 0.0;
+        const double incl = block_inclusive_scan_d(gc, wsum) + carry;
+        if (c < NC) off[c] = incl - gc;   // exclusive: the offset at the start of chunk c
+        if (threadIdx.x == blockDim.x - 1) wsum[0] = incl;
+        __syncthreads();
+        carry = wsum[0];
+        __syncthreads();
     }
-    __syncthreads();
     for (int t = threadIdx.x; t < T; t += blockDim.x) {
         const double x = off[t / C] + (double)Aloc[bh * (long)NC * C + t];
         const float hi = (float)x;
@@ -78,20 +109,22 @@ cudaError_t launch_global_cumsum(const Problem& p, const float* Aloc, const floa
     return cudaGetLastError();
 }
 
-// grid BH, block 1024: walks the sequence from its end in tiles of 1024.
+// grid BH, block 1024: walks the sequence from its end in tiles of 1024.  The running sum is
+// kept in fp64: over thousands of tokens the terms largely cancel (their total is zero without
+// an initial state), and an fp32 sum would leave a rounding error comparable to the result.
 __global__ void __launch_bounds__(1024) reverse_cumsum_da_kernel(
     const float* __restrict__ a, const float* __restrict__ row, const float* __restrict__ col,
     float* __restrict__ da, int T) {
-    __shared__ float wsum[32];
-    __shared__ float carry_s;
+    __shared__ double wsum[32];
+    __shared__ double carry_s;
     const long bh = blockIdx.x;
-    float carry = 0.f;
+    double carry = 0.0;
     for (int base = T - 1; base >= 0; base -= blockDim.x) {
         const int u = base - (int)threadIdx.x;   // thread 0 holds the latest token of the tile
-        float x = 0.f;
-        if (u >= 0) x = row[bh * T + u] - (col ? col[bh * T + u] : 0.f);
-        float s = block_inclusive_scan(x, wsum) + carry;
-        if (u >= 0) da[bh * T + u] = -sigmoid_f(a[bh * T + u]) * s;
+        double x = 0.0;
+        if (u >= 0) x = (double)row[bh * T + u] - (col ? (double)col[bh * T + u] : 0.0);
+        const double s = block_inclusive_scan_d(x, wsum) + carry;
+        if (u >= 0) da[bh * T + u] = -sigmoid_f(a[bh * T + u]) * (float)s;
         if (threadIdx.x == blockDim.x - 1) carry_s = s;
         __syncthreads();
         carry = carry_s;
@@ -149,13 +182,13 @@ __global__ void __launch_bounds__(256) tc_dy_prep_kernel(const float* __restrict
                                                          const __nv_bfloat16* __restrict__ dO,
                                                          const float* __restrict__ Aloc, float* __restrict__ zeta,
                                                          float* __restrict__ ucol, float* __restrict__ rowterm,
-                                                         float* __restrict__ zmax, int T, int C, int NC,
-                                                         bool normalize) {
-    __shared__ float wmax[8];
+                                                         float* __restrict__ zmax, unsigned* __restrict__ amax, int T,
+                                                         int C, int NC, bool normalize) {
+    __shared__ float wmax[8], wumax[8];
     const int c = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int sub = lane >> 3, l8 = lane & 7;   // four tokens per warp pass, eight lanes per token
     const long bh = blockIdx.y;
-    float mx = 0.f;
+    float mx = 0.f, umx = 0.f;
     for (int j0 = warp * 4; j0 < C; j0 += 32) {
         const long t = (long)c * C + j0 + sub;
         const bool in = t < T;
@@ -183,39 +216,113 @@ __global__ void __launch_bounds__(256) tc_dy_prep_kernel(const float* __restrict
                 rowterm[tok] = normalize ? 0.f : D;
             }
             mx = fmaxf(mx, __expf(Aloc[bh * (long)NC * C + t]) * ze);
+            if (normalize) umx = fmaxf(umx, fabsf(D));
         }
     }
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-    if (lane == 0) wmax[warp] = mx;
+    umx = fmaxf(umx, __shfl_xor_sync(0xffffffffu, umx, 8));
+    umx = fmaxf(umx, __shfl_xor_sync(0xffffffffu, umx, 16));
+    if (lane == 0) {
+        wmax[warp] = mx;
+        wumax[warp] = umx;
+    }
     __syncthreads();
     if (threadIdx.x == 0) {
-        float m = 0.f;
-        for (int w = 0; w < 8; ++w) m = fmaxf(m, wmax[w]);
+        float m = 0.f, um = 0.f;
+        for (int w = 0; w < 8; ++w) {
+            m = fmaxf(m, wmax[w]);
+            um = fmaxf(um, wumax[w]);
+        }
         zmax[bh * NC + c] = m > 0.f ? m : 1.f;
+        atomicMax(amax + bh * 4 + 2, __float_as_uint(um));   // largest |ucol| of the head
     }
 }
 
 cudaError_t launch_tc_dy_prep(const Problem& p, const float* o, const float* Z, const void* dO, const float* Aloc,
-                              float* zeta, float* ucol, float* rowterm, float* zmax, cudaStream_t s) {
+                              float* zeta, float* ucol, float* rowterm, float* zmax, unsigned* amax, cudaStream_t s) {
+    cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(unsigned) * 4 * (size_t)p.BH(), s);
+    if (e != cudaSuccess) return e;
     dim3 grid(p.NC, (unsigned)p.BH());
-    tc_dy_prep_kernel<<<grid, 256, 0, s>>>(o, Z, (const __nv_bfloat16*)dO, Aloc, zeta, ucol, rowterm, zmax, p.T, p.C,
-                                          p.NC, p.normalize);
+    tc_dy_prep_kernel<<<grid, 256, 0, s>>>(o, Z, (const __nv_bfloat16*)dO, Aloc, zeta, ucol, rowterm, zmax, amax, p.T,
+                                          p.C, p.NC, p.normalize);
+    return cudaGetLastError();
+}
+
+// Largest |x| of each (b, h) of two bf16 tensors (BH, T, 64), max-combined into amax[bh * 4]
+// and amax[bh * 4 + 1] as fp32 bit patterns (non-negative floats order like their bits).
+// grid (ceil(T / 128), BH), 256 threads: 128 tokens x 8 sixteen-byte pieces per block.
+TM2_DEV uint32_t bf16x8_absmax_bits(uint4 a) {
+    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) m = max(m, max(w[i] & 0x7fffu, (w[i] >> 16) & 0x7fffu));
+    return m << 16;
+}
+__global__ void __launch_bounds__(256) head_absmax_kernel(const __nv_bfloat16* __restrict__ x,
+                                                          const __nv_bfloat16* __restrict__ y,
+                                                          unsigned* __restrict__ amax, int T) {
+    __shared__ uint32_t red[2][8];
+    const long bh = blockIdx.y;
+    const long t0 = (long)blockIdx.x * 128;
+    uint32_t mx = 0, my = 0;
+    for (int e = threadIdx.x; e < 1024; e += 256) {
+        const long t = t0 + (e >> 3);
+        if (t < T) {
+            const long off = (bh * T + t) * 64 + 8 * (e & 7);
+            mx = max(mx, bf16x8_absmax_bits(*reinterpret_cast<const uint4*>(x + off)));
+            my = max(my, bf16x8_absmax_bits(*reinterpret_cast<const uint4*>(y + off)));
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        my = max(my, __shfl_xor_sync(0xffffffffu, my, o));
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) {
+        red[0][warp] = mx;
+        red[1][warp] = my;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < 8; ++w) {
+            mx = max(mx, red[0][w]);
+            my = max(my, red[1][w]);
+        }
+        atomicMax(amax + bh * 4, mx);
+        atomicMax(amax + bh * 4 + 1, my);
+    }
+}
+
+cudaError_t launch_head_absmax(const Problem& p, const void* x, const void* y, unsigned* amax, bool zero_first,
+                               cudaStream_t s) {
+    if (zero_first) {
+        cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(unsigned) * 4 * (size_t)p.BH(), s);
+        if (e != cudaSuccess) return e;
+    }
+    dim3 grid((unsigned)((p.T + 127) / 128), (unsigned)p.BH());
+    head_absmax_kernel<<<grid, 256, 0, s>>>((const __nv_bfloat16*)x, (const __nv_bfloat16*)y, amax, p.T);
     return cudaGetLastError();
 }
 
 // Operands of the tensor-core chunk-state scan, one block of 256 threads per 64-token stage
 // of one (b, h), written as one [136][64] fp16 block per stage (token j = stage*64 + column):
-//   rows   0-63 : [n][j]   = fp16(key_j[n])         (the key block, transposed)
-//   rows  64-127: [col][j] = fp16(w_j val_j[col])   (the weighted values, transposed)
-//   row   128   : [j]      = fp16(w_j zc_j)         (the normaliser column)
+//   rows   0-63 : [n][j]   = fp16(ks key_j[n])         (the key block, transposed)
+//   rows  64-127: [col][j] = fp16(vs w_j val_j[col])   (the weighted values, transposed)
+//   row   128   : [j]      = fp16(zs w_j zc_j)         (the normaliser column)
 //   rows 129-135: 0
 // with the scan's weight w_t = exp(g_c - A_t), zc = 1 (forward walk) or
 // w_t = exp(A_t) zeta_t / zmax_c, zc = ucol_t (reverse walk); tokens past T give zeros.
+// ks, vs, zs are the powers of two that bring the head's largest |key|, |val| and (reverse
+// walk) |ucol| into [0.5, 1) (amax, from launch_head_absmax and launch_tc_dy_prep; zs = 1
+// forward): the fp16 operands and the products k[m] k[n] then sit in fp16's normal range
+// whatever the scale of the inputs, and the state comes out multiplied by ks^2 vs exactly.
 __global__ void __launch_bounds__(256) tc_scan_operands_kernel(
     const __nv_bfloat16* __restrict__ key, const __nv_bfloat16* __restrict__ val, const float* __restrict__ Aloc,
     const float* __restrict__ g, const float* __restrict__ zeta, const float* __restrict__ ucol,
-    const float* __restrict__ zmax, __half* __restrict__ ops, int T, int C, int NC, int rev) {
+    const float* __restrict__ zmax, const unsigned* __restrict__ amax, __half* __restrict__ ops, int T, int C, int NC,
+    int rev) {
     __shared__ float sk[64][65];
     __shared__ float sv[64][65];
     __shared__ float sw[64], szc[64];
@@ -223,6 +330,8 @@ __global__ void __launch_bounds__(256) tc_scan_operands_kernel(
     const long bh = blockIdx.y;
     const int Tp = NC * C, c = (st * 64) / C;
     const long t0 = (long)st * 64;
+    const float ks = pow2_scale(amax[bh * 4]), vs = pow2_scale(amax[bh * 4 + 1]);
+    const float zs = rev ? pow2_scale(amax[bh * 4 + 2]) : 1.f;
     if (tid < 64) {
         const long t = t0 + tid;
         const float A = Aloc[bh * Tp + t];
@@ -252,8 +361,8 @@ __global__ void __launch_bounds__(256) tc_scan_operands_kernel(
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const float2 kk = __bfloat1622float2(kb[u]), vv = __bfloat1622float2(vb[u]);
-                kf[2 * u] = kk.x; kf[2 * u + 1] = kk.y;
-                vf[2 * u] = vv.x * sw[j]; vf[2 * u + 1] = vv.y * sw[j];
+                kf[2 * u] = kk.x * ks; kf[2 * u + 1] = kk.y * ks;
+                vf[2 * u] = vv.x * vs * sw[j]; vf[2 * u + 1] = vv.y * vs * sw[j];
             }
         } else {
 #pragma unroll
@@ -288,16 +397,16 @@ __global__ void __launch_bounds__(256) tc_scan_operands_kernel(
     // the normaliser row and the zero rows after it
     for (int e = tid; e < 8 * 64; e += 256) {
         const int r = e >> 6, j = e & 63;
-        blk[(128 + r) * 64 + j] = __float2half_rn(r == 0 ? sw[j] * szc[j] : 0.f);
+        blk[(128 + r) * 64 + j] = __float2half_rn(r == 0 ? zs * sw[j] * szc[j] : 0.f);
     }
 }
 
 cudaError_t launch_tc_scan_operands(const Problem& p, bool rev, const void* key, const void* val, const float* Aloc,
                                     const float* g, const float* zeta, const float* ucol, const float* zmax,
-                                    void* ops, cudaStream_t s) {
+                                    const unsigned* amax, void* ops, cudaStream_t s) {
     dim3 grid((unsigned)(p.Tp() / 64), (unsigned)p.BH());
     tc_scan_operands_kernel<<<grid, 256, 0, s>>>((const __nv_bfloat16*)key, (const __nv_bfloat16*)val, Aloc, g, zeta,
-                                                 ucol, zmax, (__half*)ops, p.T, p.C, p.NC, rev ? 1 : 0);
+                                                 ucol, zmax, amax, (__half*)ops, p.T, p.C, p.NC, rev ? 1 : 0);
     return cudaGetLastError();
 }
 

@@ -22,6 +22,9 @@
 // dkx[m] += k_j[4g+n'] U'_g, dvx[col] += k_j[4g+n'] U_g.  A tensor-core instruction costs about
 // the same for any N up to 256, so four slices per instruction keeps this part short.
 // A 17th product U'_z = K dzm^T (dzm[m][n] = dz[(m,n)]) adds the normaliser column.
+// The gradient state planes and normaliser states carry the reverse scan's operand scales
+// ks^2 vs (exact powers of two) on top of 1/Gamma_c; the inter-chunk terms are divided by
+// them together with the multiplication by Gamma_c.
 // The intra-chunk part follows in the same tensor memory: per 64-query block, s^T = K Q^T and
 // (u.Vt)^T = V dO^T (bf16), dSs^T and (W zeta)^T as bf16 hi + lo in tensor memory, then
 // dk += dSs^T Q and dv += (W zeta)^T dO.
@@ -70,6 +73,7 @@ struct Args {
     const float* rowterm; // [BH][T]
     const float* dzx;     // [BH][NC][4096] gradient normaliser states (unscaled)
     const float* sscale;  // [BH][NC] scale of the gradient state planes
+    const unsigned* amax; // [BH][4] the reverse scan's operand maxima (key, value, normaliser)
     float* dk;            // [BH][T][64]
     float* dv;            // [BH][T][64]
     float* dcum;          // [BH][T]
@@ -415,7 +419,9 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
             tmem_ld32(tmem + lane_base + TM_PARK + h * 64, dkx);
             tmem_ld32(tmem + lane_base + TM_PARK + h * 64 + 32, dvx);
             const float wj = __expf(gcv - Aj);
-            const float fk = 2.f * wj * gsc, fv = wj * gsc;
+            const float ks = pow2_scale(a.amax[bh * 4]), vs = pow2_scale(a.amax[bh * 4 + 1]);
+            const float gu = gsc / (ks * ks * vs);   // Gamma_c out of the planes' units (exact)
+            const float fk = 2.f * wj * gu, fv = wj * gu;
             float vdot = 0.f;
             const uint8_t* vrow = smem + SVH;
 #pragma unroll
@@ -449,8 +455,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
 
 cudaError_t tc_bwd_dkdv(const Problem& p, const void* q, const void* k, const void* v, const void* dO,
                         const float* Aloc, const float* g, const float* zeta, const float* ucol, const float* rowterm,
-                        const void* dSx, const float* dzx, const float* sscale, float* dk, float* dv, float* dcum,
-                        cudaStream_t s) {
+                        const void* dSx, const float* dzx, const float* sscale, const unsigned* amax_r, float* dk,
+                        float* dv, float* dcum, cudaStream_t s) {
     CUtensorMap tk, tv, tq, td, ts;
     const uint64_t BH = (uint64_t)p.BH(), T = (uint64_t)p.T;
     if (!make_tmap_bf16_3d(&tk, k, BH, T, 64, 128) || !make_tmap_bf16_3d(&tv, v, BH, T, 64, 128) ||
@@ -459,7 +465,7 @@ cudaError_t tc_bwd_dkdv(const Problem& p, const void* q, const void* k, const vo
         return cudaErrorInvalidValue;
     int* status = tc_status_ptr();
     if (!status) return cudaErrorInvalidValue;
-    Args a{Aloc, g, zeta, ucol, rowterm, dzx, sscale, dk, dv, dcum, status, p.T, p.NC, (int)p.Tp()};
+    Args a{Aloc, g, zeta, ucol, rowterm, dzx, sscale, amax_r, dk, dv, dcum, status, p.T, p.NC, (int)p.Tp()};
     cudaError_t e = cudaFuncSetAttribute(tc_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, BYTES);
     if (e != cudaSuccess) return e;
     dim3 grid(2 * p.NC, (unsigned)p.BH());

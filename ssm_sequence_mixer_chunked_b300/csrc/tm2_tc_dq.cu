@@ -16,6 +16,9 @@
 // for any N up to 256, so four slices per instruction is what keeps this part short; the
 // slices arrive one plane of one group (32 KB) per TMA request.  A 17th product
 // U_z = Q zm^T (zm[m][n] = z[(m, n)]) carries the normaliser column.
+// The state planes hold ks^2 vs S and the normaliser state ks^2 z (the forward scan's operand
+// scales, exact powers of two): the normaliser matrix is built times vs, so that both inter-chunk
+// terms carry ks^2 vs, and their sum is divided by it at the end.
 // The intra-chunk part follows in the same tensor memory: per 64-key block, s = Q K^T and
 // u.Vt = dO V^T (bf16 MMAs), dSs as bf16 hi + lo in tensor memory, dq += dSs K.
 // Warps 0-7 compute (warp w: tensor-memory lane quadrant w % 4, column half w / 4), warp 8
@@ -62,6 +65,7 @@ struct Args {
     const float* zeta;   // [BH][T]
     const float* ucol;   // [BH][T]
     const float* zx;     // [BH][NC][4096] forward normaliser states (slot c = entering chunk c)
+    const unsigned* amax;   // [BH][4] the forward scan's operand maxima (key, value)
     float* dq;           // [BH][T][64]
     int* status;
     int T, NC, Tp;
@@ -258,6 +262,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_cons
         const float Ai = sAv[i];
         const float ze = in ? a.zeta[bh * a.T + tok] : 0.f;
         const float uc = in ? a.ucol[bh * a.T + tok] : 0.f;
+        const float ks = pow2_scale(a.amax[bh * 4]), vs = pow2_scale(a.amax[bh * 4 + 1]);
+        const float un = 1.f / (ks * ks * vs);           // exact: a power of two
         int kg = 0;                                      // group-wait counter
         float4 zr[4];
         z_tiles_load(a.zx + (bh * NC + c) * 4096, threadIdx.x, zr);   // in flight during the tile wait
@@ -284,7 +290,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_cons
                 break;
             if (g == NG - 2) {   // group NG-2's products are done: its lo slot takes the normaliser matrix
                 const uint32_t zh = RING + slot_of(ZREQ) * RB;
-                z_tiles_store(smem + zh, smem + zh + 8192, zr, 1.f, threadIdx.x);
+                z_tiles_store(smem + zh, smem + zh + 8192, zr, vs, threadIdx.x);
                 fence_proxy_async();
                 mbar_arrive(smem_u32(&bar_zrdy));
             }
@@ -354,6 +360,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_cons
             tmem_ld32(tmem + lane_base + TM_DQ + h * 32, d0);
             if (in) {
                 const float f = 2.f * __expf(Ai);
+#pragma unroll
+                for (int k = 0; k < 32; ++k) dqx[k] *= un;
                 float4* dst = reinterpret_cast<float4*>(a.dq + (bh * a.T + tok) * 64 + h * 32);
 #pragma unroll
                 for (int u = 0; u < 8; ++u)
@@ -369,7 +377,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_cons
 }
 
 cudaError_t tc_bwd_dq(const Problem& p, const void* q, const void* k, const void* v, const void* dO, const float* Aloc,
-                      const float* zeta, const float* ucol, const void* Sx, const float* zx, float* dq, cudaStream_t s) {
+                      const float* zeta, const float* ucol, const void* Sx, const float* zx, const unsigned* amax_f,
+                      float* dq, cudaStream_t s) {
     CUtensorMap tq, td, tk, tv, ts;
     const uint64_t BH = (uint64_t)p.BH(), T = (uint64_t)p.T;
     if (!make_tmap_bf16_3d(&tq, q, BH, T, 64, 128) || !make_tmap_bf16_3d(&td, dO, BH, T, 64, 128) ||
@@ -378,7 +387,7 @@ cudaError_t tc_bwd_dq(const Problem& p, const void* q, const void* k, const void
         return cudaErrorInvalidValue;
     int* status = tc_status_ptr();
     if (!status) return cudaErrorInvalidValue;
-    Args a{Aloc, zeta, ucol, zx, dq, status, p.T, p.NC, (int)p.Tp()};
+    Args a{Aloc, zeta, ucol, zx, amax_f, dq, status, p.T, p.NC, (int)p.Tp()};
     cudaError_t e = cudaFuncSetAttribute(tc_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, BYTES);
     if (e != cudaSuccess) return e;
     dim3 grid(2 * p.NC, (unsigned)p.BH());

@@ -10,12 +10,17 @@
 // block: s = Q K^T by tcgen05.mma (M = N = 128, K = 64, bf16 tiles from TMA) into one of two
 // tensor-memory score buffers; the compute warps (row = tensor-memory lane, half h = 64 of
 // the block's keys) add the decay bias, mask, take the row maximum across both halves and
-// write P = exp(x - m) as bf16 into one of two tensor-memory P buffers; O += P V (P from
-// tensor memory, V MN-major from its tile).  The maximum is lazy: O and the row sums are
-// rescaled only when a block's maximum exceeds the one in use by more than 8 (so P <= e^8,
-// well inside bf16), which makes rescales rare.  The next block's QK^T overlaps this block's
-// softmax, and its softmax overlaps this block's PV.  The row sums add the bf16-rounded P
-// that the MMA uses, so o = O / l is exactly normalised for those weights.
+// write P = exp(x - m) as two bf16 terms, P_hi into one of two tensor-memory P buffers and
+// P_lo = bf16(P - P_hi) over the score columns the writing thread has already read;
+// O += P_hi V + P_lo V (P from tensor memory, V MN-major from its tile).  One bf16 rounding
+// of P costs 2^-9 relative per weight, which over a long undecayed context (a -> -inf:
+// thousands of keys of similar weight) puts o and the backward's dv past the 2e-2 bar;
+// hi + lo carries 16 bits.  The maximum is lazy: O and the row sums are rescaled only when a
+// block's maximum exceeds the one in use by more than 8 (so P <= e^8), which makes rescales
+// rare.  The next block's QK^T overlaps this block's softmax, and its softmax overlaps this
+// block's PV; because P_lo lives in the score buffer, the scores of block b+2 are issued once
+// the products of block b have completed.  The row sums add the rounded P_hi + P_lo that the
+// MMAs use, so o = O / l is exactly normalised for those weights.
 // Logits are kept in log2 units (x log2 e); the decay terms are taken relative to the running
 // sum at the tile's first query, so the fp32 differences stay small, and each block's key
 // terms are staged once in shared memory.  Only the diagonal block is masked.
@@ -147,6 +152,9 @@ __global__ void __launch_bounds__(THREADS, 1) tc_e_fwd_kernel(const __grid_const
                     if (!(ok = mbar_wait(smem_u32(&bar_full[st]), (uint32_t)(b / NS) & 1, a.status))) break;
                     if (b >= 2 && !(ok = mbar_wait(smem_u32(&bar_sfree[x]), (uint32_t)((b >> 1) - 1) & 1, a.status)))
                         break;
+                    // the buffer also holds P_lo of block b-2 until that block's products complete
+                    if (b >= 2 && !(ok = mbar_wait(smem_u32(&bar_pfree[x]), (uint32_t)((b >> 1) - 1) & 1, a.status)))
+                        break;
                     tc_fence_after();
                     const uint32_t kb = sb0 + SSTG + st * STAGE;
 #pragma unroll
@@ -161,9 +169,11 @@ __global__ void __launch_bounds__(THREADS, 1) tc_e_fwd_kernel(const __grid_const
                     tc_fence_after();
                     const uint32_t vb = sb0 + SSTG + st * STAGE + TILE;
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk)
-                        umma_bf16_ts(tmem + TM_O, tmem + TM_P + x * 64 + kk * 8,
-                                     sdesc_sw128_ex(vb + kk * 2048, 8192, 1024), IDESC_PV, (c > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < BK / 16; ++kk) {   // keys 16 kk .. +15: half kk / 4 of the block
+                        const uint64_t vd = sdesc_sw128_ex(vb + kk * 2048, 8192, 1024);
+                        umma_bf16_ts(tmem + TM_O, tmem + TM_P + x * 64 + kk * 8, vd, IDESC_PV, (c > 0 || kk > 0) ? 1u : 0u);
+                        umma_bf16_ts(tmem + TM_O, tmem + TM_S + x * 128 + (kk >> 2) * 64 + (kk & 3) * 8, vd, IDESC_PV, 1u);
+                    }
                     umma_commit(smem_u32(&bar_pfree[x]));
                     umma_commit(smem_u32(&bar_empty[st]));
                 }
@@ -266,23 +276,29 @@ __global__ void __launch_bounds__(THREADS, 1) tc_e_fwd_kernel(const __grid_const
                     m_used = bmax;
                 }
             }
-            // P = exp(x - m) in bf16 into P buffer x.  Its last reader, the product of block b-2, was
-            // issued before the scores of block b, and the commit that announced those scores
-            // completes only when every earlier MMA of the issuing thread has, so it is free.
-            uint32_t pk[32];
+            // P = exp(x - m) as P_hi (bf16) into P buffer x and P_lo = bf16(P - P_hi) over this
+            // thread's score columns 0-31 (all 64 of its scores are in registers).  The P buffer's
+            // last reader, the product of block b-2, was issued before the scores of block b, and
+            // the commit that announced those scores completes only when every earlier MMA of the
+            // issuing thread has, so it is free.
 #pragma unroll
-            for (int c2 = 0; c2 < 32; ++c2) {
-                float p0 = m_used == -INFINITY ? 0.f : exp2f(s[2 * c2] - m_used);
-                float p1 = m_used == -INFINITY ? 0.f : exp2f(s[2 * c2 + 1] - m_used);
-                const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
-                const float2 r2 = __bfloat1622float2(b2);
-                lsum += r2.x + r2.y;
-                pk[c2] = *reinterpret_cast<const uint32_t*>(&b2);
+            for (int r8 = 0; r8 < 4; ++r8) {
+                uint32_t ph[8], pl[8];
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    const int c2 = 8 * r8 + c8;
+                    const float p0 = m_used == -INFINITY ? 0.f : exp2f(s[2 * c2] - m_used);
+                    const float p1 = m_used == -INFINITY ? 0.f : exp2f(s[2 * c2 + 1] - m_used);
+                    const uint32_t h2 = pack_bf16x2(p0, p1);
+                    const float h0 = __uint_as_float(h2 << 16), h1 = __uint_as_float(h2 & 0xffff0000u);
+                    const uint32_t l2 = pack_bf16x2(p0 - h0, p1 - h1);
+                    lsum += (h0 + __uint_as_float(l2 << 16)) + (h1 + __uint_as_float(l2 & 0xffff0000u));
+                    ph[c8] = h2;
+                    pl[c8] = l2;
+                }
+                tmem_st8(tmem + lane_base + TM_P + x * 64 + h * 32 + 8 * r8, ph);
+                tmem_st8(tmem + lane_base + TM_S + x * 128 + h * 64 + 8 * r8, pl);
             }
-            tmem_st8(tmem + lane_base + TM_P + x * 64 + h * 32, pk);
-            tmem_st8(tmem + lane_base + TM_P + x * 64 + h * 32 + 8, pk + 8);
-            tmem_st8(tmem + lane_base + TM_P + x * 64 + h * 32 + 16, pk + 16);
-            tmem_st8(tmem + lane_base + TM_P + x * 64 + h * 32 + 24, pk + 24);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(smem_u32(&bar_pfull[x]));

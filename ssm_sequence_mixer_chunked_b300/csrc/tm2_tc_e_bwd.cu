@@ -11,10 +11,11 @@
 // (the 128-token tiles arrive by TMA in a 4-stage ring, two sub-blocks per stage):
 //  * keys (kd = true): per 64-query sub-block at or after the key tile, s^T = K Q^T and
 //    dP^T = V dO^T (tcgen05.mma, M = 128, N = 64) into one of three tensor-memory buffers; the
-//    compute warps form P^T (bf16) and dx^T as bf16 hi + lo (its sums over queries cancel, so
-//    one bf16 rounding would cost the 2e-2 bar), written back over the scores and dP they
-//    have read; then dv += P^T dO and dk += (dx_hi + dx_lo)^T Q with Q, dO MN-major straight
-//    from their tiles.
+//    compute warps form P^T and dx^T, each as bf16 hi + lo (the sums of dx over queries
+//    cancel, and a long undecayed context gives a key thousands of queries of similar weight,
+//    so one bf16 rounding of either would cost the 2e-2 bar), written back over the scores and
+//    dP they have read; then dv += (P_hi + P_lo)^T dO and dk += (dx_hi + dx_lo)^T Q with Q, dO
+//    MN-major straight from their tiles.
 //  * queries (kd = false): per 64-key sub-block at or before the query tile, s = Q K^T and
 //    dP = dO V^T, dx hi + lo, dq += dx K.
 // With three sub-block buffers the MMA thread issues the scores of sub-block s while the
@@ -47,10 +48,10 @@ constexpr int SRED = SSC + 2 * 4 * BT * 4;   // [2 halves][128]
 constexpr int SMEM_BYTES = SRED + 2 * BT * 4 + 1024;
 // tensor memory: sub-block buffer u at 128 u holds the scores (columns 0-63) and dP (64-127);
 // accumulators at 384 (dk or dq) and 448 (dv).  The warp of half h owns score columns
-// 32 h .. +31 and dP columns 64 + 32 h .. +31 of its lanes and writes, per 16 tokens
-// (round q of 2), P to score columns 32 h + 16 q .. +7, dx hi to the next 8 and dx lo to dP
-// columns 64 + 32 h + 8 q .. +7, all already read.  Column c of an operand holds tokens
-// 2c, 2c+1 of its 16.
+// 32 h .. +31 and dP columns 64 + 32 h .. +31 of its lanes; per 16 tokens (round q of 2) it
+// reads score columns 32 h + 16 q .. +15 and dP columns 64 + 32 h + 16 q .. +15, then writes
+// P hi and P lo (key tiles only) over those score columns (8 each) and dx hi and dx lo over
+// those dP columns.  Column c of an operand holds tokens 2c, 2c+1 of its 16.
 constexpr uint32_t TM_ACC = 384, TM_ACC2 = 448;
 constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 64, false, false);
 constexpr uint32_t IDESC_MN = idesc_bf16_f32(128, 64, false, true);
@@ -77,11 +78,12 @@ using namespace tceb;
 // kernel, Dq (dO . o of each walked query).  P = 2^(scale log2e s + bias) and
 // dx = P (dP - D) with bias = W - crr (key tiles: W holds the query's running sum minus its
 // lse) or crr - W (query tiles: crr holds the query's, W the key's).  Masked blocks zero the
-// entries outside lo <= tt < hi.  Writes P, dx hi, dx lo as packed bf16 pairs.
+// entries outside lo <= tt < hi.  Writes P hi, P lo (key tiles), dx hi, dx lo as packed bf16
+// pairs.
 template <bool kd, bool masked>
 __device__ __forceinline__ void softmax_grad16(const float* s, const float* dp, const float* W, const float* Dq,
                                                float crr, float Dr, float sl2, int tt0, int lo, int hi, float& sum,
-                                               uint32_t* pp, uint32_t* dh, uint32_t* dl) {
+                                               uint32_t* ph, uint32_t* pl, uint32_t* dh, uint32_t* dl) {
 #pragma unroll
     for (int c2 = 0; c2 < 8; ++c2) {
         float pv[2], dx[2];
@@ -96,7 +98,11 @@ __device__ __forceinline__ void softmax_grad16(const float* s, const float* dp, 
             pv[u] = P;
             dx[u] = g;
         }
-        pp[c2] = pack_bf16x2(pv[0], pv[1]);
+        if (kd) {
+            const uint32_t p2 = pack_bf16x2(pv[0], pv[1]);
+            ph[c2] = p2;
+            pl[c2] = pack_bf16x2(pv[0] - __uint_as_float(p2 << 16), pv[1] - __uint_as_float(p2 & 0xffff0000u));
+        }
         const uint32_t h2 = pack_bf16x2(dx[0], dx[1]);
         dh[c2] = h2;
         dl[c2] = pack_bf16x2(dx[0] - __uint_as_float(h2 << 16), dx[1] - __uint_as_float(h2 & 0xffff0000u));
@@ -214,12 +220,14 @@ __global__ void __launch_bounds__(THREADS, 1) tc_e_bwd_kernel(const __grid_const
 #pragma unroll
                     for (int kk = 0; kk < SUB / 16; ++kk) {   // 16 tokens: half kk / 2, round kk % 2
                         const uint32_t acc0 = (pz > 0 || kk > 0) ? 1u : 0u;
-                        const uint32_t opP = base + (kk >> 1) * 32 + (kk & 1) * 16, opH = opP + 8;
-                        const uint32_t opL = base + 64 + (kk >> 1) * 32 + (kk & 1) * 8;
-                        if (kd) {   // dv += P^T dO, dk += (dx hi + lo)^T Q
+                        const uint32_t opP = base + (kk >> 1) * 32 + (kk & 1) * 16;        // P hi, then P lo at +8
+                        const uint32_t opH = base + 64 + (kk >> 1) * 32 + (kk & 1) * 16;   // dx hi, then dx lo at +8
+                        const uint32_t opL = opH + 8;
+                        if (kd) {   // dv += (P hi + lo)^T dO, dk += (dx hi + lo)^T Q
                             const uint64_t qd = sdesc_sw128_ex(sc + kk * 2048, 8192, 1024);
                             const uint64_t dd = sdesc_sw128_ex(sd + kk * 2048, 8192, 1024);
                             umma_bf16_ts(tmem + TM_ACC2, opP, dd, IDESC_MN, acc0);
+                            umma_bf16_ts(tmem + TM_ACC2, opP + 8, dd, IDESC_MN, 1u);
                             umma_bf16_ts(tmem + TM_ACC, opH, qd, IDESC_MN, acc0);
                             umma_bf16_ts(tmem + TM_ACC, opL, qd, IDESC_MN, 1u);
                         } else {    // dq += (dx hi + lo) K
@@ -313,15 +321,17 @@ __global__ void __launch_bounds__(THREADS, 1) tc_e_bwd_kernel(const __grid_const
                         Dq[4 * v4] = d4.x, Dq[4 * v4 + 1] = d4.y, Dq[4 * v4 + 2] = d4.z, Dq[4 * v4 + 3] = d4.w;
                     }
                 }
-                uint32_t pp[8], dh[8], dl[8];
+                uint32_t ph[8], pl[8], dh[8], dl[8];
                 if (masked)
-                    softmax_grad16<kd, true>(s, dp, W, Dq, crr, Dr, sl2, tt0, lo, hi, sum, pp, dh, dl);
+                    softmax_grad16<kd, true>(s, dp, W, Dq, crr, Dr, sl2, tt0, lo, hi, sum, ph, pl, dh, dl);
                 else
-                    softmax_grad16<kd, false>(s, dp, W, Dq, crr, Dr, sl2, tt0, lo, hi, sum, pp, dh, dl);
-                const uint32_t oc = bufc + h * 32 + q4 * 16;   // this round's P, then dx hi
-                if (kd) tmem_st8(oc, pp);
-                tmem_st8(oc + 8, dh);
-                tmem_st8(bufc + 64 + h * 32 + q4 * 8, dl);
+                    softmax_grad16<kd, false>(s, dp, W, Dq, crr, Dr, sl2, tt0, lo, hi, sum, ph, pl, dh, dl);
+                if (kd) {   // over this round's score columns
+                    tmem_st8(bufc + tt0, ph);
+                    tmem_st8(bufc + tt0 + 8, pl);
+                }
+                tmem_st8(bufc + 64 + tt0, dh);   // over this round's dP columns
+                tmem_st8(bufc + 64 + tt0 + 8, dl);
             }
             tmem_wait_st();
             tc_fence_before();

@@ -20,7 +20,9 @@
 //    fp32, keep the row sums (Z) in fp32 and write P as two bf16 terms P_hi + P_lo (one bf16
 //    term alone costs ~2^-9 relative per weight, enough to break the 2e-2 bar on
 //    unnormalised outputs); both are A operands of P V (V MN-major from its tile).
-//  * Epilogue: [N, Z] = intra + exp(A_i) [N_x, Z_x]; o = N / Z (or N), fp32; Z saved.
+//  * Epilogue: [N, Z] = intra + exp(A_i) [N_x, Z_x]; o = N / Z (or N), fp32; Z saved.  The
+//    state planes hold ks^2 vs S and the normaliser state ks^2 z (the scan's operand scales,
+//    exact powers of two), so N_x and Z_x are divided by those factors here.
 // Warps 0-7 compute (warp w: tensor-memory lane quadrant w % 4, column half w / 4), warp 8
 // issues TMA, warp 9 the MMAs.  Every mbarrier wait is bounded (TM2_ERR_TIMEOUT on expiry).
 #include "tm2.h"
@@ -60,6 +62,7 @@ constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, 64, false, true);
 struct Args {
     const float* Aloc;   // [BH][Tp]
     const float* zx;     // [BH][NC][4096]
+    const unsigned* amax;   // [BH][4] the forward scan's operand maxima (key, value)
     float* o;            // [BH][T][64]
     float* Z;            // [BH][T] or null
     int* status;
@@ -312,18 +315,21 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
                 uint32_t ph[8], pl[8];
 #pragma unroll
                 for (int k2 = 0; k2 < 8; ++k2) {
-                    float hi2[2], lo2[2];
+                    float pv[2];
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
                         const int j = b * 64 + cc * 16 + 2 * k2 + u;
                         const float sv = s[2 * k2 + u];
-                        const float pv = j <= i ? sv * sv * __expf(Ai - sAv[j]) : 0.f;
-                        zin += pv;
-                        hi2[u] = __bfloat162float(__float2bfloat16_rn(pv));
-                        lo2[u] = pv - hi2[u];
+                        pv[u] = j <= i ? sv * sv * __expf(Ai - sAv[j]) : 0.f;
                     }
-                    ph[k2] = pack_bf16x2(hi2[0], hi2[1]);
-                    pl[k2] = pack_bf16x2(lo2[0], lo2[1]);
+                    const uint32_t h2 = pack_bf16x2(pv[0], pv[1]);
+                    const float h0 = __uint_as_float(h2 << 16), h1 = __uint_as_float(h2 & 0xffff0000u);
+                    const uint32_t l2 = pack_bf16x2(pv[0] - h0, pv[1] - h1);
+                    // Z sums the weights exactly as the P V products see them (hi + rounded lo),
+                    // so a row with one dominant weight gives o = v to fp32 precision
+                    zin += (h0 + __uint_as_float(l2 << 16)) + (h1 + __uint_as_float(l2 & 0xffff0000u));
+                    ph[k2] = h2;
+                    pl[k2] = l2;
                 }
                 tmem_st8(pbb + cc * 8, ph);
                 tmem_st8(pbb + 32 + cc * 8, pl);
@@ -343,20 +349,22 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
         if (ok && !abort_s && (ok = mbar_wait(smem_u32(&bar_yfull), 0, a.status))) {
             tc_fence_after();
             const float eA = __expf(Ai);
+            const float ks = pow2_scale(a.amax[bh * 4]), vs = pow2_scale(a.amax[bh * 4 + 1]);
+            const float uz = 1.f / (ks * ks), un = uz / vs;   // exact powers of two
             const float zi = sRed[l * 2] + sRed[(128 + l) * 2];
             const float zo = sRed[l * 2 + 1] + sRed[(128 + l) * 2 + 1];
-            const float z = zi + eA * zo;
+            const float z = zi + eA * (uz * zo);
             float y[32];
             tmem_ld32(tmem + lane_base + TM_Y + h * 32, y);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) y[k] += eA * (un * nx[k]);
             const long tok = (long)c * C + i;
             if (tok < a.T) {
                 const float inv = a.normalize ? (z != 0.f ? 1.f / z : 0.f) : 1.f;
                 float4* dst = reinterpret_cast<float4*>(a.o + (bh * a.T + tok) * 64 + h * 32);
 #pragma unroll
                 for (int q4 = 0; q4 < 8; ++q4)
-                    dst[q4] = make_float4((y[4 * q4] + eA * nx[4 * q4]) * inv, (y[4 * q4 + 1] + eA * nx[4 * q4 + 1]) * inv,
-                                          (y[4 * q4 + 2] + eA * nx[4 * q4 + 2]) * inv,
-                                          (y[4 * q4 + 3] + eA * nx[4 * q4 + 3]) * inv);
+                    dst[q4] = make_float4(y[4 * q4] * inv, y[4 * q4 + 1] * inv, y[4 * q4 + 2] * inv, y[4 * q4 + 3] * inv);
                 if (a.Z && h == 0) a.Z[bh * a.T + tok] = z;
             }
         }
@@ -368,7 +376,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
 }
 
 cudaError_t tc_chunk_out(const Problem& p, const void* q, const void* k, const void* v, const float* Aloc,
-                         const void* Sx, const float* zx, float* o, float* Z, cudaStream_t s) {
+                         const void* Sx, const float* zx, const unsigned* amax, float* o, float* Z, cudaStream_t s) {
     CUtensorMap tq, tk, tv, ts;
     const uint64_t BH = (uint64_t)p.BH();
     if (!make_tmap_bf16_3d(&tq, q, BH, (uint64_t)p.T, 64, 128) || !make_tmap_bf16_3d(&tk, k, BH, (uint64_t)p.T, 64, C) ||
@@ -376,7 +384,7 @@ cudaError_t tc_chunk_out(const Problem& p, const void* q, const void* k, const v
         return cudaErrorInvalidValue;
     int* status = tc_status_ptr();
     if (!status) return cudaErrorInvalidValue;
-    Args a{Aloc, zx, o, Z, status, p.T, p.NC, (int)p.Tp(), p.normalize ? 1 : 0};
+    Args a{Aloc, zx, amax, o, Z, status, p.T, p.NC, (int)p.Tp(), p.normalize ? 1 : 0};
     cudaError_t e = cudaFuncSetAttribute(tc_chunk_out_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     dim3 grid(2 * p.NC, (unsigned)p.BH());

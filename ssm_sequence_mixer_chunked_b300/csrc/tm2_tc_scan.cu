@@ -32,6 +32,14 @@
 // weights by 1/zmax_c (zmax_c = max over chunk c of exp(A_i) zeta_i, so they are <= 1) and
 // exports slot c divided by Gamma_c = max_{c' > c} zmax_{c'} (one value per slot, the same
 // in every CTA, recorded in `sscale`), so that the 1/Z factors cannot overflow fp16.
+// Both walks take their key and value operands multiplied by powers of two ks, vs that bring
+// the head's largest |key| and |value| into [0.5, 1) (and the reverse walk's normaliser row
+// by zs, from the largest |ucol|), so the fp16 operands, the key products and the exported
+// planes stay in fp16's normal range whatever the scale of the inputs (q, k, v ~ 1e-2 would
+// otherwise leave the state in fp16's subnormal range).  The running state is kept in those
+// units: value columns times ks^2 vs, the normaliser column times ks^2 (forward) or, after
+// the reverse walk multiplies it by vs / zs, times ks^2 vs too.  S0 / z0 are brought into
+// them, S_final / z_final out of them, and the readouts divide by the same exact factors.
 //
 // Data flow.  A pre-pass (launch_tc_scan_operands) writes one [136][64] fp16 block per
 // 64-token stage: the transposed key block and the transposed weighted values with the
@@ -79,6 +87,7 @@ struct Args {
     float* sscale;        // reverse: [BH][NC] export scale per slot; forward: null (= 1)
     float* S_final;       // forward: optional (BH, 4096, 64) fp32
     float* z_final;       // forward: optional (BH, 4096) fp32
+    const unsigned* amax; // [BH][4] operand maxima (fp32 bits): key, value, normaliser (reverse)
     int* status;
     int T, NC, Tp, rev;
 };
@@ -251,6 +260,11 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
         // NK groups of 32 rows each.
         const int q = warp & 3, e = warp >= 12 ? 1 : 0;
         const bool zwarp = q == 2;
+        // units of the running state (see the header): forward value columns ks^2 vs, forward
+        // normaliser ks^2; the reverse normaliser column is brought to ks^2 vs by vs / zs
+        const float ks = pow2_scale(a.amax[bh * 4]), vs = pow2_scale(a.amax[bh * 4 + 1]);
+        const float unit = rev ? 1.f : (zwarp ? ks * ks : ks * ks * vs);
+        const float zfix = (rev && zwarp) ? vs / pow2_scale(a.amax[bh * 4 + 2]) : 1.f;
         const int col = 32 * q + lane;               // value column (q < 2)
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
         constexpr int NK = NR / 64;
@@ -293,13 +307,13 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
             if (rev) return;
             if (zwarp) {
                 if (a.z0) {
-                    const float zl = a.z0[bh * 4096 + rbase + lane];
+                    const float zl = a.z0[bh * 4096 + rbase + lane] * unit;
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = __shfl_sync(0xffffffffu, zl, i);
                 }
             } else if (a.S0) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = a.S0[(bh * 4096 + rbase + i) * 64 + col];
+                for (int i = 0; i < 32; ++i) v[i] = a.S0[(bh * 4096 + rbase + i) * 64 + col] * unit;
             }
         };
         {
@@ -315,7 +329,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
         for (int it = 0; it < nchunks && ok; ++it) {
             const int c = chunk_of(it), b = it & 1;
             const float dec = __expf(a.g[bh * NC + c]);
-            const float scl = rev ? a.zmax[bh * NC + c] : 1.f;
+            const float zm = rev ? a.zmax[bh * NC + c] : 1.f;
+            const float scl = zm * zfix;
             if (abort_s || !(ok = mbar_wait(smem_u32(&bar_hfull[b]), (uint32_t)(it >> 1) & 1, a.status))) break;
             tc_fence_after();
             // pass 1: S_c = dec S_{c-1} + scl H^T_c over the buffer of chunk c
@@ -332,7 +347,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(smem_u32(&bar_dfree[(it + 1) & 1]));   // the previous buffer has been read
-            if (rev) gam = it == 0 ? scl : fmaxf(gam, scl);
+            if (rev) gam = it == 0 ? zm : fmaxf(gam, zm);
             // pass 2: export the state of slot c + 1 (forward) / c - 1 (reverse)
             const int slot = rev ? c - 1 : c + 1;
             if (slot >= 0 && slot < NC) {
@@ -348,12 +363,13 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
                     float v[32];
                     tmem_ld32(tmem + lane_base + (uint32_t)b * NR + (NR / 2) * e + 32 * k, v);
                     const long rbase = row0 + 32 * k;
+                    const float inv_unit = 1.f / unit;   // exact: a power of two
                     if (zwarp) {
                         const float zv = gather_lane(v, 0);
-                        if (a.z_final) a.z_final[bh * 4096 + rbase + lane] = zv;
+                        if (a.z_final) a.z_final[bh * 4096 + rbase + lane] = zv * inv_unit;
                     } else if (a.S_final) {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) a.S_final[(bh * 4096 + rbase + i) * 64 + col] = v[i];
+                        for (int i = 0; i < 32; ++i) a.S_final[(bh * 4096 + rbase + i) * 64 + col] = v[i] * inv_unit;
                     }
                 }
             }
@@ -374,8 +390,9 @@ cudaError_t tc_state_scan(const Problem& p, const ScanIO& io, cudaStream_t s) {
     if (!make_tmap_f16_nd(&tops, io.ops, 3, dims, strides, box)) return cudaErrorInvalidValue;
     int* status = tc_status_ptr();
     if (!status) return cudaErrorInvalidValue;
-    Args a{io.g, io.zmax, io.S0, io.z0, (__half*)io.Sx, io.zx, io.sscale, io.S_final, io.z_final, status, p.T, p.NC,
-           (int)p.Tp(), io.rev ? 1 : 0};
+    if (!io.amax) return cudaErrorInvalidValue;
+    Args a{io.g, io.zmax, io.S0, io.z0, (__half*)io.Sx, io.zx, io.sscale, io.S_final, io.z_final, io.amax, status,
+           p.T, p.NC, (int)p.Tp(), io.rev ? 1 : 0};
     constexpr int NR = NR_ROWS, SMEM = smem_bytes(NR);
     cudaError_t e = cudaFuncSetAttribute(tc_state_scan_kernel<NR>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
