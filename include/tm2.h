@@ -150,11 +150,14 @@ int tm2e_forward(const void* q, const void* k, const void* v, const float* a,
  * for callers that cannot allocate device memory (for example a plugin hosted by an
  * inference engine that owns and pre-plans all device memory, or a latency-critical
  * loop that must not risk cudaMalloc's implicit synchronisation).
- * It computes exactly what tm2e_forward computes, with the same arguments minus the
- * workspace: its scratch is a fixed array of TM2E_NOALLOC_SCRATCH_BYTES compiled into
- * the library, held by every GPU that loads the library until the process exits.
- *  - Scratch need is about 8 * B*H*T bytes; larger problems return TM2_ERR_WORKSPACE
- *    before anything is launched (B*H*T up to roughly 1.3 million token-heads fits).
+ * It runs tm2e_forward's own checks and kernels (the tensor-core kernel for bf16 inputs with
+ * d = dv = 64, the CUDA-core kernel otherwise) with the same arguments minus the workspace,
+ * so its results are tm2e_forward's; its scratch is a fixed array of
+ * TM2E_NOALLOC_SCRATCH_BYTES compiled into the library, held by every GPU that loads the
+ * library until the process exits.
+ *  - Scratch need is about 12 * B*H*T bytes (three fp32 values per token-head, plus chunk
+ *    totals and padding to whole chunks); larger problems return TM2_ERR_WORKSPACE before
+ *    anything is launched (B*H*T up to roughly 1.3 million token-heads fits).
  *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress,
  *    with that device current); make that first call before any stream capture.
  *  - No cudaMalloc, cudaFree or other allocating routine is called.

@@ -15,12 +15,15 @@
 // first call made on that device; later calls reuse it.  Nothing else is allocated: no
 // cudaMalloc, no cudaFree, no allocating library routine.
 //
-// The scratch holds the chunk-local decay running sums, the chunk totals and the
-// global running sums of the A-mask.  Every element a call reads is first written by
-// that same call, so no part of the array needs clearing between calls.  All calls on
-// a device share the one array: calls that overlap on the GPU (different streams, or
-// different host threads without ordering) race on it and must be serialised by the
-// caller.
+// Argument checks, the scratch layout and the launch sequence are tm2e_forward's own
+// (e_forward_check, e_forward_scratch_bytes, e_forward_run in tm2_api.cu): the same kernels
+// run on the same inputs, so the results are those of tm2e_forward.  The scratch holds the
+// chunk-local decay running sums, the chunk totals and the global running sums of the A-mask
+// with their rounding residuals, about 12 bytes per token-head.  Every element a call reads
+// is first written by that same call, so no part of the array needs clearing between calls.
+// All calls on a device share the one array: calls that overlap on the GPU (different
+// streams, or different host threads without ordering) race on it and must be serialised by
+// the caller.
 #include <mutex>
 
 #include "tm2.h"
@@ -34,8 +37,6 @@ static __device__ __align__(256) unsigned char g_e_noalloc_scratch[TM2E_NOALLOC_
 static std::mutex g_noalloc_mu;
 static void* g_noalloc_addr[256];   // device address of g_e_noalloc_scratch, per device ordinal
 
-static size_t round256(size_t b) { return (b + 255) & ~(size_t)255; }
-
 }  // namespace tm2
 
 using namespace tm2;
@@ -43,49 +44,31 @@ using namespace tm2;
 extern "C" int tm2e_forward_noalloc(const void* q, const void* k, const void* v, const float* a,
                                     void* o, float* lse, int B, int H, int T, int d, int dv,
                                     float scale, int dtype, void* stream) {
-    if (B < 0 || H < 0 || T < 0 || d <= 0 || dv <= 0) return TM2_ERR_INVALID_ARG;
-    if (dtype != TM2_F32 && dtype != TM2_BF16) return TM2_ERR_UNSUPPORTED;
-    if (d != dv || (d != 16 && d != 32 && d != 64)) return TM2_ERR_UNSUPPORTED;
-    if ((long)B * H > 65535) return TM2_ERR_UNSUPPORTED;
-    if (!(scale == scale) || scale == 0.f) return TM2_ERR_INVALID_ARG;
-    if ((long)B * H == 0 || T == 0) return TM2_OK;
-    if (!q || !k || !v || !a || !o || !lse) return TM2_ERR_INVALID_ARG;
-    const void* ptrs[] = {q, k, v, a, o, lse};
-    for (const void* x : ptrs)
-        if (((uintptr_t)x & 15u) != 0) return TM2_ERR_ALIGNMENT;
-
-    Problem p;
-    p.B = B; p.H = H; p.T = T; p.d = d; p.dv = dv;
-    p.C = 64;
-    p.NC = (T + p.C - 1) / p.C;
-    p.dtype = dtype;
-    p.normalize = false;
-    // scratch: chunk-local running sums, chunk totals, global running sums and their residuals
-    const size_t off_g = round256(sizeof(float) * (size_t)p.BH() * p.Tp());
-    const size_t off_cum = off_g + round256(sizeof(float) * (size_t)p.BH() * p.NC);
-    const size_t off_lo = off_cum + round256(sizeof(float) * (size_t)p.BH() * T);
-    const size_t need = off_lo + round256(sizeof(float) * (size_t)p.BH() * T);
-    if (need > (size_t)TM2E_NOALLOC_SCRATCH_BYTES) return TM2_ERR_WORKSPACE;
+    Problem p{};
+    int st = e_forward_check(q, k, v, a, o, lse, B, H, T, d, dv, scale, dtype, p);
+    if (st != TM2_OK || p.BH() == 0 || T == 0) return st;
+    if (e_forward_scratch_bytes(p) > (size_t)TM2E_NOALLOC_SCRATCH_BYTES) return TM2_ERR_WORKSPACE;
 
     int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return TM2_ERR_CUDA;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        record_cuda_error(e);
+        return TM2_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= 256) return TM2_ERR_UNSUPPORTED;
     void* base = nullptr;
     {
         std::lock_guard<std::mutex> lock(g_noalloc_mu);
         if (!g_noalloc_addr[dev]) {
             void* addr = nullptr;
-            if (cudaGetSymbolAddress(&addr, g_e_noalloc_scratch) != cudaSuccess || !addr) return TM2_ERR_CUDA;
+            e = cudaGetSymbolAddress(&addr, g_e_noalloc_scratch);
+            if (e != cudaSuccess || !addr) {
+                record_cuda_error(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
+                return TM2_ERR_CUDA;
+            }
             g_noalloc_addr[dev] = addr;
         }
         base = g_noalloc_addr[dev];
     }
-    float* Aloc = reinterpret_cast<float*>((char*)base);
-    float* g = reinterpret_cast<float*>((char*)base + off_g);
-    float* cum = reinterpret_cast<float*>((char*)base + off_cum);
-    float* cum_lo = reinterpret_cast<float*>((char*)base + off_lo);
-    cudaStream_t s = (cudaStream_t)stream;
-    if (launch_decay(p, a, Aloc, g, s) != cudaSuccess) return TM2_ERR_CUDA;
-    if (launch_global_cumsum(p, Aloc, g, cum, cum_lo, s) != cudaSuccess) return TM2_ERR_CUDA;
-    if (simt_e_fwd(p, q, k, v, cum, cum_lo, scale, o, lse, s) != cudaSuccess) return TM2_ERR_CUDA;
-    return TM2_OK;
+    return e_forward_run(p, q, k, v, a, o, lse, scale, base, (cudaStream_t)stream);
 }

@@ -3,10 +3,12 @@
 It serves callers that cannot allocate device memory (a plugin inside an engine that
 owns all device memory, a latency-critical loop that must not call cudaMalloc): they
 pass inputs and outputs only, and the library uses a fixed scratch array compiled into
-it.  This test calls it through the C ABI twice in a row, on two different inputs,
-and checks each result against the ordinary tm2e_forward (which takes a caller
-workspace) within the bf16 parity tolerance used by the other tests.  It also checks
-that a problem too large for the fixed scratch is refused before any launch.
+it.  This test calls it through the C ABI twice in a row, on two different inputs, for
+fp32 and bf16 inputs at head dims 16 and 64 with a ragged sequence length, and checks each
+result against the ordinary tm2e_forward (which takes a caller workspace and runs the same
+kernels, so the results agree bitwise) and against the fp64 oracle within the parity
+tolerance of the other tests.  It also checks that a problem too large for the fixed
+scratch is refused before any launch.
 
 The file name sorts last so that a run stopping at the first failure has run every
 other test before this one.
@@ -17,10 +19,13 @@ import math
 import pytest
 import torch
 
+import oracle
 import ssm_sequence_mixer_chunked_b300 as tm2
 import synth_inputs as si
 
 pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-4, "bf16": 2e-2}
 
 
 def _noalloc_fn():
@@ -36,27 +41,32 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr())
 
 
-def test_noalloc_matches_workspace_entry_point_twice():
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("d", [16, 64])
+def test_noalloc_matches_workspace_entry_point_twice(dtype, d):
     fn = _noalloc_fn()
-    B, H, T, d = 2, 4, 1000, 64
+    B, H, T = 2, 3, 333
     scale = 1.0 / math.sqrt(d)
     for seed in (71, 72):   # two calls in a row, different inputs
-        inp = si.sequence_inputs(B, H, T, d, d, dtype="bf16", qkv_std=1.0, seed=seed)
+        inp = si.sequence_inputs(B, H, T, d, d, dtype=dtype, qkv_std=1.0, seed=seed + d)
         g = {k: v.cuda() for k, v in inp.items()}
-        o_ref, lse_ref = tm2.e_forward(g["q"], g["k"], g["v"], g["a"], scale=scale)
+        o_ws, lse_ws = tm2.e_forward(g["q"], g["k"], g["v"], g["a"], scale=scale)
         o = torch.empty((B, H, T, d), dtype=torch.float32, device="cuda")
         lse = torch.empty((B, H, T), dtype=torch.float32, device="cuda")
         st = fn(_ptr(g["q"]), _ptr(g["k"]), _ptr(g["v"]), _ptr(g["a"]), _ptr(o), _ptr(lse),
-                B, H, T, d, d, scale, 1, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+                B, H, T, d, d, scale, 1 if dtype == "bf16" else 0,
+                ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
         assert st == 0, tm2.status_string(st)
         torch.cuda.synchronize()
-        assert si.rel_err(o.cpu(), o_ref.cpu()) <= 2e-2
-        assert si.rel_err(lse.cpu(), lse_ref.cpu()) <= 2e-2
+        assert torch.equal(o, o_ws) and torch.equal(lse, lse_ws)
+        o_ref, lse_ref = oracle.e_fwd(inp["q"], inp["k"], inp["v"], inp["a"], scale)
+        assert si.rel_err(o.cpu(), o_ref) <= TOL[dtype]
+        assert si.rel_err(lse.cpu(), lse_ref) <= TOL[dtype]
 
 
 def test_noalloc_rejects_problem_larger_than_scratch():
     fn = _noalloc_fn()
     f = ctypes.c_void_p(0x10000000)   # never dereferenced: the size check comes first
-    # 8 * 64 * 16 * 8192 bytes of scratch is far above the 16 MiB array
+    # about 12 bytes per token-head: 64 * 16 * 8192 token-heads need ~100 MB, far above 16 MiB
     st = fn(f, f, f, f, f, f, 64, 16, 8192, 64, 64, 0.125, 1, None)
     assert st == -4, tm2.status_string(st)
