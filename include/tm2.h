@@ -132,6 +132,38 @@ int tm2_step(const void* q, const void* k, const void* v, const float* a,
              float* S, float* z, void* o, float* Z,
              int N, int H, int d, int dv, int dtype, unsigned flags, void* stream);
 
+/*
+ * Quadratic (C = T, "flash") form of the mixer, order 2 (2Mamba) or 1 (the first-order mixer
+ * of Mamba-2S with the same softplus A-mask).  "2Mamba2Furious", Sec. 1-2: the quadratic form
+ * costs O(T^2 d) but, at d = dv = 64, fewer flops than the chunked form while
+ * T < 4 d^2 dv / (d + dv) = 8192; Sec. 4 (Mamba-2S: the score q.k itself), Sec. 5 (2Mamba:
+ * its square under the A-mask):
+ *   w_ij = (q_i . k_j)^order exp(cumA_i - cumA_j)  (j <= i),  N_i = sum_j w_ij v_j,  Z_i = sum_j w_ij,
+ *   o = N / Z with TM2_NORMALIZE, else N.
+ * With order 2 the result is tm2_forward's (no initial state).  The first-order weights carry
+ * the sign of q.k, so its Z can vanish; TM2_NORMALIZE is accepted for it but rarely wanted.
+ * Layouts, dtypes and alignment as for tm2_forward; o (B,H,T,dv) and Z (B,H,T, optional) fp32.
+ * bf16 inputs with d = dv = 64 run on the tensor cores (the 2Mamba-E kernels' skeleton with
+ * the weights above), everything else on CUDA cores in fp32 arithmetic.  Any T >= 0.
+ * flags: TM2_NORMALIZE only.
+ */
+size_t tm2q_forward_workspace(int B, int H, int T, int d, int dv, int order, int dtype, unsigned flags);
+int tm2q_forward(const void* q, const void* k, const void* v, const float* a, void* o, float* Z,
+                 int B, int H, int T, int d, int dv, int order, int dtype, unsigned flags,
+                 void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Backward of tm2q_forward (App. C, C.1): gradients of sum(dO * o) w.r.t. q, k, v and the raw
+ * A-mask input a, given the forward's o and Z (both may be NULL without TM2_NORMALIZE).
+ * dq, dk, dv, da fp32; da as for tm2_backward (row-axis minus column-axis sums of
+ * w_ij dL/dw_ij, accumulated from the end, times -sigmoid(a)).
+ */
+size_t tm2q_backward_workspace(int B, int H, int T, int d, int dv, int order, int dtype, unsigned flags);
+int tm2q_backward(const void* q, const void* k, const void* v, const float* a, const void* o,
+                  const float* Z, const void* dO, void* dq, void* dk, void* dv, float* da,
+                  int B, int H, int T, int d, int dv_dim, int order, int dtype, unsigned flags,
+                  void* ws, size_t ws_bytes, void* stream);
+
 size_t tm2e_forward_workspace(int B, int H, int T, int d, int dv, int dtype);
 
 /*

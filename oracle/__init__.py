@@ -47,10 +47,11 @@ def _load():
         build()
         _lib = ctypes.CDLL(_LIB)
         i, d, p = ctypes.c_int, ctypes.c_double, ctypes.c_void_p
-        _lib.orc_fwd_quadratic.argtypes = [i] * 5 + [p] * 6 + [i, p, p]
+        _lib.orc_fwd_quadratic.argtypes = [i] * 5 + [p] * 6 + [i, i, p, p]
+        _lib.orc_fwd1_recurrent.argtypes = [i] * 5 + [p] * 4 + [i, p, p]
         _lib.orc_fwd_recurrent.argtypes = [i] * 5 + [p] * 6 + [i, p, p, p, p]
         _lib.orc_step.argtypes = [i] * 4 + [p] * 6 + [i, p, p]
-        _lib.orc_bwd_quadratic.argtypes = [i] * 5 + [p] * 5 + [i, p, p, p, p, p, p]
+        _lib.orc_bwd_quadratic.argtypes = [i] * 5 + [p] * 5 + [i, i, p, p, p, p, p, p]
         _lib.orc_e_fwd.argtypes = [i] * 5 + [p] * 4 + [d, p, p]
         _lib.orc_e_bwd.argtypes = [i] * 5 + [p] * 5 + [d, p, p, p, p]
         _lib.orc_running_log_decay.argtypes = [p, ctypes.c_long, ctypes.c_long, p]
@@ -83,15 +84,30 @@ def running_log_decay(a):
     return out
 
 
-def fwd_quadratic(q, k, v, a, normalize=True, S0=None, z0=None):
-    """O(T^2) form. q,k: (B,H,T,d); v: (B,H,T,dv); a: (B,H,T). Returns (o, Z)."""
+def fwd_quadratic(q, k, v, a, normalize=True, S0=None, z0=None, order=2):
+    """O(T^2) form. q,k: (B,H,T,d); v: (B,H,T,dv); a: (B,H,T). Returns (o, Z).
+    order 2: 2Mamba (squared scores); order 1: the first-order mixer (no initial state)."""
     q, k, v, a, S0, z0 = map(_f64, (q, k, v, a, S0, z0))
+    if order not in (1, 2) or (order == 1 and (S0 is not None or z0 is not None)):
+        raise ValueError("order 1 or 2; an initial second-order state only with order 2")
     B, H, T, d = q.shape
     dv = v.shape[-1]
     o = np.zeros((B, H, T, dv))
     Z = np.zeros((B, H, T))
     _load().orc_fwd_quadratic(B, H, T, d, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(a),
-                              _ptr(S0), _ptr(z0), int(normalize), _ptr(o), _ptr(Z))
+                              _ptr(S0), _ptr(z0), int(normalize), int(order), _ptr(o), _ptr(Z))
+    return o, Z
+
+
+def fwd1_recurrent(q, k, v, a, normalize=True):
+    """First-order mixer by its (d x dv) state recurrence. Returns (o, Z)."""
+    q, k, v, a = map(_f64, (q, k, v, a))
+    B, H, T, d = q.shape
+    dv = v.shape[-1]
+    o = np.zeros((B, H, T, dv))
+    Z = np.zeros((B, H, T))
+    _load().orc_fwd1_recurrent(B, H, T, d, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(a), int(normalize),
+                               _ptr(o), _ptr(Z))
     return o, Z
 
 
@@ -125,7 +141,7 @@ def step(q, k, v, a, S, z, normalize=True):
     return o, zeta
 
 
-def bwd_quadratic(q, k, v, a, dO, normalize=True, o=None, Z=None):
+def bwd_quadratic(q, k, v, a, dO, normalize=True, o=None, Z=None, order=2):
     """Gradients of the quadratic form (no initial state). Returns (dq, dk, dv, da).
 
     With o and Z given (normalised only), the backward uses them in place of the forward
@@ -143,8 +159,11 @@ def bwd_quadratic(q, k, v, a, dO, normalize=True, o=None, Z=None):
     dk = np.zeros_like(k)
     dvv = np.zeros_like(v)
     da = np.zeros_like(a)
+    if order not in (1, 2):
+        raise ValueError("order 1 or 2")
     _load().orc_bwd_quadratic(B, H, T, d, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(dO),
-                              int(normalize), _ptr(o), _ptr(Z), _ptr(dq), _ptr(dk), _ptr(dvv), _ptr(da))
+                              int(normalize), int(order), _ptr(o), _ptr(Z), _ptr(dq), _ptr(dk), _ptr(dvv),
+                              _ptr(da))
     return dq, dk, dvv, da
 
 

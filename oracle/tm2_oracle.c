@@ -57,8 +57,14 @@ void orc_running_log_decay(const double* a, long n_rows, long T, double* cumA) {
     for (long r = 0; r < n_rows; ++r) running_log_decay(a + r * T, T, cumA + r * T);
 }
 
+/* s^order for the two orders of the mixer: 2 (2Mamba, Sec. 5) and 1 (the first-order mixer
+   of Mamba-2S, Sec. 4: the score itself under the same A-mask). */
+static double score_pow(double s, int order) { return order == 1 ? s : s * s; }
+/* d(s^order)/ds */
+static double score_pow_grad(double s, int order) { return order == 1 ? 1.0 : 2.0 * s; }
+
 /*
- * Quadratic (parallel) form, Sec. 5:
+ * Quadratic (parallel) form, Sec. 5 (order 2; order 1 replaces the square by the score):
  *   w_ij = exp(cumA_i - cumA_j) * (q_i . k_j)^2      (j <= i)
  *   N_i  = sum_j w_ij v_j,   Z_i = sum_j w_ij
  * plus, when an initial state is given, the term it contributes through the
@@ -67,7 +73,7 @@ void orc_running_log_decay(const double* a, long n_rows, long T, double* cumA) {
  */
 void orc_fwd_quadratic(int B, int H, int T, int d, int dv,
                        const double* q, const double* k, const double* v, const double* a,
-                       const double* S0, const double* z0, int normalize,
+                       const double* S0, const double* z0, int normalize, int order,
                        double* o, double* Z) {
     long BH = (long)B * H;
     double* cum = (double*)malloc(sizeof(double) * (size_t)(BH * T + 1));
@@ -81,7 +87,7 @@ void orc_fwd_quadratic(int B, int H, int T, int d, int dv,
             double den = 0.0;
             for (long j = 0; j <= i; ++j) {
                 double s = dot(qi, k + (bh * T + j) * d, d);
-                double w = exp(cb[i] - cb[j]) * s * s;
+                double w = exp(cb[i] - cb[j]) * score_pow(s, order);
                 den += w;
                 const double* vj = v + (bh * T + j) * dv;
                 for (int c = 0; c < dv; ++c) num[c] += w * vj[c];
@@ -164,6 +170,43 @@ void orc_fwd_recurrent(int B, int H, int T, int d, int dv,
 }
 
 /*
+ * Recurrent form of the first-order mixer (Sec. 2: first-order linear attention keeps a state
+ * of size (dh, dh); Sec. 4: Mamba-2S with the softplus A-mask):
+ *   S_t = gamma_t S_{t-1} + k_t v_t^T   (d x dv),   z_t = gamma_t z_{t-1} + k_t   (d)
+ *   N_t = q_t^T S_t,  Z_t = q_t . z_t,  o_t = N_t / Z_t (normalised) or N_t.
+ */
+void orc_fwd1_recurrent(int B, int H, int T, int d, int dv,
+                        const double* q, const double* k, const double* v, const double* a,
+                        int normalize, double* o, double* Z) {
+    long BH = (long)B * H;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long bh = 0; bh < BH; ++bh) {
+        double* S = (double*)calloc((size_t)(d * dv), sizeof(double));
+        double* z = (double*)calloc((size_t)d, sizeof(double));
+        for (long t = 0; t < T; ++t) {
+            const double* qt = q + (bh * T + t) * d;
+            const double* kt = k + (bh * T + t) * d;
+            const double* vt = v + (bh * T + t) * dv;
+            double gamma = exp(-softplus(a[bh * T + t]));
+            for (int m = 0; m < d; ++m) {
+                z[m] = gamma * z[m] + kt[m];
+                for (int c = 0; c < dv; ++c) S[m * dv + c] = gamma * S[m * dv + c] + kt[m] * vt[c];
+            }
+            double zeta = dot(qt, z, d);
+            double* ot = o + (bh * T + t) * dv;
+            for (int c = 0; c < dv; ++c) {
+                double y = 0.0;
+                for (int m = 0; m < d; ++m) y += qt[m] * S[m * dv + c];
+                ot[c] = normalize ? (zeta != 0.0 ? y / zeta : 0.0) : y;
+            }
+            if (Z) Z[bh * T + t] = zeta;
+        }
+        free(S);
+        free(z);
+    }
+}
+
+/*
  * One recurrent decode step for N sequences x H heads, in place (App. A):
  * the same update and readout as orc_fwd_recurrent for a single token.
  * q,k: (N,H,d); v: (N,H,dv); a: (N,H); S: (N,H,d*d,dv); z: (N,H,d*d) or NULL.
@@ -212,7 +255,7 @@ void orc_step(int N, int H, int d, int dv,
  *                           unnormalised: dN_i = dO_i, dZ_i = 0)
  *   dw_ij = dN_i . v_j + dZ_i                      gradient into weight w_ij
  *   dv_j  = sum_{i >= j} w_ij dN_i
- *   ds_ij = 2 s_ij exp(cumA_i - cumA_j) dw_ij      s_ij = q_i . k_j
+ *   ds_ij = 2 s_ij exp(cumA_i - cumA_j) dw_ij      s_ij = q_i . k_j  (order 1: exp(..) dw_ij)
  *   dq_i  = sum_{j <= i} ds_ij k_j,   dk_j = sum_{i >= j} ds_ij q_i
  *   dcumA_t = sum_{j <= t} w_tj dw_tj  -  sum_{i >= t} w_it dw_it
  *             (row-axis sum minus column-axis sum, the two A-mask axis sums)
@@ -221,7 +264,7 @@ void orc_step(int N, int H, int d, int dv,
  */
 void orc_bwd_quadratic(int B, int H, int T, int d, int dv,
                        const double* q, const double* k, const double* v, const double* a,
-                       const double* dO, int normalize, const double* o_in, const double* Z_in,
+                       const double* dO, int normalize, int order, const double* o_in, const double* Z_in,
                        double* dq, double* dk, double* dvv, double* da) {
     long BH = (long)B * H;
     for (long bh = 0; bh < BH; ++bh) {
@@ -245,7 +288,7 @@ void orc_bwd_quadratic(int B, int H, int T, int d, int dv,
             memcpy(o, o_in + bh * T * dv, sizeof(double) * (size_t)(T * dv));
             memcpy(Zs, Z_in + bh * T, sizeof(double) * (size_t)T);
         } else {
-            orc_fwd_quadratic(1, 1, T, d, dv, qb, kb, vb, ab, NULL, NULL, normalize, o, Zs);
+            orc_fwd_quadratic(1, 1, T, d, dv, qb, kb, vb, ab, NULL, NULL, normalize, order, o, Zs);
         }
         for (long i = 0; i < T; ++i) {
             if (normalize) {
@@ -267,9 +310,9 @@ void orc_bwd_quadratic(int B, int H, int T, int d, int dv,
             for (long j = 0; j <= i; ++j) {
                 double s = dot(qb + i * d, kb + j * d, d);
                 double e = exp(cum[i] - cum[j]);
-                double w = e * s * s;
+                double w = e * score_pow(s, order);
                 double dw = dot(dN + i * dv, vb + j * dv, dv) + dZ[i];
-                double ds = 2.0 * s * e * dw;
+                double ds = score_pow_grad(s, order) * e * dw;
                 for (int m = 0; m < d; ++m) dqi[m] += ds * kb[j * d + m];
                 rs += w * dw;
             }
@@ -286,9 +329,9 @@ void orc_bwd_quadratic(int B, int H, int T, int d, int dv,
             for (long i = j; i < T; ++i) {
                 double s = dot(qb + i * d, kb + j * d, d);
                 double e = exp(cum[i] - cum[j]);
-                double w = e * s * s;
+                double w = e * score_pow(s, order);
                 double dw = dot(dN + i * dv, vb + j * dv, dv) + dZ[i];
-                double ds = 2.0 * s * e * dw;
+                double ds = score_pow_grad(s, order) * e * dw;
                 for (int m = 0; m < d; ++m) dkj[m] += ds * qb[i * d + m];
                 for (int c = 0; c < dv; ++c) dvj[c] += w * dN[i * dv + c];
                 cs += w * dw;

@@ -19,7 +19,8 @@ import os
 
 import torch
 
-__all__ = ["forward", "backward", "step", "e_forward", "e_backward", "library_path",
+__all__ = ["forward", "backward", "step", "e_forward", "e_backward", "forward_quadratic",
+           "backward_quadratic", "library_path",
            "forward_workspace_bytes", "backward_workspace_bytes", "workspace_bytes", "TM2Error",
            "NORMALIZE", "REUSE_STATES"]
 
@@ -67,6 +68,13 @@ def _load():
     lib.tm2e_forward.argtypes = [P] * 6 + [I] * 5 + [F, I, P, S, P]
     lib.tm2e_backward.restype = I
     lib.tm2e_backward.argtypes = [P] * 11 + [I] * 5 + [F, I, P, S, P]
+    for name in ("tm2q_forward_workspace", "tm2q_backward_workspace"):
+        getattr(lib, name).restype = S
+        getattr(lib, name).argtypes = [I] * 7 + [U]
+    lib.tm2q_forward.restype = I
+    lib.tm2q_forward.argtypes = [P] * 6 + [I] * 7 + [U, P, S, P]
+    lib.tm2q_backward.restype = I
+    lib.tm2q_backward.argtypes = [P] * 11 + [I] * 7 + [U, P, S, P]
     lib.tm2_poll_status.restype = I
     lib.tm2_last_cuda_error.restype = ctypes.c_char_p
     _lib = lib
@@ -197,6 +205,38 @@ def step(q, k, v, a, S, z, *, normalize=True, out=None, Z=None, stream=None):
     _check(L.tm2_step(_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(S), _ptr(z), _ptr(o), _ptr(Z), N, H, d,
                       dv, _DTYPES[q.dtype], NORMALIZE if normalize else 0, _stream(stream)))
     return o, Z
+
+
+def forward_quadratic(q, k, v, a, *, order=2, normalize=True, workspace=None, stream=None, out=None, Z=None):
+    """Quadratic (C = T) form of the mixer: order 2 is 2Mamba (the same function as forward()),
+    order 1 the first-order mixer with the softplus A-mask.  Returns (o, Z)."""
+    B, H, T, d, dv, dt = _seq_checks(q, k, v, a)
+    L = _load()
+    flags = NORMALIZE if normalize else 0
+    o = torch.empty(v.shape, dtype=torch.float32, device=q.device) if out is None else out
+    Z = torch.empty((B, H, T), dtype=torch.float32, device=q.device) if Z is None else Z
+    ws = _workspace(L.tm2q_forward_workspace(B, H, T, d, dv, order, dt, flags), q.device, workspace)
+    nbytes = 0 if ws is None else ws.numel()
+    _check(L.tm2q_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(o), _ptr(Z), B, H, T, d, dv, order, dt, flags,
+                          _ptr(ws), nbytes, _stream(stream)))
+    return o, Z
+
+
+def backward_quadratic(q, k, v, a, o, Z, dO, *, order=2, normalize=True, workspace=None, stream=None,
+                       grads=None):
+    """Backward of forward_quadratic.  Returns (dq, dk, dv, da)."""
+    B, H, T, d, dv, dt = _seq_checks(q, k, v, a)
+    L = _load()
+    flags = NORMALIZE if normalize else 0
+    if grads is None:
+        grads = tuple(torch.empty(t.shape, dtype=torch.float32, device=q.device) for t in (q, k, v, a))
+    dq, dk, dvv, da = grads
+    ws = _workspace(L.tm2q_backward_workspace(B, H, T, d, dv, order, dt, flags), q.device, workspace)
+    nbytes = 0 if ws is None else ws.numel()
+    _check(L.tm2q_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(o), _ptr(Z), _ptr(dO), _ptr(dq), _ptr(dk),
+                           _ptr(dvv), _ptr(da), B, H, T, d, dv, order, dt, flags, _ptr(ws), nbytes,
+                           _stream(stream)))
+    return dq, dk, dvv, da
 
 
 def e_forward(q, k, v, a, *, scale=None, workspace=None, stream=None, out=None, lse=None):

@@ -103,6 +103,28 @@ static BwdWs plan_bwd(const Problem& p) {
     return w;
 }
 
+// Workspace of the quadratic-form entry points (tm2q_*): decay sums as for 2Mamba-E, a
+// normaliser scratch for a NULL Z, and the backward's per-token D, zeta and axis sums.
+struct QWs { size_t Aloc, g, cum, cum_lo, Zs, D, zeta, rowsum, colsum, total; };
+static QWs plan_q(const Problem& p, bool backward) {
+    Carve c;
+    QWs w{};
+    w.Aloc = c.take(sizeof(float) * p.BH() * p.Tp());
+    w.g = c.take(sizeof(float) * p.BH() * p.NC);
+    w.cum = c.take(sizeof(float) * p.BH() * p.T);
+    w.cum_lo = c.take(sizeof(float) * p.BH() * p.T);
+    if (backward) {
+        w.D = c.take(sizeof(float) * p.BH() * p.T);
+        w.zeta = c.take(sizeof(float) * p.BH() * p.T);
+        w.rowsum = c.take(sizeof(float) * p.BH() * p.T);
+        w.colsum = c.take(sizeof(float) * p.BH() * p.T);
+    } else {
+        w.Zs = c.take(sizeof(float) * p.BH() * p.T);
+    }
+    w.total = c.off;
+    return w;
+}
+
 struct EWs { size_t Aloc, g, cum, cum_lo, Dvec, rowsum, colsum, total; };
 static EWs plan_e(const Problem& p, bool backward) {
     Carve c;
@@ -441,6 +463,91 @@ int tm2e_backward(const void* q, const void* k, const void* v, const float* a, c
                                      (float*)dv, rowsum, colsum, s));
     else
         TM2_RUN("e_bwd", simt_e_bwd(p, q, k, v, cum, cum_lo, lse, Dvec, dO, scale, dq, dk, dv, rowsum, colsum, s));
+    TM2_RUN("reverse_cumsum_da", launch_reverse_cumsum_da(p, a, rowsum, colsum, da, s));
+    return TM2_OK;
+}
+
+static int make_q_problem(int B, int H, int T, int d, int dv, int order, int dtype, unsigned flags, Problem& p) {
+    if (order != 1 && order != 2) return TM2_ERR_UNSUPPORTED;
+    return make_problem(B, H, T, d, dv, 0, dtype, flags, p);
+}
+
+static bool q_tc(const Problem& p) { return p.dtype == TM2_BF16 && p.d == 64 && p.dv == 64; }
+
+size_t tm2q_forward_workspace(int B, int H, int T, int d, int dv, int order, int dtype, unsigned flags) {
+    Problem p{};
+    if (make_q_problem(B, H, T, d, dv, order, dtype, flags, p) != TM2_OK) return 0;
+    return plan_q(p, false).total;
+}
+
+int tm2q_forward(const void* q, const void* k, const void* v, const float* a, void* o, float* Z, int B, int H,
+                 int T, int d, int dv, int order, int dtype, unsigned flags, void* ws, size_t ws_bytes,
+                 void* stream) {
+    Problem p{};
+    int st = make_q_problem(B, H, T, d, dv, order, dtype, flags, p);
+    if (st != TM2_OK) return st;
+    if (p.BH() == 0 || T == 0) return TM2_OK;
+    if (!q || !k || !v || !a || !o) return TM2_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, a, o, Z};
+    for (const void* x : ptrs)
+        if (!aligned16(x)) return TM2_ERR_ALIGNMENT;
+    const QWs w = plan_q(p, false);
+    st = check_ws(ws, ws_bytes, w.total);
+    if (st != TM2_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    float* Aloc = at<float>(ws, w.Aloc);
+    float* g = at<float>(ws, w.g);
+    float* cum = at<float>(ws, w.cum);
+    float* cum_lo = at<float>(ws, w.cum_lo);
+    float* Zo = Z ? Z : at<float>(ws, w.Zs);
+    TM2_RUN("decay_chunk", launch_decay(p, a, Aloc, g, s));
+    TM2_RUN("global_cumsum", launch_global_cumsum(p, Aloc, g, cum, cum_lo, s));
+    if (q_tc(p))
+        TM2_RUN("tc_poly_fwd", tc_poly_fwd(p, order, q, k, v, cum, cum_lo, (float*)o, Zo, s));
+    else
+        TM2_RUN("poly_fwd", simt_poly_fwd(p, order, q, k, v, cum, cum_lo, o, Zo, s));
+    return TM2_OK;
+}
+
+size_t tm2q_backward_workspace(int B, int H, int T, int d, int dv, int order, int dtype, unsigned flags) {
+    Problem p{};
+    if (make_q_problem(B, H, T, d, dv, order, dtype, flags, p) != TM2_OK) return 0;
+    return plan_q(p, true).total;
+}
+
+int tm2q_backward(const void* q, const void* k, const void* v, const float* a, const void* o, const float* Z,
+                  const void* dO, void* dq, void* dk, void* dv, float* da, int B, int H, int T, int d, int dv_dim,
+                  int order, int dtype, unsigned flags, void* ws, size_t ws_bytes, void* stream) {
+    Problem p{};
+    int st = make_q_problem(B, H, T, d, dv_dim, order, dtype, flags, p);
+    if (st != TM2_OK) return st;
+    if (p.BH() == 0 || T == 0) return TM2_OK;
+    if (!q || !k || !v || !a || !dO || !dq || !dk || !dv || !da) return TM2_ERR_INVALID_ARG;
+    if (p.normalize && (!o || !Z)) return TM2_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, a, o, Z, dO, dq, dk, dv, da};
+    for (const void* x : ptrs)
+        if (!aligned16(x)) return TM2_ERR_ALIGNMENT;
+    const QWs w = plan_q(p, true);
+    st = check_ws(ws, ws_bytes, w.total);
+    if (st != TM2_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    float* Aloc = at<float>(ws, w.Aloc);
+    float* g = at<float>(ws, w.g);
+    float* cum = at<float>(ws, w.cum);
+    float* cum_lo = at<float>(ws, w.cum_lo);
+    float* D = at<float>(ws, w.D);
+    float* zeta = at<float>(ws, w.zeta);
+    float* rowsum = at<float>(ws, w.rowsum);
+    float* colsum = at<float>(ws, w.colsum);
+    TM2_RUN("decay_chunk", launch_decay(p, a, Aloc, g, s));
+    TM2_RUN("global_cumsum", launch_global_cumsum(p, Aloc, g, cum, cum_lo, s));
+    TM2_RUN("poly_prep", launch_poly_prep(p, (const float*)o, Z, dO, D, zeta, s));
+    if (q_tc(p))
+        TM2_RUN("tc_poly_bwd", tc_poly_bwd(p, order, q, k, v, cum, cum_lo, zeta, D, dO, (float*)dq, (float*)dk,
+                                           (float*)dv, rowsum, colsum, s));
+    else
+        TM2_RUN("poly_bwd",
+                simt_poly_bwd(p, order, q, k, v, cum, cum_lo, zeta, D, dO, dq, dk, dv, rowsum, colsum, s));
     TM2_RUN("reverse_cumsum_da", launch_reverse_cumsum_da(p, a, rowsum, colsum, da, s));
     return TM2_OK;
 }

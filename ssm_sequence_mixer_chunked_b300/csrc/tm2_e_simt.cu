@@ -5,6 +5,13 @@
 // P_ij = exp(x_ij - lse_i), dx_ij = P_ij (dO_i . v_j - D_i), D_i = dO_i . o_i.
 // Blocks of 64 queries x 64 keys; thread (ti, tc) of 16 x 16 owns rows ti + 16 r and
 // columns tc + 16 s of each 64 x 64 tile.
+//
+// Instantiated with KIND = ATTN_P2 / ATTN_P1 the same kernels evaluate the quadratic (C = T)
+// form of 2Mamba and of the first-order mixer ("2Mamba2Furious", Sec. 4-5):
+//   w_ij = (q_i . k_j)^p exp(cumA_i - cumA_j),  o_i = sum_j w_ij v_j [/ Z_i],  Z_i = sum_j w_ij,
+// with no running maximum (the weights are not exponentiated scores), and the backward
+//   dw_ij = zeta_i (dO_i . v_j - D_i),  dv_j += w_ij zeta_i dO_i,  ds_ij = p s_ij^(p-1) e_ij dw_ij,
+// the A-mask axis sums taking w_ij dw_ij (zeta = 1/Z, D = dO . o normalised; 1 and 0 otherwise).
 #include "tm2_common.cuh"
 #include "tm2_launch.h"
 
@@ -12,11 +19,11 @@ namespace tm2 {
 
 constexpr int EB = 64;
 
-template <int D, int DV, typename Tin>
+template <int KIND, int D, int DV, typename Tin>
 __global__ void __launch_bounds__(256) e_fwd_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
                                                     const Tin* __restrict__ v, const float* __restrict__ cum,
                                                     const float* __restrict__ cum_lo, float scale, float* __restrict__ o,
-                                                    float* __restrict__ lse, int T) {
+                                                    float* __restrict__ lse, int T, int normalize) {
     constexpr int LDQ = D + 1, LDP = EB + 1, NCOL = DV / 16;
     extern __shared__ float sm[];
     float* sq = sm;               // [EB][LDQ]
@@ -70,6 +77,28 @@ __global__ void __launch_bounds__(256) e_fwd_kernel(const Tin* __restrict__ q, c
         for (int r = 0; r < 4; ++r) {
             const int i = ti + 16 * r;
             const long ig = (long)qb * EB + i;
+            if constexpr (KIND != ATTN_E) {   // w = s^p e, no maximum; lrow holds Z
+                float rs = 0.f;
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                    const int j = tc + 16 * s;
+                    const long jg = (long)kb * EB + j;
+                    float w = 0.f;
+                    if (jg <= ig && jg < T) {
+                        float dot = 0.f;
+#pragma unroll 16
+                        for (int n = 0; n < D; ++n) dot = fmaf(sq[i * LDQ + n], sk[j * LDQ + n], dot);
+                        const float e = expf((scq[i] - sck[j]) + (scql[i] - sckl[j]));
+                        w = KIND == ATTN_P2 ? dot * dot * e : dot * e;
+                    }
+                    sP[i * LDP + j] = w;
+                    rs += w;
+                }
+#pragma unroll
+                for (int o2 = 8; o2 > 0; o2 >>= 1) rs += __shfl_xor_sync(0xffffffffu, rs, o2);
+                lrow[r] += rs;
+                continue;
+            }
             float x[4];
             float mx = -INFINITY;
 #pragma unroll
@@ -118,15 +147,17 @@ __global__ void __launch_bounds__(256) e_fwd_kernel(const Tin* __restrict__ q, c
     for (int r = 0; r < 4; ++r) {
         const long t = (long)qb * EB + ti + 16 * r;
         if (t >= T) continue;
-        const float inv = 1.f / lrow[r];
+        float inv;
+        if constexpr (KIND == ATTN_E) inv = 1.f / lrow[r];
+        else inv = normalize ? (lrow[r] != 0.f ? 1.f / lrow[r] : 0.f) : 1.f;
 #pragma unroll
         for (int s = 0; s < NCOL; ++s) o[(bh * T + t) * DV + tc + 16 * s] = acc[r][s] * inv;
-        if (tc == 0) lse[bh * T + t] = mrow[r] + logf(lrow[r]);
+        if (tc == 0) lse[bh * T + t] = KIND == ATTN_E ? mrow[r] + logf(lrow[r]) : lrow[r];
     }
 }
 
 // dk, dv and column sums of dx for one block of 64 keys, looping over query blocks.
-template <int D, int DV, typename Tin>
+template <int KIND, int D, int DV, typename Tin>
 __global__ void __launch_bounds__(256) e_bwd_dkdv_kernel(
     const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
     const float* __restrict__ cum, const float* __restrict__ cum_lo, const float* __restrict__ lse,
@@ -140,9 +171,10 @@ __global__ void __launch_bounds__(256) e_bwd_dkdv_kernel(
     float* sdo = sq + EB * LDQ;     // [EB][LDV]
     float* sP = sdo + EB * LDV;     // [EB][LDP]
     float* sX = sP + EB * LDP;      // [EB][LDP]
-    float* sck = sX + EB * LDP;     // [EB]
+    float* sC = sX + EB * LDP;      // [EB][LDP] column-sum terms
+    float* sck = sC + EB * LDP;     // [EB]
     float* scq = sck + EB;          // [EB]
-    float* slse = scq + EB;         // [EB]
+    float* slse = scq + EB;         // [EB] lse (E) or zeta
     float* sD = slse + EB;          // [EB]
     float* sckl = sD + EB;          // [EB] residuals of the running sums
     float* scql = sckl + EB;        // [EB]
@@ -190,7 +222,7 @@ __global__ void __launch_bounds__(256) e_bwd_dkdv_kernel(
             scq[i] = t < T ? cum[bh * T + t] : 0.f;
             scql[i] = t < T ? cum_lo[bh * T + t] : 0.f;
             slse[i] = t < T ? lse[bh * T + t] : 0.f;
-            sD[i] = t < T ? Dvec[bh * T + t] : 0.f;
+            sD[i] = (t < T && Dvec) ? Dvec[bh * T + t] : 0.f;
         }
         __syncthreads();
 #pragma unroll
@@ -199,7 +231,7 @@ __global__ void __launch_bounds__(256) e_bwd_dkdv_kernel(
             for (int s = 0; s < 4; ++s) {
                 const int i = ti + 16 * r, j = tc + 16 * s;
                 const long ig = (long)qb * EB + i, jg = (long)kb * EB + j;
-                float P = 0.f, dX = 0.f;
+                float P = 0.f, dX = 0.f, cterm = 0.f;
                 if (jg <= ig && ig < T) {
                     float dot = 0.f;
 #pragma unroll 16
@@ -207,11 +239,22 @@ __global__ void __launch_bounds__(256) e_bwd_dkdv_kernel(
                     float dP = 0.f;
 #pragma unroll 16
                     for (int cc = 0; cc < DV; ++cc) dP = fmaf(sdo[i * LDV + cc], sv[j * LDV + cc], dP);
-                    P = __expf(scale * dot + (scq[i] - sck[j]) + (scql[i] - sckl[j]) - slse[i]);
-                    dX = P * (dP - sD[i]);
+                    if constexpr (KIND == ATTN_E) {
+                        P = __expf(scale * dot + (scq[i] - sck[j]) + (scql[i] - sckl[j]) - slse[i]);
+                        dX = P * (dP - sD[i]);
+                        cterm = dX;
+                    } else {   // slse holds zeta
+                        const float e = expf((scq[i] - sck[j]) + (scql[i] - sckl[j]));
+                        const float dw = slse[i] * (dP - sD[i]);
+                        const float w = KIND == ATTN_P2 ? dot * dot * e : dot * e;
+                        P = w * slse[i];
+                        dX = (KIND == ATTN_P2 ? 2.f * dot * e : e) * dw;
+                        cterm = w * dw;
+                    }
                 }
                 sP[i * LDP + j] = P;
                 sX[i * LDP + j] = dX;
+                sC[i * LDP + j] = cterm;
             }
         __syncthreads();
         for (int i = 0; i < EB; ++i) {
@@ -224,7 +267,7 @@ __global__ void __launch_bounds__(256) e_bwd_dkdv_kernel(
             for (int r = 0; r < 4; ++r) {
                 const int j = ti + 16 * r;
                 const float p = sP[i * LDP + j], dx = sX[i * LDP + j];
-                cs[r] += dx;
+                cs[r] += sC[i * LDP + j];
 #pragma unroll
                 for (int s = 0; s < NN; ++s) adk[r][s] = fmaf(dx, qn[s], adk[r][s]);
 #pragma unroll
@@ -245,7 +288,7 @@ __global__ void __launch_bounds__(256) e_bwd_dkdv_kernel(
 }
 
 // dq and row sums of dx for one block of 64 queries, looping over key blocks.
-template <int D, int DV, typename Tin>
+template <int KIND, int D, int DV, typename Tin>
 __global__ void __launch_bounds__(256) e_bwd_dq_kernel(
     const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
     const float* __restrict__ cum, const float* __restrict__ cum_lo, const float* __restrict__ lse,
@@ -281,7 +324,7 @@ __global__ void __launch_bounds__(256) e_bwd_dq_kernel(
         scq[i] = t < T ? cum[bh * T + t] : 0.f;
         scql[i] = t < T ? cum_lo[bh * T + t] : 0.f;
         slse[i] = t < T ? lse[bh * T + t] : 0.f;
-        sD[i] = t < T ? Dvec[bh * T + t] : 0.f;
+        sD[i] = (t < T && Dvec) ? Dvec[bh * T + t] : 0.f;
     }
     float adq[4][NN], rs[4];
 #pragma unroll
@@ -314,7 +357,7 @@ __global__ void __launch_bounds__(256) e_bwd_dq_kernel(
             for (int s = 0; s < 4; ++s) {
                 const int i = ti + 16 * r, j = tc + 16 * s;
                 const long ig = (long)qb * EB + i, jg = (long)kb * EB + j;
-                float dX = 0.f;
+                float dX = 0.f, rterm = 0.f;
                 if (jg <= ig && ig < T) {
                     float dot = 0.f;
 #pragma unroll 16
@@ -322,11 +365,19 @@ __global__ void __launch_bounds__(256) e_bwd_dq_kernel(
                     float dP = 0.f;
 #pragma unroll 16
                     for (int cc = 0; cc < DV; ++cc) dP = fmaf(sdo[i * LDV + cc], sv[j * LDV + cc], dP);
-                    const float P = __expf(scale * dot + (scq[i] - sck[j]) + (scql[i] - sckl[j]) - slse[i]);
-                    dX = P * (dP - sD[i]);
+                    if constexpr (KIND == ATTN_E) {
+                        const float P = __expf(scale * dot + (scq[i] - sck[j]) + (scql[i] - sckl[j]) - slse[i]);
+                        dX = P * (dP - sD[i]);
+                        rterm = dX;
+                    } else {   // slse holds zeta
+                        const float e = expf((scq[i] - sck[j]) + (scql[i] - sckl[j]));
+                        const float dw = slse[i] * (dP - sD[i]);
+                        dX = (KIND == ATTN_P2 ? 2.f * dot * e : e) * dw;
+                        rterm = (KIND == ATTN_P2 ? dot * dot * e : dot * e) * dw;
+                    }
                 }
                 sX[i * LDP + j] = dX;
-                rs[r] += dX;
+                rs[r] += rterm;
             }
         __syncthreads();
         for (int j = 0; j < EB; ++j) {
@@ -354,21 +405,21 @@ __global__ void __launch_bounds__(256) e_bwd_dq_kernel(
     }
 }
 
-template <int D, int DV, typename Tin>
+template <int KIND, int D, int DV, typename Tin>
 static cudaError_t run_e_fwd(const Problem& p, const void* q, const void* k, const void* v,
                              const float* cum, const float* cum_lo, float scale, void* o, float* lse,
                              cudaStream_t s) {
     const size_t smem = sizeof(float) * (size_t)(2 * EB * (D + 1) + EB * DV + EB * (EB + 1) + 4 * EB);
-    auto kern = e_fwd_kernel<D, DV, Tin>;
+    auto kern = e_fwd_kernel<KIND, D, DV, Tin>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((p.T + EB - 1) / EB, (unsigned)p.BH());
     kern<<<grid, 256, smem, s>>>((const Tin*)q, (const Tin*)k, (const Tin*)v, cum, cum_lo, scale, (float*)o, lse,
-                                 p.T);
+                                 p.T, p.normalize ? 1 : 0);
     return cudaGetLastError();
 }
 
-template <int D, int DV, typename Tin>
+template <int KIND, int D, int DV, typename Tin>
 static cudaError_t run_e_bwd(const Problem& p, const void* q, const void* k, const void* v,
                              const float* cum, const float* cum_lo, const float* lse, const float* Dvec,
                              const void* dO, float scale, void* dq, void* dk, void* dv, float* rowsum,
@@ -377,8 +428,8 @@ static cudaError_t run_e_bwd(const Problem& p, const void* q, const void* k, con
     dim3 grid(NQB, (unsigned)p.BH());
     {
         const size_t smem = sizeof(float) * (size_t)(2 * EB * (D + 1) + 2 * EB * (DV + 1) +
-                                                     2 * EB * (EB + 1) + 6 * EB);
-        auto kern = e_bwd_dkdv_kernel<D, DV, Tin>;
+                                                     3 * EB * (EB + 1) + 6 * EB);
+        auto kern = e_bwd_dkdv_kernel<KIND, D, DV, Tin>;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         kern<<<grid, 256, smem, s>>>((const Tin*)q, (const Tin*)k, (const Tin*)v, cum, cum_lo, lse, Dvec,
@@ -389,7 +440,7 @@ static cudaError_t run_e_bwd(const Problem& p, const void* q, const void* k, con
     {
         const size_t smem = sizeof(float) * (size_t)(2 * EB * (D + 1) + 2 * EB * (DV + 1) +
                                                      EB * (EB + 1) + 6 * EB);
-        auto kern = e_bwd_dq_kernel<D, DV, Tin>;
+        auto kern = e_bwd_dq_kernel<KIND, D, DV, Tin>;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         kern<<<grid, 256, smem, s>>>((const Tin*)q, (const Tin*)k, (const Tin*)v, cum, cum_lo, lse, Dvec,
@@ -416,15 +467,44 @@ static cudaError_t run_e_bwd(const Problem& p, const void* q, const void* k, con
 
 cudaError_t simt_e_fwd(const Problem& p, const void* q, const void* k, const void* v,
                        const float* cum, const float* cum_lo, float scale, void* o, float* lse, cudaStream_t s) {
-    TM2_E_DISPATCH(p, (run_e_fwd<D, D, Tin>(p, q, k, v, cum, cum_lo, scale, o, lse, s)));
+    TM2_E_DISPATCH(p, (run_e_fwd<ATTN_E, D, D, Tin>(p, q, k, v, cum, cum_lo, scale, o, lse, s)));
 }
 
 cudaError_t simt_e_bwd(const Problem& p, const void* q, const void* k, const void* v,
                        const float* cum, const float* cum_lo, const float* lse, const float* Dvec,
                        const void* dO, float scale, void* dq, void* dk, void* dv, float* rowsum,
                        float* colsum, cudaStream_t s) {
-    TM2_E_DISPATCH(p, (run_e_bwd<D, D, Tin>(p, q, k, v, cum, cum_lo, lse, Dvec, dO, scale, dq, dk, dv,
-                                            rowsum, colsum, s)));
+    TM2_E_DISPATCH(p, (run_e_bwd<ATTN_E, D, D, Tin>(p, q, k, v, cum, cum_lo, lse, Dvec, dO, scale, dq, dk, dv,
+                                                    rowsum, colsum, s)));
+}
+
+template <int KIND>
+static cudaError_t simt_poly_fwd_k(const Problem& p, const void* q, const void* k, const void* v, const float* cum,
+                                   const float* cum_lo, void* o, float* Z, cudaStream_t s) {
+    TM2_E_DISPATCH(p, (run_e_fwd<KIND, D, D, Tin>(p, q, k, v, cum, cum_lo, 1.f, o, Z, s)));
+}
+
+template <int KIND>
+static cudaError_t simt_poly_bwd_k(const Problem& p, const void* q, const void* k, const void* v, const float* cum,
+                                   const float* cum_lo, const float* zeta, const float* Dvec, const void* dO, void* dq,
+                                   void* dk, void* dv, float* rowsum, float* colsum, cudaStream_t s) {
+    TM2_E_DISPATCH(p, (run_e_bwd<KIND, D, D, Tin>(p, q, k, v, cum, cum_lo, zeta, Dvec, dO, 1.f, dq, dk, dv, rowsum,
+                                                  colsum, s)));
+}
+
+cudaError_t simt_poly_fwd(const Problem& p, int order, const void* q, const void* k, const void* v,
+                          const float* cum, const float* cum_lo, void* o, float* Z, cudaStream_t s) {
+    if (order == 2) return simt_poly_fwd_k<ATTN_P2>(p, q, k, v, cum, cum_lo, o, Z, s);
+    if (order == 1) return simt_poly_fwd_k<ATTN_P1>(p, q, k, v, cum, cum_lo, o, Z, s);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t simt_poly_bwd(const Problem& p, int order, const void* q, const void* k, const void* v,
+                          const float* cum, const float* cum_lo, const float* zeta, const float* D, const void* dO,
+                          void* dq, void* dk, void* dv, float* rowsum, float* colsum, cudaStream_t s) {
+    if (order == 2) return simt_poly_bwd_k<ATTN_P2>(p, q, k, v, cum, cum_lo, zeta, D, dO, dq, dk, dv, rowsum, colsum, s);
+    if (order == 1) return simt_poly_bwd_k<ATTN_P1>(p, q, k, v, cum, cum_lo, zeta, D, dO, dq, dk, dv, rowsum, colsum, s);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace tm2

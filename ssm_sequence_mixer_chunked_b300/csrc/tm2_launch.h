@@ -120,6 +120,30 @@ cudaError_t launch_decode_step(int N, int H, int d, int dv, int dtype, bool norm
                                const void* q, const void* k, const void* v, const float* a,
                                float* S, float* z, void* o, float* Z, cudaStream_t s);
 
+// ---- attention-form kernels: 2Mamba-E and the quadratic (C = T) form of 2Mamba -----
+// KIND of the tensor-core and CUDA-core attention-form kernels: 2Mamba-E (softmax of
+// scale q.k + cumA_i - cumA_j), the first-order mixer (w = q.k exp(cumA_i - cumA_j)) and
+// 2Mamba (w = (q.k)^2 exp(cumA_i - cumA_j)).
+enum AttnKind { ATTN_E = 0, ATTN_P1 = 1, ATTN_P2 = 2 };
+
+// Quadratic-form mixer of order 1 or 2 (p.normalize: o = N / Z) on the tensor cores (bf16,
+// d = dv = 64) and on CUDA cores (fp32 arithmetic, any supported d): cum / cum_lo as for
+// 2Mamba-E; o (BH,T,64 or dv) fp32, Z (BH,T) fp32 always written.
+cudaError_t tc_poly_fwd(const Problem& p, int order, const void* q, const void* k, const void* v, const float* cum,
+                        const float* cum_lo, float* o, float* Z, cudaStream_t s);
+cudaError_t simt_poly_fwd(const Problem& p, int order, const void* q, const void* k, const void* v,
+                          const float* cum, const float* cum_lo, void* o, float* Z, cudaStream_t s);
+// Backward: zeta = 1/Z (normalised) or 1 and D = dO . o (normalised) or 0 per token (launch_poly_prep);
+// rowsum / colsum the two A-mask axis sums of w_ij dw_ij, dw_ij = zeta_i (dO_i . v_j - D_i).
+cudaError_t launch_poly_prep(const Problem& p, const float* o, const float* Z, const void* dO, float* D,
+                             float* zeta, cudaStream_t s);
+cudaError_t tc_poly_bwd(const Problem& p, int order, const void* q, const void* k, const void* v, const float* cum,
+                        const float* cum_lo, const float* zeta, const float* D, const void* dO, float* dq, float* dk,
+                        float* dv, float* rowsum, float* colsum, cudaStream_t s);
+cudaError_t simt_poly_bwd(const Problem& p, int order, const void* q, const void* k, const void* v,
+                          const float* cum, const float* cum_lo, const float* zeta, const float* D, const void* dO,
+                          void* dq, void* dk, void* dv, float* rowsum, float* colsum, cudaStream_t s);
+
 // ---- 2Mamba-E ----------------------------------------------------------------------
 // The forward entry points' shared steps (tm2_api.cu): argument checks (fills p; TM2_OK with
 // p.BH() == 0 or T == 0 means nothing to do), the scratch size, and the launch sequence over a

@@ -422,6 +422,39 @@ __global__ void rowdot_kernel(const float* __restrict__ o, const Tin* __restrict
     if (lane == 0) out[tok] = D;
 }
 
+// Backward preparation of the quadratic-form mixers, one warp per token: D = dO . o and
+// zeta = 1/Z (0 where Z = 0) when normalised, D = 0 and zeta = 1 otherwise.
+template <typename Tin>
+__global__ void poly_prep_kernel(const float* __restrict__ o, const float* __restrict__ Z,
+                                 const Tin* __restrict__ dO, float* __restrict__ Dv, float* __restrict__ zeta,
+                                 long ntok, int dv, bool normalize) {
+    const long tok = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (tok >= ntok) return;
+    float D = 0.f;
+    if (normalize) {
+        for (int c = lane; c < dv; c += 32) D += to_f(dO[tok * dv + c]) * o[tok * dv + c];
+        D = warp_sum(D);
+    }
+    if (lane == 0) {
+        const float z = normalize ? Z[tok] : 1.f;
+        Dv[tok] = D;
+        zeta[tok] = z != 0.f ? 1.f / z : 0.f;
+    }
+}
+
+cudaError_t launch_poly_prep(const Problem& p, const float* o, const float* Z, const void* dO, float* D,
+                             float* zeta, cudaStream_t s) {
+    const long ntok = p.BH() * p.T;
+    const unsigned blocks = (unsigned)((ntok + 7) / 8);
+    if (p.dtype == 1)
+        poly_prep_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(o, Z, (const __nv_bfloat16*)dO, D, zeta, ntok, p.dv,
+                                                              p.normalize);
+    else
+        poly_prep_kernel<float><<<blocks, 256, 0, s>>>(o, Z, (const float*)dO, D, zeta, ntok, p.dv, p.normalize);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_rowdot(const Problem& p, const void* o, const void* dO, float* Dvec,
                           cudaStream_t s) {
     const long ntok = p.BH() * p.T;

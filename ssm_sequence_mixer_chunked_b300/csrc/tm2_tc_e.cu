@@ -26,6 +26,16 @@
 // terms are staged once in shared memory.  Only the diagonal block is masked.
 // Warps 0-7 compute (warp w: lane quadrant w % 4, key half w / 4), warp 8 issues TMA, warp 9
 // the MMAs.  Every mbarrier wait is bounded (TM2_ERR_TIMEOUT on expiry).
+//
+// The same kernel, instantiated with KIND = ATTN_P2 or ATTN_P1, evaluates the 2Mamba mixer in
+// its quadratic (C = T) form ("2Mamba2Furious", Sec. 1-2: the quadratic form costs O(T^2) but,
+// with d = 64, fewer flops than the chunked form below T = 4 d^2 dv / (d + dv) = 8192; Sec. 5:
+// the square on the QK product, the A-mask on the squared scores), or the first-order mixer
+// with the same mask (Sec. 4, Mamba-2S: the score itself, not its square):
+//   w_ij = (q_i . k_j)^p exp(cumA_i - cumA_j)  (j <= i),  N_i = sum_j w_ij v_j,  Z_i = sum_j w_ij,
+// o = N / Z (normalised) or N, with Z saved.  The weights are never exponentiated scores, so
+// there is no running maximum and no rescale: w = s^p 2^(crr - kw) with the decay in log2 units,
+// split into bf16 hi + lo exactly as P above, Z summing the rounded weights.
 #include "tm2.h"
 #include "tm2_launch.h"
 #include "tm2_sm100.cuh"
@@ -59,20 +69,22 @@ struct Args {
     const float* cum;    // [BH][T] inclusive running sum of -softplus(a), fp32
     const float* cum_lo; // [BH][T] its rounding residual
     float* o;            // [BH][T][64]
-    float* lse;          // [BH][T]
+    float* aux;          // [BH][T]: lse (ATTN_E) or the normaliser Z (ATTN_P1, ATTN_P2)
     int* status;
     int T, NQ, BH;
-    float scale;
+    float scale;         // logit scale (ATTN_E)
+    int normalize;       // o = N / Z (ATTN_P1, ATTN_P2)
 };
 
 }  // namespace tce
 
 using namespace tce;
 
-__global__ void __launch_bounds__(THREADS, 1) tc_e_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
-                                                              const __grid_constant__ CUtensorMap tmK,
-                                                              const __grid_constant__ CUtensorMap tmV,
-                                                              const __grid_constant__ Args a) {
+template <int KIND>
+__global__ void __launch_bounds__(THREADS, 1) tc_attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
+                                                                 const __grid_constant__ CUtensorMap tmK,
+                                                                 const __grid_constant__ CUtensorMap tmV,
+                                                                 const __grid_constant__ Args a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_align1024(smem_raw);
     __shared__ __align__(8) uint64_t bar_q, bar_full[NS], bar_empty[NS], bar_sfull[2], bar_sfree[2], bar_pfull[2],
@@ -215,6 +227,41 @@ __global__ void __launch_bounds__(THREADS, 1) tc_e_fwd_kernel(const __grid_const
             tc_fence_before();
             mbar_arrive(smem_u32(&bar_sfree[x]));        // the score buffer may take block b+2
             const float4* kw4 = reinterpret_cast<const float4*>(sKW + x * BK + h * 64);
+            if constexpr (KIND != ATTN_E) {
+                // w = s^p 2^(crr - kw) over this thread's 64 keys; in the diagonal block key
+                // h 64 + c is visible to row l when h 64 + c <= l.  P_hi into P buffer x, P_lo over
+                // this thread's score columns 0-31 (its 64 scores are in registers).
+#pragma unroll
+                for (int r8 = 0; r8 < 4; ++r8) {
+                    uint32_t ph[8], pl[8];
+                    const float4 w0 = kw4[4 * r8], w1 = kw4[4 * r8 + 1], w2 = kw4[4 * r8 + 2], w3 = kw4[4 * r8 + 3];
+                    const float kwv[16] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w,
+                                           w2.x, w2.y, w2.z, w2.w, w3.x, w3.y, w3.z, w3.w};
+#pragma unroll
+                    for (int c8 = 0; c8 < 8; ++c8) {
+                        float pw[2];
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const int c = 16 * r8 + 2 * c8 + u;
+                            const float sv = s[c];
+                            const float e = (b > 0 || h * 64 + c <= l) ? exp2f(crr - kwv[2 * c8 + u]) : 0.f;
+                            pw[u] = KIND == ATTN_P2 ? sv * sv * e : sv * e;
+                        }
+                        const uint32_t h2 = pack_bf16x2(pw[0], pw[1]);
+                        const float h0 = __uint_as_float(h2 << 16), h1 = __uint_as_float(h2 & 0xffff0000u);
+                        const uint32_t l2 = pack_bf16x2(pw[0] - h0, pw[1] - h1);
+                        lsum += (h0 + __uint_as_float(l2 << 16)) + (h1 + __uint_as_float(l2 & 0xffff0000u));
+                        ph[c8] = h2;
+                        pl[c8] = l2;
+                    }
+                    tmem_st8(tmem + lane_base + TM_P + x * 64 + h * 32 + 8 * r8, ph);
+                    tmem_st8(tmem + lane_base + TM_S + x * 128 + h * 64 + 8 * r8, pl);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(smem_u32(&bar_pfull[x]));
+                continue;
+            }
             float bmax = -INFINITY;
             if (b == 0) {   // the diagonal block: key h 64 + c is visible to row l when h 64 + c <= l
 #pragma unroll
@@ -303,7 +350,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_e_fwd_kernel(const __grid_const
             tc_fence_before();
             mbar_arrive(smem_u32(&bar_pfull[x]));
         }
-        // ---- o = O / l, lse = m + log l (the two halves' sums combined)
+        // ---- o = O / l, lse = m + log l (E) or o = N / Z, Z (the two halves' sums combined)
         if (ok) sSum[h * BQ + l] = lsum;
         named_bar_sync(2, 256);
         if (ok && !abort_s && (ok = mbar_wait(smem_u32(&bar_ofull), 0, a.status))) {
@@ -312,12 +359,14 @@ __global__ void __launch_bounds__(THREADS, 1) tc_e_fwd_kernel(const __grid_const
             float ov[32];
             tmem_ld32(tmem + lane_base + TM_O + h * 32, ov);
             if (i < a.T) {
-                const float inv = lt > 0.f ? 1.f / lt : 0.f;
+                float inv;
+                if constexpr (KIND == ATTN_E) inv = lt > 0.f ? 1.f / lt : 0.f;
+                else inv = a.normalize ? (lt != 0.f ? 1.f / lt : 0.f) : 1.f;
                 float4* dst = reinterpret_cast<float4*>(a.o + (bh * a.T + i) * 64 + h * 32);
 #pragma unroll
                 for (int u = 0; u < 8; ++u)
                     dst[u] = make_float4(ov[4 * u] * inv, ov[4 * u + 1] * inv, ov[4 * u + 2] * inv, ov[4 * u + 3] * inv);
-                if (h == 0) a.lse[bh * a.T + i] = m_used * LN2 + __logf(lt);
+                if (h == 0) a.aux[bh * a.T + i] = KIND == ATTN_E ? m_used * LN2 + __logf(lt) : lt;
             }
         }
         if (!ok) abort_s = 1;
@@ -327,8 +376,10 @@ __global__ void __launch_bounds__(THREADS, 1) tc_e_fwd_kernel(const __grid_const
     if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
-cudaError_t tc_e_fwd(const Problem& p, const void* q, const void* k, const void* v, const float* cum,
-                     const float* cum_lo, float scale, float* o, float* lse, cudaStream_t s) {
+template <int KIND>
+static cudaError_t launch_attn_fwd(const Problem& p, const void* q, const void* k, const void* v, const float* cum,
+                                   const float* cum_lo, float scale, int normalize, float* o, float* aux,
+                                   cudaStream_t s) {
     CUtensorMap tq, tk, tv;
     const uint64_t BH = (uint64_t)p.BH(), T = (uint64_t)p.T;
     if (!make_tmap_bf16_3d(&tq, q, BH, T, 64, BQ) || !make_tmap_bf16_3d(&tk, k, BH, T, 64, BK) ||
@@ -337,12 +388,26 @@ cudaError_t tc_e_fwd(const Problem& p, const void* q, const void* k, const void*
     int* status = tc_status_ptr();
     if (!status) return cudaErrorInvalidValue;
     const int NQ = (p.T + BQ - 1) / BQ;
-    Args a{cum, cum_lo, o, lse, status, p.T, NQ, (int)p.BH(), scale};
-    cudaError_t e = cudaFuncSetAttribute(tc_e_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    Args a{cum, cum_lo, o, aux, status, p.T, NQ, (int)p.BH(), scale, normalize};
+    cudaError_t e = cudaFuncSetAttribute(tc_attn_fwd_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         SMEM_BYTES);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)NQ, (unsigned)p.BH());
-    tc_e_fwd_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(tq, tk, tv, a);
+    tc_attn_fwd_kernel<KIND><<<grid, THREADS, SMEM_BYTES, s>>>(tq, tk, tv, a);
     return cudaGetLastError();
+}
+
+cudaError_t tc_e_fwd(const Problem& p, const void* q, const void* k, const void* v, const float* cum,
+                     const float* cum_lo, float scale, float* o, float* lse, cudaStream_t s) {
+    return launch_attn_fwd<ATTN_E>(p, q, k, v, cum, cum_lo, scale, 0, o, lse, s);
+}
+
+cudaError_t tc_poly_fwd(const Problem& p, int order, const void* q, const void* k, const void* v, const float* cum,
+                        const float* cum_lo, float* o, float* Z, cudaStream_t s) {
+    const int nrm = p.normalize ? 1 : 0;
+    if (order == 2) return launch_attn_fwd<ATTN_P2>(p, q, k, v, cum, cum_lo, 1.f, nrm, o, Z, s);
+    if (order == 1) return launch_attn_fwd<ATTN_P1>(p, q, k, v, cum, cum_lo, 1.f, nrm, o, Z, s);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace tm2

@@ -22,6 +22,13 @@
 // compute warps work on s - 1 and the gradient products of s - 2 drain, so the softmax step
 // overlaps the tensor core (a whole 128-token block needs 256 columns for scores + dP and
 // cannot be double-buffered beside the operands and accumulators).
+// Instantiated with KIND = ATTN_P2 or ATTN_P1 the same kernels are the backward of the
+// quadratic (C = T) form of 2Mamba and of the first-order mixer (App. C / C.1):
+//   w_ij = s_ij^p e_ij, e_ij = exp(cumA_i - cumA_j),  dw_ij = zeta_i (dO_i . v_j - D_i),
+//   dv_j += w_ij zeta_i dO_i,  ds_ij = p s_ij^(p-1) e_ij dw_ij,  dq_i = sum_j ds_ij k_j,
+//   dk_j = sum_i ds_ij q_i,  row / column sums of w_ij dw_ij for the A-mask gradient,
+// with zeta = 1/Z and D = dO . o when normalised (zeta = 1, D = 0 otherwise): P and dx of the
+// softmax step become w zeta and ds.
 // The per-token terms of the walked sub-blocks are staged in shared memory.  Warps 0-7
 // compute (warp w: lane quadrant w % 4, half w / 4 of the sub-block's 64 tokens), warp 8
 // issues TMA, warp 9 the MMAs.  Every mbarrier wait is bounded (TM2_ERR_TIMEOUT on expiry).
@@ -43,7 +50,7 @@ constexpr int TILE = BT * 128;               // [128][64] bf16
 constexpr int STAGE = 2 * TILE;
 constexpr int SFIX = 0;                      // this CTA's two tiles (K, V or Q, dO)
 constexpr int SSTG = 2 * TILE;
-constexpr int SSC = SSTG + NS * STAGE;       // [2 buffers][4 arrays][128] per-token scalars
+constexpr int SSC = SSTG + NS * STAGE;       // [2 buffers][3 arrays][64] per-token scalars (room for 4 x 128)
 constexpr int SRED = SSC + 2 * 4 * BT * 4;   // [2 halves][128]
 constexpr int SMEM_BYTES = SRED + 2 * BT * 4 + 1024;
 // tensor memory: sub-block buffer u at 128 u holds the scores (columns 0-63) and dP (64-127);
@@ -59,8 +66,8 @@ constexpr uint32_t IDESC_MN = idesc_bf16_f32(128, 64, false, true);
 struct Args {
     const float* cum;      // [BH][T] running sums of -softplus(a), fp32
     const float* cum_lo;   // [BH][T] their rounding residuals
-    const float* lse;      // [BH][T]
-    const float* Dv;       // [BH][T] dO . o
+    const float* lse;      // [BH][T]: lse (ATTN_E) or zeta (ATTN_P1, ATTN_P2)
+    const float* Dv;       // [BH][T] dO . o (null: 0)
     float* g1;             // dk kernel: dk [BH][T][64]; dq kernel: dq
     float* g2;             // dk kernel: dv [BH][T][64]; dq kernel: unused
     float* sums;           // dk kernel: column sums [BH][T]; dq kernel: row sums
@@ -80,10 +87,13 @@ using namespace tceb;
 // lse) or crr - W (query tiles: crr holds the query's, W the key's).  Masked blocks zero the
 // entries outside lo <= tt < hi.  Writes P hi, P lo (key tiles), dx hi, dx lo as packed bf16
 // pairs.
-template <bool kd, bool masked>
+// For KIND = ATTN_P1 / ATTN_P2 the bias is the decay exponent alone (W and crr hold running
+// sums, no lse), Zq / Zr the walked queries' / this query's zeta, and P, dx become w zeta and ds.
+template <int KIND, bool kd, bool masked>
 __device__ __forceinline__ void softmax_grad16(const float* s, const float* dp, const float* W, const float* Dq,
-                                               float crr, float Dr, float sl2, int tt0, int lo, int hi, float& sum,
-                                               uint32_t* ph, uint32_t* pl, uint32_t* dh, uint32_t* dl) {
+                                               const float* Zq, float crr, float Dr, float Zr, float sl2, int tt0,
+                                               int lo, int hi, float& sum, uint32_t* ph, uint32_t* pl, uint32_t* dh,
+                                               uint32_t* dl) {
 #pragma unroll
     for (int c2 = 0; c2 < 8; ++c2) {
         float pv[2], dx[2];
@@ -91,12 +101,23 @@ __device__ __forceinline__ void softmax_grad16(const float* s, const float* dp, 
         for (int u = 0; u < 2; ++u) {
             const int cc = 2 * c2 + u;
             const float bias = kd ? W[cc] - crr : crr - W[cc];
-            float P = exp2f(fmaf(sl2, s[cc], bias));
-            if (masked && !(tt0 + cc >= lo && tt0 + cc < hi)) P = 0.f;
-            const float g = P * (dp[cc] - (kd ? Dq[cc] : Dr));
-            sum += g;
-            pv[u] = P;
-            dx[u] = g;
+            const bool vis = !masked || (tt0 + cc >= lo && tt0 + cc < hi);
+            const float Dd = kd ? Dq[cc] : Dr;
+            if constexpr (KIND == ATTN_E) {
+                const float P = vis ? exp2f(fmaf(sl2, s[cc], bias)) : 0.f;
+                const float g = P * (dp[cc] - Dd);
+                sum += g;
+                pv[u] = P;
+                dx[u] = g;
+            } else {
+                const float e = vis ? exp2f(bias) : 0.f;
+                const float sv = s[cc];
+                const float dw = (kd ? Zq[cc] : Zr) * (dp[cc] - Dd);
+                const float w = KIND == ATTN_P2 ? sv * sv * e : sv * e;
+                sum += w * dw;
+                pv[u] = w * (kd ? Zq[cc] : Zr);
+                dx[u] = (KIND == ATTN_P2 ? 2.f * sv * e : e) * dw;
+            }
         }
         if (kd) {
             const uint32_t p2 = pack_bf16x2(pv[0], pv[1]);
@@ -110,12 +131,12 @@ __device__ __forceinline__ void softmax_grad16(const float* s, const float* dp, 
 }
 
 // kd = true: the key-tile kernel (dk, dv, column sums); false: the query-tile kernel (dq, row sums)
-template <bool kd>
-__global__ void __launch_bounds__(THREADS, 1) tc_e_bwd_kernel(const __grid_constant__ CUtensorMap tmA,
-                                                              const __grid_constant__ CUtensorMap tmB,
-                                                              const __grid_constant__ CUtensorMap tmC,
-                                                              const __grid_constant__ CUtensorMap tmD,
-                                                              const __grid_constant__ Args a) {
+template <int KIND, bool kd>
+__global__ void __launch_bounds__(THREADS, 1) tc_attn_bwd_kernel(const __grid_constant__ CUtensorMap tmA,
+                                                                 const __grid_constant__ CUtensorMap tmB,
+                                                                 const __grid_constant__ CUtensorMap tmC,
+                                                                 const __grid_constant__ CUtensorMap tmD,
+                                                                 const __grid_constant__ Args a) {
     // kd: A = K, B = V (this CTA's tiles), C = Q, D = dO (walked)
     // dq: A = Q, B = dO (this CTA's tiles), C = K, D = V (walked)
     extern __shared__ uint8_t smem_raw[];
@@ -261,28 +282,34 @@ __global__ void __launch_bounds__(THREADS, 1) tc_e_bwd_kernel(const __grid_const
         constexpr float LOG2E = 1.4426950408889634f;
         const long t_ref = base + (long)tile * BT;
         const float ref = a.cum[t_ref], reflo = a.cum_lo[t_ref];
-        float crr = 0.f, Dr = 0.f;
+        constexpr bool E = KIND == ATTN_E;
+        float crr = 0.f, Dr = 0.f, Zr = 0.f;
         if (rin) {
             const float off = (a.cum[base + r] - ref) + (a.cum_lo[base + r] - reflo);
-            crr = kd ? off * LOG2E : (off - a.lse[base + r]) * LOG2E;
-            if (!kd) Dr = a.Dv[base + r];
+            crr = (kd || !E) ? off * LOG2E : (off - a.lse[base + r]) * LOG2E;
+            if (!kd) {
+                Dr = a.Dv ? a.Dv[base + r] : 0.f;
+                if (!E) Zr = a.lse[base + r];
+            }
         }
         const float sl2 = a.scale * LOG2E;
         float sum = 0.f;
         int kg = 0;
         bool ok = true;
         const int nsb = 2 * nblk;
-        // per-token term of walked sub-block j held by this thread (threads below 64 or 128):
-        // arrays W at [0, 64) and D at [64, 128) of a staging buffer
-        const bool stager = threadIdx.x < (kd ? 2 : 1) * SUB;
+        // per-token term of walked sub-block j held by this thread: arrays W at [0, 64), D at
+        // [64, 128) and (key tiles of the polynomial kinds) zeta at [128, 192) of a staging buffer
+        constexpr int NARR = kd ? (E ? 2 : 3) : 1;
+        const bool stager = threadIdx.x < NARR * SUB;
         const int arr = threadIdx.x >> 6, tt_st = threadIdx.x & 63;
         auto term = [&](int j) {
             const long t = (long)blk0 * BT + (long)j * SUB + tt_st;
             float val = 0.f;
             if (t < a.T) {
                 const float off = (a.cum[base + t] - ref) + (a.cum_lo[base + t] - reflo);
-                if (arr == 1) val = a.Dv[base + t];
-                else val = kd ? (off - a.lse[base + t]) * LOG2E : off * LOG2E;
+                if (arr == 1) val = a.Dv ? a.Dv[base + t] : 0.f;
+                else if (arr == 2) val = a.lse[base + t];
+                else val = (kd && E) ? (off - a.lse[base + t]) * LOG2E : off * LOG2E;
             }
             return val;
         };
@@ -291,7 +318,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_e_bwd_kernel(const __grid_const
             const int x = sbk & 1, u = sbk % NB;
             const long t0 = (long)blk0 * BT + (long)sbk * SUB;
             // the walked sub-block's terms into buffer x; the next one's loads fly meanwhile
-            float* sc = sSc + x * 2 * SUB;
+            float* sc = sSc + x * 3 * SUB;
             if (stager) {
                 sc[arr * SUB + tt_st] = nxt;
                 if (sbk + 1 < nsb) nxt = term(sbk + 1);
@@ -309,7 +336,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_e_bwd_kernel(const __grid_const
 #pragma unroll 1
             for (int q4 = 0; q4 < 2; ++q4) {
                 const int tt0 = h * 32 + q4 * 16;
-                float s[16], dp[16], W[16], Dq[16];
+                float s[16], dp[16], W[16], Dq[16], Zq[16];
                 tmem_ld16(bufc + tt0, s);
                 tmem_ld16(bufc + 64 + tt0, dp);
 #pragma unroll
@@ -319,13 +346,17 @@ __global__ void __launch_bounds__(THREADS, 1) tc_e_bwd_kernel(const __grid_const
                     if (kd) {
                         const float4 d4 = reinterpret_cast<const float4*>(sc + SUB + tt0)[v4];
                         Dq[4 * v4] = d4.x, Dq[4 * v4 + 1] = d4.y, Dq[4 * v4 + 2] = d4.z, Dq[4 * v4 + 3] = d4.w;
+                        if (!E) {
+                            const float4 z4 = reinterpret_cast<const float4*>(sc + 2 * SUB + tt0)[v4];
+                            Zq[4 * v4] = z4.x, Zq[4 * v4 + 1] = z4.y, Zq[4 * v4 + 2] = z4.z, Zq[4 * v4 + 3] = z4.w;
+                        }
                     }
                 }
                 uint32_t ph[8], pl[8], dh[8], dl[8];
                 if (masked)
-                    softmax_grad16<kd, true>(s, dp, W, Dq, crr, Dr, sl2, tt0, lo, hi, sum, ph, pl, dh, dl);
+                    softmax_grad16<KIND, kd, true>(s, dp, W, Dq, Zq, crr, Dr, Zr, sl2, tt0, lo, hi, sum, ph, pl, dh, dl);
                 else
-                    softmax_grad16<kd, false>(s, dp, W, Dq, crr, Dr, sl2, tt0, lo, hi, sum, ph, pl, dh, dl);
+                    softmax_grad16<KIND, kd, false>(s, dp, W, Dq, Zq, crr, Dr, Zr, sl2, tt0, lo, hi, sum, ph, pl, dh, dl);
                 if (kd) {   // over this round's score columns
                     tmem_st8(bufc + tt0, ph);
                     tmem_st8(bufc + tt0 + 8, pl);
@@ -369,9 +400,11 @@ __global__ void __launch_bounds__(THREADS, 1) tc_e_bwd_kernel(const __grid_const
     if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
-cudaError_t tc_e_bwd(const Problem& p, const void* q, const void* k, const void* v, const float* cum,
-                     const float* cum_lo, const float* lse, const float* Dvec, const void* dO, float scale, float* dq,
-                     float* dk, float* dv, float* rowsum, float* colsum, cudaStream_t s) {
+template <int KIND>
+static cudaError_t launch_attn_bwd(const Problem& p, const void* q, const void* k, const void* v, const float* cum,
+                                   const float* cum_lo, const float* lse_or_zeta, const float* Dvec, const void* dO,
+                                   float scale, float* dq, float* dk, float* dv, float* rowsum, float* colsum,
+                                   cudaStream_t s) {
     CUtensorMap tq, tk, tv, td;
     const uint64_t BH = (uint64_t)p.BH(), T = (uint64_t)p.T;
     if (!make_tmap_bf16_3d(&tq, q, BH, T, 64, BT) || !make_tmap_bf16_3d(&tk, k, BH, T, 64, BT) ||
@@ -382,20 +415,38 @@ cudaError_t tc_e_bwd(const Problem& p, const void* q, const void* k, const void*
     const int NT = (p.T + BT - 1) / BT;
     dim3 grid((unsigned)NT, (unsigned)p.BH());
     {
-        Args a{cum, cum_lo, lse, Dvec, dk, dv, colsum, status, p.T, NT, (int)p.BH(), scale};
-        cudaError_t e = cudaFuncSetAttribute(tc_e_bwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        Args a{cum, cum_lo, lse_or_zeta, Dvec, dk, dv, colsum, status, p.T, NT, (int)p.BH(), scale};
+        cudaError_t e = cudaFuncSetAttribute(tc_attn_bwd_kernel<KIND, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        tc_e_bwd_kernel<true><<<grid, THREADS, SMEM_BYTES, s>>>(tk, tv, tq, td, a);
+        tc_attn_bwd_kernel<KIND, true><<<grid, THREADS, SMEM_BYTES, s>>>(tk, tv, tq, td, a);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     {
-        Args a{cum, cum_lo, lse, Dvec, dq, nullptr, rowsum, status, p.T, NT, (int)p.BH(), scale};
-        cudaError_t e = cudaFuncSetAttribute(tc_e_bwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        Args a{cum, cum_lo, lse_or_zeta, Dvec, dq, nullptr, rowsum, status, p.T, NT, (int)p.BH(), scale};
+        cudaError_t e = cudaFuncSetAttribute(tc_attn_bwd_kernel<KIND, false>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        tc_e_bwd_kernel<false><<<grid, THREADS, SMEM_BYTES, s>>>(tq, td, tk, tv, a);
+        tc_attn_bwd_kernel<KIND, false><<<grid, THREADS, SMEM_BYTES, s>>>(tq, td, tk, tv, a);
     }
     return cudaGetLastError();
+}
+
+cudaError_t tc_e_bwd(const Problem& p, const void* q, const void* k, const void* v, const float* cum,
+                     const float* cum_lo, const float* lse, const float* Dvec, const void* dO, float scale, float* dq,
+                     float* dk, float* dv, float* rowsum, float* colsum, cudaStream_t s) {
+    return launch_attn_bwd<ATTN_E>(p, q, k, v, cum, cum_lo, lse, Dvec, dO, scale, dq, dk, dv, rowsum, colsum, s);
+}
+
+cudaError_t tc_poly_bwd(const Problem& p, int order, const void* q, const void* k, const void* v, const float* cum,
+                        const float* cum_lo, const float* zeta, const float* D, const void* dO, float* dq, float* dk,
+                        float* dv, float* rowsum, float* colsum, cudaStream_t s) {
+    if (order == 2)
+        return launch_attn_bwd<ATTN_P2>(p, q, k, v, cum, cum_lo, zeta, D, dO, 1.f, dq, dk, dv, rowsum, colsum, s);
+    if (order == 1)
+        return launch_attn_bwd<ATTN_P1>(p, q, k, v, cum, cum_lo, zeta, D, dO, 1.f, dq, dk, dv, rowsum, colsum, s);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace tm2

@@ -25,12 +25,13 @@ def lib():
 def declared_functions():
     src = open(HEADER).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(tm2e?_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(tm2[eq]?_[a-z0-9_]+)\s*\(", src)))
 
 
 def test_header_symbols_exported(lib):
     names = declared_functions()
-    assert {"tm2_forward", "tm2_backward", "tm2_step", "tm2e_forward", "tm2e_backward"} <= set(names)
+    assert {"tm2_forward", "tm2_backward", "tm2_step", "tm2e_forward", "tm2e_backward", "tm2q_forward",
+            "tm2q_backward"} <= set(names)
     for n in names:
         assert hasattr(lib, n), n
 
@@ -117,3 +118,16 @@ def test_binding_fails_loudly_without_cuda_tensors():
     x = torch.zeros(1, 1, 4, 16)
     with pytest.raises(tm2.TM2Error):
         tm2.forward(x, x, x, torch.zeros(1, 1, 4))
+
+
+def test_quadratic_form_rejects_bad_arguments(lib):
+    f = ctypes.c_void_p(FAKE)
+    args = lambda order, d, flags: (f, f, f, f, f, f, 1, 2, 64, d, d, order, 1, flags, f, 1 << 30, None)
+    assert lib.tm2q_forward(*args(3, 64, 1)) == UNSUPPORTED          # order 1 or 2 only
+    assert lib.tm2q_forward(*args(2, 48, 1)) == UNSUPPORTED          # head dim
+    assert lib.tm2q_forward(*args(2, 64, 4)) == INVALID              # unknown flag
+    assert lib.tm2q_forward_workspace(1, 2, 64, 64, 64, 0, 1, 1) == 0
+    assert lib.tm2q_forward_workspace(1, 2, 64, 64, 64, 1, 1, 1) > 0
+    assert lib.tm2q_backward_workspace(1, 2, 64, 64, 64, 2, 1, 1) > lib.tm2q_forward_workspace(1, 2, 64, 64, 64, 2, 1, 1) - 1
+    g = (f, f, f, f, None, None, f, f, f, f, f, 1, 2, 64, 64, 64, 2, 1, 1, f, 1 << 30, None)
+    assert lib.tm2q_backward(*g) == INVALID                          # normalised needs o and Z

@@ -377,3 +377,88 @@ def test_e_variant_no_decay_is_causal_softmax():
     s = 0.5 * np.einsum("bhid,bhjd->bhij", q, k)
     s = np.where(np.tril(np.ones((40, 40), bool)), s, -np.inf)
     assert np.abs(lse - np.log(np.exp(s).sum(-1))).max() < 1e-12
+
+
+# ---------------------------------------------------------------- first-order mixer (order 1)
+# "2Mamba2Furious", Sec. 4 (Mamba-2S: the softplus A-mask on the score q.k itself) and Sec. 2
+# (first-order linear attention keeps a (dh, dh) state).
+
+def brute_force_first_order(q, k, v, a, normalize):
+    """Literal enumeration for one head: product of per-step decays times the score itself."""
+    T, d = q.shape
+    dv = v.shape[1]
+    gam = [1.0 / (1.0 + math.exp(a[t])) for t in range(T)]
+    o = np.zeros((T, dv))
+    Z = np.zeros(T)
+    for i in range(T):
+        for j in range(i + 1):
+            mask = 1.0
+            for t in range(j + 1, i + 1):
+                mask *= gam[t]
+            w = mask * sum(q[i, m] * k[j, m] for m in range(d))
+            Z[i] += w
+            o[i] += w * v[j]
+        if normalize:
+            o[i] /= Z[i]
+    return o, Z
+
+
+@pytest.mark.parametrize("normalize", [True, False])
+def test_first_order_quadratic_equals_recurrent(normalize):
+    """The O(T^2) form with order 1 and the (d x dv) state recurrence are the same function."""
+    q, k, v, a = small_case(T=29, seed=61)
+    o1, Z1 = oracle.fwd_quadratic(q, k, v, a, normalize, order=1)
+    o2, Z2 = oracle.fwd1_recurrent(q, k, v, a, normalize)
+    assert relmax(o1, o2) < 1e-12 and relmax(Z1, Z2) < 1e-12
+
+
+@pytest.mark.parametrize("T", [1, 3, 7])
+def test_first_order_brute_force_small_T(T):
+    q, k, v, a = small_case(B=1, H=1, T=T, d=3, dv=2, seed=70 + T)
+    for normalize in (True, False):
+        ob, Zb = brute_force_first_order(q[0, 0], k[0, 0], v[0, 0], a[0, 0], normalize)
+        o1, Z1 = oracle.fwd_quadratic(q, k, v, a, normalize, order=1)
+        assert relmax(o1[0, 0], ob) < 1e-12 and relmax(Z1[0, 0], Zb) < 1e-12
+
+
+def test_first_order_limits():
+    """No decay, d = 1: o_i = q_i cumsum(k v)_i; full decay: o_i = (q_i . k_i) v_i."""
+    rng = np.random.default_rng(81)
+    T = 40
+    q, k, v = rng.standard_normal((1, 1, T, 1)), rng.standard_normal((1, 1, T, 1)), rng.standard_normal((1, 1, T, 2))
+    o, _ = oracle.fwd_quadratic(q, k, v, np.full((1, 1, T), -40.0), False, order=1)
+    ckv = np.cumsum(k[0, 0, :, 0][:, None] * v[0, 0], axis=0)
+    assert relmax(o[0, 0], q[0, 0, :, 0][:, None] * ckv) < 1e-12
+    q, k, v, a = small_case(B=1, H=2, T=20, d=4, dv=3, seed=82)
+    o, _ = oracle.fwd_quadratic(q, k, v, np.full_like(a, 40.0), False, order=1)
+    assert relmax(o, np.einsum("bhtd,bhtd->bht", q, k)[..., None] * v) < 1e-12
+
+
+@pytest.mark.parametrize("normalize", [True, False])
+def test_first_order_gradients(normalize):
+    """Order-1 gradients against central differences and torch fp64 autograd of a directly
+    written dense expression; da_0 = 0 as for order 2."""
+    q, k, v, a = small_case(B=1, H=1, T=16, d=3, dv=2, seed=83)
+    rng = np.random.default_rng(84)
+    dO = rng.standard_normal(v.shape)
+    fwd = lambda q, k, v, a: oracle.fwd_quadratic(q, k, v, a, normalize, order=1)[0]
+    bwd = lambda q, k, v, a, dO: oracle.bwd_quadratic(q, k, v, a, dO, normalize, order=1)
+    idx = []
+    for which, shp in enumerate((q.shape, k.shape, v.shape, a.shape)):
+        for _ in range(8):
+            idx.append((which, tuple(int(rng.integers(0, s)) for s in shp)))
+    _fd_check(fwd, bwd, [q, k, v, a], dO, idx)
+    tq, tk, tv, ta = (torch.tensor(x, requires_grad=True) for x in (q, k, v, a))
+    cum = torch.cumsum(-torch.nn.functional.softplus(ta), -1)
+    T = q.shape[2]
+    causal = torch.tril(torch.ones(T, T, dtype=torch.bool))
+    diff = torch.where(causal, cum[..., :, None] - cum[..., None, :], torch.tensor(-math.inf, dtype=torch.float64))
+    W = torch.exp(diff) * (tq @ tk.transpose(-1, -2))
+    o = W @ tv
+    if normalize:
+        o = o / W.sum(-1, keepdim=True)
+    (o * torch.tensor(dO)).sum().backward()
+    grads = bwd(q, k, v, a, dO)
+    for g, ref in zip(grads, (tq.grad, tk.grad, tv.grad, ta.grad)):
+        assert relmax(g, ref.numpy()) < 1e-10
+    assert np.abs(grads[3][..., 0]).max() < 1e-10 * np.abs(grads[3]).max()
