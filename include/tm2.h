@@ -72,6 +72,14 @@ typedef enum { TM2_F32 = 0, TM2_BF16 = 1 } tm2_dtype;
  * left there instead of recomputing them.  (Allocate max(tm2_forward_workspace,
  * tm2_backward_workspace) bytes and pass the same buffer to both calls.) */
 #define TM2_REUSE_STATES 2u
+/* tm2_step / tm2_step_conv: S and z are kept symmetric-packed, (N,H,d(d+1)/2,dv) and
+ * (N,H,d(d+1)/2): only the rows (m, n) with m <= n, row index m*d - m(m-1)/2 + (n - m).
+ * k (x) k and q (x) q are symmetric, so the readout (q (x) q)^T S sees only the symmetric part
+ * of S and every update adds a symmetric term: with the off-diagonal rows weighted twice the
+ * outputs are exactly those of the full state, for any initial state (tm2_state_pack keeps its
+ * symmetric part), and a step moves about half the bytes ("2Mamba2Furious", Sec. 5.1: memory
+ * of the squared state; Sec. 7: hidden-state size). */
+#define TM2_PACKED_STATE 4u
 
 /* Library version (major*10000 + minor*100 + patch). */
 int tm2_version(void);
@@ -164,6 +172,48 @@ int tm2q_backward(const void* q, const void* k, const void* v, const float* a, c
                   int B, int H, int T, int d, int dv_dim, int order, int dtype, unsigned flags,
                   void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * tm2_step with the size-2 input convolution of Mamba-2S applied to q, k and v first
+ * ("2Mamba2Furious", Sec. 3-4: window 2, no activation; App. A: inference caches the previous
+ * window - 1 = 1 raw query, key and value).  Per tensor x in (q, k, v), channel c of head h:
+ *   x'_t[c] = w[h][c][0] x_t[c] + w[h][c][1] x_{t-1}[c] (+ b[h][c]),
+ * with x_{t-1} read from the cache (N,H,d) in dtype (zero before the first token) and x_t
+ * written back to it.  wq, wk, wv: (H,d,2) fp32; bq, bk, bv: (H,d) fp32 or NULL; cq, ck, cv:
+ * the caches, updated in place.  The convolved q', k', v' are fp32 (never rounded to dtype).
+ * Everything else as tm2_step (flags TM2_NORMALIZE, TM2_PACKED_STATE).
+ */
+int tm2_step_conv(const void* q, const void* k, const void* v, const float* a,
+                  const float* wq, const float* wk, const float* wv,
+                  const float* bq, const float* bk, const float* bv,
+                  void* cq, void* ck, void* cv,
+                  float* S, float* z, void* o, float* Z,
+                  int N, int H, int d, int dv, int dtype, unsigned flags, void* stream);
+
+/*
+ * Symmetric packing of NH full states S (NH,d*d,dv) / z (NH,d*d) into (NH,d(d+1)/2,dv) /
+ * (NH,d(d+1)/2) (the layout of TM2_PACKED_STATE): packed row (m, n), m <= n, holds
+ * (S[(m,n)] + S[(n,m)]) / 2.  tm2_state_unpack writes that symmetric full state back.
+ * z / z_packed may both be NULL.  d = dv in {16, 32, 64}.
+ */
+int tm2_state_pack(const float* S, const float* z, float* S_packed, float* z_packed, int NH, int d, int dv,
+                   void* stream);
+int tm2_state_unpack(const float* S_packed, const float* z_packed, float* S, float* z, int NH, int d, int dv,
+                     void* stream);
+
+/*
+ * Size-2 causal input convolution over a sequence (the training-side counterpart of
+ * tm2_step_conv): x (B,H,T,C) in dtype, w (H,C,2) fp32, b (H,C) fp32 or NULL, x_prev (B,H,C)
+ * in dtype or NULL (the token before t = 0; zero if NULL), y (B,H,T,C) in dtype:
+ *   y_t = w[..,0] x_t + w[..,1] x_{t-1} (+ b).
+ * Backward: dx (B,H,T,C), dx_prev (B,H,C, or NULL), dw (H,C,2), db (H,C, or NULL), all fp32,
+ * from dy (B,H,T,C) in dtype.  C in {16, 32, 64}.
+ */
+int tm2_conv2_forward(const void* x, const float* w, const float* b, const void* x_prev, void* y,
+                      int B, int H, int T, int C, int dtype, void* stream);
+int tm2_conv2_backward(const void* x, const float* w, const void* x_prev, const void* dy, float* dx,
+                       float* dx_prev, float* dw, float* db, int B, int H, int T, int C, int dtype,
+                       void* stream);
+
 size_t tm2e_forward_workspace(int B, int H, int T, int d, int dv, int dtype);
 
 /*
@@ -213,6 +263,33 @@ int tm2e_backward(const void* q, const void* k, const void* v, const float* a,
                   void* dq, void* dk, void* dv, float* da,
                   int B, int H, int T, int d, int dv_dim, float scale, int dtype,
                   void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * 2Mamba-E decoding over a key/value cache (Sec. 6; Sec. 1: unlike 2Mamba it needs a KV cache;
+ * Sec. 2: that cache is its recurrent state, 2 N dh elements per head).  One token per
+ * (sequence, head) at position `pos` (the same for the whole batch, 0 <= pos < L):
+ *   cumA_pos = cumA_{pos-1} - softplus(a),   o = sum_{j <= pos} softmax_j(scale q . k_j + cumA_pos - cumA_j) v_j,
+ * and k, v, cumA_pos appended to the caches.  q, k: (N,H,d); v: (N,H,dv) in dtype; a: (N,H).
+ * K_cache (N,H,L,d), V_cache (N,H,L,dv) in dtype; cum_cache (N,H,L,2) fp32, the running sums
+ * of -softplus(a) as hi + lo (rows < pos written by earlier steps or tm2e_fill_cache).
+ * o (N,H,dv) fp32; lse (N,H) fp32 or NULL.  Workspace: tm2e_step_workspace (used from
+ * pos >= 512, where the keys are split over several blocks).  The step reads the cache once:
+ * it is bound by HBM bandwidth.
+ */
+size_t tm2e_step_workspace(int N, int H, int L, int d, int dv, int dtype);
+int tm2e_step(const void* q, const void* k, const void* v, const float* a,
+              void* K_cache, void* V_cache, float* cum_cache, int pos, int L,
+              void* o, float* lse, int N, int H, int d, int dv, float scale, int dtype,
+              void* ws, size_t ws_bytes, void* stream);
+/*
+ * Fills the caches with a prefill of T <= L tokens (k (B,H,T,d), v (B,H,T,dv), a (B,H,T)):
+ * rows 0..T-1 of K_cache, V_cache and the running sums in cum_cache, so that decoding goes on
+ * at pos = T.  Workspace: tm2e_fill_cache_workspace.
+ */
+size_t tm2e_fill_cache_workspace(int B, int H, int T, int d, int dv, int dtype);
+int tm2e_fill_cache(const void* k, const void* v, const float* a, void* K_cache, void* V_cache,
+                    float* cum_cache, int B, int H, int T, int L, int d, int dv, int dtype,
+                    void* ws, size_t ws_bytes, void* stream);
 
 /*
  * Device status word of the current device: returns TM2_OK, or TM2_ERR_TIMEOUT if a

@@ -55,6 +55,8 @@ def _load():
         _lib.orc_e_fwd.argtypes = [i] * 5 + [p] * 4 + [d, p, p]
         _lib.orc_e_bwd.argtypes = [i] * 5 + [p] * 5 + [d, p, p, p, p]
         _lib.orc_running_log_decay.argtypes = [p, ctypes.c_long, ctypes.c_long, p]
+        _lib.orc_conv2_fwd.argtypes = [i] * 4 + [p] * 5
+        _lib.orc_conv2_bwd.argtypes = [i] * 4 + [p] * 8
         _lib.orc_num_threads.restype = i
     return _lib
 
@@ -195,3 +197,25 @@ def e_bwd(q, k, v, a, dO, scale=None):
     _load().orc_e_bwd(B, H, T, d, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(dO),
                       float(scale), _ptr(dq), _ptr(dk), _ptr(dvv), _ptr(da))
     return dq, dk, dvv, da
+
+
+def conv2_fwd(x, w, b=None, x_prev=None):
+    """Size-2 causal depthwise convolution: x (B,H,T,C), w (H,C,2), b (H,C), x_prev (B,H,C)."""
+    x, w, b, x_prev = map(_f64, (x, w, b, x_prev))
+    B, H, T, C = x.shape
+    y = np.zeros_like(x)
+    _load().orc_conv2_fwd(B, H, T, C, _ptr(x), _ptr(w), _ptr(b), _ptr(x_prev), _ptr(y))
+    return y
+
+
+def conv2_bwd(x, w, dy, x_prev=None):
+    """Gradients of conv2_fwd: returns (dx, dx_prev, dw, db)."""
+    x, w, dy, x_prev = map(_f64, (x, w, dy, x_prev))
+    B, H, T, C = x.shape
+    dx = np.zeros_like(x)
+    dxp = np.zeros((B, H, C))
+    dw = np.zeros((H, C, 2))
+    db = np.zeros((H, C))
+    _load().orc_conv2_bwd(B, H, T, C, _ptr(x), _ptr(w), _ptr(x_prev), _ptr(dy), _ptr(dx), _ptr(dxp), _ptr(dw),
+                          _ptr(db))
+    return dx, dxp, dw, db

@@ -461,3 +461,48 @@ int orc_num_threads(void) {
     return 1;
 #endif
 }
+
+/*
+ * Size-2 causal input convolution of Mamba-2S, kept by 2Mamba (Sec. 3: kernel size 2;
+ * Sec. 4: no activation; App. A: inference caches the previous raw token).  Per channel c of
+ * head h, a depthwise convolution over time:
+ *   y_t[c] = w[h][c][0] x_t[c] + w[h][c][1] x_{t-1}[c] + b[h][c],   x_{-1} = x_prev (or 0).
+ * x, y: (B,H,T,C); w: (H,C,2); b: (H,C) or NULL; x_prev: (B,H,C) or NULL.
+ */
+void orc_conv2_fwd(int B, int H, int T, int C, const double* x, const double* w, const double* b,
+                   const double* x_prev, double* y) {
+    for (long bb = 0; bb < B; ++bb)
+        for (long h = 0; h < H; ++h)
+            for (long t = 0; t < T; ++t)
+                for (int c = 0; c < C; ++c) {
+                    long bh = bb * H + h;
+                    double prev = t > 0 ? x[(bh * T + t - 1) * C + c] : (x_prev ? x_prev[bh * C + c] : 0.0);
+                    double out = w[(h * C + c) * 2] * x[(bh * T + t) * C + c] + w[(h * C + c) * 2 + 1] * prev;
+                    if (b) out += b[h * C + c];
+                    y[(bh * T + t) * C + c] = out;
+                }
+}
+
+/* Its gradients, by the chain rule on the definition above: dx_t gets w0 dy_t from y_t and
+ * w1 dy_{t+1} from y_{t+1}; dx_prev = w1 dy_0; dw0, dw1, db sum dy_t x_t, dy_t x_{t-1}, dy_t
+ * over every batch row and time step of the head.  dx_prev, db may be NULL. */
+void orc_conv2_bwd(int B, int H, int T, int C, const double* x, const double* w, const double* x_prev,
+                   const double* dy, double* dx, double* dx_prev, double* dw, double* db) {
+    for (long i = 0; i < (long)H * C * 2; ++i) dw[i] = 0.0;
+    if (db)
+        for (long i = 0; i < (long)H * C; ++i) db[i] = 0.0;
+    for (long bb = 0; bb < B; ++bb)
+        for (long h = 0; h < H; ++h)
+            for (long t = 0; t < T; ++t)
+                for (int c = 0; c < C; ++c) {
+                    long bh = bb * H + h;
+                    double g = dy[(bh * T + t) * C + c];
+                    double next = t + 1 < T ? dy[(bh * T + t + 1) * C + c] : 0.0;
+                    dx[(bh * T + t) * C + c] = w[(h * C + c) * 2] * g + w[(h * C + c) * 2 + 1] * next;
+                    double prev = t > 0 ? x[(bh * T + t - 1) * C + c] : (x_prev ? x_prev[bh * C + c] : 0.0);
+                    dw[(h * C + c) * 2] += g * x[(bh * T + t) * C + c];
+                    dw[(h * C + c) * 2 + 1] += g * prev;
+                    if (db) db[h * C + c] += g;
+                    if (t == 0 && dx_prev) dx_prev[bh * C + c] = w[(h * C + c) * 2 + 1] * g;
+                }
+}

@@ -19,7 +19,8 @@ import os
 
 import torch
 
-__all__ = ["forward", "backward", "step", "e_forward", "e_backward", "forward_quadratic",
+__all__ = ["forward", "backward", "step", "step_conv", "state_pack", "state_unpack", "e_forward", "e_backward",
+           "e_step", "e_fill_cache", "conv2_forward", "conv2_backward", "forward_quadratic",
            "backward_quadratic", "library_path",
            "forward_workspace_bytes", "backward_workspace_bytes", "workspace_bytes", "TM2Error",
            "NORMALIZE", "REUSE_STATES"]
@@ -28,6 +29,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(PKG, "libtm2.so")
 NORMALIZE = 1
 REUSE_STATES = 2
+PACKED_STATE = 4
 _DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 _lib = None
 
@@ -75,6 +77,23 @@ def _load():
     lib.tm2q_forward.argtypes = [P] * 6 + [I] * 7 + [U, P, S, P]
     lib.tm2q_backward.restype = I
     lib.tm2q_backward.argtypes = [P] * 11 + [I] * 7 + [U, P, S, P]
+    lib.tm2_step_conv.restype = I
+    lib.tm2_step_conv.argtypes = [P] * 17 + [I] * 5 + [U, P]
+    for name in ("tm2_state_pack", "tm2_state_unpack"):
+        getattr(lib, name).restype = I
+        getattr(lib, name).argtypes = [P] * 4 + [I] * 3 + [P]
+    lib.tm2e_step_workspace.restype = S
+    lib.tm2e_step_workspace.argtypes = [I] * 6
+    lib.tm2e_step.restype = I
+    lib.tm2e_step.argtypes = [P] * 7 + [I] * 2 + [P] * 2 + [I] * 4 + [F, I, P, S, P]
+    lib.tm2e_fill_cache_workspace.restype = S
+    lib.tm2e_fill_cache_workspace.argtypes = [I] * 6
+    lib.tm2e_fill_cache.restype = I
+    lib.tm2e_fill_cache.argtypes = [P] * 6 + [I] * 7 + [P, S, P]
+    lib.tm2_conv2_forward.restype = I
+    lib.tm2_conv2_forward.argtypes = [P] * 5 + [I] * 5 + [P]
+    lib.tm2_conv2_backward.restype = I
+    lib.tm2_conv2_backward.argtypes = [P] * 8 + [I] * 5 + [P]
     lib.tm2_poll_status.restype = I
     lib.tm2_last_cuda_error.restype = ctypes.c_char_p
     _lib = lib
@@ -190,21 +209,122 @@ def backward(q, k, v, a, o, Z, dO, *, normalize=True, chunk=0, workspace=None, s
     return dq, dk, dvv, da
 
 
-def step(q, k, v, a, S, z, *, normalize=True, out=None, Z=None, stream=None):
-    """One decode step, updating S (N,H,d*d,dv) and z (N,H,d*d) in place.  Returns (o, zeta)."""
+def _step_checks(q, k, v, a, S, z, packed):
     N, H, d = q.shape
     dv = v.shape[-1]
-    L = _load()
     for name, t in (("q", q), ("k", k), ("v", v), ("a", a), ("S", S)) + ((("z", z),) if z is not None else ()):
         if not t.is_cuda or not t.is_contiguous():
             raise TM2Error("%s must be a contiguous CUDA tensor" % name)
     if q.dtype not in _DTYPES or S.dtype != torch.float32 or a.dtype != torch.float32:
         raise TM2Error("q, k, v in {float32, bfloat16}; a, S, z float32")
+    rows = d * (d + 1) // 2 if packed else d * d
+    if S.shape != (N, H, rows, dv) or (z is not None and z.shape != (N, H, rows)):
+        raise TM2Error("S must be (N,H,%d,dv) and z (N,H,%d)" % (rows, rows))
+    return N, H, d, dv
+
+
+def step(q, k, v, a, S, z, *, normalize=True, packed=False, out=None, Z=None, stream=None):
+    """One decode step, updating S (N,H,d*d,dv) and z (N,H,d*d) in place -- or, with packed=True,
+    the symmetric-packed S (N,H,d(d+1)/2,dv) and z (N,H,d(d+1)/2).  Returns (o, zeta)."""
+    N, H, d, dv = _step_checks(q, k, v, a, S, z, packed)
+    L = _load()
     o = torch.empty(v.shape, dtype=torch.float32, device=q.device) if out is None else out
     Z = torch.empty((N, H), dtype=torch.float32, device=q.device) if Z is None else Z
+    flags = (NORMALIZE if normalize else 0) | (PACKED_STATE if packed else 0)
     _check(L.tm2_step(_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(S), _ptr(z), _ptr(o), _ptr(Z), N, H, d,
-                      dv, _DTYPES[q.dtype], NORMALIZE if normalize else 0, _stream(stream)))
+                      dv, _DTYPES[q.dtype], flags, _stream(stream)))
     return o, Z
+
+
+def step_conv(q, k, v, a, conv_w, conv_b, caches, S, z, *, normalize=True, packed=False, out=None, Z=None,
+              stream=None):
+    """Decode step with the size-2 input convolution on q, k, v: conv_w = (wq, wk, wv), each (H,d,2)
+    fp32; conv_b = (bq, bk, bv) of (H,d) fp32 or None; caches = (cq, ck, cv), each (N,H,d) in the
+    input dtype, updated in place (the raw current token replaces the previous one)."""
+    N, H, d, dv = _step_checks(q, k, v, a, S, z, packed)
+    L = _load()
+    o = torch.empty(v.shape, dtype=torch.float32, device=q.device) if out is None else out
+    Z = torch.empty((N, H), dtype=torch.float32, device=q.device) if Z is None else Z
+    bq, bk, bv = conv_b if conv_b is not None else (None, None, None)
+    flags = (NORMALIZE if normalize else 0) | (PACKED_STATE if packed else 0)
+    _check(L.tm2_step_conv(_ptr(q), _ptr(k), _ptr(v), _ptr(a), *(_ptr(t) for t in conv_w), _ptr(bq), _ptr(bk),
+                           _ptr(bv), *(_ptr(t) for t in caches), _ptr(S), _ptr(z), _ptr(o), _ptr(Z), N, H, d, dv,
+                           _DTYPES[q.dtype], flags, _stream(stream)))
+    return o, Z
+
+
+def state_pack(S, z=None, *, stream=None):
+    """Full states (NH..., d*d, dv) -> symmetric-packed (..., d(d+1)/2, dv) (their symmetric part)."""
+    d = int(round(S.shape[-2] ** 0.5))
+    lead = S.shape[:-2]
+    R = d * (d + 1) // 2
+    Sp = torch.empty(lead + (R, S.shape[-1]), dtype=torch.float32, device=S.device)
+    zp = None if z is None else torch.empty(lead + (R,), dtype=torch.float32, device=S.device)
+    nh = S.numel() // (d * d * S.shape[-1])
+    _check(_load().tm2_state_pack(_ptr(S), _ptr(z), _ptr(Sp), _ptr(zp), nh, d, S.shape[-1], _stream(stream)))
+    return Sp, zp
+
+
+def state_unpack(Sp, zp=None, *, d, stream=None):
+    """Symmetric-packed states back to the full (d*d)-row layout."""
+    lead = Sp.shape[:-2]
+    S = torch.empty(lead + (d * d, Sp.shape[-1]), dtype=torch.float32, device=Sp.device)
+    z = None if zp is None else torch.empty(lead + (d * d,), dtype=torch.float32, device=Sp.device)
+    nh = Sp.numel() // (Sp.shape[-2] * Sp.shape[-1])
+    _check(_load().tm2_state_unpack(_ptr(Sp), _ptr(zp), _ptr(S), _ptr(z), nh, d, Sp.shape[-1], _stream(stream)))
+    return S, z
+
+
+def e_step(q, k, v, a, K_cache, V_cache, cum_cache, pos, *, scale=None, out=None, lse=None, workspace=None,
+           stream=None):
+    """2Mamba-E decode step over the KV cache at position pos (caches (N,H,L,d), (N,H,L,dv),
+    (N,H,L,2)); appends the token.  Returns (o, lse)."""
+    N, H, d = q.shape
+    dv = v.shape[-1]
+    Lc = K_cache.shape[2]
+    L = _load()
+    dt = _DTYPES[q.dtype]
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty((N, H, dv), dtype=torch.float32, device=q.device) if out is None else out
+    lse = torch.empty((N, H), dtype=torch.float32, device=q.device) if lse is None else lse
+    ws = _workspace(L.tm2e_step_workspace(N, H, Lc, d, dv, dt), q.device, workspace)
+    nbytes = 0 if ws is None else ws.numel()
+    _check(L.tm2e_step(_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(K_cache), _ptr(V_cache), _ptr(cum_cache), int(pos),
+                       Lc, _ptr(o), _ptr(lse), N, H, d, dv, scale, dt, _ptr(ws), nbytes, _stream(stream)))
+    return o, lse
+
+
+def e_fill_cache(k, v, a, K_cache, V_cache, cum_cache, *, workspace=None, stream=None):
+    """Writes a prefill's keys, values and A-mask running sums into rows 0..T-1 of the caches."""
+    B, H, T, d = k.shape
+    dv = v.shape[-1]
+    L = _load()
+    dt = _DTYPES[k.dtype]
+    ws = _workspace(L.tm2e_fill_cache_workspace(B, H, T, d, dv, dt), k.device, workspace)
+    nbytes = 0 if ws is None else ws.numel()
+    _check(L.tm2e_fill_cache(_ptr(k), _ptr(v), _ptr(a), _ptr(K_cache), _ptr(V_cache), _ptr(cum_cache), B, H, T,
+                             K_cache.shape[2], d, dv, dt, _ptr(ws), nbytes, _stream(stream)))
+
+
+def conv2_forward(x, w, b=None, x_prev=None, *, stream=None):
+    """Size-2 causal input convolution of x (B,H,T,C); w (H,C,2), b (H,C) fp32; x_prev (B,H,C)."""
+    B, H, T, C = x.shape
+    y = torch.empty_like(x)
+    _check(_load().tm2_conv2_forward(_ptr(x), _ptr(w), _ptr(b), _ptr(x_prev), _ptr(y), B, H, T, C,
+                                     _DTYPES[x.dtype], _stream(stream)))
+    return y
+
+
+def conv2_backward(x, w, dy, x_prev=None, *, stream=None):
+    """Gradients of conv2_forward: (dx, dx_prev, dw, db), fp32."""
+    B, H, T, C = x.shape
+    dx = torch.empty(x.shape, dtype=torch.float32, device=x.device)
+    dxp = torch.empty((B, H, C), dtype=torch.float32, device=x.device)
+    dw = torch.empty((H, C, 2), dtype=torch.float32, device=x.device)
+    db = torch.empty((H, C), dtype=torch.float32, device=x.device)
+    _check(_load().tm2_conv2_backward(_ptr(x), _ptr(w), _ptr(x_prev), _ptr(dy), _ptr(dx), _ptr(dxp), _ptr(dw),
+                                      _ptr(db), B, H, T, C, _DTYPES[x.dtype], _stream(stream)))
+    return dx, dxp, dw, db
 
 
 def forward_quadratic(q, k, v, a, *, order=2, normalize=True, workspace=None, stream=None, out=None, Z=None):

@@ -387,23 +387,178 @@ int tm2_backward(const void* q, const void* k, const void* v, const float* a, co
     return TM2_OK;
 }
 
-int tm2_step(const void* q, const void* k, const void* v, const float* a, float* S, float* z,
-             void* o, float* Z, int N, int H, int d, int dv, int dtype, unsigned flags,
-             void* stream) {
+static int step_checks(const void* q, const void* k, const void* v, const float* a, const float* S, const float* z,
+                       const void* o, const float* Z, int N, int H, int d, int dv, int dtype, unsigned flags) {
     if (N < 0 || H < 0 || d <= 0 || dv <= 0) return TM2_ERR_INVALID_ARG;
     if (dtype != TM2_F32 && dtype != TM2_BF16) return TM2_ERR_UNSUPPORTED;
     if (d != dv || (d != 16 && d != 32 && d != 64)) return TM2_ERR_UNSUPPORTED;
-    if (flags & ~TM2_NORMALIZE) return TM2_ERR_INVALID_ARG;
-    const bool normalize = (flags & TM2_NORMALIZE) != 0;
+    if (flags & ~(TM2_NORMALIZE | TM2_PACKED_STATE)) return TM2_ERR_INVALID_ARG;
     if ((long)N * H == 0) return TM2_OK;
     if ((long)N * H > 0x7fffffffL) return TM2_ERR_UNSUPPORTED;
     if (!q || !k || !v || !a || !S || !o) return TM2_ERR_INVALID_ARG;
-    if (normalize && !z) return TM2_ERR_INVALID_ARG;
+    if ((flags & TM2_NORMALIZE) && !z) return TM2_ERR_INVALID_ARG;
     const void* ptrs[] = {q, k, v, a, S, z, o, Z};
     for (const void* x : ptrs)
         if (!aligned16(x)) return TM2_ERR_ALIGNMENT;
+    return TM2_OK;
+}
+
+int tm2_step(const void* q, const void* k, const void* v, const float* a, float* S, float* z,
+             void* o, float* Z, int N, int H, int d, int dv, int dtype, unsigned flags,
+             void* stream) {
+    const int st = step_checks(q, k, v, a, S, z, o, Z, N, H, d, dv, dtype, flags);
+    if (st != TM2_OK || (long)N * H == 0) return st;
     cudaStream_t s = (cudaStream_t)stream;
-    TM2_RUN("decode_step", launch_decode_step(N, H, d, dv, dtype, normalize, q, k, v, a, S, z, o, Z, s));
+    TM2_RUN(flags & TM2_PACKED_STATE ? "decode_step_packed" : "decode_step",
+            launch_decode_step(N, H, d, dv, dtype, (flags & TM2_NORMALIZE) != 0, (flags & TM2_PACKED_STATE) != 0,
+                               nullptr, q, k, v, a, S, z, o, Z, s));
+    return TM2_OK;
+}
+
+int tm2_step_conv(const void* q, const void* k, const void* v, const float* a, const float* wq, const float* wk,
+                  const float* wv, const float* bq, const float* bk, const float* bv, void* cq, void* ck, void* cv,
+                  float* S, float* z, void* o, float* Z, int N, int H, int d, int dv, int dtype, unsigned flags,
+                  void* stream) {
+    int st = step_checks(q, k, v, a, S, z, o, Z, N, H, d, dv, dtype, flags);
+    if (st != TM2_OK || (long)N * H == 0) return st;
+    if (!wq || !wk || !wv || !cq || !ck || !cv) return TM2_ERR_INVALID_ARG;
+    const void* ptrs[] = {wq, wk, wv, bq, bk, bv, cq, ck, cv};
+    for (const void* x : ptrs)
+        if (!aligned16(x)) return TM2_ERR_ALIGNMENT;
+    DecodeConv c{{wq, wk, wv}, {bq, bk, bv}, {cq, ck, cv}};
+    cudaStream_t s = (cudaStream_t)stream;
+    TM2_RUN(flags & TM2_PACKED_STATE ? "decode_step_conv_packed" : "decode_step_conv",
+            launch_decode_step(N, H, d, dv, dtype, (flags & TM2_NORMALIZE) != 0, (flags & TM2_PACKED_STATE) != 0,
+                               &c, q, k, v, a, S, z, o, Z, s));
+    return TM2_OK;
+}
+
+static int pack_args(const float* full, const float* packed, int NH, int d, int dv) {
+    if (NH < 0 || (d != 16 && d != 32 && d != 64) || dv != d) return NH < 0 ? TM2_ERR_INVALID_ARG : TM2_ERR_UNSUPPORTED;
+    if (NH > 0 && (!full || !packed)) return TM2_ERR_INVALID_ARG;
+    if (!aligned16(full) || !aligned16(packed)) return TM2_ERR_ALIGNMENT;
+    return TM2_OK;
+}
+
+int tm2_state_pack(const float* S, const float* z, float* S_packed, float* z_packed, int NH, int d, int dv,
+                   void* stream) {
+    int st = pack_args(S, S_packed, NH, d, dv);
+    if (st != TM2_OK) return st;
+    if ((z == nullptr) != (z_packed == nullptr) || !aligned16(z) || !aligned16(z_packed)) return TM2_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    TM2_RUN("state_pack", launch_state_pack(S, S_packed, NH, d, dv, false, s));
+    if (z) TM2_RUN("state_pack", launch_state_pack(z, z_packed, NH, d, 1, false, s));
+    return TM2_OK;
+}
+
+int tm2_state_unpack(const float* S_packed, const float* z_packed, float* S, float* z, int NH, int d, int dv,
+                     void* stream) {
+    int st = pack_args(S, S_packed, NH, d, dv);
+    if (st != TM2_OK) return st;
+    if ((z == nullptr) != (z_packed == nullptr) || !aligned16(z) || !aligned16(z_packed)) return TM2_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    TM2_RUN("state_unpack", launch_state_pack(S, const_cast<float*>(S_packed), NH, d, dv, true, s));
+    if (z) TM2_RUN("state_unpack", launch_state_pack(z, const_cast<float*>(z_packed), NH, d, 1, true, s));
+    return TM2_OK;
+}
+
+size_t tm2e_step_workspace(int N, int H, int L, int d, int dv, int dtype) {
+    if (N < 0 || H < 0 || L <= 0 || d != dv || (d != 16 && d != 32 && d != 64)) return 0;
+    if (dtype != TM2_F32 && dtype != TM2_BF16) return 0;
+    const size_t n = (size_t)N * H * e_decode_max_splits(L) * (dv + 2) * sizeof(float);
+    return (n + 255) & ~(size_t)255;
+}
+
+int tm2e_step(const void* q, const void* k, const void* v, const float* a, void* K_cache, void* V_cache,
+              float* cum_cache, int pos, int L, void* o, float* lse, int N, int H, int d, int dv, float scale,
+              int dtype, void* ws, size_t ws_bytes, void* stream) {
+    if (N < 0 || H < 0 || L <= 0) return TM2_ERR_INVALID_ARG;
+    if (dtype != TM2_F32 && dtype != TM2_BF16) return TM2_ERR_UNSUPPORTED;
+    if (d != dv || (d != 16 && d != 32 && d != 64)) return TM2_ERR_UNSUPPORTED;
+    if (pos < 0 || pos >= L) return TM2_ERR_INVALID_ARG;
+    if (!(scale == scale) || scale == 0.f) return TM2_ERR_INVALID_ARG;
+    const long NH = (long)N * H;
+    if (NH == 0) return TM2_OK;
+    if (NH > 65535L * 1024) return TM2_ERR_UNSUPPORTED;
+    if (!q || !k || !v || !a || !K_cache || !V_cache || !cum_cache || !o) return TM2_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, a, K_cache, V_cache, cum_cache, o, lse};
+    for (const void* x : ptrs)
+        if (!aligned16(x)) return TM2_ERR_ALIGNMENT;
+    const int ns = e_decode_splits(pos);
+    float* part = nullptr;
+    if (ns > 1) {
+        const int st = check_ws(ws, ws_bytes, tm2e_step_workspace(N, H, L, d, dv, dtype));
+        if (st != TM2_OK) return st;
+        part = (float*)ws;
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    TM2_RUN("e_decode", launch_e_decode(NH, d, dtype, pos, L, scale, q, k, v, a, K_cache, V_cache, cum_cache, part,
+                                        (float*)o, lse, s));
+    return TM2_OK;
+}
+
+size_t tm2e_fill_cache_workspace(int B, int H, int T, int d, int dv, int dtype) {
+    return tm2e_forward_workspace(B, H, T, d, dv, dtype);
+}
+
+int tm2e_fill_cache(const void* k, const void* v, const float* a, void* K_cache, void* V_cache, float* cum_cache,
+                    int B, int H, int T, int L, int d, int dv, int dtype, void* ws, size_t ws_bytes, void* stream) {
+    Problem p{};
+    int st = make_problem(B, H, T, d, dv, 0, dtype, 0, p);
+    if (st != TM2_OK) return st;
+    if (T > L) return TM2_ERR_INVALID_ARG;
+    if (p.BH() == 0 || T == 0) return TM2_OK;
+    if (!k || !v || !a || !K_cache || !V_cache || !cum_cache) return TM2_ERR_INVALID_ARG;
+    const void* ptrs[] = {k, v, a, K_cache, V_cache, cum_cache};
+    for (const void* x : ptrs)
+        if (!aligned16(x)) return TM2_ERR_ALIGNMENT;
+    const EWs w = plan_e(p, false);
+    st = check_ws(ws, ws_bytes, w.total);
+    if (st != TM2_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    float* Aloc = at<float>(ws, w.Aloc);
+    float* g = at<float>(ws, w.g);
+    float* cum = at<float>(ws, w.cum);
+    float* cum_lo = at<float>(ws, w.cum_lo);
+    TM2_RUN("decay_chunk", launch_decay(p, a, Aloc, g, s));
+    TM2_RUN("global_cumsum", launch_global_cumsum(p, Aloc, g, cum, cum_lo, s));
+    TM2_RUN("e_cache_fill", launch_e_cache_fill(p.BH(), T, L, d, dv, dtype, k, v, cum, cum_lo, K_cache, V_cache,
+                                                cum_cache, s));
+    return TM2_OK;
+}
+
+static int conv_args(int B, int H, int T, int C, int dtype) {
+    if (B < 0 || H < 0 || T < 0) return TM2_ERR_INVALID_ARG;
+    if (dtype != TM2_F32 && dtype != TM2_BF16) return TM2_ERR_UNSUPPORTED;
+    if (C != 16 && C != 32 && C != 64) return TM2_ERR_UNSUPPORTED;
+    return TM2_OK;
+}
+
+int tm2_conv2_forward(const void* x, const float* w, const float* b, const void* x_prev, void* y, int B, int H,
+                      int T, int C, int dtype, void* stream) {
+    int st = conv_args(B, H, T, C, dtype);
+    if (st != TM2_OK) return st;
+    if ((long)B * H * T == 0) return TM2_OK;
+    if (!x || !w || !y) return TM2_ERR_INVALID_ARG;
+    const void* ptrs[] = {x, w, b, x_prev, y};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return TM2_ERR_ALIGNMENT;
+    cudaStream_t s = (cudaStream_t)stream;
+    TM2_RUN("conv2_fwd", launch_conv2_fwd((long)B * H, H, T, C, dtype, x, w, b, x_prev, y, s));
+    return TM2_OK;
+}
+
+int tm2_conv2_backward(const void* x, const float* w, const void* x_prev, const void* dy, float* dx, float* dx_prev,
+                       float* dw, float* db, int B, int H, int T, int C, int dtype, void* stream) {
+    int st = conv_args(B, H, T, C, dtype);
+    if (st != TM2_OK) return st;
+    if ((long)B * H * T == 0) return TM2_OK;
+    if (!x || !w || !dy || !dx || !dw) return TM2_ERR_INVALID_ARG;
+    const void* ptrs[] = {x, w, x_prev, dy, dx, dx_prev, dw, db};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return TM2_ERR_ALIGNMENT;
+    cudaStream_t s = (cudaStream_t)stream;
+    TM2_RUN("conv2_bwd", launch_conv2_bwd(B, H, T, C, dtype, x, w, x_prev, dy, dx, dx_prev, dw, db, s));
     return TM2_OK;
 }
 

@@ -1,0 +1,186 @@
+// tm2_conv.cu -- the size-2 causal input convolution of Mamba-2S, kept by 2Mamba
+// ("2Mamba2Furious", Sec. 3: a convolution of kernel size 2 is, after the A-mask, the
+// component that helps linear attention most; Sec. 4: window 2, no activation; App. A: at
+// inference the previous window - 1 = 1 raw token is cached).  Per channel c of head h of
+// q, k or v (a depthwise convolution over time):
+//   y_t[c] = w[h][c][0] x_t[c] + w[h][c][1] x_{t-1}[c] (+ b[h][c]),   x_{-1} = x_prev or 0,
+// and its backward
+//   dx_t = w0 dy_t + w1 dy_{t+1} (dy_T = 0),   dx_prev = w1 dy_0,
+//   dw0 = sum_{b,t} dy_t x_t,   dw1 = sum_{b,t} dy_t x_{t-1},   db = sum_{b,t} dy_t.
+// Both passes are elementwise over (B, H, T, C) and bound by HBM bandwidth: each thread owns
+// 8 consecutive channels (one 16-byte load of bf16) of one token.  The weight gradients are
+// reduced per head by one block that walks every (b, t) of the head's channels.
+#include <algorithm>
+
+#include "tm2_common.cuh"
+#include "tm2_launch.h"
+
+namespace tm2 {
+
+template <typename Tin>
+TM2_DEV void ld8(const Tin* p, float* x);
+template <>
+TM2_DEV void ld8<float>(const float* p, float* x) {
+    const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+template <>
+TM2_DEV void ld8<__nv_bfloat16>(const __nv_bfloat16* p, float* x) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        x[2 * i] = __uint_as_float(w[i] << 16);
+        x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+template <typename Tout>
+TM2_DEV void st8(Tout* p, const float* x);
+template <>
+TM2_DEV void st8<float>(float* p, const float* x) {
+    reinterpret_cast<float4*>(p)[0] = make_float4(x[0], x[1], x[2], x[3]);
+    reinterpret_cast<float4*>(p)[1] = make_float4(x[4], x[5], x[6], x[7]);
+}
+TM2_DEV uint32_t bf16x2_bits(float lo, float hi) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+template <>
+TM2_DEV void st8<__nv_bfloat16>(__nv_bfloat16* p, const float* x) {
+    uint4 u;
+    u.x = bf16x2_bits(x[0], x[1]);
+    u.y = bf16x2_bits(x[2], x[3]);
+    u.z = bf16x2_bits(x[4], x[5]);
+    u.w = bf16x2_bits(x[6], x[7]);
+    *reinterpret_cast<uint4*>(p) = u;
+}
+
+// y (B,H,T,C) in the input type from x (B,H,T,C): one thread per (token, 8 channels).
+template <typename Tin>
+__global__ void conv2_fwd_kernel(const Tin* __restrict__ x, const float* __restrict__ w, const float* __restrict__ b,
+                                 const Tin* __restrict__ x_prev, Tin* __restrict__ y, long BH, int H, int T, int C) {
+    const int P = C / 8;
+    const long total = BH * (long)T * P;
+    for (long e = (long)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (long)gridDim.x * blockDim.x) {
+        const int pc = (int)(e % P);
+        const long tok = e / P;
+        const int t = (int)(tok % T);
+        const long bh = tok / T;
+        const int h = (int)(bh % H);
+        float cur[8], prv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, out[8];
+        ld8(x + tok * C + 8 * pc, cur);
+        if (t > 0) ld8(x + (tok - 1) * C + 8 * pc, prv);
+        else if (x_prev) ld8(x_prev + bh * C + 8 * pc, prv);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const long wc = (long)h * C + 8 * pc + i;
+            out[i] = fmaf(w[wc * 2], cur[i], w[wc * 2 + 1] * prv[i]) + (b ? b[wc] : 0.f);
+        }
+        st8(y + tok * C + 8 * pc, out);
+    }
+}
+
+// dx (B,H,T,C) fp32 and, optionally, dx_prev (B,H,C) fp32.
+template <typename Tin>
+__global__ void conv2_bwd_dx_kernel(const Tin* __restrict__ dy, const float* __restrict__ w, float* __restrict__ dx,
+                                    float* __restrict__ dx_prev, long BH, int H, int T, int C) {
+    const int P = C / 8;
+    const long total = BH * (long)T * P;
+    for (long e = (long)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (long)gridDim.x * blockDim.x) {
+        const int pc = (int)(e % P);
+        const long tok = e / P;
+        const int t = (int)(tok % T);
+        const long bh = tok / T;
+        const int h = (int)(bh % H);
+        float g0[8], g1[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, out[8];
+        ld8(dy + tok * C + 8 * pc, g0);
+        if (t + 1 < T) ld8(dy + (tok + 1) * C + 8 * pc, g1);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const long wc = (long)h * C + 8 * pc + i;
+            out[i] = fmaf(w[wc * 2], g0[i], w[wc * 2 + 1] * g1[i]);
+        }
+        st8(dx + tok * C + 8 * pc, out);
+        if (t == 0 && dx_prev) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) out[i] = w[((long)h * C + 8 * pc + i) * 2 + 1] * g0[i];
+            st8(dx_prev + bh * C + 8 * pc, out);
+        }
+    }
+}
+
+// dw (H,C,2), db (H,C) (optional): one block of 256 threads per head; thread (channel c,
+// lane group r of 256 / C) sums every (b, t) with t = r mod (256 / C), in fp64.
+template <typename Tin>
+__global__ void __launch_bounds__(256) conv2_bwd_dw_kernel(const Tin* __restrict__ x, const Tin* __restrict__ dy,
+                                                           const Tin* __restrict__ x_prev, float* __restrict__ dw,
+                                                           float* __restrict__ db, int B, int H, int T, int C) {
+    extern __shared__ double red[];   // [3][256]
+    const int h = blockIdx.x, tid = threadIdx.x, c = tid % C, r = tid / C, NR = 256 / C;
+    double s0 = 0.0, s1 = 0.0, sb = 0.0;
+    for (int bb = 0; bb < B; ++bb) {
+        const long bh = (long)bb * H + h;
+        for (int t = r; t < T; t += NR) {
+            const long tok = bh * T + t;
+            const float g = to_f(dy[tok * C + c]);
+            const float xc = to_f(x[tok * C + c]);
+            const float xp = t > 0 ? to_f(x[(tok - 1) * C + c]) : (x_prev ? to_f(x_prev[bh * C + c]) : 0.f);
+            s0 += (double)g * xc;
+            s1 += (double)g * xp;
+            sb += (double)g;
+        }
+    }
+    red[tid] = s0;
+    red[256 + tid] = s1;
+    red[512 + tid] = sb;
+    __syncthreads();
+    if (tid < C) {
+        double a0 = 0.0, a1 = 0.0, ab = 0.0;
+        for (int k = 0; k < NR; ++k) {
+            a0 += red[k * C + tid];
+            a1 += red[256 + k * C + tid];
+            ab += red[512 + k * C + tid];
+        }
+        dw[((long)h * C + tid) * 2] = (float)a0;
+        dw[((long)h * C + tid) * 2 + 1] = (float)a1;
+        if (db) db[(long)h * C + tid] = (float)ab;
+    }
+}
+
+static unsigned grid_for(long total) {
+    return (unsigned)std::max<long>(1, std::min<long>((total + 255) / 256, 148L * 16));
+}
+
+cudaError_t launch_conv2_fwd(long BH, int H, int T, int C, int dtype, const void* x, const float* w, const float* b,
+                             const void* x_prev, void* y, cudaStream_t s) {
+    const long total = BH * (long)T * (C / 8);
+    if (total == 0) return cudaSuccess;
+    if (dtype == 1)
+        conv2_fwd_kernel<__nv_bfloat16><<<grid_for(total), 256, 0, s>>>(
+            (const __nv_bfloat16*)x, w, b, (const __nv_bfloat16*)x_prev, (__nv_bfloat16*)y, BH, H, T, C);
+    else
+        conv2_fwd_kernel<float><<<grid_for(total), 256, 0, s>>>((const float*)x, w, b, (const float*)x_prev,
+                                                               (float*)y, BH, H, T, C);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_conv2_bwd(int B, int H, int T, int C, int dtype, const void* x, const float* w,
+                             const void* x_prev, const void* dy, float* dx, float* dx_prev, float* dw, float* db,
+                             cudaStream_t s) {
+    const long BH = (long)B * H;
+    const long total = BH * (long)T * (C / 8);
+    if (total == 0) return cudaSuccess;
+    if (dtype == 1) {
+        conv2_bwd_dx_kernel<__nv_bfloat16><<<grid_for(total), 256, 0, s>>>((const __nv_bfloat16*)dy, w, dx, dx_prev,
+                                                                          BH, H, T, C);
+        conv2_bwd_dw_kernel<__nv_bfloat16><<<H, 256, 3 * 256 * sizeof(double), s>>>(
+            (const __nv_bfloat16*)x, (const __nv_bfloat16*)dy, (const __nv_bfloat16*)x_prev, dw, db, B, H, T, C);
+    } else {
+        conv2_bwd_dx_kernel<float><<<grid_for(total), 256, 0, s>>>((const float*)dy, w, dx, dx_prev, BH, H, T, C);
+        conv2_bwd_dw_kernel<float><<<H, 256, 3 * 256 * sizeof(double), s>>>(
+            (const float*)x, (const float*)dy, (const float*)x_prev, dw, db, B, H, T, C);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace tm2

@@ -116,9 +116,21 @@ cudaError_t tc_chunk_out(const Problem& p, const void* q, const void* k, const v
                          const void* Sx, const float* zx, const unsigned* amax, float* o, float* Z, cudaStream_t s);
 
 // ---- decode --------------------------------------------------------------------------
-cudaError_t launch_decode_step(int N, int H, int d, int dv, int dtype, bool normalize,
-                               const void* q, const void* k, const void* v, const float* a,
-                               float* S, float* z, void* o, float* Z, cudaStream_t s);
+// The size-2 input convolution applied inside the decode step: per tensor x in (q, k, v),
+// weights (H, d, 2), optional bias (H, d), cache of the previous raw token (N, H, d) in the
+// input dtype, read and then overwritten with the current token.
+struct DecodeConv {
+    const float* w[3];
+    const float* b[3];
+    void* cache[3];
+};
+// packed: S (N,H,d(d+1)/2,dv) and z (N,H,d(d+1)/2) symmetric-packed; conv: optional.
+cudaError_t launch_decode_step(int N, int H, int d, int dv, int dtype, bool normalize, bool packed,
+                               const DecodeConv* conv, const void* q, const void* k, const void* v,
+                               const float* a, float* S, float* z, void* o, float* Z, cudaStream_t s);
+// full (nh, d*d, cols) <-> packed (nh, d(d+1)/2, cols): pack takes the symmetric part.
+cudaError_t launch_state_pack(const float* full, float* packed, long nh, int d, int cols, bool unpack,
+                              cudaStream_t s);
 
 // ---- attention-form kernels: 2Mamba-E and the quadratic (C = T) form of 2Mamba -----
 // KIND of the tensor-core and CUDA-core attention-form kernels: 2Mamba-E (softmax of
@@ -143,6 +155,25 @@ cudaError_t tc_poly_bwd(const Problem& p, int order, const void* q, const void* 
 cudaError_t simt_poly_bwd(const Problem& p, int order, const void* q, const void* k, const void* v,
                           const float* cum, const float* cum_lo, const float* zeta, const float* D, const void* dO,
                           void* dq, void* dk, void* dv, float* rowsum, float* colsum, cudaStream_t s);
+
+// ---- 2Mamba-E decoding over a key/value cache (tm2_e_decode.cu) ---------------------
+// Kc (NH, L, d), Vc (NH, L, d) in the input dtype and cumc (NH, L, 2) fp32 hi + lo running
+// sums; the token at `pos` is appended; part: NH x e_decode_max_splits(L) x (d + 2) floats.
+int e_decode_splits(int pos);
+int e_decode_max_splits(int L);
+cudaError_t launch_e_decode(long NH, int d, int dtype, int pos, int L, float scale, const void* q, const void* k,
+                            const void* v, const float* a, void* Kc, void* Vc, float* cumc, float* part, float* o,
+                            float* lse, cudaStream_t s);
+cudaError_t launch_e_cache_fill(long NH, int T, int L, int d, int dv, int dtype, const void* k, const void* v,
+                                const float* cum, const float* cum_lo, void* Kc, void* Vc, float* cumc,
+                                cudaStream_t s);
+
+// ---- the size-2 input convolution (tm2_conv.cu) ---------------------------------------
+cudaError_t launch_conv2_fwd(long BH, int H, int T, int C, int dtype, const void* x, const float* w, const float* b,
+                             const void* x_prev, void* y, cudaStream_t s);
+cudaError_t launch_conv2_bwd(int B, int H, int T, int C, int dtype, const void* x, const float* w,
+                             const void* x_prev, const void* dy, float* dx, float* dx_prev, float* dw, float* db,
+                             cudaStream_t s);
 
 // ---- 2Mamba-E ----------------------------------------------------------------------
 // The forward entry points' shared steps (tm2_api.cu): argument checks (fills p; TM2_OK with

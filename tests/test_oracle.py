@@ -462,3 +462,44 @@ def test_first_order_gradients(normalize):
     for g, ref in zip(grads, (tq.grad, tk.grad, tv.grad, ta.grad)):
         assert relmax(g, ref.numpy()) < 1e-10
     assert np.abs(grads[3][..., 0]).max() < 1e-10 * np.abs(grads[3]).max()
+
+
+# ---------------------------------------------------------------- input convolution (window 2)
+
+def test_conv2_against_torch_conv1d_and_autograd():
+    """The size-2 causal depthwise convolution (Sec. 3-4) against torch's conv1d in fp64 (groups =
+    channels, left padding 1, the kernel reversed: conv1d weight [.., 0] multiplies x_{t-1}) with
+    an initial token x_prev prepended, and its gradients against torch autograd."""
+    rng = np.random.default_rng(91)
+    B, H, T, C = 2, 3, 17, 4
+    x = rng.standard_normal((B, H, T, C))
+    w = rng.standard_normal((H, C, 2))
+    b = rng.standard_normal((H, C))
+    xp = rng.standard_normal((B, H, C))
+    dy = rng.standard_normal((B, H, T, C))
+    y = oracle.conv2_fwd(x, w, b, xp)
+    tx, tw, tb, txp = (torch.tensor(z, requires_grad=True) for z in (x, w, b, xp))
+    seq = torch.cat([txp[:, :, None], tx], dim=2)                       # (B,H,T+1,C)
+    inp = seq.permute(0, 1, 3, 2).reshape(B, H * C, T + 1)
+    ker = torch.stack([tw[..., 1], tw[..., 0]], dim=-1).reshape(H * C, 1, 2)
+    out = torch.nn.functional.conv1d(inp, ker, bias=tb.reshape(H * C), groups=H * C)   # (B,H*C,T)
+    ty = out.reshape(B, H, C, T).permute(0, 1, 3, 2)
+    assert relmax(y, ty.detach().numpy()) < 1e-13
+    (ty * torch.tensor(dy)).sum().backward()
+    dx, dxp, dw, db = oracle.conv2_bwd(x, w, dy, xp)
+    for g, ref in ((dx, tx.grad), (dxp, txp.grad), (dw, tw.grad), (db, tb.grad)):
+        assert relmax(g, ref.numpy()) < 1e-12
+
+
+def test_conv2_identity_and_shift():
+    """w = (1, 0) is the identity; w = (0, 1) shifts by one token (x_prev first)."""
+    rng = np.random.default_rng(92)
+    x = rng.standard_normal((1, 2, 9, 3))
+    xp = rng.standard_normal((1, 2, 3))
+    one = np.zeros((2, 3, 2))
+    one[..., 0] = 1.0
+    assert np.array_equal(oracle.conv2_fwd(x, one, None, xp), x)
+    sh = np.zeros((2, 3, 2))
+    sh[..., 1] = 1.0
+    ys = oracle.conv2_fwd(x, sh, None, xp)
+    assert np.array_equal(ys[:, :, 1:], x[:, :, :-1]) and np.array_equal(ys[:, :, 0], xp)
