@@ -90,7 +90,8 @@ def kernel_flops(name, d, dv, C, tokens):
 
 def kernel_bytes(name, d, dv, C, tokens, in_bytes=2):
     """Algorithmic HBM bytes of one launch over `tokens` token-heads: the token rows the kernel
-    must read or write, plus the chunk states it must write or read (two fp16 planes of
+    must read or write (inputs and the gradients dq, dk, dv in the input type, o and the
+    per-token scalars in fp32), plus the chunk states it must write or read (two fp16 planes of
     d^2 x dv and the fp32 normaliser column per chunk, amortised over the C tokens of a
     chunk).  Scratch the implementation adds (operand blocks) is not counted."""
     state = (2 * 2 * d * d * dv + 4 * d * d) / C
@@ -98,27 +99,47 @@ def kernel_bytes(name, d, dv, C, tokens, in_bytes=2):
         "tc_state_scan_fwd": state + in_bytes * (d + dv),
         "tc_state_scan_bwd": state + in_bytes * (d + dv) + 4 * 2,
         "tc_chunk_out": state + in_bytes * (2 * d + dv) + 4 * (dv + 1),
-        "tc_bwd_dq": state + in_bytes * (2 * d + 2 * dv) + 4 * (d + 2),
-        "tc_bwd_dkdv": state + in_bytes * (2 * d + 2 * dv) + 4 * (d + dv + 4),
+        "tc_bwd_dq": state + in_bytes * (2 * d + 2 * dv) + in_bytes * d + 4 * 2,
+        "tc_bwd_dkdv": state + in_bytes * (2 * d + 2 * dv) + in_bytes * (d + dv) + 4 * 4,
     }.get(name)
     return None if per is None else per * tokens
 
 
-def decode_bytes_per_head(d, dv):
-    return 2 * d * d * dv * 4 + 2 * d * d * 4 + 3 * d * 4 + 4 + dv * 4 + 4
+def decode_bytes_per_head(d, dv, packed=False):
+    """Algorithmic bytes of one decode step of one (sequence, head): the fp32 state S and z read
+    and written once (d^2 rows, or d(d+1)/2 symmetric-packed), the token in, y and zeta out."""
+    rows = d * (d + 1) // 2 if packed else d * d
+    return 2 * rows * dv * 4 + 2 * rows * 4 + 3 * d * 4 + 4 + dv * 4 + 4
 
 
-def roofline(kernel, kf, kb, ms_per_launch, pk, tc):
+def e_decode_bytes_per_head(ctx, d, dv, in_bytes=2):
+    """Algorithmic bytes of one 2Mamba-E decode step of one (sequence, head) at context ctx: the
+    cached keys, values and running sums read once, the new row appended, q in, o and lse out."""
+    return ctx * ((d + dv) * in_bytes + 8) + (d + dv) * in_bytes + 8 + d * in_bytes + 4 + dv * 4 + 4
+
+
+SUSTAINED_AFTER_MS = 1000.0   # a timed region this long runs under the power cap: sustained peak
+
+
+def tensor_peak_key(timed_ms):
+    """Which measured bf16 figure a tensor-core kernel is held to: the burst one for a timed
+    region shorter than a second (the clocks have not settled under the power cap), the
+    sustained one for a longer region."""
+    return "bf16_tflops_sustained" if timed_ms >= SUSTAINED_AFTER_MS else "bf16_tflops"
+
+
+def roofline(kernel, kf, kb, ms_per_launch, pk, tc, peak_key="bf16_tflops_sustained"):
     """Roofline entry of one kernel from its algorithmic flops kf and bytes kb per launch and its
-    live launch time.  Tensor-core kernels (timed inside a long step) are measured against the
-    sustained bf16 figure or the HBM copy bandwidth, whichever bound takes longer for the
-    kernel's algorithmic work; CUDA-core kernels against the fp32 FMA rate derived from the SM
-    count and clock.  None when the kernel's work is not counted."""
+    live launch time.  Tensor-core kernels are measured against the measured bf16 figure named by
+    peak_key (tensor_peak_key: burst or sustained) or the HBM copy bandwidth, whichever bound takes
+    longer for the kernel's algorithmic work; CUDA-core kernels against the fp32 FMA rate derived
+    from the SM count and clock.  None when the kernel's work is not counted."""
     if kf is None:
         return None
     sec = ms_per_launch * 1e-3
     if tc:
-        t_flop = kf / (pk["bf16_tflops_sustained"] * 1e12)
+        tp = pk[peak_key]
+        t_flop = kf / (tp * 1e12)
         t_byte = kb / (pk["hbm_gbs"] * 1e9)
         if t_byte > t_flop:
             roof = {"kernel": kernel, "bound": "hbm", "achieved": kb / sec / 1e9, "peak": pk["hbm_gbs"],
@@ -126,12 +147,12 @@ def roofline(kernel, kf, kb, ms_per_launch, pk, tc):
                     "peak_source": "MEASURED_PEAKS.json hbm_gbs (%s)" % pk["source"]}
         else:
             roof = {"kernel": kernel, "bound": "tensor", "achieved": kf / sec / 1e12,
-                    "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                    "frac": kf / sec / 1e12 / pk["bf16_tflops_sustained"],
-                    "peak_source": "MEASURED_PEAKS.json bf16_tflops_sustained (%s)" % pk["source"]}
+                    "peak": tp, "unit": "TFLOP/s", "frac": kf / sec / 1e12 / tp,
+                    "peak_source": "MEASURED_PEAKS.json %s (%s)" % (peak_key, pk["source"])}
         roof["algorithmic_flops_per_launch"] = kf
         roof["algorithmic_bytes_per_launch"] = kb
-        roof["tensor_frac"] = kf / sec / 1e12 / pk["bf16_tflops_sustained"]
+        roof["tensor_frac"] = kf / sec / 1e12 / tp
+        roof["tensor_peak"] = "%s = %.1f TFLOP/s" % (peak_key, tp)
         roof["hbm_frac"] = kb / sec / 1e9 / pk["hbm_gbs"]
         return roof
     peak = 148 * 128 * 2 * pk["sm_max_mhz"] * 1e6 / 1e12   # FFMA, TFLOP/s
@@ -363,6 +384,7 @@ def config_of(w, C):
                         "accumulate, normalised" % (w.B, w.H, w.T, w.d),
             "B": w.B, "H": w.H, "T": w.T, "d": w.d, "dv": w.dv, "chunk": C,
             "global_batch": w.B, "seq_len": w.T, "parallelism": "replicas (one per GPU)",
+            "outputs": "o fp32, gradients dq dk dv bf16 (TM2_GRADS_INPUT_DTYPE), da fp32",
             "l2": "flushed between timed steps (256 MiB write)"}
 
 
@@ -378,14 +400,15 @@ def run_tm2(args, world, rank, device):
     B, H, T, d, dv = w.B, w.H, w.T, w.d, w.dv
     o = torch.empty(g["v"].shape, dtype=torch.float32, device=device)
     Z = torch.empty((B, H, T), dtype=torch.float32, device=device)
-    grads = tuple(torch.empty(g[n].shape, dtype=torch.float32, device=device) for n in ("q", "k", "v", "a"))
+    grads = tuple(torch.empty(g[n].shape, dtype=g[n].dtype if n != "a" else torch.float32, device=device)
+                  for n in ("q", "k", "v", "a"))
     # one workspace for both calls: the backward reads the chunk states the forward left in it
     ws = torch.empty(tm2.workspace_bytes(B, H, T, d, dv, C), dtype=torch.uint8, device=device)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
 
     def step(q, k, v, a, dO):
         tm2.forward(q, k, v, a, chunk=C, out=o, Z=Z, workspace=ws)
-        tm2.backward(q, k, v, a, o, Z, dO, chunk=C, workspace=ws, grads=grads, reuse_states=True)
+        tm2.backward(q, k, v, a, o, Z, dO, chunk=C, workspace=ws, grads=grads, reuse_states=True, lowp_grads=True)
 
     for _ in range(args.warmup):
         step(g["q"], g["k"], g["v"], g["a"], g["dO"])
@@ -420,19 +443,31 @@ def run_tm2(args, world, rank, device):
     tc = dom.startswith("tc_")
     kf = kernel_flops(dom, d, dv, 256 if tc else 64, per_launch_tokens)
     kb = kernel_bytes(dom, d, dv, 256, per_launch_tokens) if tc else None
-    roof = roofline(dom, kf, kb, kern[dom]["ms_per_launch"], pk, tc)
+    timed_ms = step_ms * args.steps
+    peak_key = tensor_peak_key(timed_ms)
+    roof = roofline(dom, kf, kb, kern[dom]["ms_per_launch"], pk, tc, peak_key)
     if roof is not None:
         roof["traffic"] = ncu_traffic(dom, per_launch_tokens)
     CH = TC_CHUNK
     counted = (fwd_flops(d, dv, CH) + bwd_flops(d, dv, CH)) * B * H * T
-    tensor_frac = counted / (step_ms * 1e-3) / (pk["bf16_tflops_sustained"] * 1e12)
+    tensor_frac = counted / (step_ms * 1e-3) / (pk[peak_key] * 1e12)
+    per_kernel_roof = {}
+    for n, a in kern.items():
+        if n.startswith("tc_"):
+            r = roofline(n, kernel_flops(n, d, dv, 256, per_launch_tokens), kernel_bytes(n, d, dv, 256, per_launch_tokens),
+                         a["ms_per_launch"], pk, True, peak_key)
+            if r is not None:
+                per_kernel_roof[n] = {"bound": r["bound"], "frac": round(r["frac"], 4),
+                                      "tensor_frac": round(r["tensor_frac"], 4), "hbm_frac": round(r["hbm_frac"], 4)}
 
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic", "config": config_of(w, CH), "roofline": roof,
             "step_bf16_tensor_peak_frac": tensor_frac,
-            "step_tensor_peak": "bf16_tflops_sustained of MEASURED_PEAKS.json (%s)" % pk["source"],
+            "step_tensor_peak": "%s of MEASURED_PEAKS.json (%s): timed region %.0f ms (%s a second)" % (
+                peak_key, pk["source"], timed_ms, "over" if timed_ms >= SUSTAINED_AFTER_MS else "under"),
+            "kernel_roofline": per_kernel_roof,
             "step_counted_flops": counted, "gpu_launches": launches,
             "kernels": {n: {k: round(v, 4) if isinstance(v, float) else v for k, v in a.items()}
                         for n, a in kern.items()},
@@ -444,6 +479,10 @@ def run_tm2(args, world, rank, device):
         line["decode"] = run_decode(args, tm2, device, trace, pk, world)
     if not args.no_e:
         line["e_variant"] = run_e_variant(args, tm2, device, trace, world)
+    if not args.no_decode:
+        line["e_decode"] = run_e_decode(args, tm2, device, trace, pk, world)
+    if not args.no_quadratic:
+        line["quadratic_form"] = run_quadratic(args, tm2, device, trace, pk, world)
     if rank == 0 and world == 1 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(inp_cpu, w)
     if rank == 0:
@@ -457,7 +496,9 @@ def run_e2e(args, tm2, inp_cpu, device, C, world):
     model: step i+1's inputs travel in and step i-1's results travel out while step i computes
     (three streams, double-buffered device inputs and host outputs)."""
     host_in = [{k: v.pin_memory() for k, v in inp_cpu.items()} for _ in range(2)]
-    host_out = [{n: torch.empty(inp_cpu[src].shape, dtype=torch.float32).pin_memory()
+    out_types = {"o": torch.float32, "dq": inp_cpu["q"].dtype, "dk": inp_cpu["k"].dtype, "dv": inp_cpu["v"].dtype,
+                 "da": torch.float32}
+    host_out = [{n: torch.empty(inp_cpu[src].shape, dtype=out_types[n]).pin_memory()
                  for n, src in (("o", "v"), ("dq", "q"), ("dk", "k"), ("dv", "v"), ("da", "a"))} for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host_in[0].values())
     d2h = sum(t.numel() * t.element_size() for t in host_out[0].values())
@@ -466,6 +507,9 @@ def run_e2e(args, tm2, inp_cpu, device, C, world):
     ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_used = [torch.cuda.Event() for _ in range(2)]
     ev_done = [torch.cuda.Event() for _ in range(2)]
+    B0, H0, T0, d0 = inp_cpu["q"].shape
+    ws = torch.empty(tm2.workspace_bytes(B0, H0, T0, d0, inp_cpu["v"].shape[-1], C), dtype=torch.uint8,
+                     device=device)   # one workspace: the backward reads the forward's chunk states
     for e in ev_used:
         e.record(torch.cuda.current_stream())
 
@@ -480,8 +524,9 @@ def run_e2e(args, tm2, inp_cpu, device, C, world):
             with torch.cuda.stream(s_comp):
                 s_comp.wait_event(ev_in[b])
                 g = dev_in[b]
-                o, Z = tm2.forward(g["q"], g["k"], g["v"], g["a"], chunk=C)
-                dq, dk, dv, da = tm2.backward(g["q"], g["k"], g["v"], g["a"], o, Z, g["dO"], chunk=C)
+                o, Z = tm2.forward(g["q"], g["k"], g["v"], g["a"], chunk=C, workspace=ws)
+                dq, dk, dv, da = tm2.backward(g["q"], g["k"], g["v"], g["a"], o, Z, g["dO"], chunk=C, workspace=ws,
+                                              reuse_states=True, lowp_grads=True)
                 ev_used[b].record(s_comp)
                 ev_done[b].record(s_comp)
             with torch.cuda.stream(s_out):              # results of step i (host buffer b free once step i-2's are out)
@@ -508,7 +553,8 @@ def run_e2e(args, tm2, inp_cpu, device, C, world):
     return {"value": world * B * T / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
             "pipeline": "copy-in / compute / copy-out on three streams, double-buffered; every step "
-                        "moves its own inputs and results"}
+                        "moves its own inputs and results (o and da fp32, dq dk dv bf16); the backward "
+                        "reuses the forward's chunk states"}
 
 
 def run_decode(args, tm2, device, trace, pk, world):
@@ -540,14 +586,129 @@ def run_decode(args, tm2, device, trace, pk, world):
     kms = sum(m for _, m in recs) / max(len(recs), 1)
     nbytes = decode_bytes_per_head(d, dv) * N * H
     gbs = nbytes / (kms * 1e-3) / 1e9
-    return {"workload": "decode step, N=%d sequences x H=%d, d=dv=%d, fp32 state, %d steps" % (N, H, d, n),
-            "ms_per_step": ms, "kernel_ms_per_launch": kms, "bytes_per_step": nbytes,
-            "GBps": world * nbytes / (ms * 1e-3) / 1e9, "unit": "GB/s",
-            "roofline": {"kernel": "decode_step", "bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"],
-                         "unit": "GB/s", "frac": gbs / pk["hbm_gbs"],
-                         "traffic": ncu_traffic("decode_step", N * H)},
-            "tokens_per_s": world * N / (ms * 1e-3), "l2": "state (4.3 GB) larger than L2",
-            "gpu_launches": len(recs)}
+    out = {"workload": "decode step, N=%d sequences x H=%d, d=dv=%d, fp32 state, %d steps" % (N, H, d, n),
+           "ms_per_step": ms, "kernel_ms_per_launch": kms, "bytes_per_step": nbytes,
+           "GBps": world * nbytes / (ms * 1e-3) / 1e9, "unit": "GB/s",
+           "roofline": {"kernel": "decode_step", "bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"],
+                        "unit": "GB/s", "frac": gbs / pk["hbm_gbs"],
+                        "traffic": ncu_traffic("decode_step", N * H)},
+           "tokens_per_s": world * N / (ms * 1e-3), "l2": "state (4.3 GB) larger than L2",
+           "gpu_launches": len(recs)}
+    # the same workload on the symmetric-packed state (the outputs are the full state's)
+    Sp, zp = tm2.state_pack(S, z)
+    del S, z
+    torch.cuda.synchronize()
+    for t in range(3):
+        x = toks[t % 8]
+        tm2.step(x["q"], x["k"], x["v"], x["a"], Sp, zp, packed=True, out=o, Z=Zo)
+    torch.cuda.synchronize()
+    barrier(world)
+    trace.start()
+    ev0.record()
+    for t in range(n):
+        x = toks[t % 8]
+        tm2.step(x["q"], x["k"], x["v"], x["a"], Sp, zp, packed=True, out=o, Z=Zo)
+    ev1.record()
+    torch.cuda.synchronize()
+    recs = trace.stop()
+    pms = max_over_ranks(ev0.elapsed_time(ev1) / n, world)
+    pkms = sum(m for _, m in recs) / max(len(recs), 1)
+    pbytes = decode_bytes_per_head(d, dv, packed=True) * N * H
+    pgbs = pbytes / (pkms * 1e-3) / 1e9
+    out["packed"] = {"ms_per_step": pms, "kernel_ms_per_launch": pkms, "bytes_per_step": pbytes,
+                     "tokens_per_s": world * N / (pms * 1e-3),
+                     "effective_GBps": world * nbytes / (pms * 1e-3) / 1e9,
+                     "roofline": {"kernel": "decode_step_packed", "bound": "hbm", "achieved": pgbs,
+                                  "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": pgbs / pk["hbm_gbs"],
+                                  "traffic": ncu_traffic("decode_step_packed", N * H)},
+                     "note": "symmetric-packed state (d(d+1)/2 of d^2 rows); effective_GBps counts the full "
+                             "state's bytes, roofline the bytes actually moved"}
+    return out
+
+
+def run_e_decode(args, tm2, device, trace, pk, world):
+    """2Mamba-E decoding over a bf16 KV cache: 64 sequences x 16 heads, d = dv = 64, the token at
+    position 8191 attends over 8192 cached keys (2.1 GB of cache, larger than L2)."""
+    N, H, d, ctx = 64, 16, 64, 8192
+    g = torch.Generator(device).manual_seed(rank_seed(6, 0))   # cache drawn on the device (2 GB)
+    Kc = torch.randn(N, H, ctx, d, generator=g, device=device).to(torch.bfloat16)
+    Vc = torch.randn(N, H, ctx, d, generator=g, device=device).to(torch.bfloat16)
+    cc = torch.cumsum(-torch.nn.functional.softplus(torch.randn(N, H, ctx, generator=g, device=device)), -1)
+    cum = torch.stack([cc, torch.zeros_like(cc)], -1).contiguous()
+    tok = {k: v.to(device) for k, v in si.decode_token(0, N, H, d, d, dtype="bf16", qkv_std=1.0, seed=6).items()}
+    o = torch.empty((N, H, d), dtype=torch.float32, device=device)
+    lse = torch.empty((N, H), dtype=torch.float32, device=device)
+    ws = torch.empty(tm2.lib().tm2e_step_workspace(N, H, ctx, d, d, 1), dtype=torch.uint8, device=device)
+    pos = ctx - 1
+    for _ in range(3):
+        tm2.e_step(tok["q"], tok["k"], tok["v"], tok["a"], Kc, Vc, cum, pos, out=o, lse=lse, workspace=ws)
+    torch.cuda.synchronize()
+    n = max(args.steps, 10)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    trace.start()
+    ev0.record()
+    for _ in range(n):
+        tm2.e_step(tok["q"], tok["k"], tok["v"], tok["a"], Kc, Vc, cum, pos, out=o, lse=lse, workspace=ws)
+    ev1.record()
+    torch.cuda.synchronize()
+    recs = trace.stop()
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / n, world)
+    nbytes = e_decode_bytes_per_head(ctx, d, d) * N * H
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": "2Mamba-E decode over a bf16 KV cache, N=%d sequences x H=%d, d=dv=%d, context %d, %d steps"
+                        % (N, H, d, ctx, n),
+            "ms_per_step": ms, "bytes_per_step": nbytes, "tokens_per_s": world * N / (ms * 1e-3),
+            "roofline": {"kernel": "e_decode", "bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / pk["hbm_gbs"], "traffic": ncu_traffic("e_decode", N * H)},
+            "kernels": {nm: round(a["ms"], 3) for nm, a in summarize(recs).items()}, "gpu_launches": len(recs)}
+
+
+def run_quadratic(args, tm2, device, trace, pk, world):
+    """The quadratic (C = T) form against the chunked form: the forward workload B=4 H=16 T=2048
+    (bf16, d = dv = 64) and fwd+bwd at B=2 H=16 T=4096; tokens/s of each and the faster one."""
+    out = {}
+    for label, wid, bwd in (("fwd_B4_H16_T2048", 2, False), ("fwdbwd_B2_H16_T4096", 5, True)):
+        w = si.WORKLOADS[wid]
+        inp = si.sequence_inputs(w.B, w.H, w.T, 64, 64, dtype="bf16", qkv_std=0.125, seed=rank_seed(wid, 0),
+                                 with_dO=bwd)
+        g = {k: v.to(device) for k, v in inp.items()}
+        ws = torch.empty(tm2.workspace_bytes(w.B, w.H, w.T, 64, 64), dtype=torch.uint8, device=device)
+
+        def chunked():
+            o, Z = tm2.forward(g["q"], g["k"], g["v"], g["a"], workspace=ws)
+            if bwd:
+                tm2.backward(g["q"], g["k"], g["v"], g["a"], o, Z, g["dO"], workspace=ws, reuse_states=True)
+
+        def quadratic():
+            o, Z = tm2.forward_quadratic(g["q"], g["k"], g["v"], g["a"])
+            if bwd:
+                tm2.backward_quadratic(g["q"], g["k"], g["v"], g["a"], o, Z, g["dO"])
+
+        res = {}
+        flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+        for name, fn in (("chunked", chunked), ("quadratic", quadratic)):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            n = max(1, min(args.steps, 10))
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+            barrier(world)
+            for i in range(n):
+                flush.zero_()
+                evs[i][0].record()
+                fn()
+                evs[i][1].record()
+            torch.cuda.synchronize()
+            res[name] = max_over_ranks(sum(a.elapsed_time(b) for a, b in evs) / n, world)
+        T, BH = w.T, w.B * w.H
+        qflops = ((T + 1) * 128 + (((T + 1) * (3 * 64 + 2 * 64)) if bwd else 0)) * BH * T
+        best = min(res, key=res.get)
+        out[label] = {"chunked_ms": res["chunked"], "quadratic_ms": res["quadratic"], "faster": best,
+                      "tokens_per_s": world * w.B * T / (res[best] * 1e-3),
+                      "quadratic_counted_flops": qflops,
+                      "quadratic_bf16_tensor_peak_frac": qflops / (res["quadratic"] * 1e-3) / (pk["bf16_tflops"] * 1e12)}
+    return out
 
 
 def run_e_variant(args, tm2, device, trace, world):
@@ -579,7 +740,9 @@ def run_e_variant(args, tm2, device, trace, world):
     flops = ((T + 1) * (d + dv) + (T + 1) * (3 * d + 2 * dv)) * B * H * T
     return {"workload": "2Mamba-E forward+backward, B=%d H=%d T=%d d=dv=%d bf16" % (B, H, T, d),
             "ms_per_step": ms, "tokens_per_s": world * B * T / (ms * 1e-3),
-            "counted_flops": flops, "bf16_tensor_peak_frac": flops / (ms * 1e-3) / (peaks()["bf16_tflops"] * 1e12),
+            "counted_flops": flops,
+            "bf16_tensor_peak_frac": flops / (ms * 1e-3) / (peaks()[tensor_peak_key(ms * n)] * 1e12),
+            "tensor_peak": tensor_peak_key(ms * n),
             "kernels": {n: round(a["ms"], 3) for n, a in summarize(recs).items()},
             "gpu_launches": len(recs)}
 
@@ -602,6 +765,28 @@ def run_case(name):
         g = {k: v.to(dev) for k, v in inp.items()}
         o, Z = tm2.forward(g["q"], g["k"], g["v"], g["a"])
         tm2.backward(g["q"], g["k"], g["v"], g["a"], o, Z, g["dO"])
+    elif name == "fwdbwd_h16":          # B=1, H=16, T=8192: 512 MB of chunk states per walk (4x L2)
+        inp = si.sequence_inputs(1, 16, 8192, 64, 64, dtype="bf16", qkv_std=0.125, seed=3, with_dO=True)
+        g = {k: v.to(dev) for k, v in inp.items()}
+        o, Z = tm2.forward(g["q"], g["k"], g["v"], g["a"])
+        tm2.backward(g["q"], g["k"], g["v"], g["a"], o, Z, g["dO"], lowp_grads=True)
+    elif name == "decode_packed_small":   # 32 sequences x 16 heads, packed state: 272 MB
+        N, H, d = 32, 16, 64
+        S, z = si.decode_initial_state(N, H, d, d, S0_std=0.01)
+        Sp, zp = tm2.state_pack(S.to(dev), z.to(dev))
+        x = {k: v.to(dev) for k, v in si.decode_token(0, N, H, d, d, qkv_std=0.125).items()}
+        for _ in range(3):
+            tm2.step(x["q"], x["k"], x["v"], x["a"], Sp, zp, packed=True)
+    elif name == "e_decode_small":      # 2Mamba-E decode, 16 sequences x 16 heads, context 8192: 537 MB cache
+        N, H, d, ctx = 16, 16, 64, 8192
+        gen = torch.Generator(dev).manual_seed(6)
+        Kc = torch.randn(N, H, ctx, d, generator=gen, device=dev).to(torch.bfloat16)
+        Vc = torch.randn(N, H, ctx, d, generator=gen, device=dev).to(torch.bfloat16)
+        cc = torch.cumsum(-torch.nn.functional.softplus(torch.randn(N, H, ctx, generator=gen, device=dev)), -1)
+        cum = torch.stack([cc, torch.zeros_like(cc)], -1).contiguous()
+        x = {k: v.to(dev) for k, v in si.decode_token(0, N, H, d, d, dtype="bf16", qkv_std=1.0, seed=6).items()}
+        for _ in range(3):
+            tm2.e_step(x["q"], x["k"], x["v"], x["a"], Kc, Vc, cum, ctx - 1)
     elif name == "e_small":             # 2Mamba-E, B=1, H=4, T=4096
         inp = si.sequence_inputs(1, 4, 4096, 64, 64, dtype="bf16", qkv_std=1.0, seed=5, with_dO=True)
         g = {k: v.to(dev) for k, v in inp.items()}
@@ -623,6 +808,7 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-quadratic", action="store_true")
     ap.add_argument("--case", default=None, help="run one small profiling case and exit")
     args = ap.parse_args()
     if args.case:

@@ -24,9 +24,12 @@
  *  - Pointers are DEVICE pointers unless stated otherwise, owned by the caller,
  *    16-byte aligned (TM2_ERR_ALIGNMENT otherwise), and tensors are dense row-major:
  *    q, k, dq, dk: (B,H,T,d); v, o, dO, dv: (B,H,T,dv); a, Z, lse, da: (B,H,T).
- *  - dtype (tm2_dtype) is the element type of the inputs q, k, v and dO.  Every output
- *    (o, Z, lse, dq, dk, dv, da), the A-mask input a and every state are fp32: the
- *    arithmetic accumulates in fp32 and the results are returned unrounded.
+ *  - dtype (tm2_dtype) is the element type of the inputs q, k, v and dO.  The gradients dq,
+ *    dk, dv are fp32, or in dtype with TM2_GRADS_INPUT_DTYPE.  The A-mask input a, da, Z, lse
+ *    and every state are fp32, and so is the forward output o: the backward takes o and forms
+ *    D_i = dO_i . o_i from it, and rounding o to bf16 alone moves the normalised mixer's dq and
+ *    dk by about 4e-2 of their RMS (the fp64 oracle's backward evaluated at a bf16-rounded o,
+ *    B=1 H=4 T=2048 d=64), beyond the bf16 parity bar.  The arithmetic accumulates in fp32.
  *  - State layout: S is (B,H,d*d,dv) with row r = m*d + n (key feature indices m, n);
  *    z is (B,H,d*d).  The same layout serves forward (initial/final state) and decode.
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream).
@@ -80,6 +83,11 @@ typedef enum { TM2_F32 = 0, TM2_BF16 = 1 } tm2_dtype;
  * symmetric part), and a step moves about half the bytes ("2Mamba2Furious", Sec. 5.1: memory
  * of the squared state; Sec. 7: hidden-state size). */
 #define TM2_PACKED_STATE 4u
+/* Backward entry points: dq, dk, dv are written in dtype (bf16 for bf16 inputs), each the
+ * round-to-nearest of the fp32 value written without the flag.  (Rounding alone can move a
+ * heavy-tailed gradient tensor's max|err| / RMS past 2e-2, so the unrounded fp32 form is the
+ * default.) */
+#define TM2_GRADS_INPUT_DTYPE 8u
 
 /* Library version (major*10000 + minor*100 + patch). */
 int tm2_version(void);
@@ -116,8 +124,9 @@ size_t tm2_backward_workspace(int B, int H, int T, int d, int dv, int chunk, int
  * 2Mamba backward (App. C, C.1): gradients of sum(dO * o) w.r.t. q, k, v and the raw
  * A-mask input a, for a forward with no initial state.  o and Z are the forward's
  * outputs for the same inputs and flags (Z may be NULL when TM2_NORMALIZE is off).
- * o is the fp32 output of tm2_forward; dq, dk, dv, da are fp32.  flags: TM2_NORMALIZE as in
- * the forward, optionally TM2_REUSE_STATES.  The A-mask gradient is the row-axis sum minus the
+ * o is the fp32 output of tm2_forward; dq, dk, dv fp32 (in dtype with TM2_GRADS_INPUT_DTYPE), da
+ * fp32.  flags: TM2_NORMALIZE as in the forward, optionally TM2_REUSE_STATES and
+ * TM2_GRADS_INPUT_DTYPE.  The A-mask gradient is the row-axis sum minus the
  * column-axis sum of w_ij * dL/dw_ij, accumulated from the end of the sequence and
  * multiplied by d(-softplus(a))/da = -sigmoid(a).
  */
@@ -153,7 +162,7 @@ int tm2_step(const void* q, const void* k, const void* v, const float* a,
  * Layouts, dtypes and alignment as for tm2_forward; o (B,H,T,dv) and Z (B,H,T, optional) fp32.
  * bf16 inputs with d = dv = 64 run on the tensor cores (the 2Mamba-E kernels' skeleton with
  * the weights above), everything else on CUDA cores in fp32 arithmetic.  Any T >= 0.
- * flags: TM2_NORMALIZE only.
+ * flags: TM2_NORMALIZE (and, for the backward, TM2_GRADS_INPUT_DTYPE).
  */
 size_t tm2q_forward_workspace(int B, int H, int T, int d, int dv, int order, int dtype, unsigned flags);
 int tm2q_forward(const void* q, const void* k, const void* v, const float* a, void* o, float* Z,
@@ -163,7 +172,7 @@ int tm2q_forward(const void* q, const void* k, const void* v, const float* a, vo
 /*
  * Backward of tm2q_forward (App. C, C.1): gradients of sum(dO * o) w.r.t. q, k, v and the raw
  * A-mask input a, given the forward's o and Z (both may be NULL without TM2_NORMALIZE).
- * dq, dk, dv, da fp32; da as for tm2_backward (row-axis minus column-axis sums of
+ * dq, dk, dv fp32 (in dtype with TM2_GRADS_INPUT_DTYPE), da fp32; da as for tm2_backward (row-axis minus column-axis sums of
  * w_ij dL/dw_ij, accumulated from the end, times -sigmoid(a)).
  */
 size_t tm2q_backward_workspace(int B, int H, int T, int d, int dv, int order, int dtype, unsigned flags);
@@ -256,12 +265,13 @@ size_t tm2e_backward_workspace(int B, int H, int T, int d, int dv, int dtype);
 
 /*
  * 2Mamba-E backward: gradients of sum(dO * o) w.r.t. q, k, v and a, given the
- * forward's o (fp32) and lse.  dq, dk, dv, da are fp32.
+ * forward's o (fp32) and lse.  dq, dk, dv fp32 (in dtype with TM2_GRADS_INPUT_DTYPE, the only
+ * flag), da fp32.
  */
 int tm2e_backward(const void* q, const void* k, const void* v, const float* a,
                   const void* o, const float* lse, const void* dO,
                   void* dq, void* dk, void* dv, float* da,
-                  int B, int H, int T, int d, int dv_dim, float scale, int dtype,
+                  int B, int H, int T, int d, int dv_dim, float scale, int dtype, unsigned flags,
                   void* ws, size_t ws_bytes, void* stream);
 
 /*

@@ -30,6 +30,7 @@ _LIB_PATH = os.path.join(PKG, "libtm2.so")
 NORMALIZE = 1
 REUSE_STATES = 2
 PACKED_STATE = 4
+GRADS_INPUT_DTYPE = 8
 _DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 _lib = None
 
@@ -69,7 +70,7 @@ def _load():
     lib.tm2e_forward.restype = I
     lib.tm2e_forward.argtypes = [P] * 6 + [I] * 5 + [F, I, P, S, P]
     lib.tm2e_backward.restype = I
-    lib.tm2e_backward.argtypes = [P] * 11 + [I] * 5 + [F, I, P, S, P]
+    lib.tm2e_backward.argtypes = [P] * 11 + [I] * 5 + [F, I, U, P, S, P]
     for name in ("tm2q_forward_workspace", "tm2q_backward_workspace"):
         getattr(lib, name).restype = S
         getattr(lib, name).argtypes = [I] * 7 + [U]
@@ -143,6 +144,13 @@ def _seq_checks(q, k, v, a):
     return B, H, T, d, dv, _DTYPES[q.dtype]
 
 
+def _grad_buffers(q, k, v, a, lowp):
+    """dq, dk, dv in fp32 (or the input dtype with lowp), da in fp32: the backward's output types."""
+    gt = q.dtype if lowp else torch.float32
+    return (torch.empty(q.shape, dtype=gt, device=q.device), torch.empty(k.shape, dtype=gt, device=q.device),
+            torch.empty(v.shape, dtype=gt, device=q.device), torch.empty(a.shape, dtype=torch.float32, device=q.device))
+
+
 def _workspace(nbytes, device, workspace):
     if nbytes == 0:
         return None
@@ -188,18 +196,20 @@ def forward(q, k, v, a, *, normalize=True, chunk=0, S0=None, z0=None, return_sta
 
 
 def backward(q, k, v, a, o, Z, dO, *, normalize=True, chunk=0, workspace=None, stream=None,
-             grads=None, reuse_states=False):
+             grads=None, reuse_states=False, lowp_grads=False):
     """2Mamba backward.  Returns (dq, dk, dv, da).  With reuse_states=True, `workspace` must
     be the buffer the matching forward() call used (sized with workspace_bytes()); the chunk
-    states the forward left there are read instead of recomputed."""
+    states the forward left there are read instead of recomputed.  lowp_grads: dq, dk, dv in
+    the input dtype (rounded from the fp32 values) instead of fp32."""
     B, H, T, d, dv, dt = _seq_checks(q, k, v, a)
     L = _load()
-    flags = (NORMALIZE if normalize else 0) | (REUSE_STATES if reuse_states else 0)
+    flags = (NORMALIZE if normalize else 0) | (REUSE_STATES if reuse_states else 0) | \
+        (GRADS_INPUT_DTYPE if lowp_grads else 0)
     if reuse_states and (workspace is None or workspace.numel() * workspace.element_size() <
                          L.tm2_backward_workspace(B, H, T, d, dv, chunk, dt, flags)):
         raise TM2Error("reuse_states needs the forward's workspace, sized with workspace_bytes()")
     if grads is None:
-        grads = tuple(torch.empty(t.shape, dtype=torch.float32, device=q.device) for t in (q, k, v, a))
+        grads = _grad_buffers(q, k, v, a, lowp_grads)
     dq, dk, dvv, da = grads
     ws = _workspace(L.tm2_backward_workspace(B, H, T, d, dv, chunk, dt, flags), q.device, workspace)
     nbytes = 0 if ws is None else ws.numel()
@@ -343,13 +353,13 @@ def forward_quadratic(q, k, v, a, *, order=2, normalize=True, workspace=None, st
 
 
 def backward_quadratic(q, k, v, a, o, Z, dO, *, order=2, normalize=True, workspace=None, stream=None,
-                       grads=None):
+                       grads=None, lowp_grads=False):
     """Backward of forward_quadratic.  Returns (dq, dk, dv, da)."""
     B, H, T, d, dv, dt = _seq_checks(q, k, v, a)
     L = _load()
-    flags = NORMALIZE if normalize else 0
+    flags = (NORMALIZE if normalize else 0) | (GRADS_INPUT_DTYPE if lowp_grads else 0)
     if grads is None:
-        grads = tuple(torch.empty(t.shape, dtype=torch.float32, device=q.device) for t in (q, k, v, a))
+        grads = _grad_buffers(q, k, v, a, lowp_grads)
     dq, dk, dvv, da = grads
     ws = _workspace(L.tm2q_backward_workspace(B, H, T, d, dv, order, dt, flags), q.device, workspace)
     nbytes = 0 if ws is None else ws.numel()
@@ -373,18 +383,19 @@ def e_forward(q, k, v, a, *, scale=None, workspace=None, stream=None, out=None, 
     return o, lse
 
 
-def e_backward(q, k, v, a, o, lse, dO, *, scale=None, workspace=None, stream=None, grads=None):
-    """2Mamba-E backward.  Returns (dq, dk, dv, da)."""
+def e_backward(q, k, v, a, o, lse, dO, *, scale=None, workspace=None, stream=None, grads=None, lowp_grads=False):
+    """2Mamba-E backward.  Returns (dq, dk, dv, da) (dq, dk, dv fp32, or the input dtype with lowp_grads)."""
     B, H, T, d, dv, dt = _seq_checks(q, k, v, a)
     L = _load()
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    flags = GRADS_INPUT_DTYPE if lowp_grads else 0
     if grads is None:
-        grads = tuple(torch.empty(t.shape, dtype=torch.float32, device=q.device) for t in (q, k, v, a))
+        grads = _grad_buffers(q, k, v, a, lowp_grads)
     dq, dk, dvv, da = grads
     ws = _workspace(L.tm2e_backward_workspace(B, H, T, d, dv, dt), q.device, workspace)
     nbytes = 0 if ws is None else ws.numel()
     _check(L.tm2e_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(o), _ptr(lse), _ptr(dO),
-                           _ptr(dq), _ptr(dk), _ptr(dvv), _ptr(da), B, H, T, d, dv, scale, dt,
+                           _ptr(dq), _ptr(dk), _ptr(dvv), _ptr(da), B, H, T, d, dv, scale, dt, flags,
                            _ptr(ws), nbytes, _stream(stream)))
     return dq, dk, dvv, da
 

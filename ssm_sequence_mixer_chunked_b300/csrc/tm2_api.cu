@@ -45,6 +45,7 @@ static int make_problem(int B, int H, int T, int d, int dv, int chunk, int dtype
     p.NC = (T + p.C - 1) / p.C;
     p.dtype = dtype;
     p.normalize = (flags & TM2_NORMALIZE) != 0;
+    p.lowp_grads = (flags & TM2_GRADS_INPUT_DTYPE) != 0;
     return TM2_OK;
 }
 
@@ -311,7 +312,8 @@ int tm2_forward(const void* q, const void* k, const void* v, const float* a, con
 size_t tm2_backward_workspace(int B, int H, int T, int d, int dv, int chunk, int dtype,
                               unsigned flags) {
     Problem p;
-    if (make_problem(B, H, T, d, dv, chunk, dtype, flags, p, true, TM2_REUSE_STATES) != TM2_OK) return 0;
+    if (make_problem(B, H, T, d, dv, chunk, dtype, flags, p, true, TM2_REUSE_STATES | TM2_GRADS_INPUT_DTYPE) != TM2_OK)
+        return 0;
     return plan_bwd(p).total;
 }
 
@@ -320,7 +322,7 @@ int tm2_backward(const void* q, const void* k, const void* v, const float* a, co
                  int H, int T, int d, int dv_dim, int chunk, int dtype, unsigned flags, void* ws,
                  size_t ws_bytes, void* stream) {
     Problem p;
-    int st = make_problem(B, H, T, d, dv_dim, chunk, dtype, flags, p, true, TM2_REUSE_STATES);
+    int st = make_problem(B, H, T, d, dv_dim, chunk, dtype, flags, p, true, TM2_REUSE_STATES | TM2_GRADS_INPUT_DTYPE);
     if (st != TM2_OK) return st;
     const bool reuse = (flags & TM2_REUSE_STATES) != 0;
     if (p.BH() == 0 || T == 0) return TM2_OK;
@@ -365,9 +367,9 @@ int tm2_backward(const void* q, const void* k, const void* v, const float* a, co
         r.rev = true; r.ops = ops; r.g = g; r.zmax = zmax; r.amax = amax_r;
         r.Sx = dSx; r.zx = dzx; r.sscale = sscale;
         TM2_RUN("tc_state_scan_bwd", tc_state_scan(p, r, s));
-        TM2_RUN("tc_bwd_dq", tc_bwd_dq(p, q, k, v, dO, Aloc, zeta, ucol, Sx, zx, amax_f, (float*)dq, s));
+        TM2_RUN("tc_bwd_dq", tc_bwd_dq(p, q, k, v, dO, Aloc, zeta, ucol, Sx, zx, amax_f, dq, s));
         TM2_RUN("tc_bwd_dkdv", tc_bwd_dkdv(p, q, k, v, dO, Aloc, g, zeta, ucol, rowterm, dSx, dzx, sscale, amax_r,
-                                           (float*)dk, (float*)dv, dcum, s));
+                                           dk, dv, dcum, s));
         TM2_RUN("reverse_cumsum_da", launch_reverse_cumsum_da(p, a, dcum, nullptr, da, s));
         return TM2_OK;
     }
@@ -587,10 +589,11 @@ size_t tm2e_backward_workspace(int B, int H, int T, int d, int dv, int dtype) {
 
 int tm2e_backward(const void* q, const void* k, const void* v, const float* a, const void* o,
                   const float* lse, const void* dO, void* dq, void* dk, void* dv, float* da, int B,
-                  int H, int T, int d, int dv_dim, float scale, int dtype, void* ws,
+                  int H, int T, int d, int dv_dim, float scale, int dtype, unsigned flags, void* ws,
                   size_t ws_bytes, void* stream) {
     Problem p;
-    int st = make_problem(B, H, T, d, dv_dim, 0, dtype, 0, p);
+    int st = make_problem(B, H, T, d, dv_dim, 0, dtype, flags, p, false, TM2_GRADS_INPUT_DTYPE);
+    if (flags & TM2_NORMALIZE) return TM2_ERR_INVALID_ARG;
     if (st != TM2_OK) return st;
     if (!(scale == scale) || scale == 0.f) return TM2_ERR_INVALID_ARG;
     if (p.BH() == 0 || T == 0) return TM2_OK;
@@ -614,17 +617,17 @@ int tm2e_backward(const void* q, const void* k, const void* v, const float* a, c
     TM2_RUN("global_cumsum", launch_global_cumsum(p, Aloc, g, cum, cum_lo, s));
     TM2_RUN("rowdot", launch_rowdot(p, o, dO, Dvec, s));
     if (p.dtype == TM2_BF16 && p.d == 64 && p.dv == 64)
-        TM2_RUN("tc_e_bwd", tc_e_bwd(p, q, k, v, cum, cum_lo, lse, Dvec, dO, scale, (float*)dq, (float*)dk,
-                                     (float*)dv, rowsum, colsum, s));
+        TM2_RUN("tc_e_bwd", tc_e_bwd(p, q, k, v, cum, cum_lo, lse, Dvec, dO, scale, dq, dk, dv, rowsum, colsum, s));
     else
         TM2_RUN("e_bwd", simt_e_bwd(p, q, k, v, cum, cum_lo, lse, Dvec, dO, scale, dq, dk, dv, rowsum, colsum, s));
     TM2_RUN("reverse_cumsum_da", launch_reverse_cumsum_da(p, a, rowsum, colsum, da, s));
     return TM2_OK;
 }
 
-static int make_q_problem(int B, int H, int T, int d, int dv, int order, int dtype, unsigned flags, Problem& p) {
+static int make_q_problem(int B, int H, int T, int d, int dv, int order, int dtype, unsigned flags, Problem& p,
+                          unsigned extra = 0) {
     if (order != 1 && order != 2) return TM2_ERR_UNSUPPORTED;
-    return make_problem(B, H, T, d, dv, 0, dtype, flags, p);
+    return make_problem(B, H, T, d, dv, 0, dtype, flags, p, false, extra);
 }
 
 static bool q_tc(const Problem& p) { return p.dtype == TM2_BF16 && p.d == 64 && p.dv == 64; }
@@ -666,7 +669,7 @@ int tm2q_forward(const void* q, const void* k, const void* v, const float* a, vo
 
 size_t tm2q_backward_workspace(int B, int H, int T, int d, int dv, int order, int dtype, unsigned flags) {
     Problem p{};
-    if (make_q_problem(B, H, T, d, dv, order, dtype, flags, p) != TM2_OK) return 0;
+    if (make_q_problem(B, H, T, d, dv, order, dtype, flags, p, TM2_GRADS_INPUT_DTYPE) != TM2_OK) return 0;
     return plan_q(p, true).total;
 }
 
@@ -674,7 +677,7 @@ int tm2q_backward(const void* q, const void* k, const void* v, const float* a, c
                   const void* dO, void* dq, void* dk, void* dv, float* da, int B, int H, int T, int d, int dv_dim,
                   int order, int dtype, unsigned flags, void* ws, size_t ws_bytes, void* stream) {
     Problem p{};
-    int st = make_q_problem(B, H, T, d, dv_dim, order, dtype, flags, p);
+    int st = make_q_problem(B, H, T, d, dv_dim, order, dtype, flags, p, TM2_GRADS_INPUT_DTYPE);
     if (st != TM2_OK) return st;
     if (p.BH() == 0 || T == 0) return TM2_OK;
     if (!q || !k || !v || !a || !dO || !dq || !dk || !dv || !da) return TM2_ERR_INVALID_ARG;
@@ -698,8 +701,8 @@ int tm2q_backward(const void* q, const void* k, const void* v, const float* a, c
     TM2_RUN("global_cumsum", launch_global_cumsum(p, Aloc, g, cum, cum_lo, s));
     TM2_RUN("poly_prep", launch_poly_prep(p, (const float*)o, Z, dO, D, zeta, s));
     if (q_tc(p))
-        TM2_RUN("tc_poly_bwd", tc_poly_bwd(p, order, q, k, v, cum, cum_lo, zeta, D, dO, (float*)dq, (float*)dk,
-                                           (float*)dv, rowsum, colsum, s));
+        TM2_RUN("tc_poly_bwd", tc_poly_bwd(p, order, q, k, v, cum, cum_lo, zeta, D, dO, dq, dk, dv, rowsum, colsum,
+                                           s));
     else
         TM2_RUN("poly_bwd",
                 simt_poly_bwd(p, order, q, k, v, cum, cum_lo, zeta, D, dO, dq, dk, dv, rowsum, colsum, s));

@@ -17,6 +17,13 @@ template <typename T> TM2_DEV T from_f(float x);
 template <> TM2_DEV float from_f<float>(float x) { return x; }
 template <> TM2_DEV __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 
+// element i of an output that is fp32, or of the input type T when lowp (the gradients'
+// TM2_GRADS_INPUT_DTYPE form)
+template <typename T> TM2_DEV void store_out(void* p, long i, float x, bool lowp) {
+    if (lowp) reinterpret_cast<T*>(p)[i] = from_f<T>(x);
+    else reinterpret_cast<float*>(p)[i] = x;
+}
+
 // ---- the A-mask ----------------------------------------------------------------------
 // softplus(x) = log(1 + e^x) in the overflow-free form max(x,0) + log1p(e^-|x|).
 TM2_DEV float softplus_f(float x) { return fmaxf(x, 0.f) + log1pf(__expf(-fabsf(x))); }

@@ -10,10 +10,11 @@
 // with k_t, v_t appended to the cache.
 //
 // The step reads the whole cache once, so it is bound by HBM bandwidth.  The keys 0..t of a
-// (sequence, head) are split into ranges of KPS; one 256-thread block per (range, head) walks
-// its range with groups of D / 8 lanes per key (each lane 8 elements, 16 bytes of bf16), two
-// keys per group in flight, an online maximum per group, and combines its groups in shared
-// memory.  With one range the block writes o and lse itself; otherwise each block writes its
+// (sequence, head) are split into ranges of KPS; one block per (range, head): a producer warp
+// streams the range's key and value rows into shared memory with bulk copies (stages of 64
+// keys, four in flight, so the loads in flight do not depend on registers), and four consumer
+// warps walk each stage with groups of D / 8 lanes per key (each lane 8 elements), an online
+// maximum per group, and combine their groups in shared memory.  With one range the block writes o and lse itself; otherwise each block writes its
 // (max, sum, weighted values) and a second kernel combines the ranges.  The block whose range
 // holds t takes k_t, v_t from the inputs and writes them, and cumA_t, into the cache; every
 // block computes cumA_t the same way (fp64 sum of the cached hi + lo and -softplus(a_t)).
@@ -21,10 +22,14 @@
 
 #include "tm2_common.cuh"
 #include "tm2_launch.h"
+#include "tm2_sm100.cuh"
+#include "tm2_tc.h"
 
 namespace tm2 {
 
-constexpr int E_DEC_KPS = 512;   // keys per range
+constexpr int E_DEC_KPS = 512;   // keys per range (one block)
+constexpr int E_DEC_STAGE = 64;  // keys per bulk-copy stage
+constexpr int E_DEC_NST = 4;     // stages in flight
 
 TM2_DEV void load8(const float* p, float* x) {
     const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
@@ -41,99 +46,147 @@ TM2_DEV void load8(const __nv_bfloat16* p, float* x) {
 }
 
 template <int D, int DV, typename Tin>
-__global__ void __launch_bounds__(256) e_decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
+__global__ void __launch_bounds__(160) e_decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
                                                        const Tin* __restrict__ v, const float* __restrict__ a,
                                                        Tin* __restrict__ Kc, Tin* __restrict__ Vc,
                                                        float* __restrict__ cumc, int pos, int L, float scale,
                                                        float* __restrict__ part, float* __restrict__ o,
-                                                       float* __restrict__ lse) {
+                                                       float* __restrict__ lse, int* status) {
     static_assert(D == DV, "one group of lanes covers a key row and a value row");
-    constexpr int G = D / 8;              // lanes per key
-    constexpr int NGRP = 256 / G;         // key groups per block
+    constexpr int G = D / 8;                  // lanes per key
+    constexpr int NG = 128 / G;               // key groups of the four consumer warps
+    constexpr int RB = D * (int)sizeof(Tin);  // bytes per cached row
+    constexpr int SB = E_DEC_STAGE * RB;      // bytes of one stage's keys (and of its values)
     constexpr float LOG2E = 1.4426950408889634f, LN2 = 0.6931471805599453f;
-    __shared__ float sm[NGRP], sl[NGRP];
-    __shared__ float sacc[NGRP][DV + 1];
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_align1024(smem_raw);   // [E_DEC_NST][K rows | V rows]
+    __shared__ __align__(8) uint64_t bar_full[E_DEC_NST], bar_empty[E_DEC_NST];
+    __shared__ float sm[NG], sl[NG];
+    __shared__ float sacc[NG][DV + 1];
     const long s = blockIdx.y;
     const int sp = blockIdx.x, nsplit = gridDim.x;
-    const int tid = threadIdx.x, grp = tid / G, gl = tid % G;
+    const int tid = threadIdx.x, warp = tid >> 5;
     const int j0 = sp * E_DEC_KPS, j1 = min(j0 + E_DEC_KPS, pos + 1);
+    const int nst = (j1 - j0 + E_DEC_STAGE - 1) / E_DEC_STAGE;
+    const uint32_t sbase = smem_u32(smem);
+    if (tid == 0) {
+        for (int i = 0; i < E_DEC_NST; ++i) {
+            mbar_init(smem_u32(&bar_full[i]), 1);
+            mbar_init(smem_u32(&bar_empty[i]), 4);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
     // the new token's running sum, the same in every block
     double cprev = 0.0;
     if (pos > 0) cprev = (double)cumc[(s * L + pos - 1) * 2] + (double)cumc[(s * L + pos - 1) * 2 + 1];
     const double cnew = cprev - (double)softplus_f(a[s]);
     const float cq_hi = (float)cnew, cq_lo = (float)(cnew - (double)cq_hi);
-    if (sp == nsplit - 1) {   // this block's range holds pos: append the token to the cache
-        if (tid < D) Kc[(s * L + pos) * D + tid] = k[s * D + tid];
-        if (tid < DV) Vc[(s * L + pos) * DV + tid] = v[s * DV + tid];
-        if (tid == 0) {
-            cumc[(s * L + pos) * 2] = cq_hi;
-            cumc[(s * L + pos) * 2 + 1] = cq_lo;
-        }
-    }
-    float qv[8];
-    load8(q + s * D + 8 * gl, qv);
-    const float sl2 = scale * LOG2E;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) qv[i] *= sl2;
-    float m = -INFINITY, lsum = 0.f, acc[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-    // the trip count is the same for the whole block, so every lane reaches the shuffles
-    for (int jb = j0; jb < j1; jb += 2 * NGRP) {
-        float kx[2][8], vx[2][8], cr[2][2];
-        bool in[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int j = jb + u * NGRP + grp;
-            in[u] = j < j1;
-            if (!in[u]) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) kx[u][i] = vx[u][i] = 0.f;
-                cr[u][0] = cr[u][1] = 0.f;
-                continue;
+
+    if (warp == 4) {
+        // ---------------------------------------------------------------- producer: the range's
+        // rows in stages of E_DEC_STAGE keys through an E_DEC_NST-slot ring (the row at pos is read
+        // from the inputs by the consumers, and written to the cache here once its stage is issued)
+        if ((tid & 31) == 0) {
+            int issued = 0;
+            for (int i = 0; i < nst; ++i) {
+                const int sl = i % E_DEC_NST;
+                if (i >= E_DEC_NST && !mbar_wait(smem_u32(&bar_empty[sl]), (uint32_t)((i / E_DEC_NST) - 1) & 1, status))
+                    break;
+                const int js = j0 + i * E_DEC_STAGE, cnt = min(E_DEC_STAGE, j1 - js);
+                const uint32_t fb = smem_u32(&bar_full[sl]), dst = sbase + sl * 2 * SB;
+                mbar_arrive_expect_tx(fb, 2 * cnt * RB);
+                bulk_load(dst, Kc + (s * L + js) * D, cnt * RB, fb);
+                bulk_load(dst + SB, Vc + (s * L + js) * DV, cnt * RB, fb);
+                issued = i + 1;
             }
-            if (j == pos) {
-                load8(k + s * D + 8 * gl, kx[u]);
-                load8(v + s * DV + 8 * gl, vx[u]);
-                cr[u][0] = cq_hi;
-                cr[u][1] = cq_lo;
-            } else {
-                load8(Kc + (s * L + j) * D + 8 * gl, kx[u]);
-                load8(Vc + (s * L + j) * DV + 8 * gl, vx[u]);
-                const float2 c2 = *reinterpret_cast<const float2*>(cumc + (s * L + j) * 2);
-                cr[u][0] = c2.x;
-                cr[u][1] = c2.y;
+            for (int i = issued - 1; i >= 0 && i >= issued - E_DEC_NST; --i)   // no copy in flight at exit
+                mbar_wait(smem_u32(&bar_full[i % E_DEC_NST]), (uint32_t)(i / E_DEC_NST) & 1, status);
+        }
+        __syncwarp();   // the row at pos is written once every copy of the range has landed
+        if (sp == nsplit - 1) {   // this block's range holds pos: append the token to the cache
+            const int t = tid - 128;
+            for (int e = t; e < D; e += 32) Kc[(s * L + pos) * D + e] = k[s * D + e];
+            for (int e = t; e < DV; e += 32) Vc[(s * L + pos) * DV + e] = v[s * DV + e];
+            if (t == 0) {
+                cumc[(s * L + pos) * 2] = cq_hi;
+                cumc[(s * L + pos) * 2 + 1] = cq_lo;
             }
         }
+    } else {
+        // ---------------------------------------------------------------- consumers
+        const int grp = tid / G, gl = tid % G;
+        float qv[8];
+        load8(q + s * D + 8 * gl, qv);
+        const float sl2 = scale * LOG2E;
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            float x = 0.f;
+        for (int i = 0; i < 8; ++i) qv[i] *= sl2;
+        float m = -INFINITY, lsum = 0.f, acc[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) x = fmaf(qv[i], kx[u][i], x);
+        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+        constexpr int KPG = E_DEC_STAGE / NG;   // keys of a stage per group
+        for (int i = 0; i < nst; ++i) {
+            const int sl = i % E_DEC_NST;
+            const int js = j0 + i * E_DEC_STAGE, cnt = min(E_DEC_STAGE, j1 - js);
+            // this group's running sums of the stage, loaded before the wait so that their latency
+            // overlaps the stage's bulk copy
+            float2 cr[KPG];
 #pragma unroll
-            for (int o2 = G / 2; o2 > 0; o2 >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o2, G);
-            if (!in[u]) continue;
-            x += ((cq_hi - cr[u][0]) + (cq_lo - cr[u][1])) * LOG2E;
-            const float mn = fmaxf(m, x);
-            const float al = exp2f(m - mn), p = exp2f(x - mn);
-            lsum = lsum * al + p;
+            for (int u = 0; u < KPG; ++u) {
+                const int r = u * NG + grp, j = js + r;
+                cr[u] = (r < cnt && j != pos) ? *reinterpret_cast<const float2*>(cumc + (s * L + j) * 2)
+                                              : make_float2(cq_hi, cq_lo);
+            }
+            if (!mbar_wait(smem_u32(&bar_full[sl]), (uint32_t)(i / E_DEC_NST) & 1, status)) break;
+            const Tin* ks = reinterpret_cast<const Tin*>(smem + sl * 2 * SB);
+            const Tin* vs = reinterpret_cast<const Tin*>(smem + sl * 2 * SB + SB);
+            // the trip count is the same for every group, so all lanes reach the shuffles
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = fmaf(acc[i], al, p * vx[u][i]);
-            m = mn;
+            for (int u = 0; u < KPG; ++u) {
+                const int r = u * NG + grp, j = js + r;
+                const bool in = r < cnt;
+                float kx[8], vx[8];
+                const float c0 = cr[u].x, c1 = cr[u].y;
+                if (in && j == pos) {
+                    load8(k + s * D + 8 * gl, kx);
+                    load8(v + s * DV + 8 * gl, vx);
+                } else if (in) {
+                    load8(ks + r * D + 8 * gl, kx);
+                    load8(vs + r * DV + 8 * gl, vx);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) kx[e] = vx[e] = 0.f;
+                }
+                float x = 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x = fmaf(qv[e], kx[e], x);
+#pragma unroll
+                for (int o2 = G / 2; o2 > 0; o2 >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o2, G);
+                if (!in) continue;
+                x += ((cq_hi - c0) + (cq_lo - c1)) * LOG2E;
+                const float mn = fmaxf(m, x);
+                const float al = exp2f(m - mn), p = exp2f(x - mn);
+                lsum = lsum * al + p;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[e] = fmaf(acc[e], al, p * vx[e]);
+                m = mn;
+            }
+            __syncwarp();
+            if ((tid & 31) == 0) mbar_arrive(smem_u32(&bar_empty[sl]));
         }
-    }
-    if (gl == 0) {
-        sm[grp] = m;
-        sl[grp] = lsum;
-    }
+        if (gl == 0) {
+            sm[grp] = m;
+            sl[grp] = lsum;
+        }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) sacc[grp][8 * gl + i] = acc[i];
+        for (int i = 0; i < 8; ++i) sacc[grp][8 * gl + i] = acc[i];
+    }
     __syncthreads();
     if (tid < DV) {
         float M = -INFINITY;
-        for (int g = 0; g < NGRP; ++g) M = fmaxf(M, sm[g]);
+        for (int g = 0; g < NG; ++g) M = fmaxf(M, sm[g]);
         float Ls = 0.f, A = 0.f;
-        for (int g = 0; g < NGRP; ++g) {
+        for (int g = 0; g < NG; ++g) {
             if (sm[g] == -INFINITY) continue;
             const float f = exp2f(sm[g] - M);
             Ls = fmaf(sl[g], f, Ls);
@@ -182,9 +235,14 @@ static cudaError_t e_decode_run(long NH, int pos, int L, float scale, const void
                                 cudaStream_t s) {
     const int ns = e_decode_splits(pos);
     dim3 grid((unsigned)ns, (unsigned)NH);
-    e_decode_kernel<D, D, Tin><<<grid, 256, 0, s>>>((const Tin*)q, (const Tin*)k, (const Tin*)v, a, (Tin*)Kc,
-                                                    (Tin*)Vc, cumc, pos, L, scale, part, o, lse);
-    cudaError_t e = cudaGetLastError();
+    int* status = tc_status_ptr();
+    if (!status) return cudaErrorInvalidValue;
+    const int smem = E_DEC_NST * 2 * E_DEC_STAGE * D * (int)sizeof(Tin) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(e_decode_kernel<D, D, Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    e_decode_kernel<D, D, Tin><<<grid, 160, smem, s>>>((const Tin*)q, (const Tin*)k, (const Tin*)v, a, (Tin*)Kc,
+                                                       (Tin*)Vc, cumc, pos, L, scale, part, o, lse, status);
+    e = cudaGetLastError();
     if (e != cudaSuccess || ns == 1) return e;
     e_decode_combine_kernel<D><<<(unsigned)NH, D, 0, s>>>(part, ns, o, lse);
     return cudaGetLastError();

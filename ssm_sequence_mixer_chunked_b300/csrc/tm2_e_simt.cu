@@ -161,8 +161,8 @@ template <int KIND, int D, int DV, typename Tin>
 __global__ void __launch_bounds__(256) e_bwd_dkdv_kernel(
     const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
     const float* __restrict__ cum, const float* __restrict__ cum_lo, const float* __restrict__ lse,
-    const float* __restrict__ Dvec, const Tin* __restrict__ dO, float scale, float* __restrict__ dk, float* __restrict__ dvo,
-    float* __restrict__ colsum, int T, int NQB) {
+    const float* __restrict__ Dvec, const Tin* __restrict__ dO, float scale, void* __restrict__ dk, void* __restrict__ dvo,
+    float* __restrict__ colsum, int T, int NQB, bool lowp) {
     constexpr int LDQ = D + 1, LDV = DV + 1, LDP = EB + 1, NCOL = DV / 16, NN = D / 16;
     extern __shared__ float sm[];
     float* sk = sm;                 // [EB][LDQ]
@@ -280,9 +280,9 @@ __global__ void __launch_bounds__(256) e_bwd_dkdv_kernel(
         const long t = (long)kb * EB + ti + 16 * r;
         if (t >= T) continue;
 #pragma unroll
-        for (int s = 0; s < NN; ++s) dk[(bh * T + t) * D + tc + 16 * s] = scale * adk[r][s];
+        for (int s = 0; s < NN; ++s) store_out<Tin>(dk, (bh * T + t) * D + tc + 16 * s, scale * adk[r][s], lowp);
 #pragma unroll
-        for (int s = 0; s < NCOL; ++s) dvo[(bh * T + t) * DV + tc + 16 * s] = adv[r][s];
+        for (int s = 0; s < NCOL; ++s) store_out<Tin>(dvo, (bh * T + t) * DV + tc + 16 * s, adv[r][s], lowp);
         if (tc == 0) colsum[bh * T + t] = cs[r];
     }
 }
@@ -292,7 +292,8 @@ template <int KIND, int D, int DV, typename Tin>
 __global__ void __launch_bounds__(256) e_bwd_dq_kernel(
     const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
     const float* __restrict__ cum, const float* __restrict__ cum_lo, const float* __restrict__ lse,
-    const float* __restrict__ Dvec, const Tin* __restrict__ dO, float scale, float* __restrict__ dq, float* __restrict__ rowsum, int T) {
+    const float* __restrict__ Dvec, const Tin* __restrict__ dO, float scale, void* __restrict__ dq, float* __restrict__ rowsum, int T,
+    bool lowp) {
     constexpr int LDQ = D + 1, LDV = DV + 1, LDP = EB + 1, NN = D / 16;
     extern __shared__ float sm[];
     float* sq = sm;                 // [EB][LDQ]
@@ -400,7 +401,7 @@ __global__ void __launch_bounds__(256) e_bwd_dq_kernel(
         const long t = (long)qb * EB + ti + 16 * r;
         if (t >= T) continue;
 #pragma unroll
-        for (int s = 0; s < NN; ++s) dq[(bh * T + t) * D + tc + 16 * s] = scale * adq[r][s];
+        for (int s = 0; s < NN; ++s) store_out<Tin>(dq, (bh * T + t) * D + tc + 16 * s, scale * adq[r][s], lowp);
         if (tc == 0) rowsum[bh * T + t] = x;
     }
 }
@@ -433,7 +434,7 @@ static cudaError_t run_e_bwd(const Problem& p, const void* q, const void* k, con
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         kern<<<grid, 256, smem, s>>>((const Tin*)q, (const Tin*)k, (const Tin*)v, cum, cum_lo, lse, Dvec,
-                                     (const Tin*)dO, scale, (float*)dk, (float*)dv, colsum, p.T, NQB);
+                                     (const Tin*)dO, scale, dk, dv, colsum, p.T, NQB, p.lowp_grads);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -444,7 +445,7 @@ static cudaError_t run_e_bwd(const Problem& p, const void* q, const void* k, con
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         kern<<<grid, 256, smem, s>>>((const Tin*)q, (const Tin*)k, (const Tin*)v, cum, cum_lo, lse, Dvec,
-                                     (const Tin*)dO, scale, (float*)dq, rowsum, p.T);
+                                     (const Tin*)dO, scale, dq, rowsum, p.T, p.lowp_grads);
     }
     return cudaGetLastError();
 }

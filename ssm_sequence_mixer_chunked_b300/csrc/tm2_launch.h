@@ -13,6 +13,7 @@ struct Problem {
     int dtype;               // 0 fp32, 1 bf16
     bool normalize;
     bool tc;                 // bf16 tensor-core path (d = dv = 64, C = TC_CHUNK)
+    bool lowp_grads = false; // backward: dq, dk, dv in the input type (else fp32)
     long BH() const { return (long)B * H; }
     long Tp() const { return (long)NC * C; }   // padded sequence stride of chunk-local buffers
 };
@@ -99,15 +100,15 @@ cudaError_t launch_tc_dy_prep(const Problem& p, const float* o, const float* Z, 
                               float* zeta, float* ucol, float* rowterm, float* zmax, unsigned* amax, cudaStream_t s);
 
 // Gradient kernels (tm2_tc_dq.cu, tm2_tc_dkdv.cu).  dq: Sx/zx are the forward scan's states
-// (amax_f its operand maxima); dk, dv, dcum: dSx/dzx/sscale the reverse scan's (amax_r).  All
-// outputs (BH,T,·) fp32.
+// (amax_f its operand maxima); dk, dv, dcum: dSx/dzx/sscale the reverse scan's (amax_r).  dq, dk,
+// dv (BH,T,64) fp32, or bf16 with p.lowp_grads; dcum fp32.
 cudaError_t tc_bwd_dq(const Problem& p, const void* q, const void* k, const void* v, const void* dO, const float* Aloc,
                       const float* zeta, const float* ucol, const void* Sx, const float* zx, const unsigned* amax_f,
-                      float* dq, cudaStream_t s);
+                      void* dq, cudaStream_t s);
 cudaError_t tc_bwd_dkdv(const Problem& p, const void* q, const void* k, const void* v, const void* dO,
                         const float* Aloc, const float* g, const float* zeta, const float* ucol, const float* rowterm,
-                        const void* dSx, const float* dzx, const float* sscale, const unsigned* amax_r, float* dk,
-                        float* dv, float* dcum, cudaStream_t s);
+                        const void* dSx, const float* dzx, const float* sscale, const unsigned* amax_r, void* dk,
+                        void* dv, float* dcum, cudaStream_t s);
 
 // Per-chunk output (intra-chunk squared masked scores and the readout of the state
 // entering the chunk, slot c of Sx/zx from tc_state_scan, whose operand maxima are amax):
@@ -150,8 +151,8 @@ cudaError_t simt_poly_fwd(const Problem& p, int order, const void* q, const void
 cudaError_t launch_poly_prep(const Problem& p, const float* o, const float* Z, const void* dO, float* D,
                              float* zeta, cudaStream_t s);
 cudaError_t tc_poly_bwd(const Problem& p, int order, const void* q, const void* k, const void* v, const float* cum,
-                        const float* cum_lo, const float* zeta, const float* D, const void* dO, float* dq, float* dk,
-                        float* dv, float* rowsum, float* colsum, cudaStream_t s);
+                        const float* cum_lo, const float* zeta, const float* D, const void* dO, void* dq, void* dk,
+                        void* dv, float* rowsum, float* colsum, cudaStream_t s);
 cudaError_t simt_poly_bwd(const Problem& p, int order, const void* q, const void* k, const void* v,
                           const float* cum, const float* cum_lo, const float* zeta, const float* D, const void* dO,
                           void* dq, void* dk, void* dv, float* rowsum, float* colsum, cudaStream_t s);
@@ -197,11 +198,12 @@ cudaError_t simt_e_fwd(const Problem& p, const void* q, const void* k, const voi
 // Dvec[bh][t] = dO_t . o_t
 cudaError_t launch_rowdot(const Problem& p, const void* o, const void* dO, float* Dvec,
                           cudaStream_t s);
-// 2Mamba-E backward on the tensor cores (tm2_tc_e_bwd.cu): bf16, d = dv = 64; dq, dk, dv fp32;
+// 2Mamba-E backward on the tensor cores (tm2_tc_e_bwd.cu): bf16, d = dv = 64; dq, dk, dv fp32 (bf16
+// with p.lowp_grads);
 // rowsum[t] = sum_j dx_tj and colsum[t] = sum_i dx_it (the A-mask gradient's two halves).
 cudaError_t tc_e_bwd(const Problem& p, const void* q, const void* k, const void* v, const float* cum,
-                     const float* cum_lo, const float* lse, const float* Dvec, const void* dO, float scale, float* dq,
-                     float* dk, float* dv, float* rowsum, float* colsum, cudaStream_t s);
+                     const float* cum_lo, const float* lse, const float* Dvec, const void* dO, float scale, void* dq,
+                     void* dk, void* dv, float* rowsum, float* colsum, cudaStream_t s);
 cudaError_t simt_e_bwd(const Problem& p, const void* q, const void* k, const void* v,
                        const float* cum, const float* cum_lo, const float* lse, const float* Dvec, const void* dO,
                        float scale, void* dq, void* dk, void* dv, float* rowsum, float* colsum,

@@ -295,8 +295,8 @@ __global__ void __launch_bounds__(256) bwd_chunk_kernel(
     const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
     const float* __restrict__ Aloc, const float* __restrict__ g, const float* __restrict__ dY,
     const float* __restrict__ rowterm, const float* __restrict__ states,
-    const float* __restrict__ dstates, float* __restrict__ dq, float* __restrict__ dk,
-    float* __restrict__ dvo, float* __restrict__ dcum, int T, int NC) {
+    const float* __restrict__ dstates, void* __restrict__ dq, void* __restrict__ dk,
+    void* __restrict__ dvo, float* __restrict__ dcum, int T, int NC, bool lowp) {
     constexpr int C = SIMT_C, DV1 = DV + 1, NCOL = DV / 16, NN = D / 16;
     constexpr int LDQ = D + 1, LDV = DV1 + 1, LDW = C + 1;
     extern __shared__ float sm[];
@@ -472,11 +472,11 @@ __global__ void __launch_bounds__(256) bwd_chunk_kernel(
 #pragma unroll
         for (int s2 = 0; s2 < NN; ++s2) {
             const int n = tc + 16 * s2;
-            dq[(bh * T + t) * D + n] = aq[r][s2] + sdqi[i * LDQ + n];
-            dk[(bh * T + t) * D + n] = ak[r][s2] + sdki[i * LDQ + n];
+            store_out<Tin>(dq, (bh * T + t) * D + n, aq[r][s2] + sdqi[i * LDQ + n], lowp);
+            store_out<Tin>(dk, (bh * T + t) * D + n, ak[r][s2] + sdki[i * LDQ + n], lowp);
         }
 #pragma unroll
-        for (int s2 = 0; s2 < NCOL; ++s2) dvo[(bh * T + t) * DV + tc + 16 * s2] = av[r][s2];
+        for (int s2 = 0; s2 < NCOL; ++s2) store_out<Tin>(dvo, (bh * T + t) * DV + tc + 16 * s2, av[r][s2], lowp);
         if (tc == 0) dcum[bh * T + t] = rowterm[bh * T + t] - vd;
     }
 }
@@ -494,7 +494,7 @@ static cudaError_t run_bwd_chunk(const Problem& p, const void* q, const void* k,
     if (e != cudaSuccess) return e;
     dim3 grid(p.NC, (unsigned)p.BH());
     kern<<<grid, 256, smem, s>>>((const Tin*)q, (const Tin*)k, (const Tin*)v, Aloc, g, dY, rowterm,
-                                 states, dstates, (float*)dq, (float*)dk, (float*)dv, dcum, p.T, p.NC);
+                                 states, dstates, dq, dk, dv, dcum, p.T, p.NC, p.lowp_grads);
     return cudaGetLastError();
 }
 

@@ -138,6 +138,13 @@ TM2_DEV void tma_load_5d(uint32_t dst, const void* tmap, uint32_t bar, int x, in
         "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w), "r"(v)
         : "memory");
 }
+// Untiled bulk copy global -> shared (both addresses 16-byte aligned, bytes a multiple of 16),
+// completing `bytes` of transaction count on the mbarrier.
+TM2_DEV void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
 TM2_DEV void prefetch_tmap(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
@@ -265,6 +272,25 @@ TM2_DEV uint32_t pack_f16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.f16x2.f32 %0, %2, %1;" : "=r"(r) : "f"(lo), "f"(hi));
     return r;
+}
+// 32 fp32 values -> 32 bf16 (round to nearest) at a 64-byte aligned address, four 16-byte stores.
+TM2_DEV void store_bf16x32(__nv_bfloat16* dst, const float* v) {
+    uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        d[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                          pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+}
+// 32 consecutive results of one row at element offset `off` of an output that is fp32, or bf16
+// when `lowp` (the gradients' TM2_GRADS_INPUT_DTYPE form); 64-byte aligned in both cases.
+TM2_DEV void store_row32(void* base, long off, const float* v, bool lowp) {
+    if (lowp) {
+        store_bf16x32(reinterpret_cast<__nv_bfloat16*>(base) + off, v);
+    } else {
+        float4* d = reinterpret_cast<float4*>(reinterpret_cast<float*>(base) + off);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) d[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    }
 }
 // Two bf16 values (one 32-bit word) -> two fp16 values (exact inside the fp16 range).
 TM2_DEV uint32_t bf16x2_to_f16x2(uint32_t x) {

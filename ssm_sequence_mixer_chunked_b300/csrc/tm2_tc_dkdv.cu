@@ -74,9 +74,10 @@ struct Args {
     const float* dzx;     // [BH][NC][4096] gradient normaliser states (unscaled)
     const float* sscale;  // [BH][NC] scale of the gradient state planes
     const unsigned* amax; // [BH][4] the reverse scan's operand maxima (key, value, normaliser)
-    float* dk;            // [BH][T][64]
-    float* dv;            // [BH][T][64]
+    void* dk;             // [BH][T][64] fp32, or bf16 with lowp
+    void* dv;             // [BH][T][64] fp32, or bf16 with lowp
     float* dcum;          // [BH][T]
+    int lowp;
     int* status;
     int T, NC, Tp;
 };
@@ -436,13 +437,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
             mbar_arrive(smem_u32(&bar_red));
             ok = mbar_wait(smem_u32(&bar_red), 0, a.status);
             if (in) {
-                float4* dkp = reinterpret_cast<float4*>(a.dk + (bh * a.T + tok) * 64 + h * 32);
-                float4* dvp = reinterpret_cast<float4*>(a.dv + (bh * a.T + tok) * 64 + h * 32);
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    dkp[u] = make_float4(dk0[4 * u], dk0[4 * u + 1], dk0[4 * u + 2], dk0[4 * u + 3]);
-                    dvp[u] = make_float4(dv0[4 * u], dv0[4 * u + 1], dv0[4 * u + 2], dv0[4 * u + 3]);
-                }
+                store_row32(a.dk, (bh * a.T + tok) * 64 + h * 32, dk0, a.lowp != 0);
+                store_row32(a.dv, (bh * a.T + tok) * 64 + h * 32, dv0, a.lowp != 0);
                 if (h == 0 && ok) a.dcum[bh * a.T + tok] = rowt - (part + sRed[l]);
             }
         }
@@ -455,8 +451,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
 
 cudaError_t tc_bwd_dkdv(const Problem& p, const void* q, const void* k, const void* v, const void* dO,
                         const float* Aloc, const float* g, const float* zeta, const float* ucol, const float* rowterm,
-                        const void* dSx, const float* dzx, const float* sscale, const unsigned* amax_r, float* dk,
-                        float* dv, float* dcum, cudaStream_t s) {
+                        const void* dSx, const float* dzx, const float* sscale, const unsigned* amax_r, void* dk,
+                        void* dv, float* dcum, cudaStream_t s) {
     CUtensorMap tk, tv, tq, td, ts;
     const uint64_t BH = (uint64_t)p.BH(), T = (uint64_t)p.T;
     if (!make_tmap_bf16_3d(&tk, k, BH, T, 64, 128) || !make_tmap_bf16_3d(&tv, v, BH, T, 64, 128) ||
@@ -465,7 +461,8 @@ cudaError_t tc_bwd_dkdv(const Problem& p, const void* q, const void* k, const vo
         return cudaErrorInvalidValue;
     int* status = tc_status_ptr();
     if (!status) return cudaErrorInvalidValue;
-    Args a{Aloc, g, zeta, ucol, rowterm, dzx, sscale, amax_r, dk, dv, dcum, status, p.T, p.NC, (int)p.Tp()};
+    Args a{Aloc, g, zeta, ucol, rowterm, dzx, sscale, amax_r, dk, dv, dcum, p.lowp_grads ? 1 : 0, status, p.T, p.NC,
+           (int)p.Tp()};
     cudaError_t e = cudaFuncSetAttribute(tc_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, BYTES);
     if (e != cudaSuccess) return e;
     dim3 grid(2 * p.NC, (unsigned)p.BH());

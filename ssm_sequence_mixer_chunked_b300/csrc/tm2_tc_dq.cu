@@ -66,7 +66,8 @@ struct Args {
     const float* ucol;   // [BH][T]
     const float* zx;     // [BH][NC][4096] forward normaliser states (slot c = entering chunk c)
     const unsigned* amax;   // [BH][4] the forward scan's operand maxima (key, value)
-    float* dq;           // [BH][T][64]
+    void* dq;            // [BH][T][64] fp32, or bf16 with lowp
+    int lowp;
     int* status;
     int T, NC, Tp;
 };
@@ -362,11 +363,10 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_cons
                 const float f = 2.f * __expf(Ai);
 #pragma unroll
                 for (int k = 0; k < 32; ++k) dqx[k] *= un;
-                float4* dst = reinterpret_cast<float4*>(a.dq + (bh * a.T + tok) * 64 + h * 32);
+                float g[32];
 #pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    dst[u] = make_float4(ze * (d0[4 * u] + f * dqx[4 * u]), ze * (d0[4 * u + 1] + f * dqx[4 * u + 1]),
-                                         ze * (d0[4 * u + 2] + f * dqx[4 * u + 2]), ze * (d0[4 * u + 3] + f * dqx[4 * u + 3]));
+                for (int k = 0; k < 32; ++k) g[k] = ze * (d0[k] + f * dqx[k]);
+                store_row32(a.dq, (bh * a.T + tok) * 64 + h * 32, g, a.lowp != 0);
             }
         }
         if (!ok) abort_s = 1;
@@ -378,7 +378,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_cons
 
 cudaError_t tc_bwd_dq(const Problem& p, const void* q, const void* k, const void* v, const void* dO, const float* Aloc,
                       const float* zeta, const float* ucol, const void* Sx, const float* zx, const unsigned* amax_f,
-                      float* dq, cudaStream_t s) {
+                      void* dq, cudaStream_t s) {
     CUtensorMap tq, td, tk, tv, ts;
     const uint64_t BH = (uint64_t)p.BH(), T = (uint64_t)p.T;
     if (!make_tmap_bf16_3d(&tq, q, BH, T, 64, 128) || !make_tmap_bf16_3d(&td, dO, BH, T, 64, 128) ||
@@ -387,7 +387,7 @@ cudaError_t tc_bwd_dq(const Problem& p, const void* q, const void* k, const void
         return cudaErrorInvalidValue;
     int* status = tc_status_ptr();
     if (!status) return cudaErrorInvalidValue;
-    Args a{Aloc, zeta, ucol, zx, amax_f, dq, status, p.T, p.NC, (int)p.Tp()};
+    Args a{Aloc, zeta, ucol, zx, amax_f, dq, p.lowp_grads ? 1 : 0, status, p.T, p.NC, (int)p.Tp()};
     cudaError_t e = cudaFuncSetAttribute(tc_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, BYTES);
     if (e != cudaSuccess) return e;
     dim3 grid(2 * p.NC, (unsigned)p.BH());

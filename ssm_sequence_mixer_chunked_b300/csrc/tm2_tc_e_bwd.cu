@@ -68,9 +68,10 @@ struct Args {
     const float* cum_lo;   // [BH][T] their rounding residuals
     const float* lse;      // [BH][T]: lse (ATTN_E) or zeta (ATTN_P1, ATTN_P2)
     const float* Dv;       // [BH][T] dO . o (null: 0)
-    float* g1;             // dk kernel: dk [BH][T][64]; dq kernel: dq
-    float* g2;             // dk kernel: dv [BH][T][64]; dq kernel: unused
+    void* g1;              // dk kernel: dk [BH][T][64]; dq kernel: dq (fp32, or bf16 with lowp)
+    void* g2;              // dk kernel: dv [BH][T][64]; dq kernel: unused
     float* sums;           // dk kernel: column sums [BH][T]; dq kernel: row sums
+    int lowp;
     int* status;
     int T, NT, BH;
     float scale;
@@ -377,19 +378,15 @@ __global__ void __launch_bounds__(THREADS, 1) tc_attn_bwd_kernel(const __grid_co
             float g[32];
             tmem_ld32(tmem + lane_base + TM_ACC + h * 32, g);
             if (rin) {
-                float4* d1 = reinterpret_cast<float4*>(a.g1 + (base + r) * 64 + h * 32);
 #pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    d1[u] = make_float4(a.scale * g[4 * u], a.scale * g[4 * u + 1], a.scale * g[4 * u + 2],
-                                        a.scale * g[4 * u + 3]);
+                for (int u = 0; u < 32; ++u) g[u] *= a.scale;
+                store_row32(a.g1, (base + r) * 64 + h * 32, g, a.lowp != 0);
                 if (h == 0) a.sums[base + r] = tot;
             }
             if (kd) {
                 tmem_ld32(tmem + lane_base + TM_ACC2 + h * 32, g);
                 if (rin) {
-                    float4* d2 = reinterpret_cast<float4*>(a.g2 + (base + r) * 64 + h * 32);
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) d2[u] = make_float4(g[4 * u], g[4 * u + 1], g[4 * u + 2], g[4 * u + 3]);
+                    store_row32(a.g2, (base + r) * 64 + h * 32, g, a.lowp != 0);
                 }
             }
         }
@@ -403,7 +400,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_attn_bwd_kernel(const __grid_co
 template <int KIND>
 static cudaError_t launch_attn_bwd(const Problem& p, const void* q, const void* k, const void* v, const float* cum,
                                    const float* cum_lo, const float* lse_or_zeta, const float* Dvec, const void* dO,
-                                   float scale, float* dq, float* dk, float* dv, float* rowsum, float* colsum,
+                                   float scale, void* dq, void* dk, void* dv, float* rowsum, float* colsum,
                                    cudaStream_t s) {
     CUtensorMap tq, tk, tv, td;
     const uint64_t BH = (uint64_t)p.BH(), T = (uint64_t)p.T;
@@ -415,7 +412,8 @@ static cudaError_t launch_attn_bwd(const Problem& p, const void* q, const void* 
     const int NT = (p.T + BT - 1) / BT;
     dim3 grid((unsigned)NT, (unsigned)p.BH());
     {
-        Args a{cum, cum_lo, lse_or_zeta, Dvec, dk, dv, colsum, status, p.T, NT, (int)p.BH(), scale};
+        Args a{cum, cum_lo, lse_or_zeta, Dvec, dk, dv, colsum, p.lowp_grads ? 1 : 0, status, p.T, NT, (int)p.BH(),
+               scale};
         cudaError_t e = cudaFuncSetAttribute(tc_attn_bwd_kernel<KIND, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              SMEM_BYTES);
         if (e != cudaSuccess) return e;
@@ -424,7 +422,8 @@ static cudaError_t launch_attn_bwd(const Problem& p, const void* q, const void* 
         if (e != cudaSuccess) return e;
     }
     {
-        Args a{cum, cum_lo, lse_or_zeta, Dvec, dq, nullptr, rowsum, status, p.T, NT, (int)p.BH(), scale};
+        Args a{cum, cum_lo, lse_or_zeta, Dvec, dq, nullptr, rowsum, p.lowp_grads ? 1 : 0, status, p.T, NT, (int)p.BH(),
+               scale};
         cudaError_t e = cudaFuncSetAttribute(tc_attn_bwd_kernel<KIND, false>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess) return e;
@@ -434,14 +433,14 @@ static cudaError_t launch_attn_bwd(const Problem& p, const void* q, const void* 
 }
 
 cudaError_t tc_e_bwd(const Problem& p, const void* q, const void* k, const void* v, const float* cum,
-                     const float* cum_lo, const float* lse, const float* Dvec, const void* dO, float scale, float* dq,
-                     float* dk, float* dv, float* rowsum, float* colsum, cudaStream_t s) {
+                     const float* cum_lo, const float* lse, const float* Dvec, const void* dO, float scale, void* dq,
+                     void* dk, void* dv, float* rowsum, float* colsum, cudaStream_t s) {
     return launch_attn_bwd<ATTN_E>(p, q, k, v, cum, cum_lo, lse, Dvec, dO, scale, dq, dk, dv, rowsum, colsum, s);
 }
 
 cudaError_t tc_poly_bwd(const Problem& p, int order, const void* q, const void* k, const void* v, const float* cum,
-                        const float* cum_lo, const float* zeta, const float* D, const void* dO, float* dq, float* dk,
-                        float* dv, float* rowsum, float* colsum, cudaStream_t s) {
+                        const float* cum_lo, const float* zeta, const float* D, const void* dO, void* dq, void* dk,
+                        void* dv, float* rowsum, float* colsum, cudaStream_t s) {
     if (order == 2)
         return launch_attn_bwd<ATTN_P2>(p, q, k, v, cum, cum_lo, zeta, D, dO, 1.f, dq, dk, dv, rowsum, colsum, s);
     if (order == 1)

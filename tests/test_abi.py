@@ -103,7 +103,9 @@ def test_step_and_e_reject_bad_arguments(lib):
     assert lib.tm2e_forward(f, f, f, f, f, None, 1, 1, 128, 64, 64, ctypes.c_float(0.125), 1, f,
                             1 << 30, None) == INVALID
     assert lib.tm2e_backward(f, f, f, f, f, f, f, f, f, f, f, 1, 1, 128, 64, 64, ctypes.c_float(0.125),
-                             1, f, 8, None) == WORKSPACE
+                             1, 0, f, 8, None) == WORKSPACE
+    assert lib.tm2e_backward(f, f, f, f, f, f, f, f, f, f, f, 1, 1, 128, 64, 64, ctypes.c_float(0.125),
+                             1, 1, f, 1 << 30, None) == INVALID     # no normalisation flag for 2Mamba-E
 
 
 def test_backward_needs_Z_when_normalised(lib):

@@ -38,8 +38,11 @@ def test_algorithmic_units_per_token_head():
     assert bench.kernel_flops("tc_bwd_dkdv", D, DV, C, 1) == 1_114_304
     # bytes: the chunk state (4,160) plus the token rows each kernel must move
     assert bench.kernel_bytes("tc_chunk_out", D, DV, C, 1) == 4160 + 2 * 192 + 4 * 65       # q k v in; o, Z out
-    assert bench.kernel_bytes("tc_bwd_dq", D, DV, C, 1) == 4160 + 2 * 256 + 4 * 66          # q k v dO in; dq, two scalars
-    assert bench.kernel_bytes("tc_bwd_dkdv", D, DV, C, 1) == 4160 + 2 * 256 + 4 * 132
+    assert bench.kernel_bytes("tc_bwd_dq", D, DV, C, 1) == 4160 + 2 * 256 + 2 * 64 + 4 * 2   # q k v dO in; dq (bf16), two scalars
+    assert bench.kernel_bytes("tc_bwd_dkdv", D, DV, C, 1) == 4160 + 2 * 256 + 2 * 128 + 4 * 4
+    # decode: the fp32 state read and written once, full (d^2 rows) or symmetric-packed (d(d+1)/2)
+    assert bench.decode_bytes_per_head(64, 64) - bench.decode_bytes_per_head(64, 64, packed=True) == \
+        2 * (4096 - 2080) * (64 + 1) * 4
     assert bench.kernel_flops("not_a_kernel", D, DV, C, 1) is None
     assert bench.kernel_bytes("not_a_kernel", D, DV, C, 1) is None
 
@@ -53,12 +56,17 @@ def test_roofline_picks_the_slower_bound():
     assert r["achieved"] == pytest.approx(kb / 0.616e-3 / 1e9)
     assert r["frac"] == pytest.approx(r["achieved"] / PK["hbm_gbs"])
     assert r["tensor_frac"] == pytest.approx(kf / 0.616e-3 / 1e12 / PK["bf16_tflops_sustained"])
-    # dk/dv sits just past the ridge on the tensor side (0.216 ms of flops, 0.210 ms of bytes)
+    # dk/dv sits just past the ridge on the tensor side against the sustained figure (0.216 ms of
+    # flops, 0.20 ms of bytes) and on the HBM side against the burst figure (0.168 ms of flops)
     kf = bench.kernel_flops("tc_bwd_dkdv", D, DV, C, TOKENS)
     kb = bench.kernel_bytes("tc_bwd_dkdv", D, DV, C, TOKENS)
     r = bench.roofline("tc_bwd_dkdv", kf, kb, 0.606, PK, tc=True)
     assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and r["peak"] == PK["bf16_tflops_sustained"]
     assert r["frac"] == pytest.approx(kf / 0.606e-3 / 1e12 / PK["bf16_tflops_sustained"])
+    rb = bench.roofline("tc_bwd_dkdv", kf, kb, 0.606, PK, tc=True, peak_key="bf16_tflops")
+    assert rb["bound"] == "hbm" and rb["tensor_frac"] == pytest.approx(kf / 0.606e-3 / 1e12 / PK["bf16_tflops"])
+    # the tensor figure follows the length of the timed region
+    assert bench.tensor_peak_key(53.0) == "bf16_tflops" and bench.tensor_peak_key(1200.0) == "bf16_tflops_sustained"
     # the same work with twice the bandwidth is tensor-bound, with half of it HBM-bound
     assert bench.roofline("k", kf, kb, 1.0, dict(PK, hbm_gbs=2 * PK["hbm_gbs"]), tc=True)["bound"] == "tensor"
     assert bench.roofline("k", kf, kb, 1.0, dict(PK, hbm_gbs=PK["hbm_gbs"] / 2), tc=True)["bound"] == "hbm"

@@ -137,9 +137,11 @@ def test_conv2_sequence_forward_backward(dtype, C):
     refs = oracle.conv2_bwd(x, w, dy, xp)
     if dtype == "f32":
         assert si.rel_err(y.cpu(), y_r) <= 1e-6
-    else:   # the output is rounded to bf16: within half an ulp (2^-9 relative) of the exact value, plus fp32 slack
-        err = (y.float().cpu().double() - torch.as_tensor(y_r)).abs()
-        assert bool((err <= 2.0 ** -9 * torch.as_tensor(y_r).abs() * (1 + 1e-5) + 1e-30).all())
+    else:   # the output is rounded to bf16: within half an ulp (2^-8 relative) of the exact value, plus the
+        # fp32 arithmetic's error, which matters only where the two terms cancel
+        yr = torch.as_tensor(y_r)
+        err = (y.float().cpu().double() - yr).abs()
+        assert bool((err <= 2.0 ** -8 * yr.abs() + 1e-6 * yr.pow(2).mean().sqrt()).all())
     for name, got, ref in zip(("dx", "dx_prev", "dw", "db"), (dx, dxp, dw, db), refs):
         assert si.rel_err(got.cpu(), ref) <= 1e-5, name
 

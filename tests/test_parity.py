@@ -410,3 +410,34 @@ def test_e_fwd_bwd_bf16_B2_H16_T4096_sampled_heads():
         for name, x, ref in zip(("dq", "dk", "dv", "da"), (dq, dk, dv, da), refs):
             e = err(x.cpu()[sel], ref)
             assert e <= 2e-2, (name, e)
+
+
+
+# ------------------------------------------------------------------------ gradient output type
+
+def test_grads_in_input_dtype_are_the_rounded_fp32_grads():
+    """TM2_GRADS_INPUT_DTYPE: dq, dk, dv come out in bf16, each exactly the round-to-nearest of
+    the fp32 gradient the same backward writes without the flag -- on the tensor-core chunked
+    path, the CUDA-core chunked path, 2Mamba-E and the quadratic form."""
+    inp = si.sequence_inputs(2, 2, 333, 64, 64, dtype="bf16", qkv_std=0.125, seed=801, with_dO=True)
+    g = cuda(inp)
+    for chunk in (0, 64):
+        o, Z = tm2.forward(g["q"], g["k"], g["v"], g["a"], chunk=chunk)
+        full = tm2.backward(g["q"], g["k"], g["v"], g["a"], o, Z, g["dO"], chunk=chunk)
+        low = tm2.backward(g["q"], g["k"], g["v"], g["a"], o, Z, g["dO"], chunk=chunk, lowp_grads=True)
+        torch.cuda.synchronize()
+        for x, y in zip(full[:3], low[:3]):
+            assert y.dtype == torch.bfloat16 and torch.equal(y, x.to(torch.bfloat16))
+        assert torch.equal(full[3], low[3])
+    ie = si.sequence_inputs(2, 2, 333, 64, 64, dtype="bf16", qkv_std=1.0, seed=802, with_dO=True)
+    ge = cuda(ie)
+    oe, lse = tm2.e_forward(ge["q"], ge["k"], ge["v"], ge["a"])
+    full = tm2.e_backward(ge["q"], ge["k"], ge["v"], ge["a"], oe, lse, ge["dO"])
+    low = tm2.e_backward(ge["q"], ge["k"], ge["v"], ge["a"], oe, lse, ge["dO"], lowp_grads=True)
+    oq, Zq = tm2.forward_quadratic(g["q"], g["k"], g["v"], g["a"])
+    fq = tm2.backward_quadratic(g["q"], g["k"], g["v"], g["a"], oq, Zq, g["dO"])
+    lq = tm2.backward_quadratic(g["q"], g["k"], g["v"], g["a"], oq, Zq, g["dO"], lowp_grads=True)
+    torch.cuda.synchronize()
+    for F, L in ((full, low), (fq, lq)):
+        for x, y in zip(F[:3], L[:3]):
+            assert y.dtype == torch.bfloat16 and torch.equal(y, x.to(torch.bfloat16))
