@@ -43,7 +43,10 @@
  *    chunk in {0 (library choice), 64, 256}.  chunk 0 picks 256 (the tensor-core path)
  *    for bf16 inputs with d = dv = 64 and 64 otherwise; 256 is accepted only where the
  *    tensor-core path applies (bf16, d = dv = 64).  Other values return
- *    TM2_ERR_UNSUPPORTED.
+ *    TM2_ERR_UNSUPPORTED; 128 and 512 among them: the tensor-core kernels are built around
+ *    256-token chunks (four 64-token stages per chunk in the state walk, two 128-token
+ *    readout tiles per chunk state), and the other end of the range, one chunk of T
+ *    tokens, is the quadratic form (tm2q_forward).
  *    B*H <= 65535 for the sequence entry points.
  */
 #ifndef TM2_H
