@@ -74,16 +74,17 @@ struct ScanIO {
 };
 cudaError_t tc_state_scan(const Problem& p, const ScanIO& io, cudaStream_t s);
 
-// Operands of the chunk-state scan (tm2_scan.cu): ops [BH][Tp/64][136][64] fp16, one block
+// Operands of the chunk-state scan (tm2_scan.cu): ops [BH][Tp/64][144][64] fp16, one block
 // per 64-token stage (one TMA request each): rows 0-63 the key block transposed (row n =
 // key_t[n] over the stage's tokens t), rows 64-127 the weighted values transposed (row col =
-// w_t val_t[col]), row 128 = w_t zc_t, rows 129-135 zero.  Forward: key = k, val = v,
+// w_t val_t[col]), row 128 = w_t zc_t, rows 129-143 zero (rows 64-143 are the walk's N = 80
+// operand).  Forward: key = k, val = v,
 // w = exp(g_c - A_t), zc = 1.  Reverse: key = q, val = dO, w = exp(A_t) zeta_t / zmax_c,
 // zc = ucol_t.
 // The key and value operands (and the reverse walk's normaliser row) are multiplied by the
 // powers of two pow2_scale(amax[bh][0]), pow2_scale(amax[bh][1]) (and pow2_scale(amax[bh][2])),
 // so the walk's states come out multiplied by ks^2 vs (value columns) and ks^2 zs (normaliser).
-constexpr int TC_OPS_ROWS = 136;
+constexpr int TC_OPS_ROWS = 144;
 cudaError_t launch_tc_scan_operands(const Problem& p, bool rev, const void* key, const void* val, const float* Aloc,
                                     const float* g, const float* zeta, const float* ucol, const float* zmax,
                                     const unsigned* amax, void* ops, cudaStream_t s);

@@ -395,7 +395,7 @@ __global__ void __launch_bounds__(256) tc_scan_operands_kernel(
         dv[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
     }
     // the normaliser row and the zero rows after it
-    for (int e = tid; e < 8 * 64; e += 256) {
+    for (int e = tid; e < (TC_OPS_ROWS - 128) * 64; e += 256) {
         const int r = e >> 6, j = e & 63;
         blk[(128 + r) * 64 + j] = __float2half_rn(r == 0 ? zs * sw[j] * szc[j] : 0.f);
     }

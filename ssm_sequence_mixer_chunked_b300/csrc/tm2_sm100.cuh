@@ -138,6 +138,17 @@ TM2_DEV void tma_load_5d(uint32_t dst, const void* tmap, uint32_t bar, int x, in
         "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w), "r"(v)
         : "memory");
 }
+// Tiled TMA store shared -> global (3-D map), tracked by the thread's bulk async-group.
+TM2_DEV void tma_store_3d(const void* tmap, uint32_t src, int x, int y, int z) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(tmap),
+                 "r"(src), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+TM2_DEV void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until every committed bulk group of this thread has finished reading its shared source.
+TM2_DEV void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Waits until every committed bulk group of this thread has completed.
+TM2_DEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // Untiled bulk copy global -> shared (both addresses 16-byte aligned, bytes a multiple of 16),
 // completing `bytes` of transaction count on the mbarrier.
 TM2_DEV void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
@@ -246,6 +257,15 @@ TM2_DEV void tmem_st8(uint32_t taddr, const uint32_t* r) {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
                  "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
                  : "memory");
+}
+// 16 registers per thread -> 32 lanes x 16 consecutive columns (no wait).
+TM2_DEV void tmem_st16(uint32_t taddr, const uint32_t* r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
 }
 // 32 registers per thread -> 32 lanes x 32 consecutive columns (no wait).
 TM2_DEV void tmem_st32(uint32_t taddr, const float* v) {

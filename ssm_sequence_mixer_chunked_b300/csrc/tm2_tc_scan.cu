@@ -9,16 +9,23 @@
 //     dS_{c-1} = exp(g_c) dS_c + sum_{i in c} exp(A_i) zeta_i (q_i (x) q_i) [dO_i, ucol_i]^T,
 // with zeta_i = 1/Z_i and ucol_i = -dO_i . o_i (normalised) or zeta = 1, ucol = 0.
 //
-// One CTA owns NR (128 or 256) state rows r = m*64 + n with m in {MP Q .. MP Q + MP - 1}
-// (MP = NR / 64) of one (b, h) and walks every chunk in order.  The chunk's contribution is
-// computed transposed,
-//     H^T[col][(m,n)] = sum_j (w_j val_j[col]) key_j[m] key_j[n],
-// as tcgen05.mma with M = 128 (the 64 value columns, the normaliser column and zero rows),
-// N = NR (the CTA's state rows) and K = tokens: 8 instructions per 64-token stage.  NR = 128
-// would give 32 CTAs per head (1024 at B = 2, H = 16: 6.9 waves on 148 SMs where NR = 256
-// gives 3.5, i.e. 4 with a half-empty last one) and halve each stage's operand building, but
-// a stage still costs its 8 instructions (0.85 us at N = 128 against 1.2 us at N = 256), so
-// the walk took 0.76 ms against 0.62 ms at B = 2, H = 16, T = 8192: NR = 256 is used.
+// One CTA owns 256 state rows r = m*64 + n with m in {4Q .. 4Q + 3} of one (b, h) and walks
+// every chunk in order.  The chunk's contribution is computed with the state rows on M,
+//     H[(m,n)][col] = sum_j (key_j[m] key_j[n]) (w_j val_j[col]),
+// as tcgen05.mma with M = 128 state rows (two M-blocks per CTA), N = 80 (the 64 value columns,
+// the normaliser column and 15 zero rows of the operand block) and K = tokens; the key (x)
+// key operand is A, built by the builder warps straight into tensor memory, and the weighted
+// values are B, the operand block's rows 64-143 as the TMA brought them.  A single issuing
+// thread gets about one such instruction per 120-150 SM cycles whatever N <= 128, while
+// instructions of different issuing threads overlap, so each M-block has its own issuing warp
+// and accumulators: 16 instructions per 64-token stage and CTA, 8 per issuer.  A commit
+// (tcgen05.commit) costs its thread about as much as two of these instructions, so each
+// issuer commits once per 32 tokens; that commit both frees the 32-token key-product buffer
+// for the builders and, for a stage's second half, the ring slot for the TMA producer.  Shared memory
+// carries only the TMA'd operand blocks (the earlier orientation, state rows on N = 256 with
+// the key products staged in shared memory, was bound by shared-memory traffic at 1.2 us per
+// stage; this one needs none of it), and each epilogue thread owns one whole state row, so the
+// fp16 state planes go out as 128-byte rows.
 //
 // Precision.  Tokens whose query is nearly orthogonal to the state read it out with heavy
 // cancellation, so the state must carry more than one 16-bit rounding (a single fp16
@@ -41,17 +48,17 @@
 // the reverse walk multiplies it by vs / zs, times ks^2 vs too.  S0 / z0 are brought into
 // them, S_final / z_final out of them, and the readouts divide by the same exact factors.
 //
-// Data flow.  A pre-pass (launch_tc_scan_operands) writes one [136][64] fp16 block per
-// 64-token stage: the transposed key block and the transposed weighted values with the
-// normaliser row (and 7 zero rows); one TMA request brings a stage into a ring slot.  Warps
-// 0-7 build the key (x) key operand of a stage in shared memory (thread = one key index n and
-// 16 tokens, the four state rows of that n, hi and lo planes, 128-byte swizzled K-major),
-// double-buffered; warp 15 issues the MMAs into tensor-memory buffer
-// (chunk & 1); warps 8, 9, 12, 13 (value columns, lane quadrants 0 and 1) and 10, 14 (the
-// normaliser column, lane 64) fold the chunk into the running state,
-//     S_c = exp(g_c) S_{c-1} + scale H^T_c,
-// written back over H^T_c in tensor memory (so the buffer of chunk c-1 frees as soon as it
-// has been read), and export it; warp 11 issues the TMA loads.
+// Data flow.  A pre-pass (launch_tc_scan_operands) writes one [144][64] fp16 block per
+// 64-token stage: the transposed key block, the transposed weighted values, the normaliser row
+// and 15 zero rows; one TMA request brings a stage into a ring slot (warp 8).  Warps 0-7 build
+// the key (x) key operand of each 32 tokens (two groups of four warps taking turns; thread =
+// one key index n and its state row in each M-block, hi and lo planes) into one of three
+// tensor-memory buffers; warps 9 and 10 issue the MMAs of M-block 0 and 1 into accumulator
+// (chunk & 1); warps 11-18 (thread = one state row, kept in registers) fold the chunk into the
+// running state,
+//     S_c = exp(g_c) S_{c-1} + scale H_c,
+// and export it (staged in shared memory, one TMA store per plane).  An accumulator is only
+// read by the fold, so the MMAs of chunk c + 1 run while chunk c is folded and exported.
 // Every mbarrier wait is bounded; on expiry the status word records TM2_ERR_TIMEOUT and
 // the CTA unwinds.
 #include "tm2.h"
@@ -63,19 +70,25 @@ namespace tm2 {
 namespace tcscan {
 
 constexpr int C = TC_CHUNK;     // chunk length
-constexpr int KS = 64;          // tokens per stage
+constexpr int KS = 64;          // tokens per stage (one TMA request)
 constexpr int SPC = C / KS;     // stages per chunk
-constexpr int NSLOT = 5;        // ring slots, one stage each
-constexpr int SLOT = TC_OPS_ROWS * 128;   // [Kt 64 rows | value^T 64 rows | normaliser row | 7 zero rows]
-constexpr int NR_ROWS = 256;    // state rows per CTA (128 or 256; 256 measured faster)
-// key (x) key operand of a stage: hi [NR][64] then lo [NR][64]
-__host__ __device__ constexpr int bbuf(int NR) { return NR * 256; }
-constexpr int SB = NSLOT * SLOT;
-__host__ __device__ constexpr int smem_bytes(int NR) { return SB + 2 * bbuf(NR) + 1024; }
-constexpr int THREADS = 16 * 32;
-constexpr int NBUILD = 256;     // builder threads (warps 0-7)
-constexpr int NEPI = 192;       // epilogue threads (warps 8, 9, 10, 12, 13, 14)
-constexpr int WARP_TMA = 11, WARP_MMA = 15;
+constexpr int NSLOT = 4;        // ring slots, one stage each
+constexpr int SLOT = TC_OPS_ROWS * 128;   // [Kt 64 rows | value^T 64 rows | normaliser row | 15 zero rows]
+constexpr int NR = 256;         // state rows per CTA (two M-blocks of 128)
+constexpr int NV = 80;          // accumulator columns: 64 value columns, the normaliser, 15 zero
+constexpr uint32_t ACC = 80;    // accumulator of chunk buffer b, M-block mb at column (2 b + mb) ACC
+constexpr uint32_t TM_A = 320;  // key-product buffer x (32 tokens) at TM_A + 64 x: [mb][hi, lo], 16 columns each
+constexpr int NAB = 3;          // key-product buffers
+constexpr int HT = 32;          // tokens per key-product buffer
+constexpr int SMEM_STG = NSLOT * SLOT;   // export staging: hi, lo planes [256 rows][128 B], 128B-swizzled
+constexpr int SMEM_BYTES = SMEM_STG + 2 * 32768 + 1024;
+constexpr int NBUILD = 128;     // builder threads per group (two groups: warps 0-3 first, 4-7 second half stages)
+constexpr int NEPI = 256;       // epilogue threads (warps 11-18), one state row each
+constexpr int WARP_TMA = 8, WARP_MMA = 9, WARP_EPI = 11;   // issuers: warps 9 (M-block 0), 10 (M-block 1)
+constexpr int THREADS = 19 * 32;
+constexpr uint32_t IDESC = idesc_f16_f32(128, NV, false, false);
+static_assert(TC_OPS_ROWS - 64 == NV, "the operand block's rows 64.. are the N = 80 operand");
+static_assert(3 * ACC + NV <= TM_A && TM_A + 64 * NAB <= 512, "tensor memory layout");
 
 struct Args {
     const float* g;       // [BH][NC] chunk totals
@@ -92,23 +105,28 @@ struct Args {
     int T, NC, Tp, rev;
 };
 
+TM2_DEV void ld_row_chunks4(uint32_t row_addr, int row, int c0, uint32_t* x) {   // 4 swizzled 16-byte chunks
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(x[4 * c]), "=r"(x[4 * c + 1]), "=r"(x[4 * c + 2]), "=r"(x[4 * c + 3])
+                     : "r"(row_addr + (uint32_t)(((c0 + c) ^ (row & 7)) << 4)));
+}
+
 }  // namespace tcscan
 
 using namespace tcscan;
 
-template <int NR>
 __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_constant__ CUtensorMap tmOps,
+                                                                   const __grid_constant__ CUtensorMap tmSx,
                                                                    const __grid_constant__ Args a) {
-    constexpr int MP = NR / 64;                  // key indices m per CTA
-    constexpr int BBUF = bbuf(NR);
-    constexpr uint32_t IDESC = idesc_f16_f32(128, NR, false, false);
-    constexpr uint32_t TCOLS = 2 * NR;           // two accumulator buffers of NR columns
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_align1024(smem_raw);
-    __shared__ __align__(8) uint64_t bar_full[NSLOT], bar_empty[NSLOT], bar_bfull[2], bar_bempty[2], bar_hfull[2],
-        bar_dfree[2], bar_done;
+    __shared__ __align__(8) uint64_t bar_full[NSLOT], bar_afull[NAB], bar_hsdone[NAB], bar_hfull[2][2],
+        bar_dfree[2][2], bar_done[2];
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_s;
+    __shared__ volatile int eflags[2];   // group waits of the epilogue warps
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int Q = blockIdx.x;
     const long bh = blockIdx.y;
@@ -119,22 +137,23 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
     const uint32_t sbase = smem_u32(smem);
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < NSLOT; ++i) {
-            mbar_init(smem_u32(&bar_full[i]), 1);
-            mbar_init(smem_u32(&bar_empty[i]), NBUILD + 1);   // builders read Kt, the MMAs read the values
+        for (int i = 0; i < NSLOT; ++i) mbar_init(smem_u32(&bar_full[i]), 1);
+        for (int i = 0; i < NAB; ++i) {
+            mbar_init(smem_u32(&bar_afull[i]), NBUILD);
+            mbar_init(smem_u32(&bar_hsdone[i]), 2);   // both issuers' MMAs of the half stage are done
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(smem_u32(&bar_bfull[i]), NBUILD);
-            mbar_init(smem_u32(&bar_bempty[i]), 1);
-            mbar_init(smem_u32(&bar_hfull[i]), 1);
-            mbar_init(smem_u32(&bar_dfree[i]), NEPI);
+            mbar_init(smem_u32(&bar_done[i]), 1);
+            for (int mb = 0; mb < 2; ++mb) {
+                mbar_init(smem_u32(&bar_hfull[i][mb]), 1);
+                mbar_init(smem_u32(&bar_dfree[i][mb]), NEPI / 2);
+            }
         }
-        mbar_init(smem_u32(&bar_done), 1);
         abort_s = 0;
         fence_mbar_init();
     }
     if (warp == 0) {
-        tmem_alloc(smem_u32(&tmem_base_s), TCOLS);
+        tmem_alloc(smem_u32(&tmem_base_s), 512);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -151,10 +170,13 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
             int issued = 0;
             for (int gs = 0; gs < nstages && !abort_s; ++gs) {
                 const int sl = gs % NSLOT;
-                const uint32_t u = (uint32_t)(gs / NSLOT);
-                if (u > 0 && !mbar_wait(smem_u32(&bar_empty[sl]), (u - 1) & 1, a.status)) {
-                    abort_s = 1;
-                    break;
+                if (gs >= NSLOT) {   // the slot's previous stage: its second half stage's MMAs are done (and
+                    // with them the builders' reads of it, which the issuers waited for)
+                    const int ghs = 2 * (gs - NSLOT) + 1;
+                    if (!mbar_wait(smem_u32(&bar_hsdone[ghs % NAB]), (uint32_t)(ghs / NAB) & 1, a.status)) {
+                        abort_s = 1;
+                        break;
+                    }
                 }
                 const int stg = chunk_of(gs / SPC) * SPC + gs % SPC;   // stage index within the sequence
                 const uint32_t fb = smem_u32(&bar_full[sl]);
@@ -166,219 +188,222 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
             for (int gs = issued - 1; gs >= 0 && gs >= issued - NSLOT; --gs)
                 mbar_wait(smem_u32(&bar_full[gs % NSLOT]), (uint32_t)(gs / NSLOT) & 1, a.status);
         }
-    } else if (warp == WARP_MMA) {
-        // ---------------------------------------------------------------- MMA issuer
+    } else if (warp == WARP_MMA || warp == WARP_MMA + 1) {
+        // ---------------------------------------------------------------- MMA issuer of M-block mb
+        const int mb = warp - WARP_MMA;
         if (lane == 0) {
             bool ok = true;
             for (int it = 0; it < nchunks && ok; ++it) {
                 const int b = it & 1;
-                if (it >= 1 && !(ok = mbar_wait(smem_u32(&bar_dfree[b]), (uint32_t)((it - 1) >> 1) & 1, a.status)))
+                // accumulator b was last read by the fold of chunk it - 2
+                if (it >= 2 &&
+                    !(ok = mbar_wait(smem_u32(&bar_dfree[b][mb]), (uint32_t)((it - 2) >> 1) & 1, a.status)))
                     break;
-                for (int s = 0; s < SPC; ++s) {
-                    const int gs = it * SPC + s, sl = gs % NSLOT, sb = gs & 1;
+                const uint32_t d = tmem + (uint32_t)(2 * b + mb) * ACC;
+                for (int s = 0; s < SPC && ok; ++s) {
+                    const int gs = it * SPC + s, sl = gs % NSLOT;
                     if (abort_s) { ok = false; break; }
                     if (!(ok = mbar_wait(smem_u32(&bar_full[sl]), (uint32_t)(gs / NSLOT) & 1, a.status))) break;
-                    if (!(ok = mbar_wait(smem_u32(&bar_bfull[sb]), (uint32_t)(gs >> 1) & 1, a.status))) break;
-                    tc_fence_after();
-                    // value^T rows (M), K-major.  M rows 72-127 read whatever follows the slot: they
-                    // only reach accumulator lanes 72-127, which nothing reads.
-                    const uint32_t av = sbase + sl * SLOT + 8192;
-                    const uint32_t bhi = sbase + SB + sb * BBUF, blo = bhi + NR * 128;
-                    const uint32_t d = tmem + (uint32_t)b * NR;
+                    const uint32_t bv = sbase + sl * SLOT + 64 * 128;   // rows 64-143: N = 80, K-major
+                    for (int hs = 0; hs < KS / HT; ++hs) {
+                        const int ghs = gs * (KS / HT) + hs, x = ghs % NAB;
+                        if (!(ok = mbar_wait(smem_u32(&bar_afull[x]), (uint32_t)(ghs / NAB) & 1, a.status))) break;
+                        tc_fence_after();
+                        const uint32_t ah = tmem + TM_A + 64 * x + 32 * mb;
 #pragma unroll
-                    for (int kk = 0; kk < KS / 16; ++kk)
-                        umma_bf16(d, sdesc_sw128(av + kk * 32), sdesc_sw128(bhi + kk * 32), IDESC, (s > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-                    for (int kk = 0; kk < KS / 16; ++kk)
-                        umma_bf16(d, sdesc_sw128(av + kk * 32), sdesc_sw128(blo + kk * 32), IDESC, 1u);
-                    umma_commit(smem_u32(&bar_empty[sl]));
-                    umma_commit(smem_u32(&bar_bempty[sb]));
+                        for (int kk = 0; kk < HT / 16; ++kk) {
+                            const uint64_t bd = sdesc_sw128(bv + (2 * hs + kk) * 32);
+                            umma_bf16_ts(d, ah + kk * 8, bd, IDESC, (s > 0 || hs > 0 || kk > 0) ? 1u : 0u);
+                            umma_bf16_ts(d, ah + 16 + kk * 8, bd, IDESC, 1u);
+                        }
+                        // one commit per half stage: a commit costs the issuing thread about as
+                        // much as two of these MMAs
+                        umma_commit(smem_u32(&bar_hsdone[x]));
+                    }
                 }
                 if (!ok) break;
-                umma_commit(smem_u32(&bar_hfull[b]));
+                umma_commit(smem_u32(&bar_hfull[b][mb]));
             }
             if (!ok) abort_s = 1;
-            umma_commit(smem_u32(&bar_done));
-            mbar_wait(smem_u32(&bar_done), 0, a.status);
+            umma_commit(smem_u32(&bar_done[mb]));
+            mbar_wait(smem_u32(&bar_done[mb]), 0, a.status);
         }
     } else if (warp < 8) {
         // ---------------------------------------------------------------- key (x) key builders
-        // thread: key index n = t & 63, tokens 16 * (t >> 6) .. +15, the MP state rows
-        // (m' = 0..MP-1, m = MP Q + m') of that n: the Kt row of n is read once, the rows of m
-        // are warp-uniform (broadcast).
-        const int n = threadIdx.x & 63, kq = threadIdx.x >> 6;
+        // group gp = warp / 4 builds the half stages hs = gp of every stage (so each group has
+        // two half stages of MMA time for one build); thread: key index n, state rows (m0, n) in
+        // M-block 0 and (m0 + 2, n) in M-block 1 (both at tensor-memory lane 32 (warp % 4) +
+        // lane); the Kt row of n is read once, the rows of m are warp-uniform (broadcast).  A
+        // column holds two consecutive tokens (the lower one in the low half), 16 columns per
+        // 32 tokens; hi and lo planes.
+        const int gp = warp >> 2, quad = warp & 3;
+        const int r0 = quad * 32 + lane, n = r0 & 63, m0 = 4 * Q + (r0 >> 6);
+        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         for (int gs = 0; gs < nstages; ++gs) {
-            const int sl = gs % NSLOT, sb = gs & 1;
+            const int sl = gs % NSLOT;
             if (abort_s || !mbar_wait(smem_u32(&bar_full[sl]), (uint32_t)(gs / NSLOT) & 1, a.status)) {
                 abort_s = 1;
                 break;
             }
-            if (gs >= 2 && !mbar_wait(smem_u32(&bar_bempty[sb]), (uint32_t)((gs >> 1) - 1) & 1, a.status)) {
+            const uint32_t kt = sbase + sl * SLOT;   // Kt: row x = key_j[x] over the stage's 64 tokens j
+            const int hs = gp, ghs = gs * (KS / HT) + hs, x = ghs % NAB;
+            if (ghs >= NAB && !mbar_wait(smem_u32(&bar_hsdone[x]), (uint32_t)(ghs / NAB - 1) & 1, a.status)) {
                 abort_s = 1;
                 break;
             }
-            const uint32_t kt = sbase + sl * SLOT;   // Kt: row x = key_j[x] over the stage's 64 tokens j
-            uint32_t xn[8];
+            uint32_t xn[16];
+            ld_row_chunks4(kt + n * 128, n, 4 * hs, xn);
 #pragma unroll
-            for (int c2 = 0; c2 < 2; ++c2)
-                asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                             : "=r"(xn[4 * c2]), "=r"(xn[4 * c2 + 1]), "=r"(xn[4 * c2 + 2]), "=r"(xn[4 * c2 + 3])
-                             : "r"(kt + n * 128 + (((2 * kq + c2) ^ (n & 7)) << 4)));
+            for (int mb = 0; mb < 2; ++mb) {
+                const int m = m0 + 2 * mb;
+                uint32_t xm[16], rh[16], rl[16];
+                ld_row_chunks4(kt + m * 128, m, 4 * hs, xm);
 #pragma unroll
-            for (int mp = 0; mp < MP; ++mp) {
-                const int m = MP * Q + mp, r = mp * 64 + n;
-                const uint32_t dhi = sbase + SB + sb * BBUF + r * 128, dlo = dhi + NR * 128;
-#pragma unroll
-                for (int c2 = 0; c2 < 2; ++c2) {
-                    const int k8 = 2 * kq + c2;
-                    uint32_t xm[4], rh[4], rl[4];
-                    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                                 : "=r"(xm[0]), "=r"(xm[1]), "=r"(xm[2]), "=r"(xm[3])
-                                 : "r"(kt + m * 128 + ((k8 ^ (m & 7)) << 4)));
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const __half2 km2 = *reinterpret_cast<const __half2*>(&xm[i]);
-                        const __half2 kn2 = *reinterpret_cast<const __half2*>(&xn[4 * c2 + i]);
-                        const __half2 hi2 = __hmul2(km2, kn2);
-                        const __half2 lo2 = __hfma2(km2, kn2, __hneg2(hi2));
-                        rh[i] = *reinterpret_cast<const uint32_t*>(&hi2);
-                        rl[i] = *reinterpret_cast<const uint32_t*>(&lo2);
-                    }
-                    const uint32_t off = (uint32_t)((k8 ^ (r & 7)) << 4);
-                    st_shared_v4(dhi + off, rh[0], rh[1], rh[2], rh[3]);
-                    st_shared_v4(dlo + off, rl[0], rl[1], rl[2], rl[3]);
+                for (int i = 0; i < 16; ++i) {
+                    const __half2 km2 = *reinterpret_cast<const __half2*>(&xm[i]);
+                    const __half2 kn2 = *reinterpret_cast<const __half2*>(&xn[i]);
+                    const __half2 hi2 = __hmul2(km2, kn2);
+                    const __half2 lo2 = __hfma2(km2, kn2, __hneg2(hi2));
+                    rh[i] = *reinterpret_cast<const uint32_t*>(&hi2);
+                    rl[i] = *reinterpret_cast<const uint32_t*>(&lo2);
                 }
+                const uint32_t ta = tmem + lane_base + TM_A + 64 * x + 32 * mb;
+                tmem_st16(ta, rh);
+                tmem_st16(ta + 16, rl);
             }
-            fence_proxy_async();
-            mbar_arrive(smem_u32(&bar_bfull[sb]));
-            mbar_arrive(smem_u32(&bar_empty[sl]));
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bar_afull[x]));
         }
-    } else {
+    } else if (warp >= WARP_EPI) {
         // ---------------------------------------------------------------- running state (epilogue)
-        // warps 8, 12: value columns 0-31; 9, 13: columns 32-63; 10, 14: the normaliser column
-        // (tensor-memory lane 64 = lane 0 of the warp); e = which half of the NR state rows,
-        // NK groups of 32 rows each.
-        const int q = warp & 3, e = warp >= 12 ? 1 : 0;
-        const bool zwarp = q == 2;
+        // thread: state row r = 128 mb + 32 quad + lane (M-block mb = (w - 11) / 4, lane quadrant
+        // w % 4), held in registers: S[0..63] the values, S[64] the normaliser.  The accumulator
+        // of a chunk is only read (16 columns at a time; the group of the normaliser carries 15
+        // zero columns), so the MMAs of the next chunk never wait for this fold.
+        const int mb = (warp - WARP_EPI) >> 2, quad = warp & 3;
+        const int r = mb * 128 + quad * 32 + lane;
+        const long R = (long)Q * NR + r;
+        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         // units of the running state (see the header): forward value columns ks^2 vs, forward
         // normaliser ks^2; the reverse normaliser column is brought to ks^2 vs by vs / zs
         const float ks = pow2_scale(a.amax[bh * 4]), vs = pow2_scale(a.amax[bh * 4 + 1]);
-        const float unit = rev ? 1.f : (zwarp ? ks * ks : ks * ks * vs);
-        const float zfix = (rev && zwarp) ? vs / pow2_scale(a.amax[bh * 4 + 2]) : 1.f;
-        const int col = 32 * q + lane;               // value column (q < 2)
-        const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-        constexpr int NK = NR / 64;
-        const long row0 = (long)Q * NR + (NR / 2) * e;   // first state row of this warp's NR / 2
+        const float unit_v = rev ? 1.f : ks * ks * vs, unit_z = rev ? 1.f : ks * ks;
+        const float zfix = rev ? vs / pow2_scale(a.amax[bh * 4 + 2]) : 1.f;
+        const bool lead = warp == WARP_EPI && lane == 0;   // records sscale, issues the TMA stores
+        float S[65];
         float gam = 1.f;   // reverse: running max of zmax over the chunks walked so far
-        // the 32 values of rows row0 + 32k + i (i = 0..31) held by lane `src` move to lane i
-        auto gather_lane = [&](const float* v, int src) {
-            float out = 0.f;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const float t = __shfl_sync(0xffffffffu, v[i], src);
-                if (lane == i) out = t;
-            }
-            return out;
-        };
-        // exports 32 rows (row0 + 32k ..) of the state held as v[i] (divided by gam)
-        auto export_rows = [&](int slot, int k, const float* v) {
-            const float inv = 1.f / gam;
-            const long rbase = row0 + 32 * k;
-            if (zwarp) {
-                const float zv = gather_lane(v, 0);
-                a.zx[(bh * NC + slot) * 4096 + rbase + lane] = zv;
-                return;
-            }
-            __half* hi = a.Sx + ((bh * NC + slot) * 2) * (4096L * 64) + rbase * 64 + col;
-            __half* lo = hi + 4096L * 64;
+        for (int i = 0; i < 65; ++i) S[i] = 0.f;
+        if (!rev) {   // the initial state (forward: S0 / z0 or zero; reverse: zero)
+            if (a.S0) {
+                const float4* src = reinterpret_cast<const float4*>(a.S0 + (bh * 4096 + R) * 64);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const float x = v[i] * inv;
-                const __half h = __float2half_rn(x);
-                hi[i * 64] = h;
-                lo[i * 64] = __float2half_rn(x - __half2float(h));
-            }
-        };
-        // the initial state (forward: S0 / z0 or zero; reverse: zero), rows row0 + 32k + i
-        auto initial_rows = [&](int k, float* v) {
-            const long rbase = row0 + 32 * k;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = 0.f;
-            if (rev) return;
-            if (zwarp) {
-                if (a.z0) {
-                    const float zl = a.z0[bh * 4096 + rbase + lane] * unit;
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = __shfl_sync(0xffffffffu, zl, i);
+                for (int q4 = 0; q4 < 16; ++q4) {
+                    const float4 x4 = src[q4];
+                    S[4 * q4] = x4.x * unit_v; S[4 * q4 + 1] = x4.y * unit_v;
+                    S[4 * q4 + 2] = x4.z * unit_v; S[4 * q4 + 3] = x4.w * unit_v;
                 }
-            } else if (a.S0) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = a.S0[(bh * 4096 + rbase + i) * 64 + col] * unit;
             }
+            if (a.z0) S[64] = a.z0[bh * 4096 + R] * unit_z;
+        }
+        // export of the state after a chunk: the values, divided by gam, as hi and residual fp16
+        // planes into the swizzled staging rows (one 32 KB TMA store per plane), the normaliser
+        // as fp32 straight to zx
+        const uint32_t stg = sbase + SMEM_STG;
+        auto export_row = [&](int slot) {
+            const float inv = 1.f / gam;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {   // 16-byte chunk j: columns 8j .. 8j + 7
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float x0 = S[8 * j + 2 * i] * inv, x1 = S[8 * j + 2 * i + 1] * inv;
+                    const __half2 h2 = __floats2half2_rn(x0, x1);
+                    const float2 hf = __half22float2(h2);
+                    const __half2 l2 = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+                    hi[i] = *reinterpret_cast<const uint32_t*>(&h2);
+                    lo[i] = *reinterpret_cast<const uint32_t*>(&l2);
+                }
+                const uint32_t off = (uint32_t)r * 128 + ((uint32_t)(j ^ (r & 7)) << 4);
+                st_shared_v4(stg + off, hi[0], hi[1], hi[2], hi[3]);
+                st_shared_v4(stg + 32768 + off, lo[0], lo[1], lo[2], lo[3]);
+            }
+            a.zx[(bh * NC + slot) * 4096 + R] = S[64];
+            fence_proxy_async();
+            named_bar_sync(2, NEPI);   // every row staged
+            if (lead) {
+                const int z0 = (int)((bh * NC + slot) * 2);
+                tma_store_3d(&tmSx, stg, 0, Q * NR, z0);
+                tma_store_3d(&tmSx, stg + 32768, 0, Q * NR, z0 + 1);
+                bulk_commit_group();
+            }
+        };
+        auto stage_begin = [&]() {   // the previous stores have read the staging rows
+            if (lead) bulk_wait_read_all();
+            named_bar_sync(2, NEPI);
         };
         {
             const int slot0 = rev ? NC - 1 : 0;
-            if (a.sscale && Q == 0 && warp == 8 && lane == 0) a.sscale[bh * NC + slot0] = 1.f;
-            for (int k = 0; k < NK; ++k) {
-                float v[32];
-                initial_rows(k, v);
-                export_rows(slot0, k, v);
-            }
+            if (a.sscale && lead && Q == 0) a.sscale[bh * NC + slot0] = 1.f;
+            stage_begin();
+            export_row(slot0);
         }
         bool ok = true;
+        int kg = 0;   // group-wait counter
         for (int it = 0; it < nchunks && ok; ++it) {
             const int c = chunk_of(it), b = it & 1;
             const float dec = __expf(a.g[bh * NC + c]);
             const float zm = rev ? a.zmax[bh * NC + c] : 1.f;
-            const float scl = zm * zfix;
-            if (abort_s || !(ok = mbar_wait(smem_u32(&bar_hfull[b]), (uint32_t)(it >> 1) & 1, a.status))) break;
-            tc_fence_after();
-            // pass 1: S_c = dec S_{c-1} + scl H^T_c over the buffer of chunk c
-            for (int k = 0; k < NK; ++k) {
-                const uint32_t cur = tmem + lane_base + (uint32_t)b * NR + (NR / 2) * e + 32 * k;
-                float h[32], p[32];
-                tmem_ld32(cur, h);
-                if (it > 0) tmem_ld32(tmem + lane_base + (uint32_t)(1 - b) * NR + (NR / 2) * e + 32 * k, p);
-                else initial_rows(k, p);
+            // one warp waits, the others sleep on the named barrier, and all take its outcome
+            // (every epilogue thread must reach the same named barriers)
+            if (!(ok = group_wait(smem_u32(&bar_hfull[b][0]), (uint32_t)(it >> 1) & 1, a.status, warp == WARP_EPI, 2,
+                                  NEPI, eflags, kg, &abort_s)))
+                break;
+            if (!(ok = group_wait(smem_u32(&bar_hfull[b][1]), (uint32_t)(it >> 1) & 1, a.status, warp == WARP_EPI, 2,
+                                  NEPI, eflags, kg, &abort_s)))
+                break;
+            // S_c = dec S_{c-1} + scale H_c
+            const uint32_t cur = tmem + lane_base + (uint32_t)(2 * b + mb) * ACC;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) h[i] = fmaf(dec, p[i], scl * h[i]);
-                tmem_st32(cur, h);
+            for (int k = 0; k < 4; ++k) {
+                float h[16];
+                tmem_ld16(cur + 16 * k, h);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) S[16 * k + i] = fmaf(dec, S[16 * k + i], zm * h[i]);
             }
-            tmem_wait_st();
+            {
+                float h[16];
+                tmem_ld16(cur + 64, h);
+                S[64] = fmaf(dec, S[64], zm * zfix * h[0]);
+            }
             tc_fence_before();
-            mbar_arrive(smem_u32(&bar_dfree[(it + 1) & 1]));   // the previous buffer has been read
+            mbar_arrive(smem_u32(&bar_dfree[b][mb]));   // accumulator (b, mb) has been read
             if (rev) gam = it == 0 ? zm : fmaxf(gam, zm);
-            // pass 2: export the state of slot c + 1 (forward) / c - 1 (reverse)
+            // export the state of slot c + 1 (forward) / c - 1 (reverse)
             const int slot = rev ? c - 1 : c + 1;
             if (slot >= 0 && slot < NC) {
-                if (a.sscale && Q == 0 && warp == 8 && lane == 0) a.sscale[bh * NC + slot] = gam;
-                for (int k = 0; k < NK; ++k) {
-                    float v[32];
-                    tmem_ld32(tmem + lane_base + (uint32_t)b * NR + (NR / 2) * e + 32 * k, v);
-                    export_rows(slot, k, v);
-                }
+                if (a.sscale && lead && Q == 0) a.sscale[bh * NC + slot] = gam;
+                stage_begin();
+                export_row(slot);
             }
-            if (!rev && it == nchunks - 1 && (a.S_final || a.z_final)) {
-                for (int k = 0; k < NK; ++k) {
-                    float v[32];
-                    tmem_ld32(tmem + lane_base + (uint32_t)b * NR + (NR / 2) * e + 32 * k, v);
-                    const long rbase = row0 + 32 * k;
-                    const float inv_unit = 1.f / unit;   // exact: a power of two
-                    if (zwarp) {
-                        const float zv = gather_lane(v, 0);
-                        if (a.z_final) a.z_final[bh * 4096 + rbase + lane] = zv * inv_unit;
-                    } else if (a.S_final) {
+            if (!rev && it == nchunks - 1) {
+                const float iu = 1.f / unit_v;   // exact: a power of two
+                if (a.S_final) {
+                    float4* dst = reinterpret_cast<float4*>(a.S_final + (bh * 4096 + R) * 64);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) a.S_final[(bh * 4096 + rbase + i) * 64 + col] = v[i] * inv_unit;
-                    }
+                    for (int q4 = 0; q4 < 16; ++q4)
+                        dst[q4] = make_float4(S[4 * q4] * iu, S[4 * q4 + 1] * iu, S[4 * q4 + 2] * iu, S[4 * q4 + 3] * iu);
                 }
+                if (a.z_final) a.z_final[bh * 4096 + R] = S[64] / unit_z;
             }
         }
+        if (lead) bulk_wait_all();
         if (!ok) abort_s = 1;
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, TCOLS);
+    if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
 cudaError_t tc_state_scan(const Problem& p, const ScanIO& io, cudaStream_t s) {
@@ -388,16 +413,20 @@ cudaError_t tc_state_scan(const Problem& p, const ScanIO& io, cudaStream_t s) {
     const uint64_t strides[2] = {128, (uint64_t)TC_OPS_ROWS * 128};
     const uint32_t box[3] = {64, (uint32_t)TC_OPS_ROWS, 1};
     if (!make_tmap_f16_nd(&tops, io.ops, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    CUtensorMap tsx;   // the state planes as (64 columns, 4096 rows, BH x NC x 2 planes), 256-row boxes
+    const uint64_t sdims[3] = {64, 4096, BH * (uint64_t)p.NC * 2};
+    const uint64_t sstrides[2] = {128, 4096 * 128};
+    const uint32_t sbox[3] = {64, (uint32_t)NR, 1};
+    if (!make_tmap_f16_nd(&tsx, io.Sx, 3, sdims, sstrides, sbox)) return cudaErrorInvalidValue;
     int* status = tc_status_ptr();
     if (!status) return cudaErrorInvalidValue;
     if (!io.amax) return cudaErrorInvalidValue;
     Args a{io.g, io.zmax, io.S0, io.z0, (__half*)io.Sx, io.zx, io.sscale, io.S_final, io.z_final, io.amax, status,
            p.T, p.NC, (int)p.Tp(), io.rev ? 1 : 0};
-    constexpr int NR = NR_ROWS, SMEM = smem_bytes(NR);
-    cudaError_t e = cudaFuncSetAttribute(tc_state_scan_kernel<NR>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    cudaError_t e = cudaFuncSetAttribute(tc_state_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     dim3 grid(4096 / NR, (unsigned)p.BH());
-    tc_state_scan_kernel<NR><<<grid, THREADS, SMEM, s>>>(tops, a);
+    tc_state_scan_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(tops, tsx, a);
     return cudaGetLastError();
 }
 
