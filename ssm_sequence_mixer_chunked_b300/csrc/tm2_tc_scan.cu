@@ -72,13 +72,14 @@ namespace tcscan {
 constexpr int C = TC_CHUNK;     // chunk length
 constexpr int KS = 64;          // tokens per stage (one TMA request)
 constexpr int SPC = C / KS;     // stages per chunk
-constexpr int NSLOT = 4;        // ring slots, one stage each
+constexpr int NSLOT = 8;        // ring slots, one stage each
 constexpr int SLOT = TC_OPS_ROWS * 128;   // [Kt 64 rows | value^T 64 rows | normaliser row | 15 zero rows]
 constexpr int NR = 256;         // state rows per CTA (two M-blocks of 128)
 constexpr int NV = 80;          // accumulator columns: 64 value columns, the normaliser, 15 zero
-constexpr uint32_t ACC = 80;    // accumulator of chunk buffer b, M-block mb at column (2 b + mb) ACC
-constexpr uint32_t TM_A = 320;  // key-product buffer x (32 tokens) at TM_A + 64 x: [mb][hi, lo], 16 columns each
-constexpr int NAB = 3;          // key-product buffers
+constexpr int NACCB = 2;        // accumulator buffers per M-block (chunk it uses buffer it % NACCB)
+constexpr uint32_t ACC = 80;    // accumulator of buffer b, M-block mb at column (2 b + mb) ACC
+constexpr uint32_t TM_A = 2 * NACCB * ACC;   // key-product buffer x (32 tokens) at TM_A + 64 x: [mb][hi, lo]
+constexpr int NAB = (512 - (int)TM_A) / 64;  // key-product buffers (5 with one accumulator buffer)
 constexpr int HT = 32;          // tokens per key-product buffer
 constexpr int SMEM_STG = NSLOT * SLOT;   // export staging: hi, lo planes [256 rows][128 B], 128B-swizzled
 constexpr int SMEM_BYTES = SMEM_STG + 2 * 32768 + 1024;
@@ -88,7 +89,7 @@ constexpr int WARP_TMA = 8, WARP_MMA = 9, WARP_EPI = 11;   // issuers: warps 9 (
 constexpr int THREADS = 19 * 32;
 constexpr uint32_t IDESC = idesc_f16_f32(128, NV, false, false);
 static_assert(TC_OPS_ROWS - 64 == NV, "the operand block's rows 64.. are the N = 80 operand");
-static_assert(3 * ACC + NV <= TM_A && TM_A + 64 * NAB <= 512, "tensor memory layout");
+static_assert(NAB >= 3 && TM_A + 64 * NAB <= 512, "tensor memory layout");
 
 struct Args {
     const float* g;       // [BH][NC] chunk totals
@@ -122,8 +123,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
                                                                    const __grid_constant__ Args a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_align1024(smem_raw);
-    __shared__ __align__(8) uint64_t bar_full[NSLOT], bar_afull[NAB], bar_hsdone[NAB], bar_hfull[2][2],
-        bar_dfree[2][2], bar_done[2];
+    __shared__ __align__(8) uint64_t bar_full[NSLOT], bar_afull[NAB], bar_hsdone[NAB], bar_hfull[NACCB][2],
+        bar_dfree[NACCB][2], bar_done[2];
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_s;
     __shared__ volatile int eflags[2];   // group waits of the epilogue warps
@@ -142,8 +143,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
             mbar_init(smem_u32(&bar_afull[i]), NBUILD);
             mbar_init(smem_u32(&bar_hsdone[i]), 2);   // both issuers' MMAs of the half stage are done
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(smem_u32(&bar_done[i]), 1);
+        for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&bar_done[i]), 1);
+        for (int i = 0; i < NACCB; ++i) {
             for (int mb = 0; mb < 2; ++mb) {
                 mbar_init(smem_u32(&bar_hfull[i][mb]), 1);
                 mbar_init(smem_u32(&bar_dfree[i][mb]), NEPI / 2);
@@ -194,10 +195,10 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
         if (lane == 0) {
             bool ok = true;
             for (int it = 0; it < nchunks && ok; ++it) {
-                const int b = it & 1;
-                // accumulator b was last read by the fold of chunk it - 2
-                if (it >= 2 &&
-                    !(ok = mbar_wait(smem_u32(&bar_dfree[b][mb]), (uint32_t)((it - 2) >> 1) & 1, a.status)))
+                const int b = it % NACCB;
+                // accumulator b was last read by the fold of chunk it - NACCB
+                if (it >= NACCB &&
+                    !(ok = mbar_wait(smem_u32(&bar_dfree[b][mb]), (uint32_t)((it - NACCB) / NACCB) & 1, a.status)))
                     break;
                 const uint32_t d = tmem + (uint32_t)(2 * b + mb) * ACC;
                 for (int s = 0; s < SPC && ok; ++s) {
@@ -352,15 +353,15 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
         bool ok = true;
         int kg = 0;   // group-wait counter
         for (int it = 0; it < nchunks && ok; ++it) {
-            const int c = chunk_of(it), b = it & 1;
+            const int c = chunk_of(it), b = it % NACCB;
             const float dec = __expf(a.g[bh * NC + c]);
             const float zm = rev ? a.zmax[bh * NC + c] : 1.f;
             // one warp waits, the others sleep on the named barrier, and all take its outcome
             // (every epilogue thread must reach the same named barriers)
-            if (!(ok = group_wait(smem_u32(&bar_hfull[b][0]), (uint32_t)(it >> 1) & 1, a.status, warp == WARP_EPI, 2,
+            if (!(ok = group_wait(smem_u32(&bar_hfull[b][0]), (uint32_t)(it / NACCB) & 1, a.status, warp == WARP_EPI, 2,
                                   NEPI, eflags, kg, &abort_s)))
                 break;
-            if (!(ok = group_wait(smem_u32(&bar_hfull[b][1]), (uint32_t)(it >> 1) & 1, a.status, warp == WARP_EPI, 2,
+            if (!(ok = group_wait(smem_u32(&bar_hfull[b][1]), (uint32_t)(it / NACCB) & 1, a.status, warp == WARP_EPI, 2,
                                   NEPI, eflags, kg, &abort_s)))
                 break;
             // S_c = dec S_{c-1} + scale H_c
