@@ -15,13 +15,15 @@
 //
 // One CTA per (128-key tile, chunk, b, h).  The inter-chunk sums run first, over 16 groups of
 // four state slices n = 4g .. 4g+3, each one TMA box per plane ([n'][m][col], fp16 hi and
-// residual planes):
-//   U'_g[j][(n', m)]   = sum_col v_j[col] dS[(m, 4g+n'), col]   (N = 256, the box K-major)
-//   U_g[j][(n', col)]  = sum_m   k_j[m]   dS[(m, 4g+n'), col]   (N = 256, the box MN-major)
-// in the two halves of tensor memory, and the compute warps fold them into fp32 registers,
-// dkx[m] += k_j[4g+n'] U'_g, dvx[col] += k_j[4g+n'] U_g.  A tensor-core instruction costs about
-// the same for any N up to 256, so four slices per instruction keeps this part short.
-// A 17th product U'_z = K dzm^T (dzm[m][n] = dz[(m,n)]) adds the normaliser column.
+// residual planes), as one product per group,
+//   U_g[j][(n', col)]  = sum_m k_j[m] dS[(m, 4g+n'), col]     (N = 256, the box MN-major),
+// double-buffered in tensor memory.  dS is symmetric in (m, n), so U_g also carries the key
+// term: the compute warps fold it into dvx[col] += k_j[4g+n'] U_g[j][(n', col)] (registers)
+// and sum_col v_j[col] U_g[j][(n', col)] into the dk sum of key index 4g+n' (shared memory,
+// each column half adding its share).  One product instead of a second, V-side chain halves
+// the tensor work of this part.  A 17th product U'_z = K dzm^T (dzm[m][n] = dz[(m,n)]) adds
+// the normaliser column; its tiles are built in the ring slot of the last group's residual
+// plane once that group's product is done.
 // The gradient state planes and normaliser states carry the reverse scan's operand scales
 // ks^2 vs (exact powers of two) on top of 1/Gamma_c; the inter-chunk terms are divided by
 // them together with the multiplication by Gamma_c.
@@ -50,16 +52,18 @@ constexpr int NREQ = 2 * NG + 3;              // hi/lo plane of each group, then
 constexpr int EARLY = NR - 1;                 // slot NR-1 first holds the K and V tiles for conversion
 // shared memory
 constexpr int RING = 0;
-constexpr int SKH = NR * RB, SVH = SKH + 16384;      // fp16 copies of the K and V tiles [128][64]
-constexpr int SZH = SVH + 16384, SZL = SZH + 8192;   // normaliser gradient matrix hi / lo
-constexpr int SAV = SZL + 8192;                      // A, zeta, ucol: 3 x 256 floats
+constexpr int SKH = NR * RB;                         // fp16 copy of the K tile [128][64] (A operand of U)
+constexpr int SDK = SKH + 16384;                     // inter-chunk sums of dk [64 m][128 rows] fp32
+constexpr int SAV = SDK + 32768;                     // A, zeta, ucol: 3 x 256 floats
+// the normaliser gradient matrix (hi, lo [64][64] fp16) goes into the ring slot of group NG-1's
+// lo plane, which no later request uses, once that group's products are done
+constexpr int ZREQ = 2 * NG - 1;
+static_assert(ZREQ + NR >= NREQ, "no later request may reuse the normaliser slot");
 constexpr int SRED = SAV + 3072;                     // 128 partial sums
 constexpr int BYTES = SRED + 1024 + 1024;
-// tensor memory: U' in [0, 256), U in [256, 512); the intra part reuses both afterwards
-constexpr uint32_t TM_UP = 0, TM_U = 256;
+// tensor memory: U of group g in buffer (g & 1) at 256 (g & 1); the intra part reuses it afterwards
 constexpr uint32_t TM_DK = 0, TM_DV = 64, TM_S = 128, TM_W = 192, TM_DH = 256, TM_DL = 288, TM_WH = 320, TM_WL = 352;
 constexpr uint32_t TM_PARK = 384;             // inter-chunk sums parked during the intra part: 384 + 64h
-constexpr uint32_t IDESC_UP = idesc_f16_f32(128, 256, false, false);
 constexpr uint32_t IDESC_U = idesc_f16_f32(128, 256, false, true);
 constexpr uint32_t IDESC_Z = idesc_f16_f32(128, 64, false, false);
 constexpr uint32_t IDESC_BF_K = idesc_bf16_f32(128, 64, false, false);
@@ -98,7 +102,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_align1024(smem_raw);
     __shared__ __align__(8) uint64_t bar_ld, bar_full[NR], bar_empty[NR], bar_cvt, bar_sfull[4], bar_sfree[4],
-        bar_pfull[4], bar_ufull[2], bar_uempty[2], bar_kvfull, bar_red, bar_done;
+        bar_pfull[4], bar_ufull[2], bar_uempty[2], bar_kvfull, bar_red, bar_zrdy, bar_done;
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_s;
     __shared__ volatile int gflags[2];         // group waits of the compute warps
@@ -131,6 +135,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
         }
         mbar_init(smem_u32(&bar_kvfull), 1);
         mbar_init(smem_u32(&bar_red), 256);
+        mbar_init(smem_u32(&bar_zrdy), 256);
         mbar_init(smem_u32(&bar_done), 1);
         abort_s = 0;
         fence_mbar_init();
@@ -192,55 +197,48 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
         if (lane == 0) {
             bool ok = mbar_wait(smem_u32(&bar_cvt), 0, a.status);
             tc_fence_after();
-            // ---- inter-chunk: U'_g = V B_g^T (K-major view), U_g = K B_g (MN-major view), then U'_z
+            // ---- inter-chunk: U_g = K B_g (MN-major view of the group's box, hi + lo plane) into
+            // buffer g & 1, then U'_z = K dzm^T
             for (int g = 0; g <= NG && ok; ++g) {
+                const int ub = g & 1;
+                const uint32_t k = (uint32_t)(g >> 1);
                 if (abort_s) { ok = false; break; }
                 if (g < NG) {
                     const int r0 = 2 * g, r1 = 2 * g + 1;
                     if (!(ok = mbar_wait(smem_u32(&bar_full[slot_of(r0)]), use_of(r0) & 1, a.status))) break;
                     if (!(ok = mbar_wait(smem_u32(&bar_full[slot_of(r1)]), use_of(r1) & 1, a.status))) break;
                 }
-                if (g > 0 && !(ok = mbar_wait(smem_u32(&bar_uempty[0]), (uint32_t)(g - 1) & 1, a.status))) break;
+                if (k > 0 && !(ok = mbar_wait(smem_u32(&bar_uempty[ub]), (k - 1) & 1, a.status))) break;
                 tc_fence_after();
+                const uint32_t d = tmem + ub * 256;
                 if (g < NG) {
                     const uint32_t bhi = sb0 + RING + slot_of(2 * g) * RB, blo = sb0 + RING + slot_of(2 * g + 1) * RB;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        umma_bf16(tmem + TM_UP, sdesc_sw128(sb0 + SVH + kk * 32), sdesc_sw128(bhi + kk * 32), IDESC_UP,
+                        umma_bf16(d, sdesc_sw128(sb0 + SKH + kk * 32), sdesc_sw128_ex(bhi + kk * 2048, 8192, 1024), IDESC_U,
                                   kk > 0);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        umma_bf16(tmem + TM_UP, sdesc_sw128(sb0 + SVH + kk * 32), sdesc_sw128(blo + kk * 32), IDESC_UP,
+                        umma_bf16(d, sdesc_sw128(sb0 + SKH + kk * 32), sdesc_sw128_ex(blo + kk * 2048, 8192, 1024), IDESC_U,
                                   1u);
-                    umma_commit(smem_u32(&bar_ufull[0]));
-                    if (g > 0 && !(ok = mbar_wait(smem_u32(&bar_uempty[1]), (uint32_t)(g - 1) & 1, a.status))) break;
-                    tc_fence_after();
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        umma_bf16(tmem + TM_U, sdesc_sw128(sb0 + SKH + kk * 32),
-                                  sdesc_sw128_ex(bhi + kk * 2048, 8192, 1024), IDESC_U, kk > 0);
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        umma_bf16(tmem + TM_U, sdesc_sw128(sb0 + SKH + kk * 32),
-                                  sdesc_sw128_ex(blo + kk * 2048, 8192, 1024), IDESC_U, 1u);
                     umma_commit(smem_u32(&bar_empty[slot_of(2 * g)]));
                     umma_commit(smem_u32(&bar_empty[slot_of(2 * g + 1)]));
-                    umma_commit(smem_u32(&bar_ufull[1]));
                 } else {
+                    if (!(ok = mbar_wait(smem_u32(&bar_zrdy), 0, a.status))) break;   // normaliser tiles built
+                    tc_fence_after();
+                    const uint32_t zh = sb0 + RING + slot_of(ZREQ) * RB, zl = zh + 8192;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        umma_bf16(tmem + TM_UP, sdesc_sw128(sb0 + SKH + kk * 32), sdesc_sw128(sb0 + SZH + kk * 32),
-                                  IDESC_Z, kk > 0);
-                        umma_bf16(tmem + TM_UP, sdesc_sw128(sb0 + SKH + kk * 32), sdesc_sw128(sb0 + SZL + kk * 32),
-                                  IDESC_Z, 1u);
+                        umma_bf16(d, sdesc_sw128(sb0 + SKH + kk * 32), sdesc_sw128(zh + kk * 32), IDESC_Z, kk > 0);
+                        umma_bf16(d, sdesc_sw128(sb0 + SKH + kk * 32), sdesc_sw128(zl + kk * 32), IDESC_Z, 1u);
                     }
-                    umma_commit(smem_u32(&bar_ufull[0]));
                 }
+                umma_commit(smem_u32(&bar_ufull[ub]));
             }
             // ---- intra-chunk: dk += (dSs^T) Q, dv += (W zeta)^T dO over the 64-query blocks
             const int rkv = 2 * NG, rq = 2 * NG + 1, rd = 2 * NG + 2;
-            if (ok) ok = mbar_wait(smem_u32(&bar_uempty[0]), (uint32_t)NG & 1, a.status);          // U'_z read
-            if (ok) ok = mbar_wait(smem_u32(&bar_uempty[1]), (uint32_t)(NG - 1) & 1, a.status);    // last U read
+            if (ok) ok = mbar_wait(smem_u32(&bar_uempty[0]), (uint32_t)(NG >> 1) & 1, a.status);          // U'_z read
+            if (ok) ok = mbar_wait(smem_u32(&bar_uempty[1]), (uint32_t)((NG - 1) >> 1) & 1, a.status);    // last U read
             if (ok) ok = mbar_wait(smem_u32(&bar_full[slot_of(rkv)]), use_of(rkv) & 1, a.status);
             if (ok) ok = mbar_wait(smem_u32(&bar_full[slot_of(rq)]), use_of(rq) & 1, a.status);
             if (ok) ok = mbar_wait(smem_u32(&bar_full[slot_of(rd)]), use_of(rd) & 1, a.status);
@@ -293,75 +291,86 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
         const float gsc = a.sscale[bh * NC + c];
         const float gcv = a.g[bh * NC + c];
         const float rowt = in ? a.rowterm[bh * a.T + tok] : 0.f;
-        float4 zr[4];
-        z_tiles_load(a.dzx + (bh * NC + c) * 4096, threadIdx.x, zr);
+        float* sDK = reinterpret_cast<float*>(smem + SDK);   // [m][row]: sum_col v_j[col] U[(m, col)]
+#pragma unroll
+        for (int m = 0; m < 32; ++m) sDK[(32 * h + m) * 128 + l] = 0.f;
+        float vj[32];   // this row's value columns 32h .. 32h + 31 (fp32)
         bool ok = mbar_wait(smem_u32(&bar_ld), 0, a.status);
-        if (ok) {   // fp16 copies of the key and value tiles; the normaliser gradient matrix / scale
+        if (ok) {   // fp16 copy of the key tile (the A operand of U); this row's values
             const int t256 = threadIdx.x;
-            for (int pc = t256; pc < 1024; pc += 256) {
-                tile_bf16_to_f16(early, sb0 + SKH, pc);
-                tile_bf16_to_f16(early + 16384, sb0 + SVH, pc);
+            for (int pc = t256; pc < 1024; pc += 256) tile_bf16_to_f16(early, sb0 + SKH, pc);
+#pragma unroll
+            for (int c8 = 0; c8 < 4; ++c8) {
+                uint32_t x[4];
+                asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                             : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3])
+                             : "r"(early + 16384 + swz_elem(l, 32 * h + 8 * c8)));
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    vj[8 * c8 + 2 * u] = __uint_as_float(x[u] << 16);
+                    vj[8 * c8 + 2 * u + 1] = __uint_as_float(x[u] & 0xffff0000u);
+                }
             }
-            z_tiles_store(smem + SZH, smem + SZL, zr, 1.f / gsc, t256);
             fence_proxy_async();
         }
         mbar_arrive(smem_u32(&bar_cvt));
-        // ---- inter-chunk groups
-        float dkx[32], dvx[32];
+        // ---- inter-chunk groups: dvx[col] += k_j[n] U[(n, col)]; sDK[n] += sum_col v_j[col] U[(n, col)]
+        // (each column half adds its share; U[(n, col)] = sum_m k_j[m] dS[(m, n), col] and dS is
+        // symmetric in (m, n), so the second sum is the dk term of key index n)
+        float dvx[32];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) dkx[k] = dvx[k] = 0.f;
+        for (int k = 0; k < 32; ++k) dvx[k] = 0.f;
         float dv64x = 0.f;
+        float4 zr[4];
         const uint8_t* krow = smem + SKH;
 #pragma unroll 1
         for (int g = 0; g <= NG && ok; ++g) {
-            if (!(ok = group_wait(smem_u32(&bar_ufull[0]), (uint32_t)g & 1, a.status, warp == 0, 1, 256, gflags, kg,
-                                  &abort_s)))
+            const int ub = g & 1;
+            if (g == NG - 3) z_tiles_load(a.dzx + (bh * NC + c) * 4096, threadIdx.x, zr);   // in flight meanwhile
+            if (!(ok = group_wait(smem_u32(&bar_ufull[ub]), (uint32_t)(g >> 1) & 1, a.status, warp == 0, 1, 256, gflags,
+                                  kg, &abort_s)))
                 break;
+            if (g == NG - 1) {   // group NG-1's products are done: its lo slot takes the normaliser matrix
+                const uint32_t zh = RING + slot_of(ZREQ) * RB;
+                z_tiles_store(smem + zh, smem + zh + 8192, zr, 1.f / gsc, threadIdx.x);
+                fence_proxy_async();
+                mbar_arrive(smem_u32(&bar_zrdy));
+            }
+            const uint32_t ua = tmem + lane_base + ub * 256 + h * 32;
             if (g < NG) {
 #pragma unroll 1
                 for (int np = 0; np < 4; ++np) {
                     float u[32];
-                    tmem_ld32(tmem + lane_base + TM_UP + np * 64 + h * 32, u);
+                    tmem_ld32(ua + np * 64, u);
                     if (np == 3) {
                         tc_fence_before();
-                        mbar_arrive(smem_u32(&bar_uempty[0]));
+                        mbar_arrive(smem_u32(&bar_uempty[ub]));
                     }
                     const float kn = __half2float(*reinterpret_cast<const __half*>(krow + swz_elem(l, 4 * g + np)));
+                    float p = 0.f;
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) dkx[k] = fmaf(kn, u[k], dkx[k]);
-                }
-                if (!(ok = group_wait(smem_u32(&bar_ufull[1]), (uint32_t)g & 1, a.status, warp == 0, 1, 256, gflags, kg,
-                                      &abort_s)))
-                    break;
-#pragma unroll 1
-                for (int np = 0; np < 4; ++np) {
-                    float u[32];
-                    tmem_ld32(tmem + lane_base + TM_U + np * 64 + h * 32, u);
-                    if (np == 3) {
-                        tc_fence_before();
-                        mbar_arrive(smem_u32(&bar_uempty[1]));
+                    for (int k = 0; k < 32; ++k) {
+                        dvx[k] = fmaf(kn, u[k], dvx[k]);
+                        p = fmaf(vj[k], u[k], p);
                     }
-                    const float kn = __half2float(*reinterpret_cast<const __half*>(krow + swz_elem(l, 4 * g + np)));
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) dvx[k] = fmaf(kn, u[k], dvx[k]);
+                    atomicAdd(&sDK[(4 * g + np) * 128 + l], p);
                 }
             } else {
                 float u[32];
-                tmem_ld32(tmem + lane_base + TM_UP + h * 32, u);
+                tmem_ld32(ua, u);
                 tc_fence_before();
-                mbar_arrive(smem_u32(&bar_uempty[0]));
+                mbar_arrive(smem_u32(&bar_uempty[ub]));
 #pragma unroll
                 for (int k = 0; k < 32; ++k) {
-                    dkx[k] += u[k];
+                    atomicAdd(&sDK[(32 * h + k) * 128 + l], u[k]);
                     const float km = __half2float(*reinterpret_cast<const __half*>(krow + swz_elem(l, h * 32 + k)));
                     dv64x = fmaf(km, u[k], dv64x);
                 }
             }
         }
-        // park the inter-chunk sums in tensor memory (outside the intra part's columns), once
-        // every compute warp has read the last U (whose columns these are)
+        // park the inter-chunk value sums in tensor memory (outside the intra part's columns),
+        // once every compute warp has read the last U (whose columns these are)
         named_bar_sync(1, 256);
-        tmem_st32(tmem + lane_base + TM_PARK + h * 64, dkx);
         tmem_st32(tmem + lane_base + TM_PARK + h * 64 + 32, dvx);
         tmem_wait_st();
         // ---- intra-chunk blocks (queries i >= j)
@@ -417,20 +426,17 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
             float dk0[32], dv0[32];
             tmem_ld32(tmem + lane_base + TM_DK + h * 32, dk0);
             tmem_ld32(tmem + lane_base + TM_DV + h * 32, dv0);
-            tmem_ld32(tmem + lane_base + TM_PARK + h * 64, dkx);
             tmem_ld32(tmem + lane_base + TM_PARK + h * 64 + 32, dvx);
             const float wj = __expf(gcv - Aj);
             const float ks = pow2_scale(a.amax[bh * 4]), vs = pow2_scale(a.amax[bh * 4 + 1]);
             const float gu = gsc / (ks * ks * vs);   // Gamma_c out of the planes' units (exact)
             const float fk = 2.f * wj * gu, fv = wj * gu;
             float vdot = 0.f;
-            const uint8_t* vrow = smem + SVH;
 #pragma unroll
             for (int k = 0; k < 32; ++k) {
-                dk0[k] += fk * dkx[k];
+                dk0[k] += fk * sDK[(32 * h + k) * 128 + l];
                 dv0[k] += fv * dvx[k];
-                const float vv = __half2float(*reinterpret_cast<const __half*>(vrow + swz_elem(l, h * 32 + k)));
-                vdot = fmaf(vv, dv0[k], vdot);
+                vdot = fmaf(vj[k], dv0[k], vdot);
             }
             const float part = vdot + dv64_in + fv * dv64x;   // this half's share of Vt_j . dVt_j
             if (h == 1) sRed[l] = part;
