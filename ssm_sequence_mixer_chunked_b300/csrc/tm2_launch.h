@@ -52,12 +52,28 @@ cudaError_t simt_bwd_chunk(const Problem& p, const void* q, const void* k, const
 
 // ---- bf16 tensor-core path (d = dv = 64, chunk TC_CHUNK) ------------------------------
 constexpr int TC_CHUNK = 256;
+// Block-packed chunk states (the forward walk's export, read by the chunk output and dq): the
+// (m, n) index square of the d^2 = 4096 state rows is cut into 16 x 16 blocks and only the 10
+// blocks with bm <= bn are kept, block (bm, bn) at index bm * 4 - bm (bm - 1) / 2 + (bn - bm),
+// its rows ordered r = 16 (m - 16 bm) + (n - 16 bn).  The state is symmetric in (m, n) up to the
+// initial state's antisymmetric part, which no readout sees, so an off-diagonal block is stored
+// doubled (it stands for (m, n) and (n, m)) and a diagonal block as is:
+//   sum_{m,n} x[m] x[n] S[(m,n), :] = sum_{blocks} sum_{(m,n) in block} x[m] x[n] T[(m,n), :].
+// Layout [BH][NC][2 planes][TC_PACKED_ROWS][64] fp16; the normaliser states stay full.
+constexpr int TC_PACKED_BLOCKS = 10;
+constexpr int TC_PACKED_ROWS = TC_PACKED_BLOCKS * 256;
+__host__ __device__ constexpr int tc_block_index(int bm, int bn) { return bm * 4 - bm * (bm - 1) / 2 + (bn - bm); }
+__host__ __device__ inline void tc_block_of(int idx, int& bm, int& bn) {   // inverse of tc_block_index
+    bm = idx < 4 ? 0 : idx < 7 ? 1 : idx < 9 ? 2 : 3;
+    bn = bm + (idx - tc_block_index(bm, bm));
+}
 // Chunk-state scan (tm2_tc_scan.cu).  Forward (rev = false): key = k, val = v, normaliser
 // column 1, weight exp(g_c - A_j); slot c = the state entering chunk c (slot 0 = S0/z0 or
 // zero); S_final/z_final (optional) = the state after the last token.  Reverse (rev = true):
 // key = q, val = dO, normaliser column ucol, weight exp(A_i) zeta_i; slot c = the gradient
 // w.r.t. the state at the end of chunk c, scaled per (slot, CTA) by 1/sscale.
-// Sx: [BH][NC][2][4096][64] fp16 (hi plane, residual plane); zx: [BH][NC][4096] fp32.
+// Sx: forward [BH][NC][2][TC_PACKED_ROWS][64] block-packed, reverse [BH][NC][2][4096][64] fp16
+// (hi plane, residual plane); zx: [BH][NC][4096] fp32 (full layout in both walks).
 struct ScanIO {
     bool rev;
     const void* ops;       // operand blocks from launch_tc_scan_operands

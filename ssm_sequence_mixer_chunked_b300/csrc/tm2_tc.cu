@@ -7,6 +7,7 @@
 #include <mutex>
 
 #include "tm2.h"
+#include "tm2_launch.h"
 #include "tm2_sm100.cuh"
 #include "tm2_tc.h"
 
@@ -75,6 +76,20 @@ bool make_tmap_state_tquads(CUtensorMap* map, const void* base, uint64_t nchunks
     const uint64_t strides[4] = {64 * 128, 128, 4096 * 128, 2 * 4096 * 128};
     const uint32_t box[5] = {64, 64, 4, 1, 1};
     return make_tmap_f16_nd(map, base, 5, dims, strides, box);
+}
+
+bool make_tmap_state_packed_quads(CUtensorMap* map, const void* base, uint64_t nchunks) {
+    const uint64_t dims[4] = {64, 16, (uint64_t)TC_PACKED_BLOCKS * 16, 2 * nchunks};
+    const uint64_t strides[3] = {128, 16 * 128, (uint64_t)TC_PACKED_ROWS * 128};
+    const uint32_t box[4] = {64, 16, 4, 1};
+    return make_tmap_f16_nd(map, base, 4, dims, strides, box);
+}
+
+bool make_tmap_state_packed_blocks(CUtensorMap* map, const void* base, uint64_t nchunks) {
+    const uint64_t dims[3] = {64, (uint64_t)TC_PACKED_ROWS, 2 * nchunks};
+    const uint64_t strides[2] = {128, (uint64_t)TC_PACKED_ROWS * 128};
+    const uint32_t box[3] = {64, 256, 1};
+    return make_tmap_f16_nd(map, base, 3, dims, strides, box);
 }
 
 bool make_tmap_f16_nd(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,

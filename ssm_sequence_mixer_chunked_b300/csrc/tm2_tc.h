@@ -28,6 +28,13 @@ bool make_tmap_f16_nd(CUtensorMap* map, const void* base, int rank, const uint64
 // make_tmap_state_tquads the transposed slices n = 4g .. 4g+3 (smem [n'][m][col],
 // coordinates (0, 0, 4g, plane, chunk)).
 bool make_tmap_state_quads(CUtensorMap* map, const void* base, uint64_t nchunks);
+// Block-packed states (TC_PACKED_ROWS rows per plane): four rows m' = 4 mq .. 4 mq + 3 of one
+// 16 x 16 block, all its 16 columns n' (smem [m'][n'][col], 8 KB).  Coordinates
+// (0, 0, 16 block + 4 mq, 2 chunk + plane).
+bool make_tmap_state_packed_quads(CUtensorMap* map, const void* base, uint64_t nchunks);
+// One whole block plane of the block-packed states as [256 rows][64] (32 KB), rows r = 16 m' + n'.
+// Coordinates (0, 256 block, 2 chunk + plane).
+bool make_tmap_state_packed_blocks(CUtensorMap* map, const void* base, uint64_t nchunks);
 bool make_tmap_state_tquads(CUtensorMap* map, const void* base, uint64_t nchunks);
 
 // Reads (and optionally clears) the device status word of the current device.

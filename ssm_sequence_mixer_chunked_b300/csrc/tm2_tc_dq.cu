@@ -8,14 +8,17 @@
 //   dq_i[m] = sum_j dSs_ij k_j[m]
 //           + 2 exp(A_i) zeta_i sum_n q_i[n] ( sum_col dO_i[col] S[(m,n), col] + ucol_i z[(m,n)] ).
 //
-// One CTA per (128-token tile, chunk, b, h).  The inter-chunk sum runs first, over 16 groups
-// of four state slices: U_g[i][(n', m)] = sum_col dO_i[col] S[(m, 4g + n'), col] is one
-// tcgen05.mma of N = 256 per K step and plane (the state as two fp16 planes, hi and residual;
-// dO exact in fp16), and the compute warps fold U into fp32 registers,
-// dqx[m] += q_i[4g + n'] U_g[i][(n', m)].  A tensor-core instruction costs about the same
-// for any N up to 256, so four slices per instruction is what keeps this part short; the
-// slices arrive one plane of one group (32 KB) per TMA request.  A 17th product
-// U_z = Q zm^T (zm[m][n] = z[(m, n)]) carries the normaliser column.
+// One CTA per (128-token tile, chunk, b, h).  The inter-chunk sum runs first, over the 10 blocks
+// of the block-packed forward state (tm2_launch.h: the 16 x 16 blocks bm <= bn of the (m, n)
+// index square, off-diagonal ones doubled): V_b[i][(m', n')] = sum_col dO_i[col] T_b[(m', n'),
+// col] is one tcgen05.mma of N = 256 per K step and plane (the block plane K-major straight
+// from its 32 KB TMA box; dO exact in fp16), and the compute warps fold it into fp32 registers
+// on both sides, dqx[16 bm + m'] += q_i[16 bn + n'] V and dqx[16 bn + n'] += q_i[16 bm + m'] V,
+// which over all blocks is 2 sum_n q_i[n] sum_col dO_i[col] S[(m, n), col] with 62.5% of the
+// full state's products and bytes.  A tensor-core instruction costs about the same for any N up
+// to 256, so a whole block per instruction is what keeps this part short.  An 11th product
+// U_z = Q zm^T (zm[m][n] = z[(m, n)], the normaliser state, full layout) carries the
+// normaliser column.
 // The state planes hold ks^2 vs S and the normaliser state ks^2 z (the forward scan's operand
 // scales, exact powers of two): the normaliser matrix is built times vs, so that both inter-chunk
 // terms carry ks^2 vs, and their sum is divided by it at the end.
@@ -38,8 +41,8 @@ constexpr int THREADS = 10 * 32;
 constexpr int WARP_TMA = 8, WARP_MMA = 9;
 constexpr int NR = 6;                         // ring slots of 32 KB
 constexpr int RB = 32768;
-constexpr int NG = 16;                        // groups of four state slices
-constexpr int NREQ = 2 * NG + 3;              // hi/lo plane of each group, then Q|dO, K, V (intra part)
+constexpr int NG = TC_PACKED_BLOCKS;          // state blocks (block-packed layout), one product each
+constexpr int NREQ = 2 * NG + 3;              // hi/lo plane of each block, then Q|dO, K, V (intra part)
 constexpr int EARLY = NR - 1;                 // slot NR-1 first holds the Q and dO tiles for conversion
 // shared memory
 constexpr int RING = 0;
@@ -156,7 +159,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_cons
                 const uint32_t fb = smem_u32(&bar_full[sl]), dst = sb0 + RING + sl * RB;
                 mbar_arrive_expect_tx(fb, RB);
                 if (r < 2 * NG) {
-                    tma_load_5d(dst, &tmS, fb, 0, 0, 4 * (r >> 1), r & 1, chunk_id);
+                    tma_load_3d(dst, &tmS, fb, 0, 256 * (r >> 1), 2 * chunk_id + (r & 1));
                 } else if (r == 2 * NG) {
                     tma_load_3d(dst, &tmQ, fb, 0, c * C + it * 128, (int)bh);
                     tma_load_3d(dst + 16384, &tmD, fb, 0, c * C + it * 128, (int)bh);
@@ -278,44 +281,86 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_cons
             fence_proxy_async();
         }
         mbar_arrive(smem_u32(&bar_cvt));
-        // ---- inter-chunk: dqx[m] += q_i[n] U[i][(n, m)]  (U_z: ucol_i U_z[i][m])
+        // ---- inter-chunk: dqx[m] = 2 sum_n q_i[n] (G_i + ucol_i z)[(m, n)], G_i = dO_i . S[(m, n), :],
+        // for this thread's half of m (32 h .. 32 h + 31), from the block products
+        // V_b[i][(m', n')] = dO_i . T_b[(m', n'), :] of the block-packed state (T_b = S on the
+        // diagonal blocks, 2 S off it): block (bm, bn) adds q_i[n] V to dqx[m] (its rows) and
+        // q_i[m] V to dqx[n] (its columns, the mirror (n, m)); a diagonal block holds both orders,
+        // so both sums together give its 2 sum_n.  A half reads a block when either side is in its
+        // range.  (S is symmetric: the backward has no initial state.)
         float dqx[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k) dqx[k] = 0.f;
         const uint8_t* qrow = smem + SQH;
+        auto qv = [&](int col) { return __half2float(*reinterpret_cast<const __half*>(qrow + swz_elem(l, col))); };
 #pragma unroll 1
         for (int g = 0; g <= NG && ok; ++g) {
             const int ub = g & 1;
             if (!(ok = group_wait(smem_u32(&bar_ufull[ub]), (uint32_t)(g >> 1) & 1, a.status, warp == 0, 1, 256, gflags,
                                   kg, &abort_s)))
                 break;
-            if (g == NG - 2) {   // group NG-2's products are done: its lo slot takes the normaliser matrix
+            if (g == NG - 2) {   // block NG-2's products are done: its lo slot takes the normaliser matrix
                 const uint32_t zh = RING + slot_of(ZREQ) * RB;
                 z_tiles_store(smem + zh, smem + zh + 8192, zr, vs, threadIdx.x);
                 fence_proxy_async();
                 mbar_arrive(smem_u32(&bar_zrdy));
             }
-            const uint32_t ua = tmem + lane_base + ub * 256 + h * 32;
+            const uint32_t ub_base = tmem + lane_base + ub * 256;
             if (g < NG) {
-#pragma unroll 1
-                for (int np = 0; np < 4; ++np) {
-                    float u[32];
-                    tmem_ld32(ua + np * 64, u);
-                    if (np == 3) {
+                int bm, bn;
+                tc_block_of(g, bm, bn);
+                const bool side_m = (bm >> 1) == h, side_n = (bn >> 1) == h;
+                if (!side_m && !side_n) {   // neither side in this half's range
+                    tc_fence_before();
+                    mbar_arrive(smem_u32(&bar_uempty[ub]));
+                    continue;
+                }
+                float qn[16], rm[16], rn[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    qn[k] = qv(16 * bn + k);
+                    rm[k] = rn[k] = 0.f;
+                }
+#pragma unroll
+                for (int mp = 0; mp < 16; ++mp) {   // columns 16 mp .. 16 mp + 15: row m' = mp, all n'
+                    float v[16];
+                    tmem_ld16(ub_base + 16 * mp, v);
+                    if (mp == 15) {
                         tc_fence_before();
                         mbar_arrive(smem_u32(&bar_uempty[ub]));
                     }
-                    const float qn = __half2float(*reinterpret_cast<const __half*>(qrow + swz_elem(l, 4 * g + np)));
+                    const float qm = qv(16 * bm + mp);
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) dqx[k] = fmaf(qn, u[k], dqx[k]);
+                    for (int k = 0; k < 16; ++k) {
+                        rm[mp] = fmaf(qn[k], v[k], rm[mp]);
+                        rn[k] = fmaf(qm, v[k], rn[k]);
+                    }
+                }
+                if (side_m) {
+                    if ((bm & 1) == 0) {
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) dqx[k] += rm[k];
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) dqx[16 + k] += rm[k];
+                    }
+                }
+                if (side_n) {
+                    if ((bn & 1) == 0) {
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) dqx[k] += rn[k];
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) dqx[16 + k] += rn[k];
+                    }
                 }
             } else {
                 float u[32];
-                tmem_ld32(ua, u);
+                tmem_ld32(ub_base + h * 32, u);
                 tc_fence_before();
                 mbar_arrive(smem_u32(&bar_uempty[ub]));
 #pragma unroll
-                for (int k = 0; k < 32; ++k) dqx[k] = fmaf(uc, u[k], dqx[k]);
+                for (int k = 0; k < 32; ++k) dqx[k] = fmaf(2.f * uc, u[k], dqx[k]);
             }
         }
         // ---- intra-chunk blocks
@@ -360,7 +405,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_cons
             float d0[32];
             tmem_ld32(tmem + lane_base + TM_DQ + h * 32, d0);
             if (in) {
-                const float f = 2.f * __expf(Ai);
+                const float f = __expf(Ai);   // dqx already carries the factor 2
 #pragma unroll
                 for (int k = 0; k < 32; ++k) dqx[k] *= un;
                 float g[32];
@@ -383,7 +428,7 @@ cudaError_t tc_bwd_dq(const Problem& p, const void* q, const void* k, const void
     const uint64_t BH = (uint64_t)p.BH(), T = (uint64_t)p.T;
     if (!make_tmap_bf16_3d(&tq, q, BH, T, 64, 128) || !make_tmap_bf16_3d(&td, dO, BH, T, 64, 128) ||
         !make_tmap_bf16_3d(&tk, k, BH, T, 64, 256) || !make_tmap_bf16_3d(&tv, v, BH, T, 64, 256) ||
-        !make_tmap_state_tquads(&ts, Sx, BH * (uint64_t)p.NC))
+        !make_tmap_state_packed_blocks(&ts, Sx, BH * (uint64_t)p.NC))
         return cudaErrorInvalidValue;
     int* status = tc_status_ptr();
     if (!status) return cudaErrorInvalidValue;

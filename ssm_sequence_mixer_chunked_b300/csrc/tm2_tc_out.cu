@@ -7,12 +7,15 @@
 // (written by the chunk-state scan as two fp16 planes, hi and residual, and fp32 z).
 //
 // One CTA per (128-token tile, chunk, b, h).
-//  * Inter-chunk readout first, over 16 groups of four state slices: U_g[i][(m', col)] =
-//    sum_n q_i[n] S[(4g + m', n), col] is one tcgen05.mma of N = 256 per K step and plane
-//    (Q exact in fp16, the slices MN-major straight from their TMA box), and the compute warps
-//    fold it into fp32 registers, N_x[col] += q_i[4g + m'] U_g[i][(m', col)].  A tensor-core
-//    instruction costs about the same for any N up to 256, so four slices per instruction is
-//    what keeps the readout short.  A 17th product U_z = Q zm^T with zm[m][n] = z[(m,n)] gives
+//  * Inter-chunk readout first, over 16 groups of four state rows m = 4g .. 4g + 3 of the
+//    block-packed state (tm2_launch.h: only the 16 x 16 blocks bm <= bn, off-diagonal ones
+//    doubled): U_g[i][(m', col)] = sum_{n >= 16 bm} q_i[n] T[(4g + m', n), col], bm = g / 4,
+//    one tcgen05.mma of N = 256 per 16-key block bn >= bm and plane (Q exact in fp16, the four
+//    rows of each block MN-major straight from their 8 KB TMA box), and the compute warps fold
+//    it into fp32 registers, N_x[col] += q_i[4g + m'] U_g[i][(m', col)]; over all groups this
+//    is sum_{m,n} q_i[m] q_i[n] S[(m,n), col] with 62.5% of the full state's products and
+//    bytes.  A tensor-core instruction costs about the same for any N up to 256, so four rows
+//    per instruction is what keeps the readout short.  A 17th product U_z = Q zm^T with zm[m][n] = z[(m,n)] gives
 //    Z_x = sum_m q_i[m] U_z[i][m].  No operand is a rounded product, so the readout of nearly
 //    orthogonal queries keeps its precision.
 //  * Intra-chunk (causal 128 x 64 key blocks) in the same tensor memory afterwards: s = Q K^T
@@ -150,9 +153,12 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
                     break;
                 }
                 const uint32_t fb = smem_u32(&bar_full[sl]), dst = sb0 + RING + sl * RB;
-                if (r < 2 * NG) {
-                    mbar_arrive_expect_tx(fb, RB);
-                    tma_load_4d(dst, &tmS, fb, 0, (r >> 1) * 256, r & 1, chunk_id);
+                if (r < 2 * NG) {   // rows 4 mq .. 4 mq + 3 of the blocks (bm, bm .. 3) of one plane
+                    const int g = r >> 1, bm = g >> 2, mq = g & 3;
+                    mbar_arrive_expect_tx(fb, (uint32_t)(4 - bm) * 8192);
+                    for (int j = 0; j < 4 - bm; ++j)
+                        tma_load_4d(dst + j * 8192, &tmS, fb, 0, 0, 16 * tc_block_index(bm, bm + j) + 4 * mq,
+                                    2 * chunk_id + (r & 1));
                 } else if (r == 2 * NG) {
                     mbar_arrive_expect_tx(fb, 16384);
                     tma_load_3d(dst, &tmQ, fb, 0, c * C + t * 128, (int)bh);
@@ -185,14 +191,14 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
                 tc_fence_after();
                 const uint32_t d = tmem + ub * 256;
                 if (g < NG) {
+                    // K over the key indices n >= 16 bm only: block (bm, bn) is box j = bn - bm
                     const uint32_t bhi = sb0 + RING + slot_of(2 * g) * RB, blo = sb0 + RING + slot_of(2 * g + 1) * RB;
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        umma_bf16(d, sdesc_sw128(sb0 + SQH + kk * 32), sdesc_sw128_ex(bhi + kk * 2048, 8192, 1024),
-                                  IDESC_U, kk > 0);
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        umma_bf16(d, sdesc_sw128(sb0 + SQH + kk * 32), sdesc_sw128_ex(blo + kk * 2048, 8192, 1024),
+                    const int bm = g >> 2;
+                    for (int j = 0; j < 4 - bm; ++j)
+                        umma_bf16(d, sdesc_sw128(sb0 + SQH + (bm + j) * 32), sdesc_sw128_ex(bhi + j * 8192, 2048, 1024),
+                                  IDESC_U, j > 0);
+                    for (int j = 0; j < 4 - bm; ++j)
+                        umma_bf16(d, sdesc_sw128(sb0 + SQH + (bm + j) * 32), sdesc_sw128_ex(blo + j * 8192, 2048, 1024),
                                   IDESC_U, 1u);
                     umma_commit(smem_u32(&bar_empty[slot_of(2 * g)]));
                     umma_commit(smem_u32(&bar_empty[slot_of(2 * g + 1)]));
@@ -380,7 +386,7 @@ cudaError_t tc_chunk_out(const Problem& p, const void* q, const void* k, const v
     CUtensorMap tq, tk, tv, ts;
     const uint64_t BH = (uint64_t)p.BH();
     if (!make_tmap_bf16_3d(&tq, q, BH, (uint64_t)p.T, 64, 128) || !make_tmap_bf16_3d(&tk, k, BH, (uint64_t)p.T, 64, C) ||
-        !make_tmap_bf16_3d(&tv, v, BH, (uint64_t)p.T, 64, C) || !make_tmap_state_quads(&ts, Sx, BH * (uint64_t)p.NC))
+        !make_tmap_bf16_3d(&tv, v, BH, (uint64_t)p.T, 64, C) || !make_tmap_state_packed_quads(&ts, Sx, BH * (uint64_t)p.NC))
         return cudaErrorInvalidValue;
     int* status = tc_status_ptr();
     if (!status) return cudaErrorInvalidValue;

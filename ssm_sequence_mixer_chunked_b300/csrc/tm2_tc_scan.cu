@@ -104,7 +104,21 @@ struct Args {
     const unsigned* amax; // [BH][4] operand maxima (fp32 bits): key, value, normaliser (reverse)
     int* status;
     int T, NC, Tp, rev;
+    int packed;           // forward only: export the block-packed layout (see tm2_launch.h)
 };
+
+// The state rows of CTA Q.  Full layout: rows r = 64 m' + n of m = 4Q + m', i.e. (m, n) =
+// (4Q + r / 64, r % 64).  Block-packed (the forward walk): CTA Q owns the 16 x 16 block (bm, bn),
+// bm <= bn, Q = tc_block_index(bm, bn), rows r = 16 m' + n', (m, n) = (16 bm + m', 16 bn + n').
+TM2_DEV void row_mn(bool packed, int Q, int bm, int bn, int r, int& m, int& n) {
+    if (packed) {
+        m = 16 * bm + (r >> 4);
+        n = 16 * bn + (r & 15);
+    } else {
+        m = 4 * Q + (r >> 6);
+        n = r & 63;
+    }
+}
 
 TM2_DEV void ld_row_chunks4(uint32_t row_addr, int row, int c0, uint32_t* x) {   // 4 swizzled 16-byte chunks
 #pragma unroll
@@ -136,6 +150,9 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
     const int nchunks = rev ? NC - 1 : NC;   // the reverse walk never needs the update of chunk 0
     const int nstages = nchunks * SPC;
     const uint32_t sbase = smem_u32(smem);
+    const bool packed = a.packed != 0 && !rev;
+    int bm = 0, bn = 0;
+    if (packed) tc_block_of(Q, bm, bn);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NSLOT; ++i) mbar_init(smem_u32(&bar_full[i]), 1);
@@ -238,7 +255,10 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
         // column holds two consecutive tokens (the lower one in the low half), 16 columns per
         // 32 tokens; hi and lo planes.
         const int gp = warp >> 2, quad = warp & 3;
-        const int r0 = quad * 32 + lane, n = r0 & 63, m0 = 4 * Q + (r0 >> 6);
+        const int r0 = quad * 32 + lane;
+        int m0, m1, n;   // the key indices of rows r0 (M-block 0) and r0 + 128 (M-block 1; same n)
+        row_mn(packed, Q, bm, bn, r0, m0, n);
+        row_mn(packed, Q, bm, bn, r0 + 128, m1, n);
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         for (int gs = 0; gs < nstages; ++gs) {
             const int sl = gs % NSLOT;
@@ -256,7 +276,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
             ld_row_chunks4(kt + n * 128, n, 4 * hs, xn);
 #pragma unroll
             for (int mb = 0; mb < 2; ++mb) {
-                const int m = m0 + 2 * mb;
+                const int m = mb ? m1 : m0;
                 uint32_t xm[16], rh[16], rl[16];
                 ld_row_chunks4(kt + m * 128, m, 4 * hs, xm);
 #pragma unroll
@@ -284,7 +304,13 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
         // zero columns), so the MMAs of the next chunk never wait for this fold.
         const int mb = (warp - WARP_EPI) >> 2, quad = warp & 3;
         const int r = mb * 128 + quad * 32 + lane;
-        const long R = (long)Q * NR + r;
+        int m, n;
+        row_mn(packed, Q, bm, bn, r, m, n);
+        const long R = (long)m * 64 + n;          // the row in the full (m, n) layout
+        const long Rm = (long)n * 64 + m;         // its mirror (m, n) -> (n, m)
+        // an off-diagonal block of the packed layout stands for both (m, n) and (n, m): it is
+        // exported doubled, and S0 / S_final / the normaliser carry both rows
+        const bool mirror = packed && bm != bn;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         // units of the running state (see the header): forward value columns ks^2 vs, forward
         // normaliser ks^2; the reverse normaliser column is brought to ks^2 vs by vs / zs
@@ -296,24 +322,33 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
         float gam = 1.f;   // reverse: running max of zmax over the chunks walked so far
 #pragma unroll
         for (int i = 0; i < 65; ++i) S[i] = 0.f;
-        if (!rev) {   // the initial state (forward: S0 / z0 or zero; reverse: zero)
+        if (!rev) {   // the initial state (forward: S0 / z0 or zero; reverse: zero); an off-diagonal
+            // packed row starts from the symmetric part (S0[(m,n)] + S0[(n,m)]) / 2, which is all
+            // that the readouts see; the antisymmetric rest only decays (see S_final below)
+            const float f = mirror ? 0.5f : 1.f;
             if (a.S0) {
                 const float4* src = reinterpret_cast<const float4*>(a.S0 + (bh * 4096 + R) * 64);
+                const float4* srm = reinterpret_cast<const float4*>(a.S0 + (bh * 4096 + Rm) * 64);
 #pragma unroll
                 for (int q4 = 0; q4 < 16; ++q4) {
-                    const float4 x4 = src[q4];
-                    S[4 * q4] = x4.x * unit_v; S[4 * q4 + 1] = x4.y * unit_v;
-                    S[4 * q4 + 2] = x4.z * unit_v; S[4 * q4 + 3] = x4.w * unit_v;
+                    float4 x4 = src[q4];
+                    if (mirror) {
+                        const float4 y4 = srm[q4];
+                        x4.x += y4.x; x4.y += y4.y; x4.z += y4.z; x4.w += y4.w;
+                    }
+                    S[4 * q4] = f * x4.x * unit_v; S[4 * q4 + 1] = f * x4.y * unit_v;
+                    S[4 * q4 + 2] = f * x4.z * unit_v; S[4 * q4 + 3] = f * x4.w * unit_v;
                 }
             }
-            if (a.z0) S[64] = a.z0[bh * 4096 + R] * unit_z;
+            if (a.z0) S[64] = f * (a.z0[bh * 4096 + R] + (mirror ? a.z0[bh * 4096 + Rm] : 0.f)) * unit_z;
         }
+        float dtot = 1.f;   // total decay of the walk so far (for S_final's antisymmetric part)
         // export of the state after a chunk: the values, divided by gam, as hi and residual fp16
         // planes into the swizzled staging rows (one 32 KB TMA store per plane), the normaliser
         // as fp32 straight to zx
         const uint32_t stg = sbase + SMEM_STG;
         auto export_row = [&](int slot) {
-            const float inv = 1.f / gam;
+            const float inv = (mirror ? 2.f : 1.f) / gam;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {   // 16-byte chunk j: columns 8j .. 8j + 7
                 uint32_t hi[4], lo[4];
@@ -331,6 +366,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
                 st_shared_v4(stg + 32768 + off, lo[0], lo[1], lo[2], lo[3]);
             }
             a.zx[(bh * NC + slot) * 4096 + R] = S[64];
+            if (mirror) a.zx[(bh * NC + slot) * 4096 + Rm] = S[64];
             fence_proxy_async();
             named_bar_sync(2, NEPI);   // every row staged
             if (lead) {
@@ -356,6 +392,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
             const int c = chunk_of(it), b = it % NACCB;
             const float dec = __expf(a.g[bh * NC + c]);
             const float zm = rev ? a.zmax[bh * NC + c] : 1.f;
+            dtot *= dec;
             // one warp waits, the others sleep on the named barrier, and all take its outcome
             // (every epilogue thread must reach the same named barriers)
             if (!(ok = group_wait(smem_u32(&bar_hfull[b][0]), (uint32_t)(it / NACCB) & 1, a.status, warp == WARP_EPI, 2,
@@ -389,14 +426,38 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
                 export_row(slot);
             }
             if (!rev && it == nchunks - 1) {
+                // full-layout final state; a mirrored row writes (m, n) and (n, m), each with its
+                // decayed antisymmetric part of S0 restored: +-dtot (S0[(m,n)] - S0[(n,m)]) / 2
                 const float iu = 1.f / unit_v;   // exact: a power of two
                 if (a.S_final) {
                     float4* dst = reinterpret_cast<float4*>(a.S_final + (bh * 4096 + R) * 64);
+                    float4* dsm = reinterpret_cast<float4*>(a.S_final + (bh * 4096 + Rm) * 64);
 #pragma unroll
-                    for (int q4 = 0; q4 < 16; ++q4)
-                        dst[q4] = make_float4(S[4 * q4] * iu, S[4 * q4 + 1] * iu, S[4 * q4 + 2] * iu, S[4 * q4 + 3] * iu);
+                    for (int q4 = 0; q4 < 16; ++q4) {
+                        float4 v4 = make_float4(S[4 * q4] * iu, S[4 * q4 + 1] * iu, S[4 * q4 + 2] * iu,
+                                                S[4 * q4 + 3] * iu);
+                        if (!mirror) {
+                            dst[q4] = v4;
+                            continue;
+                        }
+                        float4 d4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (a.S0) {
+                            const float4 x4 = reinterpret_cast<const float4*>(a.S0 + (bh * 4096 + R) * 64)[q4];
+                            const float4 y4 = reinterpret_cast<const float4*>(a.S0 + (bh * 4096 + Rm) * 64)[q4];
+                            const float hd = 0.5f * dtot;
+                            d4 = make_float4(hd * (x4.x - y4.x), hd * (x4.y - y4.y), hd * (x4.z - y4.z), hd * (x4.w - y4.w));
+                        }
+                        dst[q4] = make_float4(v4.x + d4.x, v4.y + d4.y, v4.z + d4.z, v4.w + d4.w);
+                        dsm[q4] = make_float4(v4.x - d4.x, v4.y - d4.y, v4.z - d4.z, v4.w - d4.w);
+                    }
                 }
-                if (a.z_final) a.z_final[bh * 4096 + R] = S[64] / unit_z;
+                if (a.z_final) {
+                    const float zr = S[64] / unit_z;
+                    float dz = 0.f;
+                    if (mirror && a.z0) dz = 0.5f * dtot * (a.z0[bh * 4096 + R] - a.z0[bh * 4096 + Rm]);
+                    a.z_final[bh * 4096 + R] = zr + dz;
+                    if (mirror) a.z_final[bh * 4096 + Rm] = zr - dz;
+                }
             }
         }
         if (lead) bulk_wait_all();
@@ -414,19 +475,21 @@ cudaError_t tc_state_scan(const Problem& p, const ScanIO& io, cudaStream_t s) {
     const uint64_t strides[2] = {128, (uint64_t)TC_OPS_ROWS * 128};
     const uint32_t box[3] = {64, (uint32_t)TC_OPS_ROWS, 1};
     if (!make_tmap_f16_nd(&tops, io.ops, 3, dims, strides, box)) return cudaErrorInvalidValue;
-    CUtensorMap tsx;   // the state planes as (64 columns, 4096 rows, BH x NC x 2 planes), 256-row boxes
-    const uint64_t sdims[3] = {64, 4096, BH * (uint64_t)p.NC * 2};
-    const uint64_t sstrides[2] = {128, 4096 * 128};
+    const bool packed = !io.rev;   // the forward walk exports the block-packed layout
+    CUtensorMap tsx;   // the state planes as (64 columns, rows, BH x NC x 2 planes), 256-row boxes
+    const uint64_t rows = packed ? (uint64_t)TC_PACKED_ROWS : 4096;
+    const uint64_t sdims[3] = {64, rows, BH * (uint64_t)p.NC * 2};
+    const uint64_t sstrides[2] = {128, rows * 128};
     const uint32_t sbox[3] = {64, (uint32_t)NR, 1};
     if (!make_tmap_f16_nd(&tsx, io.Sx, 3, sdims, sstrides, sbox)) return cudaErrorInvalidValue;
     int* status = tc_status_ptr();
     if (!status) return cudaErrorInvalidValue;
     if (!io.amax) return cudaErrorInvalidValue;
     Args a{io.g, io.zmax, io.S0, io.z0, (__half*)io.Sx, io.zx, io.sscale, io.S_final, io.z_final, io.amax, status,
-           p.T, p.NC, (int)p.Tp(), io.rev ? 1 : 0};
+           p.T, p.NC, (int)p.Tp(), io.rev ? 1 : 0, packed ? 1 : 0};
     cudaError_t e = cudaFuncSetAttribute(tc_state_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    dim3 grid(4096 / NR, (unsigned)p.BH());
+    dim3 grid(packed ? TC_PACKED_BLOCKS : 4096 / NR, (unsigned)p.BH());
     tc_state_scan_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(tops, tsx, a);
     return cudaGetLastError();
 }

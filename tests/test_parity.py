@@ -146,6 +146,35 @@ def test_fwd_bf16_d64_antisymmetric_initial_state():
     assert err(Sf.cpu(), Sf_r) <= 2e-2 and err(zf.cpu(), zf_r) <= 2e-2
 
 
+def test_fwd_bf16_d64_antisymmetric_state_survives():
+    """As above at a = -8 (softplus(-8) = 3.4e-4 per token: the state barely decays over the 600
+    tokens), so the antisymmetric part of S0, z0 is still most of the final state's: the forward
+    walk keeps only the symmetric part in its (m <= n block-packed) running state and restores
+    the decayed antisymmetric part in S_final, z_final."""
+    B, H, T, d = 1, 2, 600, 64
+    pre = si.sequence_inputs(B, H, 300, d, d, dtype="bf16", qkv_std=0.125, seed=16)
+    _, _, S0, z0 = oracle.fwd_recurrent(pre["q"], pre["k"], pre["v"], pre["a"], True)
+    S0 = torch.as_tensor(S0).double()
+    z0 = torch.as_tensor(z0).double()
+    g = torch.Generator().manual_seed(24)
+    R = torch.randn(B, H, d, d, d, generator=g, dtype=torch.float64) * 10 * S0.abs().mean()
+    S0 = (S0.view(B, H, d, d, d) + 0.5 * (R - R.transpose(2, 3))).reshape(B, H, d * d, d).float()
+    r = torch.randn(B, H, d, d, generator=g, dtype=torch.float64) * 10 * z0.abs().mean()
+    z0 = (z0.view(B, H, d, d) + 0.5 * (r - r.transpose(2, 3))).reshape(B, H, d * d).float()
+    inp = si.sequence_inputs(B, H, T, d, d, dtype="bf16", qkv_std=0.125, seed=18)
+    inp["a"] = torch.full_like(inp["a"], -8.0)
+    gi = cuda(inp)
+    o, Z, Sf, zf = tm2.forward(gi["q"], gi["k"], gi["v"], gi["a"], normalize=True, S0=S0.cuda(),
+                               z0=z0.cuda(), return_state=True)
+    torch.cuda.synchronize()
+    o_r, Z_r, Sf_r, zf_r = oracle.fwd_recurrent(inp["q"], inp["k"], inp["v"], inp["a"], True, S0=S0, z0=z0)
+    asym = torch.as_tensor(Sf_r).view(B, H, d, d, d)
+    asym = (asym - asym.transpose(2, 3)).abs().max() / torch.as_tensor(Sf_r).abs().max()
+    assert asym > 0.1   # the antisymmetric part is a visible share of the final state
+    assert err(o.cpu(), o_r) <= 2e-2 and err(Z.cpu(), Z_r) <= 2e-2
+    assert err(Sf.cpu(), Sf_r) <= 2e-2 and err(zf.cpu(), zf_r) <= 2e-2
+
+
 @pytest.mark.parametrize("normalize", [True, False])
 def test_fwd_chunk_invariance_bf16_d64(normalize):
     """chunk 64 (CUDA-core path) and chunk 256 (tensor-core path) give the same outputs,
