@@ -109,32 +109,40 @@ cudaError_t launch_global_cumsum(const Problem& p, const float* Aloc, const floa
     return cudaGetLastError();
 }
 
-// grid BH, block 1024: walks the sequence from its end in tiles of 1024.  The running sum is
-// kept in fp64: over thousands of tokens the terms largely cancel (their total is zero without
-// an initial state), and an fp32 sum would leave a rounding error comparable to the result.
+// grid (tiles, BH), block 1024: tile j holds the 1024 tokens ending at T - 1 - 1024 j (thread 0
+// the latest).  Its carry is the sum over every later token, read directly (a block reduction:
+// the later tokens of all tiles of a head total T^2 / 2048 reads, small next to the rest), so
+// the tiles of a head run in parallel.  The sums are kept in fp64: over thousands of tokens the
+// terms largely cancel (their total is zero without an initial state), and an fp32 sum would
+// leave a rounding error comparable to the result.
 __global__ void __launch_bounds__(1024) reverse_cumsum_da_kernel(
     const float* __restrict__ a, const float* __restrict__ row, const float* __restrict__ col,
     float* __restrict__ da, int T) {
     __shared__ double wsum[32];
+    const int j = blockIdx.x;
+    const long bh = blockIdx.y;
+    const int top = T - 1 - 1024 * j;            // the latest token of this tile
+    auto term = [&](int u) { return (double)row[bh * T + u] - (col ? (double)col[bh * T + u] : 0.0); };
+    double part = 0.0;
+    for (int u = top + 1 + (int)threadIdx.x; u < T; u += blockDim.x) part += term(u);
+    // block total of `part`: the last element of the inclusive scan
+    const double run = block_inclusive_scan_d(part, wsum);
     __shared__ double carry_s;
-    const long bh = blockIdx.x;
-    double carry = 0.0;
-    for (int base = T - 1; base >= 0; base -= blockDim.x) {
-        const int u = base - (int)threadIdx.x;   // thread 0 holds the latest token of the tile
-        double x = 0.0;
-        if (u >= 0) x = (double)row[bh * T + u] - (col ? (double)col[bh * T + u] : 0.0);
-        const double s = block_inclusive_scan_d(x, wsum) + carry;
-        if (u >= 0) da[bh * T + u] = -sigmoid_f(a[bh * T + u]) * (float)s;
-        if (threadIdx.x == blockDim.x - 1) carry_s = s;
-        __syncthreads();
-        carry = carry_s;
-        __syncthreads();
-    }
+    if (threadIdx.x == blockDim.x - 1) carry_s = run;
+    __syncthreads();
+    const double carry = carry_s;
+    __syncthreads();
+    const int u = top - (int)threadIdx.x;
+    const double x = u >= 0 ? term(u) : 0.0;
+    const double sres = block_inclusive_scan_d(x, wsum) + carry;
+    if (u >= 0) da[bh * T + u] = -sigmoid_f(a[bh * T + u]) * (float)sres;
 }
 
 cudaError_t launch_reverse_cumsum_da(const Problem& p, const float* a, const float* row,
                                      const float* col, float* da, cudaStream_t s) {
-    reverse_cumsum_da_kernel<<<(unsigned)p.BH(), 1024, 0, s>>>(a, row, col, da, p.T);
+    if (p.T <= 0 || p.BH() == 0) return cudaSuccess;
+    dim3 grid((unsigned)((p.T + 1023) / 1024), (unsigned)p.BH());
+    reverse_cumsum_da_kernel<<<grid, 1024, 0, s>>>(a, row, col, da, p.T);
     return cudaGetLastError();
 }
 

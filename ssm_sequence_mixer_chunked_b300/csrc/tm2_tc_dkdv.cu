@@ -47,6 +47,7 @@ constexpr int THREADS = 10 * 32;
 constexpr int WARP_TMA = 8, WARP_MMA = 9;
 constexpr int NR = 5;                         // ring slots of 32 KB
 constexpr int RB = 32768;
+static_assert(NR <= 7, "a slot is reused less than four groups later (gdone ring of four)");
 constexpr int NG = 16;                        // groups of four state slices
 constexpr int NREQ = 2 * NG + 3;              // hi/lo plane of each group, then K|V, Q, dO (intra part)
 constexpr int EARLY = NR - 1;                 // slot NR-1 first holds the K and V tiles for conversion
@@ -101,8 +102,10 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
                                                                  const __grid_constant__ Args a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_align1024(smem_raw);
-    __shared__ __align__(8) uint64_t bar_ld, bar_full[NR], bar_empty[NR], bar_cvt, bar_sfull[4], bar_sfree[4],
-        bar_pfull[4], bar_ufull[2], bar_uempty[2], bar_kvfull, bar_red, bar_zrdy, bar_done;
+    // gdone[g % 4]: the products of group g are done (its ring slots are free and its U buffer
+    // is full): one commit per group serves the TMA producer and the compute warps
+    __shared__ __align__(8) uint64_t bar_ld, bar_full[NR], bar_gdone[4], bar_cvt, bar_sfull[4], bar_sfree[4],
+        bar_pfull[4], bar_uempty[2], bar_kvfull, bar_red, bar_zrdy, bar_done;
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_s;
     __shared__ volatile int gflags[2];         // group waits of the compute warps
@@ -121,7 +124,6 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
         mbar_init(smem_u32(&bar_ld), 1);
         for (int i = 0; i < NR; ++i) {
             mbar_init(smem_u32(&bar_full[i]), 1);
-            mbar_init(smem_u32(&bar_empty[i]), 1);
         }
         mbar_init(smem_u32(&bar_cvt), 256);
         for (int b = 0; b < 4; ++b) {
@@ -130,7 +132,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
             mbar_init(smem_u32(&bar_pfull[b]), 256);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(smem_u32(&bar_ufull[i]), 1);
+            mbar_init(smem_u32(&bar_gdone[i]), 1);
+            mbar_init(smem_u32(&bar_gdone[i + 2]), 1);
             mbar_init(smem_u32(&bar_uempty[i]), 256);
         }
         mbar_init(smem_u32(&bar_kvfull), 1);
@@ -168,7 +171,10 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
             for (int r = 0; r < NREQ && !abort_s; ++r) {
                 const int sl = slot_of(r);
                 const uint32_t u = use_of(r);
-                if (u > 0 && !mbar_wait(smem_u32(&bar_empty[sl]), (u - 1) & 1, a.status)) {
+                // the slot's previous request belonged to group (r - NR) / 2 (fewer than four groups
+                // behind, so gdone of that group cannot have moved on yet)
+                if (u > 0 && !mbar_wait(smem_u32(&bar_gdone[((r - NR) >> 1) & 3]), (uint32_t)((r - NR) >> 3) & 1,
+                                        a.status)) {
                     abort_s = 1;
                     break;
                 }
@@ -221,8 +227,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
                     for (int kk = 0; kk < 4; ++kk)
                         umma_bf16(d, sdesc_sw128(sb0 + SKH + kk * 32), sdesc_sw128_ex(blo + kk * 2048, 8192, 1024), IDESC_U,
                                   1u);
-                    umma_commit(smem_u32(&bar_empty[slot_of(2 * g)]));
-                    umma_commit(smem_u32(&bar_empty[slot_of(2 * g + 1)]));
+
                 } else {
                     if (!(ok = mbar_wait(smem_u32(&bar_zrdy), 0, a.status))) break;   // normaliser tiles built
                     tc_fence_after();
@@ -233,7 +238,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
                         umma_bf16(d, sdesc_sw128(sb0 + SKH + kk * 32), sdesc_sw128(zl + kk * 32), IDESC_Z, 1u);
                     }
                 }
-                umma_commit(smem_u32(&bar_ufull[ub]));
+                umma_commit(smem_u32(&bar_gdone[g & 3]));
             }
             // ---- intra-chunk: dk += (dSs^T) Q, dv += (W zeta)^T dO over the 64-query blocks
             const int rkv = 2 * NG, rq = 2 * NG + 1, rd = 2 * NG + 2;
@@ -327,7 +332,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
         for (int g = 0; g <= NG && ok; ++g) {
             const int ub = g & 1;
             if (g == NG - 3) z_tiles_load(a.dzx + (bh * NC + c) * 4096, threadIdx.x, zr);   // in flight meanwhile
-            if (!(ok = group_wait(smem_u32(&bar_ufull[ub]), (uint32_t)(g >> 1) & 1, a.status, warp == 0, 1, 256, gflags,
+            if (!(ok = group_wait(smem_u32(&bar_gdone[g & 3]), (uint32_t)(g >> 2) & 1, a.status, warp == 0, 1, 256, gflags,
                                   kg, &abort_s)))
                 break;
             if (g == NG - 1) {   // group NG-1's products are done: its lo slot takes the normaliser matrix
@@ -339,21 +344,24 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
             const uint32_t ua = tmem + lane_base + ub * 256 + h * 32;
             if (g < NG) {
 #pragma unroll 1
-                for (int np = 0; np < 4; ++np) {
-                    float u[32];
-                    tmem_ld32(ua + np * 64, u);
-                    if (np == 3) {
+                for (int np = 0; np < 4; np += 2) {   // two slices per load pair (one wait for both)
+                    float u0[32], u1[32];
+                    tmem_ld32x2(ua + np * 64, ua + (np + 1) * 64, u0, u1);
+                    if (np == 2) {
                         tc_fence_before();
                         mbar_arrive(smem_u32(&bar_uempty[ub]));
                     }
-                    const float kn = __half2float(*reinterpret_cast<const __half*>(krow + swz_elem(l, 4 * g + np)));
-                    float p = 0.f;
+                    const float k0 = __half2float(*reinterpret_cast<const __half*>(krow + swz_elem(l, 4 * g + np)));
+                    const float k1 = __half2float(*reinterpret_cast<const __half*>(krow + swz_elem(l, 4 * g + np + 1)));
+                    float p0 = 0.f, p1 = 0.f;
 #pragma unroll
                     for (int k = 0; k < 32; ++k) {
-                        dvx[k] = fmaf(kn, u[k], dvx[k]);
-                        p = fmaf(vj[k], u[k], p);
+                        dvx[k] = fmaf(k1, u1[k], fmaf(k0, u0[k], dvx[k]));
+                        p0 = fmaf(vj[k], u0[k], p0);
+                        p1 = fmaf(vj[k], u1[k], p1);
                     }
-                    atomicAdd(&sDK[(4 * g + np) * 128 + l], p);
+                    atomicAdd(&sDK[(4 * g + np) * 128 + l], p0);
+                    atomicAdd(&sDK[(4 * g + np + 1) * 128 + l], p1);
                 }
             } else {
                 float u[32];

@@ -41,6 +41,7 @@ constexpr int THREADS = 10 * 32;
 constexpr int WARP_TMA = 8, WARP_MMA = 9;
 constexpr int NR = 6;                         // ring slots of 32 KB
 constexpr int RB = 32768;
+static_assert(NR <= 7, "a slot is reused less than four groups later (gdone ring of four)");
 constexpr int NG = TC_PACKED_BLOCKS;          // state blocks (block-packed layout), one product each
 constexpr int NREQ = 2 * NG + 3;              // hi/lo plane of each block, then Q|dO, K, V (intra part)
 constexpr int EARLY = NR - 1;                 // slot NR-1 first holds the Q and dO tiles for conversion
@@ -90,8 +91,10 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_cons
                                                                const __grid_constant__ Args a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_align1024(smem_raw);
-    __shared__ __align__(8) uint64_t bar_ld, bar_full[NR], bar_empty[NR], bar_cvt, bar_sfull[4], bar_sfree[4],
-        bar_pfull[4], bar_ufull[2], bar_uempty[2], bar_dqfull, bar_zrdy, bar_done;
+    // gdone[g % 4]: the products of group g are done (its ring slots are free and its U buffer
+    // is full): one commit per group serves the TMA producer and the compute warps
+    __shared__ __align__(8) uint64_t bar_ld, bar_full[NR], bar_gdone[4], bar_cvt, bar_sfull[4], bar_sfree[4],
+        bar_pfull[4], bar_uempty[2], bar_dqfull, bar_zrdy, bar_done;
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_s;
     __shared__ volatile int gflags[2];         // group waits of the compute warps
@@ -107,7 +110,6 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_cons
         mbar_init(smem_u32(&bar_ld), 1);
         for (int i = 0; i < NR; ++i) {
             mbar_init(smem_u32(&bar_full[i]), 1);
-            mbar_init(smem_u32(&bar_empty[i]), 1);
         }
         mbar_init(smem_u32(&bar_cvt), 256);
         for (int b = 0; b < 4; ++b) {
@@ -116,7 +118,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_cons
             mbar_init(smem_u32(&bar_pfull[b]), 256);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(smem_u32(&bar_ufull[i]), 1);
+            mbar_init(smem_u32(&bar_gdone[i]), 1);
+            mbar_init(smem_u32(&bar_gdone[i + 2]), 1);
             mbar_init(smem_u32(&bar_uempty[i]), 256);
         }
         mbar_init(smem_u32(&bar_dqfull), 1);
@@ -148,7 +151,10 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_cons
             for (int r = 0; r < NREQ && !abort_s; ++r) {
                 const int sl = slot_of(r);
                 const uint32_t u = use_of(r);
-                if (u > 0 && !mbar_wait(smem_u32(&bar_empty[sl]), (u - 1) & 1, a.status)) {
+                // the slot's previous request belonged to group (r - NR) / 2 (fewer than four groups
+                // behind, so gdone of that group cannot have moved on yet)
+                if (u > 0 && !mbar_wait(smem_u32(&bar_gdone[((r - NR) >> 1) & 3]), (uint32_t)((r - NR) >> 3) & 1,
+                                        a.status)) {
                     abort_s = 1;
                     break;
                 }
@@ -198,8 +204,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_cons
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         umma_bf16(d, sdesc_sw128(sb0 + SDH + kk * 32), sdesc_sw128(blo + kk * 32), IDESC_U, 1u);
-                    umma_commit(smem_u32(&bar_empty[slot_of(2 * g)]));
-                    umma_commit(smem_u32(&bar_empty[slot_of(2 * g + 1)]));
+
                 } else {
                     if (!(ok = mbar_wait(smem_u32(&bar_zrdy), 0, a.status))) break;   // normaliser tiles built
                     tc_fence_after();
@@ -210,7 +215,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_cons
                         umma_bf16(d, sdesc_sw128(sb0 + SQH + kk * 32), sdesc_sw128(zl + kk * 32), IDESC_Z, 1u);
                     }
                 }
-                umma_commit(smem_u32(&bar_ufull[ub]));
+                umma_commit(smem_u32(&bar_gdone[g & 3]));
             }
             // ---- intra-chunk: dq += (hi + lo of dSs) K over the 64-key blocks
             const int rq = 2 * NG, rk = 2 * NG + 1, rv = 2 * NG + 2;
@@ -296,7 +301,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_cons
 #pragma unroll 1
         for (int g = 0; g <= NG && ok; ++g) {
             const int ub = g & 1;
-            if (!(ok = group_wait(smem_u32(&bar_ufull[ub]), (uint32_t)(g >> 1) & 1, a.status, warp == 0, 1, 256, gflags,
+            if (!(ok = group_wait(smem_u32(&bar_gdone[g & 3]), (uint32_t)(g >> 2) & 1, a.status, warp == 0, 1, 256, gflags,
                                   kg, &abort_s)))
                 break;
             if (g == NG - 2) {   // block NG-2's products are done: its lo slot takes the normaliser matrix

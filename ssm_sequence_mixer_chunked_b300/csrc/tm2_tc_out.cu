@@ -42,6 +42,7 @@ constexpr int C = TC_CHUNK;
 constexpr int THREADS = 10 * 32;
 constexpr int WARP_TMA = 8, WARP_MMA = 9;
 constexpr int NR = 6;                        // ring slots of 32 KB
+static_assert(NR <= 7, "a slot is reused less than four groups later (gdone ring of four)");
 constexpr int RB = 32768;
 constexpr int NG = 16;                       // groups of four state slices
 constexpr int NREQ = 2 * NG + 3;             // hi/lo plane of each group, then Q, K, V (intra part)
@@ -86,8 +87,10 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
                                                                   const __grid_constant__ Args a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_align1024(smem_raw);
-    __shared__ __align__(8) uint64_t bar_ld, bar_full[NR], bar_empty[NR], bar_cvt, bar_sfull[4], bar_sfree[4],
-        bar_pfull[4], bar_ufull[2], bar_uempty[2], bar_yfull, bar_red, bar_done;
+    // gdone[g % 4]: the products of group g are done (its ring slots are free and its U buffer
+    // is full): one commit per group serves the TMA producer and the compute warps
+    __shared__ __align__(8) uint64_t bar_ld, bar_full[NR], bar_cvt, bar_sfull[4], bar_sfree[4], bar_pfull[4],
+        bar_gdone[4], bar_uempty[2], bar_yfull, bar_red, bar_done;
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_s;
     __shared__ volatile int gflags[2];         // group waits of the compute warps
@@ -104,7 +107,6 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
         mbar_init(smem_u32(&bar_ld), 1);
         for (int i = 0; i < NR; ++i) {
             mbar_init(smem_u32(&bar_full[i]), 1);
-            mbar_init(smem_u32(&bar_empty[i]), 1);
         }
         mbar_init(smem_u32(&bar_cvt), 256);
         for (int b = 0; b < 4; ++b) {
@@ -113,7 +115,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
             mbar_init(smem_u32(&bar_pfull[b]), 256);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(smem_u32(&bar_ufull[i]), 1);
+            mbar_init(smem_u32(&bar_gdone[i]), 1);
+            mbar_init(smem_u32(&bar_gdone[i + 2]), 1);
             mbar_init(smem_u32(&bar_uempty[i]), 256);
         }
         mbar_init(smem_u32(&bar_yfull), 1);
@@ -144,7 +147,10 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
             for (int r = 0; r < NREQ && !abort_s; ++r) {
                 const int sl = slot_of(r);
                 const uint32_t u = use_of(r);
-                if (u > 0 && !mbar_wait(smem_u32(&bar_empty[sl]), (u - 1) & 1, a.status)) {
+                // the slot's previous request belonged to group (r - NR) / 2 (NR > 3 groups behind the
+                // products of group r / 2, so gdone of that group cannot have moved on yet)
+                if (u > 0 && !mbar_wait(smem_u32(&bar_gdone[((r - NR) >> 1) & 3]), (uint32_t)((r - NR) >> 3) & 1,
+                                        a.status)) {
                     abort_s = 1;
                     break;
                 }
@@ -200,8 +206,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
                     for (int j = 0; j < 4 - bm; ++j)
                         umma_bf16(d, sdesc_sw128(sb0 + SQH + (bm + j) * 32), sdesc_sw128_ex(blo + j * 8192, 2048, 1024),
                                   IDESC_U, 1u);
-                    umma_commit(smem_u32(&bar_empty[slot_of(2 * g)]));
-                    umma_commit(smem_u32(&bar_empty[slot_of(2 * g + 1)]));
+
                 } else {
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
@@ -209,7 +214,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
                         umma_bf16(d, sdesc_sw128(sb0 + SQH + kk * 32), sdesc_sw128(sb0 + SZL + kk * 32), IDESC_Z, 1u);
                     }
                 }
-                umma_commit(smem_u32(&bar_ufull[ub]));
+                umma_commit(smem_u32(&bar_gdone[g & 3]));
             }
             // ---- intra-chunk blocks (64 keys each), once the last U and U_z have been read
             const int rq = 2 * NG, rk = 2 * NG + 1, rv = 2 * NG + 2;
@@ -278,22 +283,24 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
 #pragma unroll 1
         for (int g = 0; g <= NG && ok; ++g) {
             const int ub = g & 1;
-            if (!(ok = group_wait(smem_u32(&bar_ufull[ub]), (uint32_t)(g >> 1) & 1, a.status, warp == 0, 1, 256, gflags,
+            if (!(ok = group_wait(smem_u32(&bar_gdone[g & 3]), (uint32_t)(g >> 2) & 1, a.status, warp == 0, 1, 256, gflags,
                                   kg, &abort_s)))
                 break;
             const uint32_t ua = tmem + lane_base + ub * 256 + h * 32;
             if (g < NG) {
+                // two slices per load pair (one wait for both)
 #pragma unroll 1
-                for (int mp = 0; mp < 4; ++mp) {
-                    float u[32];
-                    tmem_ld32(ua + mp * 64, u);
-                    if (mp == 3) {
+                for (int mp = 0; mp < 4; mp += 2) {
+                    float u0[32], u1[32];
+                    tmem_ld32x2(ua + mp * 64, ua + (mp + 1) * 64, u0, u1);
+                    if (mp == 2) {
                         tc_fence_before();
                         mbar_arrive(smem_u32(&bar_uempty[ub]));
                     }
-                    const float qm = __half2float(*reinterpret_cast<const __half*>(qrow + swz_elem(l, 4 * g + mp)));
+                    const float q0 = __half2float(*reinterpret_cast<const __half*>(qrow + swz_elem(l, 4 * g + mp)));
+                    const float q1 = __half2float(*reinterpret_cast<const __half*>(qrow + swz_elem(l, 4 * g + mp + 1)));
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) nx[k] = fmaf(qm, u[k], nx[k]);
+                    for (int k = 0; k < 32; ++k) nx[k] = fmaf(q1, u1[k], fmaf(q0, u0[k], nx[k]));
                 }
             } else {
                 float u[32];
