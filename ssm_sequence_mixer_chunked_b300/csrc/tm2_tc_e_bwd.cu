@@ -18,9 +18,9 @@
 //    MN-major straight from their tiles.
 //  * queries (kd = false): per 64-key sub-block at or before the query tile, s = Q K^T and
 //    dP = dO V^T, dx hi + lo, dq += dx K.
-// With three sub-block buffers the MMA thread issues the scores of sub-block s while the
-// compute warps work on s - 1 and the gradient products of s - 2 drain, so the softmax step
-// overlaps the tensor core (a whole 128-token block needs 256 columns for scores + dP and
+// With three sub-block buffers the scores of sub-block s are issued while the compute warps
+// work on s - 1 and the gradient products of s - 2 drain, so the softmax step overlaps the
+// tensor core (a whole 128-token block needs 256 columns for scores + dP and
 // cannot be double-buffered beside the operands and accumulators).
 // Instantiated with KIND = ATTN_P2 or ATTN_P1 the same kernels are the backward of the
 // quadratic (C = T) form of 2Mamba and of the first-order mixer (App. C / C.1):
@@ -31,7 +31,9 @@
 // softmax step become w zeta and ds.
 // The per-token terms of the walked sub-blocks are staged in shared memory.  Warps 0-7
 // compute (warp w: lane quadrant w % 4, half w / 4 of the sub-block's 64 tokens), warp 8
-// issues TMA, warp 9 the MMAs.  Every mbarrier wait is bounded (TM2_ERR_TIMEOUT on expiry).
+// issues TMA, warp 9 the score and dP products, warp 10 the dk (or dq) products and warp 11
+// the dv products: one N = 64 instruction takes its issuing thread far longer than the tensor
+// core needs for it, and instructions from different threads overlap.  Every mbarrier wait is bounded (TM2_ERR_TIMEOUT on expiry).
 #include "tm2.h"
 #include "tm2_launch.h"
 #include "tm2_sm100.cuh"
@@ -43,8 +45,8 @@ namespace tceb {
 constexpr int BT = 128;                      // tokens per tile / block
 constexpr int SUB = 64;                      // walked tokens per sub-block
 constexpr int NB = 3;                        // tensor-memory sub-block buffers
-constexpr int THREADS = 10 * 32;
-constexpr int WARP_TMA = 8, WARP_MMA = 9;
+constexpr int THREADS = 12 * 32;
+constexpr int WARP_TMA = 8, WARP_MMA = 9;   // warp 9: scores + dP; warps 10 (dk or dq), 11 (dv)
 constexpr int NS = 4;                        // stages of the walked blocks (two tiles each)
 constexpr int TILE = BT * 128;               // [128][64] bf16
 constexpr int STAGE = 2 * TILE;
@@ -156,6 +158,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_attn_bwd_kernel(const __grid_co
     const int nblk = kd ? a.NT - tile : tile + 1;   // walked blocks: queries at or after / keys at or before
     const int blk0 = kd ? tile : 0;
     const uint32_t sb0 = smem_u32(smem);
+    constexpr int NGI = kd ? 2 : 1;                  // gradient-product issuers
+    const int nsb = 2 * nblk;
     float* sSc = reinterpret_cast<float*>(smem + SSC);
     float* sRed = reinterpret_cast<float*>(smem + SRED);
 
@@ -163,15 +167,15 @@ __global__ void __launch_bounds__(THREADS, 1) tc_attn_bwd_kernel(const __grid_co
         mbar_init(smem_u32(&bar_fix), 1);
         for (int i = 0; i < NS; ++i) {
             mbar_init(smem_u32(&bar_full[i]), 1);
-            mbar_init(smem_u32(&bar_empty[i]), 1);
+            mbar_init(smem_u32(&bar_empty[i]), NGI);
         }
         for (int i = 0; i < NB; ++i) {
             mbar_init(smem_u32(&bar_sfull[i]), 1);
             mbar_init(smem_u32(&bar_pfull[i]), 256);
-            mbar_init(smem_u32(&bar_bfree[i]), 1);
+            mbar_init(smem_u32(&bar_bfree[i]), NGI);
         }
-        mbar_init(smem_u32(&bar_accfull), 1);
-        mbar_init(smem_u32(&bar_done), 1);
+        mbar_init(smem_u32(&bar_accfull), NGI);
+        mbar_init(smem_u32(&bar_done), 1 + NGI);
         abort_s = 0;
         fence_mbar_init();
     }
@@ -208,59 +212,65 @@ __global__ void __launch_bounds__(THREADS, 1) tc_attn_bwd_kernel(const __grid_co
                 mbar_wait(smem_u32(&bar_full[c % NS]), (uint32_t)(c / NS) & 1, a.status);
         }
     } else if (warp == WARP_MMA) {
+        // scores and dP of every walked sub-block
         if (lane == 0) {
             bool ok = mbar_wait(smem_u32(&bar_fix), 0, a.status);
             tc_fence_after();
-            const int nsb = 2 * nblk;
-            // scores of sub-block s, then the gradient products of sub-block s - 1
-            for (int s = 0; s <= nsb && ok; ++s) {
+            for (int s = 0; s < nsb && ok; ++s) {
                 if (abort_s) { ok = false; break; }
-                if (s < nsb) {
-                    const int c = s >> 1, st = c % NS, u = s % NB;
-                    if ((s & 1) == 0 && !(ok = mbar_wait(smem_u32(&bar_full[st]), (uint32_t)(c / NS) & 1, a.status)))
-                        break;
-                    if (s >= NB && !(ok = mbar_wait(smem_u32(&bar_bfree[u]), (uint32_t)((s / NB) - 1) & 1, a.status)))
-                        break;
-                    tc_fence_after();
-                    const uint32_t sc = sb0 + SSTG + st * STAGE + (s & 1) * (SUB * 128), sd = sc + TILE;
-                    const uint32_t d = tmem + 128u * (uint32_t)u;
-                    // scores and dP: (fixed tile) x (walked sub-block)^T, M = 128, N = 64, K = 64
+                const int c = s >> 1, st = c % NS, u = s % NB;
+                if ((s & 1) == 0 && !(ok = mbar_wait(smem_u32(&bar_full[st]), (uint32_t)(c / NS) & 1, a.status)))
+                    break;
+                if (s >= NB && !(ok = mbar_wait(smem_u32(&bar_bfree[u]), (uint32_t)((s / NB) - 1) & 1, a.status)))
+                    break;
+                tc_fence_after();
+                const uint32_t sc = sb0 + SSTG + st * STAGE + (s & 1) * (SUB * 128), sd = sc + TILE;
+                const uint32_t d = tmem + 128u * (uint32_t)u;
+                // (fixed tile) x (walked sub-block)^T, M = 128, N = 64, K = 64
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        umma_bf16(d, sdesc_sw128(sb0 + SFIX + kk * 32), sdesc_sw128(sc + kk * 32), IDESC_S, kk > 0);
-                        umma_bf16(d + 64, sdesc_sw128(sb0 + SFIX + TILE + kk * 32), sdesc_sw128(sd + kk * 32), IDESC_S,
-                                  kk > 0);
-                    }
-                    umma_commit(smem_u32(&bar_sfull[u]));
+                for (int kk = 0; kk < 4; ++kk) {
+                    umma_bf16(d, sdesc_sw128(sb0 + SFIX + kk * 32), sdesc_sw128(sc + kk * 32), IDESC_S, kk > 0);
+                    umma_bf16(d + 64, sdesc_sw128(sb0 + SFIX + TILE + kk * 32), sdesc_sw128(sd + kk * 32), IDESC_S,
+                              kk > 0);
                 }
-                if (s >= 1) {
-                    const int pz = s - 1, c = pz >> 1, st = c % NS, u = pz % NB;
-                    if (!(ok = mbar_wait(smem_u32(&bar_pfull[u]), (uint32_t)(pz / NB) & 1, a.status))) break;
-                    tc_fence_after();
-                    const uint32_t sc = sb0 + SSTG + st * STAGE + (pz & 1) * (SUB * 128), sd = sc + TILE;
-                    const uint32_t base = tmem + 128u * (uint32_t)u;
+                umma_commit(smem_u32(&bar_sfull[u]));
+            }
+            if (!ok) abort_s = 1;
+            umma_commit(smem_u32(&bar_done));
+            mbar_wait(smem_u32(&bar_done), 0, a.status);
+        }
+    } else if (warp > WARP_MMA) {
+        // gradient products of every sub-block once the compute warps have written P and dx:
+        // part 0 accumulates dk (key tiles) or dq (query tiles), part 1 dv (key tiles only).
+        // Each chain has its own issuing thread so that their instructions overlap.
+        const int part = warp - WARP_MMA - 1;
+        if (lane == 0 && part < NGI) {
+            bool ok = true;
+            for (int pz = 0; pz < nsb && ok; ++pz) {
+                if (abort_s) { ok = false; break; }
+                const int c = pz >> 1, st = c % NS, u = pz % NB;
+                if (!(ok = mbar_wait(smem_u32(&bar_pfull[u]), (uint32_t)(pz / NB) & 1, a.status))) break;
+                tc_fence_after();
+                const uint32_t sc = sb0 + SSTG + st * STAGE + (pz & 1) * (SUB * 128), sd = sc + TILE;
+                const uint32_t base = tmem + 128u * (uint32_t)u;
 #pragma unroll
-                    for (int kk = 0; kk < SUB / 16; ++kk) {   // 16 tokens: half kk / 2, round kk % 2
-                        const uint32_t acc0 = (pz > 0 || kk > 0) ? 1u : 0u;
-                        const uint32_t opP = base + (kk >> 1) * 32 + (kk & 1) * 16;        // P hi, then P lo at +8
-                        const uint32_t opH = base + 64 + (kk >> 1) * 32 + (kk & 1) * 16;   // dx hi, then dx lo at +8
-                        const uint32_t opL = opH + 8;
-                        if (kd) {   // dv += (P hi + lo)^T dO, dk += (dx hi + lo)^T Q
-                            const uint64_t qd = sdesc_sw128_ex(sc + kk * 2048, 8192, 1024);
-                            const uint64_t dd = sdesc_sw128_ex(sd + kk * 2048, 8192, 1024);
-                            umma_bf16_ts(tmem + TM_ACC2, opP, dd, IDESC_MN, acc0);
-                            umma_bf16_ts(tmem + TM_ACC2, opP + 8, dd, IDESC_MN, 1u);
-                            umma_bf16_ts(tmem + TM_ACC, opH, qd, IDESC_MN, acc0);
-                            umma_bf16_ts(tmem + TM_ACC, opL, qd, IDESC_MN, 1u);
-                        } else {    // dq += (dx hi + lo) K
-                            const uint64_t kdsc = sdesc_sw128_ex(sc + kk * 2048, 8192, 1024);
-                            umma_bf16_ts(tmem + TM_ACC, opH, kdsc, IDESC_MN, acc0);
-                            umma_bf16_ts(tmem + TM_ACC, opL, kdsc, IDESC_MN, 1u);
-                        }
+                for (int kk = 0; kk < SUB / 16; ++kk) {   // 16 tokens: half kk / 2, round kk % 2
+                    const uint32_t acc0 = (pz > 0 || kk > 0) ? 1u : 0u;
+                    const uint32_t off = (kk >> 1) * 32 + (kk & 1) * 16;
+                    if (part == 1) {   // dv += (P hi + lo)^T dO
+                        const uint32_t opP = base + off;   // P hi, then P lo at +8
+                        const uint64_t dd = sdesc_sw128_ex(sd + kk * 2048, 8192, 1024);
+                        umma_bf16_ts(tmem + TM_ACC2, opP, dd, IDESC_MN, acc0);
+                        umma_bf16_ts(tmem + TM_ACC2, opP + 8, dd, IDESC_MN, 1u);
+                    } else {           // dk += (dx hi + lo)^T Q, or dq += (dx hi + lo) K
+                        const uint32_t opH = base + 64 + off;   // dx hi, then dx lo at +8
+                        const uint64_t qd = sdesc_sw128_ex(sc + kk * 2048, 8192, 1024);
+                        umma_bf16_ts(tmem + TM_ACC, opH, qd, IDESC_MN, acc0);
+                        umma_bf16_ts(tmem + TM_ACC, opH + 8, qd, IDESC_MN, 1u);
                     }
-                    umma_commit(smem_u32(&bar_bfree[u]));
-                    if (pz & 1) umma_commit(smem_u32(&bar_empty[st]));   // both sub-blocks of the stage done
                 }
+                umma_commit(smem_u32(&bar_bfree[u]));
+                if (pz & 1) umma_commit(smem_u32(&bar_empty[st]));   // both sub-blocks of the stage done
             }
             if (ok) umma_commit(smem_u32(&bar_accfull));
             else abort_s = 1;
@@ -297,7 +307,6 @@ __global__ void __launch_bounds__(THREADS, 1) tc_attn_bwd_kernel(const __grid_co
         float sum = 0.f;
         int kg = 0;
         bool ok = true;
-        const int nsb = 2 * nblk;
         // per-token term of walked sub-block j held by this thread: arrays W at [0, 64), D at
         // [64, 128) and (key tiles of the polynomial kinds) zeta at [128, 192) of a staging buffer
         constexpr int NARR = kd ? (E ? 2 : 3) : 1;
