@@ -211,12 +211,25 @@ __global__ void __launch_bounds__(THREADS, 1) tc_attn_fwd_kernel(const __grid_co
         float m_used = -INFINITY, lsum = 0.f;
         int kg = 0;
         bool ok = true;
+        // key terms: the raw running sums of block b + 1 are loaded while block b is worked on,
+        // so no thread waits on their latency
+        float kh = 0.f, kl = 0.f;
+        bool kin = false;
+        auto fetch = [&](int b) {
+            const long j = (long)(qt - b) * BK + threadIdx.x;
+            kin = j < a.T;
+            if (kin) {
+                kh = cumh[j];
+                kl = cuml[j];
+            }
+        };
+        if (threadIdx.x < BK) fetch(0);
         for (int b = 0; b < nkb && ok; ++b) {
             const int x = b & 1;
             // this block's key terms into buffer x (published by the group wait's barrier)
             if (threadIdx.x < BK) {
-                const long j = (long)(qt - b) * BK + threadIdx.x;
-                sKW[x * BK + threadIdx.x] = j < a.T ? ((cumh[j] - ref) + (cuml[j] - reflo)) * LOG2E : 0.f;
+                sKW[x * BK + threadIdx.x] = kin ? ((kh - ref) + (kl - reflo)) * LOG2E : 0.f;
+                if (b + 1 < nkb) fetch(b + 1);
             }
             if (!(ok = group_wait(smem_u32(&bar_sfull[x]), (uint32_t)(b >> 1) & 1, a.status, warp == 0, 1, 256, gflags,
                                   kg, &abort_s)))

@@ -312,26 +312,41 @@ __global__ void __launch_bounds__(THREADS, 1) tc_attn_bwd_kernel(const __grid_co
         constexpr int NARR = kd ? (E ? 2 : 3) : 1;
         const bool stager = threadIdx.x < NARR * SUB;
         const int arr = threadIdx.x >> 6, tt_st = threadIdx.x & 63;
-        auto term = [&](int j) {
-            const long t = (long)blk0 * BT + (long)j * SUB + tt_st;
-            float val = 0.f;
-            if (t < a.T) {
-                const float off = (a.cum[base + t] - ref) + (a.cum_lo[base + t] - reflo);
-                if (arr == 1) val = a.Dv ? a.Dv[base + t] : 0.f;
-                else if (arr == 2) val = a.lse[base + t];
-                else val = (kd && E) ? (off - a.lse[base + t]) * LOG2E : off * LOG2E;
-            }
-            return val;
+        // the raw loads for sub-block j are issued one sub-block ahead and finished (the
+        // arithmetic that needs them) only when stored, so no thread waits on their latency
+        struct Raw {
+            float c, cl, l;
+            bool in;
         };
-        float nxt = stager ? term(0) : 0.f;
+        auto fetch = [&](int j) {
+            const long t = (long)blk0 * BT + (long)j * SUB + tt_st;
+            Raw w{0.f, 0.f, 0.f, t < a.T};
+            if (w.in) {
+                if (arr == 1) w.l = a.Dv ? a.Dv[base + t] : 0.f;
+                else if (arr == 2) w.l = a.lse[base + t];
+                else {
+                    w.c = a.cum[base + t];
+                    w.cl = a.cum_lo[base + t];
+                    if (kd && E) w.l = a.lse[base + t];
+                }
+            }
+            return w;
+        };
+        auto finish = [&](const Raw& w) {
+            if (!w.in) return 0.f;
+            if (arr != 0) return w.l;
+            const float off = (w.c - ref) + (w.cl - reflo);
+            return (kd && E) ? (off - w.l) * LOG2E : off * LOG2E;
+        };
+        Raw nxt = stager ? fetch(0) : Raw{0.f, 0.f, 0.f, false};
         for (int sbk = 0; sbk < nsb && ok; ++sbk) {
             const int x = sbk & 1, u = sbk % NB;
             const long t0 = (long)blk0 * BT + (long)sbk * SUB;
             // the walked sub-block's terms into buffer x; the next one's loads fly meanwhile
             float* sc = sSc + x * 3 * SUB;
             if (stager) {
-                sc[arr * SUB + tt_st] = nxt;
-                if (sbk + 1 < nsb) nxt = term(sbk + 1);
+                sc[arr * SUB + tt_st] = finish(nxt);
+                if (sbk + 1 < nsb) nxt = fetch(sbk + 1);
             }
             // masks only on the diagonal block's sub-blocks and on a sub-block that runs past
             // the sequence end
@@ -343,12 +358,15 @@ __global__ void __launch_bounds__(THREADS, 1) tc_attn_bwd_kernel(const __grid_co
                                   gflags, kg, &abort_s)))
                 break;
             const uint32_t bufc = tmem + lane_base + 128u * (uint32_t)u;
-#pragma unroll 1
+            // this warp's 32 score and 32 dP columns under one wait
+            float s32[32], dp32[32];
+            tmem_ld32x2(bufc + h * 32, bufc + 64 + h * 32, s32, dp32);
+#pragma unroll
             for (int q4 = 0; q4 < 2; ++q4) {
                 const int tt0 = h * 32 + q4 * 16;
-                float s[16], dp[16], W[16], Dq[16], Zq[16];
-                tmem_ld16(bufc + tt0, s);
-                tmem_ld16(bufc + 64 + tt0, dp);
+                const float* s = s32 + 16 * q4;
+                const float* dp = dp32 + 16 * q4;
+                float W[16], Dq[16], Zq[16];
 #pragma unroll
                 for (int v4 = 0; v4 < 4; ++v4) {
                     const float4 w4 = reinterpret_cast<const float4*>(sc + tt0)[v4];
