@@ -70,27 +70,45 @@ cudaError_t launch_decay(const Problem& p, const float* a, float* Aloc, float* g
     return cudaGetLastError();
 }
 
-// grid BH, block 256.  Chunk offsets are summed in fp64 (a block-wide scan over the chunk
-// totals, 256 chunks per pass) so that only the final rounding to fp32 enters cum.
+// grid (ceil(T / GC_TOK), BH), block 256: each block writes the running sums of GC_TOK tokens.
+// The offset at the start of chunk c is the fp64 sum of the chunk totals before it: a block
+// reduction over the chunks before the tile, then one thread runs through the tile's own
+// chunks, so only the final rounding to fp32 (and its residual cum_lo) enters cum.
+constexpr int GC_TOK = 1024;
+
+TM2_DEV double block_sum_d(double v, double* wsum /* >= 32 doubles */) {
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = (blockDim.x + 31) >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) wsum[w] = v;
+    __syncthreads();
+    double t = 0.0;
+    for (int i = 0; i < nw; ++i) t += wsum[i];
+    __syncthreads();
+    return t;
+}
+
 __global__ void __launch_bounds__(256) global_cumsum_kernel(const float* __restrict__ Aloc, const float* __restrict__ g,
                                                             float* __restrict__ cum, float* __restrict__ cum_lo, int T,
                                                             int C, int NC) {
-    extern __shared__ double off[];   // NC doubles
+    extern __shared__ double off[];   // offsets of the tile's chunks
     __shared__ double wsum[32];
-    const long bh = blockIdx.x;
-    double carry = 0.0;
-    for (int c0 = 0; c0 < NC; c0 += blockDim.x) {
-        const int c = c0 + (int)threadIdx.x;
-        const double gc = c < NC ? (double)g[bh * NC + c] : 0.0;
-        const double incl = block_inclusive_scan_d(gc, wsum) + carry;
-        if (c < NC) off[c] = incl - gc;   // exclusive: the offset at the start of chunk c
-        if (threadIdx.x == blockDim.x - 1) wsum[0] = incl;
-        __syncthreads();
-        carry = wsum[0];
-        __syncthreads();
+    const long bh = blockIdx.y;
+    const int t0 = blockIdx.x * GC_TOK, t1 = min(T, t0 + GC_TOK);
+    const int c0 = t0 / C, c1 = (t1 - 1) / C;
+    double before = 0.0;
+    for (int c = threadIdx.x; c < c0; c += blockDim.x) before += (double)g[bh * NC + c];
+    before = block_sum_d(before, wsum);
+    if (threadIdx.x == 0) {
+        double run = before;
+        for (int c = c0; c <= c1; ++c) {
+            off[c - c0] = run;
+            run += (double)g[bh * NC + c];
+        }
     }
-    for (int t = threadIdx.x; t < T; t += blockDim.x) {
-        const double x = off[t / C] + (double)Aloc[bh * (long)NC * C + t];
+    __syncthreads();
+    for (int t = t0 + (int)threadIdx.x; t < t1; t += blockDim.x) {
+        const double x = off[t / C - c0] + (double)Aloc[bh * (long)NC * C + t];
         const float hi = (float)x;
         cum[bh * T + t] = hi;
         if (cum_lo) cum_lo[bh * T + t] = (float)(x - (double)hi);
@@ -99,13 +117,9 @@ __global__ void __launch_bounds__(256) global_cumsum_kernel(const float* __restr
 
 cudaError_t launch_global_cumsum(const Problem& p, const float* Aloc, const float* g, float* cum, float* cum_lo,
                                  cudaStream_t s) {
-    size_t smem = sizeof(double) * (size_t)p.NC;
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(global_cumsum_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-    }
-    global_cumsum_kernel<<<(unsigned)p.BH(), 256, smem, s>>>(Aloc, g, cum, cum_lo, p.T, p.C, p.NC);
+    const size_t smem = sizeof(double) * (size_t)(GC_TOK / p.C + 2);
+    dim3 grid((unsigned)((p.T + GC_TOK - 1) / GC_TOK), (unsigned)p.BH());
+    global_cumsum_kernel<<<grid, 256, smem, s>>>(Aloc, g, cum, cum_lo, p.T, p.C, p.NC);
     return cudaGetLastError();
 }
 
@@ -418,61 +432,100 @@ cudaError_t launch_tc_scan_operands(const Problem& p, bool rev, const void* key,
     return cudaGetLastError();
 }
 
-template <typename Tin>
-__global__ void rowdot_kernel(const float* __restrict__ o, const Tin* __restrict__ dO,
-                              float* __restrict__ out, long ntok, int dv) {
+// Backward preparation, one warp per token: D = dO . o (rowdot), and for the quadratic-form
+// mixers zeta = 1/Z (0 where Z = 0) and D when normalised, D = 0 and zeta = 1 otherwise.
+template <typename Tin, bool POLY>
+__global__ void prep_kernel(const float* __restrict__ o, const float* __restrict__ Z, const Tin* __restrict__ dO,
+                            float* __restrict__ Dv, float* __restrict__ zeta, long ntok, int dv, bool normalize) {
     const long tok = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (tok >= ntok) return;
     float D = 0.f;
-    for (int c = lane; c < dv; c += 32) D += to_f(dO[tok * dv + c]) * o[tok * dv + c];
-    D = warp_sum(D);
-    if (lane == 0) out[tok] = D;
-}
-
-// Backward preparation of the quadratic-form mixers, one warp per token: D = dO . o and
-// zeta = 1/Z (0 where Z = 0) when normalised, D = 0 and zeta = 1 otherwise.
-template <typename Tin>
-__global__ void poly_prep_kernel(const float* __restrict__ o, const float* __restrict__ Z,
-                                 const Tin* __restrict__ dO, float* __restrict__ Dv, float* __restrict__ zeta,
-                                 long ntok, int dv, bool normalize) {
-    const long tok = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (tok >= ntok) return;
-    float D = 0.f;
-    if (normalize) {
+    if (!POLY || normalize) {
         for (int c = lane; c < dv; c += 32) D += to_f(dO[tok * dv + c]) * o[tok * dv + c];
         D = warp_sum(D);
     }
     if (lane == 0) {
-        const float z = normalize ? Z[tok] : 1.f;
         Dv[tok] = D;
-        zeta[tok] = z != 0.f ? 1.f / z : 0.f;
+        if (POLY) {
+            const float z = normalize ? Z[tok] : 1.f;
+            zeta[tok] = z != 0.f ? 1.f / z : 0.f;
+        }
     }
+}
+
+// The same for dv = 64 with 16-byte aligned rows: eight threads per token, eight elements each
+// (one 16-byte load of bf16 dO, or two of fp32, and two of o), combined by shuffles.
+TM2_DEV void load8(const __nv_bfloat16* p, float* f) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+TM2_DEV void load8(const float* p, float* f) {
+    const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+    f[0] = a.x, f[1] = a.y, f[2] = a.z, f[3] = a.w, f[4] = b.x, f[5] = b.y, f[6] = b.z, f[7] = b.w;
+}
+
+template <typename Tin, bool POLY>
+__global__ void __launch_bounds__(256) prep64_kernel(const float* __restrict__ o, const float* __restrict__ Z,
+                                                     const Tin* __restrict__ dO, float* __restrict__ Dv,
+                                                     float* __restrict__ zeta, long ntok, bool normalize) {
+    const long tok = (long)blockIdx.x * 32 + (threadIdx.x >> 3);
+    const int part = threadIdx.x & 7;
+    float D = 0.f;
+    if (tok < ntok && (!POLY || normalize)) {
+        float x[8], y[8];
+        load8(dO + tok * 64 + part * 8, x);
+        load8(o + tok * 64 + part * 8, y);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) D = fmaf(x[i], y[i], D);
+    }
+    D += __shfl_xor_sync(0xffffffffu, D, 4);
+    D += __shfl_xor_sync(0xffffffffu, D, 2);
+    D += __shfl_xor_sync(0xffffffffu, D, 1);
+    if (tok < ntok && part == 0) {
+        Dv[tok] = D;
+        if (POLY) {
+            const float z = normalize ? Z[tok] : 1.f;
+            zeta[tok] = z != 0.f ? 1.f / z : 0.f;
+        }
+    }
+}
+
+template <bool POLY>
+static cudaError_t launch_prep(const Problem& p, const float* o, const float* Z, const void* dO, float* D, float* zeta,
+                               cudaStream_t s) {
+    const long ntok = p.BH() * p.T;
+    const bool vec = p.dv == 64 && ((reinterpret_cast<uintptr_t>(o) | reinterpret_cast<uintptr_t>(dO)) & 15) == 0;
+    if (vec) {
+        const unsigned blocks = (unsigned)((ntok + 31) / 32);
+        if (p.dtype == 1)
+            prep64_kernel<__nv_bfloat16, POLY><<<blocks, 256, 0, s>>>(o, Z, (const __nv_bfloat16*)dO, D, zeta, ntok,
+                                                                     p.normalize);
+        else
+            prep64_kernel<float, POLY><<<blocks, 256, 0, s>>>(o, Z, (const float*)dO, D, zeta, ntok, p.normalize);
+    } else {
+        const unsigned blocks = (unsigned)((ntok + 7) / 8);
+        if (p.dtype == 1)
+            prep_kernel<__nv_bfloat16, POLY><<<blocks, 256, 0, s>>>(o, Z, (const __nv_bfloat16*)dO, D, zeta, ntok,
+                                                                   p.dv, p.normalize);
+        else
+            prep_kernel<float, POLY><<<blocks, 256, 0, s>>>(o, Z, (const float*)dO, D, zeta, ntok, p.dv, p.normalize);
+    }
+    return cudaGetLastError();
 }
 
 cudaError_t launch_poly_prep(const Problem& p, const float* o, const float* Z, const void* dO, float* D,
                              float* zeta, cudaStream_t s) {
-    const long ntok = p.BH() * p.T;
-    const unsigned blocks = (unsigned)((ntok + 7) / 8);
-    if (p.dtype == 1)
-        poly_prep_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(o, Z, (const __nv_bfloat16*)dO, D, zeta, ntok, p.dv,
-                                                              p.normalize);
-    else
-        poly_prep_kernel<float><<<blocks, 256, 0, s>>>(o, Z, (const float*)dO, D, zeta, ntok, p.dv, p.normalize);
-    return cudaGetLastError();
+    return launch_prep<true>(p, o, Z, dO, D, zeta, s);
 }
 
-cudaError_t launch_rowdot(const Problem& p, const void* o, const void* dO, float* Dvec,
-                          cudaStream_t s) {
-    const long ntok = p.BH() * p.T;
-    const unsigned blocks = (unsigned)((ntok + 7) / 8);
-    if (p.dtype == 1)
-        rowdot_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>((const float*)o,
-                                                           (const __nv_bfloat16*)dO, Dvec, ntok, p.dv);
-    else
-        rowdot_kernel<float><<<blocks, 256, 0, s>>>((const float*)o, (const float*)dO, Dvec, ntok, p.dv);
-    return cudaGetLastError();
+cudaError_t launch_rowdot(const Problem& p, const void* o, const void* dO, float* Dvec, cudaStream_t s) {
+    return launch_prep<false>(p, (const float*)o, nullptr, dO, Dvec, nullptr, s);
 }
 
 }  // namespace tm2
