@@ -41,6 +41,9 @@ import synth_inputs as si  # noqa: E402
 
 METRIC = "2Mamba fwd+bwd tokens/s at T=8192 on 1 B300; % bf16 tensor peak; decode GB/s"
 FLUSH_BYTES = 256 << 20
+# kernels launched beside another one (their event-timed span includes sharing the SMs)
+OVERLAPPED = {"tc_bwd_dq": "runs beside the reverse state walk (which has stream priority); the span is "
+                           "from its first to its last CTA, not its own device time"}
 
 
 def peaks():
@@ -451,8 +454,9 @@ def run_tm2(args, world, rank, device):
     kern = summarize(recs)
     launches = len(recs)
 
-    # roofline of the dominant kernel (largest share of step time)
-    dom = max(kern, key=lambda n: kern[n]["ms"])
+    # roofline of the dominant kernel (largest share of step time), among the kernels that run
+    # alone: dq runs beside the reverse walk, so its event-timed span includes that sharing
+    dom = max((n for n in kern if n not in OVERLAPPED), key=lambda n: kern[n]["ms"])
     per_launch_tokens = B * H * T
     tc = dom.startswith("tc_")
     kf = kernel_flops(dom, d, dv, 256 if tc else 64, per_launch_tokens)
@@ -473,6 +477,8 @@ def run_tm2(args, world, rank, device):
             if r is not None:
                 per_kernel_roof[n] = {"bound": r["bound"], "frac": round(r["frac"], 4),
                                       "tensor_frac": round(r["tensor_frac"], 4), "hbm_frac": round(r["hbm_frac"], 4)}
+                if n in OVERLAPPED:
+                    per_kernel_roof[n]["note"] = OVERLAPPED[n]
 
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,

@@ -5,6 +5,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <mutex>
 #include <vector>
 
 #include "tm2.h"
@@ -193,6 +194,41 @@ struct TraceScope {
     }
 };
 
+// A high-priority stream per device that takes the backward's reverse state walk, so that dq,
+// which reads only the forward states, runs beside it on the caller's stream: the block
+// scheduler prefers the walk's CTAs and dq's CTAs fill the SMs its last wave leaves idle.
+// Fork and join are events made per call (destroyed once their work is enqueued).
+static cudaError_t side_stream(cudaStream_t* out) {
+    static std::mutex mu;
+    static cudaStream_t streams[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!streams[dev]) {
+        int least = 0, greatest = 0;
+        e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
+        if (e != cudaSuccess) return e;
+        e = cudaStreamCreateWithPriority(&streams[dev], cudaStreamNonBlocking, greatest);
+        if (e != cudaSuccess) return e;
+    }
+    *out = streams[dev];
+    return cudaSuccess;
+}
+
+struct ForkJoin {
+    cudaEvent_t fork = nullptr, join = nullptr;
+    cudaError_t make() {
+        cudaError_t e = cudaEventCreateWithFlags(&fork, cudaEventDisableTiming);
+        return e != cudaSuccess ? e : cudaEventCreateWithFlags(&join, cudaEventDisableTiming);
+    }
+    ~ForkJoin() {
+        if (fork) cudaEventDestroy(fork);
+        if (join) cudaEventDestroy(join);
+    }
+};
+
 #define TM2_RUN(name, call)                  \
     do {                                     \
         TraceScope ts_(name, s);             \
@@ -366,8 +402,20 @@ int tm2_backward(const void* q, const void* k, const void* v, const float* a, co
         ScanIO r{};
         r.rev = true; r.ops = ops; r.g = g; r.zmax = zmax; r.amax = amax_r;
         r.Sx = dSx; r.zx = dzx; r.sscale = sscale;
-        TM2_RUN("tc_state_scan_bwd", tc_state_scan(p, r, s));
+        // the reverse walk on the side stream, dq beside it; dk/dv waits for the walk
+        cudaStream_t side = nullptr;
+        ForkJoin fj;
+        TM2_CK(side_stream(&side));
+        TM2_CK(fj.make());
+        TM2_CK(cudaEventRecord(fj.fork, s));
+        TM2_CK(cudaStreamWaitEvent(side, fj.fork, 0));
+        {
+            cudaStream_t s = side;
+            TM2_RUN("tc_state_scan_bwd", tc_state_scan(p, r, s));
+        }
+        TM2_CK(cudaEventRecord(fj.join, side));
         TM2_RUN("tc_bwd_dq", tc_bwd_dq(p, q, k, v, dO, Aloc, zeta, ucol, Sx, zx, amax_f, dq, s));
+        TM2_CK(cudaStreamWaitEvent(s, fj.join, 0));
         TM2_RUN("tc_bwd_dkdv", tc_bwd_dkdv(p, q, k, v, dO, Aloc, g, zeta, ucol, rowterm, dSx, dzx, sscale, amax_r,
                                            dk, dv, dcum, s));
         TM2_RUN("reverse_cumsum_da", launch_reverse_cumsum_da(p, a, dcum, nullptr, da, s));
