@@ -41,18 +41,24 @@ using namespace tctile;
 constexpr int C = TC_CHUNK;
 constexpr int THREADS = 10 * 32;
 constexpr int WARP_TMA = 8, WARP_MMA = 9;
-constexpr int NR = 6;                        // ring slots of 32 KB
-static_assert(NR <= 7, "a slot is reused less than four groups later (gdone ring of four)");
+// The TMA ring is a byte ring of 24 units of 8 KB: request r takes the next size(r) units
+// (wrapping to unit 0 when they would run past the end).  One request (one transaction
+// barrier) carries both planes of a group, 2 (4 - bm) boxes: a CTA streams at a fixed cost
+// per request plus a small cost per byte (measured: 8 KB requests 25 GB/s per SM, 32 KB
+// requests 80-95 GB/s), so few large requests keep the readout short.
+constexpr int UNIT = 8192;
+constexpr int NUNIT = 24;
 constexpr int RB = 32768;
 constexpr int NG = 16;                       // groups of four state slices
-constexpr int NREQ = 2 * NG + 3;             // hi/lo plane of each group, then Q, K, V (intra part)
-constexpr int EARLY = NR - 1;                // slot NR-1 first holds the Q tile for conversion
+constexpr int NREQ = NG + 3;                 // both planes of each group, then Q, K, V (intra part)
+constexpr int EARLY_U = NUNIT - 2;           // units 22, 23 first hold the Q tile for conversion
+constexpr int NGD = 16;                      // group-done barriers (a ring of 16, see the producer)
 // shared memory
 constexpr int RING = 0;
-constexpr int SQH = NR * RB;                 // fp16 copy of the Q tile [128][64]
+constexpr int SQH = NUNIT * UNIT;            // fp16 copy of the Q tile [128][64]
 constexpr int SZH = SQH + 16384, SZL = SZH + 8192;   // zm hi / lo, [64][64] fp16
 constexpr int SAV = SZL + 8192;              // chunk-local A, 256 floats
-constexpr int SRED = RING;                   // [2 halves][128 rows][2], in ring slot 0 (idle by then)
+constexpr int SRED = SQH;                    // [2 halves][128 rows][2], over the Q copy (read by then)
 constexpr int SMEM_BYTES = SAV + 1024 + 1024;
 // tensor memory: U buffers at 0 and 256; the intra part reuses it after the readout: the
 // intra accumulator, two score buffers and two (P hi, P lo) buffers, so that block b+1's
@@ -73,8 +79,30 @@ struct Args {
     int T, NC, Tp, normalize;
 };
 
-TM2_DEV int slot_of(int r) { return r % NR; }
-TM2_DEV uint32_t use_of(int r) { return (uint32_t)(r / NR); }
+TM2_DEV int req_units(int r) { return r < NG ? 2 * (4 - (r >> 2)) : (r == NG ? 2 : 4); }
+
+// Placement of the tile's requests in the byte ring (one thread, before the roles start): the
+// first unit of each request, the latest earlier request whose units it reuses (-1: none),
+// and whether it reuses the early Q tile's units (freed by the conversion).
+TM2_DEV void place_requests(int8_t* off, int8_t* wait_req, int8_t* wait_cvt) {
+    int8_t owner[NUNIT];
+    for (int u = 0; u < NUNIT; ++u) owner[u] = (int8_t)(u >= EARLY_U ? -2 : -1);
+    int at = 0;
+    for (int r = 0; r < NREQ; ++r) {
+        const int sz = req_units(r);
+        if (at + sz > NUNIT) at = 0;
+        int w = -1, cv = 0;
+        for (int u = at; u < at + sz; ++u) {
+            if (owner[u] == -2) cv = 1;
+            else if (owner[u] > w) w = owner[u];
+            owner[u] = (int8_t)r;
+        }
+        off[r] = (int8_t)at;
+        wait_req[r] = (int8_t)w;
+        wait_cvt[r] = (int8_t)cv;
+        at += sz;
+    }
+}
 
 }  // namespace tcout
 
@@ -89,8 +117,9 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
     uint8_t* smem = smem_align1024(smem_raw);
     // gdone[g % 4]: the products of group g are done (its ring slots are free and its U buffer
     // is full): one commit per group serves the TMA producer and the compute warps
-    __shared__ __align__(8) uint64_t bar_ld, bar_full[NR], bar_cvt, bar_sfull[4], bar_sfree[4], bar_pfull[4],
-        bar_gdone[4], bar_uempty[2], bar_yfull, bar_red, bar_done;
+    __shared__ __align__(8) uint64_t bar_ld, bar_full[NREQ], bar_cvt, bar_sfull[4], bar_sfree[4], bar_pfull[4],
+        bar_gdone[NGD], bar_uempty[2], bar_yfull, bar_red, bar_done;
+    __shared__ int8_t s_off[NREQ], s_wreq[NREQ], s_wcvt[NREQ];
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_s;
     __shared__ volatile int gflags[2];         // group waits of the compute warps
@@ -105,27 +134,22 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
 
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(&bar_ld), 1);
-        for (int i = 0; i < NR; ++i) {
-            mbar_init(smem_u32(&bar_full[i]), 1);
-        }
+        for (int i = 0; i < NREQ; ++i) mbar_init(smem_u32(&bar_full[i]), 1);
         mbar_init(smem_u32(&bar_cvt), 256);
         for (int b = 0; b < 4; ++b) {
             mbar_init(smem_u32(&bar_sfull[b]), 1);
             mbar_init(smem_u32(&bar_sfree[b]), 256);
             mbar_init(smem_u32(&bar_pfull[b]), 256);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(smem_u32(&bar_gdone[i]), 1);
-            mbar_init(smem_u32(&bar_gdone[i + 2]), 1);
-            mbar_init(smem_u32(&bar_uempty[i]), 256);
-        }
+        for (int i = 0; i < NGD; ++i) mbar_init(smem_u32(&bar_gdone[i]), 1);
+        for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&bar_uempty[i]), 256);
         mbar_init(smem_u32(&bar_yfull), 1);
         mbar_init(smem_u32(&bar_red), 256);
         mbar_init(smem_u32(&bar_done), 1);
         abort_s = 0;
+        place_requests(s_off, s_wreq, s_wcvt);
         fence_mbar_init();
     }
-    for (int j = threadIdx.x; j < C; j += THREADS) sAv[j] = a.Aloc[bh * a.Tp + (long)c * C + j];
     if (warp == 0) {
         tmem_alloc(smem_u32(&tmem_base_s), 512);
         tmem_relinquish();
@@ -134,7 +158,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base_s;
-    const uint32_t early = sb0 + RING + EARLY * RB;   // the Q tile, converted at the start
+    const uint32_t early = sb0 + RING + EARLY_U * UNIT;   // the Q tile, converted at the start
 
     if (warp == WARP_TMA) {
         if (lane == 0) {
@@ -145,39 +169,39 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
             const int chunk_id = (int)(bh * NC + c);
             int issued = 0;
             for (int r = 0; r < NREQ && !abort_s; ++r) {
-                const int sl = slot_of(r);
-                const uint32_t u = use_of(r);
-                // the slot's previous request belonged to group (r - NR) / 2 (NR > 3 groups behind the
-                // products of group r / 2, so gdone of that group cannot have moved on yet)
-                if (u > 0 && !mbar_wait(smem_u32(&bar_gdone[((r - NR) >> 1) & 3]), (uint32_t)((r - NR) >> 3) & 1,
-                                        a.status)) {
+                // the units of the latest earlier request (group w) they reuse are free once that
+                // group's products are done.  w is at most 12 groups (12 two-unit requests)
+                // behind request r, and the products cannot pass group r, so the ring of 16
+                // group-done barriers cannot have moved a phase past it.
+                const int w = s_wreq[r];
+                if (w >= 0 && !mbar_wait(smem_u32(&bar_gdone[w & (NGD - 1)]), (uint32_t)(w / NGD) & 1, a.status)) {
                     abort_s = 1;
                     break;
                 }
-                if (r == EARLY && !mbar_wait(smem_u32(&bar_cvt), 0, a.status)) {   // copy made: slot free
+                if (s_wcvt[r] && !mbar_wait(smem_u32(&bar_cvt), 0, a.status)) {   // copy made: units free
                     abort_s = 1;
                     break;
                 }
-                const uint32_t fb = smem_u32(&bar_full[sl]), dst = sb0 + RING + sl * RB;
-                if (r < 2 * NG) {   // rows 4 mq .. 4 mq + 3 of the blocks (bm, bm .. 3) of one plane
-                    const int g = r >> 1, bm = g >> 2, mq = g & 3;
-                    mbar_arrive_expect_tx(fb, (uint32_t)(4 - bm) * 8192);
-                    for (int j = 0; j < 4 - bm; ++j)
-                        tma_load_4d(dst + j * 8192, &tmS, fb, 0, 0, 16 * tc_block_index(bm, bm + j) + 4 * mq,
-                                    2 * chunk_id + (r & 1));
-                } else if (r == 2 * NG) {
+                const uint32_t fb = smem_u32(&bar_full[r]), dst = sb0 + RING + s_off[r] * UNIT;
+                if (r < NG) {   // rows 4 mq .. 4 mq + 3 of the blocks (bm, bm .. 3), hi then lo plane
+                    const int bm = r >> 2, mq = r & 3, nb = 4 - bm;
+                    mbar_arrive_expect_tx(fb, (uint32_t)(2 * nb) * 8192);
+                    for (int pl = 0; pl < 2; ++pl)
+                        for (int j = 0; j < nb; ++j)
+                            tma_load_4d(dst + (pl * nb + j) * 8192, &tmS, fb, 0, 0, 16 * tc_block_index(bm, bm + j) + 4 * mq,
+                                        2 * chunk_id + pl);
+                } else if (r == NG) {
                     mbar_arrive_expect_tx(fb, 16384);
                     tma_load_3d(dst, &tmQ, fb, 0, c * C + t * 128, (int)bh);
                 } else {
                     mbar_arrive_expect_tx(fb, RB);
-                    tma_load_3d(dst, r == 2 * NG + 1 ? &tmK : &tmV, fb, 0, c * C, (int)bh);
+                    tma_load_3d(dst, r == NG + 1 ? &tmK : &tmV, fb, 0, c * C, (int)bh);
                 }
                 issued = r + 1;
             }
             // no copy may be in flight at exit
             mbar_wait(lb, 0, a.status);
-            for (int r = issued - 1; r >= 0 && r >= issued - NR; --r)
-                mbar_wait(smem_u32(&bar_full[slot_of(r)]), use_of(r) & 1, a.status);
+            for (int r = 0; r < issued; ++r) mbar_wait(smem_u32(&bar_full[r]), 0, a.status);
         }
     } else if (warp == WARP_MMA) {
         if (lane == 0) {
@@ -188,18 +212,14 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
                 const int ub = g & 1;
                 const uint32_t k = (uint32_t)(g >> 1);
                 if (abort_s) { ok = false; break; }
-                if (g < NG) {
-                    const int r0 = 2 * g, r1 = 2 * g + 1;
-                    if (!(ok = mbar_wait(smem_u32(&bar_full[slot_of(r0)]), use_of(r0) & 1, a.status))) break;
-                    if (!(ok = mbar_wait(smem_u32(&bar_full[slot_of(r1)]), use_of(r1) & 1, a.status))) break;
-                }
+                if (g < NG && !(ok = mbar_wait(smem_u32(&bar_full[g]), 0, a.status))) break;
                 if (k > 0 && !(ok = mbar_wait(smem_u32(&bar_uempty[ub]), (k - 1) & 1, a.status))) break;
                 tc_fence_after();
                 const uint32_t d = tmem + ub * 256;
                 if (g < NG) {
                     // K over the key indices n >= 16 bm only: block (bm, bn) is box j = bn - bm
-                    const uint32_t bhi = sb0 + RING + slot_of(2 * g) * RB, blo = sb0 + RING + slot_of(2 * g + 1) * RB;
                     const int bm = g >> 2;
+                    const uint32_t bhi = sb0 + RING + s_off[g] * UNIT, blo = bhi + (4 - bm) * 8192;
                     for (int j = 0; j < 4 - bm; ++j)
                         umma_bf16(d, sdesc_sw128(sb0 + SQH + (bm + j) * 32), sdesc_sw128_ex(bhi + j * 8192, 2048, 1024),
                                   IDESC_U, j > 0);
@@ -214,18 +234,18 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
                         umma_bf16(d, sdesc_sw128(sb0 + SQH + kk * 32), sdesc_sw128(sb0 + SZL + kk * 32), IDESC_Z, 1u);
                     }
                 }
-                umma_commit(smem_u32(&bar_gdone[g & 3]));
+                umma_commit(smem_u32(&bar_gdone[g & (NGD - 1)]));
             }
             // ---- intra-chunk blocks (64 keys each), once the last U and U_z have been read
-            const int rq = 2 * NG, rk = 2 * NG + 1, rv = 2 * NG + 2;
+            const int rq = NG, rk = NG + 1, rv = NG + 2;
             if (ok) ok = mbar_wait(smem_u32(&bar_uempty[0]), (uint32_t)(NG >> 1) & 1, a.status);
             if (ok) ok = mbar_wait(smem_u32(&bar_uempty[1]), (uint32_t)((NG - 1) >> 1) & 1, a.status);
-            if (ok) ok = mbar_wait(smem_u32(&bar_full[slot_of(rq)]), use_of(rq) & 1, a.status);
-            if (ok) ok = mbar_wait(smem_u32(&bar_full[slot_of(rk)]), use_of(rk) & 1, a.status);
-            if (ok) ok = mbar_wait(smem_u32(&bar_full[slot_of(rv)]), use_of(rv) & 1, a.status);
+            if (ok) ok = mbar_wait(smem_u32(&bar_full[rq]), 0, a.status);
+            if (ok) ok = mbar_wait(smem_u32(&bar_full[rk]), 0, a.status);
+            if (ok) ok = mbar_wait(smem_u32(&bar_full[rv]), 0, a.status);
             tc_fence_after();
-            const uint32_t SQ = sb0 + RING + slot_of(rq) * RB;
-            const uint32_t SK = sb0 + RING + slot_of(rk) * RB, SV = sb0 + RING + slot_of(rv) * RB;
+            const uint32_t SQ = sb0 + RING + s_off[rq] * UNIT;
+            const uint32_t SK = sb0 + RING + s_off[rk] * UNIT, SV = sb0 + RING + s_off[rv] * UNIT;
             auto issue_s = [&](int b) {   // s = Q K_b^T into score buffer b & 1
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
@@ -262,11 +282,17 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
         const int l = quad * 32 + lane;              // tile row
         const int i = t * 128 + l;                   // token index inside the chunk
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-        const float Ai = sAv[i];
         int kg = 0;                                  // group-wait counter
+        // per-chunk terms, loaded while the Q tile is on its way: the chunk-local A of token
+        // threadIdx.x (C = 256 compute threads; published by the group waits' barriers), the
+        // operand maxima of the epilogue, and the normaliser matrix of the state
+        static_assert(C == 256, "one chunk-local A per compute thread");
+        const float av = a.Aloc[bh * a.Tp + (long)c * C + threadIdx.x];
+        const unsigned am_k = a.amax[bh * 4], am_v = a.amax[bh * 4 + 1];
         float4 zr[4];
-        z_tiles_load(a.zx + (bh * NC + c) * 4096, threadIdx.x, zr);   // in flight during the tile wait
+        z_tiles_load(a.zx + (bh * NC + c) * 4096, threadIdx.x, zr);
         bool ok = mbar_wait(smem_u32(&bar_ld), 0, a.status);
+        sAv[threadIdx.x] = av;
         if (ok) {   // fp16 copy of the Q tile; the normaliser matrix of the state as hi + lo fp16
             const int t256 = threadIdx.x;
             for (int pc = t256; pc < 1024; pc += 256) tile_bf16_to_f16(early, sb0 + SQH, pc);
@@ -283,7 +309,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
 #pragma unroll 1
         for (int g = 0; g <= NG && ok; ++g) {
             const int ub = g & 1;
-            if (!(ok = group_wait(smem_u32(&bar_gdone[g & 3]), (uint32_t)(g >> 2) & 1, a.status, warp == 0, 1, 256, gflags,
+            if (!(ok = group_wait(smem_u32(&bar_gdone[g & (NGD - 1)]), (uint32_t)(g / NGD) & 1, a.status, warp == 0, 1, 256, gflags,
                                   kg, &abort_s)))
                 break;
             const uint32_t ua = tmem + lane_base + ub * 256 + h * 32;
@@ -313,6 +339,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
             }
         }
         // ---- intra-chunk blocks; half h covers 32 of the 64 keys of a block
+        const float Ai = sAv[i];
         for (int b = 0; b < nblk && ok; ++b) {
             if (!(ok = group_wait(smem_u32(&bar_sfull[b]), 0, a.status, warp == 0, 1, 256, gflags, kg, &abort_s))) break;
             // (the P buffer's last reader, the product of block b-2, was issued before this block's
@@ -362,7 +389,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
         if (ok && !abort_s && (ok = mbar_wait(smem_u32(&bar_yfull), 0, a.status))) {
             tc_fence_after();
             const float eA = __expf(Ai);
-            const float ks = pow2_scale(a.amax[bh * 4]), vs = pow2_scale(a.amax[bh * 4 + 1]);
+            const float ks = pow2_scale(am_k), vs = pow2_scale(am_v);
             const float uz = 1.f / (ks * ks), un = uz / vs;   // exact powers of two
             const float zi = sRed[l * 2] + sRed[(128 + l) * 2];
             const float zo = sRed[l * 2 + 1] + sRed[(128 + l) * 2 + 1];
