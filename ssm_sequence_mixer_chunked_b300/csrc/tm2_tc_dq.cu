@@ -39,20 +39,26 @@ using namespace tctile;
 constexpr int C = TC_CHUNK;
 constexpr int THREADS = 10 * 32;
 constexpr int WARP_TMA = 8, WARP_MMA = 9;
-constexpr int NR = 6;                         // ring slots of 32 KB
-constexpr int RB = 32768;
-static_assert(NR <= 7, "a slot is reused less than four groups later (gdone ring of four)");
+// One TMA transaction per state block carries both planes (2 x 32 KB): a CTA streams at a fixed
+// cost per transaction plus a small cost per byte, so few large transactions keep the inter
+// part short.
+constexpr int NR = 3;                         // ring slots of 64 KB
+constexpr int RB = 65536;
+constexpr int PLANE = 32768;                  // the lo plane of a block at +32 KB
+static_assert(NR <= 5, "a slot is reused less than four groups later (gdone ring of four)");
 constexpr int NG = TC_PACKED_BLOCKS;          // state blocks (block-packed layout), one product each
-constexpr int NREQ = 2 * NG + 3;              // hi/lo plane of each block, then Q|dO, K, V (intra part)
+constexpr int NREQ = NG + 3;                  // both planes of each block, then Q|dO, K, V (intra part)
 constexpr int EARLY = NR - 1;                 // slot NR-1 first holds the Q and dO tiles for conversion
 // shared memory
 constexpr int RING = 0;
 constexpr int SQH = NR * RB;                  // fp16 copy of the Q tile [128][64]
 constexpr int SDH = SQH + 16384;              // fp16 copy of the dO tile
-// the normaliser matrix (hi, lo [64][64]) goes into the ring slot of group NG-2's lo plane,
-// which no later request uses, once that group's products are done
-constexpr int ZREQ = 2 * NG - 3;
-static_assert(ZREQ + NR >= 2 * NG + 3, "no later request may reuse the normaliser slot");
+// the normaliser matrix (hi, lo [64][64]) goes into the upper half of the slot of the Q|dO
+// request (its tiles take the lower 32 KB; no later request uses the slot) once the slot's
+// previous group, NG - NR, is done
+constexpr int ZREQ = NG;
+constexpr int ZFREE = NG - NR;
+static_assert(ZFREE >= 0 && ZREQ + NR >= NREQ, "no later request may reuse the normaliser slot");
 constexpr int SAV = SDH + 16384;              // chunk-local A, 256 floats
 constexpr int BYTES = SAV + 1024 + 1024;
 // tensor memory: U buffers at 0 and 256; the intra part reuses it after the inter part: dq
@@ -151,10 +157,9 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_cons
             for (int r = 0; r < NREQ && !abort_s; ++r) {
                 const int sl = slot_of(r);
                 const uint32_t u = use_of(r);
-                // the slot's previous request belonged to group (r - NR) / 2 (fewer than four groups
-                // behind, so gdone of that group cannot have moved on yet)
-                if (u > 0 && !mbar_wait(smem_u32(&bar_gdone[((r - NR) >> 1) & 3]), (uint32_t)((r - NR) >> 3) & 1,
-                                        a.status)) {
+                // the slot's previous request was group r - NR (fewer than four groups behind, so
+                // gdone of that group cannot have moved on yet)
+                if (u > 0 && !mbar_wait(smem_u32(&bar_gdone[(r - NR) & 3]), (uint32_t)((r - NR) >> 2) & 1, a.status)) {
                     abort_s = 1;
                     break;
                 }
@@ -163,14 +168,17 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_cons
                     break;
                 }
                 const uint32_t fb = smem_u32(&bar_full[sl]), dst = sb0 + RING + sl * RB;
-                mbar_arrive_expect_tx(fb, RB);
-                if (r < 2 * NG) {
-                    tma_load_3d(dst, &tmS, fb, 0, 256 * (r >> 1), 2 * chunk_id + (r & 1));
-                } else if (r == 2 * NG) {
+                if (r < NG) {
+                    mbar_arrive_expect_tx(fb, 2 * PLANE);
+                    tma_load_3d(dst, &tmS, fb, 0, 256 * r, 2 * chunk_id);
+                    tma_load_3d(dst + PLANE, &tmS, fb, 0, 256 * r, 2 * chunk_id + 1);
+                } else if (r == NG) {
+                    mbar_arrive_expect_tx(fb, 2 * 16384);
                     tma_load_3d(dst, &tmQ, fb, 0, c * C + it * 128, (int)bh);
                     tma_load_3d(dst + 16384, &tmD, fb, 0, c * C + it * 128, (int)bh);
                 } else {
-                    tma_load_3d(dst, r == 2 * NG + 1 ? &tmK : &tmV, fb, 0, c * C, (int)bh);
+                    mbar_arrive_expect_tx(fb, 32768);
+                    tma_load_3d(dst, r == NG + 1 ? &tmK : &tmV, fb, 0, c * C, (int)bh);
                 }
                 issued = r + 1;
             }
@@ -188,16 +196,12 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_cons
                 const int ub = g & 1;
                 const uint32_t k = (uint32_t)(g >> 1);
                 if (abort_s) { ok = false; break; }
-                if (g < NG) {
-                    const int r0 = 2 * g, r1 = 2 * g + 1;
-                    if (!(ok = mbar_wait(smem_u32(&bar_full[slot_of(r0)]), use_of(r0) & 1, a.status))) break;
-                    if (!(ok = mbar_wait(smem_u32(&bar_full[slot_of(r1)]), use_of(r1) & 1, a.status))) break;
-                }
+                if (g < NG && !(ok = mbar_wait(smem_u32(&bar_full[slot_of(g)]), use_of(g) & 1, a.status))) break;
                 if (k > 0 && !(ok = mbar_wait(smem_u32(&bar_uempty[ub]), (k - 1) & 1, a.status))) break;
                 tc_fence_after();
                 const uint32_t d = tmem + ub * 256;
                 if (g < NG) {
-                    const uint32_t bhi = sb0 + RING + slot_of(2 * g) * RB, blo = sb0 + RING + slot_of(2 * g + 1) * RB;
+                    const uint32_t bhi = sb0 + RING + slot_of(g) * RB, blo = bhi + PLANE;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         umma_bf16(d, sdesc_sw128(sb0 + SDH + kk * 32), sdesc_sw128(bhi + kk * 32), IDESC_U, kk > 0);
@@ -208,7 +212,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_cons
                 } else {
                     if (!(ok = mbar_wait(smem_u32(&bar_zrdy), 0, a.status))) break;   // normaliser tiles built
                     tc_fence_after();
-                    const uint32_t zh = sb0 + RING + slot_of(ZREQ) * RB, zl = zh + 8192;
+                    const uint32_t zh = sb0 + RING + slot_of(ZREQ) * RB + PLANE, zl = zh + 8192;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         umma_bf16(d, sdesc_sw128(sb0 + SQH + kk * 32), sdesc_sw128(zh + kk * 32), IDESC_Z, kk > 0);
@@ -218,7 +222,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_cons
                 umma_commit(smem_u32(&bar_gdone[g & 3]));
             }
             // ---- intra-chunk: dq += (hi + lo of dSs) K over the 64-key blocks
-            const int rq = 2 * NG, rk = 2 * NG + 1, rv = 2 * NG + 2;
+            const int rq = NG, rk = NG + 1, rv = NG + 2;
             if (ok) ok = mbar_wait(smem_u32(&bar_uempty[0]), (uint32_t)(NG >> 1) & 1, a.status);          // U_z read
             if (ok) ok = mbar_wait(smem_u32(&bar_uempty[1]), (uint32_t)((NG - 1) >> 1) & 1, a.status);    // last U read
             if (ok) ok = mbar_wait(smem_u32(&bar_full[slot_of(rq)]), use_of(rq) & 1, a.status);
@@ -304,8 +308,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_cons
             if (!(ok = group_wait(smem_u32(&bar_gdone[g & 3]), (uint32_t)(g >> 2) & 1, a.status, warp == 0, 1, 256, gflags,
                                   kg, &abort_s)))
                 break;
-            if (g == NG - 2) {   // block NG-2's products are done: its lo slot takes the normaliser matrix
-                const uint32_t zh = RING + slot_of(ZREQ) * RB;
+            if (g == ZFREE) {   // block ZFREE's products are done: its slot's upper half takes the normaliser
+                const uint32_t zh = RING + slot_of(ZREQ) * RB + PLANE;
                 z_tiles_store(smem + zh, smem + zh + 8192, zr, vs, threadIdx.x);
                 fence_proxy_async();
                 mbar_arrive(smem_u32(&bar_zrdy));
