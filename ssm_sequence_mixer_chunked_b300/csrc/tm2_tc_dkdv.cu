@@ -104,7 +104,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
     uint8_t* smem = smem_align1024(smem_raw);
     // gdone[g % 4]: the products of group g are done (its ring slots are free and its U buffer
     // is full): one commit per group serves the TMA producer and the compute warps
-    __shared__ __align__(8) uint64_t bar_ld, bar_full[NR], bar_gdone[4], bar_cvt, bar_sfull[4], bar_sfree[4],
+    __shared__ __align__(8) uint64_t bar_ld, bar_full[NR], bar_gdone[4], bar_cvt, bar_sfull[4], bar_pdone[4],
         bar_pfull[4], bar_uempty[2], bar_kvfull, bar_red, bar_zrdy, bar_done;
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_s;
@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
         mbar_init(smem_u32(&bar_cvt), 256);
         for (int b = 0; b < 4; ++b) {
             mbar_init(smem_u32(&bar_sfull[b]), 1);
-            mbar_init(smem_u32(&bar_sfree[b]), 256);
+            mbar_init(smem_u32(&bar_pdone[b]), 1);
             mbar_init(smem_u32(&bar_pfull[b]), 256);
         }
         for (int i = 0; i < 2; ++i) {
@@ -142,12 +142,6 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
         mbar_init(smem_u32(&bar_done), 1);
         abort_s = 0;
         fence_mbar_init();
-    }
-    for (int j = threadIdx.x; j < C; j += THREADS) {
-        const long tok = (long)c * C + j;
-        sAv[j] = a.Aloc[bh * a.Tp + tok];
-        sZe[j] = tok < a.T ? a.zeta[bh * a.T + tok] : 0.f;
-        sUc[j] = tok < a.T ? a.ucol[bh * a.T + tok] : 0.f;
     }
     if (warp == 0) {
         tmem_alloc(smem_u32(&tmem_base_s), 512);
@@ -250,11 +244,12 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
             tc_fence_after();
             const uint32_t SK = sb0 + RING + slot_of(rkv) * RB, SV = SK + 16384;
             const uint32_t SQ = sb0 + RING + slot_of(rq) * RB, SD = sb0 + RING + slot_of(rd) * RB;
-            for (int b = 0; b < nblk && ok; ++b) {
+            // block b + 1's scores go into S / W as soon as the compute warps have read block b's
+            // (pfull[b]), ahead of block b's products, so that the softmax-free weight step of
+            // b + 1 runs while those products do; pdone[b] tells the compute warps that the
+            // products of block b have read the P buffers they are about to overwrite
+            auto issue_sw = [&](int b) {
                 const int ib = 2 * tj + b;
-                if (abort_s) { ok = false; break; }
-                if (b > 0 && !(ok = mbar_wait(smem_u32(&bar_sfree[b - 1]), 0, a.status))) break;
-                tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                     umma_bf16(tmem + TM_S, sdesc_sw128(SK + kk * 32), sdesc_sw128(SQ + ib * 8192 + kk * 32), IDESC_BF_K,
@@ -263,8 +258,14 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
                               kk > 0);
                 }
                 umma_commit(smem_u32(&bar_sfull[b]));
+            };
+            if (ok && nblk > 0) issue_sw(0);
+            for (int b = 0; b < nblk && ok; ++b) {
+                const int ib = 2 * tj + b;
+                if (abort_s) { ok = false; break; }
                 if (!(ok = mbar_wait(smem_u32(&bar_pfull[b]), 0, a.status))) break;
                 tc_fence_after();
+                if (b + 1 < nblk) issue_sw(b + 1);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                     const uint64_t qd = sdesc_sw128_ex(SQ + ib * 8192 + kk * 2048, 8192, 1024);
@@ -275,6 +276,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
                     umma_bf16_ts(tmem + TM_DV, tmem + TM_WH + kk * 8, dd, IDESC_BF_MN, acc0);
                     umma_bf16_ts(tmem + TM_DV, tmem + TM_WL + kk * 8, dd, IDESC_BF_MN, 1u);
                 }
+                umma_commit(smem_u32(&bar_pdone[b]));
             }
             if (ok) umma_commit(smem_u32(&bar_kvfull));
             else abort_s = 1;
@@ -289,18 +291,28 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
         const long tok = (long)c * C + j;
         const bool in = tok < a.T;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-        const float Aj = sAv[j];
         float dv64_in = 0.f;
         int kg = 0;                                      // group-wait counter
         // global reads issued before the first wait, so their latency hides under the tile loads
         const float gsc = a.sscale[bh * NC + c];
         const float gcv = a.g[bh * NC + c];
         const float rowt = in ? a.rowterm[bh * a.T + tok] : 0.f;
+        const unsigned am_k = a.amax[bh * 4], am_v = a.amax[bh * 4 + 1];
+        // the chunk's per-token terms, one token per compute thread (C = 256), stored once the
+        // key tile has arrived and published by the group waits' barriers
+        static_assert(C == 256, "one chunk token per compute thread");
+        const long tok_s = (long)c * C + threadIdx.x;
+        const float av_s = a.Aloc[bh * a.Tp + tok_s];
+        const float ze_s = tok_s < a.T ? a.zeta[bh * a.T + tok_s] : 0.f;
+        const float uc_s = tok_s < a.T ? a.ucol[bh * a.T + tok_s] : 0.f;
         float* sDK = reinterpret_cast<float*>(smem + SDK);   // [m][row]: sum_col v_j[col] U[(m, col)]
 #pragma unroll
         for (int m = 0; m < 32; ++m) sDK[(32 * h + m) * 128 + l] = 0.f;
         float vj[32];   // this row's value columns 32h .. 32h + 31 (fp32)
         bool ok = mbar_wait(smem_u32(&bar_ld), 0, a.status);
+        sAv[threadIdx.x] = av_s;
+        sZe[threadIdx.x] = ze_s;
+        sUc[threadIdx.x] = uc_s;
         if (ok) {   // fp16 copy of the key tile (the A operand of U); this row's values
             const int t256 = threadIdx.x;
             for (int pc = t256; pc < 1024; pc += 256) tile_bf16_to_f16(early, sb0 + SKH, pc);
@@ -381,20 +393,20 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
         named_bar_sync(1, 256);
         tmem_st32(tmem + lane_base + TM_PARK + h * 64 + 32, dvx);
         tmem_wait_st();
+        const float Aj = sAv[j];
         // ---- intra-chunk blocks (queries i >= j)
         for (int b = 0; b < nblk && ok; ++b) {
             const int ib = 2 * tj + b;
             if (!(ok = group_wait(smem_u32(&bar_sfull[b]), 0, a.status, warp == 0, 1, 256, gflags, kg, &abort_s))) break;
-            // (the P buffer's last reader, the product of block b-1, was issued before this block's
-            // scores; the commit that announced them completes only after every earlier MMA of the
-            // issuing thread, so the buffer is free)
+            // both rounds' weights in registers while the products of block b - 1 may still read
+            // the P buffers; stored once those products are done
+            uint32_t dh[2][8], dl[2][8], wh[2][8], wl[2][8];
 #pragma unroll
             for (int g2 = 0; g2 < 2; ++g2) {
                 const int cc = 2 * h + g2;
                 float sv[16], wv[16];
                 tmem_ld16(tmem + lane_base + TM_S + cc * 16, sv);
                 tmem_ld16(tmem + lane_base + TM_W + cc * 16, wv);
-                uint32_t dh[8], dl[8], wh[8], wl[8];
 #pragma unroll
                 for (int k2 = 0; k2 < 8; ++k2) {
                     float d2h[2], d2l[2], w2h[2], w2l[2];
@@ -414,19 +426,26 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
                         w2h[u] = __bfloat162float(__float2bfloat16_rn(wz));
                         w2l[u] = wz - w2h[u];
                     }
-                    dh[k2] = pack_bf16x2(d2h[0], d2h[1]);
-                    dl[k2] = pack_bf16x2(d2l[0], d2l[1]);
-                    wh[k2] = pack_bf16x2(w2h[0], w2h[1]);
-                    wl[k2] = pack_bf16x2(w2l[0], w2l[1]);
+                    dh[g2][k2] = pack_bf16x2(d2h[0], d2h[1]);
+                    dl[g2][k2] = pack_bf16x2(d2l[0], d2l[1]);
+                    wh[g2][k2] = pack_bf16x2(w2h[0], w2h[1]);
+                    wl[g2][k2] = pack_bf16x2(w2l[0], w2l[1]);
                 }
-                tmem_st8(tmem + lane_base + TM_DH + cc * 8, dh);
-                tmem_st8(tmem + lane_base + TM_DL + cc * 8, dl);
-                tmem_st8(tmem + lane_base + TM_WH + cc * 8, wh);
-                tmem_st8(tmem + lane_base + TM_WL + cc * 8, wl);
+            }
+            if (b > 0 && !(ok = group_wait(smem_u32(&bar_pdone[b - 1]), 0, a.status, warp == 0, 1, 256, gflags, kg,
+                                           &abort_s)))
+                break;
+            tc_fence_after();
+#pragma unroll
+            for (int g2 = 0; g2 < 2; ++g2) {
+                const int cc = 2 * h + g2;
+                tmem_st8(tmem + lane_base + TM_DH + cc * 8, dh[g2]);
+                tmem_st8(tmem + lane_base + TM_DL + cc * 8, dl[g2]);
+                tmem_st8(tmem + lane_base + TM_WH + cc * 8, wh[g2]);
+                tmem_st8(tmem + lane_base + TM_WL + cc * 8, wl[g2]);
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(smem_u32(&bar_sfree[b]));
             mbar_arrive(smem_u32(&bar_pfull[b]));
         }
         if (ok && !abort_s && (ok = mbar_wait(smem_u32(&bar_kvfull), 0, a.status))) {
@@ -436,7 +455,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
             tmem_ld32(tmem + lane_base + TM_DV + h * 32, dv0);
             tmem_ld32(tmem + lane_base + TM_PARK + h * 64 + 32, dvx);
             const float wj = __expf(gcv - Aj);
-            const float ks = pow2_scale(a.amax[bh * 4]), vs = pow2_scale(a.amax[bh * 4 + 1]);
+            const float ks = pow2_scale(am_k), vs = pow2_scale(am_v);
             const float gu = gsc / (ks * ks * vs);   // Gamma_c out of the planes' units (exact)
             const float fk = 2.f * wj * gu, fv = wj * gu;
             float vdot = 0.f;
