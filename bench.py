@@ -43,7 +43,11 @@ METRIC = "2Mamba fwd+bwd tokens/s at T=8192 on 1 B300; % bf16 tensor peak; decod
 FLUSH_BYTES = 256 << 20
 # kernels launched beside another one (their event-timed span includes sharing the SMs)
 OVERLAPPED = {"tc_bwd_dq": "runs beside the reverse state walk (which has stream priority); the span is "
-                           "from its first to its last CTA, not its own device time"}
+                           "from its first to its last CTA, not its own device time",
+              "tc_state_scan_fwd": "two concurrent launches per step (the heads in two halves on two streams); "
+                                   "the sum of their spans exceeds the walk's wall time",
+              "tc_chunk_out": "two launches per step, the first beside the second half's walk; the sum of "
+                              "their spans includes that sharing"}
 
 
 def peaks():
@@ -472,8 +476,10 @@ def run_tm2(args, world, rank, device):
     per_kernel_roof = {}
     for n, a in kern.items():
         if n.startswith("tc_"):
+            # per step: every tc kernel covers the step's B H T token-heads once, in one launch
+            # or (the split forward) two; the time is the sum of its launches' spans per step
             r = roofline(n, kernel_flops(n, d, dv, 256, per_launch_tokens), kernel_bytes(n, d, dv, 256, per_launch_tokens),
-                         a["ms_per_launch"], pk, True, peak_key)
+                         a["ms"] / args.steps, pk, True, peak_key)
             if r is not None:
                 per_kernel_roof[n] = {"bound": r["bound"], "frac": round(r["frac"], 4),
                                       "tensor_frac": round(r["tensor_frac"], 4), "hbm_frac": round(r["hbm_frac"], 4)}

@@ -194,26 +194,28 @@ struct TraceScope {
     }
 };
 
-// A high-priority stream per device that takes the backward's reverse state walk, so that dq,
-// which reads only the forward states, runs beside it on the caller's stream: the block
-// scheduler prefers the walk's CTAs and dq's CTAs fill the SMs its last wave leaves idle.
-// Fork and join are events made per call (destroyed once their work is enqueued).
-static cudaError_t side_stream(cudaStream_t* out) {
+// High-priority streams per device (two) that take the state walks, so that readouts run beside
+// them on the caller's stream: the block scheduler prefers the walks' CTAs and the readouts'
+// CTAs fill the SMs a walk's last wave leaves idle.  The backward's reverse walk runs beside dq
+// (which reads only the forward states); the forward splits the heads into two halves whose
+// walks run concurrently, each half's chunk output following its own walk.  Fork and join are
+// events made per call (destroyed once their work is enqueued).
+static cudaError_t side_stream(cudaStream_t* out, int which = 0) {
     static std::mutex mu;
-    static cudaStream_t streams[64] = {};
+    static cudaStream_t streams[64][2] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (dev < 0 || dev >= 64 || which < 0 || which > 1) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lk(mu);
-    if (!streams[dev]) {
+    if (!streams[dev][which]) {
         int least = 0, greatest = 0;
         e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
         if (e != cudaSuccess) return e;
-        e = cudaStreamCreateWithPriority(&streams[dev], cudaStreamNonBlocking, greatest);
+        e = cudaStreamCreateWithPriority(&streams[dev][which], cudaStreamNonBlocking, greatest);
         if (e != cudaSuccess) return e;
     }
-    *out = streams[dev];
+    *out = streams[dev][which];
     return cudaSuccess;
 }
 
@@ -333,11 +335,53 @@ int tm2_forward(const void* q, const void* k, const void* v, const float* a, con
         TM2_RUN("head_absmax", launch_head_absmax(p, k, v, amax, true, s));
         TM2_RUN("tc_scan_operands",
                 launch_tc_scan_operands(p, false, k, v, Aloc, g, nullptr, nullptr, nullptr, amax, ops, s));
-        ScanIO io{};
-        io.rev = false; io.ops = ops; io.g = g; io.S0 = S0; io.z0 = z0; io.amax = amax;
-        io.Sx = states; io.zx = zx; io.S_final = S_final; io.z_final = z_final;
-        TM2_RUN("tc_state_scan_fwd", tc_state_scan(p, io, s));
-        TM2_RUN("tc_chunk_out", tc_chunk_out(p, q, k, v, Aloc, states, zx, amax, (float*)o, Z, s));
+        // Every walk CTA takes about the same time, so the last of its waves leaves most SMs
+        // idle.  The heads are split into two halves walked concurrently on the two side
+        // streams; the first half's chunk output (on the caller's stream) starts as soon as its
+        // walk is done and fills the SMs the second half's walk leaves idle.
+        const long BH = p.BH();
+        const int parts = BH >= 2 ? 2 : 1;
+        const size_t T = (size_t)p.T, Tp = (size_t)p.Tp(), NC = (size_t)p.NC;
+        ForkJoin fj[2];
+        cudaStream_t side[2] = {nullptr, nullptr};
+        for (int i = 0; i < parts; ++i) {
+            TM2_CK(side_stream(&side[i], i));
+            TM2_CK(fj[i].make());
+        }
+        TM2_CK(cudaEventRecord(fj[0].fork, s));
+        Problem pp[2];
+        ScanIO io[2];
+        for (int i = 0; i < parts; ++i) {
+            const long lo = BH * i / parts, hi = BH * (i + 1) / parts;
+            pp[i] = p;
+            pp[i].B = 1;
+            pp[i].H = (int)(hi - lo);
+            io[i] = ScanIO{};
+            io[i].rev = false;
+            io[i].ops = (const char*)ops + (size_t)lo * Tp * 2 * TC_OPS_ROWS;   // [BH][Tp/64][144][64] fp16
+            io[i].g = g + lo * NC;
+            io[i].S0 = S0 ? S0 + lo * 4096 * 64 : nullptr;
+            io[i].z0 = z0 ? z0 + lo * 4096 : nullptr;
+            io[i].amax = amax + lo * 4;
+            io[i].Sx = (char*)states + (size_t)lo * NC * 2 * TC_PACKED_ROWS * 64 * 2;   // packed planes
+            io[i].zx = zx + lo * NC * 4096;
+            io[i].S_final = S_final ? S_final + lo * 4096 * 64 : nullptr;
+            io[i].z_final = z_final ? z_final + lo * 4096 : nullptr;
+            TM2_CK(cudaStreamWaitEvent(side[i], fj[0].fork, 0));
+            {
+                cudaStream_t s = side[i];
+                TM2_RUN("tc_state_scan_fwd", tc_state_scan(pp[i], io[i], s));
+            }
+            TM2_CK(cudaEventRecord(fj[i].join, side[i]));
+        }
+        for (int i = 0; i < parts; ++i) {
+            const long lo = BH * i / parts;
+            const size_t tok = (size_t)lo * T;
+            TM2_CK(cudaStreamWaitEvent(s, fj[i].join, 0));
+            TM2_RUN("tc_chunk_out", tc_chunk_out(pp[i], (const char*)q + tok * 64 * 2, (const char*)k + tok * 64 * 2,
+                                                 (const char*)v + tok * 64 * 2, Aloc + lo * Tp, io[i].Sx, io[i].zx,
+                                                 io[i].amax, (float*)o + tok * 64, Z ? Z + tok : nullptr, s));
+        }
         return TM2_OK;
     }
     TM2_RUN("state_scan_fwd", simt_state_scan_fwd(p, k, v, Aloc, g, S0, z0, states, S_final, z_final, s));
