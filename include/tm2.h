@@ -33,7 +33,10 @@
  *  - State layout: S is (B,H,d*d,dv) with row r = m*d + n (key feature indices m, n);
  *    z is (B,H,d*d).  The same layout serves forward (initial/final state) and decode.
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream).
- *    Calls are asynchronous and never synchronise the host.
+ *    Calls are asynchronous and never synchronise the host.  The tensor-core forward and
+ *    backward also run their state walks on two high-priority streams of the library's own
+ *    (created once per device), forked from `stream` and joined back into it with events,
+ *    so the call's work is ordered with respect to `stream` as if it all ran there.
  *  - Argument errors are reported before anything is launched.  A launch failure
  *    returns TM2_ERR_CUDA.  Kernels whose waits are bounded record TM2_ERR_TIMEOUT in
  *    a per-device status word that tm2_poll_status() returns after the stream drains.
