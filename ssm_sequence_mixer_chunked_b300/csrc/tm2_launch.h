@@ -56,9 +56,12 @@ constexpr int TC_CHUNK = 256;
 // (m, n) index square of the d^2 = 4096 state rows is cut into 16 x 16 blocks and only the 10
 // blocks with bm <= bn are kept, block (bm, bn) at index bm * 4 - bm (bm - 1) / 2 + (bn - bm),
 // its rows ordered r = 16 (m - 16 bm) + (n - 16 bn).  The state is symmetric in (m, n) up to the
-// initial state's antisymmetric part, which no readout sees, so an off-diagonal block is stored
-// doubled (it stands for (m, n) and (n, m)) and a diagonal block as is:
+// initial state's antisymmetric part, which no readout sees.  In the forward states an
+// off-diagonal block is stored doubled (it stands for (m, n) and (n, m)) and a diagonal block
+// as is, so the readouts contract each stored row once:
 //   sum_{m,n} x[m] x[n] S[(m,n), :] = sum_{blocks} sum_{(m,n) in block} x[m] x[n] T[(m,n), :].
+// The gradient states (no initial state, exactly symmetric) are stored as they are: dk/dv reads
+// each off-diagonal block in both orientations (make_tmap_state_packed_quads / _tquads).
 // Layout [BH][NC][2 planes][TC_PACKED_ROWS][64] fp16; the normaliser states stay full.
 constexpr int TC_PACKED_BLOCKS = 10;
 constexpr int TC_PACKED_ROWS = TC_PACKED_BLOCKS * 256;
@@ -72,8 +75,9 @@ __host__ __device__ inline void tc_block_of(int idx, int& bm, int& bn) {   // in
 // zero); S_final/z_final (optional) = the state after the last token.  Reverse (rev = true):
 // key = q, val = dO, normaliser column ucol, weight exp(A_i) zeta_i; slot c = the gradient
 // w.r.t. the state at the end of chunk c, scaled per (slot, CTA) by 1/sscale.
-// Sx: forward [BH][NC][2][TC_PACKED_ROWS][64] block-packed, reverse [BH][NC][2][4096][64] fp16
-// (hi plane, residual plane); zx: [BH][NC][4096] fp32 (full layout in both walks).
+// Sx: [BH][NC][2][TC_PACKED_ROWS][64] block-packed fp16 (hi plane, residual plane; forward
+// off-diagonal blocks doubled, reverse as is); zx: [BH][NC][4096] fp32 (full layout in both
+// walks).
 struct ScanIO {
     bool rev;
     const void* ops;       // operand blocks from launch_tc_scan_operands

@@ -85,6 +85,13 @@ bool make_tmap_state_packed_quads(CUtensorMap* map, const void* base, uint64_t n
     return make_tmap_f16_nd(map, base, 4, dims, strides, box);
 }
 
+bool make_tmap_state_packed_tquads(CUtensorMap* map, const void* base, uint64_t nchunks) {
+    const uint64_t dims[4] = {64, 16, 16, (uint64_t)TC_PACKED_BLOCKS * 2 * nchunks};
+    const uint64_t strides[3] = {16 * 128, 128, 256 * 128};
+    const uint32_t box[4] = {64, 16, 4, 1};
+    return make_tmap_f16_nd(map, base, 4, dims, strides, box);
+}
+
 bool make_tmap_state_packed_blocks(CUtensorMap* map, const void* base, uint64_t nchunks) {
     const uint64_t dims[3] = {64, (uint64_t)TC_PACKED_ROWS, 2 * nchunks};
     const uint64_t strides[2] = {128, (uint64_t)TC_PACKED_ROWS * 128};

@@ -35,6 +35,10 @@ bool make_tmap_state_packed_quads(CUtensorMap* map, const void* base, uint64_t n
 // One whole block plane of the block-packed states as [256 rows][64] (32 KB), rows r = 16 m' + n'.
 // Coordinates (0, 256 block, 2 chunk + plane).
 bool make_tmap_state_packed_blocks(CUtensorMap* map, const void* base, uint64_t nchunks);
+// Block-packed states seen the other way round: all 16 rows m' of one 16 x 16 block for four
+// of its columns n' = 4 nq .. 4 nq + 3 (smem [n'][m'][col], 8 KB).  Coordinates
+// (0, 0, 4 nq, 10 (2 chunk + plane) + block).
+bool make_tmap_state_packed_tquads(CUtensorMap* map, const void* base, uint64_t nchunks);
 bool make_tmap_state_tquads(CUtensorMap* map, const void* base, uint64_t nchunks);
 
 // Reads (and optionally clears) the device status word of the current device.

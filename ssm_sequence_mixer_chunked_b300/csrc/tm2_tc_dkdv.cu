@@ -14,8 +14,9 @@
 // when normalised; dVt_j[dv] = sum_i W_ij zeta_i ucol_i + w_j Gamma_c sum_{m,n} k_j[m] k_j[n] dz[(m,n)]).
 //
 // One CTA per (128-key tile, chunk, b, h).  The inter-chunk sums run first, over 16 groups of
-// four state slices n = 4g .. 4g+3, each one TMA box per plane ([n'][m][col], fp16 hi and
-// residual planes), as one product per group,
+// four state slices n = 4g .. 4g+3, four 8 KB TMA boxes per plane (fp16 hi and residual planes
+// of the block-packed gradient state: for each 16-row block of m the stored block holding the
+// rows (m, n), or its mirror rows (n, m); both land as [n'][m'][col]), as one product per group,
 //   U_g[j][(n', col)]  = sum_m k_j[m] dS[(m, 4g+n'), col]     (N = 256, the box MN-major),
 // double-buffered in tensor memory.  dS is symmetric in (m, n), so U_g also carries the key
 // term: the compute warps fold it into dvx[col] += k_j[4g+n'] U_g[j][(n', col)] (registers)
@@ -99,6 +100,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
                                                                  const __grid_constant__ CUtensorMap tmQ,
                                                                  const __grid_constant__ CUtensorMap tmD,
                                                                  const __grid_constant__ CUtensorMap tmS,
+                                                                 const __grid_constant__ CUtensorMap tmSt,
                                                                  const __grid_constant__ Args a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_align1024(smem_raw);
@@ -179,7 +181,19 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
                 const uint32_t fb = smem_u32(&bar_full[sl]), dst = sb0 + RING + sl * RB;
                 mbar_arrive_expect_tx(fb, RB);
                 if (r < 2 * NG) {
-                    tma_load_5d(dst, &tmS, fb, 0, 0, 4 * (r >> 1), r & 1, chunk_id);
+                    // the rows (m, n) of key indices n = 4 nq .. 4 nq + 3 (block column bn) for every m,
+                    // one 8 KB box per 16-row block bm of m, landing as [n'][m'][col]: from the
+                    // stored block (bm, bn) (tmSt: contract over its first index) when bm <= bn,
+                    // else as the mirror rows (n, m) of the stored block (bn, bm) (tmS: contract
+                    // over its second index); the gradient state is symmetric and stored as is
+                    const int g = r >> 1, bn = g >> 2, nq = g & 3, pc = 2 * chunk_id + (r & 1);
+                    for (int bm = 0; bm < 4; ++bm) {
+                        if (bm <= bn)
+                            tma_load_4d(dst + bm * 8192, &tmSt, fb, 0, 0, 4 * nq,
+                                        TC_PACKED_BLOCKS * pc + tc_block_index(bm, bn));
+                        else
+                            tma_load_4d(dst + bm * 8192, &tmS, fb, 0, 0, 16 * tc_block_index(bn, bm) + 4 * nq, pc);
+                    }
                 } else if (r == 2 * NG) {
                     tma_load_3d(dst, &tmK, fb, 0, c * C + tj * 128, (int)bh);
                     tma_load_3d(dst + 16384, &tmV, fb, 0, c * C + tj * 128, (int)bh);
@@ -213,13 +227,14 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
                 const uint32_t d = tmem + ub * 256;
                 if (g < NG) {
                     const uint32_t bhi = sb0 + RING + slot_of(2 * g) * RB, blo = sb0 + RING + slot_of(2 * g + 1) * RB;
+                    // K block kk = m in 16 kk .. 16 kk + 15: box kk ([n'][m'][col], n' blocks 2 KB apart)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        umma_bf16(d, sdesc_sw128(sb0 + SKH + kk * 32), sdesc_sw128_ex(bhi + kk * 2048, 8192, 1024), IDESC_U,
+                        umma_bf16(d, sdesc_sw128(sb0 + SKH + kk * 32), sdesc_sw128_ex(bhi + kk * 8192, 2048, 1024), IDESC_U,
                                   kk > 0);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        umma_bf16(d, sdesc_sw128(sb0 + SKH + kk * 32), sdesc_sw128_ex(blo + kk * 2048, 8192, 1024), IDESC_U,
+                        umma_bf16(d, sdesc_sw128(sb0 + SKH + kk * 32), sdesc_sw128_ex(blo + kk * 8192, 2048, 1024), IDESC_U,
                                   1u);
 
                 } else {
@@ -486,11 +501,12 @@ cudaError_t tc_bwd_dkdv(const Problem& p, const void* q, const void* k, const vo
                         const float* Aloc, const float* g, const float* zeta, const float* ucol, const float* rowterm,
                         const void* dSx, const float* dzx, const float* sscale, const unsigned* amax_r, void* dk,
                         void* dv, float* dcum, cudaStream_t s) {
-    CUtensorMap tk, tv, tq, td, ts;
+    CUtensorMap tk, tv, tq, td, ts, tst;
     const uint64_t BH = (uint64_t)p.BH(), T = (uint64_t)p.T;
     if (!make_tmap_bf16_3d(&tk, k, BH, T, 64, 128) || !make_tmap_bf16_3d(&tv, v, BH, T, 64, 128) ||
         !make_tmap_bf16_3d(&tq, q, BH, T, 64, 256) || !make_tmap_bf16_3d(&td, dO, BH, T, 64, 256) ||
-        !make_tmap_state_tquads(&ts, dSx, BH * (uint64_t)p.NC))
+        !make_tmap_state_packed_quads(&ts, dSx, BH * (uint64_t)p.NC) ||
+        !make_tmap_state_packed_tquads(&tst, dSx, BH * (uint64_t)p.NC))
         return cudaErrorInvalidValue;
     int* status = tc_status_ptr();
     if (!status) return cudaErrorInvalidValue;
@@ -499,7 +515,7 @@ cudaError_t tc_bwd_dkdv(const Problem& p, const void* q, const void* k, const vo
     cudaError_t e = cudaFuncSetAttribute(tc_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, BYTES);
     if (e != cudaSuccess) return e;
     dim3 grid(2 * p.NC, (unsigned)p.BH());
-    tc_bwd_dkdv_kernel<<<grid, THREADS, BYTES, s>>>(tk, tv, tq, td, ts, a);
+    tc_bwd_dkdv_kernel<<<grid, THREADS, BYTES, s>>>(tk, tv, tq, td, ts, tst, a);
     return cudaGetLastError();
 }
 

@@ -9,8 +9,9 @@
 //     dS_{c-1} = exp(g_c) dS_c + sum_{i in c} exp(A_i) zeta_i (q_i (x) q_i) [dO_i, ucol_i]^T,
 // with zeta_i = 1/Z_i and ucol_i = -dO_i . o_i (normalised) or zeta = 1, ucol = 0.
 //
-// One CTA owns 256 state rows r = m*64 + n with m in {4Q .. 4Q + 3} of one (b, h) and walks
-// every chunk in order.  The chunk's contribution is computed with the state rows on M,
+// One CTA owns one 16 x 16 block (bm <= bn) of the (m, n) index square of one (b, h), 256 state
+// rows r = 16 (m - 16 bm) + (n - 16 bn) (the block-packed layout of tm2_launch.h; the state is
+// symmetric in (m, n), so 10 of the 16 blocks carry it), and walks every chunk in order.  The chunk's contribution is computed with the state rows on M,
 //     H[(m,n)][col] = sum_j (key_j[m] key_j[n]) (w_j val_j[col]),
 // as tcgen05.mma with M = 128 state rows (two M-blocks per CTA), N = 80 (the 64 value columns,
 // the normaliser column and 15 zero rows of the operand block) and K = tokens; the key (x)
@@ -104,11 +105,11 @@ struct Args {
     const unsigned* amax; // [BH][4] operand maxima (fp32 bits): key, value, normaliser (reverse)
     int* status;
     int T, NC, Tp, rev;
-    int packed;           // forward only: export the block-packed layout (see tm2_launch.h)
+    int packed;           // export the block-packed layout (see tm2_launch.h)
 };
 
 // The state rows of CTA Q.  Full layout: rows r = 64 m' + n of m = 4Q + m', i.e. (m, n) =
-// (4Q + r / 64, r % 64).  Block-packed (the forward walk): CTA Q owns the 16 x 16 block (bm, bn),
+// (4Q + r / 64, r % 64).  Block-packed (both walks): CTA Q owns the 16 x 16 block (bm, bn),
 // bm <= bn, Q = tc_block_index(bm, bn), rows r = 16 m' + n', (m, n) = (16 bm + m', 16 bn + n').
 TM2_DEV void row_mn(bool packed, int Q, int bm, int bn, int r, int& m, int& n) {
     if (packed) {
@@ -150,7 +151,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
     const int nchunks = rev ? NC - 1 : NC;   // the reverse walk never needs the update of chunk 0
     const int nstages = nchunks * SPC;
     const uint32_t sbase = smem_u32(smem);
-    const bool packed = a.packed != 0 && !rev;
+    const bool packed = a.packed != 0;
     int bm = 0, bn = 0;
     if (packed) tc_block_of(Q, bm, bn);
 
@@ -308,9 +309,12 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
         row_mn(packed, Q, bm, bn, r, m, n);
         const long R = (long)m * 64 + n;          // the row in the full (m, n) layout
         const long Rm = (long)n * 64 + m;         // its mirror (m, n) -> (n, m)
-        // an off-diagonal block of the packed layout stands for both (m, n) and (n, m): it is
-        // exported doubled, and S0 / S_final / the normaliser carry both rows
+        // an off-diagonal block of the packed layout stands for both (m, n) and (n, m): the
+        // forward exports it doubled (its readouts contract each stored row once), the reverse
+        // as is (dk/dv reads each stored block in both orientations), and S0 / S_final / the
+        // normaliser carry both rows
         const bool mirror = packed && bm != bn;
+        const bool twice = mirror && !rev;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         // units of the running state (see the header): forward value columns ks^2 vs, forward
         // normaliser ks^2; the reverse normaliser column is brought to ks^2 vs by vs / zs
@@ -348,7 +352,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
         // as fp32 straight to zx
         const uint32_t stg = sbase + SMEM_STG;
         auto export_row = [&](int slot) {
-            const float inv = (mirror ? 2.f : 1.f) / gam;
+            const float inv = (twice ? 2.f : 1.f) / gam;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {   // 16-byte chunk j: columns 8j .. 8j + 7
                 uint32_t hi[4], lo[4];
@@ -475,7 +479,7 @@ cudaError_t tc_state_scan(const Problem& p, const ScanIO& io, cudaStream_t s) {
     const uint64_t strides[2] = {128, (uint64_t)TC_OPS_ROWS * 128};
     const uint32_t box[3] = {64, (uint32_t)TC_OPS_ROWS, 1};
     if (!make_tmap_f16_nd(&tops, io.ops, 3, dims, strides, box)) return cudaErrorInvalidValue;
-    const bool packed = !io.rev;   // the forward walk exports the block-packed layout
+    const bool packed = true;   // both walks export the block-packed layout
     CUtensorMap tsx;   // the state planes as (64 columns, rows, BH x NC x 2 planes), 256-row boxes
     const uint64_t rows = packed ? (uint64_t)TC_PACKED_ROWS : 4096;
     const uint64_t sdims[3] = {64, rows, BH * (uint64_t)p.NC * 2};
