@@ -85,16 +85,17 @@ def packed_rows(d):
 def kernel_flops(name, d, dv, C, tokens):
     """Algorithmic flops of one launch of a named kernel over `tokens` token-heads: the
     method's own work at chunk length C (causal pairs only, no recompute counted twice;
-    the tensor-core kernels' hi + lo split of operands is not counted).  The forward walk, the
-    chunk output and dq work on the block-packed state (packed_rows of the d^2 rows: the state
-    is symmetric in its two key indices); dk/dv contracts the full gradient state once and
-    takes the key term from the same product (2 d dv more per token)."""
+    the tensor-core kernels' hi + lo split of operands is not counted).  Both walks, the chunk
+    output and dq work on the block-packed state (packed_rows of the d^2 rows: the state is
+    symmetric in its two key indices); dk/dv contracts the full gradient state once (each stored
+    off-diagonal block in both orientations) and takes the key term from the same product
+    (2 d dv more per token)."""
     dv1 = dv + 1
     state = 2 * d * d * dv1          # one d^2 x (dv+1) contraction per token
     pstate = 2 * packed_rows(d) * dv1
     per = {
         "tc_state_scan_fwd": pstate + 2 * packed_rows(d) * dv1 / C,
-        "tc_state_scan_bwd": state + 2 * d * d * dv1 / C,
+        "tc_state_scan_bwd": pstate + 2 * packed_rows(d) * dv1 / C,
         "tc_chunk_out": pstate + (C + 1) * (d + dv),
         "tc_bwd_dq": pstate + (C + 1) * (d + dv),
         "tc_bwd_dkdv": state + 2 * d * dv + (C + 1) * (2 * d + dv),
@@ -111,17 +112,17 @@ def kernel_bytes(name, d, dv, C, tokens, in_bytes=2):
     must read or write (inputs and the gradients dq, dk, dv in the input type, o and the
     per-token scalars in fp32), plus the chunk states it must write or read (two fp16 planes of
     d^2 x dv and the fp32 normaliser column per chunk, amortised over the C tokens of a
-    chunk).  The forward walk, the chunk output and dq move the block-packed state (packed_rows
-    of the d^2 rows; the normaliser stays full).  Scratch the implementation adds (operand
+    chunk).  Every kernel moves the block-packed state (packed_rows of the d^2 rows; the
+    normaliser stays full).  Scratch the implementation adds (operand
     blocks) is not counted."""
     state = (2 * 2 * d * d * dv + 4 * d * d) / C
     pstate = (2 * 2 * packed_rows(d) * dv + 4 * d * d) / C
     per = {
         "tc_state_scan_fwd": pstate + in_bytes * (d + dv),
-        "tc_state_scan_bwd": state + in_bytes * (d + dv) + 4 * 2,
+        "tc_state_scan_bwd": pstate + in_bytes * (d + dv) + 4 * 2,
         "tc_chunk_out": pstate + in_bytes * (2 * d + dv) + 4 * (dv + 1),
         "tc_bwd_dq": pstate + in_bytes * (2 * d + 2 * dv) + in_bytes * d + 4 * 2,
-        "tc_bwd_dkdv": state + in_bytes * (2 * d + 2 * dv) + in_bytes * (d + dv) + 4 * 4,
+        "tc_bwd_dkdv": pstate + in_bytes * (2 * d + 2 * dv) + in_bytes * (d + dv) + 4 * 4,
     }.get(name)
     return None if per is None else per * tokens
 

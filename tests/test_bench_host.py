@@ -26,7 +26,7 @@ def test_chunk_state_bytes_per_token_head():
     # the forward walk also reads each token's k and v rows (bf16, 64 + 64 values)
     assert bench.packed_rows(D) == 2560   # 10 of the 16 blocks of 16 x 16
     assert bench.kernel_bytes("tc_state_scan_fwd", D, DV, C, 1) == 2624 + 256   # packed planes + z
-    assert bench.kernel_bytes("tc_state_scan_bwd", D, DV, C, 1) == 4160 + 256 + 8
+    assert bench.kernel_bytes("tc_state_scan_bwd", D, DV, C, 1) == 2624 + 256 + 8   # packed gradient state
 
 
 def test_algorithmic_units_per_token_head():
@@ -34,14 +34,14 @@ def test_algorithmic_units_per_token_head():
     # one state update per chunk (2 * 4096 * 65 / 256 = 2,080 per token); a readout adds the
     # causal pairs of its chunk, (C+1)/2 per token on average, each a 64-dot and a 64-axpy
     assert bench.kernel_flops("tc_state_scan_fwd", D, DV, C, 1) == 2 * 2560 * 65 + 2 * 2560 * 65 / 256
-    assert bench.kernel_flops("tc_state_scan_bwd", D, DV, C, 1) == 534_560
+    assert bench.kernel_flops("tc_state_scan_bwd", D, DV, C, 1) == 2 * 2560 * 65 + 2 * 2560 * 65 / 256
     assert bench.kernel_flops("tc_chunk_out", D, DV, C, 1) == 2 * 2560 * 65 + 257 * 128
     assert bench.kernel_flops("tc_bwd_dq", D, DV, C, 1) == 2 * 2560 * 65 + 257 * 128
     assert bench.kernel_flops("tc_bwd_dkdv", D, DV, C, 1) == 532_480 + 2 * 64 * 64 + 257 * 192
     # bytes: the chunk state (4,160) plus the token rows each kernel must move
     assert bench.kernel_bytes("tc_chunk_out", D, DV, C, 1) == 2624 + 2 * 192 + 4 * 65       # q k v in; o, Z out
     assert bench.kernel_bytes("tc_bwd_dq", D, DV, C, 1) == 2624 + 2 * 256 + 2 * 64 + 4 * 2   # q k v dO in; dq (bf16), two scalars
-    assert bench.kernel_bytes("tc_bwd_dkdv", D, DV, C, 1) == 4160 + 2 * 256 + 2 * 128 + 4 * 4
+    assert bench.kernel_bytes("tc_bwd_dkdv", D, DV, C, 1) == 2624 + 2 * 256 + 2 * 128 + 4 * 4
     # decode: the fp32 state read and written once, full (d^2 rows) or symmetric-packed (d(d+1)/2)
     assert bench.decode_bytes_per_head(64, 64) - bench.decode_bytes_per_head(64, 64, packed=True) == \
         2 * (4096 - 2080) * (64 + 1) * 4
@@ -59,8 +59,8 @@ def test_roofline_picks_the_slower_bound():
     assert r["frac"] == pytest.approx(r["achieved"] / PK["hbm_gbs"])
     assert r["tensor_frac"] == pytest.approx(kf / 0.616e-3 / 1e12 / PK["bf16_tflops_sustained"])
     # dk/dv (one contraction of the full gradient state per token, the key term taken from the
-    # same product) is HBM-bound against either tensor figure: 1.30 GB at 6.5 TB/s (0.20 ms)
-    # against 155 GFLOP (0.11 ms sustained, 0.09 ms burst)
+    # same product, the packed state read) is HBM-bound against either tensor figure: 0.89 GB at
+    # 6.5 TB/s (0.14 ms) against 155 GFLOP (0.11 ms sustained, 0.09 ms burst)
     kf = bench.kernel_flops("tc_bwd_dkdv", D, DV, C, TOKENS)
     kb = bench.kernel_bytes("tc_bwd_dkdv", D, DV, C, TOKENS)
     for key in ("bf16_tflops_sustained", "bf16_tflops"):
