@@ -578,7 +578,7 @@ int tm2e_step(const void* q, const void* k, const void* v, const float* a, void*
     const void* ptrs[] = {q, k, v, a, K_cache, V_cache, cum_cache, o, lse};
     for (const void* x : ptrs)
         if (!aligned16(x)) return TM2_ERR_ALIGNMENT;
-    const int ns = e_decode_splits(pos);
+    const int ns = e_decode_splits(NH, pos);
     float* part = nullptr;
     if (ns > 1) {
         const int st = check_ws(ws, ws_bytes, tm2e_step_workspace(N, H, L, d, dv, dtype));

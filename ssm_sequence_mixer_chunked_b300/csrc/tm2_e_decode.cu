@@ -10,7 +10,10 @@
 // with k_t, v_t appended to the cache.
 //
 // The step reads the whole cache once, so it is bound by HBM bandwidth.  The keys 0..t of a
-// (sequence, head) are split into ranges of KPS; one block per (range, head): a producer warp
+// (sequence, head) are split into ranges (at least 512 keys each, as few as give about eight
+// waves of blocks: per-block set-up and the combine cost less with long ranges, measured 0.49 ms
+// at 512 keys against 0.445 at 2048 for 64 x 16 heads at context 8192); one block per (range,
+// head): a producer warp
 // streams the range's key and value rows into shared memory with bulk copies (stages of 64
 // keys, four in flight, so the loads in flight do not depend on registers), and four consumer
 // warps walk each stage with groups of D / 8 lanes per key (each lane 8 elements), an online
@@ -27,7 +30,7 @@
 
 namespace tm2 {
 
-constexpr int E_DEC_KPS = 512;   // keys per range (one block)
+constexpr int E_DEC_KPS = 512;   // fewest keys per range (one block)
 constexpr int E_DEC_STAGE = 64;  // keys per bulk-copy stage
 constexpr int E_DEC_NST = 4;     // stages in flight
 
@@ -49,7 +52,7 @@ template <int D, int DV, typename Tin>
 __global__ void __launch_bounds__(160) e_decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
                                                        const Tin* __restrict__ v, const float* __restrict__ a,
                                                        Tin* __restrict__ Kc, Tin* __restrict__ Vc,
-                                                       float* __restrict__ cumc, int pos, int L, float scale,
+                                                       float* __restrict__ cumc, int pos, int L, int kps, float scale,
                                                        float* __restrict__ part, float* __restrict__ o,
                                                        float* __restrict__ lse, int* status) {
     static_assert(D == DV, "one group of lanes covers a key row and a value row");
@@ -66,7 +69,7 @@ __global__ void __launch_bounds__(160) e_decode_kernel(const Tin* __restrict__ q
     const long s = blockIdx.y;
     const int sp = blockIdx.x, nsplit = gridDim.x;
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int j0 = sp * E_DEC_KPS, j1 = min(j0 + E_DEC_KPS, pos + 1);
+    const int j0 = sp * kps, j1 = min(j0 + kps, pos + 1);
     const int nst = (j1 - j0 + E_DEC_STAGE - 1) / E_DEC_STAGE;
     const uint32_t sbase = smem_u32(smem);
     if (tid == 0) {
@@ -226,14 +229,32 @@ __global__ void e_decode_combine_kernel(const float* __restrict__ part, int nspl
     if (c == 0 && lse) lse[s] = (M + log2f(Ls)) * LN2;
 }
 
-int e_decode_splits(int pos) { return (pos + E_DEC_KPS) / E_DEC_KPS; }
+// Ranges of the step at position pos: kps keys each (a multiple of the stage), ns of them; the
+// last one holds pos.  About eight waves of blocks (three resident per SM), ranges of at least
+// E_DEC_KPS keys.
+static void e_decode_plan(long NH, int pos, int& ns, int& kps) {
+    const int keys = pos + 1;
+    int sms = 148, dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long maxs = (keys + E_DEC_KPS - 1) / E_DEC_KPS;
+    const long want = (8L * 3 * sms + NH - 1) / std::max(1L, NH);
+    const int n0 = (int)std::max(1L, std::min(maxs, want));
+    kps = ((keys + n0 - 1) / n0 + E_DEC_STAGE - 1) / E_DEC_STAGE * E_DEC_STAGE;
+    ns = (keys + kps - 1) / kps;
+}
+int e_decode_splits(long NH, int pos) {
+    int ns, kps;
+    e_decode_plan(NH, pos, ns, kps);
+    return ns;
+}
 int e_decode_max_splits(int L) { return (L + E_DEC_KPS - 1) / E_DEC_KPS; }
 
 template <int D, typename Tin>
 static cudaError_t e_decode_run(long NH, int pos, int L, float scale, const void* q, const void* k, const void* v,
                                 const float* a, void* Kc, void* Vc, float* cumc, float* part, float* o, float* lse,
                                 cudaStream_t s) {
-    const int ns = e_decode_splits(pos);
+    int ns, kps;
+    e_decode_plan(NH, pos, ns, kps);
     dim3 grid((unsigned)ns, (unsigned)NH);
     int* status = tc_status_ptr();
     if (!status) return cudaErrorInvalidValue;
@@ -241,7 +262,7 @@ static cudaError_t e_decode_run(long NH, int pos, int L, float scale, const void
     cudaError_t e = cudaFuncSetAttribute(e_decode_kernel<D, D, Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     e_decode_kernel<D, D, Tin><<<grid, 160, smem, s>>>((const Tin*)q, (const Tin*)k, (const Tin*)v, a, (Tin*)Kc,
-                                                       (Tin*)Vc, cumc, pos, L, scale, part, o, lse, status);
+                                                       (Tin*)Vc, cumc, pos, L, kps, scale, part, o, lse, status);
     e = cudaGetLastError();
     if (e != cudaSuccess || ns == 1) return e;
     e_decode_combine_kernel<D><<<(unsigned)NH, D, 0, s>>>(part, ns, o, lse);

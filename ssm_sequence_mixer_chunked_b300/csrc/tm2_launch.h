@@ -181,7 +181,7 @@ cudaError_t simt_poly_bwd(const Problem& p, int order, const void* q, const void
 // ---- 2Mamba-E decoding over a key/value cache (tm2_e_decode.cu) ---------------------
 // Kc (NH, L, d), Vc (NH, L, d) in the input dtype and cumc (NH, L, 2) fp32 hi + lo running
 // sums; the token at `pos` is appended; part: NH x e_decode_max_splits(L) x (d + 2) floats.
-int e_decode_splits(int pos);
+int e_decode_splits(long NH, int pos);   // ranges of the step (at most e_decode_max_splits(L))
 int e_decode_max_splits(int L);
 cudaError_t launch_e_decode(long NH, int d, int dtype, int pos, int L, float scale, const void* q, const void* k,
                             const void* v, const float* a, void* Kc, void* Vc, float* cumc, float* part, float* o,
