@@ -35,8 +35,10 @@
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream).
  *    Calls are asynchronous and never synchronise the host.  The tensor-core forward and
  *    backward also run their state walks on two high-priority streams of the library's own
- *    (created once per device), forked from `stream` and joined back into it with events,
- *    so the call's work is ordered with respect to `stream` as if it all ran there.
+ *    (created once per device), forked from `stream` and joined back into it with events
+ *    (made once per host thread and device), so the call's work is ordered with respect to
+ *    `stream` as if it all ran there.  The calls can be captured into a CUDA graph; a call
+ *    captured before its thread has made a non-captured one runs on `stream` alone.
  *  - Argument errors are reported before anything is launched.  A launch failure
  *    returns TM2_ERR_CUDA.  Kernels whose waits are bounded record TM2_ERR_TIMEOUT in
  *    a per-device status word that tm2_poll_status() returns after the stream drains.

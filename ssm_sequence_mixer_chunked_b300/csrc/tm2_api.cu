@@ -198,38 +198,58 @@ struct TraceScope {
 // them on the caller's stream: the block scheduler prefers the walks' CTAs and the readouts'
 // CTAs fill the SMs a walk's last wave leaves idle.  The backward's reverse walk runs beside dq
 // (which reads only the forward states); the forward splits the heads into two halves whose
-// walks run concurrently, each half's chunk output following its own walk.  Fork and join are
-// events made per call (destroyed once their work is enqueued).
-static cudaError_t side_stream(cudaStream_t* out, int which = 0) {
+// walks run concurrently, each half's chunk output following its own walk.  The streams are
+// shared by the process; the fork / join events belong to the calling host thread (a call
+// records and waits them in order, so calls from different threads never share one).  Both are
+// made on first use; a call whose stream is being captured into a CUDA graph before they exist
+// runs everything on the caller's stream in the same order (creating them is not capturable).
+struct Side {
+    cudaStream_t st[2];
+    cudaEvent_t fork, join[2];
+};
+static cudaError_t side_resources(cudaStream_t caller, const Side** out) {
     static std::mutex mu;
     static cudaStream_t streams[64][2] = {};
+    thread_local Side mine[64] = {};
+    *out = nullptr;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || which < 0 || which > 1) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lk(mu);
-    if (!streams[dev][which]) {
-        int least = 0, greatest = 0;
-        e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
-        if (e != cudaSuccess) return e;
-        e = cudaStreamCreateWithPriority(&streams[dev][which], cudaStreamNonBlocking, greatest);
-        if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    Side& x = mine[dev];
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        if (!streams[dev][0] || !x.fork) {
+            cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+            e = cudaStreamIsCapturing(caller, &cs);
+            if (e != cudaSuccess) return e;
+            if (cs != cudaStreamCaptureStatusNone) return cudaSuccess;   // one stream this time
+        }
+        if (!streams[dev][0]) {
+            int least = 0, greatest = 0;
+            e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
+            if (e != cudaSuccess) return e;
+            for (int i = 0; i < 2; ++i) {
+                e = cudaStreamCreateWithPriority(&streams[dev][i], cudaStreamNonBlocking, greatest);
+                if (e != cudaSuccess) return e;
+            }
+        }
+        x.st[0] = streams[dev][0];
+        x.st[1] = streams[dev][1];
     }
-    *out = streams[dev][which];
+    if (!x.fork) {
+        cudaEvent_t ev[3];
+        for (int i = 0; i < 3; ++i) {
+            e = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming);
+            if (e != cudaSuccess) return e;
+        }
+        x.join[0] = ev[1];
+        x.join[1] = ev[2];
+        x.fork = ev[0];
+    }
+    *out = &x;
     return cudaSuccess;
 }
-
-struct ForkJoin {
-    cudaEvent_t fork = nullptr, join = nullptr;
-    cudaError_t make() {
-        cudaError_t e = cudaEventCreateWithFlags(&fork, cudaEventDisableTiming);
-        return e != cudaSuccess ? e : cudaEventCreateWithFlags(&join, cudaEventDisableTiming);
-    }
-    ~ForkJoin() {
-        if (fork) cudaEventDestroy(fork);
-        if (join) cudaEventDestroy(join);
-    }
-};
 
 #define TM2_RUN(name, call)                  \
     do {                                     \
@@ -339,16 +359,12 @@ int tm2_forward(const void* q, const void* k, const void* v, const float* a, con
         // idle.  The heads are split into two halves walked concurrently on the two side
         // streams; the first half's chunk output (on the caller's stream) starts as soon as its
         // walk is done and fills the SMs the second half's walk leaves idle.
+        const Side* sd = nullptr;
+        TM2_CK(side_resources(s, &sd));
         const long BH = p.BH();
-        const int parts = BH >= 2 ? 2 : 1;
+        const int parts = sd ? (BH >= 2 ? 2 : 1) : 1;
         const size_t T = (size_t)p.T, Tp = (size_t)p.Tp(), NC = (size_t)p.NC;
-        ForkJoin fj[2];
-        cudaStream_t side[2] = {nullptr, nullptr};
-        for (int i = 0; i < parts; ++i) {
-            TM2_CK(side_stream(&side[i], i));
-            TM2_CK(fj[i].make());
-        }
-        TM2_CK(cudaEventRecord(fj[0].fork, s));
+        if (sd) TM2_CK(cudaEventRecord(sd->fork, s));
         Problem pp[2];
         ScanIO io[2];
         for (int i = 0; i < parts; ++i) {
@@ -367,17 +383,21 @@ int tm2_forward(const void* q, const void* k, const void* v, const float* a, con
             io[i].zx = zx + lo * NC * 4096;
             io[i].S_final = S_final ? S_final + lo * 4096 * 64 : nullptr;
             io[i].z_final = z_final ? z_final + lo * 4096 : nullptr;
-            TM2_CK(cudaStreamWaitEvent(side[i], fj[0].fork, 0));
+            if (!sd) {
+                TM2_RUN("tc_state_scan_fwd", tc_state_scan(pp[i], io[i], s));
+                continue;
+            }
+            TM2_CK(cudaStreamWaitEvent(sd->st[i], sd->fork, 0));
             {
-                cudaStream_t s = side[i];
+                cudaStream_t s = sd->st[i];
                 TM2_RUN("tc_state_scan_fwd", tc_state_scan(pp[i], io[i], s));
             }
-            TM2_CK(cudaEventRecord(fj[i].join, side[i]));
+            TM2_CK(cudaEventRecord(sd->join[i], sd->st[i]));
         }
         for (int i = 0; i < parts; ++i) {
             const long lo = BH * i / parts;
             const size_t tok = (size_t)lo * T;
-            TM2_CK(cudaStreamWaitEvent(s, fj[i].join, 0));
+            if (sd) TM2_CK(cudaStreamWaitEvent(s, sd->join[i], 0));
             TM2_RUN("tc_chunk_out", tc_chunk_out(pp[i], (const char*)q + tok * 64 * 2, (const char*)k + tok * 64 * 2,
                                                  (const char*)v + tok * 64 * 2, Aloc + lo * Tp, io[i].Sx, io[i].zx,
                                                  io[i].amax, (float*)o + tok * 64, Z ? Z + tok : nullptr, s));
@@ -446,20 +466,22 @@ int tm2_backward(const void* q, const void* k, const void* v, const float* a, co
         ScanIO r{};
         r.rev = true; r.ops = ops; r.g = g; r.zmax = zmax; r.amax = amax_r;
         r.Sx = dSx; r.zx = dzx; r.sscale = sscale;
-        // the reverse walk on the side stream, dq beside it; dk/dv waits for the walk
-        cudaStream_t side = nullptr;
-        ForkJoin fj;
-        TM2_CK(side_stream(&side));
-        TM2_CK(fj.make());
-        TM2_CK(cudaEventRecord(fj.fork, s));
-        TM2_CK(cudaStreamWaitEvent(side, fj.fork, 0));
-        {
-            cudaStream_t s = side;
+        // the reverse walk on a side stream, dq beside it; dk/dv waits for the walk
+        const Side* sd = nullptr;
+        TM2_CK(side_resources(s, &sd));
+        if (sd) {
+            TM2_CK(cudaEventRecord(sd->fork, s));
+            TM2_CK(cudaStreamWaitEvent(sd->st[0], sd->fork, 0));
+            {
+                cudaStream_t s = sd->st[0];
+                TM2_RUN("tc_state_scan_bwd", tc_state_scan(p, r, s));
+            }
+            TM2_CK(cudaEventRecord(sd->join[0], sd->st[0]));
+        } else {
             TM2_RUN("tc_state_scan_bwd", tc_state_scan(p, r, s));
         }
-        TM2_CK(cudaEventRecord(fj.join, side));
         TM2_RUN("tc_bwd_dq", tc_bwd_dq(p, q, k, v, dO, Aloc, zeta, ucol, Sx, zx, amax_f, dq, s));
-        TM2_CK(cudaStreamWaitEvent(s, fj.join, 0));
+        if (sd) TM2_CK(cudaStreamWaitEvent(s, sd->join[0], 0));
         TM2_RUN("tc_bwd_dkdv", tc_bwd_dkdv(p, q, k, v, dO, Aloc, g, zeta, ucol, rowterm, dSx, dzx, sscale, amax_r,
                                            dk, dv, dcum, s));
         TM2_RUN("reverse_cumsum_da", launch_reverse_cumsum_da(p, a, dcum, nullptr, da, s));
