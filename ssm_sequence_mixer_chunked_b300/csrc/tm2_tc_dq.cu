@@ -134,7 +134,6 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_cons
         abort_s = 0;
         fence_mbar_init();
     }
-    for (int j = threadIdx.x; j < C; j += THREADS) sAv[j] = a.Aloc[bh * a.Tp + (long)c * C + j];
     if (warp == 0) {
         tmem_alloc(smem_u32(&tmem_base_s), 512);
         tmem_relinquish();
@@ -272,15 +271,21 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_cons
         const long tok = (long)c * C + i;
         const bool in = tok < a.T;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-        const float Ai = sAv[i];
+        // per-chunk and per-token terms, all loaded while the tiles are on their way: the chunk-local
+        // A of token threadIdx.x (C = 256 compute threads; published by the group waits' barriers),
+        // this row's zeta and ucol, the operand maxima, the normaliser matrix of the state
+        static_assert(C == 256, "one chunk-local A per compute thread");
+        const float av = a.Aloc[bh * a.Tp + (long)c * C + threadIdx.x];
         const float ze = in ? a.zeta[bh * a.T + tok] : 0.f;
         const float uc = in ? a.ucol[bh * a.T + tok] : 0.f;
-        const float ks = pow2_scale(a.amax[bh * 4]), vs = pow2_scale(a.amax[bh * 4 + 1]);
-        const float un = 1.f / (ks * ks * vs);           // exact: a power of two
+        const unsigned am_k = a.amax[bh * 4], am_v = a.amax[bh * 4 + 1];
         int kg = 0;                                      // group-wait counter
         float4 zr[4];
-        z_tiles_load(a.zx + (bh * NC + c) * 4096, threadIdx.x, zr);   // in flight during the tile wait
+        z_tiles_load(a.zx + (bh * NC + c) * 4096, threadIdx.x, zr);
         bool ok = mbar_wait(smem_u32(&bar_ld), 0, a.status);
+        sAv[threadIdx.x] = av;
+        const float ks = pow2_scale(am_k), vs = pow2_scale(am_v);
+        const float un = 1.f / (ks * ks * vs);           // exact: a power of two
         if (ok) {   // fp16 copies of the Q and dO tiles
             const int t256 = threadIdx.x;
             for (int pc = t256; pc < 1024; pc += 256) {
@@ -372,6 +377,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_cons
                 for (int k = 0; k < 32; ++k) dqx[k] = fmaf(2.f * uc, u[k], dqx[k]);
             }
         }
+        const float Ai = sAv[i];
         // ---- intra-chunk blocks
         for (int b = 0; b < nblk && ok; ++b) {
             if (!(ok = group_wait(smem_u32(&bar_sfull[b]), 0, a.status, warp == 0, 1, 256, gflags, kg, &abort_s))) break;
