@@ -352,6 +352,20 @@ __global__ void __launch_bounds__(256) tc_scan_operands_kernel(
     const long bh = blockIdx.y;
     const int Tp = NC * C, c = (st * 64) / C;
     const long t0 = (long)st * 64;
+    // the stage's key and value rows (16 bytes per thread and token half) are loaded first, so
+    // their latency overlaps the weights' loads and exponentials
+    const int q8 = tid & 7, jb = tid >> 3;   // token jb and jb + 32, elements 8 q8 .. 8 q8 + 7
+    uint4 k8[2], v8[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const long t = t0 + jb + 32 * h;
+        if (t < T) {
+            k8[h] = *reinterpret_cast<const uint4*>(key + (bh * T + t) * 64 + 8 * q8);
+            v8[h] = *reinterpret_cast<const uint4*>(val + (bh * T + t) * 64 + 8 * q8);
+        } else {
+            k8[h] = v8[h] = make_uint4(0, 0, 0, 0);
+        }
+    }
     const float ks = pow2_scale(amax[bh * 4]), vs = pow2_scale(amax[bh * 4 + 1]);
     const float zs = rev ? pow2_scale(amax[bh * 4 + 2]) : 1.f;
     if (tid < 64) {
@@ -371,29 +385,19 @@ __global__ void __launch_bounds__(256) tc_scan_operands_kernel(
         szc[tid] = zc;
     }
     __syncthreads();
-    for (int e = tid; e < 64 * 8; e += 256) {   // 16-byte loads: token j, elements 8*q8 .. 8*q8+7
-        const int j = e >> 3, q8 = e & 7;
-        const long t = t0 + j;
-        float kf[8], vf[8];
-        if (t < T) {
-            const uint4 k8 = *reinterpret_cast<const uint4*>(key + (bh * T + t) * 64 + 8 * q8);
-            const uint4 v8 = *reinterpret_cast<const uint4*>(val + (bh * T + t) * 64 + 8 * q8);
-            const __nv_bfloat162* kb = reinterpret_cast<const __nv_bfloat162*>(&k8);
-            const __nv_bfloat162* vb = reinterpret_cast<const __nv_bfloat162*>(&v8);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float2 kk = __bfloat1622float2(kb[u]), vv = __bfloat1622float2(vb[u]);
-                kf[2 * u] = kk.x * ks; kf[2 * u + 1] = kk.y * ks;
-                vf[2 * u] = vv.x * vs * sw[j]; vf[2 * u + 1] = vv.y * vs * sw[j];
-            }
-        } else {
+    for (int h = 0; h < 2; ++h) {
+        const int j = jb + 32 * h;
+        const __nv_bfloat162* kb = reinterpret_cast<const __nv_bfloat162*>(&k8[h]);
+        const __nv_bfloat162* vb = reinterpret_cast<const __nv_bfloat162*>(&v8[h]);
+        const float wv = vs * sw[j];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) kf[u] = vf[u] = 0.f;
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            sk[j][8 * q8 + u] = kf[u];
-            sv[j][8 * q8 + u] = vf[u];
+        for (int u = 0; u < 4; ++u) {
+            const float2 kk = __bfloat1622float2(kb[u]), vv = __bfloat1622float2(vb[u]);
+            sk[j][8 * q8 + 2 * u] = kk.x * ks;
+            sk[j][8 * q8 + 2 * u + 1] = kk.y * ks;
+            sv[j][8 * q8 + 2 * u] = vv.x * wv;
+            sv[j][8 * q8 + 2 * u + 1] = vv.y * wv;
         }
     }
     __syncthreads();
@@ -401,26 +405,34 @@ __global__ void __launch_bounds__(256) tc_scan_operands_kernel(
     // transposed key and weighted-value blocks: thread writes 16 consecutive j of one row
     {
         const int n = tid >> 2, j0 = (tid & 3) * 16;
-        uint32_t wk[8], wv[8];
+        uint32_t wk[8], wvv[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             const __half2 hk = __floats2half2_rn(sk[j0 + 2 * u][n], sk[j0 + 2 * u + 1][n]);
             const __half2 hv = __floats2half2_rn(sv[j0 + 2 * u][n], sv[j0 + 2 * u + 1][n]);
             wk[u] = *reinterpret_cast<const uint32_t*>(&hk);
-            wv[u] = *reinterpret_cast<const uint32_t*>(&hv);
+            wvv[u] = *reinterpret_cast<const uint32_t*>(&hv);
         }
         uint4* dk = reinterpret_cast<uint4*>(blk + n * 64 + j0);
         dk[0] = make_uint4(wk[0], wk[1], wk[2], wk[3]);
         dk[1] = make_uint4(wk[4], wk[5], wk[6], wk[7]);
         uint4* dv = reinterpret_cast<uint4*>(blk + (64 + n) * 64 + j0);
-        dv[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-        dv[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
+        dv[0] = make_uint4(wvv[0], wvv[1], wvv[2], wvv[3]);
+        dv[1] = make_uint4(wvv[4], wvv[5], wvv[6], wvv[7]);
     }
-    // the normaliser row and the zero rows after it
-    for (int e = tid; e < (TC_OPS_ROWS - 128) * 64; e += 256) {
-        const int r = e >> 6, j = e & 63;
-        blk[(128 + r) * 64 + j] = __float2half_rn(r == 0 ? zs * sw[j] * szc[j] : 0.f);
+    // the normaliser row (8 threads, 8 tokens each) and the zero rows after it, 16 bytes a store
+    if (tid < 8) {
+        uint32_t wz[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int j = 8 * tid + 2 * u;
+            const __half2 hz = __floats2half2_rn(zs * sw[j] * szc[j], zs * sw[j + 1] * szc[j + 1]);
+            wz[u] = *reinterpret_cast<const uint32_t*>(&hz);
+        }
+        reinterpret_cast<uint4*>(blk + 128 * 64)[tid] = make_uint4(wz[0], wz[1], wz[2], wz[3]);
     }
+    for (int e = tid; e < (TC_OPS_ROWS - 129) * 8; e += 256)
+        reinterpret_cast<uint4*>(blk + 129 * 64)[e] = make_uint4(0, 0, 0, 0);
 }
 
 cudaError_t launch_tc_scan_operands(const Problem& p, bool rev, const void* key, const void* val, const float* Aloc,
