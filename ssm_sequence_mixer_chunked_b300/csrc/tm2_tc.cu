@@ -60,24 +60,6 @@ bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t heads, uint6
     return r == CUDA_SUCCESS;
 }
 
-// Four contiguous slices m = 4g .. 4g+3 of one plane: box rows 256g .. 256g+255,
-// landing as [m'][n][col] (32 KB).  Coordinates (0, 256g, plane, chunk).
-bool make_tmap_state_quads(CUtensorMap* map, const void* base, uint64_t nchunks) {
-    const uint64_t dims[4] = {64, 4096, 2, nchunks};
-    const uint64_t strides[3] = {128, 4096 * 128, 2 * 4096 * 128};
-    const uint32_t box[4] = {64, 256, 1, 1};
-    return make_tmap_f16_nd(map, base, 4, dims, strides, box);
-}
-
-// Four transposed slices n = 4g .. 4g+3 of one plane: landing as [n'][m][col] (32 KB).
-// Coordinates (0, 0, 4g, plane, chunk).
-bool make_tmap_state_tquads(CUtensorMap* map, const void* base, uint64_t nchunks) {
-    const uint64_t dims[5] = {64, 64, 64, 2, nchunks};
-    const uint64_t strides[4] = {64 * 128, 128, 4096 * 128, 2 * 4096 * 128};
-    const uint32_t box[5] = {64, 64, 4, 1, 1};
-    return make_tmap_f16_nd(map, base, 5, dims, strides, box);
-}
-
 bool make_tmap_state_packed_quads(CUtensorMap* map, const void* base, uint64_t nchunks) {
     const uint64_t dims[4] = {64, 16, (uint64_t)TC_PACKED_BLOCKS * 16, 2 * nchunks};
     const uint64_t strides[3] = {128, 16 * 128, (uint64_t)TC_PACKED_ROWS * 128};

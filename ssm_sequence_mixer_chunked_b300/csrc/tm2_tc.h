@@ -23,11 +23,6 @@ bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t heads, uint6
 bool make_tmap_f16_nd(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
                       const uint32_t* box);
 
-// One plane of four slices per box (32 KB): make_tmap_state_quads boxes the contiguous slices
-// m = 4g .. 4g+3 (smem [m'][n][col], coordinates (0, 256g, plane, chunk));
-// make_tmap_state_tquads the transposed slices n = 4g .. 4g+3 (smem [n'][m][col],
-// coordinates (0, 0, 4g, plane, chunk)).
-bool make_tmap_state_quads(CUtensorMap* map, const void* base, uint64_t nchunks);
 // Block-packed states (TC_PACKED_ROWS rows per plane): four rows m' = 4 mq .. 4 mq + 3 of one
 // 16 x 16 block, all its 16 columns n' (smem [m'][n'][col], 8 KB).  Coordinates
 // (0, 0, 16 block + 4 mq, 2 chunk + plane).
@@ -39,7 +34,6 @@ bool make_tmap_state_packed_blocks(CUtensorMap* map, const void* base, uint64_t 
 // of its columns n' = 4 nq .. 4 nq + 3 (smem [n'][m'][col], 8 KB).  Coordinates
 // (0, 0, 4 nq, 10 (2 chunk + plane) + block).
 bool make_tmap_state_packed_tquads(CUtensorMap* map, const void* base, uint64_t nchunks);
-bool make_tmap_state_tquads(CUtensorMap* map, const void* base, uint64_t nchunks);
 
 // Reads (and optionally clears) the device status word of the current device.
 int read_tc_status(bool clear);
