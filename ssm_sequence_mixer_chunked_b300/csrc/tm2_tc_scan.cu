@@ -105,20 +105,13 @@ struct Args {
     const unsigned* amax; // [BH][4] operand maxima (fp32 bits): key, value, normaliser (reverse)
     int* status;
     int T, NC, Tp, rev;
-    int packed;           // export the block-packed layout (see tm2_launch.h)
 };
 
-// The state rows of CTA Q.  Full layout: rows r = 64 m' + n of m = 4Q + m', i.e. (m, n) =
-// (4Q + r / 64, r % 64).  Block-packed (both walks): CTA Q owns the 16 x 16 block (bm, bn),
+// The state rows of CTA Q, block-packed (tm2_launch.h): CTA Q owns the 16 x 16 block (bm, bn),
 // bm <= bn, Q = tc_block_index(bm, bn), rows r = 16 m' + n', (m, n) = (16 bm + m', 16 bn + n').
-TM2_DEV void row_mn(bool packed, int Q, int bm, int bn, int r, int& m, int& n) {
-    if (packed) {
-        m = 16 * bm + (r >> 4);
-        n = 16 * bn + (r & 15);
-    } else {
-        m = 4 * Q + (r >> 6);
-        n = r & 63;
-    }
+TM2_DEV void row_mn(int bm, int bn, int r, int& m, int& n) {
+    m = 16 * bm + (r >> 4);
+    n = 16 * bn + (r & 15);
 }
 
 TM2_DEV void ld_row_chunks4(uint32_t row_addr, int row, int c0, uint32_t* x) {   // 4 swizzled 16-byte chunks
@@ -151,9 +144,9 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
     const int nchunks = rev ? NC - 1 : NC;   // the reverse walk never needs the update of chunk 0
     const int nstages = nchunks * SPC;
     const uint32_t sbase = smem_u32(smem);
-    const bool packed = a.packed != 0;
+
     int bm = 0, bn = 0;
-    if (packed) tc_block_of(Q, bm, bn);
+    tc_block_of(Q, bm, bn);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NSLOT; ++i) mbar_init(smem_u32(&bar_full[i]), 1);
@@ -258,8 +251,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
         const int gp = warp >> 2, quad = warp & 3;
         const int r0 = quad * 32 + lane;
         int m0, m1, n;   // the key indices of rows r0 (M-block 0) and r0 + 128 (M-block 1; same n)
-        row_mn(packed, Q, bm, bn, r0, m0, n);
-        row_mn(packed, Q, bm, bn, r0 + 128, m1, n);
+        row_mn(bm, bn, r0, m0, n);
+        row_mn(bm, bn, r0 + 128, m1, n);
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         for (int gs = 0; gs < nstages; ++gs) {
             const int sl = gs % NSLOT;
@@ -306,14 +299,14 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
         const int mb = (warp - WARP_EPI) >> 2, quad = warp & 3;
         const int r = mb * 128 + quad * 32 + lane;
         int m, n;
-        row_mn(packed, Q, bm, bn, r, m, n);
+        row_mn(bm, bn, r, m, n);
         const long R = (long)m * 64 + n;          // the row in the full (m, n) layout
         const long Rm = (long)n * 64 + m;         // its mirror (m, n) -> (n, m)
         // an off-diagonal block of the packed layout stands for both (m, n) and (n, m): the
         // forward exports it doubled (its readouts contract each stored row once), the reverse
         // as is (dk/dv reads each stored block in both orientations), and S0 / S_final / the
         // normaliser carry both rows
-        const bool mirror = packed && bm != bn;
+        const bool mirror = bm != bn;
         const bool twice = mirror && !rev;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         // units of the running state (see the header): forward value columns ks^2 vs, forward
@@ -479,9 +472,8 @@ cudaError_t tc_state_scan(const Problem& p, const ScanIO& io, cudaStream_t s) {
     const uint64_t strides[2] = {128, (uint64_t)TC_OPS_ROWS * 128};
     const uint32_t box[3] = {64, (uint32_t)TC_OPS_ROWS, 1};
     if (!make_tmap_f16_nd(&tops, io.ops, 3, dims, strides, box)) return cudaErrorInvalidValue;
-    const bool packed = true;   // both walks export the block-packed layout
     CUtensorMap tsx;   // the state planes as (64 columns, rows, BH x NC x 2 planes), 256-row boxes
-    const uint64_t rows = packed ? (uint64_t)TC_PACKED_ROWS : 4096;
+    const uint64_t rows = (uint64_t)TC_PACKED_ROWS;   // both walks export the block-packed layout
     const uint64_t sdims[3] = {64, rows, BH * (uint64_t)p.NC * 2};
     const uint64_t sstrides[2] = {128, rows * 128};
     const uint32_t sbox[3] = {64, (uint32_t)NR, 1};
@@ -490,10 +482,10 @@ cudaError_t tc_state_scan(const Problem& p, const ScanIO& io, cudaStream_t s) {
     if (!status) return cudaErrorInvalidValue;
     if (!io.amax) return cudaErrorInvalidValue;
     Args a{io.g, io.zmax, io.S0, io.z0, (__half*)io.Sx, io.zx, io.sscale, io.S_final, io.z_final, io.amax, status,
-           p.T, p.NC, (int)p.Tp(), io.rev ? 1 : 0, packed ? 1 : 0};
+           p.T, p.NC, (int)p.Tp(), io.rev ? 1 : 0};
     cudaError_t e = cudaFuncSetAttribute(tc_state_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    dim3 grid(packed ? TC_PACKED_BLOCKS : 4096 / NR, (unsigned)p.BH());
+    dim3 grid(TC_PACKED_BLOCKS, (unsigned)p.BH());
     tc_state_scan_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(tops, tsx, a);
     return cudaGetLastError();
 }
