@@ -70,7 +70,8 @@ typedef enum {
     TM2_ERR_ALIGNMENT = -3,     /* a pointer is not 16-byte aligned (workspace: 256)     */
     TM2_ERR_WORKSPACE = -4,     /* ws_bytes smaller than the *_workspace() size          */
     TM2_ERR_CUDA = -5,          /* a CUDA launch or runtime call failed                  */
-    TM2_ERR_TIMEOUT = -6        /* a bounded device wait expired (see tm2_poll_status)   */
+    TM2_ERR_TIMEOUT = -6,       /* a bounded device wait expired (see tm2_poll_status)   */
+    TM2_ERR_BOUNDS = -7         /* bounds-checked build only: a device index check failed */
 } tm2_status;
 
 typedef enum { TM2_F32 = 0, TM2_BF16 = 1 } tm2_dtype;
@@ -311,8 +312,16 @@ int tm2e_fill_cache(const void* k, const void* v, const float* a, void* K_cache,
 
 /*
  * Device status word of the current device: returns TM2_OK, or TM2_ERR_TIMEOUT if a
- * kernel's bounded wait expired since the last poll, and clears it.  Synchronises
- * with the device (call it after the stream of interest has drained).
+ * kernel's bounded wait expired since the last poll (TM2_ERR_BOUNDS in the bounds-checked
+ * build if an index check failed), and clears it.  Synchronises with the device (call it
+ * after the stream of interest has drained).
+ *
+ * Bounds-checked build (libtm2_debug.so, compiled with -DTM2_DEBUG): the tensor-core kernels
+ * check the shared-memory, tensor-memory and global indices they compute before using them;
+ * a failed check records TM2_ERR_BOUNDS in the status word and the access is skipped (no trap,
+ * no assert).  Every call then synchronises its stream after each launch and returns a
+ * non-zero status word, so a failure is reported by the call that caused it.  Calls of this
+ * build cannot be captured into a CUDA graph.
  */
 int tm2_poll_status(void);
 

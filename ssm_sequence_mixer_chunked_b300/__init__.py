@@ -26,7 +26,8 @@ __all__ = ["forward", "backward", "step", "step_conv", "state_pack", "state_unpa
            "NORMALIZE", "REUSE_STATES"]
 
 PKG = os.path.dirname(os.path.abspath(__file__))
-_LIB_PATH = os.path.join(PKG, "libtm2.so")
+# TM2_DEBUG=1 selects the bounds-checked build (python -m ssm_sequence_mixer_chunked_b300.build --debug)
+_LIB_PATH = os.path.join(PKG, "libtm2_debug.so" if os.environ.get("TM2_DEBUG") == "1" else "libtm2.so")
 NORMALIZE = 1
 REUSE_STATES = 2
 PACKED_STATE = 4
@@ -48,8 +49,8 @@ def _load():
     if _lib is not None:
         return _lib
     if not os.path.exists(_LIB_PATH):
-        raise TM2Error("libtm2.so is not built (%s); run `python -m ssm_sequence_mixer_chunked_b300.build`"
-                       % _LIB_PATH)
+        raise TM2Error("%s is not built; run `python -m ssm_sequence_mixer_chunked_b300.build%s`"
+                       % (_LIB_PATH, " --debug" if _LIB_PATH.endswith("_debug.so") else ""))
     lib = ctypes.CDLL(_LIB_PATH)
     P, I, U, S, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint, ctypes.c_size_t, ctypes.c_float
     lib.tm2_version.restype = I

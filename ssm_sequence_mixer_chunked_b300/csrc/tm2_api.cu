@@ -251,11 +251,26 @@ static cudaError_t side_resources(cudaStream_t caller, const Side** out) {
     return cudaSuccess;
 }
 
+#ifdef TM2_DEBUG
+// bounds-checked build: every launch is followed by a stream synchronisation and a read of the
+// device status word, so the call that broke an index check reports it
+#define TM2_RUN(name, call)                          \
+    do {                                             \
+        {                                            \
+            TraceScope ts_(name, s);                 \
+            TM2_CK(call);                            \
+        }                                            \
+        TM2_CK(cudaStreamSynchronize(s));            \
+        const int st_ = ::tm2::read_tc_status(true); \
+        if (st_ != TM2_OK) return st_;               \
+    } while (0)
+#else
 #define TM2_RUN(name, call)                  \
     do {                                     \
         TraceScope ts_(name, s);             \
         TM2_CK(call);                        \
     } while (0)
+#endif
 
 // ---- the 2Mamba-E forward, shared by tm2e_forward and tm2e_forward_noalloc ----------------
 int e_forward_check(const void* q, const void* k, const void* v, const float* a, const void* o, const float* lse,
@@ -308,6 +323,7 @@ const char* tm2_status_string(int status) {
         case TM2_ERR_WORKSPACE: return "TM2_ERR_WORKSPACE: workspace missing or smaller than required";
         case TM2_ERR_CUDA: return "TM2_ERR_CUDA: a CUDA launch or runtime call failed";
         case TM2_ERR_TIMEOUT: return "TM2_ERR_TIMEOUT: a bounded device wait expired";
+        case TM2_ERR_BOUNDS: return "TM2_ERR_BOUNDS: a device index check failed (bounds-checked build)";
         default: return "TM2: unknown status";
     }
 }

@@ -8,6 +8,20 @@
 
 #define TM2_DEV __device__ __forceinline__
 
+// Bounds-checked build (-DTM2_DEBUG): TM2_CHECK(cond, status) is cond, and a false cond also
+// records TM2_ERR_BOUNDS (-7) in the device status word `status` unless it already holds a
+// status; the caller skips the access it guards (no trap, no assert).  Without TM2_DEBUG it is
+// the constant true and costs nothing.
+#ifdef TM2_DEBUG
+#define TM2_CHECK(cond, status) (::tm2_debug_check((cond), (status)))
+__device__ __forceinline__ bool tm2_debug_check(bool ok, int* status) {
+    if (!ok && status) atomicCAS(status, 0, -7);
+    return ok;
+}
+#else
+#define TM2_CHECK(cond, status) true
+#endif
+
 namespace tm2 {
 
 // ---- element conversion -------------------------------------------------------------

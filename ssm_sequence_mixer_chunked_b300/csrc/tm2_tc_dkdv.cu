@@ -188,6 +188,9 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
                     // over its second index); the gradient state is symmetric and stored as is
                     const int g = r >> 1, bn = g >> 2, nq = g & 3, pc = 2 * chunk_id + (r & 1);
                     for (int bm = 0; bm < 4; ++bm) {
+                        if (!TM2_CHECK(tc_block_index(min(bm, bn), max(bm, bn)) < TC_PACKED_BLOCKS && nq < 4,
+                                       a.status))
+                            continue;   // (the request then never completes: the consumer's bounded wait ends it)
                         if (bm <= bn)
                             tma_load_4d(dst + bm * 8192, &tmSt, fb, 0, 0, 4 * nq,
                                         TC_PACKED_BLOCKS * pc + tc_block_index(bm, bn));

@@ -166,6 +166,10 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dq_kernel(const __grid_cons
                     abort_s = 1;
                     break;
                 }
+                if (!TM2_CHECK(sl >= 0 && sl < NR, a.status)) {
+                    abort_s = 1;
+                    break;
+                }
                 const uint32_t fb = smem_u32(&bar_full[sl]), dst = sb0 + RING + sl * RB;
                 if (r < NG) {
                     mbar_arrive_expect_tx(fb, 2 * PLANE);

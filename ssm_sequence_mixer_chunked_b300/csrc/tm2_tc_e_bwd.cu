@@ -344,7 +344,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_attn_bwd_kernel(const __grid_co
             const long t0 = (long)blk0 * BT + (long)sbk * SUB;
             // the walked sub-block's terms into buffer x; the next one's loads fly meanwhile
             float* sc = sSc + x * 3 * SUB;
-            if (stager) {
+            if (stager && TM2_CHECK(arr * SUB + tt_st < 3 * SUB && u < NB, a.status)) {
                 sc[arr * SUB + tt_st] = finish(nxt);
                 if (sbk + 1 < nsb) nxt = fetch(sbk + 1);
             }

@@ -182,6 +182,10 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
                     abort_s = 1;
                     break;
                 }
+                if (!TM2_CHECK(s_off[r] >= 0 && s_off[r] + req_units(r) <= NUNIT, a.status)) {
+                    abort_s = 1;
+                    break;
+                }
                 const uint32_t fb = smem_u32(&bar_full[r]), dst = sb0 + RING + s_off[r] * UNIT;
                 if (r < NG) {   // rows 4 mq .. 4 mq + 3 of the blocks (bm, bm .. 3), hi then lo plane
                     const int bm = r >> 2, mq = r & 3, nb = 4 - bm;
@@ -399,7 +403,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_chunk_out_kernel(const __grid_c
 #pragma unroll
             for (int k = 0; k < 32; ++k) y[k] += eA * (un * nx[k]);
             const long tok = (long)c * C + i;
-            if (tok < a.T) {
+            if (tok < a.T && TM2_CHECK(i >= 0 && i < C && h >= 0 && h < 2, a.status)) {
                 const float inv = a.normalize ? (z != 0.f ? 1.f / z : 0.f) : 1.f;
                 float4* dst = reinterpret_cast<float4*>(a.o + (bh * a.T + tok) * 64 + h * 32);
 #pragma unroll

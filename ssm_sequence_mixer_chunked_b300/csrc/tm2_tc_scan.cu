@@ -301,6 +301,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_state_scan_kernel(const __grid_
         int m, n;
         row_mn(bm, bn, r, m, n);
         const long R = (long)m * 64 + n;          // the row in the full (m, n) layout
+        if (!TM2_CHECK(m >= 0 && m < 64 && n >= 0 && n < 64 && r >= 0 && r < NR, a.status)) abort_s = 1;
         const long Rm = (long)n * 64 + m;         // its mirror (m, n) -> (n, m)
         // an off-diagonal block of the packed layout stands for both (m, n) and (n, m): the
         // forward exports it doubled (its readouts contract each stored row once), the reverse

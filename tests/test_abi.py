@@ -36,9 +36,21 @@ def test_header_symbols_exported(lib):
         assert hasattr(lib, n), n
 
 
+def test_bounds_checked_build_exports_the_same_symbols():
+    # the TM2_DEBUG variant (device index checks, a synchronisation and status read after
+    # every launch) is a drop-in: same header, same exports
+    path = tm2_build.build(debug=True)
+    assert path.endswith("libtm2_debug.so") and os.path.exists(path)
+    dbg = ctypes.CDLL(path)
+    for n in declared_functions():
+        assert hasattr(dbg, n), n
+    dbg.tm2_status_string.restype = ctypes.c_char_p
+    assert dbg.tm2_status_string(-7).decode().startswith("TM2_ERR_BOUNDS")
+
+
 def test_version_and_status_strings(lib):
     assert lib.tm2_version() >= 100
-    for st in (OK, INVALID, UNSUPPORTED, ALIGNMENT, WORKSPACE, -5, -6, 12345):
+    for st in (OK, INVALID, UNSUPPORTED, ALIGNMENT, WORKSPACE, -5, -6, -7, 12345):
         s = tm2.status_string(st)
         assert s.startswith("TM2")
 
