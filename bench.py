@@ -221,20 +221,54 @@ def summarize(trace):
 
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
+    """SM clock, its maximum, power and the throttle reasons, sampled during the timed region:
+    every 5 ms from NVML in a thread (read-only queries), else every 100 ms by nvidia-smi.  The
+    samples are CSV lines in nvidia-smi's format either way (parse_clocks)."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
+    # NVML clock-event reason bits: hw slowdown, hw thermal slowdown, sw thermal slowdown, sw power cap
+    BITS = (0x8, 0x40, 0x20, 0x4)
 
     def __init__(self, device):
         self.proc = None
         self.path = None
+        self.thread = None
         try:
             uuid = str(torch.cuda.get_device_properties(device).uuid)
             self.gpu = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
         except Exception:
             self.gpu = str(device)
 
+    def _nvml_loop(self, nv, h):
+        while not self.stop_flag:
+            try:
+                sm = nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM)
+                smax = nv.nvmlDeviceGetMaxClockInfo(h, nv.NVML_CLOCK_SM)
+                pw = nv.nvmlDeviceGetPowerUsage(h) / 1000.0
+                r = nv.nvmlDeviceGetCurrentClocksEventReasons(h)
+                flags = ["Active" if r & b else "Not Active" for b in self.BITS]
+                self.lines.append("%d, %d, %.1f, %s\n" % (sm, smax, pw, ", ".join(flags)))
+            except Exception:
+                break
+            time.sleep(0.005)
+
     def start(self):
+        self.stop_flag = False
+        self.lines = []
+        try:
+            import threading
+            import pynvml as nv
+            nv.nvmlInit()
+            try:
+                h = nv.nvmlDeviceGetHandleByUUID(self.gpu)
+            except Exception:
+                h = nv.nvmlDeviceGetHandleByUUID(self.gpu.encode())
+            self.thread = threading.Thread(target=self._nvml_loop, args=(nv, h), daemon=True)
+            self.thread.start()
+            return
+        except Exception:
+            self.thread = None
         try:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
@@ -247,6 +281,10 @@ class ClockSampler:
             self.proc = None
 
     def stop(self):
+        if self.thread is not None:
+            self.stop_flag = True
+            self.thread.join(timeout=5)
+            return parse_clocks(self.lines)
         if self.proc is None:
             return None
         time.sleep(0.25)
