@@ -222,7 +222,7 @@ def summarize(trace):
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
     """SM clock, its maximum, power and the throttle reasons, sampled during the timed region:
-    every 5 ms from NVML in a thread (read-only queries), else every 100 ms by nvidia-smi.  The
+    every ~2 ms from NVML in a thread (read-only queries), else every 100 ms by nvidia-smi.  The
     samples are CSV lines in nvidia-smi's format either way (parse_clocks)."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
@@ -251,7 +251,7 @@ class ClockSampler:
                 self.lines.append("%d, %d, %.1f, %s\n" % (sm, smax, pw, ", ".join(flags)))
             except Exception:
                 break
-            time.sleep(0.005)
+            time.sleep(0.001)
 
     def start(self):
         self.stop_flag = False
