@@ -329,11 +329,11 @@ cudaError_t launch_head_absmax(const Problem& p, const void* x, const void* y, u
 }
 
 // Operands of the tensor-core chunk-state scan, one block of 256 threads per 64-token stage
-// of one (b, h), written as one [136][64] fp16 block per stage (token j = stage*64 + column):
+// of one (b, h), written as one [144][64] fp16 block per stage (token j = stage*64 + column):
 //   rows   0-63 : [n][j]   = fp16(ks key_j[n])         (the key block, transposed)
 //   rows  64-127: [col][j] = fp16(vs w_j val_j[col])   (the weighted values, transposed)
 //   row   128   : [j]      = fp16(zs w_j zc_j)         (the normaliser column)
-//   rows 129-135: 0
+//   rows 129-143: 0                                    (rows 64-143: the walk's N = 80 operand)
 // with the scan's weight w_t = exp(g_c - A_t), zc = 1 (forward walk) or
 // w_t = exp(A_t) zeta_t / zmax_c, zc = ucol_t (reverse walk); tokens past T give zeros.
 // ks, vs, zs are the powers of two that bring the head's largest |key|, |val| and (reverse
