@@ -61,7 +61,7 @@ constexpr int TC_CHUNK = 256;
 // as is, so the readouts contract each stored row once:
 //   sum_{m,n} x[m] x[n] S[(m,n), :] = sum_{blocks} sum_{(m,n) in block} x[m] x[n] T[(m,n), :].
 // The gradient states (no initial state, exactly symmetric) are stored as they are: dk/dv reads
-// each off-diagonal block in both orientations (make_tmap_state_packed_quads / _tquads).
+// each off-diagonal block in both orientations (make_tmap_state_packed_rowrun / _tquads).
 // Layout [BH][NC][2 planes][TC_PACKED_ROWS][64] fp16; the normaliser states stay full.
 constexpr int TC_PACKED_BLOCKS = 10;
 constexpr int TC_PACKED_ROWS = TC_PACKED_BLOCKS * 256;

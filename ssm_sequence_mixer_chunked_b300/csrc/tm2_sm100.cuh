@@ -132,6 +132,12 @@ TM2_DEV void tma_load_4d(uint32_t dst, const void* tmap, uint32_t bar, int x, in
         "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w)
         : "memory");
 }
+TM2_DEV void tma_load_5d(uint32_t dst, const void* tmap, uint32_t bar, int x, int y, int z, int w, int u) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+        "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w), "r"(u)
+        : "memory");
+}
 // Tiled TMA store shared -> global (3-D map), tracked by the thread's bulk async-group.
 TM2_DEV void tma_store_3d(const void* tmap, uint32_t src, int x, int y, int z) {
     asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(tmap),

@@ -74,6 +74,14 @@ bool make_tmap_state_packed_tquads(CUtensorMap* map, const void* base, uint64_t 
     return make_tmap_f16_nd(map, base, 4, dims, strides, box);
 }
 
+bool make_tmap_state_packed_rowrun(CUtensorMap* map, const void* base, uint64_t nchunks, int nb) {
+    if (nb < 1 || nb > 4) return false;
+    const uint64_t dims[5] = {64, 16, 16, (uint64_t)TC_PACKED_BLOCKS, 2 * nchunks};
+    const uint64_t strides[4] = {128, 16 * 128, 256 * 128, (uint64_t)TC_PACKED_ROWS * 128};
+    const uint32_t box[5] = {64, 16, 4, (uint32_t)nb, 1};
+    return make_tmap_f16_nd(map, base, 5, dims, strides, box);
+}
+
 bool make_tmap_state_packed_blocks(CUtensorMap* map, const void* base, uint64_t nchunks) {
     const uint64_t dims[3] = {64, (uint64_t)TC_PACKED_ROWS, 2 * nchunks};
     const uint64_t strides[2] = {128, (uint64_t)TC_PACKED_ROWS * 128};

@@ -34,6 +34,10 @@ bool make_tmap_state_packed_blocks(CUtensorMap* map, const void* base, uint64_t 
 // of its columns n' = 4 nq .. 4 nq + 3 (smem [n'][m'][col], 8 KB).  Coordinates
 // (0, 0, 4 nq, 10 (2 chunk + plane) + block).
 bool make_tmap_state_packed_tquads(CUtensorMap* map, const void* base, uint64_t nchunks);
+// A run of nb consecutive packed blocks (one block row (bm, bm + i), i < nb), from each its
+// rows m' = 4 mq .. 4 mq + 3 with all 16 columns n' (smem [block][m'][n'][col], nb x 8 KB).
+// Coordinates (0, 0, 4 mq, first block, 2 chunk + plane).  nb = 1 .. 4.
+bool make_tmap_state_packed_rowrun(CUtensorMap* map, const void* base, uint64_t nchunks, int nb);
 
 // Reads (and optionally clears) the device status word of the current device.
 int read_tc_status(bool clear);

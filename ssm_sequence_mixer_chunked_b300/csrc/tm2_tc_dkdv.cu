@@ -14,15 +14,18 @@
 // when normalised; dVt_j[dv] = sum_i W_ij zeta_i ucol_i + w_j Gamma_c sum_{m,n} k_j[m] k_j[n] dz[(m,n)]).
 //
 // One CTA per (128-key tile, chunk, b, h).  The inter-chunk sums run first, over 16 groups of
-// four state slices n = 4g .. 4g+3, four 8 KB TMA boxes per plane (fp16 hi and residual planes
-// of the block-packed gradient state: for each 16-row block of m the stored block holding the
-// rows (m, n), or its mirror rows (n, m); both land as [n'][m'][col]), as one product per group,
-//   U_g[j][(n', col)]  = sum_m k_j[m] dS[(m, 4g+n'), col]     (N = 256, the box MN-major),
-// double-buffered in tensor memory.  dS is symmetric in (m, n), so U_g also carries the key
-// term: the compute warps fold it into dvx[col] += k_j[4g+n'] U_g[j][(n', col)] (registers)
-// and sum_col v_j[col] U_g[j][(n', col)] into the dk sum of key index 4g+n' (shared memory,
-// each column half adding its share).  One product instead of a second, V-side chain halves
-// the tensor work of this part.  A 17th product U'_z = K dzm^T (dzm[m][n] = dz[(m,n)]) adds
+// four state slices m = 4g .. 4g+3 (first index, in the 16-row block bm = g / 4), as one
+// product per group,
+//   U_g[j][(m', col)]  = sum_n k_j[n] dS[(4g+m', n), col]     (N = 256, the box MN-major),
+// double-buffered in tensor memory.  The fp16 hi and residual planes of the block-packed
+// gradient state come as one TMA box per plane over the run of stored blocks (bm, bm .. 3)
+// (their rows (m, n), n >= 16 bm) plus one 8 KB box for each stored block (bn, bm), bn < bm,
+// seen the other way round (its rows (n, m): dS is symmetric and stored as it is); all land
+// as [m'][n'][col], 1 + bm boxes per plane instead of one per 16-column block.  The compute
+// warps fold U_g into dvx[col] += k_j[4g+m'] U_g[j][(m', col)] (registers) and
+// sum_col v_j[col] U_g[j][(m', col)] into the dk sum of key index 4g+m' (shared memory, each
+// column half adding its share).  One product instead of a second, V-side chain halves the
+// tensor work of this part.  A 17th product U'_z = K dzm^T (dzm[m][n] = dz[(m,n)]) adds
 // the normaliser column; its tiles are built in the ring slot of the last group's residual
 // plane once that group's product is done.
 // The gradient state planes and normaliser states carry the reverse scan's operand scales
@@ -32,7 +35,11 @@
 // (u.Vt)^T = V dO^T (bf16), dSs^T and (W zeta)^T as bf16 hi + lo in tensor memory, then
 // dk += dSs^T Q and dv += (W zeta)^T dO.
 // Warps 0-7 compute (warp w: tensor-memory lane quadrant w % 4, column half w / 4), warp 8
-// issues TMA, warp 9 the MMAs.  Every mbarrier wait is bounded (TM2_ERR_TIMEOUT on expiry).
+// issues TMA, warp 9 the inter-chunk products and the intra-chunk scores, warps 10 and 11 the
+// intra-chunk dk and dv products (one thread's tcgen05.mma instructions do not overlap, and an
+// N = 64 one holds its issuer for several times its tensor-core time, so three issuers let a
+// block's scores and both of its products run together).  Every mbarrier wait is bounded
+// (TM2_ERR_TIMEOUT on expiry).
 #include "tm2.h"
 #include "tm2_launch.h"
 #include "tm2_sm100.cuh"
@@ -44,8 +51,9 @@ namespace tckv {
 using namespace tctile;
 
 constexpr int C = TC_CHUNK;
-constexpr int THREADS = 10 * 32;
-constexpr int WARP_TMA = 8, WARP_MMA = 9;
+constexpr int THREADS = 12 * 32;
+constexpr int WARP_TMA = 8, WARP_MMA = 9, WARP_PK = 10;   // warps 10 (dk) and 11 (dv): products
+static_assert(THREADS == (WARP_PK + 2) * 32, "two product warps last");
 constexpr int NR = 5;                         // ring slots of 32 KB
 constexpr int RB = 32768;
 static_assert(NR <= 7, "a slot is reused less than four groups later (gdone ring of four)");
@@ -88,6 +96,11 @@ struct Args {
     int T, NC, Tp;
 };
 
+// runs of 1 .. 4 consecutive packed blocks (make_tmap_state_packed_rowrun), run[nb - 1]
+struct RunMaps {
+    CUtensorMap run[4];
+};
+
 TM2_DEV int slot_of(int r) { return r % NR; }
 TM2_DEV uint32_t use_of(int r) { return (uint32_t)(r / NR); }
 
@@ -99,7 +112,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
                                                                  const __grid_constant__ CUtensorMap tmV,
                                                                  const __grid_constant__ CUtensorMap tmQ,
                                                                  const __grid_constant__ CUtensorMap tmD,
-                                                                 const __grid_constant__ CUtensorMap tmS,
+                                                                 const __grid_constant__ RunMaps rm,
                                                                  const __grid_constant__ CUtensorMap tmSt,
                                                                  const __grid_constant__ Args a) {
     extern __shared__ uint8_t smem_raw[];
@@ -107,7 +120,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
     // gdone[g % 4]: the products of group g are done (its ring slots are free and its U buffer
     // is full): one commit per group serves the TMA producer and the compute warps
     __shared__ __align__(8) uint64_t bar_ld, bar_full[NR], bar_gdone[4], bar_cvt, bar_sfull[4], bar_pdone[4],
-        bar_pfull[4], bar_uempty[2], bar_kvfull, bar_red, bar_zrdy, bar_done;
+        bar_pfull[4], bar_uempty[2], bar_kvfull, bar_red, bar_zrdy, bar_done, bar_pend[2];
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_s;
     __shared__ volatile int gflags[2];         // group waits of the compute warps
@@ -130,7 +143,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
         mbar_init(smem_u32(&bar_cvt), 256);
         for (int b = 0; b < 4; ++b) {
             mbar_init(smem_u32(&bar_sfull[b]), 1);
-            mbar_init(smem_u32(&bar_pdone[b]), 1);
+            mbar_init(smem_u32(&bar_pdone[b]), 2);   // dk and dv products
             mbar_init(smem_u32(&bar_pfull[b]), 256);
         }
         for (int i = 0; i < 2; ++i) {
@@ -138,10 +151,12 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
             mbar_init(smem_u32(&bar_gdone[i + 2]), 1);
             mbar_init(smem_u32(&bar_uempty[i]), 256);
         }
-        mbar_init(smem_u32(&bar_kvfull), 1);
+        mbar_init(smem_u32(&bar_kvfull), 2);
         mbar_init(smem_u32(&bar_red), 256);
         mbar_init(smem_u32(&bar_zrdy), 256);
         mbar_init(smem_u32(&bar_done), 1);
+        mbar_init(smem_u32(&bar_pend[0]), 1);
+        mbar_init(smem_u32(&bar_pend[1]), 1);
         abort_s = 0;
         fence_mbar_init();
     }
@@ -157,7 +172,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
 
     if (warp == WARP_TMA) {
         if (lane == 0) {
-            prefetch_tmap(&tmS);
+            for (int i = 0; i < 4; ++i) prefetch_tmap(&rm.run[i]);
             const uint32_t lb = smem_u32(&bar_ld);
             mbar_arrive_expect_tx(lb, 2 * 16384);
             tma_load_3d(early, &tmK, lb, 0, c * C + tj * 128, (int)bh);
@@ -181,22 +196,17 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
                 const uint32_t fb = smem_u32(&bar_full[sl]), dst = sb0 + RING + sl * RB;
                 mbar_arrive_expect_tx(fb, RB);
                 if (r < 2 * NG) {
-                    // the rows (m, n) of key indices n = 4 nq .. 4 nq + 3 (block column bn) for every m,
-                    // one 8 KB box per 16-row block bm of m, landing as [n'][m'][col]: from the
-                    // stored block (bm, bn) (tmSt: contract over its first index) when bm <= bn,
-                    // else as the mirror rows (n, m) of the stored block (bn, bm) (tmS: contract
-                    // over its second index); the gradient state is symmetric and stored as is
-                    const int g = r >> 1, bn = g >> 2, nq = g & 3, pc = 2 * chunk_id + (r & 1);
-                    for (int bm = 0; bm < 4; ++bm) {
-                        if (!TM2_CHECK(tc_block_index(min(bm, bn), max(bm, bn)) < TC_PACKED_BLOCKS && nq < 4,
-                                       a.status))
-                            continue;   // (the request then never completes: the consumer's bounded wait ends it)
-                        if (bm <= bn)
-                            tma_load_4d(dst + bm * 8192, &tmSt, fb, 0, 0, 4 * nq,
-                                        TC_PACKED_BLOCKS * pc + tc_block_index(bm, bn));
-                        else
-                            tma_load_4d(dst + bm * 8192, &tmS, fb, 0, 0, 16 * tc_block_index(bn, bm) + 4 * nq, pc);
-                    }
+                    // the rows (m, n) of key indices m = 4 mq .. 4 mq + 3 (block row bm) for every n,
+                    // landing as [m'][n'][col] with the 16-column block bn of n at 8 KB bn: the
+                    // stored blocks (bm, bm .. 3) as one run (rows (m, n)), then each stored block
+                    // (bn, bm), bn < bm, seen the other way round (rows (n, m))
+                    const int g = r >> 1, bm = g >> 2, mq = g & 3, pc = 2 * chunk_id + (r & 1);
+                    if (TM2_CHECK(tc_block_index(bm, 3) < TC_PACKED_BLOCKS && mq < 4, a.status)) {
+                        tma_load_5d(dst + bm * 8192, &rm.run[3 - bm], fb, 0, 0, 4 * mq, tc_block_index(bm, bm), pc);
+                        for (int bn = 0; bn < bm; ++bn)
+                            tma_load_4d(dst + bn * 8192, &tmSt, fb, 0, 0, 4 * mq,
+                                        TC_PACKED_BLOCKS * pc + tc_block_index(bn, bm));
+                    }   // (else the request never completes: the consumer's bounded wait ends it)
                 } else if (r == 2 * NG) {
                     tma_load_3d(dst, &tmK, fb, 0, c * C + tj * 128, (int)bh);
                     tma_load_3d(dst + 16384, &tmV, fb, 0, c * C + tj * 128, (int)bh);
@@ -230,7 +240,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
                 const uint32_t d = tmem + ub * 256;
                 if (g < NG) {
                     const uint32_t bhi = sb0 + RING + slot_of(2 * g) * RB, blo = sb0 + RING + slot_of(2 * g + 1) * RB;
-                    // K block kk = m in 16 kk .. 16 kk + 15: box kk ([n'][m'][col], n' blocks 2 KB apart)
+                    // K block kk = n in 16 kk .. 16 kk + 15 at 8 KB kk ([m'][n'][col], m' slices 2 KB apart)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         umma_bf16(d, sdesc_sw128(sb0 + SKH + kk * 32), sdesc_sw128_ex(bhi + kk * 8192, 2048, 1024), IDESC_U,
@@ -263,9 +273,9 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
             const uint32_t SK = sb0 + RING + slot_of(rkv) * RB, SV = SK + 16384;
             const uint32_t SQ = sb0 + RING + slot_of(rq) * RB, SD = sb0 + RING + slot_of(rd) * RB;
             // block b + 1's scores go into S / W as soon as the compute warps have read block b's
-            // (pfull[b]), ahead of block b's products, so that the softmax-free weight step of
-            // b + 1 runs while those products do; pdone[b] tells the compute warps that the
-            // products of block b have read the P buffers they are about to overwrite
+            // (pfull[b]), while the product warps run block b's products, so that the weight step
+            // of b + 1 overlaps them; pdone[b] tells the compute warps that the products of block
+            // b have read the P buffers they are about to overwrite
             auto issue_sw = [&](int b) {
                 const int ib = 2 * tj + b;
 #pragma unroll
@@ -278,28 +288,44 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
                 umma_commit(smem_u32(&bar_sfull[b]));
             };
             if (ok && nblk > 0) issue_sw(0);
+            for (int b = 0; b + 1 < nblk && ok; ++b) {
+                if (abort_s) { ok = false; break; }
+                if (!(ok = mbar_wait(smem_u32(&bar_pfull[b]), 0, a.status))) break;
+                tc_fence_after();
+                issue_sw(b + 1);
+            }
+            if (!ok) abort_s = 1;
+            umma_commit(smem_u32(&bar_done));
+            mbar_wait(smem_u32(&bar_done), 0, a.status);
+        }
+    } else if (warp >= WARP_PK) {
+        // ---- intra-chunk products: dk += dSs^T Q (warp 10) or dv += (W zeta)^T dO (warp 11), the
+        // A operand as bf16 hi + lo in tensor memory.  The accumulators share columns with the
+        // inter-chunk U buffers: pfull[0] comes after the compute warps have read the last U.
+        const int part = warp - WARP_PK;
+        if (lane == 0) {
+            const int rx = part == 0 ? 2 * NG + 1 : 2 * NG + 2;   // Q or dO (last requests: no reuse)
+            bool ok = mbar_wait(smem_u32(&bar_full[slot_of(rx)]), use_of(rx) & 1, a.status);
+            const uint32_t SX = sb0 + RING + slot_of(rx) * RB;
+            const uint32_t acc = tmem + (part == 0 ? TM_DK : TM_DV);
+            const uint32_t ph = tmem + (part == 0 ? TM_DH : TM_WH), pl = tmem + (part == 0 ? TM_DL : TM_WL);
             for (int b = 0; b < nblk && ok; ++b) {
                 const int ib = 2 * tj + b;
                 if (abort_s) { ok = false; break; }
                 if (!(ok = mbar_wait(smem_u32(&bar_pfull[b]), 0, a.status))) break;
                 tc_fence_after();
-                if (b + 1 < nblk) issue_sw(b + 1);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t qd = sdesc_sw128_ex(SQ + ib * 8192 + kk * 2048, 8192, 1024);
-                    const uint64_t dd = sdesc_sw128_ex(SD + ib * 8192 + kk * 2048, 8192, 1024);
-                    const uint32_t acc0 = (b > 0 || kk > 0) ? 1u : 0u;
-                    umma_bf16_ts(tmem + TM_DK, tmem + TM_DH + kk * 8, qd, IDESC_BF_MN, acc0);
-                    umma_bf16_ts(tmem + TM_DK, tmem + TM_DL + kk * 8, qd, IDESC_BF_MN, 1u);
-                    umma_bf16_ts(tmem + TM_DV, tmem + TM_WH + kk * 8, dd, IDESC_BF_MN, acc0);
-                    umma_bf16_ts(tmem + TM_DV, tmem + TM_WL + kk * 8, dd, IDESC_BF_MN, 1u);
+                    const uint64_t xd = sdesc_sw128_ex(SX + ib * 8192 + kk * 2048, 8192, 1024);
+                    umma_bf16_ts(acc, ph + kk * 8, xd, IDESC_BF_MN, (b > 0 || kk > 0) ? 1u : 0u);
+                    umma_bf16_ts(acc, pl + kk * 8, xd, IDESC_BF_MN, 1u);
                 }
                 umma_commit(smem_u32(&bar_pdone[b]));
             }
             if (ok) umma_commit(smem_u32(&bar_kvfull));
             else abort_s = 1;
-            umma_commit(smem_u32(&bar_done));
-            mbar_wait(smem_u32(&bar_done), 0, a.status);
+            umma_commit(smem_u32(&bar_pend[part]));   // none of this thread's MMAs in flight at exit
+            mbar_wait(smem_u32(&bar_pend[part]), 0, a.status);
         }
     } else {
         // ---------------------------------------------------------------- compute warps
@@ -350,8 +376,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_bwd_dkdv_kernel(const __grid_co
         }
         mbar_arrive(smem_u32(&bar_cvt));
         // ---- inter-chunk groups: dvx[col] += k_j[n] U[(n, col)]; sDK[n] += sum_col v_j[col] U[(n, col)]
-        // (each column half adds its share; U[(n, col)] = sum_m k_j[m] dS[(m, n), col] and dS is
-        // symmetric in (m, n), so the second sum is the dk term of key index n)
+        // (each column half adds its share; U[(m, col)] = sum_n k_j[n] dS[(m, n), col], so the
+        // second sum is the dk term of key index m)
         float dvx[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k) dvx[k] = 0.f;
@@ -504,11 +530,15 @@ cudaError_t tc_bwd_dkdv(const Problem& p, const void* q, const void* k, const vo
                         const float* Aloc, const float* g, const float* zeta, const float* ucol, const float* rowterm,
                         const void* dSx, const float* dzx, const float* sscale, const unsigned* amax_r, void* dk,
                         void* dv, float* dcum, cudaStream_t s) {
-    CUtensorMap tk, tv, tq, td, ts, tst;
+    CUtensorMap tk, tv, tq, td, tst;
+    RunMaps rm;
     const uint64_t BH = (uint64_t)p.BH(), T = (uint64_t)p.T;
     if (!make_tmap_bf16_3d(&tk, k, BH, T, 64, 128) || !make_tmap_bf16_3d(&tv, v, BH, T, 64, 128) ||
         !make_tmap_bf16_3d(&tq, q, BH, T, 64, 256) || !make_tmap_bf16_3d(&td, dO, BH, T, 64, 256) ||
-        !make_tmap_state_packed_quads(&ts, dSx, BH * (uint64_t)p.NC) ||
+        !make_tmap_state_packed_rowrun(&rm.run[0], dSx, BH * (uint64_t)p.NC, 1) ||
+        !make_tmap_state_packed_rowrun(&rm.run[1], dSx, BH * (uint64_t)p.NC, 2) ||
+        !make_tmap_state_packed_rowrun(&rm.run[2], dSx, BH * (uint64_t)p.NC, 3) ||
+        !make_tmap_state_packed_rowrun(&rm.run[3], dSx, BH * (uint64_t)p.NC, 4) ||
         !make_tmap_state_packed_tquads(&tst, dSx, BH * (uint64_t)p.NC))
         return cudaErrorInvalidValue;
     int* status = tc_status_ptr();
@@ -518,7 +548,7 @@ cudaError_t tc_bwd_dkdv(const Problem& p, const void* q, const void* k, const vo
     cudaError_t e = cudaFuncSetAttribute(tc_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, BYTES);
     if (e != cudaSuccess) return e;
     dim3 grid(2 * p.NC, (unsigned)p.BH());
-    tc_bwd_dkdv_kernel<<<grid, THREADS, BYTES, s>>>(tk, tv, tq, td, ts, tst, a);
+    tc_bwd_dkdv_kernel<<<grid, THREADS, BYTES, s>>>(tk, tv, tq, td, rm, tst, a);
     return cudaGetLastError();
 }
 
