@@ -200,7 +200,7 @@ cudaError_t launch_dy_prep(const Problem& p, const void* o, const float* Z, cons
 //   zeta = 1/Z (normalised) or 1, ucol = -D (normalised) or 0, rowterm = 0 (normalised)
 //   or D, so that dL/dY_i = zeta_i [dO_i, ucol_i];  zmax[c] = max over the chunk of
 //   exp(A_i) zeta_i (the scale of the reverse state scan's generated operand).
-__global__ void __launch_bounds__(256) tc_dy_prep_kernel(const float* __restrict__ o, const float* __restrict__ Z,
+__global__ void __launch_bounds__(256, 3) tc_dy_prep_kernel(const float* __restrict__ o, const float* __restrict__ Z,
                                                          const __nv_bfloat16* __restrict__ dO,
                                                          const float* __restrict__ Aloc, float* __restrict__ zeta,
                                                          float* __restrict__ ucol, float* __restrict__ rowterm,
@@ -211,34 +211,47 @@ __global__ void __launch_bounds__(256) tc_dy_prep_kernel(const float* __restrict
     const int sub = lane >> 3, l8 = lane & 7;   // four tokens per warp pass, eight lanes per token
     const long bh = blockIdx.y;
     float mx = 0.f, umx = 0.f;
-    for (int j0 = warp * 4; j0 < C; j0 += 32) {
-        const long t = (long)c * C + j0 + sub;
-        const bool in = t < T;
-        const long tok = bh * T + (in ? t : 0);
-        float D = 0.f;
-        if (in) {   // elements 8*l8 .. 8*l8+7 of the row: one 16-byte dO load, two 16-byte o loads
-            const uint4 d8 = *reinterpret_cast<const uint4*>(dO + tok * 64 + 8 * l8);
-            const float4 o0 = *reinterpret_cast<const float4*>(o + tok * 64 + 8 * l8);
-            const float4 o1 = *reinterpret_cast<const float4*>(o + tok * 64 + 8 * l8 + 4);
-            const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&d8);
+    constexpr int NP = 4;   // passes whose loads are in flight together
+    for (int jp = 0; jp < C; jp += 32 * NP) {
+        // elements 8*l8 .. 8*l8+7 of each pass's row: one 16-byte dO load, two 16-byte o loads
+        uint4 d8[NP];
+        float4 o0[NP], o1[NP];
+        float zr[NP], ar[NP];
+#pragma unroll
+        for (int k = 0; k < NP; ++k) {
+            const long t = (long)c * C + jp + 32 * k + warp * 4 + sub;
+            const bool in = t < T && jp + 32 * k < C;
+            const long tok = bh * T + (in ? t : 0);
+            d8[k] = in ? *reinterpret_cast<const uint4*>(dO + tok * 64 + 8 * l8) : make_uint4(0, 0, 0, 0);
+            o0[k] = in ? *reinterpret_cast<const float4*>(o + tok * 64 + 8 * l8) : make_float4(0.f, 0.f, 0.f, 0.f);
+            o1[k] = in ? *reinterpret_cast<const float4*>(o + tok * 64 + 8 * l8 + 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+            zr[k] = in && normalize ? Z[tok] : 1.f;
+            ar[k] = in ? Aloc[bh * (long)NC * C + t] : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < NP; ++k) {
+            const long t = (long)c * C + jp + 32 * k + warp * 4 + sub;
+            const bool in = t < T && jp + 32 * k < C;
+            const long tok = bh * T + (in ? t : 0);
+            const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&d8[k]);
             const float2 f0 = __bfloat1622float2(b2[0]), f1 = __bfloat1622float2(b2[1]);
             const float2 f2 = __bfloat1622float2(b2[2]), f3 = __bfloat1622float2(b2[3]);
-            D = f0.x * o0.x + f0.y * o0.y + f1.x * o0.z + f1.y * o0.w + f2.x * o1.x + f2.y * o1.y + f3.x * o1.z +
-                f3.y * o1.w;
-        }
-        D += __shfl_xor_sync(0xffffffffu, D, 1);
-        D += __shfl_xor_sync(0xffffffffu, D, 2);
-        D += __shfl_xor_sync(0xffffffffu, D, 4);
-        if (in) {
-            const float z = normalize ? Z[tok] : 1.f;
-            const float ze = normalize ? (z != 0.f ? 1.f / z : 0.f) : 1.f;
-            if (l8 == 0) {
-                zeta[tok] = ze;
-                ucol[tok] = normalize ? -D : 0.f;
-                rowterm[tok] = normalize ? 0.f : D;
+            float D = f0.x * o0[k].x + f0.y * o0[k].y + f1.x * o0[k].z + f1.y * o0[k].w + f2.x * o1[k].x +
+                      f2.y * o1[k].y + f3.x * o1[k].z + f3.y * o1[k].w;
+            D += __shfl_xor_sync(0xffffffffu, D, 1);
+            D += __shfl_xor_sync(0xffffffffu, D, 2);
+            D += __shfl_xor_sync(0xffffffffu, D, 4);
+            if (in) {
+                const float z = zr[k];
+                const float ze = normalize ? (z != 0.f ? 1.f / z : 0.f) : 1.f;
+                if (l8 == 0) {
+                    zeta[tok] = ze;
+                    ucol[tok] = normalize ? -D : 0.f;
+                    rowterm[tok] = normalize ? 0.f : D;
+                }
+                mx = fmaxf(mx, __expf(ar[k]) * ze);
+                if (normalize) umx = fmaxf(umx, fabsf(D));
             }
-            mx = fmaxf(mx, __expf(Aloc[bh * (long)NC * C + t]) * ze);
-            if (normalize) umx = fmaxf(umx, fabsf(D));
         }
     }
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
@@ -287,14 +300,20 @@ __global__ void __launch_bounds__(256) head_absmax_kernel(const __nv_bfloat16* _
     __shared__ uint32_t red[2][8];
     const long bh = blockIdx.y;
     const long t0 = (long)blockIdx.x * 128;
-    uint32_t mx = 0, my = 0;
-    for (int e = threadIdx.x; e < 1024; e += 256) {
+    uint4 xr[4], yr[4];   // all eight 16-byte loads in flight before the reduction
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int e = threadIdx.x + 256 * i;
         const long t = t0 + (e >> 3);
-        if (t < T) {
-            const long off = (bh * T + t) * 64 + 8 * (e & 7);
-            mx = max(mx, bf16x8_absmax_bits(*reinterpret_cast<const uint4*>(x + off)));
-            my = max(my, bf16x8_absmax_bits(*reinterpret_cast<const uint4*>(y + off)));
-        }
+        const long off = (bh * T + t) * 64 + 8 * (e & 7);
+        xr[i] = t < T ? *reinterpret_cast<const uint4*>(x + off) : make_uint4(0, 0, 0, 0);
+        yr[i] = t < T ? *reinterpret_cast<const uint4*>(y + off) : make_uint4(0, 0, 0, 0);
+    }
+    uint32_t mx = 0, my = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        mx = max(mx, bf16x8_absmax_bits(xr[i]));
+        my = max(my, bf16x8_absmax_bits(yr[i]));
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -328,8 +347,8 @@ cudaError_t launch_head_absmax(const Problem& p, const void* x, const void* y, u
     return cudaGetLastError();
 }
 
-// Operands of the tensor-core chunk-state scan, one block of 256 threads per 64-token stage
-// of one (b, h), written as one [144][64] fp16 block per stage (token j = stage*64 + column):
+// Operands of the tensor-core chunk-state scan, one thread per token (256 tokens per block of
+// one (b, h)), written as one [144][64] fp16 block per 64-token stage (token j = stage*64 + column):
 //   rows   0-63 : [n][j]   = fp16(ks key_j[n])         (the key block, transposed)
 //   rows  64-127: [col][j] = fp16(vs w_j val_j[col])   (the weighted values, transposed)
 //   row   128   : [j]      = fp16(zs w_j zc_j)         (the normaliser column)
@@ -345,100 +364,80 @@ __global__ void __launch_bounds__(256) tc_scan_operands_kernel(
     const float* __restrict__ g, const float* __restrict__ zeta, const float* __restrict__ ucol,
     const float* __restrict__ zmax, const unsigned* __restrict__ amax, __half* __restrict__ ops, int T, int C, int NC,
     int rev) {
-    __shared__ float sk[64][65];
-    __shared__ float sv[64][65];
-    __shared__ float sw[64], szc[64];
-    const int st = blockIdx.x, tid = threadIdx.x;
+    // one token per thread, one warp per 32 tokens (half a stage); the transposition goes
+    // through registers: the lanes of a pair trade halves so that each writes two adjacent
+    // tokens of one row (even lane: row 2p, odd lane: row 2p + 1), 128 bytes per warp store
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long bh = blockIdx.y;
-    const int Tp = NC * C, c = (st * 64) / C;
-    const long t0 = (long)st * 64;
-    // the stage's key and value rows (16 bytes per thread and token half) are loaded first, so
-    // their latency overlaps the weights' loads and exponentials
-    const int q8 = tid & 7, jb = tid >> 3;   // token jb and jb + 32, elements 8 q8 .. 8 q8 + 7
-    uint4 k8[2], v8[2];
+    const int Tp = NC * C;
+    const long tw = (long)blockIdx.x * 256 + warp * 32;   // the warp's first token
+    if (tw >= Tp) return;
+    const long t = tw + lane;
+    const int st = (int)(tw / 64), c = (int)(t / C);
+    const bool in = t < T;
+    // the token's key and value rows first (16 loads in flight), then its weight's terms
+    uint4 kr[8], vr[8];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const long t = t0 + jb + 32 * h;
-        if (t < T) {
-            k8[h] = *reinterpret_cast<const uint4*>(key + (bh * T + t) * 64 + 8 * q8);
-            v8[h] = *reinterpret_cast<const uint4*>(val + (bh * T + t) * 64 + 8 * q8);
-        } else {
-            k8[h] = v8[h] = make_uint4(0, 0, 0, 0);
-        }
+    for (int i = 0; i < 8; ++i) {
+        kr[i] = in ? reinterpret_cast<const uint4*>(key + (bh * T + t) * 64)[i] : make_uint4(0, 0, 0, 0);
+        vr[i] = in ? reinterpret_cast<const uint4*>(val + (bh * T + t) * 64)[i] : make_uint4(0, 0, 0, 0);
     }
     const float ks = pow2_scale(amax[bh * 4]), vs = pow2_scale(amax[bh * 4 + 1]);
     const float zs = rev ? pow2_scale(amax[bh * 4 + 2]) : 1.f;
-    if (tid < 64) {
-        const long t = t0 + tid;
-        const float A = Aloc[bh * Tp + t];
-        float w = 0.f, zc = 0.f;
-        if (rev) {
-            if (t < T) {
-                w = __expf(A) * zeta[bh * T + t] / zmax[bh * NC + c];
-                zc = ucol[bh * T + t];
-            }
-        } else {
-            w = t < T ? __expf(g[bh * NC + c] - A) : 0.f;
-            zc = 1.f;
+    const float A = Aloc[bh * Tp + t];
+    float w = 0.f, zc = 0.f;
+    if (rev) {
+        if (in) {
+            w = __expf(A) * zeta[bh * T + t] / zmax[bh * NC + c];
+            zc = ucol[bh * T + t];
         }
-        sw[tid] = w;
-        szc[tid] = zc;
+    } else {
+        w = in ? __expf(g[bh * NC + c] - A) : 0.f;
+        zc = 1.f;
     }
-    __syncthreads();
+    const float wv = vs * w;
+    // fp16(ks key[n]) and fp16(vs w val[col]) as half2 words (element pairs 2p, 2p + 1)
+    uint32_t kh[32], vh[32];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int j = jb + 32 * h;
-        const __nv_bfloat162* kb = reinterpret_cast<const __nv_bfloat162*>(&k8[h]);
-        const __nv_bfloat162* vb = reinterpret_cast<const __nv_bfloat162*>(&v8[h]);
-        const float wv = vs * sw[j];
+    for (int i = 0; i < 8; ++i) {
+        const __nv_bfloat162* kb = reinterpret_cast<const __nv_bfloat162*>(&kr[i]);
+        const __nv_bfloat162* vb = reinterpret_cast<const __nv_bfloat162*>(&vr[i]);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const float2 kk = __bfloat1622float2(kb[u]), vv = __bfloat1622float2(vb[u]);
-            sk[j][8 * q8 + 2 * u] = kk.x * ks;
-            sk[j][8 * q8 + 2 * u + 1] = kk.y * ks;
-            sv[j][8 * q8 + 2 * u] = vv.x * wv;
-            sv[j][8 * q8 + 2 * u + 1] = vv.y * wv;
+            const __half2 hk = __floats2half2_rn(kk.x * ks, kk.y * ks);
+            const __half2 hv = __floats2half2_rn(vv.x * wv, vv.y * wv);
+            kh[4 * i + u] = *reinterpret_cast<const uint32_t*>(&hk);
+            vh[4 * i + u] = *reinterpret_cast<const uint32_t*>(&hv);
         }
     }
-    __syncthreads();
     __half* blk = ops + (bh * (Tp / 64) + st) * (long)(TC_OPS_ROWS * 64);
-    // transposed key and weighted-value blocks: thread writes 16 consecutive j of one row
-    {
-        const int n = tid >> 2, j0 = (tid & 3) * 16;
-        uint32_t wk[8], wvv[8];
+    const bool odd = lane & 1;
+    const int j = (int)(tw % 64) + (lane & ~1);   // the pair's first token column in the stage
+    uint32_t* rk = reinterpret_cast<uint32_t*>(blk + (odd ? 64 : 0) + j);         // row 2p (+1 odd) at 128 p
+    uint32_t* rv = reinterpret_cast<uint32_t*>(blk + 64 * 64 + (odd ? 64 : 0) + j);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const __half2 hk = __floats2half2_rn(sk[j0 + 2 * u][n], sk[j0 + 2 * u + 1][n]);
-            const __half2 hv = __floats2half2_rn(sv[j0 + 2 * u][n], sv[j0 + 2 * u + 1][n]);
-            wk[u] = *reinterpret_cast<const uint32_t*>(&hk);
-            wvv[u] = *reinterpret_cast<const uint32_t*>(&hv);
-        }
-        uint4* dk = reinterpret_cast<uint4*>(blk + n * 64 + j0);
-        dk[0] = make_uint4(wk[0], wk[1], wk[2], wk[3]);
-        dk[1] = make_uint4(wk[4], wk[5], wk[6], wk[7]);
-        uint4* dv = reinterpret_cast<uint4*>(blk + (64 + n) * 64 + j0);
-        dv[0] = make_uint4(wvv[0], wvv[1], wvv[2], wvv[3]);
-        dv[1] = make_uint4(wvv[4], wvv[5], wvv[6], wvv[7]);
+    for (int q = 0; q < 32; ++q) {
+        const uint32_t sk = odd ? (kh[q] & 0xffffu) : (kh[q] >> 16);   // what the partner lane needs
+        const uint32_t sv = odd ? (vh[q] & 0xffffu) : (vh[q] >> 16);
+        const uint32_t gk = __shfl_xor_sync(0xffffffffu, sk, 1), gv = __shfl_xor_sync(0xffffffffu, sv, 1);
+        rk[q * 64] = odd ? (gk | (kh[q] & 0xffff0000u)) : ((kh[q] & 0xffffu) | (gk << 16));
+        rv[q * 64] = odd ? (gv | (vh[q] & 0xffff0000u)) : ((vh[q] & 0xffffu) | (gv << 16));
     }
-    // the normaliser row (8 threads, 8 tokens each) and the zero rows after it, 16 bytes a store
-    if (tid < 8) {
-        uint32_t wz[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int j = 8 * tid + 2 * u;
-            const __half2 hz = __floats2half2_rn(zs * sw[j] * szc[j], zs * sw[j + 1] * szc[j + 1]);
-            wz[u] = *reinterpret_cast<const uint32_t*>(&hz);
-        }
-        reinterpret_cast<uint4*>(blk + 128 * 64)[tid] = make_uint4(wz[0], wz[1], wz[2], wz[3]);
-    }
-    for (int e = tid; e < (TC_OPS_ROWS - 129) * 8; e += 256)
-        reinterpret_cast<uint4*>(blk + 129 * 64)[e] = make_uint4(0, 0, 0, 0);
+    // the normaliser row (even lanes, two tokens a word) and this half-stage's part of the zero rows
+    const __half hz = __float2half_rn(zs * w * zc);
+    const uint32_t zb = *reinterpret_cast<const unsigned short*>(&hz);
+    const uint32_t zo = __shfl_xor_sync(0xffffffffu, zb, 1);
+    if (!odd) reinterpret_cast<uint32_t*>(blk + 128 * 64 + j)[0] = zb | (zo << 16);
+    const int half = (int)(tw % 64) / 32;
+    for (int e = lane; e < (TC_OPS_ROWS - 129) * 4; e += 32)   // 15 rows x 64 bytes, 16 bytes a store
+        reinterpret_cast<uint4*>(blk + (129 + e / 4) * 64 + 32 * half)[e & 3] = make_uint4(0, 0, 0, 0);
 }
 
 cudaError_t launch_tc_scan_operands(const Problem& p, bool rev, const void* key, const void* val, const float* Aloc,
                                     const float* g, const float* zeta, const float* ucol, const float* zmax,
                                     const unsigned* amax, void* ops, cudaStream_t s) {
-    dim3 grid((unsigned)(p.Tp() / 64), (unsigned)p.BH());
+    dim3 grid((unsigned)((p.Tp() + 255) / 256), (unsigned)p.BH());
     tc_scan_operands_kernel<<<grid, 256, 0, s>>>((const __nv_bfloat16*)key, (const __nv_bfloat16*)val, Aloc, g, zeta,
                                                  ucol, zmax, amax, (__half*)ops, p.T, p.C, p.NC, rev ? 1 : 0);
     return cudaGetLastError();
