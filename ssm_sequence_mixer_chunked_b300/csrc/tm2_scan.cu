@@ -24,28 +24,53 @@ TM2_DEV float block_inclusive_scan(float v, float* wsum /* >= 32 floats */) {
     return s;
 }
 
-// The same in fp64 (the long reverse sums of the A-mask gradient).
-TM2_DEV double block_inclusive_scan_d(double v, double* wsum /* >= 32 doubles */) {
+// Double-float sums (an unevaluated pair hi + lo of fp32 values, about 48 significant bits)
+// for the long reverse sums of the A-mask gradient: the error-free sum of two floats is
+// Knuth's TwoSum, and the pair is renormalised with Dekker's Fast2Sum.  fp64 arithmetic would
+// do as well but runs at a small fraction of the fp32 rate on this part; these are plain fp32
+// adds and subtracts (no products, so nothing can be contracted into an FMA).
+struct df32 {
+    float hi, lo;
+};
+TM2_DEV df32 df_two_sum(float a, float b) {
+    const float s = a + b, bb = s - a;
+    return {s, (a - (s - bb)) + (b - bb)};
+}
+TM2_DEV df32 df_fast_two_sum(float a, float b) {   // |a| >= |b|
+    const float s = a + b;
+    return {s, b - (s - a)};
+}
+// Sum of two pairs with both the high and the low parts added error-free, so that the
+// cancelling sums stay accurate relative to the result.
+TM2_DEV df32 df_add(df32 x, df32 y) {
+    const df32 s = df_two_sum(x.hi, y.hi), t = df_two_sum(x.lo, y.lo);
+    df32 r = df_fast_two_sum(s.hi, s.lo + t.hi);
+    return df_fast_two_sum(r.hi, r.lo + t.lo);
+}
+TM2_DEV df32 df_shfl_up(df32 v, int o) {
+    return {__shfl_up_sync(0xffffffffu, v.hi, o), __shfl_up_sync(0xffffffffu, v.lo, o)};
+}
+TM2_DEV df32 block_inclusive_scan_df(df32 v, df32* wsum /* >= 32 */) {
     const int t = threadIdx.x, w = t >> 5, lane = t & 31, nw = (blockDim.x + 31) >> 5;
-    double s = v;
+    df32 s = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const double u = __shfl_up_sync(0xffffffffu, s, o);
-        if (lane >= o) s += u;
+        const df32 u = df_shfl_up(s, o);
+        if (lane >= o) s = df_add(s, u);
     }
     if (lane == 31) wsum[w] = s;
     __syncthreads();
     if (w == 0) {
-        double x = lane < nw ? wsum[lane] : 0.0;
+        df32 x = lane < nw ? wsum[lane] : df32{0.f, 0.f};
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const double u = __shfl_up_sync(0xffffffffu, x, o);
-            if (lane >= o) x += u;
+            const df32 u = df_shfl_up(x, o);
+            if (lane >= o) x = df_add(x, u);
         }
         wsum[lane] = x;
     }
     __syncthreads();
-    if (w > 0) s += wsum[w - 1];
+    if (w > 0) s = df_add(s, wsum[w - 1]);
     __syncthreads();
     return s;
 }
@@ -126,30 +151,31 @@ cudaError_t launch_global_cumsum(const Problem& p, const float* Aloc, const floa
 // grid (tiles, BH), block 1024: tile j holds the 1024 tokens ending at T - 1 - 1024 j (thread 0
 // the latest).  Its carry is the sum over every later token, read directly (a block reduction:
 // the later tokens of all tiles of a head total T^2 / 2048 reads, small next to the rest), so
-// the tiles of a head run in parallel.  The sums are kept in fp64: over thousands of tokens the
-// terms largely cancel (their total is zero without an initial state), and an fp32 sum would
-// leave a rounding error comparable to the result.
+// the tiles of a head run in parallel.  The sums are kept as double-float pairs: over
+// thousands of tokens the terms largely cancel (their total is zero without an initial state),
+// and an fp32 sum would leave a rounding error comparable to the result.  Each term
+// row - col is formed exactly (TwoSum).
 __global__ void __launch_bounds__(1024) reverse_cumsum_da_kernel(
     const float* __restrict__ a, const float* __restrict__ row, const float* __restrict__ col,
     float* __restrict__ da, int T) {
-    __shared__ double wsum[32];
+    __shared__ df32 wsum[32];
+    __shared__ df32 carry_s;
     const int j = blockIdx.x;
     const long bh = blockIdx.y;
     const int top = T - 1 - 1024 * j;            // the latest token of this tile
-    auto term = [&](int u) { return (double)row[bh * T + u] - (col ? (double)col[bh * T + u] : 0.0); };
-    double part = 0.0;
-    for (int u = top + 1 + (int)threadIdx.x; u < T; u += blockDim.x) part += term(u);
+    auto term = [&](int u) { return df_two_sum(row[bh * T + u], col ? -col[bh * T + u] : 0.f); };
+    df32 part = {0.f, 0.f};
+    for (int u = top + 1 + (int)threadIdx.x; u < T; u += blockDim.x) part = df_add(part, term(u));
     // block total of `part`: the last element of the inclusive scan
-    const double run = block_inclusive_scan_d(part, wsum);
-    __shared__ double carry_s;
+    const df32 run = block_inclusive_scan_df(part, wsum);
     if (threadIdx.x == blockDim.x - 1) carry_s = run;
     __syncthreads();
-    const double carry = carry_s;
+    const df32 carry = carry_s;
     __syncthreads();
     const int u = top - (int)threadIdx.x;
-    const double x = u >= 0 ? term(u) : 0.0;
-    const double sres = block_inclusive_scan_d(x, wsum) + carry;
-    if (u >= 0) da[bh * T + u] = -sigmoid_f(a[bh * T + u]) * (float)sres;
+    const df32 x = u >= 0 ? term(u) : df32{0.f, 0.f};
+    const df32 sres = df_add(block_inclusive_scan_df(x, wsum), carry);
+    if (u >= 0) da[bh * T + u] = -sigmoid_f(a[bh * T + u]) * (sres.hi + sres.lo);
 }
 
 cudaError_t launch_reverse_cumsum_da(const Problem& p, const float* a, const float* row,
