@@ -222,8 +222,9 @@ def summarize(trace):
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
     """SM clock, its maximum, power and the throttle reasons, sampled during the timed region:
-    every ~2 ms from NVML in a thread (read-only queries), else every 100 ms by nvidia-smi.  The
-    samples are CSV lines in nvidia-smi's format either way (parse_clocks)."""
+    about every millisecond from NVML in a thread (read-only queries; the power reading every
+    eighth sample), else every 100 ms by nvidia-smi.  The samples are CSV lines in
+    nvidia-smi's format either way (parse_clocks)."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
@@ -241,17 +242,23 @@ class ClockSampler:
             self.gpu = str(device)
 
     def _nvml_loop(self, nv, h):
+        # the clock and the reasons every sample; the maximum clock once and the power every
+        # eighth sample (the slowest query), carried between
+        smax, pw, i = None, 0.0, 0
         while not self.stop_flag:
             try:
+                if smax is None:
+                    smax = nv.nvmlDeviceGetMaxClockInfo(h, nv.NVML_CLOCK_SM)
+                if i % 8 == 0:
+                    pw = nv.nvmlDeviceGetPowerUsage(h) / 1000.0
                 sm = nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM)
-                smax = nv.nvmlDeviceGetMaxClockInfo(h, nv.NVML_CLOCK_SM)
-                pw = nv.nvmlDeviceGetPowerUsage(h) / 1000.0
                 r = nv.nvmlDeviceGetCurrentClocksEventReasons(h)
                 flags = ["Active" if r & b else "Not Active" for b in self.BITS]
                 self.lines.append("%d, %d, %.1f, %s\n" % (sm, smax, pw, ", ".join(flags)))
             except Exception:
                 break
-            time.sleep(0.001)
+            i += 1
+            time.sleep(0.0005)
 
     def start(self):
         self.stop_flag = False
@@ -866,7 +873,7 @@ def run_case(name):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="tm2", choices=["tm2", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
