@@ -555,6 +555,8 @@ def run_tm2(args, world, rank, device):
         line["e_decode"] = run_e_decode(args, tm2, device, trace, pk, world)
     if not args.no_quadratic:
         line["quadratic_form"] = run_quadratic(args, tm2, device, trace, pk, world)
+    if not args.no_conv:
+        line["conv"] = run_conv(args, tm2, device, trace, pk, world)
     if rank == 0 and world == 1 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(inp_cpu, w)
     if rank == 0:
@@ -695,6 +697,79 @@ def run_decode(args, tm2, device, trace, pk, world):
                                   "traffic": ncu_traffic("decode_step_packed", N * H)},
                      "note": "symmetric-packed state (d(d+1)/2 of d^2 rows); effective_GBps counts the full "
                              "state's bytes, roofline the bytes actually moved"}
+    return out
+
+
+def conv_bytes_per_element(backward=False):
+    """Algorithmic bytes per (b, h, t, channel) element of the size-2 input convolution with bf16
+    tensors: forward x in, y out; backward dy in and fp32 dx out (dx pass), x and dy in (weight
+    gradient pass).  The weights, biases and per-head gradients are negligible."""
+    return (2 + 4) + (2 + 2) if backward else 2 + 2
+
+
+def run_conv(args, tm2, device, trace, pk, world):
+    """The size-2 input convolution over q, k and v at the main workload's shape (forward), its
+    backward for one tensor, and the decode step with the fused convolution."""
+    w = si.WORKLOADS[3]
+    B, H, T, C = w.B, w.H, w.T, w.d
+    gen = torch.Generator(device).manual_seed(7)
+    xs = [torch.randn(B, H, T, C, generator=gen, device=device).to(torch.bfloat16) for _ in range(3)]
+    dy = torch.randn(B, H, T, C, generator=gen, device=device).to(torch.bfloat16)
+    wt = torch.randn(H, C, 2, generator=gen, device=device) * 0.7
+    bt = torch.randn(H, C, generator=gen, device=device) * 0.1
+    n = max(args.steps, 10)
+
+    def timed(fn, name):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        barrier(world)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        trace.start()
+        ev0.record()
+        for _ in range(n):
+            fn()
+        ev1.record()
+        torch.cuda.synchronize()
+        recs = [m for nm, m in trace.stop() if nm == name]
+        return max_over_ranks(ev0.elapsed_time(ev1) / n, world), sum(recs) / max(len(recs), 1), len(recs)
+
+    fwd_ms, fwd_kms, nf = timed(lambda: [tm2.conv2_forward(x, wt, bt) for x in xs], "conv2_fwd")
+    bwd_ms, bwd_kms, nb = timed(lambda: tm2.conv2_backward(xs[0], wt, dy), "conv2_bwd")
+    elems = B * H * T * C
+    fb, bb = conv_bytes_per_element() * elems, conv_bytes_per_element(True) * elems
+    out = {"workload": "size-2 input convolution, B=%d H=%d T=%d C=%d bf16: forward of q, k, v; backward of one "
+                       "tensor (dx, dw, db); %d steps" % (B, H, T, C, n),
+           "fwd_ms_per_step": fwd_ms, "bwd_ms_per_step": bwd_ms,
+           "roofline_fwd": {"kernel": "conv2_fwd", "bound": "hbm", "achieved": fb / (fwd_kms * 1e-3) / 1e9,
+                            "peak": pk["hbm_gbs"], "unit": "GB/s",
+                            "frac": fb / (fwd_kms * 1e-3) / 1e9 / pk["hbm_gbs"], "traffic": None},
+           "roofline_bwd": {"kernel": "conv2_bwd (dx and weight-gradient passes)", "bound": "hbm",
+                            "achieved": bb / (bwd_kms * 1e-3) / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                            "frac": bb / (bwd_kms * 1e-3) / 1e9 / pk["hbm_gbs"], "traffic": None},
+           "gpu_launches": nf + 2 * nb}
+    del xs, dy
+    # decode step with the fused convolution against the plain step, the decode workload's shape
+    wd = si.WORKLOADS[4]
+    N, d = wd.B, wd.d
+    S, z = si.decode_initial_state(N, wd.H, d, d, S0_std=wd.S0_std)
+    S, z = S.to(device), z.to(device)
+    tok = {k: v.to(device) for k, v in si.decode_token(0, N, wd.H, d, d, qkv_std=wd.qkv_std).items()}
+    cw = tuple(torch.randn(wd.H, d, 2, generator=gen, device=device) * 0.7 for _ in range(3))
+    cb = tuple(torch.randn(wd.H, d, generator=gen, device=device) * 0.1 for _ in range(3))
+    caches = tuple(torch.zeros(N, wd.H, d, device=device) for _ in range(3))
+    o = torch.empty((N, wd.H, d), dtype=torch.float32, device=device)
+    Zo = torch.empty((N, wd.H), dtype=torch.float32, device=device)
+    conv_ms, conv_kms, _ = timed(lambda: tm2.step_conv(tok["q"], tok["k"], tok["v"], tok["a"], cw, cb, caches, S, z,
+                                                       out=o, Z=Zo), "decode_step_conv")
+    dbytes = decode_bytes_per_head(d, d) * N * wd.H
+    out["decode_step_conv"] = {"ms_per_step": conv_ms, "kernel_ms_per_launch": conv_kms,
+                               "roofline": {"kernel": "decode_step (fused convolution)", "bound": "hbm",
+                                            "achieved": dbytes / (conv_kms * 1e-3) / 1e9, "peak": pk["hbm_gbs"],
+                                            "unit": "GB/s", "frac": dbytes / (conv_kms * 1e-3) / 1e9 / pk["hbm_gbs"],
+                                            "traffic": None},
+                               "note": "N=%d x H=%d, d=%d, fp32 state; bytes as the plain step (the caches add "
+                                       "3 x N x H x d x 8 B)" % (N, wd.H, d)}
     return out
 
 
@@ -881,6 +956,7 @@ def main():
     ap.add_argument("--no-e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-quadratic", action="store_true")
+    ap.add_argument("--no-conv", action="store_true")
     ap.add_argument("--case", default=None, help="run one small profiling case and exit")
     args = ap.parse_args()
     if args.case:

@@ -224,7 +224,8 @@ int tm2_state_unpack(const float* S_packed, const float* z_packed, float* S, flo
  * in dtype or NULL (the token before t = 0; zero if NULL), y (B,H,T,C) in dtype:
  *   y_t = w[..,0] x_t + w[..,1] x_{t-1} (+ b).
  * Backward: dx (B,H,T,C), dx_prev (B,H,C, or NULL), dw (H,C,2), db (H,C, or NULL), all fp32,
- * from dy (B,H,T,C) in dtype.  C in {16, 32, 64}.
+ * from dy (B,H,T,C) in dtype.  C in {16, 32, 64}.  The weight gradients are reduced in
+ * double-float pairs by a cluster of 8 blocks per head (deterministic, no scratch).
  */
 int tm2_conv2_forward(const void* x, const float* w, const float* b, const void* x_prev, void* y,
                       int B, int H, int T, int C, int dtype, void* stream);

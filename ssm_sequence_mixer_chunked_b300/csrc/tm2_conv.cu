@@ -9,13 +9,17 @@
 //   dw0 = sum_{b,t} dy_t x_t,   dw1 = sum_{b,t} dy_t x_{t-1},   db = sum_{b,t} dy_t.
 // Both passes are elementwise over (B, H, T, C) and bound by HBM bandwidth: each thread owns
 // 8 consecutive channels (one 16-byte load of bf16) of one token.  The weight gradients are
-// reduced per head by one block that walks every (b, t) of the head's channels.
+// reduced per head by a cluster of 8 blocks over token splits, in double-float pairs.
 #include <algorithm>
+
+#include <cooperative_groups.h>
 
 #include "tm2_common.cuh"
 #include "tm2_launch.h"
 
 namespace tm2 {
+
+namespace cg = cooperative_groups;
 
 template <typename Tin>
 TM2_DEV void ld8(const Tin* p, float* x);
@@ -109,42 +113,55 @@ __global__ void conv2_bwd_dx_kernel(const Tin* __restrict__ dy, const float* __r
     }
 }
 
-// dw (H,C,2), db (H,C) (optional): one block of 256 threads per head; thread (channel c,
-// lane group r of 256 / C) sums every (b, t) with t = r mod (256 / C), in fp64.
+// dw (H,C,2), db (H,C) (optional), with the sums carried as double-float pairs (the products
+// dy x exact, TwoProduct; every addition TwoSum-based).  One cluster of DW_SPLIT blocks per
+// head, grid (DW_SPLIT, H), 256 threads: block rank sp sums the (b, t) items
+// [n sp / DW_SPLIT, n (sp + 1) / DW_SPLIT) of the head, n = B T; thread (channel c, lane
+// group r of 256 / C) takes every (256 / C)-th item, and the groups are added in a fixed
+// order.  Block rank 0 then adds the blocks' sums in rank order through distributed shared
+// memory and writes the head's gradients: deterministic, and no scratch in global memory.
+constexpr int DW_SPLIT = 8;
+
 template <typename Tin>
-__global__ void __launch_bounds__(256) conv2_bwd_dw_kernel(const Tin* __restrict__ x, const Tin* __restrict__ dy,
-                                                           const Tin* __restrict__ x_prev, float* __restrict__ dw,
-                                                           float* __restrict__ db, int B, int H, int T, int C) {
-    extern __shared__ double red[];   // [3][256]
-    const int h = blockIdx.x, tid = threadIdx.x, c = tid % C, r = tid / C, NR = 256 / C;
-    double s0 = 0.0, s1 = 0.0, sb = 0.0;
-    for (int bb = 0; bb < B; ++bb) {
-        const long bh = (long)bb * H + h;
-        for (int t = r; t < T; t += NR) {
-            const long tok = bh * T + t;
-            const float g = to_f(dy[tok * C + c]);
-            const float xc = to_f(x[tok * C + c]);
-            const float xp = t > 0 ? to_f(x[(tok - 1) * C + c]) : (x_prev ? to_f(x_prev[bh * C + c]) : 0.f);
-            s0 += (double)g * xc;
-            s1 += (double)g * xp;
-            sb += (double)g;
-        }
+__global__ void __cluster_dims__(DW_SPLIT, 1, 1) __launch_bounds__(256)
+    conv2_bwd_dw_kernel(const Tin* __restrict__ x, const Tin* __restrict__ dy, const Tin* __restrict__ x_prev,
+                        float* __restrict__ dw, float* __restrict__ db, int B, int H, int T, int C) {
+    __shared__ df32 red[3][256];
+    __shared__ df32 part[3][64];
+    cg::cluster_group cluster = cg::this_cluster();
+    const int h = blockIdx.y, sp = (int)cluster.block_rank(), tid = threadIdx.x, c = tid % C, r = tid / C,
+              NR = 256 / C;
+    const long n = (long)B * T, i0 = n * sp / DW_SPLIT, i1 = n * (sp + 1) / DW_SPLIT;
+    df32 s0{0.f, 0.f}, s1{0.f, 0.f}, sb{0.f, 0.f};
+    for (long i = i0 + r; i < i1; i += NR) {
+        const int bb = (int)(i / T), t = (int)(i % T);
+        const long bh = (long)bb * H + h, tok = bh * T + t;
+        const float g = to_f(dy[tok * C + c]);
+        const float xc = to_f(x[tok * C + c]);
+        const float xp = t > 0 ? to_f(x[(tok - 1) * C + c]) : (x_prev ? to_f(x_prev[bh * C + c]) : 0.f);
+        s0 = df_add(s0, df_two_prod(g, xc));
+        s1 = df_add(s1, df_two_prod(g, xp));
+        sb = df_add(sb, df32{g, 0.f});
     }
-    red[tid] = s0;
-    red[256 + tid] = s1;
-    red[512 + tid] = sb;
+    red[0][tid] = s0;
+    red[1][tid] = s1;
+    red[2][tid] = sb;
     __syncthreads();
-    if (tid < C) {
-        double a0 = 0.0, a1 = 0.0, ab = 0.0;
-        for (int k = 0; k < NR; ++k) {
-            a0 += red[k * C + tid];
-            a1 += red[256 + k * C + tid];
-            ab += red[512 + k * C + tid];
-        }
-        dw[((long)h * C + tid) * 2] = (float)a0;
-        dw[((long)h * C + tid) * 2 + 1] = (float)a1;
-        if (db) db[(long)h * C + tid] = (float)ab;
+    const int k = tid / C, cc = tid % C;
+    if (tid < 3 * C) {
+        df32 acc = red[k][cc];
+        for (int q = 1; q < NR; ++q) acc = df_add(acc, red[k][q * C + cc]);
+        part[k][cc] = acc;
     }
+    cluster.sync();   // every block's sums are in its shared memory
+    if (sp == 0 && tid < 3 * C) {
+        df32 acc = part[k][cc];
+        for (int q = 1; q < DW_SPLIT; ++q) acc = df_add(acc, cluster.map_shared_rank(&part[0][0], q)[k * 64 + cc]);
+        const float v = acc.hi + acc.lo;
+        if (k < 2) dw[((long)h * C + cc) * 2 + k] = v;
+        else if (db) db[(long)h * C + cc] = v;
+    }
+    cluster.sync();   // no block leaves while rank 0 reads its shared memory
 }
 
 static unsigned grid_for(long total) {
@@ -170,15 +187,16 @@ cudaError_t launch_conv2_bwd(int B, int H, int T, int C, int dtype, const void* 
     const long BH = (long)B * H;
     const long total = BH * (long)T * (C / 8);
     if (total == 0) return cudaSuccess;
+    const dim3 gw(DW_SPLIT, H);
     if (dtype == 1) {
         conv2_bwd_dx_kernel<__nv_bfloat16><<<grid_for(total), 256, 0, s>>>((const __nv_bfloat16*)dy, w, dx, dx_prev,
                                                                           BH, H, T, C);
-        conv2_bwd_dw_kernel<__nv_bfloat16><<<H, 256, 3 * 256 * sizeof(double), s>>>(
-            (const __nv_bfloat16*)x, (const __nv_bfloat16*)dy, (const __nv_bfloat16*)x_prev, dw, db, B, H, T, C);
+        conv2_bwd_dw_kernel<__nv_bfloat16><<<gw, 256, 0, s>>>((const __nv_bfloat16*)x, (const __nv_bfloat16*)dy,
+                                                              (const __nv_bfloat16*)x_prev, dw, db, B, H, T, C);
     } else {
         conv2_bwd_dx_kernel<float><<<grid_for(total), 256, 0, s>>>((const float*)dy, w, dx, dx_prev, BH, H, T, C);
-        conv2_bwd_dw_kernel<float><<<H, 256, 3 * 256 * sizeof(double), s>>>(
-            (const float*)x, (const float*)dy, (const float*)x_prev, dw, db, B, H, T, C);
+        conv2_bwd_dw_kernel<float><<<gw, 256, 0, s>>>((const float*)x, (const float*)dy, (const float*)x_prev, dw, db,
+                                                      B, H, T, C);
     }
     return cudaGetLastError();
 }

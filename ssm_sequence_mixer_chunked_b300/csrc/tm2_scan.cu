@@ -24,29 +24,7 @@ TM2_DEV float block_inclusive_scan(float v, float* wsum /* >= 32 floats */) {
     return s;
 }
 
-// Double-float sums (an unevaluated pair hi + lo of fp32 values, about 48 significant bits)
-// for the long reverse sums of the A-mask gradient: the error-free sum of two floats is
-// Knuth's TwoSum, and the pair is renormalised with Dekker's Fast2Sum.  fp64 arithmetic would
-// do as well but runs at a small fraction of the fp32 rate on this part; these are plain fp32
-// adds and subtracts (no products, so nothing can be contracted into an FMA).
-struct df32 {
-    float hi, lo;
-};
-TM2_DEV df32 df_two_sum(float a, float b) {
-    const float s = a + b, bb = s - a;
-    return {s, (a - (s - bb)) + (b - bb)};
-}
-TM2_DEV df32 df_fast_two_sum(float a, float b) {   // |a| >= |b|
-    const float s = a + b;
-    return {s, b - (s - a)};
-}
-// Sum of two pairs with both the high and the low parts added error-free, so that the
-// cancelling sums stay accurate relative to the result.
-TM2_DEV df32 df_add(df32 x, df32 y) {
-    const df32 s = df_two_sum(x.hi, y.hi), t = df_two_sum(x.lo, y.lo);
-    df32 r = df_fast_two_sum(s.hi, s.lo + t.hi);
-    return df_fast_two_sum(r.hi, r.lo + t.lo);
-}
+// (double-float pairs: tm2_common.cuh)
 TM2_DEV df32 df_shfl_up(df32 v, int o) {
     return {__shfl_up_sync(0xffffffffu, v.hi, o), __shfl_up_sync(0xffffffffu, v.lo, o)};
 }

@@ -146,6 +146,25 @@ def test_conv2_sequence_forward_backward(dtype, C):
         assert si.rel_err(got.cpu(), ref) <= 1e-5, name
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_conv2_weight_gradients_long_sequence(dtype):
+    # the weight gradients are reduced by a cluster of 8 blocks per head over token splits:
+    # B T = 6002 items per head (splits of 750 and 751), several heads, C = 64
+    B, H, T, C = 2, 5, 3001, 64
+    g = torch.Generator().manual_seed(733)
+    x = (torch.randn(B, H, T, C, generator=g) * 0.5).to(si.TORCH_DTYPE[dtype])
+    dy = torch.randn(B, H, T, C, generator=g).to(si.TORCH_DTYPE[dtype])
+    w = torch.randn(H, C, 2, generator=g) * 0.7
+    dx, dxp, dw, db = tm2.conv2_backward(x.cuda(), w.cuda(), dy.cuda(), None)
+    torch.cuda.synchronize()
+    refs = oracle.conv2_bwd(x, w, dy, None)
+    for name, got, ref in zip(("dx", "dx_prev", "dw", "db"), (dx, dxp, dw, db), refs):
+        assert si.rel_err(got.cpu(), ref) <= 1e-5, name
+    # the same call again gives the same bits (fixed reduction order)
+    dx2, dxp2, dw2, db2 = tm2.conv2_backward(x.cuda(), w.cuda(), dy.cuda(), None)
+    assert torch.equal(dw2.cpu(), dw.cpu()) and torch.equal(db2.cpu(), db.cpu())
+
+
 # ------------------------------------------------------------------------ 2Mamba-E decode
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
