@@ -9,7 +9,8 @@
 //   dw0 = sum_{b,t} dy_t x_t,   dw1 = sum_{b,t} dy_t x_{t-1},   db = sum_{b,t} dy_t.
 // Both passes are elementwise over (B, H, T, C) and bound by HBM bandwidth: each thread owns
 // 8 consecutive channels (one 16-byte load of bf16) of one token.  The weight gradients are
-// reduced per head by a cluster of 8 blocks over token splits, in double-float pairs.
+// reduced per head by a cluster of 8 blocks over token splits (compensated fp32 sums per
+// thread, double-float pairs above).
 #include <algorithm>
 
 #include <cooperative_groups.h>
@@ -71,15 +72,15 @@ __global__ void conv2_fwd_kernel(const Tin* __restrict__ x, const float* __restr
         const int t = (int)(tok % T);
         const long bh = tok / T;
         const int h = (int)(bh % H);
-        float cur[8], prv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, out[8];
+        float cur[8], prv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, out[8], wv[16], bv[8];
         ld8(x + tok * C + 8 * pc, cur);
         if (t > 0) ld8(x + (tok - 1) * C + 8 * pc, prv);
         else if (x_prev) ld8(x_prev + bh * C + 8 * pc, prv);
+        ld8(w + ((long)h * C + 8 * pc) * 2, wv);   // (w0, w1) of the 8 channels
+        ld8(w + ((long)h * C + 8 * pc) * 2 + 8, wv + 8);
+        if (b) ld8(b + (long)h * C + 8 * pc, bv);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const long wc = (long)h * C + 8 * pc + i;
-            out[i] = fmaf(w[wc * 2], cur[i], w[wc * 2 + 1] * prv[i]) + (b ? b[wc] : 0.f);
-        }
+        for (int i = 0; i < 8; ++i) out[i] = fmaf(wv[2 * i], cur[i], wv[2 * i + 1] * prv[i]) + (b ? bv[i] : 0.f);
         st8(y + tok * C + 8 * pc, out);
     }
 }
@@ -96,61 +97,87 @@ __global__ void conv2_bwd_dx_kernel(const Tin* __restrict__ dy, const float* __r
         const int t = (int)(tok % T);
         const long bh = tok / T;
         const int h = (int)(bh % H);
-        float g0[8], g1[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, out[8];
+        float g0[8], g1[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, out[8], wv[16];
         ld8(dy + tok * C + 8 * pc, g0);
         if (t + 1 < T) ld8(dy + (tok + 1) * C + 8 * pc, g1);
+        ld8(w + ((long)h * C + 8 * pc) * 2, wv);
+        ld8(w + ((long)h * C + 8 * pc) * 2 + 8, wv + 8);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const long wc = (long)h * C + 8 * pc + i;
-            out[i] = fmaf(w[wc * 2], g0[i], w[wc * 2 + 1] * g1[i]);
-        }
+        for (int i = 0; i < 8; ++i) out[i] = fmaf(wv[2 * i], g0[i], wv[2 * i + 1] * g1[i]);
         st8(dx + tok * C + 8 * pc, out);
         if (t == 0 && dx_prev) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) out[i] = w[((long)h * C + 8 * pc + i) * 2 + 1] * g0[i];
+            for (int i = 0; i < 8; ++i) out[i] = wv[2 * i + 1] * g0[i];
             st8(dx_prev + bh * C + 8 * pc, out);
         }
     }
 }
 
-// dw (H,C,2), db (H,C) (optional), with the sums carried as double-float pairs (the products
-// dy x exact, TwoProduct; every addition TwoSum-based).  One cluster of DW_SPLIT blocks per
-// head, grid (DW_SPLIT, H), 256 threads: block rank sp sums the (b, t) items
-// [n sp / DW_SPLIT, n (sp + 1) / DW_SPLIT) of the head, n = B T; thread (channel c, lane
-// group r of 256 / C) takes every (256 / C)-th item, and the groups are added in a fixed
-// order.  Block rank 0 then adds the blocks' sums in rank order through distributed shared
-// memory and writes the head's gradients: deterministic, and no scratch in global memory.
-constexpr int DW_SPLIT = 8;
+// dw (H,C,2), db (H,C) (optional).  One cluster of DW_SPLIT blocks per head, grid
+// (DW_SPLIT, H), DW_THREADS threads: block rank sp sums the (b, t) items
+// [n sp / DW_SPLIT, n (sp + 1) / DW_SPLIT) of the head, n = B T; thread (token lane tl,
+// channel group cg of 8 channels, one 16-byte load of bf16) takes every NL-th item and keeps
+// its 24 sums in fp32 with Neumaier's compensation (the products dy x rounded once each).
+// The token lanes of a warp are then added as double-float pairs by a butterfly, the warps
+// in warp order, and block rank 0 adds the blocks' sums in rank order through distributed
+// shared memory and writes the head's gradients: deterministic, no scratch in global memory.
+constexpr int DW_SPLIT = 8, DW_THREADS = 512;
+
+struct comp32 {   // Neumaier-compensated fp32 sum: s + c
+    float s = 0.f, c = 0.f;
+    TM2_DEV void add(float x) {
+        const float t = s + x;
+        c += fabsf(s) >= fabsf(x) ? (s - t) + x : (x - t) + s;
+        s = t;
+    }
+};
+
+TM2_DEV df32 df_shfl_xor(df32 v, int o) {
+    return {__shfl_xor_sync(0xffffffffu, v.hi, o), __shfl_xor_sync(0xffffffffu, v.lo, o)};
+}
 
 template <typename Tin>
-__global__ void __cluster_dims__(DW_SPLIT, 1, 1) __launch_bounds__(256)
+__global__ void __cluster_dims__(DW_SPLIT, 1, 1) __launch_bounds__(DW_THREADS)
     conv2_bwd_dw_kernel(const Tin* __restrict__ x, const Tin* __restrict__ dy, const Tin* __restrict__ x_prev,
                         float* __restrict__ dw, float* __restrict__ db, int B, int H, int T, int C) {
-    __shared__ df32 red[3][256];
+    __shared__ df32 wred[DW_THREADS / 32][3][64];
     __shared__ df32 part[3][64];
     cg::cluster_group cluster = cg::this_cluster();
-    const int h = blockIdx.y, sp = (int)cluster.block_rank(), tid = threadIdx.x, c = tid % C, r = tid / C,
-              NR = 256 / C;
+    const int h = blockIdx.y, sp = (int)cluster.block_rank(), tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int G = C / 8, cgp = tid % G, tl = tid / G, NL = DW_THREADS / G;
     const long n = (long)B * T, i0 = n * sp / DW_SPLIT, i1 = n * (sp + 1) / DW_SPLIT;
-    df32 s0{0.f, 0.f}, s1{0.f, 0.f}, sb{0.f, 0.f};
-    for (long i = i0 + r; i < i1; i += NR) {
+    comp32 s0[8], s1[8], sb[8];
+    for (long i = i0 + tl; i < i1; i += NL) {
         const int bb = (int)(i / T), t = (int)(i % T);
         const long bh = (long)bb * H + h, tok = bh * T + t;
-        const float g = to_f(dy[tok * C + c]);
-        const float xc = to_f(x[tok * C + c]);
-        const float xp = t > 0 ? to_f(x[(tok - 1) * C + c]) : (x_prev ? to_f(x_prev[bh * C + c]) : 0.f);
-        s0 = df_add(s0, df_two_prod(g, xc));
-        s1 = df_add(s1, df_two_prod(g, xp));
-        sb = df_add(sb, df32{g, 0.f});
+        float g[8], xc[8], xp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        ld8(dy + tok * C + 8 * cgp, g);
+        ld8(x + tok * C + 8 * cgp, xc);
+        if (t > 0) ld8(x + (tok - 1) * C + 8 * cgp, xp);
+        else if (x_prev) ld8(x_prev + bh * C + 8 * cgp, xp);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            s0[j].add(__fmul_rn(g[j], xc[j]));   // (never contracted into the compensated add)
+            s1[j].add(__fmul_rn(g[j], xp[j]));
+            sb[j].add(g[j]);
+        }
     }
-    red[0][tid] = s0;
-    red[1][tid] = s1;
-    red[2][tid] = sb;
+    // the warp's token lanes (lanes with the same channel group: lane mod G) as pairs
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        df32 v[3] = {df_two_sum(s0[j].s, s0[j].c), df_two_sum(s1[j].s, s1[j].c), df_two_sum(sb[j].s, sb[j].c)};
+        for (int o = G; o < 32; o <<= 1)
+#pragma unroll
+            for (int k = 0; k < 3; ++k) v[k] = df_add(v[k], df_shfl_xor(v[k], o));
+        if (lane < G)
+#pragma unroll
+            for (int k = 0; k < 3; ++k) wred[warp][k][8 * cgp + j] = v[k];
+    }
     __syncthreads();
     const int k = tid / C, cc = tid % C;
     if (tid < 3 * C) {
-        df32 acc = red[k][cc];
-        for (int q = 1; q < NR; ++q) acc = df_add(acc, red[k][q * C + cc]);
+        df32 acc = wred[0][k][cc];
+        for (int q = 1; q < DW_THREADS / 32; ++q) acc = df_add(acc, wred[q][k][cc]);
         part[k][cc] = acc;
     }
     cluster.sync();   // every block's sums are in its shared memory
@@ -191,11 +218,11 @@ cudaError_t launch_conv2_bwd(int B, int H, int T, int C, int dtype, const void* 
     if (dtype == 1) {
         conv2_bwd_dx_kernel<__nv_bfloat16><<<grid_for(total), 256, 0, s>>>((const __nv_bfloat16*)dy, w, dx, dx_prev,
                                                                           BH, H, T, C);
-        conv2_bwd_dw_kernel<__nv_bfloat16><<<gw, 256, 0, s>>>((const __nv_bfloat16*)x, (const __nv_bfloat16*)dy,
+        conv2_bwd_dw_kernel<__nv_bfloat16><<<gw, DW_THREADS, 0, s>>>((const __nv_bfloat16*)x, (const __nv_bfloat16*)dy,
                                                               (const __nv_bfloat16*)x_prev, dw, db, B, H, T, C);
     } else {
         conv2_bwd_dx_kernel<float><<<grid_for(total), 256, 0, s>>>((const float*)dy, w, dx, dx_prev, BH, H, T, C);
-        conv2_bwd_dw_kernel<float><<<gw, 256, 0, s>>>((const float*)x, (const float*)dy, (const float*)x_prev, dw, db,
+        conv2_bwd_dw_kernel<float><<<gw, DW_THREADS, 0, s>>>((const float*)x, (const float*)dy, (const float*)x_prev, dw, db,
                                                       B, H, T, C);
     }
     return cudaGetLastError();
